@@ -1,0 +1,91 @@
+"""GB300 (sm_103a) fused exact-attention forward.
+
+``attn_fwd(q, k, v, causal=False, sm_scale=None)`` returns ``(out, lse)`` for
+q [B,Hq,N,D] and k, v [B,Hkv,N,D] (bf16, CUDA, contiguous): out = softmax(sm_scale QK^T
+[+ causal mask]) V in bf16 and the natural-log LSE of each row in fp32.  All arithmetic runs in
+the hand-written CUDA kernels behind the C ABI (``include/attn.h``); this module only allocates
+outputs with PyTorch and marshals pointers, sizes and the current stream.
+"""
+from __future__ import annotations
+
+import math
+
+from . import _lib
+
+ATTN_OK = 0
+STATUS_NAMES = {
+    0: "ATTN_OK", -1: "ATTN_ERR_NULL", -2: "ATTN_ERR_SHAPE", -3: "ATTN_ERR_HEADS",
+    -4: "ATTN_ERR_HEADDIM", -5: "ATTN_ERR_ALIGN", -6: "ATTN_ERR_SCALE", -7: "ATTN_ERR_ARCH",
+    -8: "ATTN_ERR_CUDA", -9: "ATTN_ERR_TIMEOUT", -10: "ATTN_ERR_MEMORY", -11: "ATTN_ERR_ALIAS",
+}
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str = "attn_fwd"):
+        lib = _lib.load()
+        msg = lib.attn_status_string(status).decode()
+        extra = ""
+        if status == -8:
+            extra = f" (cudaError {lib.attn_last_cuda_error()})"
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}: {msg}{extra}")
+        self.status = status
+
+
+def _stream_handle(device):
+    import torch
+
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def attn_fwd(q, k, v, causal: bool = False, sm_scale: float | None = None, out=None, lse=None):
+    """Fused attention forward on the current CUDA stream of ``q``'s device.
+
+    Returns ``(out, lse)``: out bf16 [B,Hq,N,D], lse fp32 [B,Hq,N].  ``out``/``lse`` may be passed
+    preallocated (contiguous, right shape and dtype).  Raises ``AttnError`` on a nonzero status.
+    """
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or t.dim() != 4:
+            raise ValueError(f"{name} must be a 4-D torch tensor [B, H, N, D]")
+        if t.dtype != torch.bfloat16:
+            raise ValueError(f"{name} must be bf16, got {t.dtype}")
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous ([B, H, N, D] row-major); call "
+                             ".contiguous() first")
+    B, Hq, N, D = q.shape
+    if k.shape != v.shape or k.shape[0] != B or k.shape[2] != N or k.shape[3] != D:
+        raise ValueError(f"shape mismatch: q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    if k.device != q.device or v.device != q.device:
+        raise ValueError("q, k, v must be on the same device")
+    Hkv = k.shape[1]
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+    if out.shape != q.shape or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor shaped like q")
+    if lse.shape != (B, Hq, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor [B, Hq, N]")
+    lib = _lib.load()
+    with torch.cuda.device(q.device):
+        st = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                          B, Hq, Hkv, N, D, int(bool(causal)), float(sm_scale),
+                          _stream_handle(q.device))
+    if st != ATTN_OK:
+        raise AttnError(st)
+    return out, lse
+
+
+def device_status(device=None) -> int:
+    """Synchronise the current stream and return (and clear) the device status word:
+    0 if no kernel recorded a failure, else a negative status (e.g. -9 for an expired wait)."""
+    import torch
+
+    dev = device if device is not None else torch.cuda.current_device()
+    with torch.cuda.device(dev):
+        return int(_lib.load().attn_debug_status(_stream_handle(dev)))

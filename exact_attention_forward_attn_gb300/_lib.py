@@ -1,0 +1,45 @@
+"""ctypes loader for the C ABI in ``include/attn.h`` (``_build/libgb300attn.so``).
+
+There is no fallback: if the library has not been built (``build.build()``), loading raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from .build import LIB_PATH
+
+# Every symbol include/attn.h declares, with its ctypes signature.
+_c_int, _c_float, _vp = ctypes.c_int, ctypes.c_float, ctypes.c_void_p
+SIGNATURES = {
+    "attn_fwd": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                          _c_float, _vp]),
+    "attn_status_string": (ctypes.c_char_p, [_c_int]),
+    "attn_last_cuda_error": (_c_int, []),
+    "attn_debug_status": (_c_int, [_vp]),
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load(path: str | None = None):
+    """Load the built library once and attach the signatures of every exported function."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(
+                f"CUDA library not found at {p}; build it first "
+                "(python -m exact_attention_forward_attn_gb300.build or __graft_entry__.build())")
+        lib = ctypes.CDLL(p)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        if path is None:
+            _lib = lib
+        return lib

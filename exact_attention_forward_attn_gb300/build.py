@@ -1,0 +1,72 @@
+"""Build the sm_103a CUDA library ``_build/libgb300attn.so`` in-tree with nvcc.
+
+One translation unit (``csrc/attn_api.cu``), one ``-gencode`` (compute_103a -> sm_103a), the CUDA
+runtime linked as a shared library (the same ``libcudart`` PyTorch already loaded) with an rpath to
+the toolkit's lib64 for stand-alone C callers.
+"""
+from __future__ import annotations
+
+import os
+import shutil
+import subprocess
+import sys
+
+PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG_DIR)
+CSRC = os.path.join(PKG_DIR, "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+BUILD_DIR = os.path.join(PKG_DIR, "_build")
+LIB_NAME = "libgb300attn.so"
+LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
+SOURCES = [os.path.join(CSRC, "attn_api.cu")]
+DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("attn_fwd_kernel.cuh", "ptx.cuh")] + [
+    os.path.join(INCLUDE, "attn.h")]
+ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def cuda_home() -> str:
+    home = os.environ.get("CUDA_HOME") or os.environ.get("CUDA_PATH")
+    if home and os.path.isdir(home):
+        return home
+    nvcc = shutil.which("nvcc")
+    if nvcc:
+        return os.path.dirname(os.path.dirname(os.path.realpath(nvcc)))
+    return "/usr/local/cuda"
+
+
+def nvcc_command(out_path: str, extra=()) -> list:
+    home = cuda_home()
+    lib64 = os.path.join(home, "lib64")
+    return [os.path.join(home, "bin", "nvcc"), *ARCH_FLAGS, "-lineinfo", "-O3", "-std=c++17",
+            "-Xcompiler", "-fPIC,-O2", "-shared", "-cudart", "shared", f"-I{INCLUDE}",
+            f"-I{CSRC}", f"-Xlinker", f"-rpath,{lib64}", *extra, "-o", out_path, *SOURCES]
+
+
+def is_fresh() -> bool:
+    if not os.path.exists(LIB_PATH):
+        return False
+    t = os.path.getmtime(LIB_PATH)
+    return all(os.path.getmtime(p) <= t for p in DEPENDS)
+
+
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
+    """Compile the library unless it is up to date; returns its path."""
+    if is_fresh() and not force and not ptxas_info:
+        return LIB_PATH
+    os.makedirs(BUILD_DIR, exist_ok=True)
+    tmp = f"{LIB_PATH}.{os.getpid()}.tmp"
+    extra = ["-Xptxas", "-v"] if ptxas_info else []
+    cmd = nvcc_command(tmp, extra)
+    if verbose:
+        print(" ".join(cmd), file=sys.stderr)
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    if res.returncode != 0:
+        raise RuntimeError(f"nvcc failed ({res.returncode}):\n{res.stdout}\n{res.stderr}")
+    if ptxas_info or verbose:
+        print(res.stdout + res.stderr, file=sys.stderr)
+    os.replace(tmp, LIB_PATH)
+    return LIB_PATH
+
+
+if __name__ == "__main__":
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv))

@@ -1,0 +1,405 @@
+// attn_fwd_kernel.cuh - fused exact-attention forward for sm_103a (tcgen05 + TMEM + TMA).
+//
+// What it computes (per batch b, query head hq, query row i):
+//   O[i,:] = softmax_j(sm_scale * q_i . k_j)[j in J(i)] . V,   LSE[i] = ln sum_j exp(sm_scale q_i.k_j)
+//   with h_kv = hq * Hkv / Hq and J(i) = {0..i} (causal, top-left) or {0..N-1}.
+// How ("Attention Kernel 实现与正确性验证", walkerchi.com, sections 1.1-1.2; "Triton-CUDA Attention",
+// skillmd.com, online-softmax algorithm and the Causal/GQA variants; "Flash Attention 与 Kernel
+// 优化", fangpin.github.io, running state and saved LSE):
+//   a Q tile stays on chip while K/V tiles stream past it; per KV tile the running row maximum m,
+//   the running denominator l and the fp32 output accumulator are updated with the online-softmax
+//   recurrence (exp2 domain: scores are pre-multiplied by sm_scale*log2(e)); after the last tile
+//   O = acc / l and LSE = ln2 * (m + log2 l).  The N x N score matrix never leaves the SM.
+//
+// GB300 mapping (one CTA per pair of 128-row Q tiles, 320 threads):
+//   warp 9      TMA producer: Q0/Q1 once, then K_j, V_j through a KV_STAGES-deep mbarrier ring.
+//   warp 8      MMA issuer (one lane): S_t = Q_t K_j^T (SS form, fp32 in TMEM) and
+//               O_t += P_t V_j (P from TMEM, V from smem); tcgen05.commit signals completion.
+//   warps 0-3   softmax for Q tile 0, warps 4-7 for Q tile 1: one thread per query row reads its
+//               S row from TMEM, masks (diagonal causal tile / ragged last key tile only), updates
+//               m and l, rescales its O row in TMEM when m moved, writes P (bf16) over S in TMEM;
+//               after the last tile it normalises O, stages it in smem and TMA-stores it, and
+//               writes LSE.
+//   The two Q tiles ping-pong: while one softmax group works, the tensor core runs the other
+//   tile's MMAs.
+//   The running maximum is only moved when it grows by more than 8 (log2 units): p <= 2^8 stays
+//   exact in fp32/bf16 range and the final O = acc / l and LSE = m + log2 l use the same m, so
+//   the result is unchanged while most O rescales are skipped.
+#pragma once
+
+#include <cuda.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace gb300attn {
+
+constexpr int kBM = 128;          // query rows per Q tile (MMA M)
+constexpr int kBN = 128;          // key rows per KV tile (MMA N of S, K of P.V)
+constexpr int kQTiles = 2;        // Q tiles per CTA
+constexpr int kStages = 4;        // K/V ring slots (K_j and V_j take one slot each)
+constexpr int kThreads = 320;     // 10 warps
+constexpr int kMmaWarp = 8;
+constexpr int kLoadWarp = 9;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kLn2 = 0.69314718055994530942f;
+
+struct AttnParams {
+    int B, Hq, Hkv, N;
+    int group;         // Hq / Hkv
+    int causal;
+    int n_tiles;       // ceil(N / 128): number of Q tiles and of KV tiles per head
+    int n_pairs;       // ceil(n_tiles / 2): CTAs per (b, hq)
+    float scale_log2;  // sm_scale * log2(e)
+    float* lse;        // [B, Hq, N] fp32
+};
+
+template <int D>
+struct SmemLayout {
+    static constexpr int kPanelBytes = kBM * 64 * 2;        // 128 rows x 64 bf16 (one 128B-swizzle panel)
+    static constexpr int kTileBytes = kBM * D * 2;          // 128 x D bf16 = D/64 panels
+    static constexpr int kQ = 0;                            // Q tiles (reused as O staging)
+    static constexpr int kKV = kQ + kQTiles * kTileBytes;   // K/V ring
+    static constexpr int kBars = kKV + kStages * kTileBytes;
+    // barrier indices
+    static constexpr int kBarQ = 0;
+    static constexpr int kBarKvFull = 1;
+    static constexpr int kBarKvEmpty = kBarKvFull + kStages;
+    static constexpr int kBarSFull = kBarKvEmpty + kStages;   // [2]
+    static constexpr int kBarPReady = kBarSFull + 2;          // [2]
+    static constexpr int kBarODone = kBarPReady + 2;          // [2]
+    static constexpr int kNumBars = kBarODone + 2;
+    static constexpr int kTmemSlot = kBars + kNumBars * 8;
+    static constexpr int kAbort = kTmemSlot + 8;
+    static constexpr int kBytes = kAbort + 8;
+    static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024 bytes
+};
+
+// TMEM column map: S_t at 128*t (P_t aliases the first 64 columns of S_t), O_t at 256 + 128*t.
+__device__ __forceinline__ uint32_t tmem_s_col(int t) { return 128u * t; }
+__device__ __forceinline__ uint32_t tmem_o_col(int t) { return 256u + 128u * t; }
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                    const __grid_constant__ CUtensorMap tmap_k,
+                    const __grid_constant__ CUtensorMap tmap_v,
+                    const __grid_constant__ CUtensorMap tmap_o, const AttnParams p,
+                    unsigned int* status_word) {
+    using L = SmemLayout<D>;
+    static_assert(D == 64 || D == 128, "head dim");
+    constexpr int kPanels = D / 64;
+    constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, 0);   // Q (K-major) x K (K-major)
+    constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, D, 1);    // P (TMEM) x V (MN-major)
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_addr(smem);
+    auto bar = [=](int i) -> uint32_t { return sbase + L::kBars + 8u * i; };
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // ---- work decomposition: heaviest (latest) Q-tile pairs first, heads innermost -------------
+    const int bh_count = p.B * p.Hq;
+    const int pair = p.n_pairs - 1 - static_cast<int>(blockIdx.x / bh_count);
+    const int bh = static_cast<int>(blockIdx.x % bh_count);
+    const int b = bh / p.Hq;
+    const int hq = bh % p.Hq;
+    const int bh_kv = b * p.Hkv + hq / p.group;
+    const int tile0 = 2 * pair;
+    const bool has_q1 = tile0 + 1 < p.n_tiles;
+    // last KV tile each Q tile needs (BM == BN: the causal diagonal tile has the Q tile's index)
+    const int last0 = p.causal ? tile0 : p.n_tiles - 1;
+    const int last1 = p.causal ? tile0 + 1 : p.n_tiles - 1;
+    const int n_kv = has_q1 ? last1 + 1 : last0 + 1;
+
+    // ---- setup ---------------------------------------------------------------------------------
+    if (threadIdx.x == 0) {
+        mbar_init(bar(L::kBarQ), 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bar(L::kBarKvFull + s), 1);
+            mbar_init(bar(L::kBarKvEmpty + s), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(bar(L::kBarSFull + t), 1);
+            mbar_init(bar(L::kBarPReady + t), 128);
+            mbar_init(bar(L::kBarODone + t), 1);
+        }
+        *abort_flag = 0;
+        fence_mbarrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == kLoadWarp && lane == 0) {
+        tma_prefetch_desc(&tmap_q);
+        tma_prefetch_desc(&tmap_k);
+        tma_prefetch_desc(&tmap_v);
+        tma_prefetch_desc(&tmap_o);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kLoadWarp) {
+        // =========================== TMA producer (one lane) ===================================
+        if (lane == 0) {
+            const int nq = has_q1 ? 2 : 1;
+            mbar_arrive_expect_tx(bar(L::kBarQ), nq * L::kTileBytes);
+            for (int t = 0; t < nq; ++t)
+                for (int h = 0; h < kPanels; ++h)
+                    tma_load_3d(sbase + L::kQ + t * L::kTileBytes + h * L::kPanelBytes, &tmap_q,
+                                bar(L::kBarQ), h * 64, (tile0 + t) * kBM, bh);
+            for (int j = 0; j < n_kv; ++j) {
+                for (int kv = 0; kv < 2; ++kv) {
+                    const int idx = 2 * j + kv;
+                    const int slot = idx % kStages;
+                    const uint32_t ph = (idx / kStages) & 1;
+                    if (!mbar_wait_bounded(bar(L::kBarKvEmpty + slot), ph ^ 1u, abort_flag,
+                                           status_word))
+                        goto producer_done;
+                    mbar_arrive_expect_tx(bar(L::kBarKvFull + slot), L::kTileBytes);
+                    const CUtensorMap* map = kv ? &tmap_v : &tmap_k;
+                    for (int h = 0; h < kPanels; ++h)
+                        tma_load_3d(sbase + L::kKV + slot * L::kTileBytes + h * L::kPanelBytes, map,
+                                    bar(L::kBarKvFull + slot), h * 64, j * kBN, bh_kv);
+                }
+            }
+        producer_done:;
+        }
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        // =========================== MMA issuer (one lane) =====================================
+        if (lane == 0) {
+            auto s_mma = [=](int t, int kslot) {
+                const uint32_t qa = sbase + L::kQ + t * L::kTileBytes;
+                const uint32_t ka = sbase + L::kKV + kslot * L::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
+                    mma_bf16_ss(tmem + tmem_s_col(t), smem_desc_sw128(qa + off, 16, 1024),
+                                smem_desc_sw128(ka + off, 16, 1024), kIdescS, kk > 0);
+                }
+            };
+            auto pv_mma = [=](int t, int vslot, bool accumulate_first) {
+                const uint32_t va = sbase + L::kKV + vslot * L::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk) {
+                    mma_bf16_ts(tmem + tmem_o_col(t), tmem + tmem_s_col(t) + kk * 8,
+                                smem_desc_sw128(va + kk * 2048, L::kPanelBytes, 1024), kIdescPV,
+                                (accumulate_first || kk > 0) ? 1u : 0u);
+                }
+            };
+            auto kv_slot = [](int idx) { return idx % kStages; };
+            auto kv_phase = [](int idx) { return static_cast<uint32_t>((idx / kStages) & 1); };
+            uint32_t p_phase[2] = {0, 0};
+
+            bool ok = mbar_wait_bounded(bar(L::kBarQ), 0, abort_flag, status_word);
+            if (ok) ok = mbar_wait_bounded(bar(L::kBarKvFull + kv_slot(0)), kv_phase(0),
+                                           abort_flag, status_word);
+            if (ok) {
+                tc_fence_after();
+                s_mma(0, kv_slot(0));
+                mma_commit(bar(L::kBarSFull + 0));
+                if (has_q1) {
+                    s_mma(1, kv_slot(0));
+                    mma_commit(bar(L::kBarSFull + 1));
+                }
+                mma_commit(bar(L::kBarKvEmpty + kv_slot(0)));
+            }
+            for (int j = 0; ok && j < n_kv; ++j) {
+                const int vidx = 2 * j + 1;
+                const int kidx = 2 * j + 2;  // K_{j+1}
+                ok = mbar_wait_bounded(bar(L::kBarKvFull + kv_slot(vidx)), kv_phase(vidx),
+                                       abort_flag, status_word);
+                if (!ok) break;
+                if (j <= last0) {
+                    ok = mbar_wait_bounded(bar(L::kBarPReady + 0), p_phase[0], abort_flag,
+                                           status_word);
+                    if (!ok) break;
+                    p_phase[0] ^= 1u;
+                    tc_fence_after();
+                    pv_mma(0, kv_slot(vidx), j > 0);
+                    if (j == last0) mma_commit(bar(L::kBarODone + 0));
+                }
+                const bool next = j + 1 < n_kv;
+                if (next) {
+                    ok = mbar_wait_bounded(bar(L::kBarKvFull + kv_slot(kidx)), kv_phase(kidx),
+                                           abort_flag, status_word);
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (j + 1 <= last0) {
+                        s_mma(0, kv_slot(kidx));
+                        mma_commit(bar(L::kBarSFull + 0));
+                    }
+                }
+                if (has_q1 && j <= last1) {
+                    ok = mbar_wait_bounded(bar(L::kBarPReady + 1), p_phase[1], abort_flag,
+                                           status_word);
+                    if (!ok) break;
+                    p_phase[1] ^= 1u;
+                    tc_fence_after();
+                    pv_mma(1, kv_slot(vidx), j > 0);
+                    if (j == last1) mma_commit(bar(L::kBarODone + 1));
+                }
+                mma_commit(bar(L::kBarKvEmpty + kv_slot(vidx)));
+                if (next) {
+                    if (has_q1 && j + 1 <= last1) {
+                        s_mma(1, kv_slot(kidx));
+                        mma_commit(bar(L::kBarSFull + 1));
+                    }
+                    mma_commit(bar(L::kBarKvEmpty + kv_slot(kidx)));
+                }
+            }
+        }
+        __syncwarp();
+    } else {
+        // =========================== softmax + epilogue (warps 0-7) ============================
+        const int t = warp >> 2;          // which Q tile
+        const int quarter = warp & 3;     // TMEM lane quarter this warp may access
+        const int row = quarter * 32 + lane;  // row within the Q tile
+        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+        if (t == 0 || has_q1) {
+            const int q_tile = tile0 + t;
+            const int last = t == 0 ? last0 : last1;
+            const int row_g = q_tile * kBM + row;
+            const uint32_t s_addr = tmem + lane_base + tmem_s_col(t);
+            const uint32_t o_addr = tmem + lane_base + tmem_o_col(t);
+            const float c = p.scale_log2;
+            float m = -INFINITY;  // running max of c*s (log2 units)
+            float l = 0.f;        // running denominator
+            bool ok = true;
+            for (int j = 0; j <= last; ++j) {
+                ok = mbar_wait_warp(bar(L::kBarSFull + t), j & 1, abort_flag, status_word);
+                if (!ok) break;
+                tc_fence_after();
+                float s[kBN];
+                {
+                    uint32_t r[32];
+#pragma unroll
+                    for (int cc = 0; cc < kBN / 32; ++cc) {
+                        tmem_ld32(s_addr + cc * 32, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) s[cc * 32 + i] = __uint_as_float(r[i]);
+                    }
+                }
+                // masks: only on the causal diagonal tile, or on a ragged last key tile
+                if (p.causal && j == q_tile) {
+#pragma unroll
+                    for (int i = 0; i < kBN; ++i)
+                        if (i > row) s[i] = -INFINITY;
+                } else if (!p.causal && j == p.n_tiles - 1 && (p.N % kBN) != 0) {
+                    const int valid = p.N - j * kBN;
+#pragma unroll
+                    for (int i = 0; i < kBN; ++i)
+                        if (i >= valid) s[i] = -INFINITY;
+                }
+                float mx[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx[i] = s[i];
+#pragma unroll
+                for (int i = 8; i < kBN; ++i) mx[i & 7] = fmaxf(mx[i & 7], s[i]);
+#pragma unroll
+                for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+                    for (int i = 0; i < w; ++i) mx[i] = fmaxf(mx[i], mx[i + w]);
+                const float m_cand = mx[0] * c;
+                const float m_new = (m_cand > m + kRescaleThreshold) ? m_cand : m;
+                const float alpha = ex2_approx(m - m_new);  // 1 if unchanged, 0 on the first tile
+                const bool rescale = j > 0 && __any_sync(0xffffffffu, m_new != m);
+                l *= alpha;
+                m = m_new;
+                const float neg_m = -m;
+                float sum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int cc = 0; cc < kBN / 32; ++cc) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float p0 = ex2_approx(fmaf(s[cc * 32 + 2 * i], c, neg_m));
+                        const float p1 = ex2_approx(fmaf(s[cc * 32 + 2 * i + 1], c, neg_m));
+                        sum[(2 * i) & 3] += p0;
+                        sum[(2 * i + 1) & 3] += p1;
+                        pk[i] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st16(s_addr + cc * 16, pk);
+                }
+                l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
+                if (rescale) {
+                    // correction: O_row *= alpha.  The PV MMA of tile j-1 completed before S of
+                    // tile j (in-order MMAs, one commit), and PV of tile j waits for P_ready.
+#pragma unroll
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        uint32_t r[32];
+                        tmem_ld32(o_addr + cc * 32, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                        tmem_st32(o_addr + cc * 32, r);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(bar(L::kBarPReady + t));
+            }
+
+            // ---- epilogue: O = acc / l -> bf16 -> smem (over Q_t) -> TMA store; LSE ----------
+            if (ok) ok = mbar_wait_warp(bar(L::kBarODone + t), 0, abort_flag, status_word);
+            if (ok) {
+                tc_fence_after();
+                const float inv_l = 1.0f / l;
+                const uint32_t stage = sbase + L::kQ + t * L::kTileBytes;
+#pragma unroll
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t r[32];
+                    tmem_ld32(o_addr + cc * 32, r);
+                    tmem_wait_ld();
+                    const int panel = cc >> 1;
+#pragma unroll
+                    for (int c16 = 0; c16 < 4; ++c16) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            w[i] = pack_bf16x2(__uint_as_float(r[c16 * 8 + 2 * i]) * inv_l,
+                                               __uint_as_float(r[c16 * 8 + 2 * i + 1]) * inv_l);
+                        const int chunk = (cc & 1) * 4 + c16;  // 16-byte chunk within the 128B row
+                        const uint32_t dst = stage + panel * L::kPanelBytes + row * 128 +
+                                             ((chunk ^ (row & 7)) << 4);
+                        st_shared_v4(dst, w[0], w[1], w[2], w[3]);
+                    }
+                }
+                if (row_g < p.N)
+                    p.lse[static_cast<size_t>(bh) * p.N + row_g] = (m + __log2f(l)) * kLn2;
+            }
+            fence_proxy_async_smem();
+            named_barrier_sync(1 + t, 128);
+            if (ok && quarter == 0 && lane == 0) {
+                const uint32_t stage = sbase + L::kQ + t * L::kTileBytes;
+                for (int h = 0; h < kPanels; ++h)
+                    tma_store_3d(&tmap_o, stage + h * L::kPanelBytes, h * 64, q_tile * kBM, bh);
+                tma_store_commit_and_wait();
+            }
+            __syncwarp();
+        }
+    }
+
+    // ---- teardown ------------------------------------------------------------------------------
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace gb300attn

@@ -1,0 +1,90 @@
+/*
+ * attn.h - C ABI of the GB300 (sm_103a) exact-attention forward library (libgb300attn.so).
+ *
+ * The operation.  For Q [B, Hq, N, D] and K, V [B, Hkv, N, D] (bf16), every query row i of head
+ * (b, hq) gets
+ *     O[b,hq,i,:]  = sum_{j in J(i)} softmax_j(sm_scale * Q[b,hq,i,:] . K[b,hkv,j,:]) V[b,hkv,j,:]
+ *     LSE[b,hq,i]  = ln sum_{j in J(i)} exp(sm_scale * Q[b,hq,i,:] . K[b,hkv,j,:])
+ * with hkv = hq * Hkv / Hq (integer division) and J(i) = {0..i} under the causal mask (top-left
+ * aligned, key j visible to query i iff j <= i), else {0..N-1}.
+ * Sources: "Attention Kernel 实现与正确性验证" (walkerchi.com), section 1.1 (tiling + online softmax,
+ * the score matrix never written to memory) and section 1.2 (the GQA-aware forward kernel and its
+ * causal condition); "Triton-CUDA Attention" (skillmd.com), the standard forward with its
+ * (B, H, L, D) contiguous layout and sm_scale = 1/sqrt(D), and the GQA/MQA variants (heads map by
+ * integer division, grid over the query heads); "Flash Attention 与 Kernel 优化"
+ * (fangpin.github.io), the interface section (inputs already projected, no RoPE inside) and the
+ * saved per-row log-sum-exp statistic.
+ *
+ * Ownership.  Every tensor pointer is a DEVICE pointer (cudaMalloc / cudaMallocManaged memory of the
+ * current device), owned by the caller.  The library never allocates, frees or retains them, and
+ * allocates no device memory of its own per call.
+ *
+ * Errors.  Argument validation happens before anything is launched; on any validation failure the
+ * call returns a negative attn_status_t and writes nothing.  Kernel execution is asynchronous on
+ * `stream`: a return of ATTN_OK means "enqueued".  Device-side bounded waits that expire (which a
+ * correct build never hits) are recorded in a device status word read by attn_debug_status().
+ *
+ * Thread safety.  Calls from several host threads are safe; the only mutable host state is the
+ * per-thread last CUDA error.
+ */
+#ifndef GB300_ATTN_H
+#define GB300_ATTN_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_NULL = -1,     /* a required pointer is NULL */
+    ATTN_ERR_SHAPE = -2,    /* B, Hq, Hkv or N negative, Hq or Hkv zero, or sizes overflow */
+    ATTN_ERR_HEADS = -3,    /* Hq is not a multiple of Hkv */
+    ATTN_ERR_HEADDIM = -4,  /* D is not 64 or 128 */
+    ATTN_ERR_ALIGN = -5,    /* a tensor pointer is not 16-byte aligned */
+    ATTN_ERR_SCALE = -6,    /* sm_scale is not finite and positive */
+    ATTN_ERR_ARCH = -7,     /* the current device is not compute capability 10.3 (sm_103) */
+    ATTN_ERR_CUDA = -8,     /* a CUDA runtime/driver call failed; see attn_last_cuda_error() */
+    ATTN_ERR_TIMEOUT = -9,  /* a device-side bounded wait expired (reported by attn_debug_status) */
+    ATTN_ERR_MEMORY = -10,  /* a pointer is not device memory of the current device */
+    ATTN_ERR_ALIAS = -11    /* out or lse overlaps q, k, v or each other */
+} attn_status_t;
+
+/*
+ * attn_fwd - fused exact-attention forward (tiled, online softmax, O and LSE).
+ *
+ *   q        bf16 [B, Hq,  N, D], contiguous (row-major, D innermost)
+ *   k        bf16 [B, Hkv, N, D], contiguous
+ *   v        bf16 [B, Hkv, N, D], contiguous
+ *   out      bf16 [B, Hq,  N, D], contiguous; written (round-to-nearest-even); must not overlap
+ *            q, k, v or lse
+ *   lse      fp32 [B, Hq, N]; written with the natural-log LSE of the scaled, masked scores
+ *   B, Hq, Hkv, N, D   sizes; Hq % Hkv == 0 (MQA is Hkv == 1); D in {64, 128}; B == 0 or N == 0
+ *            is a valid empty problem (returns ATTN_OK, launches nothing)
+ *   causal   0: every key visible; nonzero: key j visible to query i iff j <= i
+ *   sm_scale score scale (callers usually pass 1/sqrt(D)); finite and > 0
+ *   stream   a cudaStream_t of the current device, passed as void* (NULL = legacy default stream)
+ *
+ * Returns ATTN_OK once the kernel is enqueued on `stream`, else a negative attn_status_t.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
+             int Hkv, int N, int D, int causal, float sm_scale, void* stream);
+
+/* Static, human-readable text for an attn_status_t value (never NULL). */
+const char* attn_status_string(int status);
+
+/* The cudaError_t behind this thread's most recent ATTN_ERR_CUDA (0 if none). */
+int attn_last_cuda_error(void);
+
+/*
+ * attn_debug_status - synchronise `stream`, then read and clear the device status word.
+ * Returns ATTN_OK if no kernel of this library recorded a failure since the last call,
+ * ATTN_ERR_TIMEOUT if a device-side bounded wait expired, or ATTN_ERR_CUDA if the
+ * synchronisation itself failed.  The status word is shared by all streams of the device.
+ */
+int attn_debug_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300_ATTN_H */

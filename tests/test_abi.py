@@ -1,0 +1,87 @@
+"""C-ABI checks that need no GPU: the library builds, loads, exports every symbol that
+include/attn.h declares, and rejects bad arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from exact_attention_forward_attn_gb300 import _lib, build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(attn_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_boundary():
+    assert _declared_functions() == sorted(
+        ["attn_fwd", "attn_status_string", "attn_last_cuda_error", "attn_debug_status"])
+
+
+def test_library_exports_every_declared_symbol(lib):
+    nm = subprocess.run(["nm", "-D", "--defined-only", build.LIB_PATH], capture_output=True,
+                        text=True, check=True).stdout
+    exported = set(re.findall(r"\bT\s+(\w+)$", nm, re.M))
+    for name in _declared_functions():
+        assert name in exported, f"{name} declared in attn.h but not exported"
+        assert callable(getattr(lib, name))
+    assert set(_lib.SIGNATURES) == set(_declared_functions())
+
+
+def test_built_for_sm_103a_only():
+    cmd = build.nvcc_command("/dev/null")
+    assert "arch=compute_103a,code=sm_103a" in cmd
+    assert sum(1 for c in cmd if c == "-gencode") == 1
+
+
+def test_status_strings(lib):
+    for st in range(-11, 1):
+        s = lib.attn_status_string(st)
+        assert isinstance(s, bytes) and len(s) > 0
+    assert lib.attn_status_string(0) == b"ok"
+    assert lib.attn_status_string(12345) == b"unknown status"
+
+
+# Host-side validation returns before any CUDA call; fake, aligned, never-dereferenced addresses.
+P = 0x10000
+
+
+def _call(lib, q=P, k=P * 2, v=P * 3, out=P * 4, lse=P * 5, B=1, Hq=2, Hkv=1, N=128, D=64,
+          causal=0, scale=0.125):
+    return lib.attn_fwd(q, k, v, out, lse, B, Hq, Hkv, N, D, causal, ctypes.c_float(scale), None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=0), -1), (dict(out=0), -1), (dict(lse=0), -1),
+    (dict(B=-1), -2), (dict(N=-5), -2), (dict(Hq=0), -2), (dict(Hkv=0), -2),
+    (dict(Hq=6, Hkv=4), -3),
+    (dict(D=96), -4), (dict(D=256), -4), (dict(D=0), -4),
+    (dict(scale=0.0), -6), (dict(scale=-1.0), -6), (dict(scale=float("inf")), -6),
+    (dict(scale=float("nan")), -6),
+    (dict(q=P + 8), -5), (dict(lse=P * 5 + 4), -5),
+])
+def test_host_validation(lib, kw, status):
+    assert _call(lib, **kw) == status
+
+
+def test_empty_problem_is_a_no_op(lib):
+    assert _call(lib, B=0) == 0
+    assert _call(lib, N=0) == 0
+
+
+def test_aliasing_output_is_rejected(lib):
+    # out overlapping q: rejected before any device query
+    assert _call(lib, out=P) == -11
+    assert _call(lib, lse=P * 4 + 64) == -11
