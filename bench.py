@@ -1,0 +1,409 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 exact-attention forward.
+
+One step = one ``attn_fwd`` call (the whole hot path: TMA loads, QK^T and P.V on the tensor cores,
+online softmax, O/LSE stores) over the long-context workload B=1, Hq=32, Hkv=8, N=32768, D=128,
+causal, bf16 (FLOPs = 4*B*Hq*N^2*D / 2).  Inputs (402 MB) and the output (268 MB) exceed the
+129 MB L2, so steps run back to back without an explicit flush.
+
+Prints one JSON line.  ``--impl reference`` times the fp64 CPU oracle instead (bounded sample per
+step, on the host cores).  Under torchrun (``--gpus N``) each rank runs an independent replica on
+its own GPU; the time is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOPS and ms (causal-adjusted) at N=1K–32K; % of bf16 TC peak"
+UNIT = "TFLOPS"
+DEFAULT_WORKLOAD = "long-gqa8-causal-n32768"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+KERNEL_SOURCES = ["exact_attention_forward_attn_gb300/csrc/attn_fwd_kernel.cuh",
+                  "exact_attention_forward_attn_gb300/csrc/ptx.cuh",
+                  "exact_attention_forward_attn_gb300/csrc/attn_api.cu"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def load_traffic(workload_name: str):
+    """DRAM bytes per launch from the committed ncu summary, if it matches this kernel build."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    kv = {}
+    with open(TRAFFIC_FILE) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#") and "=" in line:
+                k, v = line.split("=", 1)
+                kv[k.strip()] = v.strip()
+    if kv.get("kernel_sha") != kernel_hash():
+        return None
+    key = f"bytes_per_launch[{workload_name}]"
+    return float(kv[key]) if key in kv else None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.5)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(self.REASONS, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def physical_gpu_index(local: int):
+    """nvidia-smi index of CUDA device `local` (honours a numeric CUDA_VISIBLE_DEVICES)."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [x.strip() for x in vis.split(",") if x.strip()]
+        if local < len(ids) and ids[local].isdigit():
+            return int(ids[local])
+    return local
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def cpu_sample_rows(w, n_rows_per_head):
+    """Seeded query rows for the CPU oracle's bounded sample (same rows for every head)."""
+    import torch
+
+    n_rows_per_head = min(n_rows_per_head, w.N)
+    g = torch.Generator().manual_seed(9000 + w.N)
+    rows = torch.randperm(w.N, generator=g)[:n_rows_per_head].sort().values.to(torch.int32)
+    return rows.view(1, 1, -1).expand(w.B, w.Hq, -1).contiguous()
+
+
+def sample_flops(w, rows) -> float:
+    """FLOPs of the oracle's work on the sampled rows (4*D per visible key)."""
+    vis = (rows.long() + 1).sum().item() if w.causal else rows.numel() * w.N
+    return 4.0 * w.D * float(vis)
+
+
+def time_oracle(w, q, k, v, seconds_target: float, max_rows: int = 4096):
+    """Calibrate the number of sampled rows per head so one oracle call takes ~seconds_target."""
+    import oracle
+
+    rows = cpu_sample_rows(w, 8)
+    t0 = time.perf_counter()
+    oracle.attn_ref(q, k, v, w.causal, w.sm_scale, rows=rows.numpy())
+    dt = max(time.perf_counter() - t0, 1e-3)
+    rate = sample_flops(w, rows) / dt
+    n = int(min(max_rows, w.N, max(8, 8 * seconds_target / dt)))
+    return n, rate
+
+
+def run_reference(args, w):
+    """The reference arm: the fp64 CPU oracle as it stands, on the host cores."""
+    import oracle
+    from exact_attention_forward_attn_gb300 import workloads as wl
+
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    q, k, v = wl.make_qkv(w)
+    n_rows, _ = time_oracle(w, q, k, v, args.ref_step_seconds)
+    rows = cpu_sample_rows(w, n_rows)
+    flops = sample_flops(w, rows)
+    for _ in range(args.warmup):
+        oracle.attn_ref(q, k, v, w.causal, w.sm_scale, rows=rows.numpy())
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.attn_ref(q, k, v, w.causal, w.sm_scale, rows=rows.numpy())
+    dt = time.perf_counter() - t0
+    value = flops * args.steps / dt / 1e12
+    cores = oracle.default_threads()
+    sample = (f"{n_rows} seeded query rows per head x {w.B * w.Hq} heads of {w.name} "
+              f"({flops / 1e9:.2f} GFLOP per step)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_of(w, "host cores, no GPU"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(w, l2_note):
+    return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "D": w.D,
+            "causal": w.causal, "sm_scale": w.sm_scale, "l2": l2_note,
+            "inputs": "iid N(0,1) fp32 rounded to bf16, seeded"}
+
+
+def timed_launches(fn, stream, n):
+    """Run fn() n times back to back on `stream`; per-launch CUDA-event durations (ms)."""
+    import torch
+
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    with torch.cuda.stream(stream):
+        ev[0].record(stream)
+        for i in range(n):
+            fn()
+            ev[i + 1].record(stream)
+    stream.synchronize()
+    return [ev[i].elapsed_time(ev[i + 1]) for i in range(n)]
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--profile", action="store_true",
+                    help="timed launches only (no e2e, sweep, clocks or CPU baseline): for ncu")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target duration of the oracle's bounded CPU-baseline sample")
+    ap.add_argument("--ref-step-seconds", type=float, default=1.0,
+                    help="target duration of one reference-arm step")
+    args = ap.parse_args()
+    if args.warmup < 0 or args.steps < 1:
+        ap.error("--steps >= 1 and --warmup >= 0")
+
+    from exact_attention_forward_attn_gb300 import workloads as wl
+
+    w = wl.BY_NAME[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    import torch
+
+    import exact_attention_forward_attn_gb300 as attn
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    q, k, v = (t.to(dev) for t in wl.make_qkv(w))
+    out = torch.empty_like(q)
+    lse = torch.empty(w.B, w.Hq, w.N, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def step():
+        attn.attn_fwd(q, k, v, causal=w.causal, sm_scale=w.sm_scale, out=out, lse=lse)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    stream.synchronize()
+    if attn.device_status(dev) != 0:
+        raise SystemExit("device status word reports an expired wait during warm-up")
+
+    if args.profile:
+        t = timed_launches(step, stream, args.steps)
+        print(json.dumps({"profile": w.name, "ms": t}), flush=True)
+        return 0
+
+    # ---- timed region: K steps, barrier + synchronize on both sides, max over ranks ----------
+    sampler = ClockSampler(physical_gpu_index(local))
+    with sampler:
+        if pg:
+            pg.barrier()
+        torch.cuda.synchronize()
+        launch_ms = timed_launches(step, stream, args.steps)
+        torch.cuda.synchronize()
+        if pg:
+            pg.barrier()
+    total_ms = sum(launch_ms)
+    if pg:
+        t = torch.tensor([total_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item())
+    if attn.device_status(dev) != 0:
+        raise SystemExit("device status word reports an expired wait in the timed region")
+    clocks = sampler.summary()
+
+    ms_per_step = total_ms / args.steps
+    value = w.flops * args.steps * world / (total_ms * 1e-3) / 1e12
+    mean_launch_ms = statistics.mean(launch_ms)
+    achieved = w.flops / (mean_launch_ms * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    peak_sus = float(peaks.get("bf16_tflops_sustained", peak))
+    roofline = {
+        "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+        "frac": achieved / peak, "traffic": load_traffic(w.name),
+        "peak_source": f"{peak_src} bf16 dense (burst)",
+        "frac_of_sustained": achieved / peak_sus,
+        "hbm_gbs_algorithmic": w.bytes / (mean_launch_ms * 1e-3) / 1e9,
+    }
+
+    # ---- end to end through the public API: pinned host buffers, copies inside the region -----
+    e2e = None
+    if rank == 0 or world > 1:
+        hq_, hk_, hv_ = (t.cpu().pin_memory() for t in (q, k, v))
+        ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+        def e2e_step():
+            dq.copy_(hq_, non_blocking=True)
+            dk.copy_(hk_, non_blocking=True)
+            dv.copy_(hv_, non_blocking=True)
+            attn.attn_fwd(dq, dk, dv, causal=w.causal, sm_scale=w.sm_scale, out=out, lse=lse)
+            ho.copy_(out, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+
+        n_e2e = max(3, min(args.steps, 20))
+        with torch.cuda.stream(stream):
+            e2e_step()
+        stream.synchronize()
+        e_ms = timed_launches(e2e_step, stream, n_e2e)
+        h2d = sum(t.numel() * t.element_size() for t in (hq_, hk_, hv_))
+        d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+        e2e = {"value": w.flops / (statistics.mean(e_ms) * 1e-3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": statistics.mean(e_ms), "steps": n_e2e}
+
+    # ---- context: the other long-context lengths (same kernel), not the headline -------------
+    sweep = []
+    if not args.no_sweep and rank == 0:
+        for n in sorted(wl.LONG):
+            if n == w.N and w.name.startswith("long"):
+                sweep.append({"N": n, "ms": mean_launch_ms, "tflops": achieved,
+                              "frac": achieved / peak})
+                continue
+            ws = wl.LONG[n]
+            sq, sk, sv = (t.to(dev) for t in wl.make_qkv(ws))
+            so, sl = torch.empty_like(sq), torch.empty(ws.B, ws.Hq, ws.N, dtype=torch.float32,
+                                                       device=dev)
+
+            def sstep():
+                attn.attn_fwd(sq, sk, sv, causal=ws.causal, sm_scale=ws.sm_scale, out=so, lse=sl)
+
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    sstep()
+            ms = statistics.mean(timed_launches(sstep, stream, 20))
+            tf = ws.flops / (ms * 1e-3) / 1e12
+            sweep.append({"N": n, "ms": ms, "tflops": tf, "frac": tf / peak})
+            del sq, sk, sv, so, sl
+
+    # ---- CPU baseline: the oracle as it stands, bounded sample, rank 0 at N=1 only -----------
+    cpu = None
+    if rank == 0 and world == 1:
+        import oracle
+
+        qc, kc, vc = (t.cpu() for t in (q, k, v))
+        n_rows, _ = time_oracle(w, qc, kc, vc, args.cpu_seconds)
+        rows = cpu_sample_rows(w, n_rows)
+        t0 = time.perf_counter()
+        oracle.attn_ref(qc, kc, vc, w.causal, w.sm_scale, rows=rows.numpy())
+        dt = time.perf_counter() - t0
+        f = sample_flops(w, rows)
+        cpu = {"value": f / dt / 1e12, "unit": UNIT, "cores": oracle.default_threads(),
+               "kind": "oracle",
+               "sample": f"{n_rows} seeded query rows per head x {w.B * w.Hq} heads of {w.name}; "
+                         f"{f / 1e9:.2f} GFLOP in {dt:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": config_of(w, "inputs and output exceed the 129 MB L2; no flush"),
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": args.steps, "clocks": clocks, "sweep": sweep,
+            "kernel_sha": kernel_hash(),
+        }
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

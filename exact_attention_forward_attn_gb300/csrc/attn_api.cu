@@ -132,11 +132,12 @@ int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
 extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B,
                         int Hq, int Hkv, int N, int D, int causal, float sm_scale, void* stream) {
     // ---- host-side validation: nothing is launched or written on failure ---------------------
-    if (!q || !k || !v || !out || !lse) return ATTN_ERR_NULL;
     if (B < 0 || N < 0 || Hq <= 0 || Hkv <= 0) return ATTN_ERR_SHAPE;
     if (Hq % Hkv != 0) return ATTN_ERR_HEADS;
     if (D != 64 && D != 128) return ATTN_ERR_HEADDIM;
     if (!std::isfinite(sm_scale) || !(sm_scale > 0.f)) return ATTN_ERR_SCALE;
+    if (B == 0 || N == 0) return ATTN_OK;  // empty problem: nothing to read or write
+    if (!q || !k || !v || !out || !lse) return ATTN_ERR_NULL;
     const uintptr_t align_bits = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
                                  reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out) |
                                  reinterpret_cast<uintptr_t>(lse);
@@ -148,7 +149,6 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* out, 
     const int64_t n_pairs = (n_tiles + 1) / 2;
     const int64_t grid = n_pairs * bh;
     if (grid > 0x7fffffffLL || bh > 0x7fffffffLL) return ATTN_ERR_SHAPE;
-    if (B == 0 || N == 0) return ATTN_OK;  // empty problem: nothing to compute
 
     const int64_t q_bytes = bh * N * D * 2, kv_bytes = bh_kv * N * D * 2, lse_bytes = bh * N * 4;
     if (overlaps(out, q_bytes, q, q_bytes) || overlaps(out, q_bytes, k, kv_bytes) ||

@@ -59,7 +59,8 @@ typedef enum {
  *            q, k, v or lse
  *   lse      fp32 [B, Hq, N]; written with the natural-log LSE of the scaled, masked scores
  *   B, Hq, Hkv, N, D   sizes; Hq % Hkv == 0 (MQA is Hkv == 1); D in {64, 128}; B == 0 or N == 0
- *            is a valid empty problem (returns ATTN_OK, launches nothing)
+ *            is a valid empty problem (returns ATTN_OK, launches nothing; the pointers may then
+ *            be NULL, as zero-size allocations often are)
  *   causal   0: every key visible; nonzero: key j visible to query i iff j <= i
  *   sm_scale score scale (callers usually pass 1/sqrt(D)); finite and > 0
  *   stream   a cudaStream_t of the current device, passed as void* (NULL = legacy default stream)

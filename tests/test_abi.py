@@ -79,6 +79,11 @@ def test_host_validation(lib, kw, status):
 def test_empty_problem_is_a_no_op(lib):
     assert _call(lib, B=0) == 0
     assert _call(lib, N=0) == 0
+    # zero-size tensors often have NULL data pointers
+    assert _call(lib, B=0, q=0, k=0, v=0, out=0, lse=0) == 0
+    assert _call(lib, N=0, q=0, k=0, v=0, out=0, lse=0) == 0
+    # shape errors still win over the empty shortcut
+    assert _call(lib, B=0, Hq=3, Hkv=2) == -3
 
 
 def test_aliasing_output_is_rejected(lib):
