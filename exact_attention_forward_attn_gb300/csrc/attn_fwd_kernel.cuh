@@ -67,8 +67,8 @@ struct SmemLayout {
     static constexpr int kBarKvFull = 1;
     static constexpr int kBarKvEmpty = kBarKvFull + kStages;
     static constexpr int kBarSFull = kBarKvEmpty + kStages;   // [2]
-    static constexpr int kBarPReady = kBarSFull + 2;          // [2]
-    static constexpr int kBarODone = kBarPReady + 2;          // [2]
+    static constexpr int kBarPReady = kBarSFull + 2;          // [2 tiles][2 halves]
+    static constexpr int kBarODone = kBarPReady + 4;          // [2]
     static constexpr int kNumBars = kBarODone + 2;
     static constexpr int kTmemSlot = kBars + kNumBars * 8;
     static constexpr int kAbort = kTmemSlot + 8;
@@ -127,7 +127,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(bar(L::kBarSFull + t), 1);
-            mbar_init(bar(L::kBarPReady + t), 128);
+            mbar_init(bar(L::kBarPReady + 2 * t + 0), 128);
+            mbar_init(bar(L::kBarPReady + 2 * t + 1), 128);
             mbar_init(bar(L::kBarODone + t), 1);
         }
         *abort_flag = 0;
@@ -189,14 +190,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 smem_desc_sw128(ka + off, 16, 1024), kIdescS, kk > 0);
                 }
             };
-            auto pv_mma = [=](int t, int vslot, bool accumulate_first) {
+            // O_t += P_t[:, 64h : 64h+64] . V[64h : 64h+64, :] (4 MMAs of K = 16 per half)
+            auto pv_mma_half = [=](int t, int vslot, int half, bool accumulate_first) {
                 const uint32_t va = sbase + L::kKV + vslot * L::kTileBytes;
 #pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk) {
+                for (int k4 = 0; k4 < kBN / 32; ++k4) {
+                    const int kk = half * (kBN / 32) + k4;
                     mma_bf16_ts(tmem + tmem_o_col(t), tmem + tmem_s_col(t) + kk * 8,
                                 smem_desc_sw128(va + kk * 2048, L::kPanelBytes, 1024), kIdescPV,
                                 (accumulate_first || kk > 0) ? 1u : 0u);
                 }
+            };
+            // P_t arrives in two halves (keys 0-63, 64-127); each half's MMAs start on arrival.
+            auto pv_mma = [=](int t, int vslot, bool accumulate_first, uint32_t phase) -> bool {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    if (!mbar_wait_bounded(bar(L::kBarPReady + 2 * t + h), phase, abort_flag,
+                                           status_word))
+                        return false;
+                    tc_fence_after();
+                    pv_mma_half(t, vslot, h, accumulate_first);
+                }
+                return true;
             };
             auto kv_slot = [](int idx) { return idx % kStages; };
             auto kv_phase = [](int idx) { return static_cast<uint32_t>((idx / kStages) & 1); };
@@ -222,12 +237,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        abort_flag, status_word);
                 if (!ok) break;
                 if (j <= last0) {
-                    ok = mbar_wait_bounded(bar(L::kBarPReady + 0), p_phase[0], abort_flag,
-                                           status_word);
+                    ok = pv_mma(0, kv_slot(vidx), j > 0, p_phase[0]);
                     if (!ok) break;
                     p_phase[0] ^= 1u;
-                    tc_fence_after();
-                    pv_mma(0, kv_slot(vidx), j > 0);
                     if (j == last0) mma_commit(bar(L::kBarODone + 0));
                 }
                 const bool next = j + 1 < n_kv;
@@ -242,12 +254,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (has_q1 && j <= last1) {
-                    ok = mbar_wait_bounded(bar(L::kBarPReady + 1), p_phase[1], abort_flag,
-                                           status_word);
+                    ok = pv_mma(1, kv_slot(vidx), j > 0, p_phase[1]);
                     if (!ok) break;
                     p_phase[1] ^= 1u;
-                    tc_fence_after();
-                    pv_mma(1, kv_slot(vidx), j > 0);
                     if (j == last1) mma_commit(bar(L::kBarODone + 1));
                 }
                 mma_commit(bar(L::kBarKvEmpty + kv_slot(vidx)));
@@ -283,14 +292,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 float s[kBN];
                 {
-                    uint32_t r[32];
+                    uint32_t r[kBN];
 #pragma unroll
-                    for (int cc = 0; cc < kBN / 32; ++cc) {
-                        tmem_ld32(s_addr + cc * 32, r);
-                        tmem_wait_ld();
+                    for (int cc = 0; cc < kBN / 32; ++cc)
+                        tmem_ld32(s_addr + cc * 32,
+                                  *reinterpret_cast<uint32_t(*)[32]>(&r[cc * 32]));
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) s[cc * 32 + i] = __uint_as_float(r[i]);
-                    }
+                    for (int i = 0; i < kBN; ++i) s[i] = __uint_as_float(r[i]);
                 }
                 // masks: only on the causal diagonal tile, or on a ragged last key tile
                 if (p.causal && j == q_tile) {
@@ -303,54 +312,59 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = 0; i < kBN; ++i)
                         if (i >= valid) s[i] = -INFINITY;
                 }
+                // row maximum: 8 independent chains of 3-input max
                 float mx[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) mx[i] = s[i];
+                for (int k = 0; k < 8; ++k) mx[k] = fmaxf(s[k], s[k + 8]);
 #pragma unroll
-                for (int i = 8; i < kBN; ++i) mx[i & 7] = fmaxf(mx[i & 7], s[i]);
+                for (int i = 16; i < kBN; i += 16)
 #pragma unroll
-                for (int w = 4; w >= 1; w >>= 1)
-#pragma unroll
-                    for (int i = 0; i < w; ++i) mx[i] = fmaxf(mx[i], mx[i + w]);
-                const float m_cand = mx[0] * c;
+                    for (int k = 0; k < 8; ++k) mx[k] = fmax3(mx[k], s[i + k], s[i + 8 + k]);
+                const float row_max =
+                    fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+                const float m_cand = row_max * c;
                 const float m_new = (m_cand > m + kRescaleThreshold) ? m_cand : m;
                 const float alpha = ex2_approx(m - m_new);  // 1 if unchanged, 0 on the first tile
                 const bool rescale = j > 0 && __any_sync(0xffffffffu, m_new != m);
-                l *= alpha;
                 m = m_new;
                 const float neg_m = -m;
-                float sum[4] = {0.f, 0.f, 0.f, 0.f};
+                // p = exp2(c*s - m) in two halves of 64 keys; each half is published to the MMA
+                // warp as soon as it is in TMEM, so P.V on keys 0-63 overlaps the second half.
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int cc = 0; cc < kBN / 32; ++cc) {
-                    uint32_t pk[16];
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t pk[32];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float p0 = ex2_approx(fmaf(s[cc * 32 + 2 * i], c, neg_m));
-                        const float p1 = ex2_approx(fmaf(s[cc * 32 + 2 * i + 1], c, neg_m));
-                        sum[(2 * i) & 3] += p0;
-                        sum[(2 * i + 1) & 3] += p1;
+                    for (int i = 0; i < 32; ++i) {
+                        const int col = h * 64 + 2 * i;
+                        float x0, x1;
+                        ffma2(x0, x1, s[col], s[col + 1], c, c, neg_m, neg_m);
+                        const float p0 = ex2_approx(x0);
+                        const float p1 = ex2_approx(x1);
+                        const int a = (i & 1) * 2;
+                        fadd2(acc[a], acc[a + 1], acc[a], acc[a + 1], p0, p1);
                         pk[i] = pack_bf16x2(p0, p1);
                     }
-                    tmem_st16(s_addr + cc * 16, pk);
-                }
-                l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
-                if (rescale) {
-                    // correction: O_row *= alpha.  The PV MMA of tile j-1 completed before S of
-                    // tile j (in-order MMAs, one commit), and PV of tile j waits for P_ready.
+                    tmem_st32(s_addr + h * 32, pk);
+                    if (h == 0 && rescale) {
+                        // correction: O_row *= alpha before this tile's P.V is issued.  The P.V of
+                        // tile j-1 completed before S of tile j (in-order MMAs, one commit).
 #pragma unroll
-                    for (int cc = 0; cc < D / 32; ++cc) {
-                        uint32_t r[32];
-                        tmem_ld32(o_addr + cc * 32, r);
-                        tmem_wait_ld();
+                        for (int cc = 0; cc < D / 32; ++cc) {
+                            uint32_t r[32];
+                            tmem_ld32(o_addr + cc * 32, r);
+                            tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                        tmem_st32(o_addr + cc * 32, r);
+                            for (int i = 0; i < 32; ++i)
+                                r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                            tmem_st32(o_addr + cc * 32, r);
+                        }
                     }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(bar(L::kBarPReady + 2 * t + h));
                 }
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(bar(L::kBarPReady + t));
+                l = l * alpha + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
             }
 
             // ---- epilogue: O = acc / l -> bf16 -> smem (over Q_t) -> TMA store; LSE ----------
