@@ -11,10 +11,11 @@
 //   recurrence (exp2 domain: scores are pre-multiplied by sm_scale*log2(e)); after the last tile
 //   O = acc / l and LSE = ln2 * (m + log2 l).  The N x N score matrix never leaves the SM.
 //
-// GB300 mapping (one CTA per pair of 128-row Q tiles, 320 threads):
-//   warp 9      TMA producer: Q0/Q1 once, then K_j, V_j through a KV_STAGES-deep mbarrier ring.
-//   warp 8      MMA issuer (one lane): S_t = Q_t K_j^T (SS form, fp32 in TMEM) and
-//               O_t += P_t V_j (P from TMEM, V from smem); tcgen05.commit signals completion.
+// GB300 mapping (one CTA per pair of 128-row Q tiles, 352 threads):
+//   warp 10     TMA producer: Q0/Q1 once, then K_j, V_j through a KV_STAGES-deep mbarrier ring.
+//   warps 8, 9  MMA issuers (one lane each), warp 8 + t for Q tile t: S_t = Q_t K_j^T (SS form,
+//               fp32 in TMEM) and O_t += P_t V_j (P from TMEM, V from smem); tcgen05.commit
+//               signals completion.
 //   warps 0-3   softmax for Q tile 0, warps 4-7 for Q tile 1: one thread per query row reads its
 //               S row from TMEM, masks (diagonal causal tile / ragged last key tile only), updates
 //               m and l, rescales its O row in TMEM when m moved, writes P (bf16) over S in TMEM;
@@ -38,9 +39,9 @@ constexpr int kBM = 128;          // query rows per Q tile (MMA M)
 constexpr int kBN = 128;          // key rows per KV tile (MMA N of S, K of P.V)
 constexpr int kQTiles = 2;        // Q tiles per CTA
 constexpr int kStages = 4;        // K/V ring slots (K_j and V_j take one slot each)
-constexpr int kThreads = 320;     // 10 warps
-constexpr int kMmaWarp = 8;
-constexpr int kLoadWarp = 9;
+constexpr int kThreads = 352;     // 11 warps
+constexpr int kMmaWarp0 = 8;      // issues the MMAs of Q tile 0; warp 9 those of Q tile 1
+constexpr int kLoadWarp = 10;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLn2 = 0.69314718055994530942f;
@@ -69,7 +70,8 @@ struct SmemLayout {
     static constexpr int kBarSFull = kBarKvEmpty + kStages;   // [2]
     static constexpr int kBarPReady = kBarSFull + 2;          // [2 tiles][2 halves]
     static constexpr int kBarODone = kBarPReady + 4;          // [2]
-    static constexpr int kNumBars = kBarODone + 2;
+    static constexpr int kBarTurn = kBarODone + 2;            // [2]: softmax group t may run exp2
+    static constexpr int kNumBars = kBarTurn + 2;
     static constexpr int kTmemSlot = kBars + kNumBars * 8;
     static constexpr int kAbort = kTmemSlot + 8;
     static constexpr int kBytes = kAbort + 8;
@@ -123,19 +125,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar(L::kBarQ), 1);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar(L::kBarKvFull + s), 1);
-            mbar_init(bar(L::kBarKvEmpty + s), 1);
+            mbar_init(bar(L::kBarKvEmpty + s), has_q1 ? 2 : 1);  // one release per issuer
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(bar(L::kBarSFull + t), 1);
             mbar_init(bar(L::kBarPReady + 2 * t + 0), 128);
             mbar_init(bar(L::kBarPReady + 2 * t + 1), 128);
             mbar_init(bar(L::kBarODone + t), 1);
+            mbar_init(bar(L::kBarTurn + t), 128);
         }
         *abort_flag = 0;
         fence_mbarrier_init();
         fence_proxy_async_smem();
     }
-    if (warp == kMmaWarp) {
+    if (warp == kMmaWarp0) {
         tmem_alloc(smem_addr(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
@@ -177,95 +180,89 @@ __global__ void __launch_bounds__(kThreads, 1)
         producer_done:;
         }
         __syncwarp();
-    } else if (warp == kMmaWarp) {
-        // =========================== MMA issuer (one lane) =====================================
-        if (lane == 0) {
-            auto s_mma = [=](int t, int kslot) {
-                const uint32_t qa = sbase + L::kQ + t * L::kTileBytes;
+    } else if (warp == kMmaWarp0 || warp == kMmaWarp0 + 1) {
+        // ============ MMA issuers: warp 8 for Q tile 0, warp 9 for Q tile 1 (one lane each) =====
+        // A single thread can start a tcgen05.mma only every ~120 cycles, about twice the tensor
+        // time of an M=128, N=128, K=16 MMA; two issuers with independent accumulators keep the
+        // tensor core fed while the other tile's issuer waits for its softmax.
+        const int t = warp - kMmaWarp0;
+        if (lane == 0 && (t == 0 || has_q1)) {
+            const int last = t == 0 ? last0 : last1;
+            const uint32_t s_tmem = tmem + tmem_s_col(t);
+            const uint32_t o_tmem = tmem + tmem_o_col(t);
+            const uint32_t qa = sbase + L::kQ + t * L::kTileBytes;
+            auto kv_slot = [](int idx) { return idx % kStages; };
+            auto kv_phase = [](int idx) { return static_cast<uint32_t>((idx / kStages) & 1); };
+            auto wait_full = [=](int idx) {
+                return mbar_wait_bounded(bar(L::kBarKvFull + kv_slot(idx)), kv_phase(idx),
+                                         abort_flag, status_word);
+            };
+            // S_t = Q_t . K^T  (8 MMAs of K = 16 at D = 128)
+            auto s_mma = [=](int kslot) {
                 const uint32_t ka = sbase + L::kKV + kslot * L::kTileBytes;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
-                    mma_bf16_ss(tmem + tmem_s_col(t), smem_desc_sw128(qa + off, 16, 1024),
+                    mma_bf16_ss(s_tmem, smem_desc_sw128(qa + off, 16, 1024),
                                 smem_desc_sw128(ka + off, 16, 1024), kIdescS, kk > 0);
                 }
             };
-            // O_t += P_t[:, 64h : 64h+64] . V[64h : 64h+64, :] (4 MMAs of K = 16 per half)
-            auto pv_mma_half = [=](int t, int vslot, int half, bool accumulate_first) {
+            // O_t += P_t . V, P_t arriving in two halves (keys 0-63, 64-127): each half's four
+            // MMAs start as soon as that half is in TMEM.
+            auto pv_mma = [=](int vslot, bool accumulate_first, uint32_t phase) -> bool {
                 const uint32_t va = sbase + L::kKV + vslot * L::kTileBytes;
-#pragma unroll
-                for (int k4 = 0; k4 < kBN / 32; ++k4) {
-                    const int kk = half * (kBN / 32) + k4;
-                    mma_bf16_ts(tmem + tmem_o_col(t), tmem + tmem_s_col(t) + kk * 8,
-                                smem_desc_sw128(va + kk * 2048, L::kPanelBytes, 1024), kIdescPV,
-                                (accumulate_first || kk > 0) ? 1u : 0u);
-                }
-            };
-            // P_t arrives in two halves (keys 0-63, 64-127); each half's MMAs start on arrival.
-            auto pv_mma = [=](int t, int vslot, bool accumulate_first, uint32_t phase) -> bool {
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     if (!mbar_wait_bounded(bar(L::kBarPReady + 2 * t + h), phase, abort_flag,
                                            status_word))
                         return false;
                     tc_fence_after();
-                    pv_mma_half(t, vslot, h, accumulate_first);
+#pragma unroll
+                    for (int k4 = 0; k4 < kBN / 32; ++k4) {
+                        const int kk = h * (kBN / 32) + k4;
+                        mma_bf16_ts(o_tmem, s_tmem + kk * 8,
+                                    smem_desc_sw128(va + kk * 2048, L::kPanelBytes, 1024),
+                                    kIdescPV, (accumulate_first || kk > 0) ? 1u : 0u);
+                    }
                 }
                 return true;
             };
-            auto kv_slot = [](int idx) { return idx % kStages; };
-            auto kv_phase = [](int idx) { return static_cast<uint32_t>((idx / kStages) & 1); };
-            uint32_t p_phase[2] = {0, 0};
 
+            uint32_t p_phase = 0;
             bool ok = mbar_wait_bounded(bar(L::kBarQ), 0, abort_flag, status_word);
-            if (ok) ok = mbar_wait_bounded(bar(L::kBarKvFull + kv_slot(0)), kv_phase(0),
-                                           abort_flag, status_word);
+            if (ok) ok = wait_full(0);
             if (ok) {
                 tc_fence_after();
-                s_mma(0, kv_slot(0));
-                mma_commit(bar(L::kBarSFull + 0));
-                if (has_q1) {
-                    s_mma(1, kv_slot(0));
-                    mma_commit(bar(L::kBarSFull + 1));
-                }
+                s_mma(kv_slot(0));
+                mma_commit(bar(L::kBarSFull + t));
                 mma_commit(bar(L::kBarKvEmpty + kv_slot(0)));
             }
-            for (int j = 0; ok && j < n_kv; ++j) {
+            for (int j = 0; ok && j <= last; ++j) {
                 const int vidx = 2 * j + 1;
                 const int kidx = 2 * j + 2;  // K_{j+1}
-                ok = mbar_wait_bounded(bar(L::kBarKvFull + kv_slot(vidx)), kv_phase(vidx),
-                                       abort_flag, status_word);
+                ok = wait_full(vidx);
                 if (!ok) break;
-                if (j <= last0) {
-                    ok = pv_mma(0, kv_slot(vidx), j > 0, p_phase[0]);
-                    if (!ok) break;
-                    p_phase[0] ^= 1u;
-                    if (j == last0) mma_commit(bar(L::kBarODone + 0));
-                }
-                const bool next = j + 1 < n_kv;
-                if (next) {
-                    ok = mbar_wait_bounded(bar(L::kBarKvFull + kv_slot(kidx)), kv_phase(kidx),
-                                           abort_flag, status_word);
+                ok = pv_mma(kv_slot(vidx), j > 0, p_phase);
+                if (!ok) break;
+                p_phase ^= 1u;
+                if (j == last) mma_commit(bar(L::kBarODone + t));
+                mma_commit(bar(L::kBarKvEmpty + kv_slot(vidx)));
+                if (j + 1 <= last) {
+                    ok = wait_full(kidx);
                     if (!ok) break;
                     tc_fence_after();
-                    if (j + 1 <= last0) {
-                        s_mma(0, kv_slot(kidx));
-                        mma_commit(bar(L::kBarSFull + 0));
-                    }
-                }
-                if (has_q1 && j <= last1) {
-                    ok = pv_mma(1, kv_slot(vidx), j > 0, p_phase[1]);
-                    if (!ok) break;
-                    p_phase[1] ^= 1u;
-                    if (j == last1) mma_commit(bar(L::kBarODone + 1));
-                }
-                mma_commit(bar(L::kBarKvEmpty + kv_slot(vidx)));
-                if (next) {
-                    if (has_q1 && j + 1 <= last1) {
-                        s_mma(1, kv_slot(kidx));
-                        mma_commit(bar(L::kBarSFull + 1));
-                    }
+                    s_mma(kv_slot(kidx));
+                    mma_commit(bar(L::kBarSFull + t));
                     mma_commit(bar(L::kBarKvEmpty + kv_slot(kidx)));
+                }
+            }
+            // KV tiles this Q tile does not need (under the causal mask, the last one for Q tile
+            // 0): release each slot once its data has landed, so every slot phase gets one
+            // release per issuer and never completes early.
+            for (int j = last + 1; ok && j < n_kv; ++j) {
+                for (int kv = 0; ok && kv < 2; ++kv) {
+                    ok = wait_full(2 * j + kv);
+                    if (ok) mbar_arrive(bar(L::kBarKvEmpty + kv_slot(2 * j + kv)));
                 }
             }
         }
@@ -328,6 +325,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool rescale = j > 0 && __any_sync(0xffffffffu, m_new != m);
                 m = m_new;
                 const float neg_m = -m;
+                // Ping-pong: the exp2 phases of the two softmax groups alternate (tile 0 step j,
+                // tile 1 step j, tile 0 step j+1, ...), so one group's exponentials overlap the
+                // other tile's MMAs instead of competing for the same issue slots and MUFU.
+                const bool turn_wait = has_q1 && (t == 0 ? j > 0 : j <= last0);
+                if (turn_wait) {
+                    ok = mbar_wait_warp(bar(L::kBarTurn + t), (t == 0 ? j - 1 : j) & 1, abort_flag,
+                                        status_word);
+                    if (!ok) break;
+                }
                 // p = exp2(c*s - m) in two halves of 64 keys; each half is published to the MMA
                 // warp as soon as it is in TMEM, so P.V on keys 0-63 overlaps the second half.
                 float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -365,6 +371,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive(bar(L::kBarPReady + 2 * t + h));
                 }
                 l = l * alpha + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
+                // hand the turn to the other group (tile 1 only while tile 0 has steps left)
+                if (has_q1 && (t == 1 ? j < last0 : true)) mbar_arrive(bar(L::kBarTurn + (t ^ 1)));
             }
 
             // ---- epilogue: O = acc / l -> bf16 -> smem (over Q_t) -> TMA store; LSE ----------
@@ -410,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- teardown ------------------------------------------------------------------------------
     tc_fence_before();
     __syncthreads();
-    if (warp == kMmaWarp) {
+    if (warp == kMmaWarp0) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
