@@ -287,6 +287,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = mbar_wait_warp(bar(L::kBarSFull + t), j & 1, abort_flag, status_word);
                 if (!ok) break;
                 tc_fence_after();
+                // Masks (the causal diagonal tile, or the ragged last key tile) are applied in
+                // TMEM before the row is loaded, so the common unmasked step carries no mask code.
+                const bool diag = p.causal && j == q_tile;
+                const bool tail = !p.causal && j == p.n_tiles - 1 && (p.N % kBN) != 0;
+                if (diag || tail) {
+                    const int lim = diag ? row + 1 : p.N - j * kBN;  // first masked key
+#pragma unroll
+                    for (int cc = 0; cc < kBN / 32; ++cc) {
+                        uint32_t r[32];
+                        tmem_ld32(s_addr + cc * 32, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (cc * 32 + i >= lim) r[i] = __float_as_uint(-INFINITY);
+                        tmem_st32(s_addr + cc * 32, r);
+                    }
+                    tmem_wait_st();
+                }
                 float s[kBN];
                 {
                     uint32_t r[kBN];
@@ -297,17 +315,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < kBN; ++i) s[i] = __uint_as_float(r[i]);
-                }
-                // masks: only on the causal diagonal tile, or on a ragged last key tile
-                if (p.causal && j == q_tile) {
-#pragma unroll
-                    for (int i = 0; i < kBN; ++i)
-                        if (i > row) s[i] = -INFINITY;
-                } else if (!p.causal && j == p.n_tiles - 1 && (p.N % kBN) != 0) {
-                    const int valid = p.N - j * kBN;
-#pragma unroll
-                    for (int i = 0; i < kBN; ++i)
-                        if (i >= valid) s[i] = -INFINITY;
                 }
                 // row maximum: 8 independent chains of 3-input max
                 float mx[8];
