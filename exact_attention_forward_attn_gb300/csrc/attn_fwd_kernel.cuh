@@ -181,12 +181,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else if (warp == kMmaWarp0 || warp == kMmaWarp0 + 1) {
-        // ============ MMA issuers: warp 8 for Q tile 0, warp 9 for Q tile 1 (one lane each) =====
-        // A single thread can start a tcgen05.mma only every ~120 cycles, about twice the tensor
-        // time of an M=128, N=128, K=16 MMA; two issuers with independent accumulators keep the
-        // tensor core fed while the other tile's issuer waits for its softmax.
+        // ============ MMA issuers: warp 8 for Q tile 0, warp 9 for Q tile 1 ======================
+        // One issuing thread starts a tcgen05.mma only every ~95 cycles (warp-uniform loop,
+        // elected lane), more than the 64 tensor cycles of an M=128, N=128, K=16 MMA; two issuers
+        // with independent accumulators keep the tensor core fed, also while the other tile's
+        // issuer waits for its softmax.
         const int t = warp - kMmaWarp0;
-        if (lane == 0 && (t == 0 || has_q1)) {
+        if (t == 0 || has_q1) {  // warp-uniform: every lane runs the loop, one elected lane issues
             const int last = t == 0 ? last0 : last1;
             const uint32_t s_tmem = tmem + tmem_s_col(t);
             const uint32_t o_tmem = tmem + tmem_o_col(t);
@@ -194,8 +195,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto kv_slot = [](int idx) { return idx % kStages; };
             auto kv_phase = [](int idx) { return static_cast<uint32_t>((idx / kStages) & 1); };
             auto wait_full = [=](int idx) {
-                return mbar_wait_bounded(bar(L::kBarKvFull + kv_slot(idx)), kv_phase(idx),
-                                         abort_flag, status_word);
+                return mbar_wait_warp(bar(L::kBarKvFull + kv_slot(idx)), kv_phase(idx),
+                                      abort_flag, status_word);
             };
             // S_t = Q_t . K^T  (8 MMAs of K = 16 at D = 128)
             auto s_mma = [=](int kslot) {
@@ -203,8 +204,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
-                    mma_bf16_ss(s_tmem, smem_desc_sw128(qa + off, 16, 1024),
-                                smem_desc_sw128(ka + off, 16, 1024), kIdescS, kk > 0);
+                    mma_bf16_ss_warp(s_tmem, smem_desc_sw128(qa + off, 16, 1024),
+                                     smem_desc_sw128(ka + off, 16, 1024), kIdescS, kk > 0);
                 }
             };
             // O_t += P_t . V, P_t arriving in two halves (keys 0-63, 64-127): each half's four
@@ -213,29 +214,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t va = sbase + L::kKV + vslot * L::kTileBytes;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    if (!mbar_wait_bounded(bar(L::kBarPReady + 2 * t + h), phase, abort_flag,
-                                           status_word))
+                    if (!mbar_wait_warp(bar(L::kBarPReady + 2 * t + h), phase, abort_flag,
+                                        status_word))
                         return false;
                     tc_fence_after();
 #pragma unroll
                     for (int k4 = 0; k4 < kBN / 32; ++k4) {
                         const int kk = h * (kBN / 32) + k4;
-                        mma_bf16_ts(o_tmem, s_tmem + kk * 8,
-                                    smem_desc_sw128(va + kk * 2048, L::kPanelBytes, 1024),
-                                    kIdescPV, (accumulate_first || kk > 0) ? 1u : 0u);
+                        mma_bf16_ts_warp(o_tmem, s_tmem + kk * 8,
+                                         smem_desc_sw128(va + kk * 2048, L::kPanelBytes, 1024),
+                                         kIdescPV, (accumulate_first || kk > 0) ? 1u : 0u);
                     }
                 }
                 return true;
             };
 
             uint32_t p_phase = 0;
-            bool ok = mbar_wait_bounded(bar(L::kBarQ), 0, abort_flag, status_word);
+            bool ok = mbar_wait_warp(bar(L::kBarQ), 0, abort_flag, status_word);
             if (ok) ok = wait_full(0);
             if (ok) {
                 tc_fence_after();
                 s_mma(kv_slot(0));
-                mma_commit(bar(L::kBarSFull + t));
-                mma_commit(bar(L::kBarKvEmpty + kv_slot(0)));
+                mma_commit_warp(bar(L::kBarSFull + t));
+                mma_commit_warp(bar(L::kBarKvEmpty + kv_slot(0)));
             }
             for (int j = 0; ok && j <= last; ++j) {
                 const int vidx = 2 * j + 1;
@@ -245,15 +246,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = pv_mma(kv_slot(vidx), j > 0, p_phase);
                 if (!ok) break;
                 p_phase ^= 1u;
-                if (j == last) mma_commit(bar(L::kBarODone + t));
-                mma_commit(bar(L::kBarKvEmpty + kv_slot(vidx)));
+                if (j == last) mma_commit_warp(bar(L::kBarODone + t));
+                mma_commit_warp(bar(L::kBarKvEmpty + kv_slot(vidx)));
                 if (j + 1 <= last) {
                     ok = wait_full(kidx);
                     if (!ok) break;
                     tc_fence_after();
                     s_mma(kv_slot(kidx));
-                    mma_commit(bar(L::kBarSFull + t));
-                    mma_commit(bar(L::kBarKvEmpty + kv_slot(kidx)));
+                    mma_commit_warp(bar(L::kBarSFull + t));
+                    mma_commit_warp(bar(L::kBarKvEmpty + kv_slot(kidx)));
                 }
             }
             // KV tiles this Q tile does not need (under the causal mask, the last one for Q tile
@@ -262,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = last + 1; ok && j < n_kv; ++j) {
                 for (int kv = 0; ok && kv < 2; ++kv) {
                     ok = wait_full(2 * j + kv);
-                    if (ok) mbar_arrive(bar(L::kBarKvEmpty + kv_slot(2 * j + kv)));
+                    if (ok) mbar_arrive_warp(bar(L::kBarKvEmpty + kv_slot(2 * j + kv)));
                 }
             }
         }
