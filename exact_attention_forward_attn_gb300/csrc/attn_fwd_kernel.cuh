@@ -43,6 +43,7 @@ constexpr int kThreads = 352;     // 11 warps
 constexpr int kMmaWarp0 = 8;      // issues the MMAs of Q tile 0; warp 9 those of Q tile 1
 constexpr int kLoadWarp = 10;
 constexpr uint32_t kTmemCols = 512;
+constexpr int kPParts = 2;        // P is published to the MMA issuer in this many key blocks
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -68,8 +69,8 @@ struct SmemLayout {
     static constexpr int kBarKvFull = 1;
     static constexpr int kBarKvEmpty = kBarKvFull + kStages;
     static constexpr int kBarSFull = kBarKvEmpty + kStages;   // [2]
-    static constexpr int kBarPReady = kBarSFull + 2;          // [2 tiles][2 halves]
-    static constexpr int kBarODone = kBarPReady + 4;          // [2]
+    static constexpr int kBarPReady = kBarSFull + 2;          // [2 tiles][kPParts key blocks]
+    static constexpr int kBarODone = kBarPReady + 2 * kPParts;  // [2]
     static constexpr int kBarTurn = kBarODone + 2;            // [2]: softmax group t may run exp2
     static constexpr int kNumBars = kBarTurn + 2;
     static constexpr int kTmemSlot = kBars + kNumBars * 8;
@@ -129,8 +130,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(bar(L::kBarSFull + t), 1);
-            mbar_init(bar(L::kBarPReady + 2 * t + 0), 128);
-            mbar_init(bar(L::kBarPReady + 2 * t + 1), 128);
+            for (int h = 0; h < kPParts; ++h) mbar_init(bar(L::kBarPReady + kPParts * t + h), 128);
             mbar_init(bar(L::kBarODone + t), 1);
             mbar_init(bar(L::kBarTurn + t), 128);
         }
@@ -208,19 +208,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      smem_desc_sw128(ka + off, 16, 1024), kIdescS, kk > 0);
                 }
             };
-            // O_t += P_t . V, P_t arriving in two halves (keys 0-63, 64-127): each half's four
-            // MMAs start as soon as that half is in TMEM.
+            // O_t += P_t . V, P_t arriving in kPParts key blocks: each block's MMAs start as soon
+            // as that block is in TMEM.
             auto pv_mma = [=](int vslot, bool accumulate_first, uint32_t phase) -> bool {
                 const uint32_t va = sbase + L::kKV + vslot * L::kTileBytes;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    if (!mbar_wait_warp(bar(L::kBarPReady + 2 * t + h), phase, abort_flag,
+                for (int h = 0; h < kPParts; ++h) {
+                    if (!mbar_wait_warp(bar(L::kBarPReady + kPParts * t + h), phase, abort_flag,
                                         status_word))
                         return false;
                     tc_fence_after();
 #pragma unroll
-                    for (int k4 = 0; k4 < kBN / 32; ++k4) {
-                        const int kk = h * (kBN / 32) + k4;
+                    for (int k4 = 0; k4 < kBN / 16 / kPParts; ++k4) {
+                        const int kk = h * (kBN / 16 / kPParts) + k4;
                         mma_bf16_ts_warp(o_tmem, s_tmem + kk * 8,
                                          smem_desc_sw128(va + kk * 2048, L::kPanelBytes, 1024),
                                          kIdescPV, (accumulate_first || kk > 0) ? 1u : 0u);
@@ -342,15 +342,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         status_word);
                     if (!ok) break;
                 }
-                // p = exp2(c*s - m) in two halves of 64 keys; each half is published to the MMA
-                // warp as soon as it is in TMEM, so P.V on keys 0-63 overlaps the second half.
+                // p = exp2(c*s - m) in kPParts key blocks; each block is published to the MMA
+                // issuer as soon as it is in TMEM, so its P.V overlaps the next block's exp2.
+                constexpr int kPairs = kBN / kPParts / 2;  // packed bf16 pairs per block
                 float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t pk[32];
+                for (int h = 0; h < kPParts; ++h) {
+                    uint32_t pk[kPairs];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int col = h * 64 + 2 * i;
+                    for (int i = 0; i < kPairs; ++i) {
+                        const int col = h * 2 * kPairs + 2 * i;
                         float x0, x1;
                         ffma2(x0, x1, s[col], s[col + 1], c, c, neg_m, neg_m);
                         const float p0 = ex2_approx(x0);
@@ -359,10 +360,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         fadd2(acc[a], acc[a + 1], acc[a], acc[a + 1], p0, p1);
                         pk[i] = pack_bf16x2(p0, p1);
                     }
-                    tmem_st32(s_addr + h * 32, pk);
-                    if (h == 0 && rescale) {
-                        // correction: O_row *= alpha before this tile's P.V is issued.  The P.V of
-                        // tile j-1 completed before S of tile j (in-order MMAs, one commit).
+                    if constexpr (kPairs == 32)
+                        tmem_st32(s_addr + h * kPairs, *reinterpret_cast<uint32_t(*)[32]>(pk));
+                    else
+                        tmem_st16(s_addr + h * kPairs, *reinterpret_cast<uint32_t(*)[16]>(pk));
+                    // The O correction (O_row *= alpha, rare thanks to the lazy maximum) must land
+                    // before this tile's P.V is issued; it runs once the scores of the first
+                    // blocks are dead (fewer live registers) and those blocks are published with
+                    // it.  The P.V of tile j-1 completed before S of tile j (in-order MMAs).
+                    constexpr int kRescaleAfter = kPParts > 2 ? 1 : 0;
+                    if (rescale && h < kRescaleAfter) continue;
+                    if (rescale && h == kRescaleAfter) {
 #pragma unroll
                         for (int cc = 0; cc < D / 32; ++cc) {
                             uint32_t r[32];
@@ -376,7 +384,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tmem_wait_st();
                     tc_fence_before();
-                    mbar_arrive(bar(L::kBarPReady + 2 * t + h));
+                    if (rescale && h == kRescaleAfter)
+                        for (int h0 = 0; h0 < kRescaleAfter; ++h0)
+                            mbar_arrive(bar(L::kBarPReady + kPParts * t + h0));
+                    mbar_arrive(bar(L::kBarPReady + kPParts * t + h));
                 }
                 l = l * alpha + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
                 // hand the turn to the other group (tile 1 only while tile 0 has steps left)
