@@ -107,13 +107,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // ---- work decomposition: heaviest (latest) Q-tile pairs first, heads innermost -------------
-    const int bh_count = p.B * p.Hq;
-    const int pair = p.n_pairs - 1 - static_cast<int>(blockIdx.x / bh_count);
-    const int bh = static_cast<int>(blockIdx.x % bh_count);
-    const int b = bh / p.Hq;
-    const int hq = bh % p.Hq;
-    const int bh_kv = b * p.Hkv + hq / p.group;
+    // ---- work decomposition --------------------------------------------------------------------
+    // Block order: (batch, KV head) outermost, then Q-tile pairs heaviest (latest) first, then the
+    // query heads sharing that KV head.  CTAs running together read the same K/V (which stays in
+    // L2), and the grid ends on the lightest causal pairs.
+    const int per_kv = p.n_pairs * p.group;
+    const int bh_kv = static_cast<int>(blockIdx.x / per_kv);
+    const int rem = static_cast<int>(blockIdx.x % per_kv);
+    const int pair = p.n_pairs - 1 - rem / p.group;
+    const int b = bh_kv / p.Hkv;
+    const int hq = (bh_kv % p.Hkv) * p.group + rem % p.group;
+    const int bh = b * p.Hq + hq;
     const int tile0 = 2 * pair;
     const bool has_q1 = tile0 + 1 < p.n_tiles;
     // last KV tile each Q tile needs (BM == BN: the causal diagonal tile has the Q tile's index)
