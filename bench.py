@@ -371,6 +371,41 @@ def main():
             sweep.append({"N": n, "ms": ms, "tflops": tf, "frac": tf / peak})
             del sq, sk, sv, so, sl
 
+    # ---- context: low-occupancy configurations, single pass vs split-KV (key-axis splits) -----
+    low_occ = []
+    if not args.no_sweep and rank == 0:
+        for ws_ in (wl.MHA, wl.MQA, wl.FEWHEADS):
+            lq, lk, lv = (t.to(dev) for t in wl.make_qkv(ws_))
+            lo = torch.empty_like(lq)
+            ll = torch.empty(ws_.B, ws_.Hq, ws_.N, dtype=torch.float32, device=dev)
+            # the library's choice, or 2 forced splits where it declines to split
+            n_sp = max(2, attn.splitkv_num_splits(ws_.B, ws_.Hq, ws_.N, ws_.D, ws_.causal))
+            wbuf = torch.empty(max(1, attn.splitkv_workspace_bytes(ws_.B, ws_.Hq, ws_.N, ws_.D,
+                                                                   n_sp)),
+                               dtype=torch.uint8, device=dev)
+
+            def single():
+                attn.attn_fwd(lq, lk, lv, causal=ws_.causal, sm_scale=ws_.sm_scale, out=lo,
+                              lse=ll)
+
+            def split():
+                attn.attn_fwd_splitkv(lq, lk, lv, causal=ws_.causal, sm_scale=ws_.sm_scale,
+                                      num_splits=n_sp, workspace=wbuf, out=lo, lse=ll)
+
+            entry = {"workload": ws_.name, "splits": n_sp,
+                     "library_choice": attn.splitkv_num_splits(ws_.B, ws_.Hq, ws_.N, ws_.D,
+                                                               ws_.causal)}
+            for name, fn in (("single", single), ("splitkv", split)):
+                with torch.cuda.stream(stream):
+                    for _ in range(5):
+                        fn()
+                ms = statistics.median(timed_launches(fn, stream, 50))
+                entry[f"{name}_us"] = ms * 1e3
+                entry[f"{name}_tflops"] = ws_.flops / (ms * 1e-3) / 1e12
+                entry[f"{name}_gbs"] = ws_.bytes / (ms * 1e-3) / 1e9
+            low_occ.append(entry)
+            del lq, lk, lv, lo, ll, wbuf
+
     # ---- CPU baseline: the oracle as it stands, bounded sample, rank 0 at N=1 only -----------
     cpu = None
     if rank == 0 and world == 1:
@@ -396,6 +431,7 @@ def main():
             "config": config_of(w, "inputs and output exceed the 129 MB L2; no flush"),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": args.steps, "clocks": clocks, "sweep": sweep,
+            "low_occupancy": low_occ,
             "kernel_sha": kernel_hash(),
         }
         print(json.dumps(line), flush=True)

@@ -17,6 +17,7 @@ STATUS_NAMES = {
     0: "ATTN_OK", -1: "ATTN_ERR_NULL", -2: "ATTN_ERR_SHAPE", -3: "ATTN_ERR_HEADS",
     -4: "ATTN_ERR_HEADDIM", -5: "ATTN_ERR_ALIGN", -6: "ATTN_ERR_SCALE", -7: "ATTN_ERR_ARCH",
     -8: "ATTN_ERR_CUDA", -9: "ATTN_ERR_TIMEOUT", -10: "ATTN_ERR_MEMORY", -11: "ATTN_ERR_ALIAS",
+    -12: "ATTN_ERR_SPLITS", -13: "ATTN_ERR_WORKSPACE",
 }
 
 
@@ -37,12 +38,7 @@ def _stream_handle(device):
     return torch.cuda.current_stream(device).cuda_stream
 
 
-def attn_fwd(q, k, v, causal: bool = False, sm_scale: float | None = None, out=None, lse=None):
-    """Fused attention forward on the current CUDA stream of ``q``'s device.
-
-    Returns ``(out, lse)``: out bf16 [B,Hq,N,D], lse fp32 [B,Hq,N].  ``out``/``lse`` may be passed
-    preallocated (contiguous, right shape and dtype).  Raises ``AttnError`` on a nonzero status.
-    """
+def _check_inputs(q, k, v):
     import torch
 
     for name, t in (("q", q), ("k", k), ("v", v)):
@@ -60,9 +56,13 @@ def attn_fwd(q, k, v, causal: bool = False, sm_scale: float | None = None, out=N
         raise ValueError(f"shape mismatch: q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
     if k.device != q.device or v.device != q.device:
         raise ValueError("q, k, v must be on the same device")
-    Hkv = k.shape[1]
-    if sm_scale is None:
-        sm_scale = 1.0 / math.sqrt(D)
+    return B, Hq, k.shape[1], N, D
+
+
+def _outputs(q, out, lse):
+    import torch
+
+    B, Hq, N, _ = q.shape
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
@@ -71,6 +71,21 @@ def attn_fwd(q, k, v, causal: bool = False, sm_scale: float | None = None, out=N
         raise ValueError("out must be a contiguous bf16 tensor shaped like q")
     if lse.shape != (B, Hq, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous fp32 tensor [B, Hq, N]")
+    return out, lse
+
+
+def attn_fwd(q, k, v, causal: bool = False, sm_scale: float | None = None, out=None, lse=None):
+    """Fused attention forward on the current CUDA stream of ``q``'s device.
+
+    Returns ``(out, lse)``: out bf16 [B,Hq,N,D], lse fp32 [B,Hq,N].  ``out``/``lse`` may be passed
+    preallocated (contiguous, right shape and dtype).  Raises ``AttnError`` on a nonzero status.
+    """
+    import torch
+
+    B, Hq, Hkv, N, D = _check_inputs(q, k, v)
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    out, lse = _outputs(q, out, lse)
     lib = _lib.load()
     with torch.cuda.device(q.device):
         st = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
@@ -78,6 +93,43 @@ def attn_fwd(q, k, v, causal: bool = False, sm_scale: float | None = None, out=N
                           _stream_handle(q.device))
     if st != ATTN_OK:
         raise AttnError(st)
+    return out, lse
+
+
+def splitkv_num_splits(B: int, Hq: int, N: int, D: int, causal: bool = False) -> int:
+    """Split count the library suggests for these sizes on the current device."""
+    return int(_lib.load().attn_fwd_splitkv_num_splits(B, Hq, N, D, int(bool(causal))))
+
+
+def splitkv_workspace_bytes(B: int, Hq: int, N: int, D: int, num_splits: int = 0) -> int:
+    """Workspace bytes ``attn_fwd_splitkv`` needs (0 when the call resolves to one split)."""
+    return int(_lib.load().attn_fwd_splitkv_workspace_bytes(B, Hq, N, D, int(num_splits)))
+
+
+def attn_fwd_splitkv(q, k, v, causal: bool = False, sm_scale: float | None = None,
+                     num_splits: int = 0, workspace=None, out=None, lse=None):
+    """Split-KV forward (partials over key-axis splits + fused merge); same result as
+    ``attn_fwd`` up to rounding.  ``workspace``: optional CUDA tensor of at least
+    ``splitkv_workspace_bytes(...)`` bytes (allocated here when omitted)."""
+    import torch
+
+    B, Hq, Hkv, N, D = _check_inputs(q, k, v)
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    out, lse = _outputs(q, out, lse)
+    lib = _lib.load()
+    with torch.cuda.device(q.device):
+        need = splitkv_workspace_bytes(B, Hq, N, D, num_splits)
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        ws_ptr = workspace.data_ptr() if workspace is not None else None
+        ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+        st = lib.attn_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                  lse.data_ptr(), B, Hq, Hkv, N, D, int(bool(causal)),
+                                  float(sm_scale), int(num_splits), ws_ptr, ws_bytes,
+                                  _stream_handle(q.device))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_splitkv")
     return out, lse
 
 

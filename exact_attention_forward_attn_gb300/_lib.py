@@ -18,6 +18,11 @@ SIGNATURES = {
     "attn_status_string": (ctypes.c_char_p, [_c_int]),
     "attn_last_cuda_error": (_c_int, []),
     "attn_debug_status": (_c_int, [_vp]),
+    "attn_fwd_splitkv": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                  _c_int, _c_float, _c_int, _vp, ctypes.c_size_t, _vp]),
+    "attn_fwd_splitkv_workspace_bytes": (ctypes.c_size_t, [_c_int, _c_int, _c_int, _c_int,
+                                                            _c_int]),
+    "attn_fwd_splitkv_num_splits": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int]),
 }
 
 _lib = None

@@ -4,6 +4,9 @@
 // contiguous bf16 ("Triton-CUDA Attention", skillmd.com: (B, H, L, D) layout, contiguous inputs,
 // GQA grid over the query heads), a causal flag ("Flash Attention 与 Kernel 优化",
 // fangpin.github.io: FlashAttention.apply(q, k, v, is_causal)), outputs O and the per-row LSE.
+// The split-KV entry point follows the split-T pattern of "Attention Kernel 实现与正确性验证"
+// (walkerchi.com), section 2.4: partial results per split of the key axis, then a fused
+// safe-softmax merge.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -20,6 +23,9 @@ using namespace gb300attn;
 __device__ unsigned int g_attn_status_word = 0;
 
 namespace {
+
+constexpr int kMaxSplits = 64;
+constexpr int kMergeThreads = 256;
 
 thread_local int t_last_cuda_error = 0;
 
@@ -64,15 +70,23 @@ bool make_tile_map(CUtensorMap* map, const void* base, int64_t BH, int64_t N, in
            CUDA_SUCCESS;
 }
 
-// Per-device one-time set-up: architecture check, status-word address, smem opt-in.
+// Per-device one-time set-up: architecture check, SM count, status-word address, smem opt-in.
 constexpr int kMaxDevices = 64;
 struct DeviceState {
     std::once_flag once;
     int status = ATTN_OK;
     int cuda_error = 0;
+    int num_sms = 0;
     unsigned int* status_word = nullptr;
 };
 DeviceState g_devices[kMaxDevices];
+
+template <int D, bool kSplit>
+cudaError_t opt_in_smem() {
+    return cudaFuncSetAttribute(attn_fwd_kernel<D, kSplit>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                SmemLayout<D>::kAlloc);
+}
 
 int device_state(int dev, DeviceState** out) {
     if (dev < 0 || dev >= kMaxDevices) return cuda_fail(cudaErrorInvalidDevice);
@@ -82,22 +96,27 @@ int device_state(int dev, DeviceState** out) {
         cudaError_t e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
         if (e == cudaSuccess)
             e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (e == cudaSuccess)
+            e = cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) { st.status = ATTN_ERR_CUDA; st.cuda_error = e; return; }
         if (major != 10 || minor != 3) { st.status = ATTN_ERR_ARCH; return; }
         e = cudaGetSymbolAddress(reinterpret_cast<void**>(&st.status_word), g_attn_status_word);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(attn_fwd_kernel<64>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     SmemLayout<64>::kAlloc);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(attn_fwd_kernel<128>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     SmemLayout<128>::kAlloc);
+        if (e == cudaSuccess) e = opt_in_smem<64, false>();
+        if (e == cudaSuccess) e = opt_in_smem<128, false>();
+        if (e == cudaSuccess) e = opt_in_smem<64, true>();
+        if (e == cudaSuccess) e = opt_in_smem<128, true>();
         if (e != cudaSuccess) { st.status = ATTN_ERR_CUDA; st.cuda_error = e; }
     });
     if (st.status == ATTN_ERR_CUDA) t_last_cuda_error = st.cuda_error;
     *out = &st;
     return st.status;
+}
+
+int current_device_state(DeviceState** out) {
+    int dev = 0;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return device_state(dev, out);
 }
 
 int check_memory(const void* ptr, int dev) {
@@ -117,76 +136,218 @@ bool overlaps(const void* a, int64_t a_bytes, const void* b, int64_t b_bytes) {
     return a0 < b0 + static_cast<uintptr_t>(b_bytes) && b0 < a0 + static_cast<uintptr_t>(a_bytes);
 }
 
-template <int D>
-int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-           const CUtensorMap& mo, const AttnParams& p, unsigned int* status_word, int64_t grid,
-           cudaStream_t stream) {
-    attn_fwd_kernel<D><<<static_cast<unsigned int>(grid), kThreads, SmemLayout<D>::kAlloc,
-                         stream>>>(mq, mk, mv, mo, p, status_word);
+// Everything about one call that both entry points share.
+struct Problem {
+    const void *q, *k, *v;
+    void* out;
+    float* lse;
+    int B, Hq, Hkv, N, D, causal;
+    float sm_scale;
+    int64_t bh, bh_kv, n_tiles, n_pairs, items;
+    int64_t q_bytes, kv_bytes, lse_bytes;
+};
+
+// Host-side validation; returns ATTN_OK with *empty set for an empty problem.  Nothing is
+// launched or written when this fails.
+int validate(Problem& P, bool* empty) {
+    *empty = false;
+    if (P.B < 0 || P.N < 0 || P.Hq <= 0 || P.Hkv <= 0) return ATTN_ERR_SHAPE;
+    if (P.Hq % P.Hkv != 0) return ATTN_ERR_HEADS;
+    if (P.D != 64 && P.D != 128) return ATTN_ERR_HEADDIM;
+    if (!std::isfinite(P.sm_scale) || !(P.sm_scale > 0.f)) return ATTN_ERR_SCALE;
+    if (P.B == 0 || P.N == 0) {  // empty problem: nothing to read or write
+        *empty = true;
+        return ATTN_OK;
+    }
+    if (!P.q || !P.k || !P.v || !P.out || !P.lse) return ATTN_ERR_NULL;
+    const uintptr_t align_bits =
+        reinterpret_cast<uintptr_t>(P.q) | reinterpret_cast<uintptr_t>(P.k) |
+        reinterpret_cast<uintptr_t>(P.v) | reinterpret_cast<uintptr_t>(P.out) |
+        reinterpret_cast<uintptr_t>(P.lse);
+    if (align_bits & 15u) return ATTN_ERR_ALIGN;
+
+    P.bh = static_cast<int64_t>(P.B) * P.Hq;
+    P.bh_kv = static_cast<int64_t>(P.B) * P.Hkv;
+    P.n_tiles = (static_cast<int64_t>(P.N) + kBM - 1) / kBM;
+    P.n_pairs = (P.n_tiles + 1) / 2;
+    P.items = P.n_pairs * P.bh;
+    if (P.items > 0x7fffffffLL || P.bh > 0x7fffffffLL) return ATTN_ERR_SHAPE;
+
+    P.q_bytes = P.bh * P.N * P.D * 2;
+    P.kv_bytes = P.bh_kv * P.N * P.D * 2;
+    P.lse_bytes = P.bh * P.N * 4;
+    if (overlaps(P.out, P.q_bytes, P.q, P.q_bytes) || overlaps(P.out, P.q_bytes, P.k, P.kv_bytes) ||
+        overlaps(P.out, P.q_bytes, P.v, P.kv_bytes) ||
+        overlaps(P.out, P.q_bytes, P.lse, P.lse_bytes) ||
+        overlaps(P.lse, P.lse_bytes, P.q, P.q_bytes) ||
+        overlaps(P.lse, P.lse_bytes, P.k, P.kv_bytes) ||
+        overlaps(P.lse, P.lse_bytes, P.v, P.kv_bytes))
+        return ATTN_ERR_ALIAS;
+    return ATTN_OK;
+}
+
+// Device checks and TMA descriptors; fills the kernel parameters common to both entry points.
+int prepare(const Problem& P, DeviceState** ds, CUtensorMap* mq, CUtensorMap* mk, CUtensorMap* mv,
+            CUtensorMap* mo, AttnParams* prm) {
+    int dev = 0;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const int st = device_state(dev, ds);
+    if (st != ATTN_OK) return st;
+    for (const void* ptr :
+         {P.q, P.k, P.v, static_cast<const void*>(P.out), static_cast<const void*>(P.lse)})
+        if (check_memory(ptr, dev) != ATTN_OK) return ATTN_ERR_MEMORY;
+    if (!make_tile_map(mq, P.q, P.bh, P.N, P.D) || !make_tile_map(mk, P.k, P.bh_kv, P.N, P.D) ||
+        !make_tile_map(mv, P.v, P.bh_kv, P.N, P.D) || !make_tile_map(mo, P.out, P.bh, P.N, P.D))
+        return cuda_fail(cudaErrorInvalidValue);
+    prm->B = P.B;
+    prm->Hq = P.Hq;
+    prm->Hkv = P.Hkv;
+    prm->N = P.N;
+    prm->group = P.Hq / P.Hkv;
+    prm->causal = P.causal ? 1 : 0;
+    prm->n_tiles = static_cast<int>(P.n_tiles);
+    prm->n_pairs = static_cast<int>(P.n_pairs);
+    prm->scale_log2 = P.sm_scale * 1.4426950408889634f;  // log2(e)
+    prm->lse = P.lse;
+    prm->n_splits = 1;
+    prm->split_tiles = prm->n_tiles;
+    prm->ws_o = nullptr;
+    prm->ws_lse = nullptr;
+    return ATTN_OK;
+}
+
+template <int D, bool kSplit>
+int launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+               const CUtensorMap& mo, const AttnParams& p, unsigned int* status_word,
+               int64_t grid, cudaStream_t stream) {
+    attn_fwd_kernel<D, kSplit><<<static_cast<unsigned int>(grid), kThreads,
+                                 SmemLayout<D>::kAlloc, stream>>>(mq, mk, mv, mo, p, status_word);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+template <int D>
+int launch_merge(const AttnParams& p, __nv_bfloat16* out, cudaStream_t stream) {
+    const int64_t rows = static_cast<int64_t>(p.B) * p.Hq * p.N;
+    const int64_t blocks = (rows + kMergeThreads / 32 - 1) / (kMergeThreads / 32);
+    attn_splitkv_merge_kernel<D><<<static_cast<unsigned int>(blocks), kMergeThreads, 0, stream>>>(
+        p.ws_o, p.ws_lse, out, p.lse, p.B * p.Hq, p.N, p.n_tiles, p.causal, p.n_splits,
+        p.split_tiles);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+// Effective split layout for a requested count: tiles per split and the number of non-empty
+// splits (every split but the last holds split_tiles KV tiles).
+void split_layout(int64_t n_tiles, int requested, int* split_tiles, int* n_splits) {
+    const int64_t want = requested < 1 ? 1 : (requested > kMaxSplits ? kMaxSplits : requested);
+    const int64_t tps = (n_tiles + want - 1) / want;
+    *split_tiles = static_cast<int>(tps);
+    *n_splits = static_cast<int>((n_tiles + tps - 1) / tps);
+}
+
+// Split only when the query tiles alone leave SMs idle, and only as far as every split keeps at
+// least kMinSplitTiles key tiles: below that the per-CTA start-up, the fp32 partials and the
+// merge launch cost more than the extra parallelism gains (measured on mha-n512 / mqa-n512).
+constexpr int64_t kMinSplitTiles = 4;
+int heuristic_splits(int64_t items, int64_t n_tiles, int num_sms) {
+    if (items >= num_sms) return 1;
+    int64_t s = num_sms / items;
+    if (s > n_tiles / kMinSplitTiles) s = n_tiles / kMinSplitTiles;
+    if (s > 16) s = 16;
+    return s < 1 ? 1 : static_cast<int>(s);
+}
+
+int64_t workspace_bytes_for(int64_t bh, int64_t N, int64_t D, int n_splits) {
+    return static_cast<int64_t>(n_splits) * bh * N * (D + 1) * 4;
 }
 
 }  // namespace
 
 extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B,
                         int Hq, int Hkv, int N, int D, int causal, float sm_scale, void* stream) {
-    // ---- host-side validation: nothing is launched or written on failure ---------------------
-    if (B < 0 || N < 0 || Hq <= 0 || Hkv <= 0) return ATTN_ERR_SHAPE;
-    if (Hq % Hkv != 0) return ATTN_ERR_HEADS;
-    if (D != 64 && D != 128) return ATTN_ERR_HEADDIM;
-    if (!std::isfinite(sm_scale) || !(sm_scale > 0.f)) return ATTN_ERR_SCALE;
-    if (B == 0 || N == 0) return ATTN_OK;  // empty problem: nothing to read or write
-    if (!q || !k || !v || !out || !lse) return ATTN_ERR_NULL;
-    const uintptr_t align_bits = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
-                                 reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out) |
-                                 reinterpret_cast<uintptr_t>(lse);
-    if (align_bits & 15u) return ATTN_ERR_ALIGN;
-
-    const int64_t bh = static_cast<int64_t>(B) * Hq;
-    const int64_t bh_kv = static_cast<int64_t>(B) * Hkv;
-    const int64_t n_tiles = (static_cast<int64_t>(N) + kBM - 1) / kBM;
-    const int64_t n_pairs = (n_tiles + 1) / 2;
-    const int64_t grid = n_pairs * bh;
-    if (grid > 0x7fffffffLL || bh > 0x7fffffffLL) return ATTN_ERR_SHAPE;
-
-    const int64_t q_bytes = bh * N * D * 2, kv_bytes = bh_kv * N * D * 2, lse_bytes = bh * N * 4;
-    if (overlaps(out, q_bytes, q, q_bytes) || overlaps(out, q_bytes, k, kv_bytes) ||
-        overlaps(out, q_bytes, v, kv_bytes) || overlaps(out, q_bytes, lse, lse_bytes) ||
-        overlaps(lse, lse_bytes, q, q_bytes) || overlaps(lse, lse_bytes, k, kv_bytes) ||
-        overlaps(lse, lse_bytes, v, kv_bytes))
-        return ATTN_ERR_ALIAS;
-
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e);
+    Problem P{q, k, v, out, lse, B, Hq, Hkv, N, D, causal, sm_scale};
+    bool empty = false;
+    int st = validate(P, &empty);
+    if (st != ATTN_OK || empty) return st;
     DeviceState* ds = nullptr;
-    const int st = device_state(dev, &ds);
-    if (st != ATTN_OK) return st;
-    for (const void* ptr : {q, k, v, static_cast<const void*>(out), static_cast<const void*>(lse)})
-        if (check_memory(ptr, dev) != ATTN_OK) return ATTN_ERR_MEMORY;
-
-    // ---- TMA descriptors (passed by value as __grid_constant__ kernel parameters) -------------
     CUtensorMap mq, mk, mv, mo;
-    if (!make_tile_map(&mq, q, bh, N, D) || !make_tile_map(&mk, k, bh_kv, N, D) ||
-        !make_tile_map(&mv, v, bh_kv, N, D) || !make_tile_map(&mo, out, bh, N, D))
-        return cuda_fail(cudaErrorInvalidValue);
-
-    AttnParams p;
-    p.B = B;
-    p.Hq = Hq;
-    p.Hkv = Hkv;
-    p.N = N;
-    p.group = Hq / Hkv;
-    p.causal = causal ? 1 : 0;
-    p.n_tiles = static_cast<int>(n_tiles);
-    p.n_pairs = static_cast<int>(n_pairs);
-    p.scale_log2 = sm_scale * 1.4426950408889634f;  // log2(e)
-    p.lse = lse;
-
+    AttnParams prm;
+    st = prepare(P, &ds, &mq, &mk, &mv, &mo, &prm);
+    if (st != ATTN_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return D == 64 ? launch<64>(mq, mk, mv, mo, p, ds->status_word, grid, s)
-                   : launch<128>(mq, mk, mv, mo, p, ds->status_word, grid, s);
+    return D == 64 ? launch_fwd<64, false>(mq, mk, mv, mo, prm, ds->status_word, P.items, s)
+                   : launch_fwd<128, false>(mq, mk, mv, mo, prm, ds->status_word, P.items, s);
+}
+
+extern "C" int attn_fwd_splitkv_num_splits(int B, int Hq, int N, int D, int causal) {
+    (void)D;
+    (void)causal;
+    if (B <= 0 || Hq <= 0 || N <= 0) return 1;
+    DeviceState* ds = nullptr;
+    if (current_device_state(&ds) != ATTN_OK) return 1;
+    const int64_t n_tiles = (static_cast<int64_t>(N) + kBM - 1) / kBM;
+    const int64_t items = (n_tiles + 1) / 2 * static_cast<int64_t>(B) * Hq;
+    int tps = 0, n = 0;
+    split_layout(n_tiles, heuristic_splits(items, n_tiles, ds->num_sms), &tps, &n);
+    return n;
+}
+
+extern "C" size_t attn_fwd_splitkv_workspace_bytes(int B, int Hq, int N, int D, int num_splits) {
+    if (B <= 0 || Hq <= 0 || N <= 0 || (D != 64 && D != 128)) return 0;
+    if (num_splits == 0) num_splits = attn_fwd_splitkv_num_splits(B, Hq, N, D, 0);
+    const int64_t n_tiles = (static_cast<int64_t>(N) + kBM - 1) / kBM;
+    int tps = 0, n = 0;
+    split_layout(n_tiles, num_splits, &tps, &n);
+    if (n <= 1) return 0;
+    return static_cast<size_t>(workspace_bytes_for(static_cast<int64_t>(B) * Hq, N, D, n));
+}
+
+extern "C" int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* out,
+                                float* lse, int B, int Hq, int Hkv, int N, int D, int causal,
+                                float sm_scale, int num_splits, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+    if (num_splits < 0 || num_splits > kMaxSplits) return ATTN_ERR_SPLITS;
+    Problem P{q, k, v, out, lse, B, Hq, Hkv, N, D, causal, sm_scale};
+    bool empty = false;
+    int st = validate(P, &empty);
+    if (st != ATTN_OK || empty) return st;
+    if (num_splits == 0) num_splits = attn_fwd_splitkv_num_splits(B, Hq, N, D, causal);
+    int split_tiles = 0, n_splits = 0;
+    split_layout(P.n_tiles, num_splits, &split_tiles, &n_splits);
+    if (n_splits <= 1)  // one split is the ordinary forward; the workspace is not touched
+        return attn_fwd(q, k, v, out, lse, B, Hq, Hkv, N, D, causal, sm_scale, stream);
+
+    const int64_t need = workspace_bytes_for(P.bh, N, D, n_splits);
+    if (!workspace) return ATTN_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(workspace) & 15u) return ATTN_ERR_ALIGN;
+    if (static_cast<int64_t>(workspace_bytes) < need) return ATTN_ERR_WORKSPACE;
+    if (overlaps(workspace, need, q, P.q_bytes) || overlaps(workspace, need, k, P.kv_bytes) ||
+        overlaps(workspace, need, v, P.kv_bytes) || overlaps(workspace, need, out, P.q_bytes) ||
+        overlaps(workspace, need, lse, P.lse_bytes))
+        return ATTN_ERR_ALIAS;
+    if (P.items * n_splits > 0x7fffffffLL) return ATTN_ERR_SHAPE;
+
+    DeviceState* ds = nullptr;
+    CUtensorMap mq, mk, mv, mo;
+    AttnParams prm;
+    st = prepare(P, &ds, &mq, &mk, &mv, &mo, &prm);
+    if (st != ATTN_OK) return st;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || check_memory(workspace, dev) != ATTN_OK)
+        return ATTN_ERR_MEMORY;
+    prm.n_splits = n_splits;
+    prm.split_tiles = split_tiles;
+    prm.ws_o = static_cast<float*>(workspace);
+    prm.ws_lse = prm.ws_o + static_cast<int64_t>(n_splits) * P.bh * N * D;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t grid = P.items * n_splits;
+    st = D == 64 ? launch_fwd<64, true>(mq, mk, mv, mo, prm, ds->status_word, grid, s)
+                 : launch_fwd<128, true>(mq, mk, mv, mo, prm, ds->status_word, grid, s);
+    if (st != ATTN_OK) return st;
+    auto* o = static_cast<__nv_bfloat16*>(out);
+    return D == 64 ? launch_merge<64>(prm, o, s) : launch_merge<128>(prm, o, s);
 }
 
 extern "C" const char* attn_status_string(int status) {
@@ -196,13 +357,15 @@ extern "C" const char* attn_status_string(int status) {
         case ATTN_ERR_SHAPE: return "invalid or overflowing shape (B, Hq, Hkv, N)";
         case ATTN_ERR_HEADS: return "Hq is not a multiple of Hkv";
         case ATTN_ERR_HEADDIM: return "unsupported head dimension (D must be 64 or 128)";
-        case ATTN_ERR_ALIGN: return "a tensor pointer is not 16-byte aligned";
+        case ATTN_ERR_ALIGN: return "a pointer is not 16-byte aligned";
         case ATTN_ERR_SCALE: return "sm_scale must be finite and positive";
         case ATTN_ERR_ARCH: return "the current device is not sm_103 (GB300)";
         case ATTN_ERR_CUDA: return "a CUDA call failed (see attn_last_cuda_error)";
         case ATTN_ERR_TIMEOUT: return "a device-side bounded wait expired";
         case ATTN_ERR_MEMORY: return "a pointer is not device memory of the current device";
-        case ATTN_ERR_ALIAS: return "out/lse overlap an input or each other";
+        case ATTN_ERR_ALIAS: return "out/lse/workspace overlap an input or each other";
+        case ATTN_ERR_SPLITS: return "num_splits must be in [0, 64]";
+        case ATTN_ERR_WORKSPACE: return "workspace smaller than attn_fwd_splitkv_workspace_bytes";
         default: return "unknown status";
     }
 }

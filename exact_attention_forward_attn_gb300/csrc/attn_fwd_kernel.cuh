@@ -29,6 +29,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cstdint>
 
 #include "ptx.cuh"
@@ -55,6 +56,11 @@ struct AttnParams {
     int n_pairs;       // ceil(n_tiles / 2): CTAs per (b, hq)
     float scale_log2;  // sm_scale * log2(e)
     float* lse;        // [B, Hq, N] fp32
+    // split-KV partials (split instantiation only): KV tiles [s*split_tiles, (s+1)*split_tiles)
+    int n_splits;
+    int split_tiles;
+    float* ws_o;       // [n_splits, B*Hq, N, D] fp32, O of each split normalised by its own l
+    float* ws_lse;     // [n_splits, B*Hq, N] fp32, natural-log LSE of each split
 };
 
 template <int D>
@@ -83,7 +89,11 @@ struct SmemLayout {
 __device__ __forceinline__ uint32_t tmem_s_col(int t) { return 128u * t; }
 __device__ __forceinline__ uint32_t tmem_o_col(int t) { return 256u + 128u * t; }
 
-template <int D>
+// kSplit = false: the whole KV range, bf16 O and LSE written to the outputs.
+// kSplit = true:  the KV range of one split (split index innermost in blockIdx.x); the fp32 O of
+//                 that range (normalised by its own denominator) and its LSE go to the workspace,
+//                 and attn_splitkv_merge_kernel combines the splits.
+template <int D, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
                     const __grid_constant__ CUtensorMap tmap_k,
@@ -111,26 +121,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Block order: (batch, KV head) outermost, then Q-tile pairs heaviest (latest) first, then the
     // query heads sharing that KV head.  CTAs running together read the same K/V (which stays in
     // L2), and the grid ends on the lightest causal pairs.
+    int item = static_cast<int>(blockIdx.x);
+    int split = 0;
+    if constexpr (kSplit) {
+        split = item % p.n_splits;
+        item /= p.n_splits;
+    }
     const int per_kv = p.n_pairs * p.group;
-    const int bh_kv = static_cast<int>(blockIdx.x / per_kv);
-    const int rem = static_cast<int>(blockIdx.x % per_kv);
+    const int bh_kv = item / per_kv;
+    const int rem = item % per_kv;
     const int pair = p.n_pairs - 1 - rem / p.group;
     const int b = bh_kv / p.Hkv;
     const int hq = (bh_kv % p.Hkv) * p.group + rem % p.group;
     const int bh = b * p.Hq + hq;
     const int tile0 = 2 * pair;
-    const bool has_q1 = tile0 + 1 < p.n_tiles;
-    // last KV tile each Q tile needs (BM == BN: the causal diagonal tile has the Q tile's index)
-    const int last0 = p.causal ? tile0 : p.n_tiles - 1;
-    const int last1 = p.causal ? tile0 + 1 : p.n_tiles - 1;
-    const int n_kv = has_q1 ? last1 + 1 : last0 + 1;
+    // This CTA's KV tiles: [kv_begin, kv_limit).  Each Q tile t uses [kv_begin, last_t]; under the
+    // causal mask its last tile is its diagonal (BM == BN, so it has the Q tile's index).  A Q
+    // tile takes part if that range is not empty (always, unless a later split starts past it).
+    const int kv_begin = kSplit ? split * p.split_tiles : 0;
+    const int kv_limit = kSplit ? min(kv_begin + p.split_tiles, p.n_tiles) : p.n_tiles;
+    const int last0 = min(kv_limit - 1, p.causal ? tile0 : p.n_tiles - 1);
+    const int last1 = min(kv_limit - 1, p.causal ? tile0 + 1 : p.n_tiles - 1);
+    const bool part0 = last0 >= kv_begin;
+    const bool part1 = tile0 + 1 < p.n_tiles && last1 >= kv_begin;
+    const bool pingpong = part0 && part1;
+    const int n_part = static_cast<int>(part0) + static_cast<int>(part1);
+    const int kv_end = (part1 ? last1 : last0) + 1;  // one past the last KV tile this CTA loads
 
     // ---- setup ---------------------------------------------------------------------------------
     if (threadIdx.x == 0) {
         mbar_init(bar(L::kBarQ), 1);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar(L::kBarKvFull + s), 1);
-            mbar_init(bar(L::kBarKvEmpty + s), has_q1 ? 2 : 1);  // one release per issuer
+            mbar_init(bar(L::kBarKvEmpty + s), n_part > 0 ? n_part : 1);  // one release per issuer
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(bar(L::kBarSFull + t), 1);
@@ -159,16 +182,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == kLoadWarp) {
         // =========================== TMA producer (one lane) ===================================
-        if (lane == 0) {
-            const int nq = has_q1 ? 2 : 1;
-            mbar_arrive_expect_tx(bar(L::kBarQ), nq * L::kTileBytes);
-            for (int t = 0; t < nq; ++t)
-                for (int h = 0; h < kPanels; ++h)
-                    tma_load_3d(sbase + L::kQ + t * L::kTileBytes + h * L::kPanelBytes, &tmap_q,
-                                bar(L::kBarQ), h * 64, (tile0 + t) * kBM, bh);
-            for (int j = 0; j < n_kv; ++j) {
+        if (lane == 0 && n_part > 0) {
+            mbar_arrive_expect_tx(bar(L::kBarQ), n_part * L::kTileBytes);
+            for (int t = 0; t < 2; ++t)
+                if (t == 0 ? part0 : part1)
+                    for (int h = 0; h < kPanels; ++h)
+                        tma_load_3d(sbase + L::kQ + t * L::kTileBytes + h * L::kPanelBytes,
+                                    &tmap_q, bar(L::kBarQ), h * 64, (tile0 + t) * kBM, bh);
+            for (int j = kv_begin; j < kv_end; ++j) {
                 for (int kv = 0; kv < 2; ++kv) {
-                    const int idx = 2 * j + kv;
+                    const int idx = 2 * (j - kv_begin) + kv;
                     const int slot = idx % kStages;
                     const uint32_t ph = (idx / kStages) & 1;
                     if (!mbar_wait_bounded(bar(L::kBarKvEmpty + slot), ph ^ 1u, abort_flag,
@@ -191,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // with independent accumulators keep the tensor core fed, also while the other tile's
         // issuer waits for its softmax.
         const int t = warp - kMmaWarp0;
-        if (t == 0 || has_q1) {  // warp-uniform: every lane runs the loop, one elected lane issues
+        if (t == 0 ? part0 : part1) {  // warp-uniform: every lane runs the loop, one lane issues
             const int last = t == 0 ? last0 : last1;
             const uint32_t s_tmem = tmem + tmem_s_col(t);
             const uint32_t o_tmem = tmem + tmem_o_col(t);
@@ -242,12 +265,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit_warp(bar(L::kBarSFull + t));
                 mma_commit_warp(bar(L::kBarKvEmpty + kv_slot(0)));
             }
-            for (int j = 0; ok && j <= last; ++j) {
-                const int vidx = 2 * j + 1;
-                const int kidx = 2 * j + 2;  // K_{j+1}
+            for (int j = kv_begin; ok && j <= last; ++j) {
+                const int vidx = 2 * (j - kv_begin) + 1;  // V_j
+                const int kidx = vidx + 1;                // K_{j+1}
                 ok = wait_full(vidx);
                 if (!ok) break;
-                ok = pv_mma(kv_slot(vidx), j > 0, p_phase);
+                ok = pv_mma(kv_slot(vidx), j > kv_begin, p_phase);
                 if (!ok) break;
                 p_phase ^= 1u;
                 if (j == last) mma_commit_warp(bar(L::kBarODone + t));
@@ -264,10 +287,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // KV tiles this Q tile does not need (under the causal mask, the last one for Q tile
             // 0): release each slot once its data has landed, so every slot phase gets one
             // release per issuer and never completes early.
-            for (int j = last + 1; ok && j < n_kv; ++j) {
+            for (int j = last + 1; ok && j < kv_end; ++j) {
                 for (int kv = 0; ok && kv < 2; ++kv) {
-                    ok = wait_full(2 * j + kv);
-                    if (ok) mbar_arrive_warp(bar(L::kBarKvEmpty + kv_slot(2 * j + kv)));
+                    const int idx = 2 * (j - kv_begin) + kv;
+                    ok = wait_full(idx);
+                    if (ok) mbar_arrive_warp(bar(L::kBarKvEmpty + kv_slot(idx)));
                 }
             }
         }
@@ -278,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quarter = warp & 3;     // TMEM lane quarter this warp may access
         const int row = quarter * 32 + lane;  // row within the Q tile
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-        if (t == 0 || has_q1) {
+        if (t == 0 ? part0 : part1) {
             const int q_tile = tile0 + t;
             const int last = t == 0 ? last0 : last1;
             const int row_g = q_tile * kBM + row;
@@ -288,8 +312,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             float m = -INFINITY;  // running max of c*s (log2 units)
             float l = 0.f;        // running denominator
             bool ok = true;
-            for (int j = 0; j <= last; ++j) {
-                ok = mbar_wait_warp(bar(L::kBarSFull + t), j & 1, abort_flag, status_word);
+            for (int j = kv_begin; j <= last; ++j) {
+                ok = mbar_wait_warp(bar(L::kBarSFull + t), (j - kv_begin) & 1, abort_flag,
+                                    status_word);
                 if (!ok) break;
                 tc_fence_after();
                 // Masks (the causal diagonal tile, or the ragged last key tile) are applied in
@@ -334,16 +359,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float m_cand = row_max * c;
                 const float m_new = (m_cand > m + kRescaleThreshold) ? m_cand : m;
                 const float alpha = ex2_approx(m - m_new);  // 1 if unchanged, 0 on the first tile
-                const bool rescale = j > 0 && __any_sync(0xffffffffu, m_new != m);
+                const bool rescale = j > kv_begin && __any_sync(0xffffffffu, m_new != m);
                 m = m_new;
                 const float neg_m = -m;
                 // Ping-pong: the exp2 phases of the two softmax groups alternate (tile 0 step j,
                 // tile 1 step j, tile 0 step j+1, ...), so one group's exponentials overlap the
                 // other tile's MMAs instead of competing for the same issue slots and MUFU.
-                const bool turn_wait = has_q1 && (t == 0 ? j > 0 : j <= last0);
+                const bool turn_wait = pingpong && (t == 0 ? j > kv_begin : j <= last0);
                 if (turn_wait) {
-                    ok = mbar_wait_warp(bar(L::kBarTurn + t), (t == 0 ? j - 1 : j) & 1, abort_flag,
-                                        status_word);
+                    ok = mbar_wait_warp(bar(L::kBarTurn + t), (j - kv_begin - (t == 0)) & 1,
+                                        abort_flag, status_word);
                     if (!ok) break;
                 }
                 // p = exp2(c*s - m) in kPParts key blocks; each block is published to the MMA
@@ -395,11 +420,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 l = l * alpha + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
                 // hand the turn to the other group (tile 1 only while tile 0 has steps left)
-                if (has_q1 && (t == 1 ? j < last0 : true)) mbar_arrive(bar(L::kBarTurn + (t ^ 1)));
+                if (pingpong && (t == 1 ? j < last0 : true)) mbar_arrive(bar(L::kBarTurn + (t ^ 1)));
             }
 
-            // ---- epilogue: O = acc / l -> bf16 -> smem (over Q_t) -> TMA store; LSE ----------
             if (ok) ok = mbar_wait_warp(bar(L::kBarODone + t), 0, abort_flag, status_word);
+            if constexpr (kSplit) {
+                // ---- split epilogue: O_s = acc / l (fp32) and LSE_s to the workspace ----------
+                if (ok) {
+                    tc_fence_after();
+                    const float inv_l = 1.0f / l;
+                    const size_t prow =
+                        (static_cast<size_t>(split) * p.B * p.Hq + bh) * p.N + row_g;
+                    float* dst = p.ws_o + prow * D;
+#pragma unroll
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        uint32_t r[32];
+                        tmem_ld32(o_addr + cc * 32, r);  // warp-collective: every lane loads
+                        tmem_wait_ld();
+                        if (row_g < p.N) {
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                st_global_v4f(dst + cc * 32 + 4 * i,
+                                              __uint_as_float(r[4 * i]) * inv_l,
+                                              __uint_as_float(r[4 * i + 1]) * inv_l,
+                                              __uint_as_float(r[4 * i + 2]) * inv_l,
+                                              __uint_as_float(r[4 * i + 3]) * inv_l);
+                        }
+                    }
+                    if (row_g < p.N) p.ws_lse[prow] = (m + __log2f(l)) * kLn2;
+                }
+            } else {
+            // ---- epilogue: O = acc / l -> bf16 -> smem (over Q_t) -> TMA store; LSE ----------
             if (ok) {
                 tc_fence_after();
                 const float inv_l = 1.0f / l;
@@ -434,6 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_store_3d(&tmap_o, stage + h * L::kPanelBytes, h * 64, q_tile * kBM, bh);
                 tma_store_commit_and_wait();
             }
+            }  // !kSplit
             __syncwarp();
         }
     }
@@ -445,6 +497,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
+}
+
+// Split-KV merge ("Attention Kernel 实现与正确性验证" section 2.4, the split-T pattern: partial
+// results per split of the key axis, then a safe-softmax combination), fused into one kernel.
+// For query row i of head bh, the splits s that hold keys visible to it (all those starting at or
+// before its last visible key tile) are combined as
+//   LSE = M + ln sum_s exp(LSE_s - M),  M = max_s LSE_s,   O = sum_s exp(LSE_s - LSE) * O_s.
+// One warp per row; lane k owns D/32 consecutive columns (coalesced 16-byte loads per split).
+template <int D>
+__global__ void __launch_bounds__(256)
+    attn_splitkv_merge_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_lse,
+                              __nv_bfloat16* __restrict__ out, float* __restrict__ lse, int BH,
+                              int N, int n_tiles, int causal, int n_splits, int split_tiles) {
+    constexpr int kCols = D / 32;
+    const int lane = threadIdx.x & 31;
+    const long long row = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
+    if (row >= static_cast<long long>(BH) * N) return;
+    const int i = static_cast<int>(row % N);
+    const int last_kv = causal ? i / kBN : n_tiles - 1;
+    const int n_valid = min(n_splits, last_kv / split_tiles + 1);
+    const size_t plane = static_cast<size_t>(BH) * N;  // rows per split
+    float mx = -INFINITY;
+    for (int s = 0; s < n_valid; ++s) mx = fmaxf(mx, ws_lse[s * plane + row]);
+    float acc[kCols];
+#pragma unroll
+    for (int c = 0; c < kCols; ++c) acc[c] = 0.f;
+    float wsum = 0.f;
+    for (int s = 0; s < n_valid; ++s) {
+        const float w = expf(ws_lse[s * plane + row] - mx);
+        wsum += w;
+        const float* src = ws_o + (s * plane + row) * D + lane * kCols;
+        if constexpr (kCols == 4) {
+            const float4 v = *reinterpret_cast<const float4*>(src);
+            acc[0] += w * v.x; acc[1] += w * v.y; acc[2] += w * v.z; acc[3] += w * v.w;
+        } else {
+            const float2 v = *reinterpret_cast<const float2*>(src);
+            acc[0] += w * v.x; acc[1] += w * v.y;
+        }
+    }
+    const float inv = 1.0f / wsum;
+    __nv_bfloat16* o = out + row * D + lane * kCols;
+    if constexpr (kCols == 4) {
+        uint2 packed;
+        packed.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        packed.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+        *reinterpret_cast<uint2*>(o) = packed;
+    } else {
+        *reinterpret_cast<uint32_t*>(o) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    }
+    if (lane == 0) lse[row] = mx + logf(wsum);
 }
 
 }  // namespace gb300attn

@@ -62,11 +62,14 @@ GQA8_CAUSAL = Workload("gqa8-causal-n4096", 1, 64, 8, 4096, 128, True, 2)
 MHA = Workload("mha-n512", 1, 32, 32, 512, 128, False, 3)
 MHA_OUTLIER = Workload("mha-n512-outlier", 1, 32, 32, 512, 128, False, 3, outlier_seed=104)
 MQA = Workload("mqa-n512", 1, 16, 1, 512, 128, False, 4)
+# Few query heads over a longer sequence: 32 query tiles in all, far fewer than the SMs, so the
+# key axis is split (split-KV forward).  Not one of the five configurations; a context workload.
+FEWHEADS = Workload("fewheads-n4096", 1, 2, 1, 4096, 128, False, 8)
 LONG = {n: Workload(f"long-gqa8-causal-n{n}", 1, 32, 8, n, 128, True, s)
         for n, s in ((8192, 5), (16384, 6), (32768, 7))}
 
 CONFIGS = [TINY_NONCAUSAL, TINY_CAUSAL, GQA4_CAUSAL, GQA8_CAUSAL, MHA, MHA_OUTLIER, MQA,
-           *LONG.values()]
+           *LONG.values(), FEWHEADS]
 BY_NAME = {w.name: w for w in CONFIGS}
 
 

@@ -30,6 +30,8 @@
 #ifndef GB300_ATTN_H
 #define GB300_ATTN_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -46,7 +48,9 @@ typedef enum {
     ATTN_ERR_CUDA = -8,     /* a CUDA runtime/driver call failed; see attn_last_cuda_error() */
     ATTN_ERR_TIMEOUT = -9,  /* a device-side bounded wait expired (reported by attn_debug_status) */
     ATTN_ERR_MEMORY = -10,  /* a pointer is not device memory of the current device */
-    ATTN_ERR_ALIAS = -11    /* out or lse overlaps q, k, v or each other */
+    ATTN_ERR_ALIAS = -11,   /* out, lse or the workspace overlaps q, k, v or each other */
+    ATTN_ERR_SPLITS = -12,  /* num_splits outside [0, 64] */
+    ATTN_ERR_WORKSPACE = -13 /* workspace smaller than attn_fwd_splitkv_workspace_bytes() */
 } attn_status_t;
 
 /*
@@ -69,6 +73,43 @@ typedef enum {
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
              int Hkv, int N, int D, int causal, float sm_scale, void* stream);
+
+/*
+ * attn_fwd_splitkv - the same forward, with the key axis of every query tile cut into splits.
+ *
+ * The split-T pattern of "Attention Kernel 实现与正确性验证" (walkerchi.com), section 2.4: each
+ * split of the key axis produces a partial result (here: O over that split's keys, normalised by
+ * that split's own denominator, in fp32, and that split's natural-log LSE), and a safe-softmax
+ * merge combines them: LSE = M + ln sum_s exp(LSE_s - M) with M = max_s LSE_s, and
+ * O = sum_s exp(LSE_s - LSE) O_s.  The merge is a second kernel on the same stream.  This raises
+ * the number of CTAs for problems whose query tiles alone do not fill the GPU (short sequences,
+ * few heads); the result equals attn_fwd's up to rounding.
+ *
+ *   q, k, v, out, lse, B, Hq, Hkv, N, D, causal, sm_scale, stream: as for attn_fwd.
+ *   num_splits       requested number of key-axis splits, 0..64; 0 picks
+ *                    attn_fwd_splitkv_num_splits().  Splits hold ceil(ceil(N/128)/num_splits)
+ *                    key tiles of 128, so fewer splits may be used.  One split is attn_fwd.
+ *   workspace        device memory of at least attn_fwd_splitkv_workspace_bytes(B, Hq, N, D,
+ *                    num_splits) bytes, 16-byte aligned, owned by the caller; its previous
+ *                    contents are ignored and it holds partial results afterwards.  It must not
+ *                    overlap the inputs or outputs, and calls that run concurrently on the GPU
+ *                    must not share it.  May be NULL when the call resolves to one split.
+ *   workspace_bytes  size of `workspace` in bytes.
+ *
+ * Returns ATTN_OK once both kernels are enqueued, else a negative attn_status_t (nothing written).
+ */
+int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                     int Hq, int Hkv, int N, int D, int causal, float sm_scale, int num_splits,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes attn_fwd_splitkv needs for these sizes (0 if the call resolves to one split or
+ * the sizes are invalid).  num_splits == 0 uses attn_fwd_splitkv_num_splits(). */
+size_t attn_fwd_splitkv_workspace_bytes(int B, int Hq, int N, int D, int num_splits);
+
+/* Suggested split count for the current device: when the query tiles alone leave SMs idle,
+ * as many splits as fit the SMs while every split keeps at least 4 key tiles (at most 16);
+ * else 1. */
+int attn_fwd_splitkv_num_splits(int B, int Hq, int N, int D, int causal);
 
 /* Static, human-readable text for an attn_status_t value (never NULL). */
 const char* attn_status_string(int status);

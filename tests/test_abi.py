@@ -27,7 +27,8 @@ def _declared_functions():
 
 def test_header_declares_the_boundary():
     assert _declared_functions() == sorted(
-        ["attn_fwd", "attn_status_string", "attn_last_cuda_error", "attn_debug_status"])
+        ["attn_fwd", "attn_status_string", "attn_last_cuda_error", "attn_debug_status",
+         "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_bytes", "attn_fwd_splitkv_num_splits"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -47,7 +48,7 @@ def test_built_for_sm_103a_only():
 
 
 def test_status_strings(lib):
-    for st in range(-11, 1):
+    for st in range(-13, 1):
         s = lib.attn_status_string(st)
         assert isinstance(s, bytes) and len(s) > 0
     assert lib.attn_status_string(0) == b"ok"
@@ -90,3 +91,37 @@ def test_aliasing_output_is_rejected(lib):
     # out overlapping q: rejected before any device query
     assert _call(lib, out=P) == -11
     assert _call(lib, lse=P * 4 + 64) == -11
+
+
+S = 1 << 24  # fake addresses 16 MiB apart (larger than any tensor below)
+
+
+def _split(lib, q=S, k=S * 2, v=S * 3, out=S * 4, lse=S * 5, B=1, Hq=2, Hkv=1, N=512, D=64,
+           causal=0, scale=0.125, splits=2, ws=S * 8, ws_bytes=1 << 30):
+    return lib.attn_fwd_splitkv(q, k, v, out, lse, B, Hq, Hkv, N, D, causal,
+                                ctypes.c_float(scale), splits, ws, ws_bytes, None)
+
+
+def test_splitkv_workspace_bytes(lib):
+    # n_splits * B*Hq * N * (D + 1) * 4 bytes, with the split count the tile layout allows
+    assert lib.attn_fwd_splitkv_workspace_bytes(1, 32, 512, 128, 2) == 2 * 32 * 512 * 129 * 4
+    assert lib.attn_fwd_splitkv_workspace_bytes(1, 16, 512, 128, 4) == 4 * 16 * 512 * 129 * 4
+    # 4 key tiles into 3 requested splits -> 2 tiles per split -> 2 splits
+    assert lib.attn_fwd_splitkv_workspace_bytes(1, 32, 512, 128, 3) == 2 * 32 * 512 * 129 * 4
+    assert lib.attn_fwd_splitkv_workspace_bytes(1, 32, 512, 128, 1) == 0
+    assert lib.attn_fwd_splitkv_workspace_bytes(1, 2, 100, 64, 8) == 0  # one key tile
+    assert lib.attn_fwd_splitkv_workspace_bytes(1, 2, 128, 96, 2) == 0  # bad D
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(splits=-1), -12), (dict(splits=65), -12),
+    (dict(ws=0), -1), (dict(ws=S * 8 + 4), -5), (dict(ws_bytes=1000), -13),
+    (dict(ws=S), -11),  # workspace overlaps q
+    (dict(Hq=3, Hkv=2), -3), (dict(D=32), -4),
+])
+def test_splitkv_host_validation(lib, kw, status):
+    assert _split(lib, **kw) == status
+
+
+def test_splitkv_empty_problem(lib):
+    assert _split(lib, B=0, ws=0, ws_bytes=0) == 0
