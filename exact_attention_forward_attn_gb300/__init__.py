@@ -17,7 +17,7 @@ STATUS_NAMES = {
     0: "ATTN_OK", -1: "ATTN_ERR_NULL", -2: "ATTN_ERR_SHAPE", -3: "ATTN_ERR_HEADS",
     -4: "ATTN_ERR_HEADDIM", -5: "ATTN_ERR_ALIGN", -6: "ATTN_ERR_SCALE", -7: "ATTN_ERR_ARCH",
     -8: "ATTN_ERR_CUDA", -9: "ATTN_ERR_TIMEOUT", -10: "ATTN_ERR_MEMORY", -11: "ATTN_ERR_ALIAS",
-    -12: "ATTN_ERR_SPLITS", -13: "ATTN_ERR_WORKSPACE",
+    -12: "ATTN_ERR_SPLITS", -13: "ATTN_ERR_WORKSPACE", -14: "ATTN_ERR_SCRATCH",
 }
 
 

@@ -366,6 +366,9 @@ extern "C" const char* attn_status_string(int status) {
         case ATTN_ERR_ALIAS: return "out/lse/workspace overlap an input or each other";
         case ATTN_ERR_SPLITS: return "num_splits must be in [0, 64]";
         case ATTN_ERR_WORKSPACE: return "workspace smaller than attn_fwd_splitkv_workspace_bytes";
+        case ATTN_ERR_SCRATCH:
+            return "problem needs more split-KV scratch than the built-in buffer "
+                   "(attn_fwd_splitkv_noalloc_max_bytes)";
         default: return "unknown status";
     }
 }
@@ -386,4 +389,69 @@ extern "C" int attn_debug_status(void* stream) {
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e);
     return (word & kDevTimeout) ? ATTN_ERR_TIMEOUT : ATTN_OK;
+}
+
+// ------------------------------------------------------------------------------------------------
+// Split-KV forward without any device allocation.
+//
+// Some callers cannot allocate device memory when they call us: a plug-in whose host application
+// owns the whole device-memory budget, or a latency-critical serving loop that forbids
+// allocation after start-up.  For them the split partials live in this fixed, file-scope device
+// buffer instead of a caller-provided workspace.  Every GPU that loads the library holds it
+// (kNoAllocScratchBytes) until the process exits.
+// ------------------------------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB
+static __device__ __align__(256) unsigned char g_splitkv_scratch[kNoAllocScratchBytes];
+
+// In host code `g_splitkv_scratch` only names a host-side stand-in for the device array, so the
+// device address is looked up once per device (with that device current) and cached.
+struct ScratchState {
+    std::once_flag once;
+    cudaError_t error = cudaSuccess;
+    void* ptr = nullptr;
+};
+ScratchState g_scratch[kMaxDevices];
+
+int scratch_address(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return cuda_fail(cudaErrorInvalidDevice);
+    ScratchState& st = g_scratch[dev];
+    std::call_once(st.once, [&st] {
+        st.error = cudaGetSymbolAddress(&st.ptr, g_splitkv_scratch);
+        if (st.error != cudaSuccess) st.ptr = nullptr;
+    });
+    if (st.error != cudaSuccess) return cuda_fail(st.error);
+    *out = st.ptr;
+    return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" size_t attn_fwd_splitkv_noalloc_max_bytes(void) { return kNoAllocScratchBytes; }
+
+extern "C" int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* out,
+                                        float* lse, int B, int Hq, int Hkv, int N, int D,
+                                        int causal, float sm_scale, int num_splits,
+                                        void* stream) {
+    if (num_splits < 0 || num_splits > kMaxSplits) return ATTN_ERR_SPLITS;
+    Problem P{q, k, v, out, lse, B, Hq, Hkv, N, D, causal, sm_scale};
+    bool empty = false;
+    const int st = validate(P, &empty);
+    if (st != ATTN_OK || empty) return st;
+    if (num_splits == 0) num_splits = attn_fwd_splitkv_num_splits(B, Hq, N, D, causal);
+    int split_tiles = 0, n_splits = 0;
+    split_layout(P.n_tiles, num_splits, &split_tiles, &n_splits);
+    if (n_splits > 1 && workspace_bytes_for(P.bh, N, D, n_splits) >
+                            static_cast<int64_t>(kNoAllocScratchBytes))
+        return ATTN_ERR_SCRATCH;  // checked before anything touches the device
+    void* scratch = nullptr;
+    const int sa = scratch_address(&scratch);
+    if (sa != ATTN_OK) return sa;
+    // The split kernel writes every partial the merge reads, so nothing has to start at zero.
+    return attn_fwd_splitkv(q, k, v, out, lse, B, Hq, Hkv, N, D, causal, sm_scale, num_splits,
+                            scratch, kNoAllocScratchBytes, stream);
 }

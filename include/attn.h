@@ -50,7 +50,8 @@ typedef enum {
     ATTN_ERR_MEMORY = -10,  /* a pointer is not device memory of the current device */
     ATTN_ERR_ALIAS = -11,   /* out, lse or the workspace overlaps q, k, v or each other */
     ATTN_ERR_SPLITS = -12,  /* num_splits outside [0, 64] */
-    ATTN_ERR_WORKSPACE = -13 /* workspace smaller than attn_fwd_splitkv_workspace_bytes() */
+    ATTN_ERR_WORKSPACE = -13, /* workspace smaller than attn_fwd_splitkv_workspace_bytes() */
+    ATTN_ERR_SCRATCH = -14  /* attn_fwd_splitkv_noalloc: more scratch needed than it has */
 } attn_status_t;
 
 /*
@@ -110,6 +111,32 @@ size_t attn_fwd_splitkv_workspace_bytes(int B, int Hq, int N, int D, int num_spl
  * as many splits as fit the SMs while every split keeps at least 4 key tiles (at most 16);
  * else 1. */
 int attn_fwd_splitkv_num_splits(int B, int Hq, int N, int D, int causal);
+
+/*
+ * attn_fwd_splitkv_noalloc - attn_fwd_splitkv for callers that cannot allocate device memory.
+ *
+ * No counterpart in the pages: this is a convenience of this library.  Some callers cannot hand
+ * us a workspace because they may not allocate device memory at call time (a plug-in whose host
+ * application owns the whole device-memory budget, or a serving loop that forbids allocation
+ * after start-up).  This entry point keeps the split partials in a fixed device buffer compiled
+ * into the library (attn_fwd_splitkv_noalloc_max_bytes() bytes, held on every GPU that loads the
+ * library until the process exits) and calls no allocator of any kind.
+ *
+ *   Arguments, outputs and result: as attn_fwd_splitkv, without the workspace arguments.
+ *   A problem whose partials need more than the buffer holds (attn_fwd_splitkv_workspace_bytes()
+ *   > attn_fwd_splitkv_noalloc_max_bytes()) returns ATTN_ERR_SCRATCH before touching the device.
+ *   The buffer's device address is looked up the first time this is called on a device (with that
+ *   device current); make that first call before capturing any stream.
+ *   All calls share the one buffer, and it keeps the last call's partials (nothing in it needs to
+ *   start at zero).  Calls that overlap on the GPU - on different streams, or from several host
+ *   threads without ordering - race on it and may return wrong results; serialise them.
+ */
+int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* out, float* lse,
+                             int B, int Hq, int Hkv, int N, int D, int causal, float sm_scale,
+                             int num_splits, void* stream);
+
+/* Size in bytes of the fixed buffer attn_fwd_splitkv_noalloc uses. */
+size_t attn_fwd_splitkv_noalloc_max_bytes(void);
 
 /* Static, human-readable text for an attn_status_t value (never NULL). */
 const char* attn_status_string(int status);

@@ -28,7 +28,8 @@ def _declared_functions():
 def test_header_declares_the_boundary():
     assert _declared_functions() == sorted(
         ["attn_fwd", "attn_status_string", "attn_last_cuda_error", "attn_debug_status",
-         "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_bytes", "attn_fwd_splitkv_num_splits"])
+         "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_bytes", "attn_fwd_splitkv_num_splits",
+         "attn_fwd_splitkv_noalloc", "attn_fwd_splitkv_noalloc_max_bytes"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -48,7 +49,7 @@ def test_built_for_sm_103a_only():
 
 
 def test_status_strings(lib):
-    for st in range(-13, 1):
+    for st in range(-14, 1):
         s = lib.attn_status_string(st)
         assert isinstance(s, bytes) and len(s) > 0
     assert lib.attn_status_string(0) == b"ok"
