@@ -8,6 +8,7 @@ outputs with PyTorch and marshals pointers, sizes and the current stream.
 """
 from __future__ import annotations
 
+import ctypes
 import math
 
 from . import _lib
@@ -18,6 +19,7 @@ STATUS_NAMES = {
     -4: "ATTN_ERR_HEADDIM", -5: "ATTN_ERR_ALIGN", -6: "ATTN_ERR_SCALE", -7: "ATTN_ERR_ARCH",
     -8: "ATTN_ERR_CUDA", -9: "ATTN_ERR_TIMEOUT", -10: "ATTN_ERR_MEMORY", -11: "ATTN_ERR_ALIAS",
     -12: "ATTN_ERR_SPLITS", -13: "ATTN_ERR_WORKSPACE", -14: "ATTN_ERR_SCRATCH",
+    -15: "ATTN_ERR_STRIDE",
 }
 
 
@@ -38,7 +40,7 @@ def _stream_handle(device):
     return torch.cuda.current_stream(device).cuda_stream
 
 
-def _check_inputs(q, k, v):
+def _check_inputs(q, k, v, allow_strided=False):
     import torch
 
     for name, t in (("q", q), ("k", k), ("v", v)):
@@ -48,7 +50,10 @@ def _check_inputs(q, k, v):
             raise ValueError(f"{name} must be bf16, got {t.dtype}")
         if not t.is_cuda:
             raise ValueError(f"{name} must be a CUDA tensor")
-        if not t.is_contiguous():
+        if allow_strided:
+            if t.stride(-1) != 1:
+                raise ValueError(f"{name}: the D axis must be contiguous (stride 1)")
+        elif not t.is_contiguous():
             raise ValueError(f"{name} must be contiguous ([B, H, N, D] row-major); call "
                              ".contiguous() first")
     B, Hq, N, D = q.shape
@@ -59,16 +64,18 @@ def _check_inputs(q, k, v):
     return B, Hq, k.shape[1], N, D
 
 
-def _outputs(q, out, lse):
+def _outputs(q, out, lse, allow_strided=False):
     import torch
 
     B, Hq, N, _ = q.shape
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty_like(q)  # keeps q's layout when q is dense
     if lse is None:
         lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
-    if out.shape != q.shape or out.dtype != torch.bfloat16 or not out.is_contiguous():
-        raise ValueError("out must be a contiguous bf16 tensor shaped like q")
+    ok_layout = out.stride(-1) == 1 if allow_strided else out.is_contiguous()
+    if out.shape != q.shape or out.dtype != torch.bfloat16 or not ok_layout:
+        raise ValueError("out must be a bf16 tensor shaped like q (contiguous, or with a "
+                         "contiguous D axis for strided inputs)")
     if lse.shape != (B, Hq, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous fp32 tensor [B, Hq, N]")
     return out, lse
@@ -78,19 +85,31 @@ def attn_fwd(q, k, v, causal: bool = False, sm_scale: float | None = None, out=N
     """Fused attention forward on the current CUDA stream of ``q``'s device.
 
     Returns ``(out, lse)``: out bf16 [B,Hq,N,D], lse fp32 [B,Hq,N].  ``out``/``lse`` may be passed
-    preallocated (contiguous, right shape and dtype).  Raises ``AttnError`` on a nonzero status.
+    preallocated (right shape and dtype).  q, k, v, out may be strided views (e.g. [B, N, H, D]
+    memory seen as [B, H, N, D]) as long as D is contiguous and the other strides are multiples of
+    8 elements; those go through ``attn_fwd_strided`` without a copy.  Raises ``AttnError`` on a
+    nonzero status.
     """
     import torch
 
-    B, Hq, Hkv, N, D = _check_inputs(q, k, v)
+    B, Hq, Hkv, N, D = _check_inputs(q, k, v, allow_strided=True)
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(D)
-    out, lse = _outputs(q, out, lse)
+    out, lse = _outputs(q, out, lse, allow_strided=True)
     lib = _lib.load()
     with torch.cuda.device(q.device):
-        st = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                          B, Hq, Hkv, N, D, int(bool(causal)), float(sm_scale),
-                          _stream_handle(q.device))
+        if all(t.is_contiguous() for t in (q, k, v, out)):
+            st = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                              lse.data_ptr(), B, Hq, Hkv, N, D, int(bool(causal)),
+                              float(sm_scale), _stream_handle(q.device))
+        else:
+            arrs = [(ctypes.c_longlong * 3)(t.stride(0), t.stride(1), t.stride(2))
+                    for t in (q, k, v, out)]
+            st = lib.attn_fwd_strided(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                      lse.data_ptr(), B, Hq, Hkv, N, D, int(bool(causal)),
+                                      float(sm_scale), *[ctypes.cast(a, ctypes.c_void_p)
+                                                         for a in arrs],
+                                      _stream_handle(q.device))
     if st != ATTN_OK:
         raise AttnError(st)
     return out, lse

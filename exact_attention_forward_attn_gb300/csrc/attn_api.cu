@@ -10,6 +10,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -53,18 +54,27 @@ EncodeTiledFn encode_tiled() {
     return fn;
 }
 
-// 3-D view [BH, N, D] of a contiguous bf16 tensor; box = 64 (D) x 128 (rows) x 1, 128B swizzle.
+// Element strides of a [B, H, N, D] bf16 tensor whose D axis is contiguous.
+struct Strides {
+    int64_t n, h, b;
+};
+
+Strides contiguous_strides(int64_t H, int64_t N, int64_t D) { return {D, N * D, H * N * D}; }
+
+// 4-D view [B, H, N, D] (innermost D); box = 64 (D) x 128 (rows) x 1 x 1, 128B swizzle.
 // Rows >= N of a head are out of bounds: zero-filled on load, dropped on store.
-bool make_tile_map(CUtensorMap* map, const void* base, int64_t BH, int64_t N, int64_t D) {
+bool make_tile_map(CUtensorMap* map, const void* base, int64_t B, int64_t H, int64_t N, int64_t D,
+                   const Strides& st) {
     EncodeTiledFn enc = encode_tiled();
     if (!enc) return false;
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N),
-                                static_cast<cuuint64_t>(BH)};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D * 2),
-                                   static_cast<cuuint64_t>(N * D * 2)};
-    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kBM), 1};
-    const cuuint32_t elem_strides[3] = {1, 1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N),
+                                static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(st.n * 2),
+                                   static_cast<cuuint64_t>(st.h * 2),
+                                   static_cast<cuuint64_t>(st.b * 2)};
+    const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(kBM), 1, 1};
+    const cuuint32_t elem_strides[4] = {1, 1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
                box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
            CUDA_SUCCESS;
@@ -136,7 +146,7 @@ bool overlaps(const void* a, int64_t a_bytes, const void* b, int64_t b_bytes) {
     return a0 < b0 + static_cast<uintptr_t>(b_bytes) && b0 < a0 + static_cast<uintptr_t>(a_bytes);
 }
 
-// Everything about one call that both entry points share.
+// Everything about one call that the entry points share.
 struct Problem {
     const void *q, *k, *v;
     void* out;
@@ -144,8 +154,22 @@ struct Problem {
     int B, Hq, Hkv, N, D, causal;
     float sm_scale;
     int64_t bh, bh_kv, n_tiles, n_pairs, items;
-    int64_t q_bytes, kv_bytes, lse_bytes;
+    int64_t q_bytes, kv_bytes, lse_bytes;  // byte spans: [ptr, ptr + bytes) covers each tensor
+    bool strided = false;                   // strides below given by the caller
+    Strides sq{}, sk{}, sv{}, so{};
 };
+
+// Byte span of a strided [B, H, N, D] bf16 tensor (from its first to one past its last element).
+int64_t span_bytes(int64_t B, int64_t H, int64_t N, int64_t D, const Strides& st) {
+    return ((B - 1) * st.b + (H - 1) * st.h + (N - 1) * st.n + D) * 2;
+}
+
+// TMA needs every stride to be a positive multiple of 16 bytes (8 bf16) and below 2^40 bytes.
+bool strides_ok(const Strides& st) {
+    for (int64_t x : {st.n, st.h, st.b})
+        if (x <= 0 || (x % 8) != 0 || x >= (int64_t(1) << 39)) return false;
+    return true;
+}
 
 // Host-side validation; returns ATTN_OK with *empty set for an empty problem.  Nothing is
 // launched or written when this fails.
@@ -173,12 +197,19 @@ int validate(Problem& P, bool* empty) {
     P.items = P.n_pairs * P.bh;
     if (P.items > 0x7fffffffLL || P.bh > 0x7fffffffLL) return ATTN_ERR_SHAPE;
 
-    P.q_bytes = P.bh * P.N * P.D * 2;
-    P.kv_bytes = P.bh_kv * P.N * P.D * 2;
+    if (!P.strided) {
+        P.sq = P.so = contiguous_strides(P.Hq, P.N, P.D);
+        P.sk = P.sv = contiguous_strides(P.Hkv, P.N, P.D);
+    } else if (!strides_ok(P.sq) || !strides_ok(P.sk) || !strides_ok(P.sv) || !strides_ok(P.so)) {
+        return ATTN_ERR_STRIDE;
+    }
+    P.q_bytes = span_bytes(P.B, P.Hq, P.N, P.D, P.sq);
+    P.kv_bytes = std::max(span_bytes(P.B, P.Hkv, P.N, P.D, P.sk),
+                          span_bytes(P.B, P.Hkv, P.N, P.D, P.sv));
     P.lse_bytes = P.bh * P.N * 4;
-    if (overlaps(P.out, P.q_bytes, P.q, P.q_bytes) || overlaps(P.out, P.q_bytes, P.k, P.kv_bytes) ||
-        overlaps(P.out, P.q_bytes, P.v, P.kv_bytes) ||
-        overlaps(P.out, P.q_bytes, P.lse, P.lse_bytes) ||
+    const int64_t o_bytes = span_bytes(P.B, P.Hq, P.N, P.D, P.so);
+    if (overlaps(P.out, o_bytes, P.q, P.q_bytes) || overlaps(P.out, o_bytes, P.k, P.kv_bytes) ||
+        overlaps(P.out, o_bytes, P.v, P.kv_bytes) || overlaps(P.out, o_bytes, P.lse, P.lse_bytes) ||
         overlaps(P.lse, P.lse_bytes, P.q, P.q_bytes) ||
         overlaps(P.lse, P.lse_bytes, P.k, P.kv_bytes) ||
         overlaps(P.lse, P.lse_bytes, P.v, P.kv_bytes))
@@ -197,8 +228,10 @@ int prepare(const Problem& P, DeviceState** ds, CUtensorMap* mq, CUtensorMap* mk
     for (const void* ptr :
          {P.q, P.k, P.v, static_cast<const void*>(P.out), static_cast<const void*>(P.lse)})
         if (check_memory(ptr, dev) != ATTN_OK) return ATTN_ERR_MEMORY;
-    if (!make_tile_map(mq, P.q, P.bh, P.N, P.D) || !make_tile_map(mk, P.k, P.bh_kv, P.N, P.D) ||
-        !make_tile_map(mv, P.v, P.bh_kv, P.N, P.D) || !make_tile_map(mo, P.out, P.bh, P.N, P.D))
+    if (!make_tile_map(mq, P.q, P.B, P.Hq, P.N, P.D, P.sq) ||
+        !make_tile_map(mk, P.k, P.B, P.Hkv, P.N, P.D, P.sk) ||
+        !make_tile_map(mv, P.v, P.B, P.Hkv, P.N, P.D, P.sv) ||
+        !make_tile_map(mo, P.out, P.B, P.Hq, P.N, P.D, P.so))
         return cuda_fail(cudaErrorInvalidValue);
     prm->B = P.B;
     prm->Hq = P.Hq;
@@ -268,6 +301,32 @@ int64_t workspace_bytes_for(int64_t bh, int64_t N, int64_t D, int n_splits) {
 extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B,
                         int Hq, int Hkv, int N, int D, int causal, float sm_scale, void* stream) {
     Problem P{q, k, v, out, lse, B, Hq, Hkv, N, D, causal, sm_scale};
+    bool empty = false;
+    int st = validate(P, &empty);
+    if (st != ATTN_OK || empty) return st;
+    DeviceState* ds = nullptr;
+    CUtensorMap mq, mk, mv, mo;
+    AttnParams prm;
+    st = prepare(P, &ds, &mq, &mk, &mv, &mo, &prm);
+    if (st != ATTN_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return D == 64 ? launch_fwd<64, false>(mq, mk, mv, mo, prm, ds->status_word, P.items, s)
+                   : launch_fwd<128, false>(mq, mk, mv, mo, prm, ds->status_word, P.items, s);
+}
+
+extern "C" int attn_fwd_strided(const void* q, const void* k, const void* v, void* out,
+                                float* lse, int B, int Hq, int Hkv, int N, int D, int causal,
+                                float sm_scale, const long long* q_strides,
+                                const long long* k_strides, const long long* v_strides,
+                                const long long* o_strides, void* stream) {
+    if (!q_strides || !k_strides || !v_strides || !o_strides) return ATTN_ERR_NULL;
+    Problem P{q, k, v, out, lse, B, Hq, Hkv, N, D, causal, sm_scale};
+    P.strided = true;
+    // caller order per tensor: {batch, head, row} strides in elements
+    P.sq = {q_strides[2], q_strides[1], q_strides[0]};
+    P.sk = {k_strides[2], k_strides[1], k_strides[0]};
+    P.sv = {v_strides[2], v_strides[1], v_strides[0]};
+    P.so = {o_strides[2], o_strides[1], o_strides[0]};
     bool empty = false;
     int st = validate(P, &empty);
     if (st != ATTN_OK || empty) return st;
@@ -366,6 +425,8 @@ extern "C" const char* attn_status_string(int status) {
         case ATTN_ERR_ALIAS: return "out/lse/workspace overlap an input or each other";
         case ATTN_ERR_SPLITS: return "num_splits must be in [0, 64]";
         case ATTN_ERR_WORKSPACE: return "workspace smaller than attn_fwd_splitkv_workspace_bytes";
+        case ATTN_ERR_STRIDE:
+            return "a stride is not a positive multiple of 8 elements (16 bytes) below 2^39";
         case ATTN_ERR_SCRATCH:
             return "problem needs more split-KV scratch than the built-in buffer "
                    "(attn_fwd_splitkv_noalloc_max_bytes)";

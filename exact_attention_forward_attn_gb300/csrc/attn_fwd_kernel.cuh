@@ -132,7 +132,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rem = item % per_kv;
     const int pair = p.n_pairs - 1 - rem / p.group;
     const int b = bh_kv / p.Hkv;
-    const int hq = (bh_kv % p.Hkv) * p.group + rem % p.group;
+    const int hkv = bh_kv % p.Hkv;
+    const int hq = hkv * p.group + rem % p.group;
     const int bh = b * p.Hq + hq;
     const int tile0 = 2 * pair;
     // This CTA's KV tiles: [kv_begin, kv_limit).  Each Q tile t uses [kv_begin, last_t]; under the
@@ -187,8 +188,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = 0; t < 2; ++t)
                 if (t == 0 ? part0 : part1)
                     for (int h = 0; h < kPanels; ++h)
-                        tma_load_3d(sbase + L::kQ + t * L::kTileBytes + h * L::kPanelBytes,
-                                    &tmap_q, bar(L::kBarQ), h * 64, (tile0 + t) * kBM, bh);
+                        tma_load_4d(sbase + L::kQ + t * L::kTileBytes + h * L::kPanelBytes,
+                                    &tmap_q, bar(L::kBarQ), h * 64, (tile0 + t) * kBM, hq, b);
             for (int j = kv_begin; j < kv_end; ++j) {
                 for (int kv = 0; kv < 2; ++kv) {
                     const int idx = 2 * (j - kv_begin) + kv;
@@ -200,8 +201,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_expect_tx(bar(L::kBarKvFull + slot), L::kTileBytes);
                     const CUtensorMap* map = kv ? &tmap_v : &tmap_k;
                     for (int h = 0; h < kPanels; ++h)
-                        tma_load_3d(sbase + L::kKV + slot * L::kTileBytes + h * L::kPanelBytes, map,
-                                    bar(L::kBarKvFull + slot), h * 64, j * kBN, bh_kv);
+                        tma_load_4d(sbase + L::kKV + slot * L::kTileBytes + h * L::kPanelBytes, map,
+                                    bar(L::kBarKvFull + slot), h * 64, j * kBN, hkv, b);
                 }
             }
         producer_done:;
@@ -482,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok && quarter == 0 && lane == 0) {
                 const uint32_t stage = sbase + L::kQ + t * L::kTileBytes;
                 for (int h = 0; h < kPanels; ++h)
-                    tma_store_3d(&tmap_o, stage + h * L::kPanelBytes, h * 64, q_tile * kBM, bh);
+                    tma_store_4d(&tmap_o, stage + h * L::kPanelBytes, h * 64, q_tile * kBM, hq, b);
                 tma_store_commit_and_wait();
             }
             }  // !kSplit

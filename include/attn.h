@@ -51,7 +51,8 @@ typedef enum {
     ATTN_ERR_ALIAS = -11,   /* out, lse or the workspace overlaps q, k, v or each other */
     ATTN_ERR_SPLITS = -12,  /* num_splits outside [0, 64] */
     ATTN_ERR_WORKSPACE = -13, /* workspace smaller than attn_fwd_splitkv_workspace_bytes() */
-    ATTN_ERR_SCRATCH = -14  /* attn_fwd_splitkv_noalloc: more scratch needed than it has */
+    ATTN_ERR_SCRATCH = -14, /* attn_fwd_splitkv_noalloc: more scratch needed than it has */
+    ATTN_ERR_STRIDE = -15   /* attn_fwd_strided: a stride is not usable by the TMA */
 } attn_status_t;
 
 /*
@@ -74,6 +75,25 @@ typedef enum {
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
              int Hkv, int N, int D, int causal, float sm_scale, void* stream);
+
+/*
+ * attn_fwd_strided - attn_fwd for tensors that are not contiguous, e.g. the [B, N, H, D] layout
+ * that projections usually produce.  "Triton-CUDA Attention" (skillmd.com) asks callers to
+ * transpose and make such inputs contiguous first (its common-errors table); here the TMA tensor
+ * maps take the strides directly, so no copy is needed.
+ *
+ *   q, k, v, out, lse, B, Hq, Hkv, N, D, causal, sm_scale, stream: as for attn_fwd, except that
+ *     q, k, v and out are [B, H, N, D] tensors addressed through strides (D still contiguous);
+ *     lse is contiguous [B, Hq, N].
+ *   q_strides, k_strides, v_strides, o_strides: host arrays of 3 element strides each,
+ *     {batch, head, row}; each must be a positive multiple of 8 elements (16 bytes) below 2^39,
+ *     else ATTN_ERR_STRIDE.  A contiguous tensor has {H*N*D, N*D, D}; a [B, N, H, D] one has
+ *     {N*H*D, D, H*D}.  out must not overlap any input (checked over each tensor's byte span).
+ */
+int attn_fwd_strided(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                     int Hq, int Hkv, int N, int D, int causal, float sm_scale,
+                     const long long* q_strides, const long long* k_strides,
+                     const long long* v_strides, const long long* o_strides, void* stream);
 
 /*
  * attn_fwd_splitkv - the same forward, with the key axis of every query tile cut into splits.

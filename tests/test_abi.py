@@ -29,7 +29,7 @@ def test_header_declares_the_boundary():
     assert _declared_functions() == sorted(
         ["attn_fwd", "attn_status_string", "attn_last_cuda_error", "attn_debug_status",
          "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_bytes", "attn_fwd_splitkv_num_splits",
-         "attn_fwd_splitkv_noalloc", "attn_fwd_splitkv_noalloc_max_bytes"])
+         "attn_fwd_splitkv_noalloc", "attn_fwd_splitkv_noalloc_max_bytes", "attn_fwd_strided"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -49,7 +49,7 @@ def test_built_for_sm_103a_only():
 
 
 def test_status_strings(lib):
-    for st in range(-14, 1):
+    for st in range(-15, 1):
         s = lib.attn_status_string(st)
         assert isinstance(s, bytes) and len(s) > 0
     assert lib.attn_status_string(0) == b"ok"
@@ -126,3 +126,18 @@ def test_splitkv_host_validation(lib, kw, status):
 
 def test_splitkv_empty_problem(lib):
     assert _split(lib, B=0, ws=0, ws_bytes=0) == 0
+
+
+def _strided(lib, qs=(2 * 128 * 64, 128 * 64, 64), ks=(128 * 64, 128 * 64, 64),
+             os_=(2 * 128 * 64, 128 * 64, 64), B=1, Hq=2, Hkv=1, N=128, D=64):
+    arr = lambda t: (ctypes.c_longlong * 3)(*t) if t is not None else None
+    return lib.attn_fwd_strided(S, S * 2, S * 3, S * 4, S * 5, B, Hq, Hkv, N, D, 0,
+                                ctypes.c_float(0.125), arr(qs), arr(ks), arr(ks), arr(os_), None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(qs=None), -1), (dict(ks=(0, 8192, 64)), -15), (dict(os_=(16384, 8192, 68)), -15),
+    (dict(qs=(16384, -8192, 64)), -15), (dict(qs=(16384, 8192, 12)), -15),
+])
+def test_strided_host_validation(lib, kw, status):
+    assert _strided(lib, **kw) == status
