@@ -26,6 +26,8 @@ SIGNATURES = {
     "attn_fwd_splitkv_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
                                           _c_int, _c_int, _c_int, _c_float, _c_int, _vp]),
     "attn_fwd_splitkv_noalloc_max_bytes": (ctypes.c_size_t, []),
+    "attn_fwd_test_stall": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
+                                     _c_int, _c_int, _c_float, _c_int, _vp]),
     "attn_fwd_strided": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
                                   _c_int, _c_float, _vp, _vp, _vp, _vp, _vp]),
 }

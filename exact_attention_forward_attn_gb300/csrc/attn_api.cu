@@ -247,6 +247,7 @@ int prepare(const Problem& P, DeviceState** ds, CUtensorMap* mq, CUtensorMap* mk
     prm->split_tiles = prm->n_tiles;
     prm->ws_o = nullptr;
     prm->ws_lse = nullptr;
+    prm->stall_item = -1;
     return ATTN_OK;
 }
 
@@ -335,6 +336,25 @@ extern "C" int attn_fwd_strided(const void* q, const void* k, const void* v, voi
     AttnParams prm;
     st = prepare(P, &ds, &mq, &mk, &mv, &mo, &prm);
     if (st != ATTN_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return D == 64 ? launch_fwd<64, false>(mq, mk, mv, mo, prm, ds->status_word, P.items, s)
+                   : launch_fwd<128, false>(mq, mk, mv, mo, prm, ds->status_word, P.items, s);
+}
+
+extern "C" int attn_fwd_test_stall(const void* q, const void* k, const void* v, void* out,
+                                   float* lse, int B, int Hq, int Hkv, int N, int D, int causal,
+                                   float sm_scale, int stall_item, void* stream) {
+    Problem P{q, k, v, out, lse, B, Hq, Hkv, N, D, causal, sm_scale};
+    bool empty = false;
+    int st = validate(P, &empty);
+    if (st != ATTN_OK || empty) return st;
+    if (stall_item < 0) return ATTN_ERR_SHAPE;
+    DeviceState* ds = nullptr;
+    CUtensorMap mq, mk, mv, mo;
+    AttnParams prm;
+    st = prepare(P, &ds, &mq, &mk, &mv, &mo, &prm);
+    if (st != ATTN_OK) return st;
+    prm.stall_item = stall_item;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return D == 64 ? launch_fwd<64, false>(mq, mk, mv, mo, prm, ds->status_word, P.items, s)
                    : launch_fwd<128, false>(mq, mk, mv, mo, prm, ds->status_word, P.items, s);

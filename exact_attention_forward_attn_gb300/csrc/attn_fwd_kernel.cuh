@@ -61,6 +61,9 @@ struct AttnParams {
     int split_tiles;
     float* ws_o;       // [n_splits, B*Hq, N, D] fp32, O of each split normalised by its own l
     float* ws_lse;     // [n_splits, B*Hq, N] fp32, natural-log LSE of each split
+    // Test hook (-1 normally): the producer withholds K/V ring item `stall_item` of every CTA,
+    // so the waits on it expire and the failure is reported through the status word.
+    int stall_item;
 };
 
 template <int D>
@@ -198,6 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!mbar_wait_bounded(bar(L::kBarKvEmpty + slot), ph ^ 1u, abort_flag,
                                            status_word))
                         goto producer_done;
+                    if (idx == p.stall_item) continue;  // test hook: never deliver this item
                     mbar_arrive_expect_tx(bar(L::kBarKvFull + slot), L::kTileBytes);
                     const CUtensorMap* map = kv ? &tmap_v : &tmap_k;
                     for (int h = 0; h < kPanels; ++h)

@@ -172,6 +172,20 @@ int attn_last_cuda_error(void);
  */
 int attn_debug_status(void* stream);
 
+/*
+ * attn_fwd_test_stall - test hook for the failure-reporting path (not for computing anything).
+ *
+ * Runs attn_fwd, except that every CTA's producer withholds item `stall_item` (>= 0) of its K/V
+ * load ring (item 2j is K tile j, 2j+1 is V tile j, counted from the CTA's first tile), so the
+ * bounded waits on it expire after about one second.  The CTA then stops all its roles, frees its
+ * tensor memory and returns; out and lse hold garbage, the device status word records the
+ * expiry (attn_debug_status returns ATTN_ERR_TIMEOUT) and the CUDA context stays usable.  An
+ * item past the CTA's last one stalls nothing.  Use tiny problems: each CTA waits ~1 s.
+ */
+int attn_fwd_test_stall(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                        int Hq, int Hkv, int N, int D, int causal, float sm_scale, int stall_item,
+                        void* stream);
+
 #ifdef __cplusplus
 }
 #endif

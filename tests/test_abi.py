@@ -29,7 +29,8 @@ def test_header_declares_the_boundary():
     assert _declared_functions() == sorted(
         ["attn_fwd", "attn_status_string", "attn_last_cuda_error", "attn_debug_status",
          "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_bytes", "attn_fwd_splitkv_num_splits",
-         "attn_fwd_splitkv_noalloc", "attn_fwd_splitkv_noalloc_max_bytes", "attn_fwd_strided"])
+         "attn_fwd_splitkv_noalloc", "attn_fwd_splitkv_noalloc_max_bytes", "attn_fwd_strided",
+         "attn_fwd_test_stall"])
 
 
 def test_library_exports_every_declared_symbol(lib):
