@@ -250,9 +250,12 @@ def main():
     if args.impl == "reference":
         return run_reference(args, w)
 
+    import ctypes
+
     import torch
 
     import exact_attention_forward_attn_gb300 as attn
+    from exact_attention_forward_attn_gb300 import _lib
 
     world, rank, local = dist_env()
     if not torch.cuda.is_available():
@@ -321,31 +324,64 @@ def main():
     }
 
     # ---- end to end through the public API: pinned host buffers, copies inside the region -----
+    # Every step copies its inputs host->device and its O and LSE device->host.  Two device
+    # buffer sets and a copy stream let step i+1's inputs and step i-1's results move while
+    # step i computes, as a serving loop would.
     e2e = None
     if rank == 0 or world > 1:
         hq_, hk_, hv_ = (t.cpu().pin_memory() for t in (q, k, v))
-        ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-
-        def e2e_step():
-            dq.copy_(hq_, non_blocking=True)
-            dk.copy_(hk_, non_blocking=True)
-            dv.copy_(hv_, non_blocking=True)
-            attn.attn_fwd(dq, dk, dv, causal=w.causal, sm_scale=w.sm_scale, out=out, lse=lse)
-            ho.copy_(out, non_blocking=True)
-            hl.copy_(lse, non_blocking=True)
-
+        ho = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+        hl = [torch.empty(lse.shape, dtype=lse.dtype).pin_memory() for _ in range(2)]
+        bufs = [tuple(torch.empty_like(t) for t in (q, k, v, out, lse)) for _ in range(2)]
+        copy = torch.cuda.Stream(dev)
         n_e2e = max(3, min(args.steps, 20))
-        with torch.cuda.stream(stream):
-            e2e_step()
-        stream.synchronize()
-        e_ms = timed_launches(e2e_step, stream, n_e2e)
-        h2d = sum(t.numel() * t.element_size() for t in (hq_, hk_, hv_))
-        d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
-        e2e = {"value": w.flops / (statistics.mean(e_ms) * 1e-3) / 1e12, "unit": UNIT,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": statistics.mean(e_ms), "steps": n_e2e}
+        loaded = [torch.cuda.Event() for _ in range(n_e2e)]
+        computed = [torch.cuda.Event() for _ in range(n_e2e)]
+        drained = [torch.cuda.Event() for _ in range(n_e2e)]
+
+        def h2d(i):
+            dq, dk, dv = bufs[i % 2][:3]
+            with torch.cuda.stream(copy):
+                if i >= 2:
+                    copy.wait_event(computed[i - 2])  # the buffer set is free again
+                dq.copy_(hq_, non_blocking=True)
+                dk.copy_(hk_, non_blocking=True)
+                dv.copy_(hv_, non_blocking=True)
+                loaded[i].record(copy)
+
+        def e2e_run(n):
+            start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            start.record(stream)
+            copy.wait_stream(stream)
+            h2d(0)
+            for i in range(n):
+                if i + 1 < n:
+                    h2d(i + 1)
+                dq, dk, dv, do, dl = bufs[i % 2]
+                with torch.cuda.stream(stream):
+                    stream.wait_event(loaded[i])
+                    attn.attn_fwd(dq, dk, dv, causal=w.causal, sm_scale=w.sm_scale, out=do,
+                                  lse=dl)
+                    computed[i].record(stream)
+                with torch.cuda.stream(copy):
+                    copy.wait_event(computed[i])
+                    ho[i % 2].copy_(do, non_blocking=True)
+                    hl[i % 2].copy_(dl, non_blocking=True)
+                    drained[i].record(copy)
+            stream.wait_event(drained[n - 1])
+            end.record(stream)
+            torch.cuda.synchronize()
+            return start.elapsed_time(end)
+
+        e2e_run(2)
+        total = e2e_run(n_e2e)
+        h2d_b = sum(t.numel() * t.element_size() for t in (hq_, hk_, hv_))
+        d2h_b = ho[0].numel() * ho[0].element_size() + hl[0].numel() * hl[0].element_size()
+        e2e = {"value": w.flops * n_e2e / (total * 1e-3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": h2d_b, "d2h_bytes_per_step": d2h_b,
+               "ms_per_step": total / n_e2e, "steps": n_e2e,
+               "overlap": "copies of neighbouring steps overlap compute (2 buffer sets)"}
 
     # ---- context: the other long-context lengths (same kernel), not the headline -------------
     sweep = []
@@ -384,13 +420,19 @@ def main():
                                                                    n_sp)),
                                dtype=torch.uint8, device=dev)
 
+            # Pre-bound C-ABI calls: these kernels take ~15-35 us, less than the Python
+            # binding's per-call host time, which would otherwise be what gets measured.
+            lib = _lib.load()
+            sh = ctypes.c_void_p(stream.cuda_stream)
+            common = (lq.data_ptr(), lk.data_ptr(), lv.data_ptr(), lo.data_ptr(), ll.data_ptr(),
+                      ws_.B, ws_.Hq, ws_.Hkv, ws_.N, ws_.D, int(ws_.causal),
+                      ctypes.c_float(ws_.sm_scale))
+
             def single():
-                attn.attn_fwd(lq, lk, lv, causal=ws_.causal, sm_scale=ws_.sm_scale, out=lo,
-                              lse=ll)
+                assert lib.attn_fwd(*common, sh) == 0
 
             def split():
-                attn.attn_fwd_splitkv(lq, lk, lv, causal=ws_.causal, sm_scale=ws_.sm_scale,
-                                      num_splits=n_sp, workspace=wbuf, out=lo, lse=ll)
+                assert lib.attn_fwd_splitkv(*common, n_sp, wbuf.data_ptr(), wbuf.numel(), sh) == 0
 
             entry = {"workload": ws_.name, "splits": n_sp,
                      "library_choice": attn.splitkv_num_splits(ws_.B, ws_.Hq, ws_.N, ws_.D,

@@ -80,6 +80,42 @@ bool make_tile_map(CUtensorMap* map, const void* base, int64_t B, int64_t H, int
            CUDA_SUCCESS;
 }
 
+// Encoded tensor maps depend only on (address, sizes, strides); repeated calls on the same buffers
+// (the usual case in a serving or training loop) reuse them from a small per-thread cache.
+struct MapKey {
+    const void* base;
+    int64_t B, H, N, D, sn, sh, sb;
+    bool operator==(const MapKey& o) const {
+        return base == o.base && B == o.B && H == o.H && N == o.N && D == o.D && sn == o.sn &&
+               sh == o.sh && sb == o.sb;
+    }
+};
+struct MapCache {
+    static constexpr int kEntries = 16;
+    MapKey key[kEntries];
+    CUtensorMap map[kEntries];
+    bool valid[kEntries] = {};
+    int next = 0;
+};
+thread_local MapCache t_maps;
+
+bool cached_tile_map(CUtensorMap* map, const void* base, int64_t B, int64_t H, int64_t N,
+                     int64_t D, const Strides& st) {
+    const MapKey key{base, B, H, N, D, st.n, st.h, st.b};
+    for (int i = 0; i < MapCache::kEntries; ++i)
+        if (t_maps.valid[i] && t_maps.key[i] == key) {
+            *map = t_maps.map[i];
+            return true;
+        }
+    if (!make_tile_map(map, base, B, H, N, D, st)) return false;
+    const int slot = t_maps.next;
+    t_maps.next = (slot + 1) % MapCache::kEntries;
+    t_maps.key[slot] = key;
+    t_maps.map[slot] = *map;
+    t_maps.valid[slot] = true;
+    return true;
+}
+
 // Per-device one-time set-up: architecture check, SM count, status-word address, smem opt-in.
 constexpr int kMaxDevices = 64;
 struct DeviceState {
@@ -228,10 +264,10 @@ int prepare(const Problem& P, DeviceState** ds, CUtensorMap* mq, CUtensorMap* mk
     for (const void* ptr :
          {P.q, P.k, P.v, static_cast<const void*>(P.out), static_cast<const void*>(P.lse)})
         if (check_memory(ptr, dev) != ATTN_OK) return ATTN_ERR_MEMORY;
-    if (!make_tile_map(mq, P.q, P.B, P.Hq, P.N, P.D, P.sq) ||
-        !make_tile_map(mk, P.k, P.B, P.Hkv, P.N, P.D, P.sk) ||
-        !make_tile_map(mv, P.v, P.B, P.Hkv, P.N, P.D, P.sv) ||
-        !make_tile_map(mo, P.out, P.B, P.Hq, P.N, P.D, P.so))
+    if (!cached_tile_map(mq, P.q, P.B, P.Hq, P.N, P.D, P.sq) ||
+        !cached_tile_map(mk, P.k, P.B, P.Hkv, P.N, P.D, P.sk) ||
+        !cached_tile_map(mv, P.v, P.B, P.Hkv, P.N, P.D, P.sv) ||
+        !cached_tile_map(mo, P.out, P.B, P.Hq, P.N, P.D, P.so))
         return cuda_fail(cudaErrorInvalidValue);
     prm->B = P.B;
     prm->Hq = P.Hq;
