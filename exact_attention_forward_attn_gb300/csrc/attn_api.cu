@@ -213,7 +213,7 @@ int validate(Problem& P, bool* empty) {
     *empty = false;
     if (P.B < 0 || P.N < 0 || P.Hq <= 0 || P.Hkv <= 0) return ATTN_ERR_SHAPE;
     if (P.Hq % P.Hkv != 0) return ATTN_ERR_HEADS;
-    if (P.D != 64 && P.D != 128) return ATTN_ERR_HEADDIM;
+    if (P.D % 8 != 0 || P.D < 8 || P.D > 128) return ATTN_ERR_HEADDIM;
     if (!std::isfinite(P.sm_scale) || !(P.sm_scale > 0.f)) return ATTN_ERR_SCALE;
     if (P.B == 0 || P.N == 0) {  // empty problem: nothing to read or write
         *empty = true;
@@ -298,11 +298,11 @@ int launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
 }
 
 template <int D>
-int launch_merge(const AttnParams& p, __nv_bfloat16* out, cudaStream_t stream) {
+int launch_merge(const AttnParams& p, __nv_bfloat16* out, int d_out, cudaStream_t stream) {
     const int64_t rows = static_cast<int64_t>(p.B) * p.Hq * p.N;
     const int64_t blocks = (rows + kMergeThreads / 32 - 1) / (kMergeThreads / 32);
     attn_splitkv_merge_kernel<D><<<static_cast<unsigned int>(blocks), kMergeThreads, 0, stream>>>(
-        p.ws_o, p.ws_lse, out, p.lse, p.B * p.Hq, p.N, p.n_tiles, p.causal, p.n_splits,
+        p.ws_o, p.ws_lse, out, p.lse, p.B * p.Hq, p.N, d_out, p.n_tiles, p.causal, p.n_splits,
         p.split_tiles);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
@@ -329,8 +329,12 @@ int heuristic_splits(int64_t items, int64_t n_tiles, int num_sms) {
     return s < 1 ? 1 : static_cast<int>(s);
 }
 
+// The kernels compute on D padded to 64 or 128 columns (the TMA zero-fills the rest), so the
+// fp32 partials are D_pad wide.
+int64_t padded_dim(int64_t D) { return D <= 64 ? 64 : 128; }
+
 int64_t workspace_bytes_for(int64_t bh, int64_t N, int64_t D, int n_splits) {
-    return static_cast<int64_t>(n_splits) * bh * N * (D + 1) * 4;
+    return static_cast<int64_t>(n_splits) * bh * N * (padded_dim(D) + 1) * 4;
 }
 
 }  // namespace
@@ -347,7 +351,7 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* out, 
     st = prepare(P, &ds, &mq, &mk, &mv, &mo, &prm);
     if (st != ATTN_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return D == 64 ? launch_fwd<64, false>(mq, mk, mv, mo, prm, ds->status_word, P.items, s)
+    return D <= 64 ? launch_fwd<64, false>(mq, mk, mv, mo, prm, ds->status_word, P.items, s)
                    : launch_fwd<128, false>(mq, mk, mv, mo, prm, ds->status_word, P.items, s);
 }
 
@@ -373,7 +377,7 @@ extern "C" int attn_fwd_strided(const void* q, const void* k, const void* v, voi
     st = prepare(P, &ds, &mq, &mk, &mv, &mo, &prm);
     if (st != ATTN_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return D == 64 ? launch_fwd<64, false>(mq, mk, mv, mo, prm, ds->status_word, P.items, s)
+    return D <= 64 ? launch_fwd<64, false>(mq, mk, mv, mo, prm, ds->status_word, P.items, s)
                    : launch_fwd<128, false>(mq, mk, mv, mo, prm, ds->status_word, P.items, s);
 }
 
@@ -392,7 +396,7 @@ extern "C" int attn_fwd_test_stall(const void* q, const void* k, const void* v, 
     if (st != ATTN_OK) return st;
     prm.stall_item = stall_item;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return D == 64 ? launch_fwd<64, false>(mq, mk, mv, mo, prm, ds->status_word, P.items, s)
+    return D <= 64 ? launch_fwd<64, false>(mq, mk, mv, mo, prm, ds->status_word, P.items, s)
                    : launch_fwd<128, false>(mq, mk, mv, mo, prm, ds->status_word, P.items, s);
 }
 
@@ -410,7 +414,7 @@ extern "C" int attn_fwd_splitkv_num_splits(int B, int Hq, int N, int D, int caus
 }
 
 extern "C" size_t attn_fwd_splitkv_workspace_bytes(int B, int Hq, int N, int D, int num_splits) {
-    if (B <= 0 || Hq <= 0 || N <= 0 || (D != 64 && D != 128)) return 0;
+    if (B <= 0 || Hq <= 0 || N <= 0 || D % 8 != 0 || D < 8 || D > 128) return 0;
     if (num_splits == 0) num_splits = attn_fwd_splitkv_num_splits(B, Hq, N, D, 0);
     const int64_t n_tiles = (static_cast<int64_t>(N) + kBM - 1) / kBM;
     int tps = 0, n = 0;
@@ -455,14 +459,14 @@ extern "C" int attn_fwd_splitkv(const void* q, const void* k, const void* v, voi
     prm.n_splits = n_splits;
     prm.split_tiles = split_tiles;
     prm.ws_o = static_cast<float*>(workspace);
-    prm.ws_lse = prm.ws_o + static_cast<int64_t>(n_splits) * P.bh * N * D;
+    prm.ws_lse = prm.ws_o + static_cast<int64_t>(n_splits) * P.bh * N * padded_dim(D);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int64_t grid = P.items * n_splits;
-    st = D == 64 ? launch_fwd<64, true>(mq, mk, mv, mo, prm, ds->status_word, grid, s)
+    st = D <= 64 ? launch_fwd<64, true>(mq, mk, mv, mo, prm, ds->status_word, grid, s)
                  : launch_fwd<128, true>(mq, mk, mv, mo, prm, ds->status_word, grid, s);
     if (st != ATTN_OK) return st;
     auto* o = static_cast<__nv_bfloat16*>(out);
-    return D == 64 ? launch_merge<64>(prm, o, s) : launch_merge<128>(prm, o, s);
+    return D <= 64 ? launch_merge<64>(prm, o, D, s) : launch_merge<128>(prm, o, D, s);
 }
 
 extern "C" const char* attn_status_string(int status) {
@@ -471,7 +475,7 @@ extern "C" const char* attn_status_string(int status) {
         case ATTN_ERR_NULL: return "a required pointer is NULL";
         case ATTN_ERR_SHAPE: return "invalid or overflowing shape (B, Hq, Hkv, N)";
         case ATTN_ERR_HEADS: return "Hq is not a multiple of Hkv";
-        case ATTN_ERR_HEADDIM: return "unsupported head dimension (D must be 64 or 128)";
+        case ATTN_ERR_HEADDIM: return "unsupported head dimension (D must be a multiple of 8 in [8, 128])";
         case ATTN_ERR_ALIGN: return "a pointer is not 16-byte aligned";
         case ATTN_ERR_SCALE: return "sm_scale must be finite and positive";
         case ATTN_ERR_ARCH: return "the current device is not sm_103 (GB300)";

@@ -510,11 +510,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 // before its last visible key tile) are combined as
 //   LSE = M + ln sum_s exp(LSE_s - M),  M = max_s LSE_s,   O = sum_s exp(LSE_s - LSE) * O_s.
 // One warp per row; lane k owns D/32 consecutive columns (coalesced 16-byte loads per split).
+// D is the padded width of the partials; only the first d_out columns of each row go to `out`.
 template <int D>
 __global__ void __launch_bounds__(256)
     attn_splitkv_merge_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_lse,
                               __nv_bfloat16* __restrict__ out, float* __restrict__ lse, int BH,
-                              int N, int n_tiles, int causal, int n_splits, int split_tiles) {
+                              int N, int d_out, int n_tiles, int causal, int n_splits,
+                              int split_tiles) {
     constexpr int kCols = D / 32;
     const int lane = threadIdx.x & 31;
     const long long row = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
@@ -542,14 +544,21 @@ __global__ void __launch_bounds__(256)
         }
     }
     const float inv = 1.0f / wsum;
-    __nv_bfloat16* o = out + row * D + lane * kCols;
-    if constexpr (kCols == 4) {
-        uint2 packed;
-        packed.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-        packed.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-        *reinterpret_cast<uint2*>(o) = packed;
-    } else {
-        *reinterpret_cast<uint32_t*>(o) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    const int c0 = lane * kCols;
+    __nv_bfloat16* o = out + row * d_out + c0;
+    if (d_out == D) {  // full width: one 8-byte (D=128) or 4-byte (D=64) store per lane
+        if constexpr (kCols == 4) {
+            uint2 packed;
+            packed.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+            packed.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+            *reinterpret_cast<uint2*>(o) = packed;
+        } else {
+            *reinterpret_cast<uint32_t*>(o) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        }
+    } else {  // padded head dimension: the columns at and beyond d_out are not part of O
+#pragma unroll
+        for (int c = 0; c < kCols; ++c)
+            if (c0 + c < d_out) o[c] = __float2bfloat16_rn(acc[c] * inv);
     }
     if (lane == 0) lse[row] = mx + logf(wsum);
 }

@@ -41,7 +41,7 @@ typedef enum {
     ATTN_ERR_NULL = -1,     /* a required pointer is NULL */
     ATTN_ERR_SHAPE = -2,    /* B, Hq, Hkv or N negative, Hq or Hkv zero, or sizes overflow */
     ATTN_ERR_HEADS = -3,    /* Hq is not a multiple of Hkv */
-    ATTN_ERR_HEADDIM = -4,  /* D is not 64 or 128 */
+    ATTN_ERR_HEADDIM = -4,  /* D is not a multiple of 8 in [8, 128] */
     ATTN_ERR_ALIGN = -5,    /* a tensor pointer is not 16-byte aligned */
     ATTN_ERR_SCALE = -6,    /* sm_scale is not finite and positive */
     ATTN_ERR_ARCH = -7,     /* the current device is not compute capability 10.3 (sm_103) */
@@ -64,7 +64,9 @@ typedef enum {
  *   out      bf16 [B, Hq,  N, D], contiguous; written (round-to-nearest-even); must not overlap
  *            q, k, v or lse
  *   lse      fp32 [B, Hq, N]; written with the natural-log LSE of the scaled, masked scores
- *   B, Hq, Hkv, N, D   sizes; Hq % Hkv == 0 (MQA is Hkv == 1); D in {64, 128}; B == 0 or N == 0
+ *   B, Hq, Hkv, N, D   sizes; Hq % Hkv == 0 (MQA is Hkv == 1); D a multiple of 8 in [8, 128]
+ *            (computed on D padded to 64 or 128 with zeros, as "Triton-CUDA Attention" pads D to a
+ *            power of two; the padding is never read from or written to memory); B == 0 or N == 0
  *            is a valid empty problem (returns ATTN_OK, launches nothing; the pointers may then
  *            be NULL, as zero-size allocations often are)
  *   causal   0: every key visible; nonzero: key j visible to query i iff j <= i

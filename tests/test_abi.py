@@ -70,7 +70,7 @@ def _call(lib, q=P, k=P * 2, v=P * 3, out=P * 4, lse=P * 5, B=1, Hq=2, Hkv=1, N=
     (dict(q=0), -1), (dict(out=0), -1), (dict(lse=0), -1),
     (dict(B=-1), -2), (dict(N=-5), -2), (dict(Hq=0), -2), (dict(Hkv=0), -2),
     (dict(Hq=6, Hkv=4), -3),
-    (dict(D=96), -4), (dict(D=256), -4), (dict(D=0), -4),
+    (dict(D=100), -4), (dict(D=256), -4), (dict(D=0), -4), (dict(D=136), -4), (dict(D=4), -4),
     (dict(scale=0.0), -6), (dict(scale=-1.0), -6), (dict(scale=float("inf")), -6),
     (dict(scale=float("nan")), -6),
     (dict(q=P + 8), -5), (dict(lse=P * 5 + 4), -5),
@@ -112,14 +112,17 @@ def test_splitkv_workspace_bytes(lib):
     assert lib.attn_fwd_splitkv_workspace_bytes(1, 32, 512, 128, 3) == 2 * 32 * 512 * 129 * 4
     assert lib.attn_fwd_splitkv_workspace_bytes(1, 32, 512, 128, 1) == 0
     assert lib.attn_fwd_splitkv_workspace_bytes(1, 2, 100, 64, 8) == 0  # one key tile
-    assert lib.attn_fwd_splitkv_workspace_bytes(1, 2, 128, 96, 2) == 0  # bad D
+    assert lib.attn_fwd_splitkv_workspace_bytes(1, 2, 128, 100, 2) == 0  # bad D
+    # padded head dims: partials are 64 or 128 wide
+    assert lib.attn_fwd_splitkv_workspace_bytes(1, 32, 512, 96, 2) == 2 * 32 * 512 * 129 * 4
+    assert lib.attn_fwd_splitkv_workspace_bytes(1, 32, 512, 32, 2) == 2 * 32 * 512 * 65 * 4
 
 
 @pytest.mark.parametrize("kw,status", [
     (dict(splits=-1), -12), (dict(splits=65), -12),
     (dict(ws=0), -1), (dict(ws=S * 8 + 4), -5), (dict(ws_bytes=1000), -13),
     (dict(ws=S), -11),  # workspace overlaps q
-    (dict(Hq=3, Hkv=2), -3), (dict(D=32), -4),
+    (dict(Hq=3, Hkv=2), -3), (dict(D=36), -4),
 ])
 def test_splitkv_host_validation(lib, kw, status):
     assert _split(lib, **kw) == status

@@ -91,6 +91,10 @@ RAGGED = [
     (1, 4, 1, 200, 128, True), (1, 2, 1, 255, 64, True), (1, 2, 2, 256, 128, False),
     (3, 6, 2, 300, 128, True), (1, 8, 2, 383, 64, False), (1, 8, 2, 383, 128, True),
     (2, 2, 1, 384, 128, True), (1, 16, 4, 640, 128, False), (1, 16, 4, 700, 64, True),
+    # head dims other than 64/128: computed on 64 or 128 columns zero-filled by the TMA
+    (1, 4, 2, 200, 96, True), (1, 2, 1, 130, 32, False), (2, 4, 4, 256, 48, True),
+    (1, 8, 2, 300, 80, False), (1, 2, 1, 128, 16, True), (1, 4, 1, 384, 112, True),
+    (1, 2, 2, 129, 8, False),
 ]
 
 

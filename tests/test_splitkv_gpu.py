@@ -28,7 +28,9 @@ CASES = [(wl.MHA, 2), (wl.MHA, 4), (wl.MHA_OUTLIER, 3), (wl.MQA, 4), (wl.TINY_NO
          (wl.random_case(2, 4, 2, 700, 128, True, 11), 3),
          (wl.random_case(1, 6, 3, 383, 64, False, 12), 2),
          (wl.random_case(1, 4, 1, 1000, 128, True, 13), 16),
-         (wl.random_case(3, 2, 2, 129, 64, True, 14), 2)]
+         (wl.random_case(3, 2, 2, 129, 64, True, 14), 2),
+         (wl.random_case(1, 4, 2, 1000, 96, True, 15), 4),
+         (wl.random_case(2, 2, 1, 600, 40, False, 16), 3)]
 
 
 @pytest.mark.parametrize("w,splits", CASES, ids=[f"{w.name}-s{s}" for w, s in CASES])

@@ -30,6 +30,7 @@ CASES = [
     ("bnhd", wl.random_case(1, 4, 4, 256, 64, False, 32)),
     ("padded", wl.random_case(1, 4, 1, 200, 128, False, 33)),
     ("mixed", wl.random_case(2, 6, 3, 129, 128, True, 34)),
+    ("bnhd", wl.random_case(1, 4, 2, 250, 96, True, 36)),
 ]
 
 
