@@ -15,6 +15,8 @@ skillmd.com, GQA and causal variants; "Flash Attention 与 Kernel 优化", fangp
     s_j  = sm_scale * <Q[b,hq,i,:], K[b,h_kv,j,:]>
     O    = sum_j exp(s_j - m) V[b,h_kv,j,:] / sum_j exp(s_j - m),   m = max_j s_j
     LSE  = m + ln sum_j exp(s_j - m)
+
+``attn_bwd_ref`` gives the gradients of the same definition (the pages' backward by recompute).
 """
 from __future__ import annotations
 
@@ -65,6 +67,10 @@ def _load():
                                                   c_int, c_int, ctypes.c_double, f64p, f64p, f64p,
                                                   c_int]
             lib.oracle_attn_probs_f64.restype = c_int
+            lib.oracle_attn_bwd_f64.argtypes = [u16p, u16p, u16p, u16p, c_int, c_int, c_int,
+                                                c_int, c_int, c_int, ctypes.c_double, f64p, f64p,
+                                                f64p, c_int]
+            lib.oracle_attn_bwd_f64.restype = c_int
             lib.oracle_default_threads.argtypes = []
             lib.oracle_default_threads.restype = c_int
             _lib = lib
@@ -149,3 +155,25 @@ def attn_probs(q, k, v, causal: bool, sm_scale: float, n_threads: int = 0):
     if st != 0:
         raise ValueError(f"oracle_attn_probs_f64 rejected its arguments (status {st})")
     return out, lse, probs
+
+
+def attn_bwd_ref(q, k, v, dout, causal: bool, sm_scale: float, n_threads: int = 0):
+    """Oracle gradients (dq [B,Hq,N,D], dk, dv [B,Hkv,N,D], float64) of the forward above for the
+    output gradient ``dout`` [B,Hq,N,D] (bf16).  Scores and probabilities are recomputed from the
+    definition (the pages' backward by recompute), written out densely."""
+    lib = _load()
+    qb, kb, vb, gb = _bf16_bits(q), _bf16_bits(k), _bf16_bits(v), _bf16_bits(dout)
+    B, Hq, Hkv, N, D = _shapes(qb, kb, vb)
+    if gb.shape != qb.shape:
+        raise ValueError("dout must have q's shape")
+    dq = np.zeros((B, Hq, N, D), dtype=np.float64)
+    dk = np.zeros((B, Hkv, N, D), dtype=np.float64)
+    dv = np.zeros((B, Hkv, N, D), dtype=np.float64)
+    st = lib.oracle_attn_bwd_f64(_ptr(qb, ctypes.c_uint16), _ptr(kb, ctypes.c_uint16),
+                                 _ptr(vb, ctypes.c_uint16), _ptr(gb, ctypes.c_uint16), B, Hq, Hkv,
+                                 N, D, int(bool(causal)), float(sm_scale),
+                                 _ptr(dq, ctypes.c_double), _ptr(dk, ctypes.c_double),
+                                 _ptr(dv, ctypes.c_double), int(n_threads))
+    if st != 0:
+        raise ValueError(f"oracle_attn_bwd_f64 rejected its arguments (status {st})")
+    return dq, dk, dv

@@ -225,3 +225,144 @@ int oracle_default_threads(void) {
     long hw = sysconf(_SC_NPROCESSORS_ONLN);
     return hw > 0 ? (int)hw : 1;
 }
+
+/*
+ * Backward of the same definition (test infrastructure as well).
+ *
+ * The pages train through this attention by recomputing the scores and probabilities from the
+ * saved log-sum-exp instead of storing them ("Attention Kernel 实现与正确性验证", section 1.1,
+ * third idea; "Flash Attention 与 Kernel 优化", section on autograd and backward: rebuild
+ * s = qk^T * scale, apply the causal mask, rebuild p = softmax(s), then dv, dp, ds, dq, dk).  The
+ * oracle writes that chain rule out densely, in double precision, per query row i of head
+ * (b, hq) and visible key j of its KV head:
+ *     p_ij  = exp(s_ij - LSE_i)             with s_ij = sm_scale * <q_i, k_j>, LSE from above
+ *     dp_ij = <dO_i, v_j>
+ *     D_i   = sum_j p_ij dp_ij
+ *     ds_ij = p_ij (dp_ij - D_i)
+ *     dQ_i  = sm_scale * sum_j ds_ij k_j
+ *     dK_j  = sm_scale * sum over (hq in the group, i) of ds_ij q_i
+ *     dV_j  = sum over (hq in the group, i) of p_ij dO_i
+ * Inputs are bf16 bit patterns; outputs are doubles: dq [B,Hq,N,D], dk and dv [B,Hkv,N,D].
+ * Threads split the query heads; each thread keeps private dK/dV sums for its heads, and the
+ * per-head sums are added in head order afterwards (the result does not depend on the threads).
+ */
+typedef struct {
+    const uint16_t *q, *k, *v, *dout;
+    int B, Hq, Hkv, N, D, causal;
+    double sm_scale;
+    double *dq;            /* [B*Hq, N, D] */
+    double *dk_h, *dv_h;   /* per query head: [B*Hq, N, D] */
+    int first, last;       /* query heads (b*Hq + hq) of this worker */
+    int status;
+} bjob_t;
+
+static void *bworker(void *arg) {
+    bjob_t *J = (bjob_t *)arg;
+    const int N = J->N, D = J->D;
+    double *s = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+    double *dp = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+    double *qi = (double *)malloc(sizeof(double) * (size_t)D);
+    double *gi = (double *)malloc(sizeof(double) * (size_t)D);
+    J->status = ORACLE_OK;
+    if (!s || !dp || !qi || !gi) { J->status = ORACLE_ERR_NOMEM; goto done; }
+    for (int bh = J->first; bh < J->last; ++bh) {
+        const int b = bh / J->Hq, hq = bh % J->Hq;
+        const int hkv = (int)(((long)hq * J->Hkv) / J->Hq);
+        const uint16_t *kh = J->k + ((long)b * J->Hkv + hkv) * (long)N * D;
+        const uint16_t *vh = J->v + ((long)b * J->Hkv + hkv) * (long)N * D;
+        double *dkh = J->dk_h + (long)bh * N * D, *dvh = J->dv_h + (long)bh * N * D;
+        for (int i = 0; i < N; ++i) {
+            const uint16_t *q_row = J->q + ((long)bh * N + i) * D;
+            const uint16_t *do_row = J->dout + ((long)bh * N + i) * D;
+            const int n_vis = J->causal ? i + 1 : N;
+            for (int d = 0; d < D; ++d) { qi[d] = bf16_to_f64(q_row[d]); gi[d] = bf16_to_f64(do_row[d]); }
+            /* scores and the log-sum-exp (two passes, as in the forward) */
+            double m = -INFINITY;
+            for (int j = 0; j < n_vis; ++j) {
+                double dot = 0.0;
+                for (int d = 0; d < D; ++d) dot += qi[d] * bf16_to_f64(kh[(long)j * D + d]);
+                s[j] = J->sm_scale * dot;
+                if (s[j] > m) m = s[j];
+            }
+            double Z = 0.0;
+            for (int j = 0; j < n_vis; ++j) Z += exp(s[j] - m);
+            const double lse = m + log(Z);
+            /* p, dp and D_i */
+            double Di = 0.0;
+            for (int j = 0; j < n_vis; ++j) {
+                s[j] = exp(s[j] - lse); /* now p_ij */
+                double dot = 0.0;
+                for (int d = 0; d < D; ++d) dot += gi[d] * bf16_to_f64(vh[(long)j * D + d]);
+                dp[j] = dot;
+                Di += s[j] * dp[j];
+            }
+            double *dq_row = J->dq + ((long)bh * N + i) * D;
+            for (int d = 0; d < D; ++d) dq_row[d] = 0.0;
+            for (int j = 0; j < n_vis; ++j) {
+                const double ds = s[j] * (dp[j] - Di);
+                for (int d = 0; d < D; ++d) {
+                    dq_row[d] += J->sm_scale * ds * bf16_to_f64(kh[(long)j * D + d]);
+                    dkh[(long)j * D + d] += J->sm_scale * ds * qi[d];
+                    dvh[(long)j * D + d] += s[j] * gi[d];
+                }
+            }
+        }
+    }
+done:
+    free(s); free(dp); free(qi); free(gi);
+    return NULL;
+}
+
+/*
+ * Gradients of the forward above for an output gradient `dout` [B,Hq,N,D] (bf16 bits).
+ * dq [B,Hq,N,D], dk [B,Hkv,N,D], dv [B,Hkv,N,D] in double.  Returns 0 or a negative code.
+ */
+int oracle_attn_bwd_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                        const uint16_t *dout, int B, int Hq, int Hkv, int N, int D, int causal,
+                        double sm_scale, double *dq, double *dk, double *dv, int n_threads) {
+    if (!q || !k || !v || !dout || !dq || !dk || !dv) return ORACLE_ERR_ARG;
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || N < 0 || D <= 0 || Hq % Hkv != 0) return ORACLE_ERR_ARG;
+    const long heads = (long)B * Hq;
+    const long per_head = (long)N * D;
+    for (long x = 0; x < (long)B * Hkv * per_head; ++x) { dk[x] = 0.0; dv[x] = 0.0; }
+    if (heads == 0 || N == 0) return ORACLE_OK;
+    double *dk_h = (double *)calloc((size_t)(heads * per_head), sizeof(double));
+    double *dv_h = (double *)calloc((size_t)(heads * per_head), sizeof(double));
+    if (!dk_h || !dv_h) { free(dk_h); free(dv_h); return ORACLE_ERR_NOMEM; }
+    if (n_threads <= 0) n_threads = oracle_default_threads();
+    if (n_threads > heads) n_threads = (int)heads;
+    bjob_t *jobs = (bjob_t *)calloc((size_t)n_threads, sizeof(bjob_t));
+    pthread_t *tid = (pthread_t *)calloc((size_t)n_threads, sizeof(pthread_t));
+    char *threaded = (char *)calloc((size_t)n_threads, 1);
+    int status = ORACLE_OK;
+    if (!jobs || !tid || !threaded) { status = ORACLE_ERR_NOMEM; goto out; }
+    for (int t = 0; t < n_threads; ++t) {
+        bjob_t *J = &jobs[t];
+        J->q = q; J->k = k; J->v = v; J->dout = dout;
+        J->B = B; J->Hq = Hq; J->Hkv = Hkv; J->N = N; J->D = D; J->causal = causal ? 1 : 0;
+        J->sm_scale = sm_scale; J->dq = dq; J->dk_h = dk_h; J->dv_h = dv_h;
+        J->first = (int)(heads * t / n_threads);
+        J->last = (int)(heads * (t + 1) / n_threads);
+        if (n_threads > 1 && pthread_create(&tid[t], NULL, bworker, J) == 0)
+            threaded[t] = 1;
+        else
+            bworker(J);
+    }
+    for (int t = 0; t < n_threads; ++t) {
+        if (threaded[t]) pthread_join(tid[t], NULL);
+        if (jobs[t].status != ORACLE_OK) status = jobs[t].status;
+    }
+    /* dK, dV of a KV head: the sum over its query heads, in head order */
+    for (long bh = 0; bh < heads; ++bh) {
+        const long b = bh / Hq, hq = bh % Hq;
+        const long hkv = (hq * Hkv) / Hq;
+        double *dkk = dk + (b * Hkv + hkv) * per_head, *dvv = dv + (b * Hkv + hkv) * per_head;
+        for (long x = 0; x < per_head; ++x) {
+            dkk[x] += dk_h[bh * per_head + x];
+            dvv[x] += dv_h[bh * per_head + x];
+        }
+    }
+out:
+    free(jobs); free(tid); free(threaded); free(dk_h); free(dv_h);
+    return status;
+}
