@@ -152,6 +152,73 @@ def attn_fwd_splitkv(q, k, v, causal: bool = False, sm_scale: float | None = Non
     return out, lse
 
 
+def attn_bwd(q, k, v, out, lse, dout, causal: bool = False, sm_scale: float | None = None,
+             dq=None, dk=None, dv=None, workspace=None):
+    """Gradients (dq, dk, dv) of ``attn_fwd`` by recompute from its ``out`` and ``lse``, for the
+    output gradient ``dout`` (all contiguous CUDA tensors; dq like q, dk/dv like k)."""
+    import torch
+
+    B, Hq, Hkv, N, D = _check_inputs(q, k, v)
+    for name, t, like in (("out", out, q), ("dout", dout, q)):
+        if t.shape != like.shape or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 tensor shaped like q")
+    if lse.shape != (B, Hq, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor [B, Hq, N]")
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    lib = _lib.load()
+    with torch.cuda.device(q.device):
+        need = int(lib.attn_bwd_workspace_bytes(B, Hq, N))
+        if workspace is None:
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+        st = lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                          lse.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                          dv.data_ptr(), B, Hq, Hkv, N, D, int(bool(causal)), float(sm_scale),
+                          workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                          _stream_handle(q.device))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_bwd")
+    return dq, dk, dv
+
+
+def _autograd_function():
+    import torch
+
+    class FlashAttention(torch.autograd.Function):
+        """``FlashAttention.apply(q, k, v, is_causal=False)``: the pages' autograd interface
+        ("Flash Attention 与 Kernel 优化": inputs already projected, [.., N, D] per head), here
+        for q [B,Hq,N,D] and k, v [B,Hkv,N,D]; forward and backward both run the CUDA kernels,
+        and the forward saves q, k, v, O and LSE for the backward's recompute."""
+
+        @staticmethod
+        def forward(ctx, q, k, v, is_causal=False, sm_scale=None):
+            q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+            out, lse = attn_fwd(q, k, v, causal=is_causal, sm_scale=sm_scale)
+            ctx.save_for_backward(q, k, v, out, lse)
+            ctx.is_causal, ctx.sm_scale = is_causal, sm_scale
+            return out
+
+        @staticmethod
+        def backward(ctx, dout):
+            q, k, v, out, lse = ctx.saved_tensors
+            dq, dk, dv = attn_bwd(q, k, v, out, lse, dout.contiguous(), causal=ctx.is_causal,
+                                  sm_scale=ctx.sm_scale)
+            return dq, dk, dv, None, None
+
+    return FlashAttention
+
+
+def __getattr__(name):
+    if name == "FlashAttention":
+        fn = _autograd_function()
+        globals()["FlashAttention"] = fn
+        return fn
+    raise AttributeError(name)
+
+
 def device_status(device=None) -> int:
     """Synchronise the current stream and return (and clear) the device status word:
     0 if no kernel recorded a failure, else a negative status (e.g. -9 for an expired wait)."""

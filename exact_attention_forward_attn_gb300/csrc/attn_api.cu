@@ -16,6 +16,7 @@
 #include <mutex>
 
 #include "attn.h"
+#include "attn_bwd_kernel.cuh"
 #include "attn_fwd_kernel.cuh"
 
 using namespace gb300attn;
@@ -134,6 +135,17 @@ cudaError_t opt_in_smem() {
                                 SmemLayout<D>::kAlloc);
 }
 
+template <int D>
+cudaError_t opt_in_bwd_smem() {
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         BwdSmem<D>::kAlloc);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(attn_bwd_dq_kernel<D>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, BwdSmem<D>::kAlloc);
+    return e;
+}
+
 int device_state(int dev, DeviceState** out) {
     if (dev < 0 || dev >= kMaxDevices) return cuda_fail(cudaErrorInvalidDevice);
     DeviceState& st = g_devices[dev];
@@ -151,6 +163,8 @@ int device_state(int dev, DeviceState** out) {
         if (e == cudaSuccess) e = opt_in_smem<128, false>();
         if (e == cudaSuccess) e = opt_in_smem<64, true>();
         if (e == cudaSuccess) e = opt_in_smem<128, true>();
+        if (e == cudaSuccess) e = opt_in_bwd_smem<64>();
+        if (e == cudaSuccess) e = opt_in_bwd_smem<128>();
         if (e != cudaSuccess) { st.status = ATTN_ERR_CUDA; st.cuda_error = e; }
     });
     if (st.status == ATTN_ERR_CUDA) t_last_cuda_error = st.cuda_error;
@@ -257,7 +271,10 @@ int validate(Problem& P, bool* empty) {
 int prepare(const Problem& P, DeviceState** ds, CUtensorMap* mq, CUtensorMap* mk, CUtensorMap* mv,
             CUtensorMap* mo, AttnParams* prm) {
     int dev = 0;
-    const cudaError_t e = cudaGetDevice(&dev);
+    cudaError_t e = cudaGetDevice(&dev);
+    // A host thread that has not used CUDA yet (e.g. an autograd worker) has no current context,
+    // and the driver's tensor-map encoder needs one: bind the current device's primary context.
+    if (e == cudaSuccess) e = cudaSetDevice(dev);
     if (e != cudaSuccess) return cuda_fail(e);
     const int st = device_state(dev, ds);
     if (st != ATTN_OK) return st;
@@ -467,6 +484,106 @@ extern "C" int attn_fwd_splitkv(const void* q, const void* k, const void* v, voi
     if (st != ATTN_OK) return st;
     auto* o = static_cast<__nv_bfloat16*>(out);
     return D <= 64 ? launch_merge<64>(prm, o, D, s) : launch_merge<128>(prm, o, D, s);
+}
+
+// ------------------------------------------------------------------------------------------------
+// Backward
+// ------------------------------------------------------------------------------------------------
+namespace {
+
+template <int D>
+int launch_bwd(const Problem& P, const CUtensorMap& mq, const CUtensorMap& mk,
+               const CUtensorMap& mv, const CUtensorMap& mdo, const CUtensorMap& mdq,
+               const CUtensorMap& mdk, const CUtensorMap& mdv, const BwdParams& bp,
+               const void* out, const void* dout, float* delta, unsigned int* status_word,
+               cudaStream_t s) {
+    const long long rows = P.bh * P.N;
+    attn_bwd_delta_kernel<<<static_cast<unsigned int>((rows + 7) / 8), 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), delta,
+        rows, P.D);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    attn_bwd_dkdv_kernel<D><<<static_cast<unsigned int>(P.n_tiles * P.bh_kv), kBwdThreads,
+                              BwdSmem<D>::kAlloc, s>>>(mq, mk, mv, mdo, mdk, mdv, bp, status_word);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    attn_bwd_dq_kernel<D><<<static_cast<unsigned int>(P.n_tiles * P.bh), kBwdThreads,
+                            BwdSmem<D>::kAlloc, s>>>(mq, mk, mv, mdo, mdq, bp, status_word);
+    e = cudaGetLastError();
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+extern "C" size_t attn_bwd_workspace_bytes(int B, int Hq, int N) {
+    if (B <= 0 || Hq <= 0 || N <= 0) return 0;
+    return static_cast<size_t>(B) * Hq * N * 4;
+}
+
+extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                        const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                        int Hq, int Hkv, int N, int D, int causal, float sm_scale,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+    // the forward's checks cover q, k, v, out (here an input) and lse
+    Problem P{q, k, v, const_cast<void*>(out), const_cast<float*>(lse), B, Hq, Hkv, N, D, causal,
+              sm_scale};
+    bool empty = false;
+    int st = validate(P, &empty);
+    if (st != ATTN_OK || empty) return st;
+    if (!dout || !dq || !dk || !dv || !workspace) return ATTN_ERR_NULL;
+    const uintptr_t align_bits =
+        reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(dq) |
+        reinterpret_cast<uintptr_t>(dk) | reinterpret_cast<uintptr_t>(dv) |
+        reinterpret_cast<uintptr_t>(workspace);
+    if (align_bits & 15u) return ATTN_ERR_ALIGN;
+    const int64_t ws_need = P.bh * N * 4;
+    if (static_cast<int64_t>(workspace_bytes) < ws_need) return ATTN_ERR_WORKSPACE;
+    // outputs (dq, dk, dv, workspace) must not overlap any input or each other
+    const void* ins[] = {q, k, v, out, lse, dout};
+    const int64_t in_bytes[] = {P.q_bytes, P.kv_bytes, P.kv_bytes, P.q_bytes, P.lse_bytes,
+                                P.q_bytes};
+    const void* outs[] = {dq, dk, dv, workspace};
+    const int64_t out_bytes[] = {P.q_bytes, P.kv_bytes, P.kv_bytes, ws_need};
+    for (int a = 0; a < 4; ++a) {
+        for (int x = 0; x < 6; ++x)
+            if (overlaps(outs[a], out_bytes[a], ins[x], in_bytes[x])) return ATTN_ERR_ALIAS;
+        for (int c = a + 1; c < 4; ++c)
+            if (overlaps(outs[a], out_bytes[a], outs[c], out_bytes[c])) return ATTN_ERR_ALIAS;
+    }
+    DeviceState* ds = nullptr;
+    CUtensorMap mq, mk, mv, mo_unused;
+    AttnParams prm;
+    st = prepare(P, &ds, &mq, &mk, &mv, &mo_unused, &prm);
+    if (st != ATTN_OK) return st;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+    for (const void* ptr : {dout, static_cast<const void*>(dq), static_cast<const void*>(dk),
+                            static_cast<const void*>(dv), static_cast<const void*>(workspace)})
+        if (check_memory(ptr, dev) != ATTN_OK) return ATTN_ERR_MEMORY;
+    CUtensorMap mdo, mdq, mdk, mdv;
+    if (!cached_tile_map(&mdo, dout, B, Hq, N, D, P.sq) ||
+        !cached_tile_map(&mdq, dq, B, Hq, N, D, P.sq) ||
+        !cached_tile_map(&mdk, dk, B, Hkv, N, D, P.sk) ||
+        !cached_tile_map(&mdv, dv, B, Hkv, N, D, P.sv))
+        return cuda_fail(cudaErrorInvalidValue);
+    BwdParams bp;
+    bp.B = B;
+    bp.Hq = Hq;
+    bp.Hkv = Hkv;
+    bp.N = N;
+    bp.group = Hq / Hkv;
+    bp.causal = causal ? 1 : 0;
+    bp.n_tiles = static_cast<int>(P.n_tiles);
+    bp.scale_log2 = sm_scale * 1.4426950408889634f;
+    bp.sm_scale = sm_scale;
+    bp.lse = lse;
+    bp.delta = static_cast<const float*>(workspace);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    float* delta = static_cast<float*>(workspace);
+    return D <= 64 ? launch_bwd<64>(P, mq, mk, mv, mdo, mdq, mdk, mdv, bp, out, dout, delta,
+                                    ds->status_word, s)
+                   : launch_bwd<128>(P, mq, mk, mv, mdo, mdq, mdk, mdv, bp, out, dout, delta,
+                                     ds->status_word, s);
 }
 
 extern "C" const char* attn_status_string(int status) {

@@ -1,0 +1,556 @@
+// attn_bwd_kernel.cuh - backward of the exact-attention forward for sm_103a (tcgen05 + TMA).
+//
+// The gradients are recomputed from the saved log-sum-exp instead of a stored probability matrix
+// ("Attention Kernel 实现与正确性验证", walkerchi.com, section 1.1, third idea; "Flash Attention 与
+// Kernel 优化", fangpin.github.io, autograd and backward: rebuild s, the causal mask and p, then
+// dv, dp, ds, dq, dk).  For query row i of head (b, hq) and visible key j of its KV head:
+//   p_ij  = exp(sm_scale q_i.k_j - LSE_i)      dp_ij = dO_i.v_j      Delta_i = dO_i.O_i
+//   ds_ij = p_ij (dp_ij - Delta_i)
+//   dQ_i  = sm_scale sum_j ds_ij k_j,  dK_j = sm_scale sum_(hq,i) ds_ij q_i,  dV_j = sum_(hq,i) p_ij dO_i
+// (Delta_i = sum_j p_ij dp_ij = dO_i . O_i; the kernels use the second form with the stored O.)
+//
+// Three kernels:
+//   attn_bwd_delta_kernel   Delta = rowsum(dO * O), one warp per row.
+//   attn_bwd_dkdv_kernel    one CTA per (b, KV head, 128-key tile j): K_j, V_j stay in smem; for
+//                           every query head of the group and every query tile i (i >= j under
+//                           the causal mask) it forms S^T = K_j Q_i^T and dP^T = V_j dO_i^T,
+//                           P^T and dS^T (bf16, in TMEM over S^T / dP^T), and accumulates
+//                           dV += P^T dO_i and dK += dS^T Q_i in TMEM.
+//   attn_bwd_dq_kernel      one CTA per (b, query head, 128-row tile i): S = Q_i K_j^T,
+//                           dP = dO_i V_j^T, dS (bf16 in TMEM over S), dQ += dS K_j.
+// Zero-filled rows past N contribute nothing: a padded query has dO = 0 and Delta = 0 (so its
+// ds and its dV term vanish), a padded key has K = V = 0 (so its dQ term vanishes) and its own
+// dK/dV rows are never stored.  Only the causal diagonal tile needs a mask.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "attn_fwd_kernel.cuh"
+#include "ptx.cuh"
+
+namespace gb300attn {
+
+struct BwdParams {
+    int B, Hq, Hkv, N;
+    int group;         // Hq / Hkv
+    int causal;
+    int n_tiles;       // ceil(N / 128)
+    float scale_log2;  // sm_scale * log2(e)
+    float sm_scale;
+    const float* lse;    // [B, Hq, N] natural-log LSE from the forward
+    const float* delta;  // [B, Hq, N] dO . O
+};
+
+constexpr int kBwdThreads = 192;  // warps 0-3 elementwise, 4 MMA issuer, 5 TMA producer
+constexpr int kBwdMmaWarp = 4;
+constexpr int kBwdLoadWarp = 5;
+constexpr int kBwdStages = 2;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Delta_i = dO_i . O_i (fp32 sum of bf16 products); one warp per row, D <= 128 columns.
+__global__ void __launch_bounds__(256)
+    attn_bwd_delta_kernel(const __nv_bfloat16* __restrict__ out,
+                          const __nv_bfloat16* __restrict__ dout, float* __restrict__ delta,
+                          long long rows, int D) {
+    const int lane = threadIdx.x & 31;
+    const long long row = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    const __nv_bfloat16* o = out + row * D;
+    const __nv_bfloat16* g = dout + row * D;
+    float acc = 0.f;
+    for (int d = lane; d < D; d += 32) acc += __bfloat162float(o[d]) * __bfloat162float(g[d]);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) delta[row] = acc;
+}
+
+template <int D>
+struct BwdSmem {
+    static constexpr int kPanelBytes = 128 * 64 * 2;
+    static constexpr int kTileBytes = 128 * D * 2;
+    // resident pair (dkdv: K_j, V_j; dq: Q_i, dO_i), then kBwdStages streamed pairs
+    static constexpr int kRes0 = 0;
+    static constexpr int kRes1 = kTileBytes;
+    static constexpr int kStage = 2 * kTileBytes;  // stage s: [kStage + 2*s*tile, +2 tiles)
+    static constexpr int kVec = kStage + 2 * kBwdStages * kTileBytes;  // lse2/delta [stage][2][128]
+    static constexpr int kBars = kVec + kBwdStages * 2 * 128 * 4;
+    // barriers: res_full, stage_full[S], stage_empty[S], s_full, dp_full, p_ready, ds_ready, done
+    static constexpr int kBarRes = 0;
+    static constexpr int kBarFull = 1;
+    static constexpr int kBarEmpty = kBarFull + kBwdStages;
+    static constexpr int kBarS = kBarEmpty + kBwdStages;
+    static constexpr int kBarDP = kBarS + 1;
+    static constexpr int kBarP = kBarDP + 1;
+    static constexpr int kBarDS = kBarP + 1;
+    static constexpr int kBarDone = kBarDS + 1;
+    static constexpr int kNumBars = kBarDone + 1;
+    static constexpr int kTmemSlot = kBars + kNumBars * 8;
+    static constexpr int kAbort = kTmemSlot + 8;
+    static constexpr int kBytes = kAbort + 8;
+    static constexpr int kAlloc = kBytes + 1024;
+};
+
+// Stage a 128 x D fp32 accumulator row (this thread's TMEM lane) as bf16 into a 128B-swizzled
+// panel pair at `stage` (the layout the 4-D TMA store expects).
+template <int D>
+__device__ __forceinline__ void stage_rows_bf16(uint32_t stage, uint32_t taddr, int row,
+                                                float mul) {
+#pragma unroll
+    for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t r[32];
+        tmem_ld32(taddr + cc * 32, r);
+        tmem_wait_ld();
+        const int panel = cc >> 1;
+#pragma unroll
+        for (int c16 = 0; c16 < 4; ++c16) {
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                w[i] = pack_bf16x2(__uint_as_float(r[c16 * 8 + 2 * i]) * mul,
+                                   __uint_as_float(r[c16 * 8 + 2 * i + 1]) * mul);
+            const int chunk = (cc & 1) * 4 + c16;
+            st_shared_v4(stage + panel * (128 * 128) + row * 128 + ((chunk ^ (row & 7)) << 4),
+                         w[0], w[1], w[2], w[3]);
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------------------------
+// dK, dV
+// ------------------------------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                         const __grid_constant__ CUtensorMap tmap_k,
+                         const __grid_constant__ CUtensorMap tmap_v,
+                         const __grid_constant__ CUtensorMap tmap_do,
+                         const __grid_constant__ CUtensorMap tmap_dk,
+                         const __grid_constant__ CUtensorMap tmap_dv, const BwdParams p,
+                         unsigned int* status_word) {
+    using L = BwdSmem<D>;
+    constexpr int kPanels = D / 64;
+    constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, 0);  // K-major x K-major
+    constexpr uint32_t kIdescAcc = idesc_bf16_f32(128, D, 1);  // TMEM x MN-major
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_addr(smem);
+    auto bar = [=](int i) -> uint32_t { return sbase + L::kBars + 8u * i; };
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // work: key tile j (smallest, i.e. heaviest under the causal mask, first), then (b, h_kv)
+    const int bkv_count = p.B * p.Hkv;
+    const int j = static_cast<int>(blockIdx.x / bkv_count);
+    const int bh_kv = static_cast<int>(blockIdx.x % bkv_count);
+    const int b = bh_kv / p.Hkv, hkv = bh_kv % p.Hkv;
+    const int i_first = p.causal ? j : 0;
+    const int per_head = p.n_tiles - i_first;     // query tiles per query head
+    const int n_it = per_head * p.group;          // iterations: (head in group, query tile)
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(L::kBarRes), 1);
+        for (int s = 0; s < kBwdStages; ++s) {
+            mbar_init(bar(L::kBarFull + s), 32);  // 1 expect_tx arrive + 31 vector arrives
+            mbar_init(bar(L::kBarEmpty + s), 1);
+        }
+        mbar_init(bar(L::kBarS), 1);
+        mbar_init(bar(L::kBarDP), 1);
+        mbar_init(bar(L::kBarP), 128);
+        mbar_init(bar(L::kBarDS), 128);
+        mbar_init(bar(L::kBarDone), 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == kBwdMmaWarp) {
+        tmem_alloc(smem_addr(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t t_s = tmem, t_dp = tmem + 128, t_dv = tmem + 256, t_dk = tmem + 384;
+    auto it_head = [=](int it) { return hkv * p.group + it / per_head; };
+    auto it_tile = [=](int it) { return i_first + it % per_head; };
+
+    if (warp == kBwdLoadWarp) {
+        // ---------------- producer (warp-uniform loop; lane 0 issues the TMA) ------------------
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar(L::kBarRes), 2 * L::kTileBytes);
+            for (int h = 0; h < kPanels; ++h) {
+                tma_load_4d(sbase + L::kRes0 + h * L::kPanelBytes, &tmap_k, bar(L::kBarRes),
+                            h * 64, j * 128, hkv, b);
+                tma_load_4d(sbase + L::kRes1 + h * L::kPanelBytes, &tmap_v, bar(L::kBarRes),
+                            h * 64, j * 128, hkv, b);
+            }
+        }
+        for (int it = 0; it < n_it; ++it) {
+            const int s = it % kBwdStages;
+            const uint32_t ph = (it / kBwdStages) & 1;
+            if (!mbar_wait_warp(bar(L::kBarEmpty + s), ph ^ 1u, abort_flag, status_word)) break;
+            const int hq = it_head(it), i = it_tile(it);
+            const size_t rowbase = (static_cast<size_t>(b) * p.Hq + hq) * p.N;
+            // lse2 = LSE*log2(e) and Delta for the 128 queries of tile i (0 past N: see top)
+            float* vec = reinterpret_cast<float*>(smem + L::kVec) + s * 256;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int q = i * 128 + lane * 4 + e;
+                vec[lane * 4 + e] = q < p.N ? p.lse[rowbase + q] * kLog2e : 0.f;
+                vec[128 + lane * 4 + e] = q < p.N ? p.delta[rowbase + q] : 0.f;
+            }
+            if (lane == 0) {
+                const uint32_t st = sbase + L::kStage + s * 2 * L::kTileBytes;
+                mbar_arrive_expect_tx(bar(L::kBarFull + s), 2 * L::kTileBytes);
+                for (int h = 0; h < kPanels; ++h) {
+                    tma_load_4d(st + h * L::kPanelBytes, &tmap_q, bar(L::kBarFull + s), h * 64,
+                                i * 128, hq, b);
+                    tma_load_4d(st + L::kTileBytes + h * L::kPanelBytes, &tmap_do,
+                                bar(L::kBarFull + s), h * 64, i * 128, hq, b);
+                }
+            } else {
+                mbar_arrive(bar(L::kBarFull + s));
+            }
+        }
+        __syncwarp();
+    } else if (warp == kBwdMmaWarp) {
+        // ---------------- MMA issuer (warp-uniform, elected lane) ------------------------------
+        bool ok = mbar_wait_warp(bar(L::kBarRes), 0, abort_flag, status_word);
+        const uint32_t ka = sbase + L::kRes0, va = sbase + L::kRes1;
+        for (int it = 0; ok && it < n_it; ++it) {
+            const int s = it % kBwdStages;
+            const uint32_t ph = (it / kBwdStages) & 1;
+            ok = mbar_wait_warp(bar(L::kBarFull + s), ph, abort_flag, status_word);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t qa = sbase + L::kStage + s * 2 * L::kTileBytes;
+            const uint32_t da = qa + L::kTileBytes;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {  // S^T = K_j Q_i^T
+                const uint32_t off = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
+                mma_bf16_ss_warp(t_s, smem_desc_sw128(ka + off, 16, 1024),
+                                 smem_desc_sw128(qa + off, 16, 1024), kIdescS, kk > 0);
+            }
+            mma_commit_warp(bar(L::kBarS));
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {  // dP^T = V_j dO_i^T
+                const uint32_t off = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
+                mma_bf16_ss_warp(t_dp, smem_desc_sw128(va + off, 16, 1024),
+                                 smem_desc_sw128(da + off, 16, 1024), kIdescS, kk > 0);
+            }
+            mma_commit_warp(bar(L::kBarDP));
+            ok = mbar_wait_warp(bar(L::kBarP), it & 1, abort_flag, status_word);
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO_i  (K = 128 queries)
+                mma_bf16_ts_warp(t_dv, t_s + kk * 8,
+                                 smem_desc_sw128(da + kk * 2048, L::kPanelBytes, 1024), kIdescAcc,
+                                 (it > 0 || kk > 0) ? 1u : 0u);
+            ok = mbar_wait_warp(bar(L::kBarDS), it & 1, abort_flag, status_word);
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)  // dK += dS^T Q_i
+                mma_bf16_ts_warp(t_dk, t_dp + kk * 8,
+                                 smem_desc_sw128(qa + kk * 2048, L::kPanelBytes, 1024), kIdescAcc,
+                                 (it > 0 || kk > 0) ? 1u : 0u);
+            mma_commit_warp(bar(L::kBarEmpty + s));
+        }
+        if (ok) mma_commit_warp(bar(L::kBarDone));
+        __syncwarp();
+    } else {
+        // ---------------- elementwise warps 0-3: one thread per key row of tile j --------------
+        const int row = warp * 32 + lane;  // key within the tile (TMEM lane)
+        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        const float c = p.scale_log2;
+        bool ok = true;
+        for (int it = 0; it < n_it; ++it) {
+            const int s = it % kBwdStages;
+            const float* vec = reinterpret_cast<const float*>(smem + L::kVec) + s * 256;
+            // the stage's lse2/Delta vectors were stored by the producer lanes before their
+            // arrive on stage_full: wait on it here too, so those stores are visible
+            ok = mbar_wait_warp(bar(L::kBarFull + s), (it / kBwdStages) & 1, abort_flag,
+                                status_word);
+            if (ok) ok = mbar_wait_warp(bar(L::kBarS), it & 1, abort_flag, status_word);
+            if (!ok) break;
+            tc_fence_after();
+            // P^T row: p[q] = exp2(c*s - lse2_q)
+            float pr[128];
+            {
+                uint32_t r[128];
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+                    tmem_ld32(lane_base + t_s + cc * 32,
+                              *reinterpret_cast<uint32_t(*)[32]>(&r[cc * 32]));
+                tmem_wait_ld();
+#pragma unroll
+                for (int q = 0; q < 128; q += 4) {
+                    const float4 l4 = *reinterpret_cast<const float4*>(vec + q);
+                    pr[q] = ex2_approx(fmaf(__uint_as_float(r[q]), c, -l4.x));
+                    pr[q + 1] = ex2_approx(fmaf(__uint_as_float(r[q + 1]), c, -l4.y));
+                    pr[q + 2] = ex2_approx(fmaf(__uint_as_float(r[q + 2]), c, -l4.z));
+                    pr[q + 3] = ex2_approx(fmaf(__uint_as_float(r[q + 3]), c, -l4.w));
+                }
+            }
+            if (p.causal && it_tile(it) == j) {  // diagonal tile: query q sees key `row` iff q >= row
+#pragma unroll
+                for (int q = 0; q < 128; ++q) pr[q] = q < row ? 0.f : pr[q];
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int x = 0; x < 32; ++x) pk[x] = pack_bf16x2(pr[h * 64 + 2 * x], pr[h * 64 + 2 * x + 1]);
+                tmem_st32(lane_base + t_s + h * 32, pk);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(L::kBarP));
+            // dS^T row: ds[q] = p[q] (dp[q] - Delta_q), in 32-column chunks; chunk cc's packed
+            // result lands in dP^T columns already read (16cc .. 16cc+15 < 32cc + 32).
+            ok = mbar_wait_warp(bar(L::kBarDP), it & 1, abort_flag, status_word);
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                uint32_t r[32];
+                tmem_ld32(lane_base + t_dp + cc * 32, r);
+                tmem_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int x = 0; x < 16; ++x) {
+                    const int q = cc * 32 + 2 * x;
+                    const float d0 = pr[q] * (__uint_as_float(r[2 * x]) - vec[128 + q]);
+                    const float d1 = pr[q + 1] * (__uint_as_float(r[2 * x + 1]) - vec[128 + q + 1]);
+                    pk[x] = pack_bf16x2(d0, d1);
+                }
+                tmem_st16(lane_base + t_dp + cc * 16, pk);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(L::kBarDS));
+        }
+        // epilogue: dK = sm_scale * acc, dV = acc -> bf16 -> smem (over K_j, V_j) -> TMA store
+        if (ok) ok = mbar_wait_warp(bar(L::kBarDone), 0, abort_flag, status_word);
+        if (ok) {
+            tc_fence_after();
+            stage_rows_bf16<D>(sbase + L::kRes0, lane_base + t_dk, row, p.sm_scale);
+            stage_rows_bf16<D>(sbase + L::kRes1, lane_base + t_dv, row, 1.0f);
+        }
+        fence_proxy_async_smem();
+        named_barrier_sync(1, 128);
+        if (ok && warp == 0 && lane == 0) {
+            for (int h = 0; h < kPanels; ++h) {
+                tma_store_4d(&tmap_dk, sbase + L::kRes0 + h * L::kPanelBytes, h * 64, j * 128, hkv, b);
+                tma_store_4d(&tmap_dv, sbase + L::kRes1 + h * L::kPanelBytes, h * 64, j * 128, hkv, b);
+            }
+            tma_store_commit_and_wait();
+        }
+        __syncwarp();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kBwdMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ------------------------------------------------------------------------------------------------
+// dQ
+// ------------------------------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                       const __grid_constant__ CUtensorMap tmap_k,
+                       const __grid_constant__ CUtensorMap tmap_v,
+                       const __grid_constant__ CUtensorMap tmap_do,
+                       const __grid_constant__ CUtensorMap tmap_dq, const BwdParams p,
+                       unsigned int* status_word) {
+    using L = BwdSmem<D>;
+    constexpr int kPanels = D / 64;
+    constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, 0);
+    constexpr uint32_t kIdescAcc = idesc_bf16_f32(128, D, 1);
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_addr(smem);
+    auto bar = [=](int x) -> uint32_t { return sbase + L::kBars + 8u * x; };
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // work: query tile i (latest, i.e. heaviest under the causal mask, first), then (b, hq)
+    const int bh_count = p.B * p.Hq;
+    const int i = p.n_tiles - 1 - static_cast<int>(blockIdx.x / bh_count);
+    const int bh = static_cast<int>(blockIdx.x % bh_count);
+    const int b = bh / p.Hq, hq = bh % p.Hq, hkv = hq / p.group;
+    const int n_it = p.causal ? i + 1 : p.n_tiles;  // key tiles 0 .. n_it-1
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(L::kBarRes), 1);
+        for (int s = 0; s < kBwdStages; ++s) {
+            mbar_init(bar(L::kBarFull + s), 1);
+            mbar_init(bar(L::kBarEmpty + s), 1);
+        }
+        mbar_init(bar(L::kBarS), 1);
+        mbar_init(bar(L::kBarDP), 1);
+        mbar_init(bar(L::kBarDS), 128);
+        mbar_init(bar(L::kBarDone), 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == kBwdMmaWarp) {
+        tmem_alloc(smem_addr(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t t_s = tmem, t_dp = tmem + 128, t_dq = tmem + 256;
+
+    if (warp == kBwdLoadWarp) {
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar(L::kBarRes), 2 * L::kTileBytes);
+            for (int h = 0; h < kPanels; ++h) {
+                tma_load_4d(sbase + L::kRes0 + h * L::kPanelBytes, &tmap_q, bar(L::kBarRes),
+                            h * 64, i * 128, hq, b);
+                tma_load_4d(sbase + L::kRes1 + h * L::kPanelBytes, &tmap_do, bar(L::kBarRes),
+                            h * 64, i * 128, hq, b);
+            }
+            for (int it = 0; it < n_it; ++it) {
+                const int s = it % kBwdStages;
+                const uint32_t ph = (it / kBwdStages) & 1;
+                if (!mbar_wait_bounded(bar(L::kBarEmpty + s), ph ^ 1u, abort_flag, status_word))
+                    break;
+                const uint32_t st = sbase + L::kStage + s * 2 * L::kTileBytes;
+                mbar_arrive_expect_tx(bar(L::kBarFull + s), 2 * L::kTileBytes);
+                for (int h = 0; h < kPanels; ++h) {
+                    tma_load_4d(st + h * L::kPanelBytes, &tmap_k, bar(L::kBarFull + s), h * 64,
+                                it * 128, hkv, b);
+                    tma_load_4d(st + L::kTileBytes + h * L::kPanelBytes, &tmap_v,
+                                bar(L::kBarFull + s), h * 64, it * 128, hkv, b);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == kBwdMmaWarp) {
+        bool ok = mbar_wait_warp(bar(L::kBarRes), 0, abort_flag, status_word);
+        const uint32_t qa = sbase + L::kRes0, da = sbase + L::kRes1;
+        for (int it = 0; ok && it < n_it; ++it) {
+            const int s = it % kBwdStages;
+            const uint32_t ph = (it / kBwdStages) & 1;
+            ok = mbar_wait_warp(bar(L::kBarFull + s), ph, abort_flag, status_word);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t ka = sbase + L::kStage + s * 2 * L::kTileBytes;
+            const uint32_t va = ka + L::kTileBytes;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {  // S = Q_i K_j^T
+                const uint32_t off = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
+                mma_bf16_ss_warp(t_s, smem_desc_sw128(qa + off, 16, 1024),
+                                 smem_desc_sw128(ka + off, 16, 1024), kIdescS, kk > 0);
+            }
+            mma_commit_warp(bar(L::kBarS));
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {  // dP = dO_i V_j^T
+                const uint32_t off = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
+                mma_bf16_ss_warp(t_dp, smem_desc_sw128(da + off, 16, 1024),
+                                 smem_desc_sw128(va + off, 16, 1024), kIdescS, kk > 0);
+            }
+            mma_commit_warp(bar(L::kBarDP));
+            ok = mbar_wait_warp(bar(L::kBarDS), it & 1, abort_flag, status_word);
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)  // dQ += dS K_j  (K = 128 keys)
+                mma_bf16_ts_warp(t_dq, t_s + kk * 8,
+                                 smem_desc_sw128(ka + kk * 2048, L::kPanelBytes, 1024), kIdescAcc,
+                                 (it > 0 || kk > 0) ? 1u : 0u);
+            mma_commit_warp(bar(L::kBarEmpty + s));
+        }
+        if (ok) mma_commit_warp(bar(L::kBarDone));
+        __syncwarp();
+    } else {
+        // elementwise warps 0-3: one thread per query row of tile i
+        const int row = warp * 32 + lane;
+        const int row_g = i * 128 + row;
+        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        const float c = p.scale_log2;
+        const size_t rix = static_cast<size_t>(bh) * p.N + row_g;
+        const float lse2 = row_g < p.N ? p.lse[rix] * kLog2e : 0.f;
+        const float dlt = row_g < p.N ? p.delta[rix] : 0.f;
+        bool ok = true;
+        for (int it = 0; it < n_it; ++it) {
+            ok = mbar_wait_warp(bar(L::kBarS), it & 1, abort_flag, status_word);
+            if (!ok) break;
+            tc_fence_after();
+            float pr[128];
+            {
+                uint32_t r[128];
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+                    tmem_ld32(lane_base + t_s + cc * 32,
+                              *reinterpret_cast<uint32_t(*)[32]>(&r[cc * 32]));
+                tmem_wait_ld();
+#pragma unroll
+                for (int k = 0; k < 128; ++k)
+                    pr[k] = ex2_approx(fmaf(__uint_as_float(r[k]), c, -lse2));
+            }
+            if (p.causal && it == i) {  // diagonal tile: key k visible to query `row` iff k <= row
+#pragma unroll
+                for (int k = 0; k < 128; ++k) pr[k] = k > row ? 0.f : pr[k];
+            }
+            ok = mbar_wait_warp(bar(L::kBarDP), it & 1, abort_flag, status_word);
+            if (!ok) break;
+            tc_fence_after();
+            // dS in 32-column chunks over the dP columns already read; packed dS goes over S
+            // (columns 16cc .. 16cc+15; S was fully read above).
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                uint32_t r[32];
+                tmem_ld32(lane_base + t_dp + cc * 32, r);
+                tmem_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int x = 0; x < 16; ++x) {
+                    const int k = cc * 32 + 2 * x;
+                    pk[x] = pack_bf16x2(pr[k] * (__uint_as_float(r[2 * x]) - dlt),
+                                        pr[k + 1] * (__uint_as_float(r[2 * x + 1]) - dlt));
+                }
+                tmem_st16(lane_base + t_s + cc * 16, pk);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(L::kBarDS));
+        }
+        if (ok) ok = mbar_wait_warp(bar(L::kBarDone), 0, abort_flag, status_word);
+        if (ok) {
+            tc_fence_after();
+            stage_rows_bf16<D>(sbase + L::kRes0, lane_base + t_dq, row, p.sm_scale);
+        }
+        fence_proxy_async_smem();
+        named_barrier_sync(1, 128);
+        if (ok && warp == 0 && lane == 0) {
+            for (int h = 0; h < kPanels; ++h)
+                tma_store_4d(&tmap_dq, sbase + L::kRes0 + h * L::kPanelBytes, h * 64, i * 128, hq, b);
+            tma_store_commit_and_wait();
+        }
+        __syncwarp();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kBwdMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace gb300attn

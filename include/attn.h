@@ -175,6 +175,34 @@ int attn_last_cuda_error(void);
 int attn_debug_status(void* stream);
 
 /*
+ * attn_bwd - gradients of attn_fwd by recompute (no stored probability matrix).
+ *
+ * The pages train through this attention by recomputing the scores and the probabilities from
+ * the saved log-sum-exp ("Attention Kernel 实现与正确性验证" (walkerchi.com), section 1.1, the third
+ * FA-2 idea; "Flash Attention 与 Kernel 优化" (fangpin.github.io), autograd and backward: rebuild
+ * s = qk^T * scale, the causal mask and p = softmax(s), then dv, dp, ds, dq, dk).  For query row
+ * i and visible key j: p_ij = exp(sm_scale q_i.k_j - LSE_i), dp_ij = dO_i.v_j,
+ * ds_ij = p_ij (dp_ij - dO_i.O_i); dQ_i = sm_scale sum_j ds_ij k_j, dK_j = sm_scale sum ds_ij q_i
+ * and dV_j = sum p_ij dO_i, the last two summed over the query heads that share the KV head.
+ *
+ *   q, k, v, B, Hq, Hkv, N, D, causal, sm_scale: as passed to attn_fwd (contiguous).
+ *   out, lse     attn_fwd's outputs O [B,Hq,N,D] bf16 and LSE [B,Hq,N] fp32 (inputs here).
+ *   dout         dL/dO, bf16 [B, Hq, N, D], contiguous.
+ *   dq           bf16 [B, Hq, N, D]; dk, dv bf16 [B, Hkv, N, D]: written (contiguous).
+ *   workspace    device memory of at least attn_bwd_workspace_bytes(B, Hq, N) bytes, 16-byte
+ *                aligned, owned by the caller (holds dO . O per row); contents ignored.
+ *   No output may overlap an input or another output.  Three kernels run on `stream`.
+ *
+ * Returns ATTN_OK once enqueued, else a negative attn_status_t (nothing written).
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
+             const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int D,
+             int causal, float sm_scale, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes attn_bwd needs (B * Hq * N * 4; 0 for invalid sizes). */
+size_t attn_bwd_workspace_bytes(int B, int Hq, int N);
+
+/*
  * attn_fwd_test_stall - test hook for the failure-reporting path (not for computing anything).
  *
  * Runs attn_fwd, except that every CTA's producer withholds item `stall_item` (>= 0) of its K/V

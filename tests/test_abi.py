@@ -30,7 +30,7 @@ def test_header_declares_the_boundary():
         ["attn_fwd", "attn_status_string", "attn_last_cuda_error", "attn_debug_status",
          "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_bytes", "attn_fwd_splitkv_num_splits",
          "attn_fwd_splitkv_noalloc", "attn_fwd_splitkv_noalloc_max_bytes", "attn_fwd_strided",
-         "attn_fwd_test_stall"])
+         "attn_fwd_test_stall", "attn_bwd", "attn_bwd_workspace_bytes"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -145,3 +145,8 @@ def _strided(lib, qs=(2 * 128 * 64, 128 * 64, 64), ks=(128 * 64, 128 * 64, 64),
 ])
 def test_strided_host_validation(lib, kw, status):
     assert _strided(lib, **kw) == status
+
+
+def test_bwd_workspace_bytes(lib):
+    assert lib.attn_bwd_workspace_bytes(2, 8, 1000) == 2 * 8 * 1000 * 4
+    assert lib.attn_bwd_workspace_bytes(0, 8, 1000) == 0
