@@ -448,6 +448,41 @@ def main():
             low_occ.append(entry)
             del lq, lk, lv, lo, ll, wbuf
 
+    # ---- context: the backward (by recompute) on the long-context workload -------------------
+    # Algorithmic FLOPs of the backward: 2.5x the forward's (five N x N x D matmuls: S, dP, dV,
+    # dK, dQ), halved under the causal mask like the forward's.
+    backward = []
+    if not args.no_sweep and rank == 0:
+        for n in (8192, 16384):
+            wb = wl.LONG[n]
+            bq, bk, bv = (t.to(dev) for t in wl.make_qkv(wb))
+            bo, bl = attn.attn_fwd(bq, bk, bv, causal=wb.causal, sm_scale=wb.sm_scale)
+            g = torch.Generator(device="cpu").manual_seed(77)
+            bdo = torch.randn(bq.shape, generator=g).to(torch.bfloat16).to(dev)
+            dq, dk, dv = torch.empty_like(bq), torch.empty_like(bk), torch.empty_like(bv)
+            lib = _lib.load()
+            need = int(lib.attn_bwd_workspace_bytes(wb.B, wb.Hq, wb.N))
+            wsb = torch.empty(need, dtype=torch.uint8, device=dev)
+            sh = ctypes.c_void_p(stream.cuda_stream)
+
+            def bstep():
+                assert lib.attn_bwd(bq.data_ptr(), bk.data_ptr(), bv.data_ptr(), bo.data_ptr(),
+                                    bl.data_ptr(), bdo.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                    dv.data_ptr(), wb.B, wb.Hq, wb.Hkv, wb.N, wb.D,
+                                    int(wb.causal), ctypes.c_float(wb.sm_scale), wsb.data_ptr(),
+                                    need, sh) == 0
+
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    bstep()
+            ms = statistics.median(timed_launches(bstep, stream, 10))
+            tf = 2.5 * wb.flops / (ms * 1e-3) / 1e12
+            backward.append({"workload": wb.name, "ms": ms, "tflops": tf, "frac": tf / peak,
+                             "kernels_per_step": 3})
+            del bq, bk, bv, bo, bl, bdo, dq, dk, dv, wsb
+        if attn.device_status(dev) != 0:
+            raise SystemExit("device status word reports an expired wait in the backward leg")
+
     # ---- CPU baseline: the oracle as it stands, bounded sample, rank 0 at N=1 only -----------
     cpu = None
     if rank == 0 and world == 1:
@@ -473,7 +508,7 @@ def main():
             "config": config_of(w, "inputs and output exceed the 129 MB L2; no flush"),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": args.steps, "clocks": clocks, "sweep": sweep,
-            "low_occupancy": low_occ,
+            "low_occupancy": low_occ, "backward": backward,
             "kernel_sha": kernel_hash(),
         }
         print(json.dumps(line), flush=True)
