@@ -44,7 +44,6 @@ constexpr int kThreads = 352;     // 11 warps
 constexpr int kMmaWarp0 = 8;      // issues the MMAs of Q tile 0; warp 9 those of Q tile 1
 constexpr int kLoadWarp = 10;
 constexpr uint32_t kTmemCols = 512;
-constexpr int kPParts = 2;        // P is published to the MMA issuer in this many key blocks
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -72,14 +71,17 @@ struct SmemLayout {
     static constexpr int kTileBytes = kBM * D * 2;          // 128 x D bf16 = D/64 panels
     static constexpr int kQ = 0;                            // Q tiles (reused as O staging)
     static constexpr int kKV = kQ + kQTiles * kTileBytes;   // K/V ring
-    static constexpr int kBars = kKV + kStages * kTileBytes;
+    static constexpr int kP1 = kKV + kStages * kTileBytes;     // P keys 64..127, [2 tiles]
+    static constexpr int kP1Bytes = kBM * 64 * 2;               // one 128B-swizzle panel
+    static constexpr int kBars = kP1 + 2 * kP1Bytes;
     // barrier indices
     static constexpr int kBarQ = 0;
     static constexpr int kBarKvFull = 1;
     static constexpr int kBarKvEmpty = kBarKvFull + kStages;
     static constexpr int kBarSFull = kBarKvEmpty + kStages;   // [2]
-    static constexpr int kBarPReady = kBarSFull + 2;          // [2 tiles][kPParts key blocks]
-    static constexpr int kBarODone = kBarPReady + 2 * kPParts;  // [2]
+    static constexpr int kBarPReady = kBarSFull + 2;          // [2 tiles][2 key halves]
+    static constexpr int kBarPVDone = kBarPReady + 4;         // [2]: a step's P.V completed
+    static constexpr int kBarODone = kBarPVDone + 2;          // [2]
     static constexpr int kBarTurn = kBarODone + 2;            // [2]: softmax group t may run exp2
     static constexpr int kNumBars = kBarTurn + 2;
     static constexpr int kTmemSlot = kBars + kNumBars * 8;
@@ -161,7 +163,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(bar(L::kBarSFull + t), 1);
-            for (int h = 0; h < kPParts; ++h) mbar_init(bar(L::kBarPReady + kPParts * t + h), 128);
+            mbar_init(bar(L::kBarPReady + 2 * t + 0), 128);
+            mbar_init(bar(L::kBarPReady + 2 * t + 1), 128);
+            mbar_init(bar(L::kBarPVDone + t), 1);
             mbar_init(bar(L::kBarODone + t), 1);
             mbar_init(bar(L::kBarTurn + t), 128);
         }
@@ -240,25 +244,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      smem_desc_sw128(ka + off, 16, 1024), kIdescS, kk > 0);
                 }
             };
-            // O_t += P_t . V, P_t arriving in kPParts key blocks: each block's MMAs start as soon
-            // as that block is in TMEM.
-            auto pv_mma = [=](int vslot, bool accumulate_first, uint32_t phase) -> bool {
+            // O_t += P_t . V in two halves.  Keys 0-63 of P_t arrive in TMEM over S_t (TS form);
+            // keys 64-127 arrive in a swizzled smem panel (SS form).  Because the second half
+            // does not live in TMEM, S_t(j+1) can be issued right after the first half's MMAs
+            // and computes while the softmax still works on the second half.
+            const uint32_t p1a = sbase + L::kP1 + t * L::kP1Bytes;
+            auto pv_first = [=](int vslot, bool accumulate_first) {
                 const uint32_t va = sbase + L::kKV + vslot * L::kTileBytes;
 #pragma unroll
-                for (int h = 0; h < kPParts; ++h) {
-                    if (!mbar_wait_warp(bar(L::kBarPReady + kPParts * t + h), phase, abort_flag,
-                                        status_word))
-                        return false;
-                    tc_fence_after();
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16_ts_warp(o_tmem, s_tmem + kk * 8,
+                                     smem_desc_sw128(va + kk * 2048, L::kPanelBytes, 1024),
+                                     kIdescPV, (accumulate_first || kk > 0) ? 1u : 0u);
+            };
+            auto pv_second = [=](int vslot) {
+                const uint32_t va = sbase + L::kKV + vslot * L::kTileBytes;
 #pragma unroll
-                    for (int k4 = 0; k4 < kBN / 16 / kPParts; ++k4) {
-                        const int kk = h * (kBN / 16 / kPParts) + k4;
-                        mma_bf16_ts_warp(o_tmem, s_tmem + kk * 8,
-                                         smem_desc_sw128(va + kk * 2048, L::kPanelBytes, 1024),
-                                         kIdescPV, (accumulate_first || kk > 0) ? 1u : 0u);
-                    }
-                }
-                return true;
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16_ss_warp(o_tmem, smem_desc_sw128(p1a + kk * 32, 16, 1024),
+                                     smem_desc_sw128(va + (4 + kk) * 2048, L::kPanelBytes, 1024),
+                                     kIdescPV, 1u);
             };
 
             uint32_t p_phase = 0;
@@ -274,13 +279,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int vidx = 2 * (j - kv_begin) + 1;  // V_j
                 const int kidx = vidx + 1;                // K_{j+1}
                 ok = wait_full(vidx);
+                if (ok) ok = mbar_wait_warp(bar(L::kBarPReady + 2 * t + 0), p_phase, abort_flag,
+                                            status_word);
                 if (!ok) break;
-                ok = pv_mma(kv_slot(vidx), j > kv_begin, p_phase);
-                if (!ok) break;
-                p_phase ^= 1u;
-                if (j == last) mma_commit_warp(bar(L::kBarODone + t));
-                mma_commit_warp(bar(L::kBarKvEmpty + kv_slot(vidx)));
-                if (j + 1 <= last) {
+                tc_fence_after();
+                pv_first(kv_slot(vidx), j > kv_begin);
+                if (j + 1 <= last) {  // S_t(j+1) overwrites the first half of P_t(j): issued after
                     ok = wait_full(kidx);
                     if (!ok) break;
                     tc_fence_after();
@@ -288,6 +292,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_commit_warp(bar(L::kBarSFull + t));
                     mma_commit_warp(bar(L::kBarKvEmpty + kv_slot(kidx)));
                 }
+                ok = mbar_wait_warp(bar(L::kBarPReady + 2 * t + 1), p_phase, abort_flag,
+                                    status_word);
+                if (!ok) break;
+                tc_fence_after();
+                pv_second(kv_slot(vidx));
+                p_phase ^= 1u;
+                mma_commit_warp(bar(L::kBarPVDone + t));
+                if (j == last) mma_commit_warp(bar(L::kBarODone + t));
+                mma_commit_warp(bar(L::kBarKvEmpty + kv_slot(vidx)));
             }
             // KV tiles this Q tile does not need (under the causal mask, the last one for Q tile
             // 0): release each slot once its data has landed, so every slot phase gets one
@@ -376,16 +389,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         abort_flag, status_word);
                     if (!ok) break;
                 }
-                // p = exp2(c*s - m) in kPParts key blocks; each block is published to the MMA
-                // issuer as soon as it is in TMEM, so its P.V overlaps the next block's exp2.
-                constexpr int kPairs = kBN / kPParts / 2;  // packed bf16 pairs per block
+                // p = exp2(c*s - m).  Keys 0-63 go to TMEM (over S) and are published first; keys
+                // 64-127 go to this tile's smem panel, which the previous step's second-half P.V
+                // must have finished reading (pv_done).  That P.V also had to land before the
+                // O correction (O_row *= alpha, rare thanks to the lazy maximum).
                 float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                auto exp_half = [&](int h, uint32_t (&pk)[32]) {
 #pragma unroll
-                for (int h = 0; h < kPParts; ++h) {
-                    uint32_t pk[kPairs];
-#pragma unroll
-                    for (int i = 0; i < kPairs; ++i) {
-                        const int col = h * 2 * kPairs + 2 * i;
+                    for (int i = 0; i < 32; ++i) {
+                        const int col = h * 64 + 2 * i;
                         float x0, x1;
                         ffma2(x0, x1, s[col], s[col + 1], c, c, neg_m, neg_m);
                         const float p0 = ex2_approx(x0);
@@ -394,17 +406,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         fadd2(acc[a], acc[a + 1], acc[a], acc[a + 1], p0, p1);
                         pk[i] = pack_bf16x2(p0, p1);
                     }
-                    if constexpr (kPairs == 32)
-                        tmem_st32(s_addr + h * kPairs, *reinterpret_cast<uint32_t(*)[32]>(pk));
-                    else
-                        tmem_st16(s_addr + h * kPairs, *reinterpret_cast<uint32_t(*)[16]>(pk));
-                    // The O correction (O_row *= alpha, rare thanks to the lazy maximum) must land
-                    // before this tile's P.V is issued; it runs once the scores of the first
-                    // blocks are dead (fewer live registers) and those blocks are published with
-                    // it.  The P.V of tile j-1 completed before S of tile j (in-order MMAs).
-                    constexpr int kRescaleAfter = kPParts > 2 ? 1 : 0;
-                    if (rescale && h < kRescaleAfter) continue;
-                    if (rescale && h == kRescaleAfter) {
+                };
+                const bool prev_pv = j > kv_begin;  // a previous step's P.V is in flight
+                {
+                    uint32_t pk[32];
+                    exp_half(0, pk);
+                    tmem_st32(s_addr, pk);
+                    if (rescale) {
+                        ok = mbar_wait_warp(bar(L::kBarPVDone + t), (j - 1 - kv_begin) & 1,
+                                            abort_flag, status_word);
+                        if (!ok) break;
 #pragma unroll
                         for (int cc = 0; cc < D / 32; ++cc) {
                             uint32_t r[32];
@@ -418,10 +429,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tmem_wait_st();
                     tc_fence_before();
-                    if (rescale && h == kRescaleAfter)
-                        for (int h0 = 0; h0 < kRescaleAfter; ++h0)
-                            mbar_arrive(bar(L::kBarPReady + kPParts * t + h0));
-                    mbar_arrive(bar(L::kBarPReady + kPParts * t + h));
+                    mbar_arrive(bar(L::kBarPReady + 2 * t + 0));
+                }
+                {
+                    uint32_t pk[32];
+                    exp_half(1, pk);
+                    if (prev_pv && !rescale) {
+                        ok = mbar_wait_warp(bar(L::kBarPVDone + t), (j - 1 - kv_begin) & 1,
+                                            abort_flag, status_word);
+                        if (!ok) break;
+                    }
+                    const uint32_t prow = sbase + L::kP1 + t * L::kP1Bytes + row * 128;
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch)
+                        st_shared_v4(prow + ((ch ^ (row & 7)) << 4), pk[4 * ch], pk[4 * ch + 1],
+                                     pk[4 * ch + 2], pk[4 * ch + 3]);
+                    fence_proxy_async_smem();  // generic-proxy stores -> the MMA's async reads
+                    mbar_arrive(bar(L::kBarPReady + 2 * t + 1));
                 }
                 l = l * alpha + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
                 // hand the turn to the other group (tile 1 only while tile 0 has steps left)
