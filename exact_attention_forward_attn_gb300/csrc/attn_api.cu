@@ -139,7 +139,7 @@ template <int D>
 cudaError_t opt_in_bwd_smem() {
     cudaError_t e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         BwdSmem<D>::kAlloc);
+                                         DkdvSmem<D>::kAlloc);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(attn_bwd_dq_kernel<D>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, BwdSmem<D>::kAlloc);
@@ -504,7 +504,7 @@ int launch_bwd(const Problem& P, const CUtensorMap& mq, const CUtensorMap& mk,
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
     attn_bwd_dkdv_kernel<D><<<static_cast<unsigned int>(P.n_tiles * P.bh_kv), kBwdThreads,
-                              BwdSmem<D>::kAlloc, s>>>(mq, mk, mv, mdo, mdk, mdv, bp, status_word);
+                              DkdvSmem<D>::kAlloc, s>>>(mq, mk, mv, mdo, mdk, mdv, bp, status_word);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
     attn_bwd_dq_kernel<D><<<static_cast<unsigned int>(P.n_tiles * P.bh), kBwdThreads,
@@ -626,7 +626,8 @@ extern "C" int attn_debug_status(void* stream) {
                                     cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e);
-    return (word & kDevTimeout) ? ATTN_ERR_TIMEOUT : ATTN_OK;
+    if (word & kDevTimeout) return ATTN_ERR_TIMEOUT;
+    return (word & kDevSmemAlign) ? ATTN_ERR_ARCH : ATTN_OK;
 }
 
 // ------------------------------------------------------------------------------------------------

@@ -14,8 +14,8 @@
 //   attn_bwd_dkdv_kernel    one CTA per (b, KV head, 128-key tile j): K_j, V_j stay in smem; for
 //                           every query head of the group and every query tile i (i >= j under
 //                           the causal mask) it forms S^T = K_j Q_i^T and dP^T = V_j dO_i^T,
-//                           P^T and dS^T (bf16, in TMEM over S^T / dP^T), and accumulates
-//                           dV += P^T dO_i and dK += dS^T Q_i in TMEM.
+//                           P^T (bf16, in shared memory) and dS^T (bf16, in TMEM over dP^T),
+//                           and accumulates dV += P^T dO_i and dK += dS^T Q_i in TMEM.
 //   attn_bwd_dq_kernel      one CTA per (b, query head, 128-row tile i): S = Q_i K_j^T,
 //                           dP = dO_i V_j^T, dS (bf16 in TMEM over S), dQ += dS K_j.
 // Zero-filled rows past N contribute nothing: a padded query has dO = 0 and Delta = 0 (so its
@@ -43,9 +43,14 @@ struct BwdParams {
     const float* delta;  // [B, Hq, N] dO . O
 };
 
-constexpr int kBwdThreads = 192;  // warps 0-3 elementwise, 4 MMA issuer, 5 TMA producer
-constexpr int kBwdMmaWarp = 4;
-constexpr int kBwdLoadWarp = 5;
+// Warps 0-7 elementwise: warp w serves TMEM lanes 32(w%4) .. 32(w%4)+31 (its quarter) and the
+// 64 columns 64(w/4) .. 64(w/4)+63 of the 128-wide S / dP tile, so every lane quarter has two
+// warps.  Warps 8 and 10 issue the MMAs of two independent accumulator chains, warp 9 loads.
+constexpr int kBwdMmaWarp = 8;
+constexpr int kBwdLoadWarp = 9;
+constexpr int kBwdMmaWarpB = 10;
+constexpr int kBwdThreads = 352;
+constexpr int kBwdEwThreads = 256;
 constexpr int kBwdStages = 2;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -76,12 +81,13 @@ struct BwdSmem {
     static constexpr int kStage = 2 * kTileBytes;  // stage s: [kStage + 2*s*tile, +2 tiles)
     static constexpr int kVec = kStage + 2 * kBwdStages * kTileBytes;  // lse2/delta [stage][2][128]
     static constexpr int kBars = kVec + kBwdStages * 2 * 128 * 4;
-    // barriers: res_full, stage_full[S], stage_empty[S], s_full, dp_full, p_ready, ds_ready, done
+    // barriers: res_full, stage_full[S], stage_empty[S], s_full[2], dp_full, p_ready, ds_ready,
+    // done (dkdv uses s_full[0] only)
     static constexpr int kBarRes = 0;
     static constexpr int kBarFull = 1;
     static constexpr int kBarEmpty = kBarFull + kBwdStages;
     static constexpr int kBarS = kBarEmpty + kBwdStages;
-    static constexpr int kBarDP = kBarS + 1;
+    static constexpr int kBarDP = kBarS + 2;
     static constexpr int kBarP = kBarDP + 1;
     static constexpr int kBarDS = kBarP + 1;
     static constexpr int kBarDone = kBarDS + 1;
@@ -92,13 +98,55 @@ struct BwdSmem {
     static constexpr int kAlloc = kBytes + 1024;
 };
 
-// Stage a 128 x D fp32 accumulator row (this thread's TMEM lane) as bf16 into a 128B-swizzled
-// panel pair at `stage` (the layout the 4-D TMA store expects).
+// dK/dV layout: BwdSmem's tiles, then P^T (bf16, two 128B-swizzled 128 x 64 panels) so that
+// S^T(it+1) can be formed in TMEM while P^T(it) is still being written and read.  This fills the
+// 227 KiB limit, so the layout leaves no slack for aligning the base: the kernel checks that the
+// dynamic shared memory starts 1024-aligned and reports kDevSmemAlign otherwise.
+template <int D>
+struct DkdvSmem {
+    static constexpr int kPanelBytes = 128 * 64 * 2;
+    static constexpr int kTileBytes = 128 * D * 2;
+    static constexpr int kRes0 = 0;                  // K_j
+    static constexpr int kRes1 = kTileBytes;         // V_j
+    static constexpr int kStage = 2 * kTileBytes;    // stage s: Q_i, dO_i
+    static constexpr int kPt = kStage + 2 * kBwdStages * kTileBytes;
+    static constexpr int kVec = kPt + 2 * kPanelBytes;  // lse2/delta [stage][2][128]
+    static constexpr int kBars = kVec + kBwdStages * 2 * 128 * 4;
+    // barriers: res_full, stage_full[S], stage_empty[S], s_full, s_free, dp_full, p_ready,
+    // p_free, ds_ready, done
+    static constexpr int kBarRes = 0;
+    static constexpr int kBarFull = 1;
+    static constexpr int kBarEmpty = kBarFull + kBwdStages;
+    static constexpr int kBarS = kBarEmpty + kBwdStages;
+    static constexpr int kBarSFree = kBarS + 1;
+    static constexpr int kBarDP = kBarSFree + 1;
+    static constexpr int kBarP = kBarDP + 1;
+    static constexpr int kBarPFree = kBarP + 1;
+    static constexpr int kBarDS = kBarPFree + 1;
+    static constexpr int kBarDone = kBarDS + 1;
+    static constexpr int kNumBars = kBarDone + 1;
+    static constexpr int kTmemSlot = kBars + kNumBars * 8;
+    static constexpr int kAbort = kTmemSlot + 8;
+    static constexpr int kBytes = kAbort + 8;
+    static constexpr int kAlloc = kBytes;
+    static_assert(kAlloc <= 232448, "dK/dV shared memory exceeds the per-block limit");
+};
+
+// A 128 x 128 bf16 operand (dS^T, dS) is packed into TMEM by the two column halves' warps,
+// each over the first 32 of its own 64 fp32 columns: K-step kk (16 columns of the operand)
+// starts at this column offset.
+__device__ __forceinline__ uint32_t packed_col(int kk) {
+    return static_cast<uint32_t>((kk >> 2) * 64 + (kk & 3) * 8);
+}
+
+// Stage 32-column chunks [cc_begin, cc_end) of a 128 x D fp32 accumulator row (this thread's TMEM
+// lane) as bf16 into a 128B-swizzled panel pair at `stage` (the layout the 4-D TMA store expects).
 template <int D>
 __device__ __forceinline__ void stage_rows_bf16(uint32_t stage, uint32_t taddr, int row,
-                                                float mul) {
+                                                float mul, int cc_begin, int cc_end) {
 #pragma unroll
     for (int cc = 0; cc < D / 32; ++cc) {
+        if (cc < cc_begin || cc >= cc_end) continue;
         uint32_t r[32];
         tmem_ld32(taddr + cc * 32, r);
         tmem_wait_ld();
@@ -129,14 +177,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                          const __grid_constant__ CUtensorMap tmap_dk,
                          const __grid_constant__ CUtensorMap tmap_dv, const BwdParams p,
                          unsigned int* status_word) {
-    using L = BwdSmem<D>;
+    using L = DkdvSmem<D>;
     constexpr int kPanels = D / 64;
     constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, 0);  // K-major x K-major
-    constexpr uint32_t kIdescAcc = idesc_bf16_f32(128, D, 1);  // TMEM x MN-major
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    constexpr uint32_t kIdescAcc = idesc_bf16_f32(128, D, 1);  // (TMEM or K-major) x MN-major
+    extern __shared__ __align__(1024) uint8_t dkdv_smem[];
+    uint8_t* smem = dkdv_smem;
     const uint32_t sbase = smem_addr(smem);
+    if (sbase & 1023u) {  // uniform over the CTA: every thread leaves before any barrier
+        if (threadIdx.x == 0) atomicOr(status_word, kDevSmemAlign);
+        return;
+    }
     auto bar = [=](int i) -> uint32_t { return sbase + L::kBars + 8u * i; };
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
@@ -154,14 +205,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (threadIdx.x == 0) {
         mbar_init(bar(L::kBarRes), 1);
         for (int s = 0; s < kBwdStages; ++s) {
-            mbar_init(bar(L::kBarFull + s), 32);  // 1 expect_tx arrive + 31 vector arrives
-            mbar_init(bar(L::kBarEmpty + s), 1);
+            mbar_init(bar(L::kBarFull + s), 32);  // the producer's 32 lanes (vectors) + tx bytes
+            mbar_init(bar(L::kBarEmpty + s), 2);  // one release per issuer
         }
         mbar_init(bar(L::kBarS), 1);
+        mbar_init(bar(L::kBarSFree), kBwdEwThreads);
         mbar_init(bar(L::kBarDP), 1);
-        mbar_init(bar(L::kBarP), 128);
-        mbar_init(bar(L::kBarDS), 128);
-        mbar_init(bar(L::kBarDone), 1);
+        mbar_init(bar(L::kBarP), kBwdEwThreads);
+        mbar_init(bar(L::kBarPFree), 1);
+        mbar_init(bar(L::kBarDS), kBwdEwThreads);
+        mbar_init(bar(L::kBarDone), 2);
         *abort_flag = 0;
         fence_mbarrier_init();
         fence_proxy_async_smem();
@@ -179,7 +232,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     auto it_tile = [=](int it) { return i_first + it % per_head; };
 
     if (warp == kBwdLoadWarp) {
-        // ---------------- producer (warp-uniform loop; lane 0 issues the TMA) ------------------
+        // ---------------- producer: lane 0 issues the TMA, every lane stages 4+4 vector entries,
+        // fetched into registers one iteration ahead ----------------------------------------------
         if (lane == 0) {
             mbar_arrive_expect_tx(bar(L::kBarRes), 2 * L::kTileBytes);
             for (int h = 0; h < kPanels; ++h) {
@@ -189,89 +243,129 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                             h * 64, j * 128, hkv, b);
             }
         }
+        // lse2 = LSE*log2(e) and Delta of queries lane*4 .. lane*4+3 of the iteration's tile (0
+        // past N: see top)
+        float nl[4], nd[4];
+        auto fetch = [&](int it) {
+            const size_t rowbase = (static_cast<size_t>(b) * p.Hq + it_head(it)) * p.N;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int q = it_tile(it) * 128 + lane * 4 + e;
+                nl[e] = q < p.N ? p.lse[rowbase + q] * kLog2e : 0.f;
+                nd[e] = q < p.N ? p.delta[rowbase + q] : 0.f;
+            }
+        };
+        if (n_it > 0) fetch(0);
         for (int it = 0; it < n_it; ++it) {
             const int s = it % kBwdStages;
             const uint32_t ph = (it / kBwdStages) & 1;
-            if (!mbar_wait_warp(bar(L::kBarEmpty + s), ph ^ 1u, abort_flag, status_word)) break;
-            const int hq = it_head(it), i = it_tile(it);
-            const size_t rowbase = (static_cast<size_t>(b) * p.Hq + hq) * p.N;
-            // lse2 = LSE*log2(e) and Delta for the 128 queries of tile i (0 past N: see top)
-            float* vec = reinterpret_cast<float*>(smem + L::kVec) + s * 256;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int q = i * 128 + lane * 4 + e;
-                vec[lane * 4 + e] = q < p.N ? p.lse[rowbase + q] * kLog2e : 0.f;
-                vec[128 + lane * 4 + e] = q < p.N ? p.delta[rowbase + q] : 0.f;
-            }
+            if (!mbar_wait_warp<true>(bar(L::kBarEmpty + s), ph ^ 1u, abort_flag, status_word)) break;
             if (lane == 0) {
+                const int hq = it_head(it), i = it_tile(it);
                 const uint32_t st = sbase + L::kStage + s * 2 * L::kTileBytes;
-                mbar_arrive_expect_tx(bar(L::kBarFull + s), 2 * L::kTileBytes);
+                mbar_expect_tx(bar(L::kBarFull + s), 2 * L::kTileBytes);
                 for (int h = 0; h < kPanels; ++h) {
                     tma_load_4d(st + h * L::kPanelBytes, &tmap_q, bar(L::kBarFull + s), h * 64,
                                 i * 128, hq, b);
                     tma_load_4d(st + L::kTileBytes + h * L::kPanelBytes, &tmap_do,
                                 bar(L::kBarFull + s), h * 64, i * 128, hq, b);
                 }
-            } else {
-                mbar_arrive(bar(L::kBarFull + s));
             }
+            float4* vec = reinterpret_cast<float4*>(smem + L::kVec) + s * 64;
+            vec[lane] = make_float4(nl[0], nl[1], nl[2], nl[3]);
+            vec[32 + lane] = make_float4(nd[0], nd[1], nd[2], nd[3]);
+            mbar_arrive(bar(L::kBarFull + s));
+            if (it + 1 < n_it) fetch(it + 1);
         }
         __syncwarp();
-    } else if (warp == kBwdMmaWarp) {
-        // ---------------- MMA issuer (warp-uniform, elected lane) ------------------------------
-        bool ok = mbar_wait_warp(bar(L::kBarRes), 0, abort_flag, status_word);
-        const uint32_t ka = sbase + L::kRes0, va = sbase + L::kRes1;
-        for (int it = 0; ok && it < n_it; ++it) {
-            const int s = it % kBwdStages;
-            const uint32_t ph = (it / kBwdStages) & 1;
-            ok = mbar_wait_warp(bar(L::kBarFull + s), ph, abort_flag, status_word);
-            if (!ok) break;
+    } else if (warp == kBwdMmaWarp || warp == kBwdMmaWarpB) {
+        // ---------------- MMA issuers (warp-uniform, elected lane) -----------------------------
+        // A: S^T(it+1) = K_j Q_(it+1)^T as soon as the elementwise warps have read S^T(it), then
+        //    dV += P^T(it) dO_it with P^T from shared memory;
+        // B: dP^T(it) = V_j dO_it^T, then dK += dS^T(it) Q_it with dS^T over dP^T in TMEM.
+        // Each chain reuses its own TMEM region in issue order, so the chains need no common order.
+        const bool chain_a = warp == kBwdMmaWarp;
+        bool ok = mbar_wait_warp<true>(bar(L::kBarRes), 0, abort_flag, status_word);
+        const uint32_t ka = sbase + L::kRes0, va = sbase + L::kRes1, pt = sbase + L::kPt;
+        auto stage_q = [&](int it) { return sbase + L::kStage + (it % kBwdStages) * 2 * L::kTileBytes; };
+        auto wait_full = [&](int it) {
+            const bool w = mbar_wait_warp<true>(bar(L::kBarFull + it % kBwdStages),
+                                                (it / kBwdStages) & 1, abort_flag, status_word);
             tc_fence_after();
-            const uint32_t qa = sbase + L::kStage + s * 2 * L::kTileBytes;
-            const uint32_t da = qa + L::kTileBytes;
+            return w;
+        };
+        auto s_mma = [&](int it) {  // S^T = K_j Q_it^T
+            const uint32_t qa = stage_q(it);
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {  // S^T = K_j Q_i^T
+            for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t off = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
                 mma_bf16_ss_warp(t_s, smem_desc_sw128(ka + off, 16, 1024),
                                  smem_desc_sw128(qa + off, 16, 1024), kIdescS, kk > 0);
             }
             mma_commit_warp(bar(L::kBarS));
+        };
+        if (chain_a) {
+            if (ok && n_it > 0) ok = wait_full(0);
+            if (ok && n_it > 0) s_mma(0);
+            for (int it = 0; ok && it < n_it; ++it) {
+                if (it + 1 < n_it) {
+                    ok = wait_full(it + 1);
+                    if (ok) ok = mbar_wait_warp<true>(bar(L::kBarSFree), it & 1, abort_flag,
+                                                      status_word);
+                    if (!ok) break;
+                    tc_fence_after();
+                    s_mma(it + 1);
+                }
+                ok = mbar_wait_warp<true>(bar(L::kBarP), it & 1, abort_flag, status_word);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t da = stage_q(it) + L::kTileBytes;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {  // dP^T = V_j dO_i^T
-                const uint32_t off = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
-                mma_bf16_ss_warp(t_dp, smem_desc_sw128(va + off, 16, 1024),
-                                 smem_desc_sw128(da + off, 16, 1024), kIdescS, kk > 0);
+                for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO_i  (K = 128 queries)
+                    mma_bf16_ss_warp(t_dv,
+                                     smem_desc_sw128(pt + (kk >> 2) * L::kPanelBytes + (kk & 3) * 32,
+                                                     16, 1024),
+                                     smem_desc_sw128(da + kk * 2048, L::kPanelBytes, 1024),
+                                     kIdescAcc, (it > 0 || kk > 0) ? 1u : 0u);
+                mma_commit_warp(bar(L::kBarPFree));
+                mma_commit_warp(bar(L::kBarEmpty + it % kBwdStages));
             }
-            mma_commit_warp(bar(L::kBarDP));
-            ok = mbar_wait_warp(bar(L::kBarP), it & 1, abort_flag, status_word);
-            if (!ok) break;
-            tc_fence_after();
+        } else {
+            for (int it = 0; ok && it < n_it; ++it) {
+                ok = wait_full(it);
+                if (!ok) break;
+                const uint32_t qa = stage_q(it), da = qa + L::kTileBytes;
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO_i  (K = 128 queries)
-                mma_bf16_ts_warp(t_dv, t_s + kk * 8,
-                                 smem_desc_sw128(da + kk * 2048, L::kPanelBytes, 1024), kIdescAcc,
-                                 (it > 0 || kk > 0) ? 1u : 0u);
-            ok = mbar_wait_warp(bar(L::kBarDS), it & 1, abort_flag, status_word);
-            if (!ok) break;
-            tc_fence_after();
+                for (int kk = 0; kk < D / 16; ++kk) {  // dP^T = V_j dO_i^T
+                    const uint32_t off = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
+                    mma_bf16_ss_warp(t_dp, smem_desc_sw128(va + off, 16, 1024),
+                                     smem_desc_sw128(da + off, 16, 1024), kIdescS, kk > 0);
+                }
+                mma_commit_warp(bar(L::kBarDP));
+                ok = mbar_wait_warp<true>(bar(L::kBarDS), it & 1, abort_flag, status_word);
+                if (!ok) break;
+                tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)  // dK += dS^T Q_i
-                mma_bf16_ts_warp(t_dk, t_dp + kk * 8,
-                                 smem_desc_sw128(qa + kk * 2048, L::kPanelBytes, 1024), kIdescAcc,
-                                 (it > 0 || kk > 0) ? 1u : 0u);
-            mma_commit_warp(bar(L::kBarEmpty + s));
+                for (int kk = 0; kk < 8; ++kk)  // dK += dS^T Q_i
+                    mma_bf16_ts_warp(t_dk, t_dp + packed_col(kk),
+                                     smem_desc_sw128(qa + kk * 2048, L::kPanelBytes, 1024),
+                                     kIdescAcc, (it > 0 || kk > 0) ? 1u : 0u);
+                mma_commit_warp(bar(L::kBarEmpty + it % kBwdStages));
+            }
         }
         if (ok) mma_commit_warp(bar(L::kBarDone));
         __syncwarp();
     } else {
-        // ---------------- elementwise warps 0-3: one thread per key row of tile j --------------
-        const int row = warp * 32 + lane;  // key within the tile (TMEM lane)
-        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        // ---------------- elementwise warps 0-7: key row `row` of tile j, queries c0 .. c0+63 --
+        const int quarter = warp & 3, half = warp >> 2;
+        const int row = quarter * 32 + lane;  // key within the tile (TMEM lane)
+        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+        const int c0 = half * 64;
         const float c = p.scale_log2;
         bool ok = true;
         for (int it = 0; it < n_it; ++it) {
             const int s = it % kBwdStages;
-            const float* vec = reinterpret_cast<const float*>(smem + L::kVec) + s * 256;
+            const float* vec = reinterpret_cast<const float*>(smem + L::kVec) + s * 256 + c0;
             // the stage's lse2/Delta vectors were stored by the producer lanes before their
             // arrive on stage_full: wait on it here too, so those stores are visible
             ok = mbar_wait_warp(bar(L::kBarFull + s), (it / kBwdStages) & 1, abort_flag,
@@ -280,16 +374,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (!ok) break;
             tc_fence_after();
             // P^T row: p[q] = exp2(c*s - lse2_q)
-            float pr[128];
+            float pr[64];
             {
-                uint32_t r[128];
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc)
-                    tmem_ld32(lane_base + t_s + cc * 32,
-                              *reinterpret_cast<uint32_t(*)[32]>(&r[cc * 32]));
+                uint32_t r[64];
+                tmem_ld32(lane_base + t_s + c0, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                tmem_ld32(lane_base + t_s + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
                 tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(bar(L::kBarSFree));  // S^T(it+1) may now be formed over it
 #pragma unroll
-                for (int q = 0; q < 128; q += 4) {
+                for (int q = 0; q < 64; q += 4) {
                     const float4 l4 = *reinterpret_cast<const float4*>(vec + q);
                     pr[q] = ex2_approx(fmaf(__uint_as_float(r[q]), c, -l4.x));
                     pr[q + 1] = ex2_approx(fmaf(__uint_as_float(r[q + 1]), c, -l4.y));
@@ -299,51 +393,64 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             if (p.causal && it_tile(it) == j) {  // diagonal tile: query q sees key `row` iff q >= row
 #pragma unroll
-                for (int q = 0; q < 128; ++q) pr[q] = q < row ? 0.f : pr[q];
+                for (int q = 0; q < 64; ++q) pr[q] = c0 + q < row ? 0.f : pr[q];
             }
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int x = 0; x < 32; ++x) pk[x] = pack_bf16x2(pr[h * 64 + 2 * x], pr[h * 64 + 2 * x + 1]);
-                tmem_st32(lane_base + t_s + h * 32, pk);
+            // P^T row -> bf16 -> panel `half` of the P^T tile (128B swizzle, K-major operand),
+            // once dV(it-1) has finished reading the previous P^T
+            if (it > 0) {
+                ok = mbar_wait_warp(bar(L::kBarPFree), (it - 1) & 1, abort_flag, status_word);
+                if (!ok) break;
             }
-            tmem_wait_st();
-            tc_fence_before();
+            {
+                const uint32_t prow = sbase + L::kPt + half * L::kPanelBytes + row * 128;
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch)
+                    st_shared_v4(prow + ((ch ^ (row & 7)) << 4),
+                                 pack_bf16x2(pr[8 * ch], pr[8 * ch + 1]),
+                                 pack_bf16x2(pr[8 * ch + 2], pr[8 * ch + 3]),
+                                 pack_bf16x2(pr[8 * ch + 4], pr[8 * ch + 5]),
+                                 pack_bf16x2(pr[8 * ch + 6], pr[8 * ch + 7]));
+            }
+            fence_proxy_async_smem();
             mbar_arrive(bar(L::kBarP));
             // dS^T row: ds[q] = p[q] (dp[q] - Delta_q), in 32-column chunks; chunk cc's packed
-            // result lands in dP^T columns already read (16cc .. 16cc+15 < 32cc + 32).
+            // result lands in this warp's dP^T columns already read (c0+16cc .. < c0+32cc+32).
             ok = mbar_wait_warp(bar(L::kBarDP), it & 1, abort_flag, status_word);
             if (!ok) break;
             tc_fence_after();
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
+            for (int cc = 0; cc < 2; ++cc) {
                 uint32_t r[32];
-                tmem_ld32(lane_base + t_dp + cc * 32, r);
+                tmem_ld32(lane_base + t_dp + c0 + cc * 32, r);
                 tmem_wait_ld();
                 uint32_t pk[16];
 #pragma unroll
-                for (int x = 0; x < 16; ++x) {
+                for (int x = 0; x < 16; x += 2) {
                     const int q = cc * 32 + 2 * x;
-                    const float d0 = pr[q] * (__uint_as_float(r[2 * x]) - vec[128 + q]);
-                    const float d1 = pr[q + 1] * (__uint_as_float(r[2 * x + 1]) - vec[128 + q + 1]);
-                    pk[x] = pack_bf16x2(d0, d1);
+                    const float4 d4 = *reinterpret_cast<const float4*>(vec + 128 + q);
+                    pk[x] = pack_bf16x2(pr[q] * (__uint_as_float(r[2 * x]) - d4.x),
+                                        pr[q + 1] * (__uint_as_float(r[2 * x + 1]) - d4.y));
+                    pk[x + 1] = pack_bf16x2(pr[q + 2] * (__uint_as_float(r[2 * x + 2]) - d4.z),
+                                            pr[q + 3] * (__uint_as_float(r[2 * x + 3]) - d4.w));
                 }
-                tmem_st16(lane_base + t_dp + cc * 16, pk);
+                tmem_st16(lane_base + t_dp + c0 + cc * 16, pk);
             }
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bar(L::kBarDS));
         }
-        // epilogue: dK = sm_scale * acc, dV = acc -> bf16 -> smem (over K_j, V_j) -> TMA store
+        // epilogue: dK = sm_scale * acc (warps 0-3), dV = acc (warps 4-7) -> bf16 -> smem (over
+        // K_j, V_j) -> TMA store
         if (ok) ok = mbar_wait_warp(bar(L::kBarDone), 0, abort_flag, status_word);
         if (ok) {
             tc_fence_after();
-            stage_rows_bf16<D>(sbase + L::kRes0, lane_base + t_dk, row, p.sm_scale);
-            stage_rows_bf16<D>(sbase + L::kRes1, lane_base + t_dv, row, 1.0f);
+            if (half == 0)
+                stage_rows_bf16<D>(sbase + L::kRes0, lane_base + t_dk, row, p.sm_scale, 0, D / 32);
+            else
+                stage_rows_bf16<D>(sbase + L::kRes1, lane_base + t_dv, row, 1.0f, 0, D / 32);
         }
         fence_proxy_async_smem();
-        named_barrier_sync(1, 128);
+        named_barrier_sync(1, kBwdEwThreads);
         if (ok && warp == 0 && lane == 0) {
             for (int h = 0; h < kPanels; ++h) {
                 tma_store_4d(&tmap_dk, sbase + L::kRes0 + h * L::kPanelBytes, h * 64, j * 128, hkv, b);
@@ -396,11 +503,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(bar(L::kBarRes), 1);
         for (int s = 0; s < kBwdStages; ++s) {
             mbar_init(bar(L::kBarFull + s), 1);
-            mbar_init(bar(L::kBarEmpty + s), 1);
+            mbar_init(bar(L::kBarEmpty + s), 2);  // one release per issuer
         }
         mbar_init(bar(L::kBarS), 1);
+        mbar_init(bar(L::kBarS + 1), 1);
         mbar_init(bar(L::kBarDP), 1);
-        mbar_init(bar(L::kBarDS), 128);
+        mbar_init(bar(L::kBarDS), kBwdEwThreads);
         mbar_init(bar(L::kBarDone), 1);
         *abort_flag = 0;
         fence_mbarrier_init();
@@ -414,7 +522,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t t_s = tmem, t_dp = tmem + 128, t_dq = tmem + 256;
+    // S is double-buffered (S(it+1) is formed while the elementwise warps work on S(it)); dS is
+    // written over the S buffer it came from.
+    const uint32_t t_s0 = tmem, t_dp = tmem + 128, t_dq = tmem + 256, t_s1 = tmem + 384;
 
     if (warp == kBwdLoadWarp) {
         if (lane == 0) {
@@ -428,7 +538,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int it = 0; it < n_it; ++it) {
                 const int s = it % kBwdStages;
                 const uint32_t ph = (it / kBwdStages) & 1;
-                if (!mbar_wait_bounded(bar(L::kBarEmpty + s), ph ^ 1u, abort_flag, status_word))
+                if (!mbar_wait_bounded<true>(bar(L::kBarEmpty + s), ph ^ 1u, abort_flag, status_word))
                     break;
                 const uint32_t st = sbase + L::kStage + s * 2 * L::kTileBytes;
                 mbar_arrive_expect_tx(bar(L::kBarFull + s), 2 * L::kTileBytes);
@@ -441,82 +551,110 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
         }
         __syncwarp();
-    } else if (warp == kBwdMmaWarp) {
-        bool ok = mbar_wait_warp(bar(L::kBarRes), 0, abort_flag, status_word);
+    } else if (warp == kBwdMmaWarp || warp == kBwdMmaWarpB) {
+        // A: S(it+1) = Q_i K_(it+1)^T ahead, then dQ += dS(it) K_it once dS(it) is ready;
+        // B: dP(it) = dO_i V_it^T, each after the elementwise warps have read the previous one.
+        const bool chain_a = warp == kBwdMmaWarp;
+        bool ok = mbar_wait_warp<true>(bar(L::kBarRes), 0, abort_flag, status_word);
         const uint32_t qa = sbase + L::kRes0, da = sbase + L::kRes1;
-        for (int it = 0; ok && it < n_it; ++it) {
-            const int s = it % kBwdStages;
-            const uint32_t ph = (it / kBwdStages) & 1;
-            ok = mbar_wait_warp(bar(L::kBarFull + s), ph, abort_flag, status_word);
-            if (!ok) break;
+        auto stage_k = [&](int it) { return sbase + L::kStage + (it % kBwdStages) * 2 * L::kTileBytes; };
+        auto wait_full = [&](int it) {
+            const bool w = mbar_wait_warp<true>(bar(L::kBarFull + it % kBwdStages),
+                                          (it / kBwdStages) & 1, abort_flag, status_word);
             tc_fence_after();
-            const uint32_t ka = sbase + L::kStage + s * 2 * L::kTileBytes;
-            const uint32_t va = ka + L::kTileBytes;
+            return w;
+        };
+        auto s_mma = [&](int it) {  // S(it) into buffer it&1
+            const uint32_t ka = stage_k(it);
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {  // S = Q_i K_j^T
+            for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t off = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
-                mma_bf16_ss_warp(t_s, smem_desc_sw128(qa + off, 16, 1024),
+                mma_bf16_ss_warp((it & 1) ? t_s1 : t_s0, smem_desc_sw128(qa + off, 16, 1024),
                                  smem_desc_sw128(ka + off, 16, 1024), kIdescS, kk > 0);
             }
-            mma_commit_warp(bar(L::kBarS));
+            mma_commit_warp(bar(L::kBarS + (it & 1)));
+        };
+        if (chain_a) {
+            if (ok && n_it > 0) ok = wait_full(0);
+            if (ok && n_it > 0) s_mma(0);
+            for (int it = 0; ok && it < n_it; ++it) {
+                if (it + 1 < n_it) {  // stage it+1 is free of it-1 (both chains released it)
+                    ok = wait_full(it + 1);
+                    if (!ok) break;
+                    s_mma(it + 1);
+                }
+                ok = mbar_wait_warp<true>(bar(L::kBarDS), it & 1, abort_flag, status_word);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t ka = stage_k(it), ts = (it & 1) ? t_s1 : t_s0;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {  // dP = dO_i V_j^T
-                const uint32_t off = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
-                mma_bf16_ss_warp(t_dp, smem_desc_sw128(da + off, 16, 1024),
-                                 smem_desc_sw128(va + off, 16, 1024), kIdescS, kk > 0);
+                for (int kk = 0; kk < 8; ++kk)  // dQ += dS K_j  (K = 128 keys)
+                    mma_bf16_ts_warp(t_dq, ts + packed_col(kk),
+                                     smem_desc_sw128(ka + kk * 2048, L::kPanelBytes, 1024),
+                                     kIdescAcc, (it > 0 || kk > 0) ? 1u : 0u);
+                mma_commit_warp(bar(L::kBarEmpty + it % kBwdStages));
             }
-            mma_commit_warp(bar(L::kBarDP));
-            ok = mbar_wait_warp(bar(L::kBarDS), it & 1, abort_flag, status_word);
-            if (!ok) break;
-            tc_fence_after();
+            if (ok) mma_commit_warp(bar(L::kBarDone));
+        } else {
+            for (int it = 0; ok && it < n_it; ++it) {
+                ok = wait_full(it);
+                if (!ok) break;
+                if (it > 0) {  // dP(it) overwrites dP(it-1): the elementwise warps must have read it
+                    ok = mbar_wait_warp<true>(bar(L::kBarDS), (it - 1) & 1, abort_flag, status_word);
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+                const uint32_t va = stage_k(it) + L::kTileBytes;
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)  // dQ += dS K_j  (K = 128 keys)
-                mma_bf16_ts_warp(t_dq, t_s + kk * 8,
-                                 smem_desc_sw128(ka + kk * 2048, L::kPanelBytes, 1024), kIdescAcc,
-                                 (it > 0 || kk > 0) ? 1u : 0u);
-            mma_commit_warp(bar(L::kBarEmpty + s));
+                for (int kk = 0; kk < D / 16; ++kk) {  // dP = dO_i V_j^T
+                    const uint32_t off = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
+                    mma_bf16_ss_warp(t_dp, smem_desc_sw128(da + off, 16, 1024),
+                                     smem_desc_sw128(va + off, 16, 1024), kIdescS, kk > 0);
+                }
+                mma_commit_warp(bar(L::kBarDP));
+                mma_commit_warp(bar(L::kBarEmpty + it % kBwdStages));
+            }
         }
-        if (ok) mma_commit_warp(bar(L::kBarDone));
         __syncwarp();
     } else {
-        // elementwise warps 0-3: one thread per query row of tile i
-        const int row = warp * 32 + lane;
+        // elementwise warps 0-7: query row `row` of tile i, keys c0 .. c0+63 of the key tile
+        const int quarter = warp & 3, half = warp >> 2;
+        const int row = quarter * 32 + lane;
         const int row_g = i * 128 + row;
-        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+        const int c0 = half * 64;
         const float c = p.scale_log2;
         const size_t rix = static_cast<size_t>(bh) * p.N + row_g;
         const float lse2 = row_g < p.N ? p.lse[rix] * kLog2e : 0.f;
         const float dlt = row_g < p.N ? p.delta[rix] : 0.f;
         bool ok = true;
         for (int it = 0; it < n_it; ++it) {
-            ok = mbar_wait_warp(bar(L::kBarS), it & 1, abort_flag, status_word);
+            const uint32_t ts = (it & 1) ? t_s1 : t_s0;
+            ok = mbar_wait_warp(bar(L::kBarS + (it & 1)), (it >> 1) & 1, abort_flag, status_word);
             if (!ok) break;
             tc_fence_after();
-            float pr[128];
+            float pr[64];
             {
-                uint32_t r[128];
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc)
-                    tmem_ld32(lane_base + t_s + cc * 32,
-                              *reinterpret_cast<uint32_t(*)[32]>(&r[cc * 32]));
+                uint32_t r[64];
+                tmem_ld32(lane_base + ts + c0, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                tmem_ld32(lane_base + ts + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
                 tmem_wait_ld();
 #pragma unroll
-                for (int k = 0; k < 128; ++k)
+                for (int k = 0; k < 64; ++k)
                     pr[k] = ex2_approx(fmaf(__uint_as_float(r[k]), c, -lse2));
             }
             if (p.causal && it == i) {  // diagonal tile: key k visible to query `row` iff k <= row
 #pragma unroll
-                for (int k = 0; k < 128; ++k) pr[k] = k > row ? 0.f : pr[k];
+                for (int k = 0; k < 64; ++k) pr[k] = c0 + k > row ? 0.f : pr[k];
             }
             ok = mbar_wait_warp(bar(L::kBarDP), it & 1, abort_flag, status_word);
             if (!ok) break;
             tc_fence_after();
-            // dS in 32-column chunks over the dP columns already read; packed dS goes over S
-            // (columns 16cc .. 16cc+15; S was fully read above).
+            // dS in 32-column chunks; the packed dS goes over this warp's S columns (all read)
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
+            for (int cc = 0; cc < 2; ++cc) {
                 uint32_t r[32];
-                tmem_ld32(lane_base + t_dp + cc * 32, r);
+                tmem_ld32(lane_base + t_dp + c0 + cc * 32, r);
                 tmem_wait_ld();
                 uint32_t pk[16];
 #pragma unroll
@@ -525,7 +663,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     pk[x] = pack_bf16x2(pr[k] * (__uint_as_float(r[2 * x]) - dlt),
                                         pr[k + 1] * (__uint_as_float(r[2 * x + 1]) - dlt));
                 }
-                tmem_st16(lane_base + t_s + cc * 16, pk);
+                tmem_st16(lane_base + ts + c0 + cc * 16, pk);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -534,10 +672,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (ok) ok = mbar_wait_warp(bar(L::kBarDone), 0, abort_flag, status_word);
         if (ok) {
             tc_fence_after();
-            stage_rows_bf16<D>(sbase + L::kRes0, lane_base + t_dq, row, p.sm_scale);
+            stage_rows_bf16<D>(sbase + L::kRes0, lane_base + t_dq, row, p.sm_scale,
+                               half * (D / 64), (half + 1) * (D / 64));
         }
         fence_proxy_async_smem();
-        named_barrier_sync(1, 128);
+        named_barrier_sync(1, kBwdEwThreads);
         if (ok && warp == 0 && lane == 0) {
             for (int h = 0; h < kPanels; ++h)
                 tma_store_4d(&tmap_dq, sbase + L::kRes0 + h * L::kPanelBytes, h * 64, i * 128, hq, b);

@@ -103,6 +103,12 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
+// Raise the current phase's expected transaction bytes without arriving.
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
 // Non-suspending poll of phase `parity` (test_wait: measured to wake the critical-path warps a
 // little sooner than the suspending try_wait).
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
@@ -117,22 +123,40 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return done != 0;
 }
 
+// Suspending poll: the thread may wait inside the instruction (up to a hardware time limit), so
+// a role that is off the critical path leaves the issue slots of its SM sub-partition to the warps
+// that share it.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
 // Device-side failure flags (OR-ed into the library's status word).
 constexpr unsigned kDevTimeout = 1u;
+constexpr unsigned kDevSmemAlign = 2u;  // dynamic shared memory not 1024-byte aligned
 
 // Time a wait may take before the CTA gives up (1 s; a healthy wait takes microseconds).
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
 // Wait for phase `parity` of `bar` to complete.  Returns false (and raises the CTA's abort flag and
 // the global status word) if the wait exceeds kWaitLimitNs, or returns false early if another role
-// of this CTA already aborted.  Never spins forever.
+// of this CTA already aborted.  Never spins forever.  kSleep selects the suspending poll.
+template <bool kSleep = false>
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   volatile int* abort_flag,
                                                   unsigned int* status_word) {
-    if (mbar_try_wait(bar, parity)) return true;
+    auto poll = [&]() { return kSleep ? mbar_try_wait_sleep(bar, parity) : mbar_try_wait(bar, parity); };
+    if (poll()) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (poll()) return true;
         if ((it & 31u) == 0u) {
             if (*abort_flag) return false;
             if (globaltimer_ns() - t0 > kWaitLimitNs) {
@@ -146,10 +170,11 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 
 // Warp-uniform version: every lane waits, and the warp proceeds only if every lane succeeded, so
 // the warp-collective tcgen05 instructions that follow are executed by all lanes or by none.
+template <bool kSleep = false>
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity,
                                                volatile int* abort_flag,
                                                unsigned int* status_word) {
-    const bool ok = mbar_wait_bounded(bar, parity, abort_flag, status_word);
+    const bool ok = mbar_wait_bounded<kSleep>(bar, parity, abort_flag, status_word);
     return __all_sync(0xffffffffu, ok);
 }
 

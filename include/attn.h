@@ -44,7 +44,7 @@ typedef enum {
     ATTN_ERR_HEADDIM = -4,  /* D is not a multiple of 8 in [8, 128] */
     ATTN_ERR_ALIGN = -5,    /* a tensor pointer is not 16-byte aligned */
     ATTN_ERR_SCALE = -6,    /* sm_scale is not finite and positive */
-    ATTN_ERR_ARCH = -7,     /* the current device is not compute capability 10.3 (sm_103) */
+    ATTN_ERR_ARCH = -7,     /* the device is not sm_103, or its shared memory is misaligned */
     ATTN_ERR_CUDA = -8,     /* a CUDA runtime/driver call failed; see attn_last_cuda_error() */
     ATTN_ERR_TIMEOUT = -9,  /* a device-side bounded wait expired (reported by attn_debug_status) */
     ATTN_ERR_MEMORY = -10,  /* a pointer is not device memory of the current device */
@@ -169,7 +169,8 @@ int attn_last_cuda_error(void);
 /*
  * attn_debug_status - synchronise `stream`, then read and clear the device status word.
  * Returns ATTN_OK if no kernel of this library recorded a failure since the last call,
- * ATTN_ERR_TIMEOUT if a device-side bounded wait expired, or ATTN_ERR_CUDA if the
+ * ATTN_ERR_TIMEOUT if a device-side bounded wait expired, ATTN_ERR_ARCH if a kernel found its
+ * dynamic shared memory not 1024-byte aligned (it then did no work), or ATTN_ERR_CUDA if the
  * synchronisation itself failed.  The status word is shared by all streams of the device.
  */
 int attn_debug_status(void* stream);
