@@ -11,6 +11,12 @@ The shapes are the test shapes of "Attention Kernel 实现与正确性验证" (w
 (GQA-4, GQA-8, MHA, MQA), a tiny GQA-2 case, an outlier variant of the MHA case that stresses the
 running-maximum rescale, and the long-context sweep of section 1.4 (N = 8K..32K) with 8 KV heads.
 The pages measure no public dataset; these iid N(0,1) inputs stand in for activations.
+
+Absorbed MLA decode (``MlaWorkload``, the second workload): the DeepSeek-V3 widths of section 2.3
+of the same page (d_c = 512 compressed, d_r = 64 RoPE, d_nope = 128, so sm_scale = 1/sqrt(192)),
+128 heads, one decode query per head, T cached tokens.  Recipe: one generator per workload, draw
+``randn`` float32 q [B, H, d_c + d_r] then kv [B, T, d_c + d_r], round each to bf16.  q stands for
+q_nope W_uk concatenated with q_pe, kv for c_kv concatenated with k_pe.
 """
 from __future__ import annotations
 
@@ -71,6 +77,57 @@ LONG = {n: Workload(f"long-gqa8-causal-n{n}", 1, 32, 8, n, 128, True, s)
 CONFIGS = [TINY_NONCAUSAL, TINY_CAUSAL, GQA4_CAUSAL, GQA8_CAUSAL, MHA, MHA_OUTLIER, MQA,
            *LONG.values(), FEWHEADS]
 BY_NAME = {w.name: w for w in CONFIGS}
+
+
+@dataclass(frozen=True)
+class MlaWorkload:
+    name: str
+    B: int
+    H: int
+    T: int
+    seed: int
+    d_c: int = 512
+    d_r: int = 64
+    d_nope: int = 128
+
+    @property
+    def d_qk(self) -> int:
+        return self.d_c + self.d_r
+
+    @property
+    def sm_scale(self) -> float:
+        """The un-absorbed head width sets the scale: 1/sqrt(d_nope + d_r)."""
+        return 1.0 / math.sqrt(self.d_nope + self.d_r)
+
+    @property
+    def flops(self) -> float:
+        """Algorithmic FLOPs of the compressed-space core: scores (2*d_qk) and output (2*d_c) per
+        head and token."""
+        return 2.0 * self.B * self.H * self.T * (self.d_qk + self.d_c)
+
+    @property
+    def bytes(self) -> int:
+        """Algorithmic HBM bytes: the cache and the queries read once (bf16), out_c written
+        (bf16), LSE written (fp32)."""
+        return 2 * self.B * self.T * self.d_qk + 2 * self.B * self.H * self.d_qk \
+            + 2 * self.B * self.H * self.d_c + 4 * self.B * self.H
+
+
+MLA_TINY = MlaWorkload("mla-tiny", 1, 16, 200, 30)
+MLA_RAGGED = MlaWorkload("mla-ragged", 2, 128, 777, 31)
+MLA_B1 = {t: MlaWorkload(f"mla-b1-t{t}", 1, 128, t, s) for t, s in ((4096, 32), (16384, 33))}
+MLA_B32 = MlaWorkload("mla-b32-t4096", 32, 128, 4096, 34)
+MLA_CONFIGS = [MLA_TINY, MLA_RAGGED, *MLA_B1.values(), MLA_B32]
+
+
+def make_mla(w: MlaWorkload, device="cpu"):
+    """bf16 q [B, H, d_c + d_r] and kv [B, T, d_c + d_r] for MLA workload ``w``."""
+    g = torch.Generator().manual_seed(w.seed)
+    q = torch.randn(w.B, w.H, w.d_qk, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    kv = torch.randn(w.B, w.T, w.d_qk, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    if device != "cpu":
+        q, kv = q.to(device), kv.to(device)
+    return q, kv
 
 
 def make_qkv(w: Workload, device="cpu"):

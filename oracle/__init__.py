@@ -17,6 +17,8 @@ skillmd.com, GQA and causal variants; "Flash Attention 与 Kernel 优化", fangp
     LSE  = m + ln sum_j exp(s_j - m)
 
 ``attn_bwd_ref`` gives the gradients of the same definition (the pages' backward by recompute).
+``mla_decode_ref`` (``mla_oracle.c``) is absorbed MLA decode in the compressed space ("Attention
+Kernel 实现与正确性验证", walkerchi.com, sections 2.1 and 2.2).
 """
 from __future__ import annotations
 
@@ -29,6 +31,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "attn_oracle.c")
+_SRCS = [_SRC, os.path.join(_HERE, "mla_oracle.c")]
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 
@@ -39,12 +42,13 @@ _lock = threading.Lock()
 def build(force: bool = False) -> str:
     """Compile ``attn_oracle.c`` into ``oracle/_build/liboracle.so`` (gcc, -O2, no fast-math)."""
     os.makedirs(_BUILD_DIR, exist_ok=True)
-    fresh = os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)
+    fresh = os.path.exists(_LIB_PATH) and all(
+        os.path.getmtime(_LIB_PATH) >= os.path.getmtime(src) for src in _SRCS)
     if fresh and not force:
         return _LIB_PATH
     tmp = f"{_LIB_PATH}.{os.getpid()}.tmp"
     cmd = ["gcc", "-std=c11", "-O2", "-fno-fast-math", "-ffp-contract=off", "-fPIC", "-shared",
-           "-pthread", "-o", tmp, _SRC, "-lm"]
+           "-pthread", "-o", tmp, *_SRCS, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -71,6 +75,9 @@ def _load():
                                                 c_int, c_int, c_int, ctypes.c_double, f64p, f64p,
                                                 f64p, c_int]
             lib.oracle_attn_bwd_f64.restype = c_int
+            lib.oracle_mla_decode_f64.argtypes = [f64p, f64p, c_int, c_int, c_int, c_int, c_int,
+                                                  ctypes.c_double, f64p, f64p, c_int]
+            lib.oracle_mla_decode_f64.restype = c_int
             lib.oracle_default_threads.argtypes = []
             lib.oracle_default_threads.restype = c_int
             _lib = lib
@@ -177,3 +184,33 @@ def attn_bwd_ref(q, k, v, dout, causal: bool, sm_scale: float, n_threads: int = 
     if st != 0:
         raise ValueError(f"oracle_attn_bwd_f64 rejected its arguments (status {st})")
     return dq, dk, dv
+
+
+def _f64(x) -> np.ndarray:
+    """float64 C-contiguous copy of a torch tensor (any float dtype) or a numpy array."""
+    if isinstance(x, np.ndarray):
+        return np.ascontiguousarray(x, dtype=np.float64)
+    return np.ascontiguousarray(x.detach().cpu().double().numpy())
+
+
+def mla_decode_ref(q, kv, d_c: int, sm_scale: float, n_threads: int = 0):
+    """Absorbed MLA decode oracle (``mla_oracle.c``), float64.
+
+    ``q`` [B, H, d_c + d_r] holds q_abs (the query with W_uk folded in) then q_pe; ``kv``
+    [B, T, d_c + d_r] holds c_kv then k_pe.  Returns out_c [B, H, d_c] (compressed space) and
+    LSE [B, H].  Any float dtype; bf16 inputs are widened exactly."""
+    lib = _load()
+    qd, kvd = _f64(q), _f64(kv)
+    if qd.ndim != 3 or kvd.ndim != 3 or qd.shape[0] != kvd.shape[0] or qd.shape[2] != kvd.shape[2]:
+        raise ValueError(f"q must be [B,H,dq] and kv [B,T,dq]: {qd.shape} {kvd.shape}")
+    B, H, dq = qd.shape
+    T = kvd.shape[1]
+    d_r = dq - d_c
+    out = np.zeros((B, H, d_c), dtype=np.float64)
+    lse = np.zeros((B, H), dtype=np.float64)
+    st = lib.oracle_mla_decode_f64(_ptr(qd, ctypes.c_double), _ptr(kvd, ctypes.c_double), B, H, T,
+                                   d_c, d_r, float(sm_scale), _ptr(out, ctypes.c_double),
+                                   _ptr(lse, ctypes.c_double), int(n_threads))
+    if st != 0:
+        raise ValueError(f"oracle_mla_decode_f64 rejected its arguments (status {st})")
+    return out, lse

@@ -60,3 +60,16 @@ def test_registry_matches_the_five_configurations():
     # FLOP convention: 4*B*Hq*N^2*D, halved when causal
     assert wl.LONG[8192].flops == 4 * 32 * 8192 ** 2 * 128 / 2
     assert wl.MHA.flops == 4 * 32 * 512 ** 2 * 128
+
+
+def test_mla_workloads_shapes_scale_and_determinism():
+    w = wl.MLA_B1[4096]
+    assert (w.B, w.H, w.T, w.d_c, w.d_r, w.d_qk) == (1, 128, 4096, 512, 64, 576)
+    assert abs(w.sm_scale - 192 ** -0.5) < 1e-15  # d_nope + d_r, not the absorbed width
+    q, kv = wl.make_mla(wl.MLA_TINY)
+    assert q.shape == (1, 16, 576) and kv.shape == (1, 200, 576)
+    assert q.dtype == kv.dtype == torch.bfloat16
+    q2, kv2 = wl.make_mla(wl.MLA_TINY)
+    assert torch.equal(q, q2) and torch.equal(kv, kv2)
+    assert w.flops == 2 * 128 * 4096 * (576 + 512)
+    assert w.bytes == 2 * 4096 * 576 + 2 * 128 * 576 + 2 * 128 * 512 + 4 * 128
