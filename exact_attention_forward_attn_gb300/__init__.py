@@ -152,6 +152,55 @@ def attn_fwd_splitkv(q, k, v, causal: bool = False, sm_scale: float | None = Non
     return out, lse
 
 
+MLA_D_C = 512
+MLA_D_R = 64
+
+
+def mla_decode_num_splits(B: int, H: int, T: int) -> int:
+    """Token-axis splits ``mla_decode`` picks by default."""
+    return int(_lib.load().attn_mla_decode_num_splits(B, H, T))
+
+
+def mla_decode_workspace_bytes(B: int, H: int, T: int, num_splits: int = 0) -> int:
+    return int(_lib.load().attn_mla_decode_workspace_bytes(B, H, T, num_splits))
+
+
+def mla_decode(q, kv, sm_scale: float, num_splits: int = 0, workspace=None, out=None, lse=None):
+    """Absorbed MLA decode: q [B, H, 576] (q_abs | q_pe), kv [B, T, 576] (c_kv | k_pe), bf16 CUDA
+    tensors.  Returns out_c [B, H, 512] (bf16, compressed space) and LSE [B, H] (fp32).
+    ``sm_scale`` is the un-absorbed one, 1/sqrt(d_nope + d_r)."""
+    import torch
+
+    for t in (q, kv):
+        if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
+            raise TypeError("q and kv must be CUDA tensors")
+        if t.dtype != torch.bfloat16 or not t.is_contiguous() or t.dim() != 3:
+            raise ValueError("q and kv must be contiguous 3-D bf16 tensors")
+    if q.device != kv.device:
+        raise ValueError("q and kv must be on the same device")
+    B, H, dq = q.shape
+    if kv.shape[0] != B or kv.shape[2] != dq:
+        raise ValueError(f"kv must be [B, T, {dq}], got {tuple(kv.shape)}")
+    T = kv.shape[1]
+    if out is None:
+        out = torch.empty(B, H, MLA_D_C, dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty(B, H, dtype=torch.float32, device=q.device)
+    lib = _lib.load()
+    with torch.cuda.device(q.device):
+        need = mla_decode_workspace_bytes(B, H, T, num_splits)
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        ws_ptr = workspace.data_ptr() if workspace is not None else None
+        ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+        st = lib.attn_mla_decode(q.data_ptr(), kv.data_ptr(), out.data_ptr(), lse.data_ptr(), B,
+                                 H, T, MLA_D_C, dq - MLA_D_C, float(sm_scale), int(num_splits),
+                                 ws_ptr, ws_bytes, _stream_handle(q.device))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_mla_decode")
+    return out, lse
+
+
 def attn_bwd(q, k, v, out, lse, dout, causal: bool = False, sm_scale: float | None = None,
              dq=None, dk=None, dv=None, workspace=None):
     """Gradients (dq, dk, dv) of ``attn_fwd`` by recompute from its ``out`` and ``lse``, for the

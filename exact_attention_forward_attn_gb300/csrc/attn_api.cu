@@ -18,6 +18,7 @@
 #include "attn.h"
 #include "attn_bwd_kernel.cuh"
 #include "attn_fwd_kernel.cuh"
+#include "mla_decode_kernel.cuh"
 
 using namespace gb300attn;
 
@@ -165,6 +166,9 @@ int device_state(int dev, DeviceState** out) {
         if (e == cudaSuccess) e = opt_in_smem<128, true>();
         if (e == cudaSuccess) e = opt_in_bwd_smem<64>();
         if (e == cudaSuccess) e = opt_in_bwd_smem<128>();
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     MlaSmem::kAlloc);
         if (e != cudaSuccess) { st.status = ATTN_ERR_CUDA; st.cuda_error = e; }
     });
     if (st.status == ATTN_ERR_CUDA) t_last_cuda_error = st.cuda_error;
@@ -586,13 +590,172 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
                                      ds->status_word, s);
 }
 
+// ------------------------------------------------------------------------------------------------
+// Absorbed MLA decode ("Attention Kernel 实现与正确性验证", walkerchi.com, sections 2.1-2.4)
+// ------------------------------------------------------------------------------------------------
+namespace {
+
+// 3-D view [B, rows, 576] of a contiguous bf16 tensor; box = 64 columns x box_rows rows, 128B
+// swizzle.  Rows past `rows` are zero-filled on load.
+bool make_mla_map(CUtensorMap* map, const void* base, int64_t B, int64_t rows, int box_rows) {
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kMlaDqk), static_cast<cuuint64_t>(rows),
+                                static_cast<cuuint64_t>(B)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kMlaDqk * 2),
+                                   static_cast<cuuint64_t>(rows * kMlaDqk * 2)};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+    const cuuint32_t elem_strides[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+               box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+int64_t mla_items(int B, int H) {
+    return static_cast<int64_t>(B) * ((H + kMlaHeads - 1) / kMlaHeads) * 2;
+}
+
+int64_t mla_tiles(int T) { return (static_cast<int64_t>(T) + kMlaBN - 1) / kMlaBN; }
+
+// Splits of the token axis.  Each CTA costs its tiles plus, when split, writing its fp32 partial
+// (about two tiles' worth of traffic); CTAs run in waves of one per SM.  Pick the split count with
+// the least waves x per-CTA cost (fewest splits on ties).
+int mla_heuristic_splits(int64_t items, int64_t n_tiles, int num_sms) {
+    const int64_t max_s = std::min<int64_t>(n_tiles, kMaxSplits);
+    int best = 1;
+    int64_t best_cost = -1;
+    for (int64_t s = 1; s <= max_s; ++s) {
+        const int64_t waves = (items * s + num_sms - 1) / num_sms;
+        const int64_t per_cta = (n_tiles + s - 1) / s + (s > 1 ? 2 : 0);
+        const int64_t cost = waves * per_cta;
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = static_cast<int>(s);
+        }
+    }
+    return best;
+}
+
+int64_t mla_workspace_for(int B, int H, int n_splits) {
+    return static_cast<int64_t>(n_splits) * B * H * (kMlaDc + 1) * 4;
+}
+
+}  // namespace
+
+extern "C" int attn_mla_decode_num_splits(int B, int H, int T) {
+    if (B <= 0 || H <= 0 || T <= 0) return 1;
+    DeviceState* ds = nullptr;
+    if (current_device_state(&ds) != ATTN_OK) return 1;
+    return mla_heuristic_splits(mla_items(B, H), mla_tiles(T), ds->num_sms);
+}
+
+extern "C" size_t attn_mla_decode_workspace_bytes(int B, int H, int T, int num_splits) {
+    if (B <= 0 || H <= 0 || T <= 0 || num_splits < 0 || num_splits > kMaxSplits) return 0;
+    if (num_splits == 0) num_splits = attn_mla_decode_num_splits(B, H, T);
+    num_splits = static_cast<int>(std::min<int64_t>(num_splits, mla_tiles(T)));
+    if (num_splits <= 1) return 0;
+    return static_cast<size_t>(mla_workspace_for(B, H, num_splits));
+}
+
+extern "C" int attn_mla_decode(const void* q, const void* kv, void* out, float* lse, int B, int H,
+                               int T, int d_c, int d_r, float sm_scale, int num_splits,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+    if (B < 0 || H <= 0 || T <= 0) return ATTN_ERR_SHAPE;
+    if (d_c != kMlaDc || d_r != kMlaDr) return ATTN_ERR_HEADDIM;
+    if (!std::isfinite(sm_scale) || !(sm_scale > 0.f)) return ATTN_ERR_SCALE;
+    if (num_splits < 0 || num_splits > kMaxSplits) return ATTN_ERR_SPLITS;
+    if (B == 0) return ATTN_OK;
+    if (!q || !kv || !out || !lse) return ATTN_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(kv) |
+         reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(lse)) & 15u)
+        return ATTN_ERR_ALIGN;
+    const int64_t n_ht = (H + kMlaHeads - 1) / kMlaHeads;
+    const int64_t n_tiles = mla_tiles(T);
+    const int64_t items = mla_items(B, H);
+    const int64_t q_bytes = static_cast<int64_t>(B) * H * kMlaDqk * 2;
+    const int64_t kv_bytes = static_cast<int64_t>(B) * T * kMlaDqk * 2;
+    const int64_t o_bytes = static_cast<int64_t>(B) * H * kMlaDc * 2;
+    const int64_t lse_bytes = static_cast<int64_t>(B) * H * 4;
+    if (overlaps(out, o_bytes, q, q_bytes) || overlaps(out, o_bytes, kv, kv_bytes) ||
+        overlaps(out, o_bytes, lse, lse_bytes) || overlaps(lse, lse_bytes, q, q_bytes) ||
+        overlaps(lse, lse_bytes, kv, kv_bytes))
+        return ATTN_ERR_ALIAS;
+
+    // An explicit split count is checked against the workspace before any CUDA call; the
+    // default one needs the SM count first.
+    auto check_workspace = [&](int n_splits) {
+        if (items * n_splits > 0x7fffffffLL) return ATTN_ERR_SHAPE;
+        if (n_splits <= 1) return ATTN_OK;
+        const int64_t need = mla_workspace_for(B, H, n_splits);
+        if (!workspace) return ATTN_ERR_NULL;
+        if (reinterpret_cast<uintptr_t>(workspace) & 15u) return ATTN_ERR_ALIGN;
+        if (static_cast<int64_t>(workspace_bytes) < need) return ATTN_ERR_WORKSPACE;
+        if (overlaps(workspace, need, q, q_bytes) || overlaps(workspace, need, kv, kv_bytes) ||
+            overlaps(workspace, need, out, o_bytes) || overlaps(workspace, need, lse, lse_bytes))
+            return ATTN_ERR_ALIAS;
+        return ATTN_OK;
+    };
+    int n_splits = static_cast<int>(std::min<int64_t>(num_splits, n_tiles));
+    int st = num_splits > 0 ? check_workspace(n_splits) : ATTN_OK;
+    if (st != ATTN_OK) return st;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaSetDevice(dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    DeviceState* ds = nullptr;
+    st = device_state(dev, &ds);
+    if (st != ATTN_OK) return st;
+    if (num_splits == 0) {
+        n_splits = mla_heuristic_splits(items, n_tiles, ds->num_sms);
+        st = check_workspace(n_splits);
+        if (st != ATTN_OK) return st;
+    }
+    for (const void* ptr : {q, kv, static_cast<const void*>(out), static_cast<const void*>(lse)})
+        if (check_memory(ptr, dev) != ATTN_OK) return ATTN_ERR_MEMORY;
+    if (n_splits > 1 && check_memory(workspace, dev) != ATTN_OK) return ATTN_ERR_MEMORY;
+
+    CUtensorMap mq, mkv;
+    if (!make_mla_map(&mq, q, B, H, kMlaHeads) || !make_mla_map(&mkv, kv, B, T, kMlaBN))
+        return cuda_fail(cudaErrorInvalidValue);
+    MlaParams prm;
+    prm.B = B;
+    prm.H = H;
+    prm.T = T;
+    prm.n_ht = static_cast<int>(n_ht);
+    prm.n_tiles = static_cast<int>(n_tiles);
+    prm.n_splits = n_splits;
+    prm.scale_log2 = sm_scale * 1.4426950408889634f;
+    prm.out = static_cast<__nv_bfloat16*>(out);
+    prm.lse = lse;
+    prm.ws_o = n_splits > 1 ? static_cast<float*>(workspace) : nullptr;
+    prm.ws_lse = n_splits > 1 ? prm.ws_o + static_cast<int64_t>(n_splits) * B * H * kMlaDc : nullptr;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    mla_decode_kernel<<<static_cast<unsigned int>(items * n_splits), kMlaThreads, MlaSmem::kAlloc,
+                        s>>>(mq, mkv, prm, ds->status_word);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (n_splits > 1) {
+        const int64_t rows = static_cast<int64_t>(B) * H;
+        const int64_t rows_per_block = 4 / mla_merge_groups(n_splits);
+        mla_merge_kernel<<<static_cast<unsigned int>((rows + rows_per_block - 1) / rows_per_block),
+                           kMlaMergeThreads, 0, s>>>(
+            prm.ws_o, prm.ws_lse, prm.out, lse, static_cast<int>(rows), n_splits);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return ATTN_OK;
+}
+
 extern "C" const char* attn_status_string(int status) {
     switch (status) {
         case ATTN_OK: return "ok";
         case ATTN_ERR_NULL: return "a required pointer is NULL";
         case ATTN_ERR_SHAPE: return "invalid or overflowing shape (B, Hq, Hkv, N)";
         case ATTN_ERR_HEADS: return "Hq is not a multiple of Hkv";
-        case ATTN_ERR_HEADDIM: return "unsupported head dimension (D must be a multiple of 8 in [8, 128])";
+        case ATTN_ERR_HEADDIM:
+            return "unsupported head dimension (attention: D a multiple of 8 in [8, 128]; "
+                   "MLA decode: d_c = 512 and d_r = 64)";
         case ATTN_ERR_ALIGN: return "a pointer is not 16-byte aligned";
         case ATTN_ERR_SCALE: return "sm_scale must be finite and positive";
         case ATTN_ERR_ARCH: return "the current device is not sm_103 (GB300)";
@@ -601,7 +764,8 @@ extern "C" const char* attn_status_string(int status) {
         case ATTN_ERR_MEMORY: return "a pointer is not device memory of the current device";
         case ATTN_ERR_ALIAS: return "out/lse/workspace overlap an input or each other";
         case ATTN_ERR_SPLITS: return "num_splits must be in [0, 64]";
-        case ATTN_ERR_WORKSPACE: return "workspace smaller than attn_fwd_splitkv_workspace_bytes";
+        case ATTN_ERR_WORKSPACE:
+            return "workspace smaller than the entry point's *_workspace_bytes() figure";
         case ATTN_ERR_STRIDE:
             return "a stride is not a positive multiple of 8 elements (16 bytes) below 2^39";
         case ATTN_ERR_SCRATCH:

@@ -204,6 +204,46 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
 size_t attn_bwd_workspace_bytes(int B, int Hq, int N);
 
 /*
+ * attn_mla_decode - absorbed multi-head latent attention (MLA), one decode query per head.
+ *
+ * "Attention Kernel 实现与正确性验证" (walkerchi.com), section 2.1: W_uk is folded into the query
+ * (q_abs = q_nope W_uk), so the scores are taken in the compressed space against the cached c_kv
+ * plus the decoupled RoPE key k_pe, and no K or V is rebuilt; section 2.2 gives the reference
+ * (softmax over all cached tokens, no mask, output c_kv-weighted, then W_uv); section 2.4 splits
+ * the token axis (split-T) and merges with a safe softmax.  For batch b, head h, token t:
+ *   s_t = sm_scale * (q[b,h,0:d_c] . kv[b,t,0:d_c] + q[b,h,d_c:] . kv[b,t,d_c:])
+ *   out[b,h,:] = sum_t softmax_t(s) kv[b,t,0:d_c]        lse[b,h] = ln sum_t exp(s_t)
+ * The query absorption and the up-projection out W_uv^T are the caller's matrix products, like
+ * the projections around attn_fwd.
+ *
+ *   q         bf16 [B, H, d_c + d_r] contiguous: q_abs then q_pe per head.
+ *   kv        bf16 [B, T, d_c + d_r] contiguous: c_kv then k_pe per cached token (all heads).
+ *   out       bf16 [B, H, d_c] contiguous (written, compressed space).
+ *   lse       fp32 [B, H] (written, natural log).
+ *   d_c, d_r  must be 512 and 64 (the page's DeepSeek-V3 widths), else ATTN_ERR_HEADDIM.
+ *   sm_scale  finite, > 0; the un-absorbed head width sets it (1/sqrt(d_nope + d_r)).
+ *   num_splits  token-axis splits in [0, 64]; 0 picks attn_mla_decode_num_splits(B, H, T).
+ *               Clamped to the number of 64-token tiles.  With one split the workspace is unused.
+ *   workspace   device memory, 16-byte aligned, of at least
+ *               attn_mla_decode_workspace_bytes(B, H, T, num_splits) bytes when that is nonzero
+ *               (per-split fp32 partials); owned by the caller, contents ignored.
+ *   T >= 1 and H >= 1; B == 0 is a no-op.  Outputs, inputs and the workspace must not overlap.
+ *   Pointers are device pointers of the current device, owned by the caller.
+ *
+ * Returns ATTN_OK once enqueued (one kernel, plus a merge kernel when split), else a negative
+ * attn_status_t and nothing is written.  Device-side wait expiries go to attn_debug_status.
+ */
+int attn_mla_decode(const void* q, const void* kv, void* out, float* lse, int B, int H, int T,
+                    int d_c, int d_r, float sm_scale, int num_splits, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
+/* Split count attn_mla_decode picks for num_splits == 0 (1 for invalid sizes). */
+int attn_mla_decode_num_splits(int B, int H, int T);
+
+/* Workspace bytes attn_mla_decode needs for `num_splits` (0 = its own choice); 0 if none. */
+size_t attn_mla_decode_workspace_bytes(int B, int H, int T, int num_splits);
+
+/*
  * attn_fwd_test_stall - test hook for the failure-reporting path (not for computing anything).
  *
  * Runs attn_fwd, except that every CTA's producer withholds item `stall_item` (>= 0) of its K/V

@@ -30,7 +30,8 @@ def test_header_declares_the_boundary():
         ["attn_fwd", "attn_status_string", "attn_last_cuda_error", "attn_debug_status",
          "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_bytes", "attn_fwd_splitkv_num_splits",
          "attn_fwd_splitkv_noalloc", "attn_fwd_splitkv_noalloc_max_bytes", "attn_fwd_strided",
-         "attn_fwd_test_stall", "attn_bwd", "attn_bwd_workspace_bytes"])
+         "attn_fwd_test_stall", "attn_bwd", "attn_bwd_workspace_bytes", "attn_mla_decode",
+         "attn_mla_decode_num_splits", "attn_mla_decode_workspace_bytes"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -150,3 +151,37 @@ def test_strided_host_validation(lib, kw, status):
 def test_bwd_workspace_bytes(lib):
     assert lib.attn_bwd_workspace_bytes(2, 8, 1000) == 2 * 8 * 1000 * 4
     assert lib.attn_bwd_workspace_bytes(0, 8, 1000) == 0
+
+
+def _mla(lib, q=S, kv=S * 2, out=S * 4, lse=S * 5, B=1, H=128, T=4096, d_c=512, d_r=64,
+         scale=192 ** -0.5, splits=4, ws=S * 8, ws_bytes=1 << 30):
+    return lib.attn_mla_decode(q, kv, out, lse, B, H, T, d_c, d_r, ctypes.c_float(scale), splits,
+                               ws, ws_bytes, None)
+
+
+def test_mla_workspace_bytes(lib):
+    # n_splits * B * H * (512 + 1) fp32, splits clamped to the 64-token tiles
+    assert lib.attn_mla_decode_workspace_bytes(2, 128, 4096, 4) == 4 * 2 * 128 * 513 * 4
+    assert lib.attn_mla_decode_workspace_bytes(1, 16, 100, 8) == 2 * 1 * 16 * 513 * 4
+    assert lib.attn_mla_decode_workspace_bytes(1, 16, 64, 8) == 0  # one tile: no split
+    assert lib.attn_mla_decode_workspace_bytes(1, 16, 4096, 1) == 0
+    assert lib.attn_mla_decode_workspace_bytes(0, 16, 4096, 4) == 0
+    assert lib.attn_mla_decode_workspace_bytes(1, 16, 4096, 65) == 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=0), -1), (dict(lse=0), -1), (dict(ws=0), -1),
+    (dict(B=-1), -2), (dict(H=0), -2), (dict(T=0), -2),
+    (dict(d_c=256), -4), (dict(d_r=32), -4),
+    (dict(q=S + 8), -5), (dict(ws=S * 8 + 4), -5),
+    (dict(scale=0.0), -6), (dict(scale=float("nan")), -6),
+    (dict(out=S + 64), -11), (dict(ws=S * 2), -11),
+    (dict(splits=-1), -12), (dict(splits=65), -12),
+    (dict(ws_bytes=1000), -13),
+])
+def test_mla_host_validation(lib, kw, status):
+    assert _mla(lib, **kw) == status
+
+
+def test_mla_empty_batch_is_a_no_op(lib):
+    assert _mla(lib, B=0, q=0, kv=0, out=0, lse=0, ws=0, ws_bytes=0) == 0
