@@ -483,6 +483,48 @@ def main():
         if attn.device_status(dev) != 0:
             raise SystemExit("device status word reports an expired wait in the backward leg")
 
+    # ---- context: absorbed MLA decode (the second workload), one decode query per head --------
+    # HBM-bound at large batch: reported as GB/s of algorithmic bytes (cache + queries read once,
+    # out_c and LSE written) against the measured copy bandwidth.  The 256 MB flush before each
+    # launch keeps the cache out of L2 for the small batches.
+    mla = []
+    if not args.no_sweep and rank == 0:
+        hbm = float(peaks["hbm_gbs"])
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        lib = _lib.load()
+        sh = ctypes.c_void_p(stream.cuda_stream)
+        for wm in (wl.MLA_B1[4096], wl.MLA_B1[16384], wl.MLA_B32):
+            mq, mkv = wl.make_mla(wm, device=dev)
+            mo = torch.empty(wm.B, wm.H, attn.MLA_D_C, dtype=torch.bfloat16, device=dev)
+            ml = torch.empty(wm.B, wm.H, dtype=torch.float32, device=dev)
+            n_sp = attn.mla_decode_num_splits(wm.B, wm.H, wm.T)
+            need = attn.mla_decode_workspace_bytes(wm.B, wm.H, wm.T, n_sp)
+            mws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+            args_ = (mq.data_ptr(), mkv.data_ptr(), mo.data_ptr(), ml.data_ptr(), wm.B, wm.H, wm.T,
+                     attn.MLA_D_C, attn.MLA_D_R, ctypes.c_float(wm.sm_scale), n_sp,
+                     mws.data_ptr(), need)
+            times = []
+            with torch.cuda.stream(stream):
+                for it in range(25):
+                    flush.zero_()
+                    a = torch.cuda.Event(enable_timing=True)
+                    b = torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    assert lib.attn_mla_decode(*args_, sh) == 0
+                    b.record(stream)
+                    b.synchronize()
+                    if it >= 5:
+                        times.append(a.elapsed_time(b))
+            ms = statistics.median(times)
+            gbs = wm.bytes / (ms * 1e-3) / 1e9
+            mla.append({"workload": wm.name, "us": ms * 1e3, "gbs": gbs, "hbm_frac": gbs / hbm,
+                        "tflops": wm.flops / (ms * 1e-3) / 1e12, "splits": n_sp,
+                        "kernels_per_step": 2 if n_sp > 1 else 1})
+            del mq, mkv, mo, ml, mws
+        del flush
+        if attn.device_status(dev) != 0:
+            raise SystemExit("device status word reports an expired wait in the MLA leg")
+
     # ---- CPU baseline: the oracle as it stands, bounded sample, rank 0 at N=1 only -----------
     cpu = None
     if rank == 0 and world == 1:
@@ -508,7 +550,7 @@ def main():
             "config": config_of(w, "inputs and output exceed the 129 MB L2; no flush"),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": args.steps, "clocks": clocks, "sweep": sweep,
-            "low_occupancy": low_occ, "backward": backward,
+            "low_occupancy": low_occ, "backward": backward, "mla_decode": mla,
             "kernel_sha": kernel_hash(),
         }
         print(json.dumps(line), flush=True)

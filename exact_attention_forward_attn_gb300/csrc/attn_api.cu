@@ -618,17 +618,18 @@ int64_t mla_items(int B, int H) {
 
 int64_t mla_tiles(int T) { return (static_cast<int64_t>(T) + kMlaBN - 1) / kMlaBN; }
 
-// Splits of the token axis.  Each CTA costs its tiles plus, when split, writing its fp32 partial
-// (about two tiles' worth of traffic); CTAs run in waves of one per SM.  Pick the split count with
-// the least waves x per-CTA cost (fewest splits on ties).
-int mla_heuristic_splits(int64_t items, int64_t n_tiles, int num_sms) {
+// Splits of the token axis, from a cost model in units of one 64-token tile per CTA (about
+// 1.8 us): CTAs run in waves of one per SM, and a split run also writes each split's fp32
+// partial rows (2 KiB per head) and merges them, about 0.57 tile per thousand partial rows
+// plus half a tile for the merge launch.  The least costly count wins (fewest splits on ties).
+int mla_heuristic_splits(int64_t items, int64_t n_tiles, int64_t rows, int num_sms) {
     const int64_t max_s = std::min<int64_t>(n_tiles, kMaxSplits);
     int best = 1;
     int64_t best_cost = -1;
     for (int64_t s = 1; s <= max_s; ++s) {
         const int64_t waves = (items * s + num_sms - 1) / num_sms;
-        const int64_t per_cta = (n_tiles + s - 1) / s + (s > 1 ? 2 : 0);
-        const int64_t cost = waves * per_cta;
+        int64_t cost = 1000 * waves * ((n_tiles + s - 1) / s);  // milli-tiles
+        if (s > 1) cost += 500 + s * rows * 57 / 100;
         if (best_cost < 0 || cost < best_cost) {
             best_cost = cost;
             best = static_cast<int>(s);
@@ -647,7 +648,8 @@ extern "C" int attn_mla_decode_num_splits(int B, int H, int T) {
     if (B <= 0 || H <= 0 || T <= 0) return 1;
     DeviceState* ds = nullptr;
     if (current_device_state(&ds) != ATTN_OK) return 1;
-    return mla_heuristic_splits(mla_items(B, H), mla_tiles(T), ds->num_sms);
+    return mla_heuristic_splits(mla_items(B, H), mla_tiles(T), static_cast<int64_t>(B) * H,
+                                ds->num_sms);
 }
 
 extern "C" size_t attn_mla_decode_workspace_bytes(int B, int H, int T, int num_splits) {
@@ -707,7 +709,7 @@ extern "C" int attn_mla_decode(const void* q, const void* kv, void* out, float* 
     st = device_state(dev, &ds);
     if (st != ATTN_OK) return st;
     if (num_splits == 0) {
-        n_splits = mla_heuristic_splits(items, n_tiles, ds->num_sms);
+        n_splits = mla_heuristic_splits(items, n_tiles, static_cast<int64_t>(B) * H, ds->num_sms);
         st = check_workspace(n_splits);
         if (st != ATTN_OK) return st;
     }
