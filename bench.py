@@ -407,6 +407,25 @@ def main():
             sweep.append({"N": n, "ms": ms, "tflops": tf, "frac": tf / peak})
             del sq, sk, sv, so, sl
 
+    # ---- context: wide heads (D = 256, one Q tile per CTA) on a long causal sequence ---------
+    wide = []
+    if not args.no_sweep and rank == 0:
+        ww = wl.WIDE
+        wq, wk, wv = (t.to(dev) for t in wl.make_qkv(ww))
+        wo = torch.empty_like(wq)
+        wlse = torch.empty(ww.B, ww.Hq, ww.N, dtype=torch.float32, device=dev)
+
+        def wstep():
+            attn.attn_fwd(wq, wk, wv, causal=ww.causal, sm_scale=ww.sm_scale, out=wo, lse=wlse)
+
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                wstep()
+        ms = statistics.median(timed_launches(wstep, stream, 20))
+        tf = ww.flops / (ms * 1e-3) / 1e12
+        wide.append({"workload": ww.name, "ms": ms, "tflops": tf, "frac": tf / peak})
+        del wq, wk, wv, wo, wlse
+
     # ---- context: low-occupancy configurations, single pass vs split-KV (key-axis splits) -----
     low_occ = []
     if not args.no_sweep and rank == 0:
@@ -550,7 +569,8 @@ def main():
             "config": config_of(w, "inputs and output exceed the 129 MB L2; no flush"),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": args.steps, "clocks": clocks, "sweep": sweep,
-            "low_occupancy": low_occ, "backward": backward, "mla_decode": mla,
+            "low_occupancy": low_occ, "wide_heads": wide, "backward": backward,
+            "mla_decode": mla,
             "kernel_sha": kernel_hash(),
         }
         print(json.dumps(line), flush=True)

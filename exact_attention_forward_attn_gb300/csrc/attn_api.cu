@@ -17,6 +17,7 @@
 
 #include "attn.h"
 #include "attn_bwd_kernel.cuh"
+#include "attn_fwd_d256_kernel.cuh"
 #include "attn_fwd_kernel.cuh"
 #include "mla_decode_kernel.cuh"
 
@@ -169,6 +170,10 @@ int device_state(int dev, DeviceState** out) {
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      MlaSmem::kAlloc);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(attn_fwd_d256_kernel,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     Fwd256Smem::kAlloc);
         if (e != cudaSuccess) { st.status = ATTN_ERR_CUDA; st.cuda_error = e; }
     });
     if (st.status == ATTN_ERR_CUDA) t_last_cuda_error = st.cuda_error;
@@ -231,7 +236,7 @@ int validate(Problem& P, bool* empty) {
     *empty = false;
     if (P.B < 0 || P.N < 0 || P.Hq <= 0 || P.Hkv <= 0) return ATTN_ERR_SHAPE;
     if (P.Hq % P.Hkv != 0) return ATTN_ERR_HEADS;
-    if (P.D % 8 != 0 || P.D < 8 || P.D > 128) return ATTN_ERR_HEADDIM;
+    if (P.D % 8 != 0 || P.D < 8 || P.D > 256) return ATTN_ERR_HEADDIM;
     if (!std::isfinite(P.sm_scale) || !(P.sm_scale > 0.f)) return ATTN_ERR_SCALE;
     if (P.B == 0 || P.N == 0) {  // empty problem: nothing to read or write
         *empty = true;
@@ -248,7 +253,7 @@ int validate(Problem& P, bool* empty) {
     P.bh_kv = static_cast<int64_t>(P.B) * P.Hkv;
     P.n_tiles = (static_cast<int64_t>(P.N) + kBM - 1) / kBM;
     P.n_pairs = (P.n_tiles + 1) / 2;
-    P.items = P.n_pairs * P.bh;
+    P.items = (P.D > 128 ? P.n_tiles : P.n_pairs) * P.bh;  // one or two Q tiles per CTA
     if (P.items > 0x7fffffffLL || P.bh > 0x7fffffffLL) return ATTN_ERR_SHAPE;
 
     if (!P.strided) {
@@ -318,6 +323,18 @@ int launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
 
+// The single-pass forward for head dimension D: two Q tiles per CTA up to D = 128, one above.
+int launch_single(int D, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                  const CUtensorMap& mo, const AttnParams& p, unsigned int* status_word,
+                  int64_t grid, cudaStream_t stream) {
+    if (D <= 64) return launch_fwd<64, false>(mq, mk, mv, mo, p, status_word, grid, stream);
+    if (D <= 128) return launch_fwd<128, false>(mq, mk, mv, mo, p, status_word, grid, stream);
+    attn_fwd_d256_kernel<<<static_cast<unsigned int>(grid), kW256Threads, Fwd256Smem::kAlloc,
+                           stream>>>(mq, mk, mv, mo, p, status_word);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
 template <int D>
 int launch_merge(const AttnParams& p, __nv_bfloat16* out, int d_out, cudaStream_t stream) {
     const int64_t rows = static_cast<int64_t>(p.B) * p.Hq * p.N;
@@ -372,8 +389,7 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* out, 
     st = prepare(P, &ds, &mq, &mk, &mv, &mo, &prm);
     if (st != ATTN_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return D <= 64 ? launch_fwd<64, false>(mq, mk, mv, mo, prm, ds->status_word, P.items, s)
-                   : launch_fwd<128, false>(mq, mk, mv, mo, prm, ds->status_word, P.items, s);
+    return launch_single(D, mq, mk, mv, mo, prm, ds->status_word, P.items, s);
 }
 
 extern "C" int attn_fwd_strided(const void* q, const void* k, const void* v, void* out,
@@ -398,13 +414,13 @@ extern "C" int attn_fwd_strided(const void* q, const void* k, const void* v, voi
     st = prepare(P, &ds, &mq, &mk, &mv, &mo, &prm);
     if (st != ATTN_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return D <= 64 ? launch_fwd<64, false>(mq, mk, mv, mo, prm, ds->status_word, P.items, s)
-                   : launch_fwd<128, false>(mq, mk, mv, mo, prm, ds->status_word, P.items, s);
+    return launch_single(D, mq, mk, mv, mo, prm, ds->status_word, P.items, s);
 }
 
 extern "C" int attn_fwd_test_stall(const void* q, const void* k, const void* v, void* out,
                                    float* lse, int B, int Hq, int Hkv, int N, int D, int causal,
                                    float sm_scale, int stall_item, void* stream) {
+    if (D > 128) return ATTN_ERR_HEADDIM;  // the hook lives in the two-tile kernel
     Problem P{q, k, v, out, lse, B, Hq, Hkv, N, D, causal, sm_scale};
     bool empty = false;
     int st = validate(P, &empty);
@@ -422,9 +438,8 @@ extern "C" int attn_fwd_test_stall(const void* q, const void* k, const void* v, 
 }
 
 extern "C" int attn_fwd_splitkv_num_splits(int B, int Hq, int N, int D, int causal) {
-    (void)D;
     (void)causal;
-    if (B <= 0 || Hq <= 0 || N <= 0) return 1;
+    if (B <= 0 || Hq <= 0 || N <= 0 || D > 128) return 1;  // D > 128: single pass only
     DeviceState* ds = nullptr;
     if (current_device_state(&ds) != ATTN_OK) return 1;
     const int64_t n_tiles = (static_cast<int64_t>(N) + kBM - 1) / kBM;
@@ -435,7 +450,8 @@ extern "C" int attn_fwd_splitkv_num_splits(int B, int Hq, int N, int D, int caus
 }
 
 extern "C" size_t attn_fwd_splitkv_workspace_bytes(int B, int Hq, int N, int D, int num_splits) {
-    if (B <= 0 || Hq <= 0 || N <= 0 || D % 8 != 0 || D < 8 || D > 128) return 0;
+    if (B <= 0 || Hq <= 0 || N <= 0 || D % 8 != 0 || D < 8 || D > 256) return 0;
+    if (D > 128) return 0;  // single pass
     if (num_splits == 0) num_splits = attn_fwd_splitkv_num_splits(B, Hq, N, D, 0);
     const int64_t n_tiles = (static_cast<int64_t>(N) + kBM - 1) / kBM;
     int tps = 0, n = 0;
@@ -456,6 +472,7 @@ extern "C" int attn_fwd_splitkv(const void* q, const void* k, const void* v, voi
     if (num_splits == 0) num_splits = attn_fwd_splitkv_num_splits(B, Hq, N, D, causal);
     int split_tiles = 0, n_splits = 0;
     split_layout(P.n_tiles, num_splits, &split_tiles, &n_splits);
+    if (D > 128) n_splits = 1;  // the wide-head kernel has no split variant
     if (n_splits <= 1)  // one split is the ordinary forward; the workspace is not touched
         return attn_fwd(q, k, v, out, lse, B, Hq, Hkv, N, D, causal, sm_scale, stream);
 
@@ -528,6 +545,7 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
                         const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
                         int Hq, int Hkv, int N, int D, int causal, float sm_scale,
                         void* workspace, size_t workspace_bytes, void* stream) {
+    if (D > 128) return ATTN_ERR_HEADDIM;  // the backward kernels hold at most 128 columns
     // the forward's checks cover q, k, v, out (here an input) and lse
     Problem P{q, k, v, const_cast<void*>(out), const_cast<float*>(lse), B, Hq, Hkv, N, D, causal,
               sm_scale};
@@ -756,8 +774,8 @@ extern "C" const char* attn_status_string(int status) {
         case ATTN_ERR_SHAPE: return "invalid or overflowing shape (B, Hq, Hkv, N)";
         case ATTN_ERR_HEADS: return "Hq is not a multiple of Hkv";
         case ATTN_ERR_HEADDIM:
-            return "unsupported head dimension (attention: D a multiple of 8 in [8, 128]; "
-                   "MLA decode: d_c = 512 and d_r = 64)";
+            return "unsupported head dimension (attention: D a multiple of 8 in [8, 256], "
+                   "backward [8, 128]; MLA decode: d_c = 512 and d_r = 64)";
         case ATTN_ERR_ALIGN: return "a pointer is not 16-byte aligned";
         case ATTN_ERR_SCALE: return "sm_scale must be finite and positive";
         case ATTN_ERR_ARCH: return "the current device is not sm_103 (GB300)";
@@ -850,6 +868,7 @@ extern "C" int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void
     if (num_splits == 0) num_splits = attn_fwd_splitkv_num_splits(B, Hq, N, D, causal);
     int split_tiles = 0, n_splits = 0;
     split_layout(P.n_tiles, num_splits, &split_tiles, &n_splits);
+    if (D > 128) n_splits = 1;
     if (n_splits > 1 && workspace_bytes_for(P.bh, N, D, n_splits) >
                             static_cast<int64_t>(kNoAllocScratchBytes))
         return ATTN_ERR_SCRATCH;  // checked before anything touches the device

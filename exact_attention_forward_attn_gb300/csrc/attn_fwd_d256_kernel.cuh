@@ -1,0 +1,322 @@
+// attn_fwd_d256_kernel.cuh - the exact-attention forward for head dimensions 136..256 (sm_103a).
+//
+// Same computation as attn_fwd_kernel ("Attention Kernel 实现与正确性验证", walkerchi.com,
+// section 1.2: scores, online softmax, P.V, O/l and LSE; GQA head map, top-left causal mask), for
+// the wide heads the robustness row asks for ("Triton-CUDA Attention", skillmd.com, pads D to a
+// power of two; D is zero-padded to 256 here by the TMA).  At D = 256 one Q tile's fp32 output
+// already takes 256 TMEM columns, so a CTA holds one 128-row Q tile instead of two:
+//   TMEM (512 columns): S[2] (128 each, double-buffered: S(j+1) forms while the softmax works
+//   on S(j); P (bf16) is written over the first 64 columns of its S) | O (256).
+//   Shared memory: Q (4 panels, 64 KiB, loaded once, reused to stage O), a 6-slot ring of 16 KiB
+//   K panels (128 keys x 64 columns; S accumulates over the four panels of a key tile, each slot
+//   refilled as soon as its MMAs have read it), V (4 panels, 64 KiB, the MN-major B operand of
+//   one N=256 MMA per 16 keys).
+// Warps: 0-3 softmax (one row per thread), 4 issues S, 5 issues P.V, 6 loads (lane 0: Q and the
+// K ring; lane 1: V).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "attn_fwd_kernel.cuh"
+#include "ptx.cuh"
+
+namespace gb300attn {
+
+constexpr int kW256Threads = 224;
+constexpr int kW256MmaS = 4, kW256MmaPV = 5, kW256Load = 6;
+
+struct Fwd256Smem {
+    static constexpr int kPanel = 128 * 128;  // 128 rows x 64 bf16
+    static constexpr int kKSlots = 6;
+    static constexpr int kQ = 0;
+    static constexpr int kK = kQ + 4 * kPanel;
+    static constexpr int kV = kK + kKSlots * kPanel;
+    static constexpr int kBars = kV + 4 * kPanel;
+    static constexpr int kBarQ = 0;
+    static constexpr int kBarKFull = 1;                    // [kKSlots]
+    static constexpr int kBarKEmpty = kBarKFull + kKSlots;  // [kKSlots]
+    static constexpr int kBarVFull = kBarKEmpty + kKSlots;
+    static constexpr int kBarVEmpty = kBarVFull + 1;
+    static constexpr int kBarSFull = kBarVEmpty + 1;  // [2]
+    static constexpr int kBarPFull = kBarSFull + 2;   // [2] (count 128)
+    static constexpr int kBarPvDone = kBarPFull + 2;  // [2]
+    static constexpr int kNumBars = kBarPvDone + 2;
+    static constexpr int kTmemSlot = kBars + kNumBars * 8;
+    static constexpr int kAbort = kTmemSlot + 8;
+    static constexpr int kBytes = kAbort + 8;
+    static constexpr int kAlloc = kBytes + 1024;
+    static_assert(kAlloc <= 232448, "D=256 forward shared memory exceeds the per-block limit");
+};
+
+__global__ void __launch_bounds__(kW256Threads, 1)
+    attn_fwd_d256_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                         const __grid_constant__ CUtensorMap tmap_k,
+                         const __grid_constant__ CUtensorMap tmap_v,
+                         const __grid_constant__ CUtensorMap tmap_o, const AttnParams p,
+                         unsigned int* status_word) {
+    using L = Fwd256Smem;
+    constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, 0);   // Q (K-major) x K (K-major)
+    constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, 1);  // P (TMEM) x V (MN-major)
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_addr(smem);
+    auto bar = [=](int i) -> uint32_t { return sbase + L::kBars + 8u * i; };
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // work: (batch, KV head) outermost so the CTAs in flight share K/V in L2, then Q tiles
+    // heaviest (latest) first, then the query heads of the group
+    const int item = static_cast<int>(blockIdx.x);
+    const int per_kv = p.n_tiles * p.group;
+    const int bh_kv = item / per_kv;
+    const int rem = item % per_kv;
+    const int m_tile = p.n_tiles - 1 - rem / p.group;
+    const int b = bh_kv / p.Hkv, hkv = bh_kv % p.Hkv;
+    const int hq = hkv * p.group + rem % p.group;
+    const int n_kv = p.causal ? m_tile + 1 : p.n_tiles;  // key tiles 0 .. n_kv-1
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(L::kBarQ), 1);
+        for (int s = 0; s < L::kKSlots; ++s) {
+            mbar_init(bar(L::kBarKFull + s), 1);
+            mbar_init(bar(L::kBarKEmpty + s), 1);
+        }
+        mbar_init(bar(L::kBarVFull), 1);
+        mbar_init(bar(L::kBarVEmpty), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(L::kBarSFull + i), 1);
+            mbar_init(bar(L::kBarPFull + i), 128);
+            mbar_init(bar(L::kBarPvDone + i), 1);
+        }
+        *abort_flag = 0;
+        fence_mbarrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == kW256MmaS) {
+        tmem_alloc(smem_addr(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    auto t_s = [=](int j) { return tmem + (j & 1) * 128; };
+    const uint32_t t_o = tmem + 256;
+
+    if (warp == kW256Load) {
+        if (lane == 0) {  // Q once, then the K panels of every key tile through the ring
+            tma_prefetch_desc(&tmap_q);
+            tma_prefetch_desc(&tmap_k);
+            mbar_arrive_expect_tx(bar(L::kBarQ), 4 * L::kPanel);
+            for (int pn = 0; pn < 4; ++pn)
+                tma_load_4d(sbase + L::kQ + pn * L::kPanel, &tmap_q, bar(L::kBarQ), pn * 64,
+                            m_tile * 128, hq, b);
+            for (int k = 0; k < 4 * n_kv; ++k) {
+                const int slot = k % L::kKSlots;
+                if (!mbar_wait_bounded<true>(bar(L::kBarKEmpty + slot),
+                                             ((k / L::kKSlots) & 1) ^ 1u, abort_flag, status_word))
+                    break;
+                mbar_arrive_expect_tx(bar(L::kBarKFull + slot), L::kPanel);
+                tma_load_4d(sbase + L::kK + slot * L::kPanel, &tmap_k, bar(L::kBarKFull + slot),
+                            (k & 3) * 64, (k >> 2) * 128, hkv, b);
+            }
+        } else if (lane == 1) {  // V tiles, each once the previous P.V has read its buffer
+            tma_prefetch_desc(&tmap_v);
+            for (int j = 0; j < n_kv; ++j) {
+                if (!mbar_wait_bounded<true>(bar(L::kBarVEmpty), (j & 1) ^ 1u, abort_flag,
+                                             status_word))
+                    break;
+                mbar_arrive_expect_tx(bar(L::kBarVFull), 4 * L::kPanel);
+                for (int pn = 0; pn < 4; ++pn)
+                    tma_load_4d(sbase + L::kV + pn * L::kPanel, &tmap_v, bar(L::kBarVFull),
+                                pn * 64, j * 128, hkv, b);
+            }
+        }
+        __syncwarp();
+    } else if (warp == kW256MmaS) {
+        // S(j) = Q K_j^T into buffer j&1, once P.V(j-2) has read the P written over it
+        bool ok = mbar_wait_warp(bar(L::kBarQ), 0, abort_flag, status_word);
+        for (int j = 0; ok && j < n_kv; ++j) {
+            if (j >= 2) {
+                ok = mbar_wait_warp(bar(L::kBarPvDone + (j & 1)), ((j - 2) >> 1) & 1, abort_flag,
+                                    status_word);
+                if (!ok) break;
+            }
+            for (int pn = 0; pn < 4; ++pn) {
+                const int k = 4 * j + pn;
+                ok = mbar_wait_warp(bar(L::kBarKFull + k % L::kKSlots), (k / L::kKSlots) & 1,
+                                    abort_flag, status_word);
+                if (!ok) break;
+            }
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int pn = 0; pn < 4; ++pn) {
+                const uint32_t kp = sbase + L::kK + ((4 * j + pn) % L::kKSlots) * L::kPanel;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16_ss_warp(t_s(j),
+                                     smem_desc_sw128(sbase + L::kQ + pn * L::kPanel + kk * 32, 16, 1024),
+                                     smem_desc_sw128(kp + kk * 32, 16, 1024), kIdescS,
+                                     (pn > 0 || kk > 0) ? 1u : 0u);
+            }
+            for (int pn = 0; pn < 4; ++pn)
+                mma_commit_warp(bar(L::kBarKEmpty + (4 * j + pn) % L::kKSlots));
+            mma_commit_warp(bar(L::kBarSFull + (j & 1)));
+        }
+        __syncwarp();
+    } else if (warp == kW256MmaPV) {
+        // O += P(j) V_j: A = P from TMEM (over S(j)), B = the four V panels (N = 256)
+        bool ok = true;
+        for (int j = 0; ok && j < n_kv; ++j) {
+            ok = mbar_wait_warp(bar(L::kBarVFull), j & 1, abort_flag, status_word);
+            if (ok) ok = mbar_wait_warp(bar(L::kBarPFull + (j & 1)), (j >> 1) & 1, abort_flag,
+                                        status_word);
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                mma_bf16_ts_warp(t_o, t_s(j) + kk * 8,
+                                 smem_desc_sw128(sbase + L::kV + kk * 2048, L::kPanel, 1024),
+                                 kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+            mma_commit_warp(bar(L::kBarPvDone + (j & 1)));
+            mma_commit_warp(bar(L::kBarVEmpty));
+        }
+        __syncwarp();
+    } else {
+        // ---------------- softmax warps 0-3: row `row` of the Q tile --------------------------
+        const int row = warp * 32 + lane;
+        const int row_g = m_tile * 128 + row;
+        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        const float c = p.scale_log2;
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; ok && j < n_kv; ++j) {
+            ok = mbar_wait_warp(bar(L::kBarSFull + (j & 1)), (j >> 1) & 1, abort_flag,
+                                status_word);
+            if (!ok) break;
+            tc_fence_after();
+            float s[128];
+            {
+                uint32_t r[128];
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+                    tmem_ld32(lane_base + t_s(j) + cc * 32,
+                              *reinterpret_cast<uint32_t(*)[32]>(&r[cc * 32]));
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(r[i]);
+            }
+            // masks: the causal diagonal tile, or the ragged last key tile
+            const bool diag = p.causal && j == m_tile;
+            const bool tail = !p.causal && j == p.n_tiles - 1 && (p.N % 128) != 0;
+            if (diag || tail) {
+                const int lim = diag ? row + 1 : p.N - j * 128;  // first masked key
+#pragma unroll
+                for (int i = 0; i < 128; ++i)
+                    if (i >= lim) s[i] = -INFINITY;
+            }
+            float mx[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) mx[k] = fmaxf(s[k], s[k + 8]);
+#pragma unroll
+            for (int i = 16; i < 128; i += 16)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) mx[k] = fmax3(mx[k], s[i + k], s[i + 8 + k]);
+            const float row_max =
+                fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+            const float m_cand = row_max * c;
+            const float m_new = (m_cand > m + kRescaleThreshold) ? m_cand : m;
+            const float alpha = ex2_approx(m - m_new);  // 1 if unchanged, 0 on the first tile
+            const bool rescale = j > 0 && __any_sync(0xffffffffu, m_new != m);
+            m = m_new;
+            const float neg_m = -m;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int col = h * 64 + 2 * i;
+                    float x0, x1;
+                    ffma2(x0, x1, s[col], s[col + 1], c, c, neg_m, neg_m);
+                    const float p0 = ex2_approx(x0);
+                    const float p1 = ex2_approx(x1);
+                    const int a = (i & 1) * 2;
+                    fadd2(acc[a], acc[a + 1], acc[a], acc[a + 1], p0, p1);
+                    pk[i] = pack_bf16x2(p0, p1);
+                }
+                tmem_st32(lane_base + t_s(j) + h * 32, pk);  // over S(j), already read
+            }
+            if (rescale) {  // O *= alpha once P.V(j-1) has landed
+                ok = mbar_wait_warp(bar(L::kBarPvDone + ((j - 1) & 1)), ((j - 1) >> 1) & 1,
+                                    abort_flag, status_word);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll 1
+                for (int cc = 0; cc < 8; ++cc) {
+                    uint32_t o[32];
+                    tmem_ld32(lane_base + t_o + cc * 32, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+                    tmem_st32(lane_base + t_o + cc * 32, o);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(L::kBarPFull + (j & 1)));
+            l = l * alpha + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
+        }
+        // epilogue: O / l -> bf16 -> the Q panels (128B swizzle) -> TMA store; LSE
+        if (ok) {
+            const int last = n_kv - 1;
+            ok = mbar_wait_warp(bar(L::kBarPvDone + (last & 1)), (last >> 1) & 1, abort_flag,
+                                status_word);
+        }
+        if (ok) {
+            tc_fence_after();
+            const float inv_l = 1.0f / l;
+#pragma unroll 1
+            for (int cc = 0; cc < 8; ++cc) {
+                uint32_t o[32];
+                tmem_ld32(lane_base + t_o + cc * 32, o);
+                tmem_wait_ld();
+                const uint32_t prow = sbase + L::kQ + (cc >> 1) * L::kPanel + row * 128;
+#pragma unroll
+                for (int c16 = 0; c16 < 4; ++c16) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        w[i] = pack_bf16x2(__uint_as_float(o[c16 * 8 + 2 * i]) * inv_l,
+                                           __uint_as_float(o[c16 * 8 + 2 * i + 1]) * inv_l);
+                    const int chunk = (cc & 1) * 4 + c16;
+                    st_shared_v4(prow + ((chunk ^ (row & 7)) << 4), w[0], w[1], w[2], w[3]);
+                }
+            }
+            if (row_g < p.N)
+                p.lse[(static_cast<size_t>(b) * p.Hq + hq) * p.N + row_g] =
+                    (m + __log2f(l)) * 0.69314718055994531f;
+        }
+        fence_proxy_async_smem();
+        named_barrier_sync(1, 128);
+        if (ok && warp == 0 && lane == 0) {
+            for (int pn = 0; pn < 4; ++pn)
+                tma_store_4d(&tmap_o, sbase + L::kQ + pn * L::kPanel, pn * 64, m_tile * 128, hq, b);
+            tma_store_commit_and_wait();
+        }
+        __syncwarp();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kW256MmaS) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace gb300attn

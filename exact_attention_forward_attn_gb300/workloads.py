@@ -74,8 +74,12 @@ FEWHEADS = Workload("fewheads-n4096", 1, 2, 1, 4096, 128, False, 8)
 LONG = {n: Workload(f"long-gqa8-causal-n{n}", 1, 32, 8, n, 128, True, s)
         for n, s in ((8192, 5), (16384, 6), (32768, 7))}
 
+# Wide heads (D = 256, one Q tile per CTA): the robustness row's widest head dimension over a long
+# causal sequence.  Not one of the five configurations.
+WIDE = Workload("wide-d256-causal-n8192", 1, 16, 4, 8192, 256, True, 9)
+
 CONFIGS = [TINY_NONCAUSAL, TINY_CAUSAL, GQA4_CAUSAL, GQA8_CAUSAL, MHA, MHA_OUTLIER, MQA,
-           *LONG.values(), FEWHEADS]
+           *LONG.values(), FEWHEADS, WIDE]
 BY_NAME = {w.name: w for w in CONFIGS}
 
 

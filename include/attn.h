@@ -41,7 +41,7 @@ typedef enum {
     ATTN_ERR_NULL = -1,     /* a required pointer is NULL */
     ATTN_ERR_SHAPE = -2,    /* B, Hq, Hkv or N negative, Hq or Hkv zero, or sizes overflow */
     ATTN_ERR_HEADS = -3,    /* Hq is not a multiple of Hkv */
-    ATTN_ERR_HEADDIM = -4,  /* D is not a multiple of 8 in [8, 128] */
+    ATTN_ERR_HEADDIM = -4,  /* D not a multiple of 8 in [8, 256] ([8, 128] for the backward) */
     ATTN_ERR_ALIGN = -5,    /* a tensor pointer is not 16-byte aligned */
     ATTN_ERR_SCALE = -6,    /* sm_scale is not finite and positive */
     ATTN_ERR_ARCH = -7,     /* the device is not sm_103, or its shared memory is misaligned */
@@ -64,10 +64,11 @@ typedef enum {
  *   out      bf16 [B, Hq,  N, D], contiguous; written (round-to-nearest-even); must not overlap
  *            q, k, v or lse
  *   lse      fp32 [B, Hq, N]; written with the natural-log LSE of the scaled, masked scores
- *   B, Hq, Hkv, N, D   sizes; Hq % Hkv == 0 (MQA is Hkv == 1); D a multiple of 8 in [8, 128]
- *            (computed on D padded to 64 or 128 with zeros, as "Triton-CUDA Attention" pads D to a
- *            power of two; the padding is never read from or written to memory); B == 0 or N == 0
- *            is a valid empty problem (returns ATTN_OK, launches nothing; the pointers may then
+ *   B, Hq, Hkv, N, D   sizes; Hq % Hkv == 0 (MQA is Hkv == 1); D a multiple of 8 in [8, 256]
+ *            (computed on D padded to 64, 128 or 256 with zeros, as "Triton-CUDA Attention" pads
+ *            D to a power of two; the padding is never read from or written to memory; D > 128
+ *            runs a one-Q-tile-per-CTA kernel, since its output fills the tensor memory);
+ *            B == 0 or N == 0 is a valid empty problem (returns ATTN_OK, launches nothing; the pointers may then
  *            be NULL, as zero-size allocations often are)
  *   causal   0: every key visible; nonzero: key j visible to query i iff j <= i
  *   sm_scale score scale (callers usually pass 1/sqrt(D)); finite and > 0
@@ -111,7 +112,8 @@ int attn_fwd_strided(const void* q, const void* k, const void* v, void* out, flo
  *   q, k, v, out, lse, B, Hq, Hkv, N, D, causal, sm_scale, stream: as for attn_fwd.
  *   num_splits       requested number of key-axis splits, 0..64; 0 picks
  *                    attn_fwd_splitkv_num_splits().  Splits hold ceil(ceil(N/128)/num_splits)
- *                    key tiles of 128, so fewer splits may be used.  One split is attn_fwd.
+ *                    key tiles of 128, so fewer splits may be used.  One split is attn_fwd;
+ *                    D > 128 always runs as one split (the wide-head kernel has no split form).
  *   workspace        device memory of at least attn_fwd_splitkv_workspace_bytes(B, Hq, N, D,
  *                    num_splits) bytes, 16-byte aligned, owned by the caller; its previous
  *                    contents are ignored and it holds partial results afterwards.  It must not
@@ -186,7 +188,8 @@ int attn_debug_status(void* stream);
  * ds_ij = p_ij (dp_ij - dO_i.O_i); dQ_i = sm_scale sum_j ds_ij k_j, dK_j = sm_scale sum ds_ij q_i
  * and dV_j = sum p_ij dO_i, the last two summed over the query heads that share the KV head.
  *
- *   q, k, v, B, Hq, Hkv, N, D, causal, sm_scale: as passed to attn_fwd (contiguous).
+ *   q, k, v, B, Hq, Hkv, N, D, causal, sm_scale: as passed to attn_fwd (contiguous); D at most
+ *                128 here (ATTN_ERR_HEADDIM above).
  *   out, lse     attn_fwd's outputs O [B,Hq,N,D] bf16 and LSE [B,Hq,N] fp32 (inputs here).
  *   dout         dL/dO, bf16 [B, Hq, N, D], contiguous.
  *   dq           bf16 [B, Hq, N, D]; dk, dv bf16 [B, Hkv, N, D]: written (contiguous).

@@ -71,7 +71,8 @@ def _call(lib, q=P, k=P * 2, v=P * 3, out=P * 4, lse=P * 5, B=1, Hq=2, Hkv=1, N=
     (dict(q=0), -1), (dict(out=0), -1), (dict(lse=0), -1),
     (dict(B=-1), -2), (dict(N=-5), -2), (dict(Hq=0), -2), (dict(Hkv=0), -2),
     (dict(Hq=6, Hkv=4), -3),
-    (dict(D=100), -4), (dict(D=256), -4), (dict(D=0), -4), (dict(D=136), -4), (dict(D=4), -4),
+    (dict(D=100), -4), (dict(D=264), -4), (dict(D=0), -4), (dict(D=512), -4), (dict(D=4), -4),
+    (dict(D=252), -4),
     (dict(scale=0.0), -6), (dict(scale=-1.0), -6), (dict(scale=float("inf")), -6),
     (dict(scale=float("nan")), -6),
     (dict(q=P + 8), -5), (dict(lse=P * 5 + 4), -5),
@@ -185,3 +186,14 @@ def test_mla_host_validation(lib, kw, status):
 
 def test_mla_empty_batch_is_a_no_op(lib):
     assert _mla(lib, B=0, q=0, kv=0, out=0, lse=0, ws=0, ws_bytes=0) == 0
+
+
+def test_wide_heads_are_forward_only(lib):
+    # the backward holds at most 128 columns: D = 192 is rejected before anything else
+    assert lib.attn_bwd(S, S * 2, S * 3, S * 4, S * 5, S * 6, S * 7, S * 8, S * 9, 1, 2, 1, 128, 192,
+                        0, ctypes.c_float(0.1), S * 10, 1 << 20, None) == -4
+    # the test hook lives in the two-tile kernel only
+    assert lib.attn_fwd_test_stall(S, S * 2, S * 3, S * 4, S * 5, 1, 2, 1, 128, 256, 0,
+                                   ctypes.c_float(0.1), 0, None) == -4
+    # split-KV with wide heads runs as one split: no workspace
+    assert lib.attn_fwd_splitkv_workspace_bytes(1, 32, 4096, 256, 4) == 0

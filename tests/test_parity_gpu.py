@@ -62,7 +62,7 @@ def test_config_full_output(w, cuda_lib):
     _check(out, lse, o_ref, l_ref, w.name)
 
 
-SAMPLED = [wl.GQA8_CAUSAL, *wl.LONG.values()]
+SAMPLED = [wl.GQA8_CAUSAL, *wl.LONG.values(), wl.WIDE]
 
 
 @pytest.mark.parametrize("w", SAMPLED, ids=[w.name for w in SAMPLED])
@@ -95,6 +95,10 @@ RAGGED = [
     (1, 4, 2, 200, 96, True), (1, 2, 1, 130, 32, False), (2, 4, 4, 256, 48, True),
     (1, 8, 2, 300, 80, False), (1, 2, 1, 128, 16, True), (1, 4, 1, 384, 112, True),
     (1, 2, 2, 129, 8, False),
+    # wide heads (one Q tile per CTA): D = 256, and 136..248 zero-padded to 256
+    (1, 2, 1, 1, 256, True), (1, 4, 2, 128, 256, False), (1, 4, 2, 300, 256, True),
+    (2, 4, 1, 383, 256, False), (1, 8, 8, 640, 256, True), (1, 4, 2, 200, 192, True),
+    (1, 2, 1, 129, 136, False), (1, 2, 2, 256, 248, True),
 ]
 
 

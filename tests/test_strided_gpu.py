@@ -31,6 +31,8 @@ CASES = [
     ("padded", wl.random_case(1, 4, 1, 200, 128, False, 33)),
     ("mixed", wl.random_case(2, 6, 3, 129, 128, True, 34)),
     ("bnhd", wl.random_case(1, 4, 2, 250, 96, True, 36)),
+    ("bnhd", wl.random_case(1, 4, 2, 300, 256, True, 37)),
+    ("padded", wl.random_case(1, 2, 1, 200, 192, False, 38)),
 ]
 
 
