@@ -226,6 +226,64 @@ def timed_launches(fn, stream, n):
     return [ev[i].elapsed_time(ev[i + 1]) for i in range(n)]
 
 
+def run_profile_leg(args):
+    """--profile for the backward or the MLA decode: warm-up, then timed launches, nothing else."""
+    import ctypes
+
+    import torch
+
+    import exact_attention_forward_attn_gb300 as attn
+    from exact_attention_forward_attn_gb300 import _lib
+    from exact_attention_forward_attn_gb300 import workloads as wl
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    lib = _lib.load()
+    sh = ctypes.c_void_p(stream.cuda_stream)
+    if args.profile_kind == "mla":
+        wm = {x.name: x for x in wl.MLA_CONFIGS}[args.workload]
+        q, kv = wl.make_mla(wm, device=dev)
+        o = torch.empty(wm.B, wm.H, attn.MLA_D_C, dtype=torch.bfloat16, device=dev)
+        l = torch.empty(wm.B, wm.H, dtype=torch.float32, device=dev)
+        n_sp = attn.mla_decode_num_splits(wm.B, wm.H, wm.T)
+        need = attn.mla_decode_workspace_bytes(wm.B, wm.H, wm.T, n_sp)
+        ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+
+        def step():
+            assert lib.attn_mla_decode(q.data_ptr(), kv.data_ptr(), o.data_ptr(), l.data_ptr(),
+                                       wm.B, wm.H, wm.T, attn.MLA_D_C, attn.MLA_D_R,
+                                       ctypes.c_float(wm.sm_scale), n_sp, ws.data_ptr(), need,
+                                       sh) == 0
+        name = wm.name
+    else:
+        wb = wl.BY_NAME[args.workload]
+        q, k, v = (t.to(dev) for t in wl.make_qkv(wb))
+        o, l = attn.attn_fwd(q, k, v, causal=wb.causal, sm_scale=wb.sm_scale)
+        g = torch.Generator(device="cpu").manual_seed(77)
+        do = torch.randn(q.shape, generator=g).to(torch.bfloat16).to(dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        need = int(lib.attn_bwd_workspace_bytes(wb.B, wb.Hq, wb.N))
+        ws = torch.empty(need, dtype=torch.uint8, device=dev)
+
+        def step():
+            assert lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                l.data_ptr(), do.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                dv.data_ptr(), wb.B, wb.Hq, wb.Hkv, wb.N, wb.D, int(wb.causal),
+                                ctypes.c_float(wb.sm_scale), ws.data_ptr(), need, sh) == 0
+        name = wb.name
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    stream.synchronize()
+    t = timed_launches(step, stream, args.steps)
+    if attn.device_status(dev) != 0:
+        raise SystemExit("device status word reports an expired wait")
+    print(json.dumps({"profile": name, "kind": args.profile_kind, "ms": t}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -235,6 +293,9 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--profile", action="store_true",
                     help="timed launches only (no e2e, sweep, clocks or CPU baseline): for ncu")
+    ap.add_argument("--profile-kind", choices=["forward", "backward", "mla"], default="forward",
+                    help="with --profile: which path --workload names (backward: the three "
+                         "backward kernels on a forward workload; mla: an MLA decode workload)")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target duration of the oracle's bounded CPU-baseline sample")
@@ -246,6 +307,8 @@ def main():
 
     from exact_attention_forward_attn_gb300 import workloads as wl
 
+    if args.profile and args.profile_kind != "forward":
+        return run_profile_leg(args)
     w = wl.BY_NAME[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)
