@@ -144,7 +144,7 @@ cudaError_t opt_in_bwd_smem() {
                                          DkdvSmem<D>::kAlloc);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(attn_bwd_dq_kernel<D>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, BwdSmem<D>::kAlloc);
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, DqSmem<D>::kAlloc);
     return e;
 }
 
@@ -529,7 +529,7 @@ int launch_bwd(const Problem& P, const CUtensorMap& mq, const CUtensorMap& mk,
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
     attn_bwd_dq_kernel<D><<<static_cast<unsigned int>(P.n_tiles * P.bh), kBwdThreads,
-                            BwdSmem<D>::kAlloc, s>>>(mq, mk, mv, mdo, mdq, bp, status_word);
+                            DqSmem<D>::kAlloc, s>>>(mq, mk, mv, mdo, mdq, bp, status_word);
     e = cudaGetLastError();
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }

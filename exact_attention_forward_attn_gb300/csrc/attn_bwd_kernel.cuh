@@ -98,26 +98,33 @@ struct BwdSmem {
     static constexpr int kAlloc = kBytes + 1024;
 };
 
-// dK/dV layout: BwdSmem's tiles, then P^T (bf16, two 128B-swizzled 128 x 64 panels) so that
-// S^T(it+1) can be formed in TMEM while P^T(it) is still being written and read.  This fills the
-// 227 KiB limit, so the layout leaves no slack for aligning the base: the kernel checks that the
-// dynamic shared memory starts 1024-aligned and reports kDevSmemAlign otherwise.
+// dK/dV layout: K_j, V_j resident; a 3-slot ring of Q_i (read by S^T(i), formed a step ahead,
+// and by dK(i), issued last, so the third slot lets Q_(i+2) load while dK(i) is pending); one dO_i
+// buffer (read by dP^T(i) and dV(i), both early in the step); P^T (bf16, two 128B-swizzled
+// 128 x 64 panels) so that S^T(i+1) can be formed while P^T(i) is still being written and read;
+// LSE/Delta vectors in two slots.  This fills the 227 KiB limit, so the layout leaves no slack for
+// aligning the base: the kernel checks that the dynamic shared memory starts 1024-aligned and
+// reports kDevSmemAlign otherwise.
 template <int D>
 struct DkdvSmem {
     static constexpr int kPanelBytes = 128 * 64 * 2;
     static constexpr int kTileBytes = 128 * D * 2;
+    static constexpr int kQSlots = 3;
     static constexpr int kRes0 = 0;                  // K_j
     static constexpr int kRes1 = kTileBytes;         // V_j
-    static constexpr int kStage = 2 * kTileBytes;    // stage s: Q_i, dO_i
-    static constexpr int kPt = kStage + 2 * kBwdStages * kTileBytes;
-    static constexpr int kVec = kPt + 2 * kPanelBytes;  // lse2/delta [stage][2][128]
-    static constexpr int kBars = kVec + kBwdStages * 2 * 128 * 4;
-    // barriers: res_full, stage_full[S], stage_empty[S], s_full, s_free, dp_full, p_ready,
-    // p_free, ds_ready, done
+    static constexpr int kQ = 2 * kTileBytes;        // Q ring
+    static constexpr int kDO = kQ + kQSlots * kTileBytes;
+    static constexpr int kPt = kDO + kTileBytes;
+    static constexpr int kVec = kPt + 2 * kPanelBytes;  // lse2/delta [slot][2][128]
+    static constexpr int kBars = kVec + 2 * 2 * 128 * 4;
     static constexpr int kBarRes = 0;
-    static constexpr int kBarFull = 1;
-    static constexpr int kBarEmpty = kBarFull + kBwdStages;
-    static constexpr int kBarS = kBarEmpty + kBwdStages;
+    static constexpr int kBarQFull = 1;                     // [kQSlots]
+    static constexpr int kBarQEmpty = kBarQFull + kQSlots;  // [kQSlots]
+    static constexpr int kBarDoFull = kBarQEmpty + kQSlots;
+    static constexpr int kBarDoEmpty = kBarDoFull + 1;      // both chains release it
+    static constexpr int kBarVecFull = kBarDoEmpty + 1;     // [2] (the producer's 32 lanes)
+    static constexpr int kBarVecFree = kBarVecFull + 2;     // [2] (the elementwise threads)
+    static constexpr int kBarS = kBarVecFree + 2;
     static constexpr int kBarSFree = kBarS + 1;
     static constexpr int kBarDP = kBarSFree + 1;
     static constexpr int kBarP = kBarDP + 1;
@@ -204,9 +211,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(bar(L::kBarRes), 1);
-        for (int s = 0; s < kBwdStages; ++s) {
-            mbar_init(bar(L::kBarFull + s), 32);  // the producer's 32 lanes (vectors) + tx bytes
-            mbar_init(bar(L::kBarEmpty + s), 2);  // one release per issuer
+        for (int s = 0; s < L::kQSlots; ++s) {
+            mbar_init(bar(L::kBarQFull + s), 1);
+            mbar_init(bar(L::kBarQEmpty + s), 1);
+        }
+        mbar_init(bar(L::kBarDoFull), 1);
+        mbar_init(bar(L::kBarDoEmpty), 2);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar(L::kBarVecFull + s), 32);
+            mbar_init(bar(L::kBarVecFree + s), kBwdEwThreads);
         }
         mbar_init(bar(L::kBarS), 1);
         mbar_init(bar(L::kBarSFree), kBwdEwThreads);
@@ -243,39 +256,59 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                             h * 64, j * 128, hkv, b);
             }
         }
-        // lse2 = LSE*log2(e) and Delta of queries lane*4 .. lane*4+3 of the iteration's tile (0
-        // past N: see top)
+        // -lse2 = -LSE*log2(e) and -Delta of queries lane*4 .. lane*4+3 of the iteration's tile
+        // (0 past N: see top), fetched into registers one step ahead; stored negated so the
+        // elementwise warps add them with packed f32x2 instructions
         float nl[4], nd[4];
         auto fetch = [&](int it) {
             const size_t rowbase = (static_cast<size_t>(b) * p.Hq + it_head(it)) * p.N;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int q = it_tile(it) * 128 + lane * 4 + e;
-                nl[e] = q < p.N ? p.lse[rowbase + q] * kLog2e : 0.f;
-                nd[e] = q < p.N ? p.delta[rowbase + q] : 0.f;
+                nl[e] = q < p.N ? -p.lse[rowbase + q] * kLog2e : 0.f;
+                nd[e] = q < p.N ? -p.delta[rowbase + q] : 0.f;
             }
         };
-        if (n_it > 0) fetch(0);
-        for (int it = 0; it < n_it; ++it) {
-            const int s = it % kBwdStages;
-            const uint32_t ph = (it / kBwdStages) & 1;
-            if (!mbar_wait_warp<true>(bar(L::kBarEmpty + s), ph ^ 1u, abort_flag, status_word)) break;
-            if (lane == 0) {
-                const int hq = it_head(it), i = it_tile(it);
-                const uint32_t st = sbase + L::kStage + s * 2 * L::kTileBytes;
-                mbar_expect_tx(bar(L::kBarFull + s), 2 * L::kTileBytes);
-                for (int h = 0; h < kPanels; ++h) {
-                    tma_load_4d(st + h * L::kPanelBytes, &tmap_q, bar(L::kBarFull + s), h * 64,
-                                i * 128, hq, b);
-                    tma_load_4d(st + L::kTileBytes + h * L::kPanelBytes, &tmap_do,
-                                bar(L::kBarFull + s), h * 64, i * 128, hq, b);
-                }
+        bool ok = true;
+        auto load_q = [&](int it) {  // Q_it into ring slot it % 3, once dK(it-3) has read it
+            const int s = it % L::kQSlots;
+            ok = mbar_wait_warp<true>(bar(L::kBarQEmpty + s), ((it / L::kQSlots) & 1) ^ 1u,
+                                      abort_flag, status_word);
+            if (ok && lane == 0) {
+                mbar_arrive_expect_tx(bar(L::kBarQFull + s), L::kTileBytes);
+                for (int h = 0; h < kPanels; ++h)
+                    tma_load_4d(sbase + L::kQ + s * L::kTileBytes + h * L::kPanelBytes, &tmap_q,
+                                bar(L::kBarQFull + s), h * 64, it_tile(it) * 128, it_head(it), b);
             }
+        };
+        auto load_vec = [&](int it) {  // vectors of step it, once step it-2 is done with the slot
+            const int s = it & 1;
+            ok = mbar_wait_warp<true>(bar(L::kBarVecFree + s), ((it >> 1) & 1) ^ 1u, abort_flag,
+                                      status_word);
+            if (!ok) return;
             float4* vec = reinterpret_cast<float4*>(smem + L::kVec) + s * 64;
             vec[lane] = make_float4(nl[0], nl[1], nl[2], nl[3]);
             vec[32 + lane] = make_float4(nd[0], nd[1], nd[2], nd[3]);
-            mbar_arrive(bar(L::kBarFull + s));
+            mbar_arrive(bar(L::kBarVecFull + s));
             if (it + 1 < n_it) fetch(it + 1);
+        };
+        auto load_do = [&](int it) {  // dO_it, once dP^T(it-1) and dV(it-1) have read the buffer
+            ok = mbar_wait_warp<true>(bar(L::kBarDoEmpty), (it & 1) ^ 1u, abort_flag, status_word);
+            if (ok && lane == 0) {
+                mbar_arrive_expect_tx(bar(L::kBarDoFull), L::kTileBytes);
+                for (int h = 0; h < kPanels; ++h)
+                    tma_load_4d(sbase + L::kDO + h * L::kPanelBytes, &tmap_do, bar(L::kBarDoFull),
+                                h * 64, it_tile(it) * 128, it_head(it), b);
+            }
+        };
+        if (n_it > 0) {
+            fetch(0);
+            load_q(0);
+        }
+        for (int it = 0; ok && it < n_it; ++it) {  // Q runs a step ahead of dO
+            if (it + 1 < n_it) load_q(it + 1);
+            if (ok) load_vec(it);
+            if (ok) load_do(it);
         }
         __syncwarp();
     } else if (warp == kBwdMmaWarp || warp == kBwdMmaWarpB) {
@@ -287,10 +320,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const bool chain_a = warp == kBwdMmaWarp;
         bool ok = mbar_wait_warp<true>(bar(L::kBarRes), 0, abort_flag, status_word);
         const uint32_t ka = sbase + L::kRes0, va = sbase + L::kRes1, pt = sbase + L::kPt;
-        auto stage_q = [&](int it) { return sbase + L::kStage + (it % kBwdStages) * 2 * L::kTileBytes; };
-        auto wait_full = [&](int it) {
-            const bool w = mbar_wait_warp<true>(bar(L::kBarFull + it % kBwdStages),
-                                                (it / kBwdStages) & 1, abort_flag, status_word);
+        auto stage_q = [&](int it) { return sbase + L::kQ + (it % L::kQSlots) * L::kTileBytes; };
+        const uint32_t da = sbase + L::kDO;
+        auto wait_full = [&](int it) {  // Q_it landed
+            const bool w = mbar_wait_warp<true>(bar(L::kBarQFull + it % L::kQSlots),
+                                                (it / L::kQSlots) & 1, abort_flag, status_word);
+            tc_fence_after();
+            return w;
+        };
+        auto wait_do = [&](int it) {  // dO_it landed
+            const bool w = mbar_wait_warp<true>(bar(L::kBarDoFull), it & 1, abort_flag,
+                                                status_word);
             tc_fence_after();
             return w;
         };
@@ -310,16 +350,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int it = 0; ok && it < n_it; ++it) {
                 if (it + 1 < n_it) {
                     ok = wait_full(it + 1);
-                    if (ok) ok = mbar_wait_warp<true>(bar(L::kBarSFree), it & 1, abort_flag,
-                                                      status_word);
+                    if (ok) ok = mbar_wait_warp(bar(L::kBarSFree), it & 1, abort_flag,
+                                                status_word);
                     if (!ok) break;
                     tc_fence_after();
                     s_mma(it + 1);
                 }
-                ok = mbar_wait_warp<true>(bar(L::kBarP), it & 1, abort_flag, status_word);
+                ok = mbar_wait_warp(bar(L::kBarP), it & 1, abort_flag, status_word);
+                if (ok) ok = wait_do(it);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t da = stage_q(it) + L::kTileBytes;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO_i  (K = 128 queries)
                     mma_bf16_ss_warp(t_dv,
@@ -328,13 +368,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                      smem_desc_sw128(da + kk * 2048, L::kPanelBytes, 1024),
                                      kIdescAcc, (it > 0 || kk > 0) ? 1u : 0u);
                 mma_commit_warp(bar(L::kBarPFree));
-                mma_commit_warp(bar(L::kBarEmpty + it % kBwdStages));
+                mma_commit_warp(bar(L::kBarDoEmpty));
             }
         } else {
             for (int it = 0; ok && it < n_it; ++it) {
-                ok = wait_full(it);
+                ok = wait_do(it);
                 if (!ok) break;
-                const uint32_t qa = stage_q(it), da = qa + L::kTileBytes;
+                const uint32_t qa = stage_q(it);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {  // dP^T = V_j dO_i^T
                     const uint32_t off = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
@@ -342,7 +382,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                      smem_desc_sw128(da + off, 16, 1024), kIdescS, kk > 0);
                 }
                 mma_commit_warp(bar(L::kBarDP));
+                mma_commit_warp(bar(L::kBarDoEmpty));
                 ok = mbar_wait_warp<true>(bar(L::kBarDS), it & 1, abort_flag, status_word);
+                if (ok) ok = wait_full(it);  // Q_it (landed before S^T(it); for visibility)
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
@@ -350,7 +392,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     mma_bf16_ts_warp(t_dk, t_dp + packed_col(kk),
                                      smem_desc_sw128(qa + kk * 2048, L::kPanelBytes, 1024),
                                      kIdescAcc, (it > 0 || kk > 0) ? 1u : 0u);
-                mma_commit_warp(bar(L::kBarEmpty + it % kBwdStages));
+                mma_commit_warp(bar(L::kBarQEmpty + it % L::kQSlots));
             }
         }
         if (ok) mma_commit_warp(bar(L::kBarDone));
@@ -364,12 +406,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const float c = p.scale_log2;
         bool ok = true;
         for (int it = 0; it < n_it; ++it) {
-            const int s = it % kBwdStages;
+            const int s = it & 1;
             const float* vec = reinterpret_cast<const float*>(smem + L::kVec) + s * 256 + c0;
-            // the stage's lse2/Delta vectors were stored by the producer lanes before their
-            // arrive on stage_full: wait on it here too, so those stores are visible
-            ok = mbar_wait_warp(bar(L::kBarFull + s), (it / kBwdStages) & 1, abort_flag,
-                                status_word);
+            // the step's lse2/Delta vectors, stored by the producer lanes before their arrive
+            ok = mbar_wait_warp(bar(L::kBarVecFull + s), (it >> 1) & 1, abort_flag, status_word);
             if (ok) ok = mbar_wait_warp(bar(L::kBarS), it & 1, abort_flag, status_word);
             if (!ok) break;
             tc_fence_after();
@@ -384,11 +424,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 mbar_arrive(bar(L::kBarSFree));  // S^T(it+1) may now be formed over it
 #pragma unroll
                 for (int q = 0; q < 64; q += 4) {
-                    const float4 l4 = *reinterpret_cast<const float4*>(vec + q);
-                    pr[q] = ex2_approx(fmaf(__uint_as_float(r[q]), c, -l4.x));
-                    pr[q + 1] = ex2_approx(fmaf(__uint_as_float(r[q + 1]), c, -l4.y));
-                    pr[q + 2] = ex2_approx(fmaf(__uint_as_float(r[q + 2]), c, -l4.z));
-                    pr[q + 3] = ex2_approx(fmaf(__uint_as_float(r[q + 3]), c, -l4.w));
+                    const float4 l4 = *reinterpret_cast<const float4*>(vec + q);  // -lse2
+                    float x0, x1, x2, x3;
+                    ffma2(x0, x1, __uint_as_float(r[q]), __uint_as_float(r[q + 1]), c, c, l4.x, l4.y);
+                    ffma2(x2, x3, __uint_as_float(r[q + 2]), __uint_as_float(r[q + 3]), c, c, l4.z,
+                          l4.w);
+                    pr[q] = ex2_approx(x0);
+                    pr[q + 1] = ex2_approx(x1);
+                    pr[q + 2] = ex2_approx(x2);
+                    pr[q + 3] = ex2_approx(x3);
                 }
             }
             if (p.causal && it_tile(it) == j) {  // diagonal tile: query q sees key `row` iff q >= row
@@ -413,31 +457,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             fence_proxy_async_smem();
             mbar_arrive(bar(L::kBarP));
-            // dS^T row: ds[q] = p[q] (dp[q] - Delta_q), in 32-column chunks; chunk cc's packed
-            // result lands in this warp's dP^T columns already read (c0+16cc .. < c0+32cc+32).
+            // dS^T row: ds[q] = p[q] (dp[q] - Delta_q); this warp's 64 dP^T columns are read in one
+            // go, and the 32 packed results go over the first 32 of them.
             ok = mbar_wait_warp(bar(L::kBarDP), it & 1, abort_flag, status_word);
             if (!ok) break;
             tc_fence_after();
-#pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                uint32_t r[32];
-                tmem_ld32(lane_base + t_dp + c0 + cc * 32, r);
+            {
+                uint32_t r[64];
+                tmem_ld32(lane_base + t_dp + c0, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                tmem_ld32(lane_base + t_dp + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
                 tmem_wait_ld();
-                uint32_t pk[16];
+                uint32_t pk[32];
 #pragma unroll
-                for (int x = 0; x < 16; x += 2) {
-                    const int q = cc * 32 + 2 * x;
-                    const float4 d4 = *reinterpret_cast<const float4*>(vec + 128 + q);
-                    pk[x] = pack_bf16x2(pr[q] * (__uint_as_float(r[2 * x]) - d4.x),
-                                        pr[q + 1] * (__uint_as_float(r[2 * x + 1]) - d4.y));
-                    pk[x + 1] = pack_bf16x2(pr[q + 2] * (__uint_as_float(r[2 * x + 2]) - d4.z),
-                                            pr[q + 3] * (__uint_as_float(r[2 * x + 3]) - d4.w));
+                for (int q = 0; q < 64; q += 4) {
+                    const float4 d4 = *reinterpret_cast<const float4*>(vec + 128 + q);  // -Delta
+                    float t0, t1, t2, t3, d0, d1, d2, d3;
+                    fadd2(t0, t1, __uint_as_float(r[q]), __uint_as_float(r[q + 1]), d4.x, d4.y);
+                    fadd2(t2, t3, __uint_as_float(r[q + 2]), __uint_as_float(r[q + 3]), d4.z, d4.w);
+                    ffma2(d0, d1, pr[q], pr[q + 1], t0, t1, 0.f, 0.f);
+                    ffma2(d2, d3, pr[q + 2], pr[q + 3], t2, t3, 0.f, 0.f);
+                    pk[q / 2] = pack_bf16x2(d0, d1);
+                    pk[q / 2 + 1] = pack_bf16x2(d2, d3);
                 }
-                tmem_st16(lane_base + t_dp + c0 + cc * 16, pk);
+                tmem_st32(lane_base + t_dp + c0, pk);
             }
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bar(L::kBarDS));
+            mbar_arrive(bar(L::kBarVecFree + s));  // this step's vectors are no longer read
         }
         // epilogue: dK = sm_scale * acc (warps 0-3), dV = acc (warps 4-7) -> bf16 -> smem (over
         // K_j, V_j) -> TMA store
@@ -468,6 +515,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
 }
 
+// dQ layout: Q_i and dO_i resident, then separate rings for K (3 slots: K_j is read by S(j),
+// formed a step ahead, and by dQ(j), issued last) and V (2 slots: read only by dP(j)), so the
+// load of K_(j+2) never waits for dQ(j) to finish.
+template <int D>
+struct DqSmem {
+    static constexpr int kPanelBytes = 128 * 64 * 2;
+    static constexpr int kTileBytes = 128 * D * 2;
+    static constexpr int kKSlots = 3, kVSlots = 2;
+    static constexpr int kRes0 = 0;                        // Q_i
+    static constexpr int kRes1 = kTileBytes;               // dO_i
+    static constexpr int kK = 2 * kTileBytes;              // K ring
+    static constexpr int kV = kK + kKSlots * kTileBytes;   // V ring
+    static constexpr int kBars = kV + kVSlots * kTileBytes;
+    static constexpr int kBarRes = 0;
+    static constexpr int kBarKFull = 1;                      // [kKSlots]
+    static constexpr int kBarKEmpty = kBarKFull + kKSlots;   // [kKSlots]
+    static constexpr int kBarVFull = kBarKEmpty + kKSlots;   // [kVSlots]
+    static constexpr int kBarVEmpty = kBarVFull + kVSlots;   // [kVSlots]
+    static constexpr int kBarS = kBarVEmpty + kVSlots;       // [2]
+    static constexpr int kBarDP = kBarS + 2;
+    static constexpr int kBarDS = kBarDP + 1;
+    static constexpr int kBarDone = kBarDS + 1;
+    static constexpr int kNumBars = kBarDone + 1;
+    static constexpr int kTmemSlot = kBars + kNumBars * 8;
+    static constexpr int kAbort = kTmemSlot + 8;
+    static constexpr int kBytes = kAbort + 8;
+    static constexpr int kAlloc = kBytes + 1024;
+    static_assert(kAlloc <= 232448, "dQ shared memory exceeds the per-block limit");
+};
+
 // ------------------------------------------------------------------------------------------------
 // dQ
 // ------------------------------------------------------------------------------------------------
@@ -479,7 +556,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                        const __grid_constant__ CUtensorMap tmap_do,
                        const __grid_constant__ CUtensorMap tmap_dq, const BwdParams p,
                        unsigned int* status_word) {
-    using L = BwdSmem<D>;
+    using L = DqSmem<D>;
     constexpr int kPanels = D / 64;
     constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, 0);
     constexpr uint32_t kIdescAcc = idesc_bf16_f32(128, D, 1);
@@ -501,9 +578,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(bar(L::kBarRes), 1);
-        for (int s = 0; s < kBwdStages; ++s) {
-            mbar_init(bar(L::kBarFull + s), 1);
-            mbar_init(bar(L::kBarEmpty + s), 2);  // one release per issuer
+        for (int s = 0; s < L::kKSlots; ++s) {
+            mbar_init(bar(L::kBarKFull + s), 1);
+            mbar_init(bar(L::kBarKEmpty + s), 1);
+        }
+        for (int s = 0; s < L::kVSlots; ++s) {
+            mbar_init(bar(L::kBarVFull + s), 1);
+            mbar_init(bar(L::kBarVEmpty + s), 1);
         }
         mbar_init(bar(L::kBarS), 1);
         mbar_init(bar(L::kBarS + 1), 1);
@@ -527,6 +608,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t t_s0 = tmem, t_dp = tmem + 128, t_dq = tmem + 256, t_s1 = tmem + 384;
 
     if (warp == kBwdLoadWarp) {
+        // lane 0: Q_i, dO_i, then the K ring; lane 1: the V ring (independent streams)
         if (lane == 0) {
             mbar_arrive_expect_tx(bar(L::kBarRes), 2 * L::kTileBytes);
             for (int h = 0; h < kPanels; ++h) {
@@ -536,18 +618,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                             h * 64, i * 128, hq, b);
             }
             for (int it = 0; it < n_it; ++it) {
-                const int s = it % kBwdStages;
-                const uint32_t ph = (it / kBwdStages) & 1;
-                if (!mbar_wait_bounded<true>(bar(L::kBarEmpty + s), ph ^ 1u, abort_flag, status_word))
+                const int s = it % L::kKSlots;
+                if (!mbar_wait_bounded<true>(bar(L::kBarKEmpty + s), ((it / L::kKSlots) & 1) ^ 1u,
+                                             abort_flag, status_word))
                     break;
-                const uint32_t st = sbase + L::kStage + s * 2 * L::kTileBytes;
-                mbar_arrive_expect_tx(bar(L::kBarFull + s), 2 * L::kTileBytes);
-                for (int h = 0; h < kPanels; ++h) {
-                    tma_load_4d(st + h * L::kPanelBytes, &tmap_k, bar(L::kBarFull + s), h * 64,
-                                it * 128, hkv, b);
-                    tma_load_4d(st + L::kTileBytes + h * L::kPanelBytes, &tmap_v,
-                                bar(L::kBarFull + s), h * 64, it * 128, hkv, b);
-                }
+                mbar_arrive_expect_tx(bar(L::kBarKFull + s), L::kTileBytes);
+                for (int h = 0; h < kPanels; ++h)
+                    tma_load_4d(sbase + L::kK + s * L::kTileBytes + h * L::kPanelBytes, &tmap_k,
+                                bar(L::kBarKFull + s), h * 64, it * 128, hkv, b);
+            }
+        } else if (lane == 1) {
+            for (int it = 0; it < n_it; ++it) {
+                const int s = it % L::kVSlots;
+                if (!mbar_wait_bounded<true>(bar(L::kBarVEmpty + s), ((it / L::kVSlots) & 1) ^ 1u,
+                                             abort_flag, status_word))
+                    break;
+                mbar_arrive_expect_tx(bar(L::kBarVFull + s), L::kTileBytes);
+                for (int h = 0; h < kPanels; ++h)
+                    tma_load_4d(sbase + L::kV + s * L::kTileBytes + h * L::kPanelBytes, &tmap_v,
+                                bar(L::kBarVFull + s), h * 64, it * 128, hkv, b);
             }
         }
         __syncwarp();
@@ -557,10 +646,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const bool chain_a = warp == kBwdMmaWarp;
         bool ok = mbar_wait_warp<true>(bar(L::kBarRes), 0, abort_flag, status_word);
         const uint32_t qa = sbase + L::kRes0, da = sbase + L::kRes1;
-        auto stage_k = [&](int it) { return sbase + L::kStage + (it % kBwdStages) * 2 * L::kTileBytes; };
-        auto wait_full = [&](int it) {
-            const bool w = mbar_wait_warp<true>(bar(L::kBarFull + it % kBwdStages),
-                                          (it / kBwdStages) & 1, abort_flag, status_word);
+        auto stage_k = [&](int it) { return sbase + L::kK + (it % L::kKSlots) * L::kTileBytes; };
+        auto stage_v = [&](int it) { return sbase + L::kV + (it % L::kVSlots) * L::kTileBytes; };
+        auto wait_k = [&](int it) {
+            const bool w = mbar_wait_warp<true>(bar(L::kBarKFull + it % L::kKSlots),
+                                                (it / L::kKSlots) & 1, abort_flag, status_word);
+            tc_fence_after();
+            return w;
+        };
+        auto wait_v = [&](int it) {
+            const bool w = mbar_wait_warp<true>(bar(L::kBarVFull + it % L::kVSlots),
+                                                (it / L::kVSlots) & 1, abort_flag, status_word);
             tc_fence_after();
             return w;
         };
@@ -575,11 +671,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mma_commit_warp(bar(L::kBarS + (it & 1)));
         };
         if (chain_a) {
-            if (ok && n_it > 0) ok = wait_full(0);
+            if (ok && n_it > 0) ok = wait_k(0);
             if (ok && n_it > 0) s_mma(0);
             for (int it = 0; ok && it < n_it; ++it) {
-                if (it + 1 < n_it) {  // stage it+1 is free of it-1 (both chains released it)
-                    ok = wait_full(it + 1);
+                if (it + 1 < n_it) {
+                    ok = wait_k(it + 1);
                     if (!ok) break;
                     s_mma(it + 1);
                 }
@@ -592,19 +688,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     mma_bf16_ts_warp(t_dq, ts + packed_col(kk),
                                      smem_desc_sw128(ka + kk * 2048, L::kPanelBytes, 1024),
                                      kIdescAcc, (it > 0 || kk > 0) ? 1u : 0u);
-                mma_commit_warp(bar(L::kBarEmpty + it % kBwdStages));
+                mma_commit_warp(bar(L::kBarKEmpty + it % L::kKSlots));
             }
             if (ok) mma_commit_warp(bar(L::kBarDone));
         } else {
             for (int it = 0; ok && it < n_it; ++it) {
-                ok = wait_full(it);
+                ok = wait_v(it);
                 if (!ok) break;
                 if (it > 0) {  // dP(it) overwrites dP(it-1): the elementwise warps must have read it
                     ok = mbar_wait_warp<true>(bar(L::kBarDS), (it - 1) & 1, abort_flag, status_word);
                     if (!ok) break;
                     tc_fence_after();
                 }
-                const uint32_t va = stage_k(it) + L::kTileBytes;
+                const uint32_t va = stage_v(it);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {  // dP = dO_i V_j^T
                     const uint32_t off = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
@@ -612,7 +708,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                      smem_desc_sw128(va + off, 16, 1024), kIdescS, kk > 0);
                 }
                 mma_commit_warp(bar(L::kBarDP));
-                mma_commit_warp(bar(L::kBarEmpty + it % kBwdStages));
+                mma_commit_warp(bar(L::kBarVEmpty + it % L::kVSlots));
             }
         }
         __syncwarp();
