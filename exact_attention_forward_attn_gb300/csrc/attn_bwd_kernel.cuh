@@ -679,7 +679,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     if (!ok) break;
                     s_mma(it + 1);
                 }
-                ok = mbar_wait_warp<true>(bar(L::kBarDS), it & 1, abort_flag, status_word);
+                ok = mbar_wait_warp(bar(L::kBarDS), it & 1, abort_flag, status_word);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t ka = stage_k(it), ts = (it & 1) ? t_s1 : t_s0;
@@ -736,8 +736,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tmem_ld32(lane_base + ts + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
                 tmem_wait_ld();
 #pragma unroll
-                for (int k = 0; k < 64; ++k)
-                    pr[k] = ex2_approx(fmaf(__uint_as_float(r[k]), c, -lse2));
+                for (int k = 0; k < 64; k += 2) {
+                    float x0, x1;
+                    ffma2(x0, x1, __uint_as_float(r[k]), __uint_as_float(r[k + 1]), c, c, -lse2,
+                          -lse2);
+                    pr[k] = ex2_approx(x0);
+                    pr[k + 1] = ex2_approx(x1);
+                }
             }
             if (p.causal && it == i) {  // diagonal tile: key k visible to query `row` iff k <= row
 #pragma unroll
@@ -756,8 +761,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
                 for (int x = 0; x < 16; ++x) {
                     const int k = cc * 32 + 2 * x;
-                    pk[x] = pack_bf16x2(pr[k] * (__uint_as_float(r[2 * x]) - dlt),
-                                        pr[k + 1] * (__uint_as_float(r[2 * x + 1]) - dlt));
+                    float t0, t1, d0, d1;
+                    fadd2(t0, t1, __uint_as_float(r[2 * x]), __uint_as_float(r[2 * x + 1]), -dlt,
+                          -dlt);
+                    ffma2(d0, d1, pr[k], pr[k + 1], t0, t1, 0.f, 0.f);
+                    pk[x] = pack_bf16x2(d0, d1);
                 }
                 tmem_st16(lane_base + ts + c0 + cc * 16, pk);
             }
