@@ -5,12 +5,13 @@
 // the wide heads the robustness row asks for ("Triton-CUDA Attention", skillmd.com, pads D to a
 // power of two; D is zero-padded to 256 here by the TMA).  At D = 256 one Q tile's fp32 output
 // already takes 256 TMEM columns, so a CTA holds one 128-row Q tile instead of two:
-//   TMEM (512 columns): S[2] (128 each, double-buffered: S(j+1) forms while the softmax works
-//   on S(j); P (bf16) is written over the first 64 columns of its S) | O (256).
-//   Shared memory: Q (4 panels, 64 KiB, loaded once, reused to stage O), a 6-slot ring of 16 KiB
-//   K panels (128 keys x 64 columns; S accumulates over the four panels of a key tile, each slot
-//   refilled as soon as its MMAs have read it), V (4 panels, 64 KiB, the MN-major B operand of
-//   one N=256 MMA per 16 keys).
+//   TMEM (512 columns): S[2] (128 each, double-buffered: S(j+2) forms as soon as the softmax
+//   has read S(j)) | O (256).
+//   Shared memory: Q (4 panels, 64 KiB, loaded once, reused to stage O), a 4-slot ring of 16 KiB
+//   K panels (128 keys x 64 columns; S accumulates over the four panels of a key tile, issued
+//   panel by panel, each slot refilled as soon as its MMAs have read it), P (bf16, two 128B-
+//   swizzled 128 x 64 panels, the K-major A operand of P.V), V (4 panels, 64 KiB, the MN-major
+//   B operand of one N=256 MMA per 16 keys).
 // Warps: 0-3 softmax (one row per thread), 4 issues S, 5 issues P.V, 6 loads (lane 0: Q and the
 // K ring; lane 1: V).
 #pragma once
@@ -29,10 +30,11 @@ constexpr int kW256MmaS = 4, kW256MmaPV = 5, kW256Load = 6;
 
 struct Fwd256Smem {
     static constexpr int kPanel = 128 * 128;  // 128 rows x 64 bf16
-    static constexpr int kKSlots = 6;
+    static constexpr int kKSlots = 4;
     static constexpr int kQ = 0;
     static constexpr int kK = kQ + 4 * kPanel;
-    static constexpr int kV = kK + kKSlots * kPanel;
+    static constexpr int kP = kK + kKSlots * kPanel;
+    static constexpr int kV = kP + 2 * kPanel;
     static constexpr int kBars = kV + 4 * kPanel;
     static constexpr int kBarQ = 0;
     static constexpr int kBarKFull = 1;                    // [kKSlots]
@@ -42,7 +44,8 @@ struct Fwd256Smem {
     static constexpr int kBarSFull = kBarVEmpty + 1;  // [2]
     static constexpr int kBarPFull = kBarSFull + 2;   // [2] (count 128)
     static constexpr int kBarPvDone = kBarPFull + 2;  // [2]
-    static constexpr int kNumBars = kBarPvDone + 2;
+    static constexpr int kBarSFree = kBarPvDone + 2;  // [2] the softmax has read S (count 128)
+    static constexpr int kNumBars = kBarSFree + 2;
     static constexpr int kTmemSlot = kBars + kNumBars * 8;
     static constexpr int kAbort = kTmemSlot + 8;
     static constexpr int kBytes = kAbort + 8;
@@ -91,6 +94,7 @@ __global__ void __launch_bounds__(kW256Threads, 1)
             mbar_init(bar(L::kBarSFull + i), 1);
             mbar_init(bar(L::kBarPFull + i), 128);
             mbar_init(bar(L::kBarPvDone + i), 1);
+            mbar_init(bar(L::kBarSFree + i), 128);
         }
         *abort_flag = 0;
         fence_mbarrier_init();
@@ -138,39 +142,38 @@ __global__ void __launch_bounds__(kW256Threads, 1)
         }
         __syncwarp();
     } else if (warp == kW256MmaS) {
-        // S(j) = Q K_j^T into buffer j&1, once P.V(j-2) has read the P written over it
+        // S(j) = Q K_j^T into buffer j&1, once the softmax has read S(j-2)
         bool ok = mbar_wait_warp(bar(L::kBarQ), 0, abort_flag, status_word);
         for (int j = 0; ok && j < n_kv; ++j) {
             if (j >= 2) {
-                ok = mbar_wait_warp(bar(L::kBarPvDone + (j & 1)), ((j - 2) >> 1) & 1, abort_flag,
+                ok = mbar_wait_warp(bar(L::kBarSFree + (j & 1)), ((j - 2) >> 1) & 1, abort_flag,
                                     status_word);
                 if (!ok) break;
+                tc_fence_after();
             }
-            for (int pn = 0; pn < 4; ++pn) {
+            // panel by panel: each panel's MMAs start as soon as it lands, and its slot is
+            // released as soon as they have read it
+            for (int pn = 0; ok && pn < 4; ++pn) {
                 const int k = 4 * j + pn;
                 ok = mbar_wait_warp(bar(L::kBarKFull + k % L::kKSlots), (k / L::kKSlots) & 1,
                                     abort_flag, status_word);
                 if (!ok) break;
-            }
-            if (!ok) break;
-            tc_fence_after();
-#pragma unroll
-            for (int pn = 0; pn < 4; ++pn) {
-                const uint32_t kp = sbase + L::kK + ((4 * j + pn) % L::kKSlots) * L::kPanel;
+                tc_fence_after();
+                const uint32_t kp = sbase + L::kK + (k % L::kKSlots) * L::kPanel;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     mma_bf16_ss_warp(t_s(j),
                                      smem_desc_sw128(sbase + L::kQ + pn * L::kPanel + kk * 32, 16, 1024),
                                      smem_desc_sw128(kp + kk * 32, 16, 1024), kIdescS,
                                      (pn > 0 || kk > 0) ? 1u : 0u);
+                mma_commit_warp(bar(L::kBarKEmpty + k % L::kKSlots));
             }
-            for (int pn = 0; pn < 4; ++pn)
-                mma_commit_warp(bar(L::kBarKEmpty + (4 * j + pn) % L::kKSlots));
+            if (!ok) break;
             mma_commit_warp(bar(L::kBarSFull + (j & 1)));
         }
         __syncwarp();
     } else if (warp == kW256MmaPV) {
-        // O += P(j) V_j: A = P from TMEM (over S(j)), B = the four V panels (N = 256)
+        // O += P(j) V_j: A = P from shared memory, B = the four V panels (N = 256)
         bool ok = true;
         for (int j = 0; ok && j < n_kv; ++j) {
             ok = mbar_wait_warp(bar(L::kBarVFull), j & 1, abort_flag, status_word);
@@ -180,7 +183,9 @@ __global__ void __launch_bounds__(kW256Threads, 1)
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-                mma_bf16_ts_warp(t_o, t_s(j) + kk * 8,
+                mma_bf16_ss_warp(t_o,
+                                 smem_desc_sw128(sbase + L::kP + (kk >> 2) * L::kPanel + (kk & 3) * 32,
+                                                 16, 1024),
                                  smem_desc_sw128(sbase + L::kV + kk * 2048, L::kPanel, 1024),
                                  kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
             mma_commit_warp(bar(L::kBarPvDone + (j & 1)));
@@ -208,6 +213,8 @@ __global__ void __launch_bounds__(kW256Threads, 1)
                     tmem_ld32(lane_base + t_s(j) + cc * 32,
                               *reinterpret_cast<uint32_t(*)[32]>(&r[cc * 32]));
                 tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(bar(L::kBarSFree + (j & 1)));  // S(j+2) may now be formed over it
 #pragma unroll
                 for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(r[i]);
             }
@@ -236,27 +243,34 @@ __global__ void __launch_bounds__(kW256Threads, 1)
             m = m_new;
             const float neg_m = -m;
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            uint32_t pk[64];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int col = h * 64 + 2 * i;
-                    float x0, x1;
-                    ffma2(x0, x1, s[col], s[col + 1], c, c, neg_m, neg_m);
-                    const float p0 = ex2_approx(x0);
-                    const float p1 = ex2_approx(x1);
-                    const int a = (i & 1) * 2;
-                    fadd2(acc[a], acc[a + 1], acc[a], acc[a + 1], p0, p1);
-                    pk[i] = pack_bf16x2(p0, p1);
-                }
-                tmem_st32(lane_base + t_s(j) + h * 32, pk);  // over S(j), already read
+            for (int i = 0; i < 64; ++i) {
+                float x0, x1;
+                ffma2(x0, x1, s[2 * i], s[2 * i + 1], c, c, neg_m, neg_m);
+                const float p0 = ex2_approx(x0);
+                const float p1 = ex2_approx(x1);
+                const int a = (i & 1) * 2;
+                fadd2(acc[a], acc[a + 1], acc[a], acc[a + 1], p0, p1);
+                pk[i] = pack_bf16x2(p0, p1);
             }
-            if (rescale) {  // O *= alpha once P.V(j-1) has landed
+            // P.V(j-1) must have read the previous P (and landed, for the O correction)
+            if (j > 0) {
                 ok = mbar_wait_warp(bar(L::kBarPvDone + ((j - 1) & 1)), ((j - 1) >> 1) & 1,
                                     abort_flag, status_word);
                 if (!ok) break;
                 tc_fence_after();
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {  // keys 64h .. 64h+63 -> panel h, 128B swizzle
+                const uint32_t prow = sbase + L::kP + h * L::kPanel + row * 128;
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch)
+                    st_shared_v4(prow + ((ch ^ (row & 7)) << 4), pk[32 * h + 4 * ch],
+                                 pk[32 * h + 4 * ch + 1], pk[32 * h + 4 * ch + 2],
+                                 pk[32 * h + 4 * ch + 3]);
+            }
+            if (rescale) {  // O *= alpha
 #pragma unroll 1
                 for (int cc = 0; cc < 8; ++cc) {
                     uint32_t o[32];
@@ -268,6 +282,7 @@ __global__ void __launch_bounds__(kW256Threads, 1)
                 }
             }
             tmem_wait_st();
+            fence_proxy_async_smem();  // generic-proxy P stores -> the MMA's async reads
             tc_fence_before();
             mbar_arrive(bar(L::kBarPFull + (j & 1)));
             l = l * alpha + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
