@@ -141,6 +141,25 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """The largest `value` over the ranks of the default process group (the value itself when
+    there is none).  NCCL needs a CUDA tensor; gloo (the CPU tests) a CPU one."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world: int, max_seconds: float) -> float:
+    """Whole-job rate of independent replicas: every rank's units over the slowest rank's time
+    (weak scaling: each rank processes the same amount of work)."""
+    return units_per_rank * world / max_seconds
+
+
 def cpu_sample_rows(w, n_rows_per_head):
     """Seeded query rows for the CPU oracle's bounded sample (same rows for every head)."""
     import torch
@@ -362,17 +381,13 @@ def main():
         torch.cuda.synchronize()
         if pg:
             pg.barrier()
-    total_ms = sum(launch_ms)
-    if pg:
-        t = torch.tensor([total_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(launch_ms), dev)
     if attn.device_status(dev) != 0:
         raise SystemExit("device status word reports an expired wait in the timed region")
     clocks = sampler.summary()
 
     ms_per_step = total_ms / args.steps
-    value = w.flops * args.steps * world / (total_ms * 1e-3) / 1e12
+    value = job_throughput(w.flops * args.steps, world, total_ms * 1e-3) / 1e12
     mean_launch_ms = statistics.mean(launch_ms)
     achieved = w.flops / (mean_launch_ms * 1e-3) / 1e12
     peaks, peak_src = load_peaks()
