@@ -42,6 +42,9 @@ CASES = [
     wl.random_case(1, 6, 2, 129, 96, True, 43),
     wl.random_case(2, 4, 1, 200, 128, False, 44),
     wl.random_case(1, 8, 2, 640, 128, True, 45),
+    # GQA-8 over 8 key tiles: 64 steps per dK/dV CTA, so every operand ring wraps many times
+    wl.random_case(1, 8, 1, 1024, 128, True, 47),
+    wl.random_case(1, 4, 1, 1000, 64, False, 48),
 ]
 
 
