@@ -71,15 +71,17 @@ __global__ void __launch_bounds__(kW256Threads, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // work: (batch, KV head) outermost so the CTAs in flight share K/V in L2, then Q tiles
-    // heaviest (latest) first, then the query heads of the group
+    // work: blocks of kv_block (batch, KV head) pairs whose K/V fit in L2 together; within a
+    // block, Q tiles heaviest (latest) first, then the KV heads, then the query heads of each
     const int item = static_cast<int>(blockIdx.x);
     const int per_kv = p.n_tiles * p.group;
-    const int bh_kv = item / per_kv;
-    const int rem = item % per_kv;
-    const int m_tile = p.n_tiles - 1 - rem / p.group;
+    const int blk = item / (p.kv_block * per_kv);
+    const int in_blk = item % (p.kv_block * per_kv);
+    const int kvs = min(p.kv_block, p.B * p.Hkv - blk * p.kv_block);
+    const int bh_kv = blk * p.kv_block + (in_blk % (kvs * p.group)) / p.group;
+    const int m_tile = p.n_tiles - 1 - in_blk / (kvs * p.group);
     const int b = bh_kv / p.Hkv, hkv = bh_kv % p.Hkv;
-    const int hq = hkv * p.group + rem % p.group;
+    const int hq = hkv * p.group + in_blk % p.group;
     const int n_kv = p.causal ? m_tile + 1 : p.n_tiles;  // key tiles 0 .. n_kv-1
 
     if (threadIdx.x == 0) {

@@ -54,6 +54,7 @@ struct AttnParams {
     int n_tiles;       // ceil(N / 128): number of Q tiles and of KV tiles per head
     int n_pairs;       // ceil(n_tiles / 2): CTAs per (b, hq)
     float scale_log2;  // sm_scale * log2(e)
+    int kv_block;      // (batch, KV head) pairs per scheduling block (their K/V fit in L2)
     float* lse;        // [B, Hq, N] fp32
     // split-KV partials (split instantiation only): KV tiles [s*split_tiles, (s+1)*split_tiles)
     int n_splits;
@@ -123,9 +124,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
 
     // ---- work decomposition --------------------------------------------------------------------
-    // Block order: (batch, KV head) outermost, then Q-tile pairs heaviest (latest) first, then the
-    // query heads sharing that KV head.  CTAs running together read the same K/V (which stays in
-    // L2), and the grid ends on the lightest causal pairs.
+    // Block order: blocks of kv_block (batch, KV head) pairs whose K/V fit in L2 together; within
+    // a block, Q-tile pairs heaviest (latest) first, then the KV heads, then the query heads
+    // sharing each KV head.  CTAs running together read K/V of one block (which stays in L2), and
+    // every block (and so the grid) ends on its lightest causal pairs.
     int item = static_cast<int>(blockIdx.x);
     int split = 0;
     if constexpr (kSplit) {
@@ -133,12 +135,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         item /= p.n_splits;
     }
     const int per_kv = p.n_pairs * p.group;
-    const int bh_kv = item / per_kv;
-    const int rem = item % per_kv;
-    const int pair = p.n_pairs - 1 - rem / p.group;
+    const int blk = item / (p.kv_block * per_kv);
+    const int in_blk = item % (p.kv_block * per_kv);
+    const int kvs = min(p.kv_block, p.B * p.Hkv - blk * p.kv_block);  // KV heads in this block
+    const int bh_kv = blk * p.kv_block + (in_blk % (kvs * p.group)) / p.group;
+    const int rem = in_blk % p.group;
+    const int pair = p.n_pairs - 1 - in_blk / (kvs * p.group);
     const int b = bh_kv / p.Hkv;
     const int hkv = bh_kv % p.Hkv;
-    const int hq = hkv * p.group + rem % p.group;
+    const int hq = hkv * p.group + rem;
     const int bh = b * p.Hq + hq;
     const int tile0 = 2 * pair;
     // This CTA's KV tiles: [kv_begin, kv_limit).  Each Q tile t uses [kv_begin, last_t]; under the
