@@ -276,14 +276,15 @@ int validate(Problem& P, bool* empty) {
     return ATTN_OK;
 }
 
-// (batch, KV head) pairs per scheduling block: at most as many as keep their K and V within half
-// of the 129 MB L2 (so the CTAs in flight, which work on one block, re-read nothing from DRAM),
-// spread evenly over the blocks so that no block is much smaller than the others (each block
-// starts on its heaviest causal tiles, so a small last block would leave a long tail).
+// (batch, KV head) pairs per scheduling block: at most as many as keep their K and V within
+// 16 MB (measured: blocks of 50-67 MB of K/V, a die's share of the 129 MB L2, made the CTAs in
+// flight read K/V from DRAM about twice), spread evenly over the blocks so that no block is much
+// smaller than the others (each block starts on its heaviest causal tiles, so a small last block
+// would leave a long tail).
 int kv_block_for(const Problem& P) {
     const int64_t d_pad = P.D <= 64 ? 64 : (P.D <= 128 ? 128 : 256);
     const int64_t kv_bytes = std::max<int64_t>(1, 2 * static_cast<int64_t>(P.N) * d_pad * 2);
-    const int64_t budget = int64_t(64) << 20;
+    const int64_t budget = int64_t(16) << 20;
     const int64_t most = std::max<int64_t>(1, std::min<int64_t>(P.bh_kv, budget / kv_bytes));
     const int64_t blocks = (P.bh_kv + most - 1) / most;
     return static_cast<int>((P.bh_kv + blocks - 1) / blocks);
