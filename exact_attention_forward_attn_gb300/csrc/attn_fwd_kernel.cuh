@@ -161,9 +161,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- setup ---------------------------------------------------------------------------------
     if (threadIdx.x == 0) {
-        mbar_init(bar(L::kBarQ), 1);
+        mbar_init(bar(L::kBarQ), n_part > 0 ? n_part * kPanels : 1);  // one arrive per Q panel
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(bar(L::kBarKvFull + s), 1);
+            mbar_init(bar(L::kBarKvFull + s), kPanels);  // one arrive (+ tx) per panel
             mbar_init(bar(L::kBarKvEmpty + s), n_part > 0 ? n_part : 1);  // one release per issuer
         }
         for (int t = 0; t < 2; ++t) {
@@ -194,31 +194,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp == kLoadWarp) {
-        // =========================== TMA producer (one lane) ===================================
-        if (lane == 0 && n_part > 0) {
-            mbar_arrive_expect_tx(bar(L::kBarQ), n_part * L::kTileBytes);
-            for (int t = 0; t < 2; ++t)
-                if (t == 0 ? part0 : part1)
-                    for (int h = 0; h < kPanels; ++h)
-                        tma_load_4d(sbase + L::kQ + t * L::kTileBytes + h * L::kPanelBytes,
-                                    &tmap_q, bar(L::kBarQ), h * 64, (tile0 + t) * kBM, hq, b);
-            for (int j = kv_begin; j < kv_end; ++j) {
-                for (int kv = 0; kv < 2; ++kv) {
-                    const int idx = 2 * (j - kv_begin) + kv;
-                    const int slot = idx % kStages;
-                    const uint32_t ph = (idx / kStages) & 1;
-                    if (!mbar_wait_bounded(bar(L::kBarKvEmpty + slot), ph ^ 1u, abort_flag,
-                                           status_word))
-                        goto producer_done;
-                    if (idx == p.stall_item) continue;  // test hook: never deliver this item
-                    mbar_arrive_expect_tx(bar(L::kBarKvFull + slot), L::kTileBytes);
-                    const CUtensorMap* map = kv ? &tmap_v : &tmap_k;
-                    for (int h = 0; h < kPanels; ++h)
-                        tma_load_4d(sbase + L::kKV + slot * L::kTileBytes + h * L::kPanelBytes, map,
-                                    bar(L::kBarKvFull + slot), h * 64, j * kBN, hkv, b);
-                }
+        // ====================== TMA producer: one lane per 64-column panel =======================
+        // One thread's bulk tensor copies are processed one after another (measured: ~29 bytes
+        // per cycle per SM from one issuing thread, ~50 from two, ~85 from four), so lane
+        // kv*kPanels + h streams panel h of every K (kv = 0) or V (kv = 1) tile, and the Q panels
+        // are spread over the same lanes.  Each lane arrives with its own panel's bytes.
+        if (lane < 2 * kPanels && n_part > 0) {
+            const int kv = lane / kPanels, h = lane % kPanels;
+            if (kv == 0 ? part0 : part1) {  // Q tile kv, panel h
+                mbar_arrive_expect_tx(bar(L::kBarQ), L::kPanelBytes);
+                tma_load_4d(sbase + L::kQ + kv * L::kTileBytes + h * L::kPanelBytes, &tmap_q,
+                            bar(L::kBarQ), h * 64, (tile0 + kv) * kBM, hq, b);
             }
-        producer_done:;
+            const CUtensorMap* map = kv ? &tmap_v : &tmap_k;
+            for (int j = kv_begin; j < kv_end; ++j) {
+                const int idx = 2 * (j - kv_begin) + kv;
+                const int slot = idx % kStages;
+                const uint32_t ph = (idx / kStages) & 1;
+                if (!mbar_wait_bounded(bar(L::kBarKvEmpty + slot), ph ^ 1u, abort_flag,
+                                       status_word))
+                    break;
+                if (idx == p.stall_item) continue;  // test hook: never deliver this item
+                mbar_arrive_expect_tx(bar(L::kBarKvFull + slot), L::kPanelBytes);
+                tma_load_4d(sbase + L::kKV + slot * L::kTileBytes + h * L::kPanelBytes, map,
+                            bar(L::kBarKvFull + slot), h * 64, j * kBN, hkv, b);
+            }
         }
         __syncwarp();
     } else if (warp == kMmaWarp0 || warp == kMmaWarp0 + 1) {

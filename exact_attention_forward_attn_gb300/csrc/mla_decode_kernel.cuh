@@ -16,17 +16,18 @@
 // One CTA per (batch, 128-head tile, value half r, token split).  The 128 heads are the MMA's M.
 // A 512-wide fp32 output would fill the whole TMEM, so each CTA of a pair owns 256 output columns
 // (c_kv panels 4r .. 4r+3, its "value panels") and both form the full scores; the cache tile is
-// read by both from L2.  Per 64-token tile the scores are two accumulators, S_a over the 5 other
-// panels and S_b over the 4 value panels, issued by two warps (the M=128, N=64 MMAs are
-// issue-bound, not pipe-bound); O += P V is one N=256 MMA per 16 tokens.
-//   TMEM (512 columns): S_a (64) | S_b (64) | P (32, bf16) | three Q panels (3 x 32, bf16, the
-//   A operand of their S_a MMAs) | O (256).
-//   Shared memory: the other six Q panels (96 KiB); X = a ring of 8 slots of 8 KiB through which
-//   the 5 other cache panels of every tile stream (a slot is refilled as soon as its MMAs have
-//   read it, so loads run 1.6 tiles ahead); Y = the 4 value panels, double-buffered (2 x 32 KiB,
-//   also the B operand of P.V).  The three TMEM-bound Q panels are staged through the X ring at
-//   start.
-// Warps: 0-3 softmax (one head row per thread), 4 issues S_a, 5 issues S_b and P.V, 6 loads.
+// read by both from L2.  Per 64-token tile the scores take 36 M=128, N=64 MMAs (one issuing
+// warp keeps up with the tensor pipe at that size); O += P V is one N=256 MMA per 16 tokens,
+// issued by a second warp.
+//   TMEM (512 columns): S (64; S(i+1) is issued as soon as the softmax has loaded S(i)) |
+//   P (32, bf16) | the five X-side Q panels (5 x 32, bf16, the A operand of their score MMAs) |
+//   O (256).
+//   Shared memory: the four value-side Q panels (64 KiB); Y = the 4 value panels, double-
+//   buffered (2 x 32 KiB, also the B operand of P.V); X = a ring of 12 slots of 8 KiB through
+//   which the 5 other cache panels of every tile stream (a slot is refilled as soon as its MMAs
+//   have read it, so loads run 2.4 tiles ahead).  The TMEM-bound Q panels are staged through the
+//   second Y buffer and the X ring at start.
+// Warps: 0-3 softmax (one head row per thread), 4 issues S, 5 issues P.V, 6 loads.
 #pragma once
 
 #include <cuda.h>
@@ -62,22 +63,24 @@ struct MlaParams {
 struct MlaSmem {
     static constexpr int kQPanel = kMlaHeads * 128;  // 16 KiB
     static constexpr int kKvPanel = kMlaBN * 128;    // 8 KiB
-    static constexpr int kQ = 0;                     // 6 Q panels: value panels 4r+y, then X 3, 4
-    static constexpr int kXSlots = 8;
-    static constexpr int kX = kQ + 6 * kQPanel;      // X ring
-    static constexpr int kY = kX + kXSlots * kKvPanel;  // 2 buffers of 4 panels
-    static constexpr int kStage = kX;                // start-up staging of the 3 TMEM Q panels
-    static constexpr int kBars = kY + 8 * kKvPanel;
+    static constexpr int kQ = 0;                     // 4 Q panels: the value panels 4r+y
+    static constexpr int kXSlots = 12;
+    static constexpr int kYBufs = 2;
+    static constexpr int kY = kQ + 4 * kQPanel;                 // kYBufs buffers of 4 panels
+    static constexpr int kX = kY + kYBufs * 4 * kKvPanel;       // X ring
+    // start-up staging of the 5 TMEM Q panels: the last Y buffer (first used by tile 1) and the
+    // X ring, which lie next to each other
+    static constexpr int kStage = kY + (kYBufs - 1) * 4 * kKvPanel;
+    static constexpr int kBars = kX + kXSlots * kKvPanel;
     // barriers
     static constexpr int kBarQ = 0;         // Q panels landed (tx)
     static constexpr int kBarQt = 1;        // TMEM Q panels written, staging free (count 128)
     static constexpr int kBarXFull = 2;     // [kXSlots]
     static constexpr int kBarXEmpty = kBarXFull + kXSlots;
-    static constexpr int kBarYFull = kBarXEmpty + kXSlots;  // [2]
-    static constexpr int kBarYEmpty = kBarYFull + 2;        // [2]
-    static constexpr int kBarSaFull = kBarYEmpty + 2;
-    static constexpr int kBarSbFull = kBarSaFull + 1;
-    static constexpr int kBarSFree = kBarSbFull + 1;   // the softmax has read S_a, S_b (count 128)
+    static constexpr int kBarYFull = kBarXEmpty + kXSlots;  // [kYBufs]
+    static constexpr int kBarYEmpty = kBarYFull + kYBufs;   // [kYBufs]
+    static constexpr int kBarSFull = kBarYEmpty + kYBufs;
+    static constexpr int kBarSFree = kBarSFull + 1;    // the softmax has read S (count 128)
     static constexpr int kBarPFull = kBarSFree + 1;    // P in TMEM (count 128)
     static constexpr int kBarPvDone = kBarPFull + 1;   // P.V complete
     static constexpr int kNumBars = kBarPvDone + 1;
@@ -85,12 +88,12 @@ struct MlaSmem {
     static constexpr int kAbort = kTmemSlot + 8;
     static constexpr int kBytes = kAbort + 8;
     static constexpr int kAlloc = kBytes + 1024;
-    static_assert(kStage + 3 * kQPanel <= kY, "staging must fit in the X ring");
+    static_assert(kStage + 5 * kQPanel <= kBars, "staging must fit in the last Y buffer + X ring");
     static_assert(kAlloc <= 232448, "MLA shared memory exceeds the per-block limit");
 };
 
 // TMEM columns
-constexpr uint32_t kMlaTSa = 0, kMlaTSb = 64, kMlaTP = 128, kMlaTQ = 160, kMlaTO = 256;
+constexpr uint32_t kMlaTS = 0, kMlaTP = 64, kMlaTQ = 96, kMlaTO = 256;
 
 // Panel (64 columns) of the cache feeding X slot x (x = 0..4) for value half r: the four c_kv
 // panels outside the value half, then the k_pe panel.
@@ -124,21 +127,21 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     const int t_begin = static_cast<int>(static_cast<long long>(p.n_tiles) * split / p.n_splits);
     const int t_end = static_cast<int>(static_cast<long long>(p.n_tiles) * (split + 1) / p.n_splits);
     const int n_t = t_end - t_begin;  // >= 1 (n_splits <= n_tiles)
-    auto ybuf = [](int i) { return i & 1; };
+    auto ybuf = [](int i) { return i % MlaSmem::kYBufs; };
+    auto yphase = [](int i) { return static_cast<uint32_t>((i / MlaSmem::kYBufs) & 1); };
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(L::kBarQ), 1);
+        mbar_init(bar(L::kBarQ), kMlaPanels);  // one arrive (+ tx) per Q panel
         mbar_init(bar(L::kBarQt), 128);
         for (int x = 0; x < L::kXSlots; ++x) {
             mbar_init(bar(L::kBarXFull + x), 1);
             mbar_init(bar(L::kBarXEmpty + x), 1);
         }
-        for (int y = 0; y < 2; ++y) {
-            mbar_init(bar(L::kBarYFull + y), 1);
+        for (int y = 0; y < L::kYBufs; ++y) {
+            mbar_init(bar(L::kBarYFull + y), 4);  // one arrive (+ tx) per value panel
             mbar_init(bar(L::kBarYEmpty + y), 1);
         }
-        mbar_init(bar(L::kBarSaFull), 1);
-        mbar_init(bar(L::kBarSbFull), 1);
+        mbar_init(bar(L::kBarSFull), 1);
         mbar_init(bar(L::kBarSFree), 128);
         mbar_init(bar(L::kBarPFull), 128);
         mbar_init(bar(L::kBarPvDone), 1);
@@ -154,27 +157,34 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t t_sa = tmem + kMlaTSa, t_sb = tmem + kMlaTSb, t_p = tmem + kMlaTP;
+    auto t_s = [=](int) { return tmem + kMlaTS; };
+    const uint32_t t_p = tmem + kMlaTP;
     const uint32_t t_q = tmem + kMlaTQ, t_o = tmem + kMlaTO;
 
     if (warp == kMlaLoad) {
-        // ---------------- producer: lane 0 streams Q and the X ring, lane 1 the Y buffers, so a
-        // wait for a Y buffer never holds back X panels (and the other way round) --------------
-        if (lane == 0) {
-            tma_prefetch_desc(&tmap_q);
-            tma_prefetch_desc(&tmap_kv);
-            mbar_arrive_expect_tx(bar(L::kBarQ), kMlaPanels * L::kQPanel);
-            for (int y = 0; y < 4; ++y)  // smem Q slots 0-3: the value panels
-                tma_load_3d(sbase + L::kQ + y * L::kQPanel, &tmap_q, bar(L::kBarQ),
-                            (4 * r + y) * 64, ht * kMlaHeads, b);
-            for (int x = 0; x < 5; ++x)  // X 0-2 -> staging (for TMEM), X 3-4 -> smem slots 4-5
-                tma_load_3d(x < 3 ? sbase + L::kStage + x * L::kQPanel
-                                  : sbase + L::kQ + (x + 1) * L::kQPanel,
-                            &tmap_q, bar(L::kBarQ), mla_x_panel(r, x) * 64, ht * kMlaHeads, b);
-            bool ok = mbar_wait_bounded<true>(bar(L::kBarQt), 0, abort_flag, status_word);
-            for (int i = 0; ok && i < n_t; ++i) {
-                const int tok = (t_begin + i) * kMlaBN;
-                for (int x = 0; ok && x < 5; ++x) {  // panel k of the stream -> slot k % kXSlots
+        // ---------------- producer: one lane per panel.  One thread's bulk tensor copies are
+        // processed one after another (~29 bytes per cycle per SM from one issuing thread), so
+        // lanes 0-4 stream the five X panels of every tile and lanes 5-8 its four value panels;
+        // lanes 0-8 first load one Q panel each ------------------------------------------------
+        if (lane < kMlaPanels) {
+            if (lane == 0) {
+                tma_prefetch_desc(&tmap_q);
+                tma_prefetch_desc(&tmap_kv);
+            }
+            __syncwarp(0x1ffu);
+            // lanes 0-3: the value-side Q panels -> smem slots 0-3; lanes 4-8: the X-side Q
+            // panels -> staging, for TMEM
+            mbar_arrive_expect_tx(bar(L::kBarQ), L::kQPanel);
+            if (lane < 4)
+                tma_load_3d(sbase + L::kQ + lane * L::kQPanel, &tmap_q, bar(L::kBarQ),
+                            (4 * r + lane) * 64, ht * kMlaHeads, b);
+            else
+                tma_load_3d(sbase + L::kStage + (lane - 4) * L::kQPanel, &tmap_q, bar(L::kBarQ),
+                            mla_x_panel(r, lane - 4) * 64, ht * kMlaHeads, b);
+            if (lane < 5) {  // X panel `lane` of every tile, once the start-up staging is done
+                const int x = lane;
+                bool ok = mbar_wait_bounded<true>(bar(L::kBarQt), 0, abort_flag, status_word);
+                for (int i = 0; ok && i < n_t; ++i) {
                     const int k = 5 * i + x, slot = k % L::kXSlots;
                     ok = mbar_wait_bounded<true>(bar(L::kBarXEmpty + slot),
                                                  ((k / L::kXSlots) & 1) ^ 1u, abort_flag,
@@ -182,39 +192,47 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
                     if (!ok) break;
                     mbar_arrive_expect_tx(bar(L::kBarXFull + slot), L::kKvPanel);
                     tma_load_3d(sbase + L::kX + slot * L::kKvPanel, &tmap_kv,
-                                bar(L::kBarXFull + slot), mla_x_panel(r, x) * 64, tok, b);
-                }
-            }
-        } else if (lane == 1) {
-            for (int i = 0; i < n_t; ++i) {
-                const int yb = ybuf(i);
-                if (!mbar_wait_bounded<true>(bar(L::kBarYEmpty + yb), ((i >> 1) & 1) ^ 1u,
-                                             abort_flag, status_word))
-                    break;
-                mbar_arrive_expect_tx(bar(L::kBarYFull + yb), 4 * L::kKvPanel);
-                for (int y = 0; y < 4; ++y)
-                    tma_load_3d(sbase + L::kY + (4 * yb + y) * L::kKvPanel, &tmap_kv,
-                                bar(L::kBarYFull + yb), (4 * r + y) * 64,
+                                bar(L::kBarXFull + slot), mla_x_panel(r, x) * 64,
                                 (t_begin + i) * kMlaBN, b);
+                }
+            } else {  // value panel lane-5 of every tile, into Y buffer i % kYBufs
+                const int y = lane - 5;
+                for (int i = 0; i < n_t; ++i) {
+                    const int yb = ybuf(i);
+                    // the last buffer holds start-up staging until the Q panels are in TMEM
+                    if (i == L::kYBufs - 1 &&
+                        !mbar_wait_bounded<true>(bar(L::kBarQt), 0, abort_flag, status_word))
+                        break;
+                    if (!mbar_wait_bounded<true>(bar(L::kBarYEmpty + yb), yphase(i) ^ 1u,
+                                                 abort_flag, status_word))
+                        break;
+                    mbar_arrive_expect_tx(bar(L::kBarYFull + yb), L::kKvPanel);
+                    tma_load_3d(sbase + L::kY + (4 * yb + y) * L::kKvPanel, &tmap_kv,
+                                bar(L::kBarYFull + yb), (4 * r + y) * 64, (t_begin + i) * kMlaBN,
+                                b);
+                }
             }
         }
         __syncwarp();
-    } else if (warp == kMlaMmaA || warp == kMlaMmaB) {
-        // ---------------- MMA issuers (warp-uniform, elected lane) -----------------------------
-        // A: S_a(i) over the X slots (Q from TMEM for slots 0-2, from smem for 3-4).
-        // B: S_b(i) over the value panels, then P.V(i-1)... in the order S_b(i+1), P.V(i), so the
-        //    next scores never wait for this tile's softmax.
-        const bool is_a = warp == kMlaMmaA;
+    } else if (warp == kMlaMmaA) {
+        // ---------------- S(i) = Q . cache tile i into S[i&1], 36 MMAs (warp-uniform issue) ----
         bool ok = mbar_wait_warp(bar(L::kBarQ), 0, abort_flag, status_word);
         if (ok) ok = mbar_wait_warp(bar(L::kBarQt), 0, abort_flag, status_word);
         tc_fence_after();
-        auto s_a = [&](int i) {  // all five panels landed, then 20 MMAs back to back
-            for (int x = 0; x < 5; ++x) {
+        for (int i = 0; ok && i < n_t; ++i) {
+            if (i >= 1) {  // the softmax has loaded S(i-1)
+                ok = mbar_wait_warp(bar(L::kBarSFree), (i - 1) & 1, abort_flag, status_word);
+                if (!ok) break;
+            }
+            for (int x = 0; ok && x < 5; ++x) {  // the tile's five X panels have landed
                 const int k = 5 * i + x;
                 ok = mbar_wait_warp(bar(L::kBarXFull + k % L::kXSlots), (k / L::kXSlots) & 1,
                                     abort_flag, status_word);
-                if (!ok) return;
             }
+            const int yb = ybuf(i);
+            if (ok) ok = mbar_wait_warp(bar(L::kBarYFull + yb), yphase(i), abort_flag,
+                                        status_word);
+            if (!ok) break;
             tc_fence_after();
 #pragma unroll
             for (int x = 0; x < 5; ++x) {
@@ -223,64 +241,39 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
                 for (int kk = 0; kk < 4; ++kk) {
                     const uint64_t bdesc = smem_desc_sw128(kv + kk * 32, 16, 1024);
                     const uint32_t acc = (x == 0 && kk == 0) ? 0u : 1u;
-                    if (x < 3)
-                        mma_bf16_ts_warp(t_sa, t_q + x * 32 + kk * 8, bdesc, kIdescS, acc);
-                    else
-                        mma_bf16_ss_warp(t_sa,
-                                         smem_desc_sw128(sbase + L::kQ + (x + 1) * L::kQPanel + kk * 32,
-                                                         16, 1024),
-                                         bdesc, kIdescS, acc);
+                    mma_bf16_ts_warp(t_s(i), t_q + x * 32 + kk * 8, bdesc, kIdescS, acc);
                 }
             }
             for (int x = 0; x < 5; ++x) mma_commit_warp(bar(L::kBarXEmpty + (5 * i + x) % L::kXSlots));
-            mma_commit_warp(bar(L::kBarSaFull));
-        };
-        auto s_b = [&](int i) {
-            const int yb = ybuf(i);
-            ok = mbar_wait_warp(bar(L::kBarYFull + yb), (i >> 1) & 1, abort_flag, status_word);
-            if (!ok) return;
-            tc_fence_after();
+#pragma unroll
             for (int y = 0; y < 4; ++y) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16_ss_warp(t_sb,
+                    mma_bf16_ss_warp(t_s(i),
                                      smem_desc_sw128(sbase + L::kQ + y * L::kQPanel + kk * 32, 16, 1024),
                                      smem_desc_sw128(sbase + L::kY + (4 * yb + y) * L::kKvPanel + kk * 32,
                                                      16, 1024),
-                                     kIdescS, (y == 0 && kk == 0) ? 0u : 1u);
+                                     kIdescS, 1u);
             }
-            mma_commit_warp(bar(L::kBarSbFull));
-        };
-        auto wait_s_free = [&](int i) {  // the softmax has read S_a(i) and S_b(i)
-            ok = mbar_wait_warp(bar(L::kBarSFree), i & 1, abort_flag, status_word);
-            if (ok) tc_fence_after();
-        };
-        if (is_a) {
-            for (int i = 0; ok && i < n_t; ++i) {
-                if (i > 0) wait_s_free(i - 1);
-                if (ok) s_a(i);
-            }
-        } else {
-            if (ok) s_b(0);
-            for (int i = 0; ok && i < n_t; ++i) {
-                if (i + 1 < n_t) {
-                    wait_s_free(i);
-                    if (ok) s_b(i + 1);
-                    if (!ok) break;
-                }
-                ok = mbar_wait_warp(bar(L::kBarPFull), i & 1, abort_flag, status_word);
-                if (!ok) break;
-                tc_fence_after();
-                const int yb = ybuf(i);
+            mma_commit_warp(bar(L::kBarSFull));
+        }
+        __syncwarp();
+    } else if (warp == kMlaMmaB) {
+        // ---------------- O += P(i) Y_i (four N=256 MMAs), once the softmax has written P(i) ---
+        bool ok = true;
+        for (int i = 0; ok && i < n_t; ++i) {
+            ok = mbar_wait_warp(bar(L::kBarPFull), i & 1, abort_flag, status_word);
+            if (!ok) break;
+            tc_fence_after();
+            const int yb = ybuf(i);
 #pragma unroll
-                for (int kk = 0; kk < kMlaBN / 16; ++kk)  // O += P Y  (K = 64 tokens, N = 256)
-                    mma_bf16_ts_warp(t_o, t_p + kk * 8,
-                                     smem_desc_sw128(sbase + L::kY + 4 * yb * L::kKvPanel + kk * 2048,
-                                                     L::kKvPanel, 1024),
-                                     kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
-                mma_commit_warp(bar(L::kBarPvDone));
-                mma_commit_warp(bar(L::kBarYEmpty + yb));
-            }
+            for (int kk = 0; kk < kMlaBN / 16; ++kk)  // O += P Y  (K = 64 tokens, N = 256)
+                mma_bf16_ts_warp(t_o, t_p + kk * 8,
+                                 smem_desc_sw128(sbase + L::kY + 4 * yb * L::kKvPanel + kk * 2048,
+                                                 L::kKvPanel, 1024),
+                                 kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
+            mma_commit_warp(bar(L::kBarPvDone));
+            mma_commit_warp(bar(L::kBarYEmpty + yb));  // S(i) also read Y_i; it completed first
         }
         __syncwarp();
     } else {
@@ -290,10 +283,10 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
         const float c = p.scale_log2;
         bool ok = mbar_wait_warp(bar(L::kBarQ), 0, abort_flag, status_word);
-        // start-up: the three staged Q panels -> TMEM (bf16 pairs, the MMA's A layout)
+        // start-up: the five staged Q panels -> TMEM (bf16 pairs, the MMA's A layout)
         if (ok) {
 #pragma unroll 1
-            for (int j = 0; j < 3; ++j) {
+            for (int j = 0; j < 5; ++j) {
                 const uint32_t src = sbase + L::kStage + j * L::kQPanel + row * 128;
                 uint32_t v[32];
 #pragma unroll
@@ -308,23 +301,19 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         mbar_arrive(bar(L::kBarQt));
         float m = -INFINITY, l = 0.f;
         for (int i = 0; ok && i < n_t; ++i) {
-            ok = mbar_wait_warp(bar(L::kBarSaFull), i & 1, abort_flag, status_word);
-            if (ok) ok = mbar_wait_warp(bar(L::kBarSbFull), i & 1, abort_flag, status_word);
+            ok = mbar_wait_warp(bar(L::kBarSFull), i & 1, abort_flag, status_word);
             if (!ok) break;
             tc_fence_after();
             float s[kMlaBN];
             {
-                uint32_t ra[kMlaBN], rb[kMlaBN];
-                tmem_ld32(lane_base + t_sa, *reinterpret_cast<uint32_t(*)[32]>(&ra[0]));
-                tmem_ld32(lane_base + t_sa + 32, *reinterpret_cast<uint32_t(*)[32]>(&ra[32]));
-                tmem_ld32(lane_base + t_sb, *reinterpret_cast<uint32_t(*)[32]>(&rb[0]));
-                tmem_ld32(lane_base + t_sb + 32, *reinterpret_cast<uint32_t(*)[32]>(&rb[32]));
+                uint32_t ra[kMlaBN];
+                tmem_ld32(lane_base + t_s(i), *reinterpret_cast<uint32_t(*)[32]>(&ra[0]));
+                tmem_ld32(lane_base + t_s(i) + 32, *reinterpret_cast<uint32_t(*)[32]>(&ra[32]));
                 tmem_wait_ld();
                 tc_fence_before();
-                mbar_arrive(bar(L::kBarSFree));
+                mbar_arrive(bar(L::kBarSFree));  // S(i+1) may now be formed over it
 #pragma unroll
-                for (int j = 0; j < kMlaBN; ++j)
-                    s[j] = (__uint_as_float(ra[j]) + __uint_as_float(rb[j])) * c;
+                for (int j = 0; j < kMlaBN; ++j) s[j] = __uint_as_float(ra[j]) * c;
             }
             const int valid = p.T - (t_begin + i) * kMlaBN;  // tokens of this tile inside T
             if (valid < kMlaBN) {
