@@ -12,8 +12,8 @@
 //   panel by panel, each slot refilled as soon as its MMAs have read it), P (bf16, two 128B-
 //   swizzled 128 x 64 panels, the K-major A operand of P.V), V (4 panels, 64 KiB, the MN-major
 //   B operand of one N=256 MMA per 16 keys).
-// Warps: 0-3 softmax (one row per thread), 4 issues S, 5 issues P.V, 6 loads (lane 0: Q and the
-// K ring; lane 1: V).
+// Warps: 0-3 softmax (one row per thread), 4 issues S, 5 issues P.V, 6 loads (lane p < 4: Q
+// panel p and K panel p of every key tile, in K slot p; lane 4+p: V panel p).
 #pragma once
 
 #include <cuda.h>
@@ -85,12 +85,12 @@ __global__ void __launch_bounds__(kW256Threads, 1)
     const int n_kv = p.causal ? m_tile + 1 : p.n_tiles;  // key tiles 0 .. n_kv-1
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(L::kBarQ), 1);
+        mbar_init(bar(L::kBarQ), 4);  // one arrive (+ tx) per Q panel
         for (int s = 0; s < L::kKSlots; ++s) {
             mbar_init(bar(L::kBarKFull + s), 1);
             mbar_init(bar(L::kBarKEmpty + s), 1);
         }
-        mbar_init(bar(L::kBarVFull), 1);
+        mbar_init(bar(L::kBarVFull), 4);  // one arrive (+ tx) per V panel
         mbar_init(bar(L::kBarVEmpty), 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(L::kBarSFull + i), 1);
@@ -114,32 +114,36 @@ __global__ void __launch_bounds__(kW256Threads, 1)
     const uint32_t t_o = tmem + 256;
 
     if (warp == kW256Load) {
-        if (lane == 0) {  // Q once, then the K panels of every key tile through the ring
-            tma_prefetch_desc(&tmap_q);
-            tma_prefetch_desc(&tmap_k);
-            mbar_arrive_expect_tx(bar(L::kBarQ), 4 * L::kPanel);
-            for (int pn = 0; pn < 4; ++pn)
-                tma_load_4d(sbase + L::kQ + pn * L::kPanel, &tmap_q, bar(L::kBarQ), pn * 64,
-                            m_tile * 128, hq, b);
-            for (int k = 0; k < 4 * n_kv; ++k) {
-                const int slot = k % L::kKSlots;
-                if (!mbar_wait_bounded<true>(bar(L::kBarKEmpty + slot),
-                                             ((k / L::kKSlots) & 1) ^ 1u, abort_flag, status_word))
-                    break;
-                mbar_arrive_expect_tx(bar(L::kBarKFull + slot), L::kPanel);
-                tma_load_4d(sbase + L::kK + slot * L::kPanel, &tmap_k, bar(L::kBarKFull + slot),
-                            (k & 3) * 64, (k >> 2) * 128, hkv, b);
+        // One thread's bulk tensor copies are processed one after another (~29 bytes per cycle
+        // per SM from one issuing thread), so every 16 KiB panel stream has its own lane.
+        static_assert(L::kKSlots == 4, "K panel p of every key tile goes to slot p");
+        if (lane < 4) {  // Q panel `lane` once, then K panel `lane` of every key tile
+            const int pn = lane;
+            if (pn == 0) {
+                tma_prefetch_desc(&tmap_q);
+                tma_prefetch_desc(&tmap_k);
             }
-        } else if (lane == 1) {  // V tiles, each once the previous P.V has read its buffer
-            tma_prefetch_desc(&tmap_v);
+            mbar_arrive_expect_tx(bar(L::kBarQ), L::kPanel);
+            tma_load_4d(sbase + L::kQ + pn * L::kPanel, &tmap_q, bar(L::kBarQ), pn * 64,
+                        m_tile * 128, hq, b);
+            for (int j = 0; j < n_kv; ++j) {
+                if (!mbar_wait_bounded<true>(bar(L::kBarKEmpty + pn), (j & 1) ^ 1u, abort_flag,
+                                             status_word))
+                    break;
+                mbar_arrive_expect_tx(bar(L::kBarKFull + pn), L::kPanel);
+                tma_load_4d(sbase + L::kK + pn * L::kPanel, &tmap_k, bar(L::kBarKFull + pn),
+                            pn * 64, j * 128, hkv, b);
+            }
+        } else if (lane < 8) {  // V panel lane-4 of every key tile, once P.V(j-1) has read V
+            const int pn = lane - 4;
+            if (pn == 0) tma_prefetch_desc(&tmap_v);
             for (int j = 0; j < n_kv; ++j) {
                 if (!mbar_wait_bounded<true>(bar(L::kBarVEmpty), (j & 1) ^ 1u, abort_flag,
                                              status_word))
                     break;
-                mbar_arrive_expect_tx(bar(L::kBarVFull), 4 * L::kPanel);
-                for (int pn = 0; pn < 4; ++pn)
-                    tma_load_4d(sbase + L::kV + pn * L::kPanel, &tmap_v, bar(L::kBarVFull),
-                                pn * 64, j * 128, hkv, b);
+                mbar_arrive_expect_tx(bar(L::kBarVFull), L::kPanel);
+                tma_load_4d(sbase + L::kV + pn * L::kPanel, &tmap_v, bar(L::kBarVFull), pn * 64,
+                            j * 128, hkv, b);
             }
         }
         __syncwarp();
