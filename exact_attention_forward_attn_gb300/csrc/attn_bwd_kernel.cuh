@@ -210,12 +210,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int n_it = per_head * p.group;          // iterations: (head in group, query tile)
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(L::kBarRes), 1);
+        mbar_init(bar(L::kBarRes), 2 * kPanels);  // one arrive (+ tx) per K_j / V_j panel
         for (int s = 0; s < L::kQSlots; ++s) {
-            mbar_init(bar(L::kBarQFull + s), 1);
+            mbar_init(bar(L::kBarQFull + s), kPanels);  // one arrive (+ tx) per panel
             mbar_init(bar(L::kBarQEmpty + s), 1);
         }
-        mbar_init(bar(L::kBarDoFull), 1);
+        mbar_init(bar(L::kBarDoFull), kPanels);
         mbar_init(bar(L::kBarDoEmpty), 2);
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar(L::kBarVecFull + s), 32);
@@ -245,16 +245,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     auto it_tile = [=](int it) { return i_first + it % per_head; };
 
     if (warp == kBwdLoadWarp) {
-        // ---------------- producer: lane 0 issues the TMA, every lane stages 4+4 vector entries,
-        // fetched into registers one iteration ahead ----------------------------------------------
-        if (lane == 0) {
-            mbar_arrive_expect_tx(bar(L::kBarRes), 2 * L::kTileBytes);
-            for (int h = 0; h < kPanels; ++h) {
+        // ---------------- producer: lanes 0..kPanels-1 issue the Q panels and lanes kPanels..
+        // 2*kPanels-1 the dO panels (one thread's bulk copies run one after another), every lane
+        // stages 4+4 vector entries, fetched into registers one iteration ahead ------------------
+        if (lane < 2 * kPanels) {  // K_j / V_j panel lane % kPanels
+            const int h = lane % kPanels;
+            mbar_arrive_expect_tx(bar(L::kBarRes), L::kPanelBytes);
+            if (lane < kPanels)
                 tma_load_4d(sbase + L::kRes0 + h * L::kPanelBytes, &tmap_k, bar(L::kBarRes),
                             h * 64, j * 128, hkv, b);
+            else
                 tma_load_4d(sbase + L::kRes1 + h * L::kPanelBytes, &tmap_v, bar(L::kBarRes),
                             h * 64, j * 128, hkv, b);
-            }
         }
         // -lse2 = -LSE*log2(e) and -Delta of queries lane*4 .. lane*4+3 of the iteration's tile
         // (0 past N: see top), fetched into registers one step ahead; stored negated so the
@@ -274,11 +276,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const int s = it % L::kQSlots;
             ok = mbar_wait_warp<true>(bar(L::kBarQEmpty + s), ((it / L::kQSlots) & 1) ^ 1u,
                                       abort_flag, status_word);
-            if (ok && lane == 0) {
-                mbar_arrive_expect_tx(bar(L::kBarQFull + s), L::kTileBytes);
-                for (int h = 0; h < kPanels; ++h)
-                    tma_load_4d(sbase + L::kQ + s * L::kTileBytes + h * L::kPanelBytes, &tmap_q,
-                                bar(L::kBarQFull + s), h * 64, it_tile(it) * 128, it_head(it), b);
+            if (ok && lane < kPanels) {
+                const int h = lane;
+                mbar_arrive_expect_tx(bar(L::kBarQFull + s), L::kPanelBytes);
+                tma_load_4d(sbase + L::kQ + s * L::kTileBytes + h * L::kPanelBytes, &tmap_q,
+                            bar(L::kBarQFull + s), h * 64, it_tile(it) * 128, it_head(it), b);
             }
         };
         auto load_vec = [&](int it) {  // vectors of step it, once step it-2 is done with the slot
@@ -294,11 +296,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         };
         auto load_do = [&](int it) {  // dO_it, once dP^T(it-1) and dV(it-1) have read the buffer
             ok = mbar_wait_warp<true>(bar(L::kBarDoEmpty), (it & 1) ^ 1u, abort_flag, status_word);
-            if (ok && lane == 0) {
-                mbar_arrive_expect_tx(bar(L::kBarDoFull), L::kTileBytes);
-                for (int h = 0; h < kPanels; ++h)
-                    tma_load_4d(sbase + L::kDO + h * L::kPanelBytes, &tmap_do, bar(L::kBarDoFull),
-                                h * 64, it_tile(it) * 128, it_head(it), b);
+            if (ok && lane >= kPanels && lane < 2 * kPanels) {
+                const int h = lane - kPanels;
+                mbar_arrive_expect_tx(bar(L::kBarDoFull), L::kPanelBytes);
+                tma_load_4d(sbase + L::kDO + h * L::kPanelBytes, &tmap_do, bar(L::kBarDoFull),
+                            h * 64, it_tile(it) * 128, it_head(it), b);
             }
         };
         if (n_it > 0) {
@@ -577,13 +579,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int n_it = p.causal ? i + 1 : p.n_tiles;  // key tiles 0 .. n_it-1
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(L::kBarRes), 1);
+        mbar_init(bar(L::kBarRes), 2 * kPanels);  // one arrive (+ tx) per Q_i / dO_i panel
         for (int s = 0; s < L::kKSlots; ++s) {
-            mbar_init(bar(L::kBarKFull + s), 1);
+            mbar_init(bar(L::kBarKFull + s), kPanels);
             mbar_init(bar(L::kBarKEmpty + s), 1);
         }
         for (int s = 0; s < L::kVSlots; ++s) {
-            mbar_init(bar(L::kBarVFull + s), 1);
+            mbar_init(bar(L::kBarVFull + s), kPanels);
             mbar_init(bar(L::kBarVEmpty + s), 1);
         }
         mbar_init(bar(L::kBarS), 1);
@@ -608,35 +610,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t t_s0 = tmem, t_dp = tmem + 128, t_dq = tmem + 256, t_s1 = tmem + 384;
 
     if (warp == kBwdLoadWarp) {
-        // lane 0: Q_i, dO_i, then the K ring; lane 1: the V ring (independent streams)
-        if (lane == 0) {
-            mbar_arrive_expect_tx(bar(L::kBarRes), 2 * L::kTileBytes);
-            for (int h = 0; h < kPanels; ++h) {
+        // one lane per panel stream (one thread's bulk copies run one after another): lanes
+        // 0..kPanels-1 load a Q_i panel, then that panel of every K_j; lanes kPanels..2*kPanels-1
+        // a dO_i panel, then that panel of every V_j
+        if (lane < 2 * kPanels) {
+            const bool kside = lane < kPanels;
+            const int h = lane % kPanels;
+            mbar_arrive_expect_tx(bar(L::kBarRes), L::kPanelBytes);
+            if (kside)
                 tma_load_4d(sbase + L::kRes0 + h * L::kPanelBytes, &tmap_q, bar(L::kBarRes),
                             h * 64, i * 128, hq, b);
+            else
                 tma_load_4d(sbase + L::kRes1 + h * L::kPanelBytes, &tmap_do, bar(L::kBarRes),
                             h * 64, i * 128, hq, b);
-            }
+            const int slots = kside ? L::kKSlots : L::kVSlots;
+            const int full0 = kside ? L::kBarKFull : L::kBarVFull;
+            const int empty0 = kside ? L::kBarKEmpty : L::kBarVEmpty;
+            const uint32_t ring = sbase + (kside ? L::kK : L::kV);
+            const CUtensorMap* map = kside ? &tmap_k : &tmap_v;
             for (int it = 0; it < n_it; ++it) {
-                const int s = it % L::kKSlots;
-                if (!mbar_wait_bounded<true>(bar(L::kBarKEmpty + s), ((it / L::kKSlots) & 1) ^ 1u,
-                                             abort_flag, status_word))
+                const int s = it % slots;
+                if (!mbar_wait_bounded<true>(bar(empty0 + s), ((it / slots) & 1) ^ 1u, abort_flag,
+                                             status_word))
                     break;
-                mbar_arrive_expect_tx(bar(L::kBarKFull + s), L::kTileBytes);
-                for (int h = 0; h < kPanels; ++h)
-                    tma_load_4d(sbase + L::kK + s * L::kTileBytes + h * L::kPanelBytes, &tmap_k,
-                                bar(L::kBarKFull + s), h * 64, it * 128, hkv, b);
-            }
-        } else if (lane == 1) {
-            for (int it = 0; it < n_it; ++it) {
-                const int s = it % L::kVSlots;
-                if (!mbar_wait_bounded<true>(bar(L::kBarVEmpty + s), ((it / L::kVSlots) & 1) ^ 1u,
-                                             abort_flag, status_word))
-                    break;
-                mbar_arrive_expect_tx(bar(L::kBarVFull + s), L::kTileBytes);
-                for (int h = 0; h < kPanels; ++h)
-                    tma_load_4d(sbase + L::kV + s * L::kTileBytes + h * L::kPanelBytes, &tmap_v,
-                                bar(L::kBarVFull + s), h * 64, it * 128, hkv, b);
+                mbar_arrive_expect_tx(bar(full0 + s), L::kPanelBytes);
+                tma_load_4d(ring + s * L::kTileBytes + h * L::kPanelBytes, map, bar(full0 + s),
+                            h * 64, it * 128, hkv, b);
             }
         }
         __syncwarp();
