@@ -4,7 +4,10 @@
 One step = one ``attn_fwd`` call (the whole hot path: TMA loads, QK^T and P.V on the tensor cores,
 online softmax, O/LSE stores) over the long-context workload B=1, Hq=32, Hkv=8, N=32768, D=128,
 causal, bf16 (FLOPs = 4*B*Hq*N^2*D / 2).  Inputs (402 MB) and the output (268 MB) exceed the
-129 MB L2, so steps run back to back without an explicit flush.
+129 MB L2, so steps run back to back without an explicit flush.  The context legs (the five
+configurations at N = 128..4096, the other long lengths, wide heads, split-KV, the backward and
+the MLA decode) follow in the same line; those whose inputs fit in L2 are timed after a 256 MB
+flush before each launch.
 
 Prints one JSON line.  ``--impl reference`` times the fp64 CPU oracle instead (bounded sample per
 step, on the host cores).  Under torchrun (``--gpus N``) each rank runs an independent replica on
@@ -243,6 +246,27 @@ def timed_launches(fn, stream, n):
             ev[i + 1].record(stream)
     stream.synchronize()
     return [ev[i].elapsed_time(ev[i + 1]) for i in range(n)]
+
+
+def cold_launch_ms(fn, stream, flush, n, warm=3):
+    """Median CUDA-event duration (ms) of fn() over n launches, each after `flush` was rewritten
+    (a buffer larger than L2), so inputs smaller than L2 are read from DRAM every time.
+
+    Everything is enqueued before the one synchronize: the flush keeps the device busy longer
+    than the host takes to enqueue fn(), so each timed interval holds the device work alone and
+    not the host's launch cost."""
+    import torch
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(warm + n)]
+    with torch.cuda.stream(stream):
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            fn()
+            b.record(stream)
+    stream.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in ev[warm:])
 
 
 def run_profile_leg(args):
@@ -504,6 +528,36 @@ def main():
         wide.append({"workload": ww.name, "ms": ms, "tflops": tf, "frac": tf / peak})
         del wq, wk, wv, wo, wlse
 
+    # ---- context: the five configurations (single pass, C-ABI, cold L2) ------------------------
+    # ms, TFLOPS against the tensor peak and algorithmic GB/s against the copy bandwidth: the short
+    # sequences are bound by latency and occupancy rather than by either roofline.
+    configs = []
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if not args.no_sweep else None
+    if not args.no_sweep and rank == 0:
+        hbm = float(peaks["hbm_gbs"])
+        lib = _lib.load()
+        sh = ctypes.c_void_p(stream.cuda_stream)
+        for wc in (wl.TINY_NONCAUSAL, wl.TINY_CAUSAL, wl.GQA4_CAUSAL, wl.GQA8_CAUSAL, wl.MHA,
+                   wl.MHA_OUTLIER, wl.MQA):
+            cq, ck, cv = (t.to(dev) for t in wl.make_qkv(wc))
+            co = torch.empty_like(cq)
+            cl = torch.empty(wc.B, wc.Hq, wc.N, dtype=torch.float32, device=dev)
+            cargs = (cq.data_ptr(), ck.data_ptr(), cv.data_ptr(), co.data_ptr(), cl.data_ptr(),
+                     wc.B, wc.Hq, wc.Hkv, wc.N, wc.D, int(wc.causal), ctypes.c_float(wc.sm_scale),
+                     sh)
+
+            def cstep():
+                assert lib.attn_fwd(*cargs) == 0
+
+            ms = cold_launch_ms(cstep, stream, flush, 20)
+            tf = wc.flops / (ms * 1e-3) / 1e12
+            gbs = wc.bytes / (ms * 1e-3) / 1e9
+            configs.append({"workload": wc.name, "B": wc.B, "Hq": wc.Hq, "Hkv": wc.Hkv, "N": wc.N,
+                            "D": wc.D, "causal": wc.causal, "us": ms * 1e3, "tflops": tf,
+                            "frac": tf / peak, "gbs": gbs, "hbm_frac": gbs / hbm,
+                            "l2": "256 MB flush before each launch"})
+            del cq, ck, cv, co, cl
+
     # ---- context: low-occupancy configurations, single pass vs split-KV (key-axis splits) -----
     low_occ = []
     if not args.no_sweep and rank == 0:
@@ -535,10 +589,7 @@ def main():
                      "library_choice": attn.splitkv_num_splits(ws_.B, ws_.Hq, ws_.N, ws_.D,
                                                                ws_.causal)}
             for name, fn in (("single", single), ("splitkv", split)):
-                with torch.cuda.stream(stream):
-                    for _ in range(5):
-                        fn()
-                ms = statistics.median(timed_launches(fn, stream, 50))
+                ms = cold_launch_ms(fn, stream, flush, 30)
                 entry[f"{name}_us"] = ms * 1e3
                 entry[f"{name}_tflops"] = ws_.flops / (ms * 1e-3) / 1e12
                 entry[f"{name}_gbs"] = ws_.bytes / (ms * 1e-3) / 1e9
@@ -587,7 +638,6 @@ def main():
     mla = []
     if not args.no_sweep and rank == 0:
         hbm = float(peaks["hbm_gbs"])
-        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
         lib = _lib.load()
         sh = ctypes.c_void_p(stream.cuda_stream)
         for wm in (wl.MLA_B1[4096], wl.MLA_B1[16384], wl.MLA_B32):
@@ -600,25 +650,16 @@ def main():
             args_ = (mq.data_ptr(), mkv.data_ptr(), mo.data_ptr(), ml.data_ptr(), wm.B, wm.H, wm.T,
                      attn.MLA_D_C, attn.MLA_D_R, ctypes.c_float(wm.sm_scale), n_sp,
                      mws.data_ptr(), need)
-            times = []
-            with torch.cuda.stream(stream):
-                for it in range(25):
-                    flush.zero_()
-                    a = torch.cuda.Event(enable_timing=True)
-                    b = torch.cuda.Event(enable_timing=True)
-                    a.record(stream)
-                    assert lib.attn_mla_decode(*args_, sh) == 0
-                    b.record(stream)
-                    b.synchronize()
-                    if it >= 5:
-                        times.append(a.elapsed_time(b))
-            ms = statistics.median(times)
+
+            def mstep():
+                assert lib.attn_mla_decode(*args_, sh) == 0
+
+            ms = cold_launch_ms(mstep, stream, flush, 20, warm=5)
             gbs = wm.bytes / (ms * 1e-3) / 1e9
             mla.append({"workload": wm.name, "us": ms * 1e3, "gbs": gbs, "hbm_frac": gbs / hbm,
                         "tflops": wm.flops / (ms * 1e-3) / 1e12, "splits": n_sp,
                         "kernels_per_step": 2 if n_sp > 1 else 1})
             del mq, mkv, mo, ml, mws
-        del flush
         if attn.device_status(dev) != 0:
             raise SystemExit("device status word reports an expired wait in the MLA leg")
 
@@ -646,7 +687,7 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": config_of(w, "inputs and output exceed the 129 MB L2; no flush"),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": args.steps, "clocks": clocks, "sweep": sweep,
+            "gpu_launches": args.steps, "clocks": clocks, "configs": configs, "sweep": sweep,
             "low_occupancy": low_occ, "wide_heads": wide, "backward": backward,
             "mla_decode": mla,
             "kernel_sha": kernel_hash(),
