@@ -11,6 +11,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -25,6 +26,9 @@ using namespace gb300attn;
 
 // Device status word: kernels OR failure flags into it (see attn_debug_status).
 __device__ unsigned int g_attn_status_word = 0;
+// Claim counters of the persistent forward kernel, handed to launches round robin (so up to
+// kSchedSlots launches may run at once on a device); each launch leaves its counter at zero.
+__device__ unsigned int g_fwd_sched[gb300attn::kSchedSlots] = {};
 
 namespace {
 
@@ -127,11 +131,20 @@ struct DeviceState {
     int cuda_error = 0;
     int num_sms = 0;
     unsigned int* status_word = nullptr;
+    unsigned int* sched = nullptr;  // g_fwd_sched
+    std::atomic<unsigned int> sched_next{0};
 };
 DeviceState g_devices[kMaxDevices];
 
+// Opt in to the large shared-memory carve-out, and check that the kernel was built with the
+// per-thread register count its setmaxnreg split assumes (a launch with fewer registers would
+// leave the softmax warpgroups waiting for registers that do not exist).
 template <int D, bool kSplit>
-cudaError_t opt_in_smem() {
+cudaError_t opt_in_smem(bool* regs_ok) {
+    cudaFuncAttributes a;
+    cudaError_t e = cudaFuncGetAttributes(&a, attn_fwd_kernel<D, kSplit>);
+    if (e != cudaSuccess) return e;
+    if (a.numRegs != kLaunchRegs) *regs_ok = false;
     return cudaFuncSetAttribute(attn_fwd_kernel<D, kSplit>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 SmemLayout<D>::kAlloc);
@@ -161,10 +174,13 @@ int device_state(int dev, DeviceState** out) {
         if (e != cudaSuccess) { st.status = ATTN_ERR_CUDA; st.cuda_error = e; return; }
         if (major != 10 || minor != 3) { st.status = ATTN_ERR_ARCH; return; }
         e = cudaGetSymbolAddress(reinterpret_cast<void**>(&st.status_word), g_attn_status_word);
-        if (e == cudaSuccess) e = opt_in_smem<64, false>();
-        if (e == cudaSuccess) e = opt_in_smem<128, false>();
-        if (e == cudaSuccess) e = opt_in_smem<64, true>();
-        if (e == cudaSuccess) e = opt_in_smem<128, true>();
+        if (e == cudaSuccess)
+            e = cudaGetSymbolAddress(reinterpret_cast<void**>(&st.sched), g_fwd_sched);
+        bool regs_ok = true;
+        if (e == cudaSuccess) e = opt_in_smem<64, false>(&regs_ok);
+        if (e == cudaSuccess) e = opt_in_smem<128, false>(&regs_ok);
+        if (e == cudaSuccess) e = opt_in_smem<64, true>(&regs_ok);
+        if (e == cudaSuccess) e = opt_in_smem<128, true>(&regs_ok);
         if (e == cudaSuccess) e = opt_in_bwd_smem<64>();
         if (e == cudaSuccess) e = opt_in_bwd_smem<128>();
         if (e == cudaSuccess)
@@ -174,7 +190,8 @@ int device_state(int dev, DeviceState** out) {
             e = cudaFuncSetAttribute(attn_fwd_d256_kernel,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      Fwd256Smem::kAlloc);
-        if (e != cudaSuccess) { st.status = ATTN_ERR_CUDA; st.cuda_error = e; }
+        if (e != cudaSuccess) { st.status = ATTN_ERR_CUDA; st.cuda_error = e; return; }
+        if (!regs_ok) st.status = ATTN_ERR_ARCH;
     });
     if (st.status == ATTN_ERR_CUDA) t_last_cuda_error = st.cuda_error;
     *out = &st;
@@ -325,15 +342,30 @@ int prepare(const Problem& P, DeviceState** ds, CUtensorMap* mq, CUtensorMap* mk
     prm->ws_o = nullptr;
     prm->ws_lse = nullptr;
     prm->stall_item = -1;
+    prm->items = static_cast<int>(P.items);
+    prm->out = static_cast<__nv_bfloat16*>(P.out);
+    prm->o_sb = P.so.b;
+    prm->o_sh = P.so.h;
+    prm->o_sn = P.so.n;
+    prm->d_out = P.D;
+    const unsigned int slot =
+        (*ds)->sched_next.fetch_add(1u, std::memory_order_relaxed) % kSchedSlots;
+    prm->sched = (*ds)->sched + slot;
     return ATTN_OK;
 }
 
+// The persistent two-tile kernel: one CTA per SM (or per item, if fewer), each claiming items
+// until all `items` are taken.
 template <int D, bool kSplit>
 int launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                const CUtensorMap& mo, const AttnParams& p, unsigned int* status_word,
-               int64_t grid, cudaStream_t stream) {
+               int64_t items, int num_sms, cudaStream_t stream) {
+    AttnParams prm = p;
+    prm.items = static_cast<int>(items);
+    const int64_t grid = std::min<int64_t>(items, std::max(1, num_sms));
     attn_fwd_kernel<D, kSplit><<<static_cast<unsigned int>(grid), kThreads,
-                                 SmemLayout<D>::kAlloc, stream>>>(mq, mk, mv, mo, p, status_word);
+                                 SmemLayout<D>::kAlloc, stream>>>(mq, mk, mv, mo, prm,
+                                                                  status_word);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
@@ -341,9 +373,11 @@ int launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
 // The single-pass forward for head dimension D: two Q tiles per CTA up to D = 128, one above.
 int launch_single(int D, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                   const CUtensorMap& mo, const AttnParams& p, unsigned int* status_word,
-                  int64_t grid, cudaStream_t stream) {
-    if (D <= 64) return launch_fwd<64, false>(mq, mk, mv, mo, p, status_word, grid, stream);
-    if (D <= 128) return launch_fwd<128, false>(mq, mk, mv, mo, p, status_word, grid, stream);
+                  int64_t grid, int num_sms, cudaStream_t stream) {
+    if (D <= 64)
+        return launch_fwd<64, false>(mq, mk, mv, mo, p, status_word, grid, num_sms, stream);
+    if (D <= 128)
+        return launch_fwd<128, false>(mq, mk, mv, mo, p, status_word, grid, num_sms, stream);
     attn_fwd_d256_kernel<<<static_cast<unsigned int>(grid), kW256Threads, Fwd256Smem::kAlloc,
                            stream>>>(mq, mk, mv, mo, p, status_word);
     const cudaError_t e = cudaGetLastError();
@@ -404,7 +438,7 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* out, 
     st = prepare(P, &ds, &mq, &mk, &mv, &mo, &prm);
     if (st != ATTN_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return launch_single(D, mq, mk, mv, mo, prm, ds->status_word, P.items, s);
+    return launch_single(D, mq, mk, mv, mo, prm, ds->status_word, P.items, ds->num_sms, s);
 }
 
 extern "C" int attn_fwd_strided(const void* q, const void* k, const void* v, void* out,
@@ -429,7 +463,7 @@ extern "C" int attn_fwd_strided(const void* q, const void* k, const void* v, voi
     st = prepare(P, &ds, &mq, &mk, &mv, &mo, &prm);
     if (st != ATTN_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return launch_single(D, mq, mk, mv, mo, prm, ds->status_word, P.items, s);
+    return launch_single(D, mq, mk, mv, mo, prm, ds->status_word, P.items, ds->num_sms, s);
 }
 
 extern "C" int attn_fwd_test_stall(const void* q, const void* k, const void* v, void* out,
@@ -448,8 +482,10 @@ extern "C" int attn_fwd_test_stall(const void* q, const void* k, const void* v, 
     if (st != ATTN_OK) return st;
     prm.stall_item = stall_item;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return D <= 64 ? launch_fwd<64, false>(mq, mk, mv, mo, prm, ds->status_word, P.items, s)
-                   : launch_fwd<128, false>(mq, mk, mv, mo, prm, ds->status_word, P.items, s);
+    return D <= 64 ? launch_fwd<64, false>(mq, mk, mv, mo, prm, ds->status_word, P.items,
+                                           ds->num_sms, s)
+                   : launch_fwd<128, false>(mq, mk, mv, mo, prm, ds->status_word, P.items,
+                                            ds->num_sms, s);
 }
 
 extern "C" int attn_fwd_splitkv_num_splits(int B, int Hq, int N, int D, int causal) {
@@ -514,9 +550,10 @@ extern "C" int attn_fwd_splitkv(const void* q, const void* k, const void* v, voi
     prm.ws_o = static_cast<float*>(workspace);
     prm.ws_lse = prm.ws_o + static_cast<int64_t>(n_splits) * P.bh * N * padded_dim(D);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int64_t grid = P.items * n_splits;
-    st = D <= 64 ? launch_fwd<64, true>(mq, mk, mv, mo, prm, ds->status_word, grid, s)
-                 : launch_fwd<128, true>(mq, mk, mv, mo, prm, ds->status_word, grid, s);
+    const int64_t items = P.items * n_splits;
+    st = D <= 64 ? launch_fwd<64, true>(mq, mk, mv, mo, prm, ds->status_word, items, ds->num_sms, s)
+                 : launch_fwd<128, true>(mq, mk, mv, mo, prm, ds->status_word, items, ds->num_sms,
+                                         s);
     if (st != ATTN_OK) return st;
     auto* o = static_cast<__nv_bfloat16*>(out);
     return D <= 64 ? launch_merge<64>(prm, o, D, s) : launch_merge<128>(prm, o, D, s);
@@ -793,7 +830,9 @@ extern "C" const char* attn_status_string(int status) {
                    "backward [8, 128]; MLA decode: d_c = 512 and d_r = 64)";
         case ATTN_ERR_ALIGN: return "a pointer is not 16-byte aligned";
         case ATTN_ERR_SCALE: return "sm_scale must be finite and positive";
-        case ATTN_ERR_ARCH: return "the current device is not sm_103 (GB300)";
+        case ATTN_ERR_ARCH:
+            return "the device is not sm_103 (GB300), its shared memory is misaligned, or a kernel "
+                   "was built with an unexpected register count";
         case ATTN_ERR_CUDA: return "a CUDA call failed (see attn_last_cuda_error)";
         case ATTN_ERR_TIMEOUT: return "a device-side bounded wait expired";
         case ATTN_ERR_MEMORY: return "a pointer is not device memory of the current device";

@@ -11,18 +11,23 @@
 //   recurrence (exp2 domain: scores are pre-multiplied by sm_scale*log2(e)); after the last tile
 //   O = acc / l and LSE = ln2 * (m + log2 l).  The N x N score matrix never leaves the SM.
 //
-// GB300 mapping (one CTA per pair of 128-row Q tiles, 352 threads):
-//   warp 10     TMA producer: Q0/Q1 once, then K_j, V_j through a KV_STAGES-deep mbarrier ring.
+// GB300 mapping (persistent: one CTA per SM, 352 threads, each CTA works through pairs of
+// 128-row Q tiles that it claims from a per-launch counter in global memory):
+//   warp 10     TMA producer: lane 0 claims the next work item and publishes it through a 2-slot
+//               item ring in shared memory; one lane per 64-column panel stream loads K_j, V_j
+//               through a 4-slot mbarrier ring and the Q tiles into their own buffers, so the next
+//               item's Q, K and V load while the current item finishes.
 //   warps 8, 9  MMA issuers (one lane each), warp 8 + t for Q tile t: S_t = Q_t K_j^T (SS form,
 //               fp32 in TMEM) and O_t += P_t V_j (P from TMEM, V from smem); tcgen05.commit
 //               signals completion.
 //   warps 0-3   softmax for Q tile 0, warps 4-7 for Q tile 1: one thread per query row reads its
 //               S row from TMEM, masks (diagonal causal tile / ragged last key tile only), updates
 //               m and l, rescales its O row in TMEM when m moved, writes P (bf16) over S in TMEM;
-//               after the last tile it normalises O, stages it in smem and TMA-stores it, and
-//               writes LSE.
+//               after the last tile it normalises O, stages it in smem one 64-column panel at a
+//               time and TMA-stores it, and writes LSE.
 //   The two Q tiles ping-pong: while one softmax group works, the tensor core runs the other
-//   tile's MMAs.
+//   tile's MMAs.  Across items every barrier keeps counting phases, so item k+1's first S MMAs
+//   run while item k's softmax and epilogue finish.
 //   The running maximum is only moved when it grows by more than 8 (log2 units): p <= 2^8 stays
 //   exact in fp32/bf16 range and the final O = acc / l and LSE = m + log2 l use the same m, so
 //   the result is unchanged while most O rescales are skipped.
@@ -38,21 +43,36 @@ namespace gb300attn {
 
 constexpr int kBM = 128;          // query rows per Q tile (MMA M)
 constexpr int kBN = 128;          // key rows per KV tile (MMA N of S, K of P.V)
-constexpr int kQTiles = 2;        // Q tiles per CTA
+constexpr int kQTiles = 2;        // Q tiles per work item
 constexpr int kStages = 4;        // K/V ring slots (K_j and V_j take one slot each)
-constexpr int kThreads = 352;     // 11 warps
+constexpr int kThreads = 384;     // 12 warps: two softmax warpgroups, one for the other roles
 constexpr int kMmaWarp0 = 8;      // issues the MMAs of Q tile 0; warp 9 those of Q tile 1
-constexpr int kLoadWarp = 10;
+constexpr int kLoadWarp = 10;     // warp 11 has no role (it completes the third warpgroup)
+// Register split (setmaxnreg): the CTA is launched with kLaunchRegs per thread; the third
+// warpgroup gives registers back and the softmax warpgroups take them.  The shares add up to the
+// launch's total exactly (setmaxnreg.inc would wait forever for registers the launch never had,
+// so the host checks the built kernel's register count before the first launch), and each SM
+// sub-partition (warps w, w+4, w+8) fits its 16384 registers.
+constexpr int kLaunchRegs = 168;
+constexpr int kSoftmaxRegs = 192;
+constexpr int kOtherRegs = 120;
+static_assert(kLaunchRegs * kThreads == 256 * kSoftmaxRegs + 128 * kOtherRegs, "register split");
+static_assert(32 * (2 * kSoftmaxRegs + kOtherRegs) <= 16384, "sub-partition register file");
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLn2 = 0.69314718055994530942f;
+// Claim counters: the host hands each launch one of kSchedSlots counters, round robin.  CTA c
+// takes item c first, then claims items gridDim.x + 0, 1, 2, ... from the counter until a claim
+// falls past the end; so a launch makes exactly `items` claims, and the CTA whose claim returns
+// items - 1 (the last one) zeroes the counter for the next launch that gets this slot.
+constexpr int kSchedSlots = 64;
 
 struct AttnParams {
     int B, Hq, Hkv, N;
     int group;         // Hq / Hkv
     int causal;
     int n_tiles;       // ceil(N / 128): number of Q tiles and of KV tiles per head
-    int n_pairs;       // ceil(n_tiles / 2): CTAs per (b, hq)
+    int n_pairs;       // ceil(n_tiles / 2): work items per (b, hq)
     float scale_log2;  // sm_scale * log2(e)
     int kv_block;      // (batch, KV head) pairs per scheduling block (their K/V fit in L2)
     float* lse;        // [B, Hq, N] fp32
@@ -61,44 +81,107 @@ struct AttnParams {
     int split_tiles;
     float* ws_o;       // [n_splits, B*Hq, N, D] fp32, O of each split normalised by its own l
     float* ws_lse;     // [n_splits, B*Hq, N] fp32, natural-log LSE of each split
-    // Test hook (-1 normally): the producer withholds K/V ring item `stall_item` of every CTA,
+    // Test hook (-1 normally): the producer withholds K/V ring entry `stall_item` of every CTA,
     // so the waits on it expire and the failure is reported through the status word.
     int stall_item;
+    int items;             // work items of the launch (Q-tile pairs x splits)
+    unsigned int* sched;   // this launch's claim counter (persistent kernels), zero at launch
+    // O for the two-tile kernel's own stores: base, element strides of batch, head and row, and
+    // the head dimension (columns at and past it are padding, not part of O)
+    __nv_bfloat16* out;
+    long long o_sb, o_sh, o_sn;
+    int d_out;
 };
 
 template <int D>
 struct SmemLayout {
     static constexpr int kPanelBytes = kBM * 64 * 2;        // 128 rows x 64 bf16 (one 128B-swizzle panel)
     static constexpr int kTileBytes = kBM * D * 2;          // 128 x D bf16 = D/64 panels
-    static constexpr int kQ = 0;                            // Q tiles (reused as O staging)
+    static constexpr int kQ = 0;                            // Q tiles
     static constexpr int kKV = kQ + kQTiles * kTileBytes;   // K/V ring
-    static constexpr int kP1 = kKV + kStages * kTileBytes;     // P keys 64..127, [2 tiles]
-    static constexpr int kP1Bytes = kBM * 64 * 2;               // one 128B-swizzle panel
+    static constexpr int kP1 = kKV + kStages * kTileBytes;  // P keys 64..127 / O staging, [2 tiles]
+    static constexpr int kP1Bytes = kBM * 64 * 2;           // one 128B-swizzle panel
     static constexpr int kBars = kP1 + 2 * kP1Bytes;
     // barrier indices
-    static constexpr int kBarQ = 0;
-    static constexpr int kBarKvFull = 1;
+    static constexpr int kBarQFull = 0;                       // [2 tiles]
+    static constexpr int kBarQFree = kBarQFull + 2;           // [2 tiles]: last S of an item done
+    static constexpr int kBarKvFull = kBarQFree + 2;
     static constexpr int kBarKvEmpty = kBarKvFull + kStages;
     static constexpr int kBarSFull = kBarKvEmpty + kStages;   // [2]
     static constexpr int kBarPReady = kBarSFull + 2;          // [2 tiles][2 key halves]
     static constexpr int kBarPVDone = kBarPReady + 4;         // [2]: a step's P.V completed
     static constexpr int kBarODone = kBarPVDone + 2;          // [2]
     static constexpr int kBarTurn = kBarODone + 2;            // [2]: softmax group t may run exp2
-    static constexpr int kNumBars = kBarTurn + 2;
-    static constexpr int kTmemSlot = kBars + kNumBars * 8;
+    static constexpr int kBarItemFull = kBarTurn + 2;         // [2]: item ring slot written
+    static constexpr int kBarItemEmpty = kBarItemFull + 2;    // [2]: item ring slot read by all
+    static constexpr int kNumBars = kBarItemEmpty + 2;
+    static constexpr int kItems = kBars + kNumBars * 8;       // int[2]: the item ring
+    static constexpr int kTmemSlot = kItems + 8;
     static constexpr int kAbort = kTmemSlot + 8;
     static constexpr int kBytes = kAbort + 8;
     static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024 bytes
+    // producer lanes: K panels, V panels, Q tile 0 panels, Q tile 1 panels
+    static constexpr int kLoadLanes = 4 * (D / 64);
+    // readers of an item ring slot besides the claiming lane: the other producer lanes, the two
+    // issuer warps and the eight softmax warps (one arrival per warp)
+    static constexpr int kItemReaders = kLoadLanes - 1 + 2 + 8;
 };
 
 // TMEM column map: S_t at 128*t (P_t aliases the first 64 columns of S_t), O_t at 256 + 128*t.
 __device__ __forceinline__ uint32_t tmem_s_col(int t) { return 128u * t; }
 __device__ __forceinline__ uint32_t tmem_o_col(int t) { return 256u + 128u * t; }
 
+// One work item: a pair of Q tiles of one (batch, query head), and for the split instantiation
+// one range of KV tiles.
+struct FwdWork {
+    int b, hkv, hq, bh, tile0, split;
+    int kv_begin;      // first KV tile of the item
+    int last0, last1;  // last KV tile of Q tile 0 / 1 (the diagonal under the causal mask)
+    int kv_end;        // one past the last KV tile the item loads
+    bool part0, part1;  // Q tile t takes part (its KV range is not empty)
+};
+
+// Item order: blocks of kv_block (batch, KV head) pairs whose K/V fit in L2 together; within a
+// block, Q-tile pairs heaviest (latest) first, then the KV heads, then the query heads sharing
+// each KV head.  Items are claimed in this order, so the CTAs working at any time read K/V of one
+// block (which stays in L2), and every block (and so the launch) ends on its lightest causal pairs.
+template <bool kSplit>
+__device__ __forceinline__ FwdWork decode_work(const AttnParams& p, int item) {
+    FwdWork w;
+    w.split = 0;
+    if constexpr (kSplit) {
+        w.split = item % p.n_splits;
+        item /= p.n_splits;
+    }
+    const int per_kv = p.n_pairs * p.group;
+    const int blk = item / (p.kv_block * per_kv);
+    const int in_blk = item % (p.kv_block * per_kv);
+    const int kvs = min(p.kv_block, p.B * p.Hkv - blk * p.kv_block);  // KV heads in this block
+    const int bh_kv = blk * p.kv_block + (in_blk % (kvs * p.group)) / p.group;
+    const int rem = in_blk % p.group;
+    const int pair = p.n_pairs - 1 - in_blk / (kvs * p.group);
+    w.b = bh_kv / p.Hkv;
+    w.hkv = bh_kv % p.Hkv;
+    w.hq = w.hkv * p.group + rem;
+    w.bh = w.b * p.Hq + w.hq;
+    w.tile0 = 2 * pair;
+    // Each Q tile t uses [kv_begin, last_t]; under the causal mask its last tile is its diagonal
+    // (BM == BN, so it has the Q tile's index).  A Q tile takes part if that range is not empty
+    // (always, unless a later split starts past it).
+    w.kv_begin = kSplit ? w.split * p.split_tiles : 0;
+    const int kv_limit = kSplit ? min(w.kv_begin + p.split_tiles, p.n_tiles) : p.n_tiles;
+    w.last0 = min(kv_limit - 1, p.causal ? w.tile0 : p.n_tiles - 1);
+    w.last1 = min(kv_limit - 1, p.causal ? w.tile0 + 1 : p.n_tiles - 1);
+    w.part0 = w.last0 >= w.kv_begin;
+    w.part1 = w.tile0 + 1 < p.n_tiles && w.last1 >= w.kv_begin;
+    w.kv_end = (w.part1 ? w.last1 : w.last0) + 1;
+    return w;
+}
+
 // kSplit = false: the whole KV range, bf16 O and LSE written to the outputs.
-// kSplit = true:  the KV range of one split (split index innermost in blockIdx.x); the fp32 O of
-//                 that range (normalised by its own denominator) and its LSE go to the workspace,
-//                 and attn_splitkv_merge_kernel combines the splits.
+// kSplit = true:  the KV range of one split (split index innermost in the item number); the fp32
+//                 O of that range (normalised by its own denominator) and its LSE go to the
+//                 workspace, and attn_splitkv_merge_kernel combines the splits.
 template <int D, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
@@ -119,60 +202,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto bar = [=](int i) -> uint32_t { return sbase + L::kBars + 8u * i; };
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
+    volatile int* item_ring = reinterpret_cast<volatile int*>(smem + L::kItems);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // ---- work decomposition --------------------------------------------------------------------
-    // Block order: blocks of kv_block (batch, KV head) pairs whose K/V fit in L2 together; within
-    // a block, Q-tile pairs heaviest (latest) first, then the KV heads, then the query heads
-    // sharing each KV head.  CTAs running together read K/V of one block (which stays in L2), and
-    // every block (and so the grid) ends on its lightest causal pairs.
-    int item = static_cast<int>(blockIdx.x);
-    int split = 0;
-    if constexpr (kSplit) {
-        split = item % p.n_splits;
-        item /= p.n_splits;
-    }
-    const int per_kv = p.n_pairs * p.group;
-    const int blk = item / (p.kv_block * per_kv);
-    const int in_blk = item % (p.kv_block * per_kv);
-    const int kvs = min(p.kv_block, p.B * p.Hkv - blk * p.kv_block);  // KV heads in this block
-    const int bh_kv = blk * p.kv_block + (in_blk % (kvs * p.group)) / p.group;
-    const int rem = in_blk % p.group;
-    const int pair = p.n_pairs - 1 - in_blk / (kvs * p.group);
-    const int b = bh_kv / p.Hkv;
-    const int hkv = bh_kv % p.Hkv;
-    const int hq = hkv * p.group + rem;
-    const int bh = b * p.Hq + hq;
-    const int tile0 = 2 * pair;
-    // This CTA's KV tiles: [kv_begin, kv_limit).  Each Q tile t uses [kv_begin, last_t]; under the
-    // causal mask its last tile is its diagonal (BM == BN, so it has the Q tile's index).  A Q
-    // tile takes part if that range is not empty (always, unless a later split starts past it).
-    const int kv_begin = kSplit ? split * p.split_tiles : 0;
-    const int kv_limit = kSplit ? min(kv_begin + p.split_tiles, p.n_tiles) : p.n_tiles;
-    const int last0 = min(kv_limit - 1, p.causal ? tile0 : p.n_tiles - 1);
-    const int last1 = min(kv_limit - 1, p.causal ? tile0 + 1 : p.n_tiles - 1);
-    const bool part0 = last0 >= kv_begin;
-    const bool part1 = tile0 + 1 < p.n_tiles && last1 >= kv_begin;
-    const bool pingpong = part0 && part1;
-    const int n_part = static_cast<int>(part0) + static_cast<int>(part1);
-    const int kv_end = (part1 ? last1 : last0) + 1;  // one past the last KV tile this CTA loads
-
-    // ---- setup ---------------------------------------------------------------------------------
+    // ---- setup (once per CTA) ------------------------------------------------------------------
     if (threadIdx.x == 0) {
-        mbar_init(bar(L::kBarQ), n_part > 0 ? n_part * kPanels : 1);  // one arrive per Q panel
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(bar(L::kBarKvFull + s), kPanels);  // one arrive (+ tx) per panel
-            mbar_init(bar(L::kBarKvEmpty + s), n_part > 0 ? n_part : 1);  // one release per issuer
-        }
         for (int t = 0; t < 2; ++t) {
+            mbar_init(bar(L::kBarQFull + t), kPanels);  // one arrive (+ tx) per Q panel
+            mbar_init(bar(L::kBarQFree + t), 1);
             mbar_init(bar(L::kBarSFull + t), 1);
             mbar_init(bar(L::kBarPReady + 2 * t + 0), 128);
             mbar_init(bar(L::kBarPReady + 2 * t + 1), 128);
             mbar_init(bar(L::kBarPVDone + t), 1);
             mbar_init(bar(L::kBarODone + t), 1);
             mbar_init(bar(L::kBarTurn + t), 128);
+            mbar_init(bar(L::kBarItemFull + t), 1);
+            mbar_init(bar(L::kBarItemEmpty + t), L::kItemReaders);
+        }
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bar(L::kBarKvFull + s), kPanels);  // one arrive (+ tx) per panel
+            mbar_init(bar(L::kBarKvEmpty + s), 2);       // one release per issuer
         }
         *abort_flag = 0;
         fence_mbarrier_init();
@@ -186,39 +237,115 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmap_q);
         tma_prefetch_desc(&tmap_k);
         tma_prefetch_desc(&tmap_v);
-        tma_prefetch_desc(&tmap_o);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    // Item ring reader (every role but the claiming lane): the item number of the k-th item, or
+    // -1 at the end (or after an abort).  Warps pass warp = true (one arrival per warp).
+    auto read_item = [&](int k, bool whole_warp) -> int {
+        const int slot = k & 1;
+        const uint32_t ph = static_cast<uint32_t>(k >> 1) & 1u;
+        bool ok;
+        if (whole_warp)
+            ok = mbar_wait_warp(bar(L::kBarItemFull + slot), ph, abort_flag, status_word);
+        else
+            ok = mbar_wait_bounded(bar(L::kBarItemFull + slot), ph, abort_flag, status_word);
+        if (!ok) return -1;
+        int item = item_ring[slot];
+        if (whole_warp) {
+            // redux.sync leaves its result in a uniform register, so everything a warp derives
+            // from the item (ring indices, smem descriptors, barrier phases) stays in the
+            // uniform datapath, as blockIdx-derived values would.
+            item = __reduce_min_sync(0xffffffffu, item);
+            mbar_arrive_warp(bar(L::kBarItemEmpty + slot));
+        } else {
+            mbar_arrive(bar(L::kBarItemEmpty + slot));
+        }
+        return item;
+    };
+
+    // Each role's code follows its warpgroup's register budget (setmaxnreg at the top of the
+    // warpgroup's branch), so the compiler allocates the softmax code with kSoftmaxRegs.
+    if (warp >= kMmaWarp0) {
+    setmaxnreg_dec<kOtherRegs>();
     if (warp == kLoadWarp) {
-        // ====================== TMA producer: one lane per 64-column panel =======================
+        // ====================== TMA producer: one lane per 64-column panel stream ===============
         // One thread's bulk tensor copies are processed one after another (measured: ~29 bytes
-        // per cycle per SM from one issuing thread, ~50 from two, ~85 from four), so lane
-        // kv*kPanels + h streams panel h of every K (kv = 0) or V (kv = 1) tile, and the Q panels
-        // are spread over the same lanes.  Each lane arrives with its own panel's bytes.
-        if (lane < 2 * kPanels && n_part > 0) {
-            const int kv = lane / kPanels, h = lane % kPanels;
-            if (kv == 0 ? part0 : part1) {  // Q tile kv, panel h
-                mbar_arrive_expect_tx(bar(L::kBarQ), L::kPanelBytes);
-                tma_load_4d(sbase + L::kQ + kv * L::kTileBytes + h * L::kPanelBytes, &tmap_q,
-                            bar(L::kBarQ), h * 64, (tile0 + kv) * kBM, hq, b);
+        // per cycle per SM from one issuing thread, ~50 from two, ~85 from four), so lane h
+        // streams panel h of every K tile, lane kPanels + h panel h of every V tile, and lane
+        // 2*kPanels + t*kPanels + h panel h of Q tile t.  Each lane arrives with its own panel's
+        // bytes.  Lane 0 also claims the items.
+        if (lane < L::kLoadLanes) {
+            int ring = 0;                // K/V ring entries of the earlier items
+            uint32_t q_loads = 0;        // Q tiles this lane loaded so far
+            bool claims_done = false;    // lane 0: this CTA's claim past the end was made
+            // One claim: the item number, or -1 past the end (the launch's last claim also
+            // zeroes the counter).
+            auto claim = [&]() -> int {
+                const unsigned int c = atomicAdd(p.sched, 1u);
+                const unsigned int it = c + gridDim.x;
+                if (it < static_cast<unsigned int>(p.items)) return static_cast<int>(it);
+                claims_done = true;
+                if (c == static_cast<unsigned int>(p.items) - 1u) atomicExch(p.sched, 0u);
+                return -1;
+            };
+            for (int k = 0;; ++k) {
+                int item;
+                if (lane == 0) {
+                    const int slot = k & 1;
+                    if (!mbar_wait_bounded(bar(L::kBarItemEmpty + slot),
+                                           (static_cast<uint32_t>(k >> 1) & 1u) ^ 1u, abort_flag,
+                                           status_word))
+                        break;
+                    item = k == 0 ? static_cast<int>(blockIdx.x) : claim();
+                    item_ring[slot] = item;
+                    mbar_arrive(bar(L::kBarItemFull + slot));
+                } else {
+                    item = read_item(k, false);
+                }
+                if (item < 0) break;
+                const FwdWork w = decode_work<kSplit>(p, item);
+                if (!(w.part0 || w.part1)) continue;
+                if (lane >= 2 * kPanels) {  // Q tile t, panel h
+                    const int t = (lane - 2 * kPanels) / kPanels, h = lane % kPanels;
+                    if (t == 0 ? w.part0 : w.part1) {
+                        if (q_loads > 0 &&
+                            !mbar_wait_bounded(bar(L::kBarQFree + t), (q_loads - 1) & 1u,
+                                               abort_flag, status_word))
+                            break;
+                        mbar_arrive_expect_tx(bar(L::kBarQFull + t), L::kPanelBytes);
+                        tma_load_4d(sbase + L::kQ + t * L::kTileBytes + h * L::kPanelBytes,
+                                    &tmap_q, bar(L::kBarQFull + t), h * 64,
+                                    (w.tile0 + t) * kBM, w.hq, w.b);
+                        ++q_loads;
+                    }
+                } else {  // K (kv = 0) or V (kv = 1), panel h
+                    const int kv = lane / kPanels, h = lane % kPanels;
+                    const CUtensorMap* map = kv ? &tmap_v : &tmap_k;
+                    bool ok = true;
+                    for (int j = w.kv_begin; j < w.kv_end; ++j) {
+                        const int idx = ring + 2 * (j - w.kv_begin) + kv;
+                        const int slot = idx % kStages;
+                        const uint32_t ph = (idx / kStages) & 1;
+                        ok = mbar_wait_bounded(bar(L::kBarKvEmpty + slot), ph ^ 1u, abort_flag,
+                                               status_word);
+                        if (!ok) break;
+                        if (idx == p.stall_item) continue;  // test hook: never deliver this entry
+                        mbar_arrive_expect_tx(bar(L::kBarKvFull + slot), L::kPanelBytes);
+                        tma_load_4d(sbase + L::kKV + slot * L::kTileBytes + h * L::kPanelBytes,
+                                    map, bar(L::kBarKvFull + slot), h * 64, j * kBN, w.hkv, w.b);
+                    }
+                    if (!ok) break;
+                }
+                ring += 2 * (w.kv_end - w.kv_begin);
             }
-            const CUtensorMap* map = kv ? &tmap_v : &tmap_k;
-            for (int j = kv_begin; j < kv_end; ++j) {
-                const int idx = 2 * (j - kv_begin) + kv;
-                const int slot = idx % kStages;
-                const uint32_t ph = (idx / kStages) & 1;
-                if (!mbar_wait_bounded(bar(L::kBarKvEmpty + slot), ph ^ 1u, abort_flag,
-                                       status_word))
-                    break;
-                if (idx == p.stall_item) continue;  // test hook: never deliver this item
-                mbar_arrive_expect_tx(bar(L::kBarKvFull + slot), L::kPanelBytes);
-                tma_load_4d(sbase + L::kKV + slot * L::kTileBytes + h * L::kPanelBytes, map,
-                            bar(L::kBarKvFull + slot), h * 64, j * kBN, hkv, b);
-            }
+            // After an abort, still make this CTA's claims up to the one past the end, so the
+            // launch's claim count (and the counter's reset) stays exact.
+            if (lane == 0)
+                while (!claims_done) (void)claim();
         }
         __syncwarp();
     } else if (warp == kMmaWarp0 || warp == kMmaWarp0 + 1) {
@@ -226,134 +353,187 @@ __global__ void __launch_bounds__(kThreads, 1)
         // One issuing thread starts a tcgen05.mma only every ~95 cycles (warp-uniform loop,
         // elected lane), more than the 64 tensor cycles of an M=128, N=128, K=16 MMA; two issuers
         // with independent accumulators keep the tensor core fed, also while the other tile's
-        // issuer waits for its softmax.
+        // issuer waits for its softmax.  Every K/V ring entry gets one release per issuer: after
+        // its MMAs, or (an entry this tile does not use) as soon as it has landed, so every slot
+        // phase gets exactly two releases and never completes early.
         const int t = warp - kMmaWarp0;
-        if (t == 0 ? part0 : part1) {  // warp-uniform: every lane runs the loop, one lane issues
-            const int last = t == 0 ? last0 : last1;
-            const uint32_t s_tmem = tmem + tmem_s_col(t);
-            const uint32_t o_tmem = tmem + tmem_o_col(t);
-            const uint32_t qa = sbase + L::kQ + t * L::kTileBytes;
-            auto kv_slot = [](int idx) { return idx % kStages; };
-            auto kv_phase = [](int idx) { return static_cast<uint32_t>((idx / kStages) & 1); };
-            auto wait_full = [=](int idx) {
-                return mbar_wait_warp(bar(L::kBarKvFull + kv_slot(idx)), kv_phase(idx),
-                                      abort_flag, status_word);
-            };
-            // S_t = Q_t . K^T  (8 MMAs of K = 16 at D = 128)
-            auto s_mma = [=](int kslot) {
-                const uint32_t ka = sbase + L::kKV + kslot * L::kTileBytes;
+        const uint32_t s_tmem = tmem + tmem_s_col(t);
+        const uint32_t o_tmem = tmem + tmem_o_col(t);
+        const uint32_t qa = sbase + L::kQ + t * L::kTileBytes;
+        auto kv_slot = [](int idx) { return idx % kStages; };
+        auto kv_phase = [](int idx) { return static_cast<uint32_t>((idx / kStages) & 1); };
+        auto wait_full = [=](int idx) {
+            return mbar_wait_warp(bar(L::kBarKvFull + kv_slot(idx)), kv_phase(idx), abort_flag,
+                                  status_word);
+        };
+        // S_t = Q_t . K^T  (8 MMAs of K = 16 at D = 128)
+        auto s_mma = [=](int kslot) {
+            const uint32_t ka = sbase + L::kKV + kslot * L::kTileBytes;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
-                    mma_bf16_ss_warp(s_tmem, smem_desc_sw128(qa + off, 16, 1024),
-                                     smem_desc_sw128(ka + off, 16, 1024), kIdescS, kk > 0);
-                }
-            };
-            // O_t += P_t . V in two halves.  Keys 0-63 of P_t arrive in TMEM over S_t (TS form);
-            // keys 64-127 arrive in a swizzled smem panel (SS form).  Because the second half
-            // does not live in TMEM, S_t(j+1) can be issued right after the first half's MMAs
-            // and computes while the softmax still works on the second half.
-            const uint32_t p1a = sbase + L::kP1 + t * L::kP1Bytes;
-            auto pv_first = [=](int vslot, bool accumulate_first) {
-                const uint32_t va = sbase + L::kKV + vslot * L::kTileBytes;
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16_ts_warp(o_tmem, s_tmem + kk * 8,
-                                     smem_desc_sw128(va + kk * 2048, L::kPanelBytes, 1024),
-                                     kIdescPV, (accumulate_first || kk > 0) ? 1u : 0u);
-            };
-            auto pv_second = [=](int vslot) {
-                const uint32_t va = sbase + L::kKV + vslot * L::kTileBytes;
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16_ss_warp(o_tmem, smem_desc_sw128(p1a + kk * 32, 16, 1024),
-                                     smem_desc_sw128(va + (4 + kk) * 2048, L::kPanelBytes, 1024),
-                                     kIdescPV, 1u);
-            };
-
-            uint32_t p_phase = 0;
-            bool ok = mbar_wait_warp(bar(L::kBarQ), 0, abort_flag, status_word);
-            if (ok) ok = wait_full(0);
-            if (ok) {
-                tc_fence_after();
-                s_mma(kv_slot(0));
-                mma_commit_warp(bar(L::kBarSFull + t));
-                mma_commit_warp(bar(L::kBarKvEmpty + kv_slot(0)));
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
+                mma_bf16_ss_warp(s_tmem, smem_desc_sw128(qa + off, 16, 1024),
+                                 smem_desc_sw128(ka + off, 16, 1024), kIdescS, kk > 0);
             }
-            for (int j = kv_begin; ok && j <= last; ++j) {
-                const int vidx = 2 * (j - kv_begin) + 1;  // V_j
-                const int kidx = vidx + 1;                // K_{j+1}
-                ok = wait_full(vidx);
-                if (ok) ok = mbar_wait_warp(bar(L::kBarPReady + 2 * t + 0), p_phase, abort_flag,
-                                            status_word);
-                if (!ok) break;
-                tc_fence_after();
-                pv_first(kv_slot(vidx), j > kv_begin);
-                if (j + 1 <= last) {  // S_t(j+1) overwrites the first half of P_t(j): issued after
-                    ok = wait_full(kidx);
+        };
+        // O_t += P_t . V in two halves.  Keys 0-63 of P_t arrive in TMEM over S_t (TS form);
+        // keys 64-127 arrive in a swizzled smem panel (SS form).  Because the second half does
+        // not live in TMEM, S_t(j+1) can be issued right after the first half's MMAs and computes
+        // while the softmax still works on the second half.
+        const uint32_t p1a = sbase + L::kP1 + t * L::kP1Bytes;
+        auto pv_first = [=](int vslot, bool accumulate_first) {
+            const uint32_t va = sbase + L::kKV + vslot * L::kTileBytes;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16_ts_warp(o_tmem, s_tmem + kk * 8,
+                                 smem_desc_sw128(va + kk * 2048, L::kPanelBytes, 1024), kIdescPV,
+                                 (accumulate_first || kk > 0) ? 1u : 0u);
+        };
+        auto pv_second = [=](int vslot) {
+            const uint32_t va = sbase + L::kKV + vslot * L::kTileBytes;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16_ss_warp(o_tmem, smem_desc_sw128(p1a + kk * 32, 16, 1024),
+                                 smem_desc_sw128(va + (4 + kk) * 2048, L::kPanelBytes, 1024),
+                                 kIdescPV, 1u);
+        };
+
+        int ring = 0;          // K/V ring entries of the earlier items
+        uint32_t steps = 0;    // KV steps this tile ran in earlier items (P-ready phases)
+        uint32_t q_items = 0;  // items this tile took part in (Q-full phases)
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            const int item = read_item(k, true);
+            if (item < 0) break;
+            const FwdWork w = decode_work<kSplit>(p, item);
+            if (!(w.part0 || w.part1)) continue;
+            const bool part = t == 0 ? w.part0 : w.part1;
+            const int last = part ? (t == 0 ? w.last0 : w.last1) : w.kv_begin - 1;
+            if (part) {
+                ok = mbar_wait_warp(bar(L::kBarQFull + t), q_items & 1u, abort_flag, status_word);
+                if (ok) ok = wait_full(ring);
+                if (ok) {
+                    tc_fence_after();
+                    s_mma(kv_slot(ring));
+                    mma_commit_warp(bar(L::kBarSFull + t));
+                    mma_commit_warp(bar(L::kBarKvEmpty + kv_slot(ring)));
+                    if (last == w.kv_begin) mma_commit_warp(bar(L::kBarQFree + t));
+                }
+                for (int j = w.kv_begin; ok && j <= last; ++j) {
+                    const int vidx = ring + 2 * (j - w.kv_begin) + 1;  // V_j
+                    const int kidx = vidx + 1;                         // K_{j+1}
+                    ok = wait_full(vidx);
+                    if (ok) ok = mbar_wait_warp(bar(L::kBarPReady + 2 * t + 0), steps & 1u,
+                                                abort_flag, status_word);
                     if (!ok) break;
                     tc_fence_after();
-                    s_mma(kv_slot(kidx));
-                    mma_commit_warp(bar(L::kBarSFull + t));
-                    mma_commit_warp(bar(L::kBarKvEmpty + kv_slot(kidx)));
+                    pv_first(kv_slot(vidx), j > w.kv_begin);
+                    if (j + 1 <= last) {  // S_t(j+1) overwrites the first half of P_t(j)
+                        ok = wait_full(kidx);
+                        if (!ok) break;
+                        tc_fence_after();
+                        s_mma(kv_slot(kidx));
+                        mma_commit_warp(bar(L::kBarSFull + t));
+                        mma_commit_warp(bar(L::kBarKvEmpty + kv_slot(kidx)));
+                        if (j + 1 == last) mma_commit_warp(bar(L::kBarQFree + t));
+                    }
+                    ok = mbar_wait_warp(bar(L::kBarPReady + 2 * t + 1), steps & 1u, abort_flag,
+                                        status_word);
+                    if (!ok) break;
+                    tc_fence_after();
+                    pv_second(kv_slot(vidx));
+                    ++steps;
+                    mma_commit_warp(bar(L::kBarPVDone + t));
+                    if (j == last) mma_commit_warp(bar(L::kBarODone + t));
+                    mma_commit_warp(bar(L::kBarKvEmpty + kv_slot(vidx)));
                 }
-                ok = mbar_wait_warp(bar(L::kBarPReady + 2 * t + 1), p_phase, abort_flag,
-                                    status_word);
-                if (!ok) break;
-                tc_fence_after();
-                pv_second(kv_slot(vidx));
-                p_phase ^= 1u;
-                mma_commit_warp(bar(L::kBarPVDone + t));
-                if (j == last) mma_commit_warp(bar(L::kBarODone + t));
-                mma_commit_warp(bar(L::kBarKvEmpty + kv_slot(vidx)));
+                ++q_items;
             }
-            // KV tiles this Q tile does not need (under the causal mask, the last one for Q tile
-            // 0): release each slot once its data has landed, so every slot phase gets one
-            // release per issuer and never completes early.
-            for (int j = last + 1; ok && j < kv_end; ++j) {
+            // K/V tiles of this item that this Q tile does not need (under the causal mask, the
+            // last one for Q tile 0; all of them if the tile takes no part)
+            for (int j = last + 1; ok && j < w.kv_end; ++j) {
                 for (int kv = 0; ok && kv < 2; ++kv) {
-                    const int idx = 2 * (j - kv_begin) + kv;
+                    const int idx = ring + 2 * (j - w.kv_begin) + kv;
                     ok = wait_full(idx);
                     if (ok) mbar_arrive_warp(bar(L::kBarKvEmpty + kv_slot(idx)));
                 }
             }
+            ring += 2 * (w.kv_end - w.kv_begin);
         }
         __syncwarp();
+    }
     } else {
+        setmaxnreg_inc<kSoftmaxRegs>();
         // =========================== softmax + epilogue (warps 0-7) ============================
         const int t = warp >> 2;          // which Q tile
         const int quarter = warp & 3;     // TMEM lane quarter this warp may access
         const int row = quarter * 32 + lane;  // row within the Q tile
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-        if (t == 0 ? part0 : part1) {
-            const int q_tile = tile0 + t;
-            const int last = t == 0 ? last0 : last1;
-            const int row_g = q_tile * kBM + row;
-            const uint32_t s_addr = tmem + lane_base + tmem_s_col(t);
-            const uint32_t o_addr = tmem + lane_base + tmem_o_col(t);
-            const float c = p.scale_log2;
+        const uint32_t s_addr = tmem + lane_base + tmem_s_col(t);
+        const uint32_t o_addr = tmem + lane_base + tmem_o_col(t);
+        const uint32_t p1 = sbase + L::kP1 + t * L::kP1Bytes;  // P keys 64..127, O staging
+        const float c = p.scale_log2;
+        // Barrier phases, one bit each: S-full / P.V-done step parity, turn parity, O-done
+        // parity; and (tile 0) the hand-back of the previous ping-pong item still to be taken.
+        constexpr uint32_t kPhStep = 1u, kPhTurn = 2u, kPhODone = 4u, kOwed = 8u;
+        uint32_t ph = 0;
+        bool ok = true;
+        // The four warps of a group leave the item loop together (they share named barriers):
+        // they agree on every item they read and on the outcome of every item's waits.
+        for (int k = 0;; ++k) {
+            const int item = read_item(k, true);
+            if (!named_barrier_and(1 + t, 128, item >= 0)) break;
+            int n, lim, tw_until, ta_until;
+            bool mask_last, tw_first;
+            {
+                const FwdWork w = decode_work<kSplit>(p, item);
+                if (!(t == 0 ? w.part0 : w.part1)) continue;
+                const bool pingpong = w.part0 && w.part1;
+                const int q_tile = w.tile0 + t;
+                const int last = t == 0 ? w.last0 : w.last1;
+                n = last - w.kv_begin + 1;  // KV steps of this tile
+                // Only the last step can need a mask: the causal diagonal tile, or the ragged
+                // last key tile (non-causal).  lim = first masked key of this row.
+                mask_last = p.causal ? last == q_tile
+                                     : (last == p.n_tiles - 1 && (p.N % kBN) != 0);
+                lim = p.causal ? row + 1 : p.N - last * kBN;
+                // Ping-pong: the exp2 phases of the two softmax groups alternate (tile 0 step j,
+                // tile 1 step j, tile 0 step j+1, ...), so one group's exponentials overlap the
+                // other tile's MMAs instead of competing for the same issue slots and MUFU.  Tile
+                // 1 hands the turn back after each of its steps up to tile 0's last; tile 0 takes
+                // the hand-back of a ping-pong item's last step at its next item's first step, so
+                // neither turn barrier ever runs two phases ahead of its waiter.
+                //   step 0 waits iff tw_first, step i >= 1 iff i <= tw_until; step i hands the
+                //   turn over iff i <= ta_until.
+                if (t == 0) {
+                    tw_first = (ph & kOwed) != 0;
+                    tw_until = pingpong ? n - 1 : 0;
+                    ta_until = pingpong ? n - 1 : -1;
+                    ph = pingpong ? (ph | kOwed) : (ph & ~kOwed);
+                } else {
+                    const int n0 = pingpong ? w.last0 - w.kv_begin : -1;
+                    tw_first = n0 >= 0;
+                    tw_until = n0;
+                    ta_until = n0;
+                }
+            }
             float m = -INFINITY;  // running max of c*s (log2 units)
             float l = 0.f;        // running denominator
-            bool ok = true;
-            for (int j = kv_begin; j <= last; ++j) {
-                ok = mbar_wait_warp(bar(L::kBarSFull + t), (j - kv_begin) & 1, abort_flag,
-                                    status_word);
+            for (int i = 0; i < n; ++i) {
+                ok = mbar_wait_warp(bar(L::kBarSFull + t), ph & kPhStep, abort_flag, status_word);
                 if (!ok) break;
                 tc_fence_after();
-                // Masks (the causal diagonal tile, or the ragged last key tile) are applied in
-                // TMEM before the row is loaded, so the common unmasked step carries no mask code.
-                const bool diag = p.causal && j == q_tile;
-                const bool tail = !p.causal && j == p.n_tiles - 1 && (p.N % kBN) != 0;
-                if (diag || tail) {
-                    const int lim = diag ? row + 1 : p.N - j * kBN;  // first masked key
+                // Masks are applied in TMEM before the row is loaded, so the common unmasked step
+                // carries no mask code.
+                if (mask_last && i == n - 1) {
 #pragma unroll
                     for (int cc = 0; cc < kBN / 32; ++cc) {
                         uint32_t r[32];
                         tmem_ld32(s_addr + cc * 32, r);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (cc * 32 + i >= lim) r[i] = __float_as_uint(-INFINITY);
+                        for (int x = 0; x < 32; ++x)
+                            if (cc * 32 + x >= lim) r[x] = __float_as_uint(-INFINITY);
                         tmem_st32(s_addr + cc * 32, r);
                     }
                     tmem_wait_st();
@@ -367,32 +547,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   *reinterpret_cast<uint32_t(*)[32]>(&r[cc * 32]));
                     tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < kBN; ++i) s[i] = __uint_as_float(r[i]);
+                    for (int x = 0; x < kBN; ++x) s[x] = __uint_as_float(r[x]);
                 }
                 // row maximum: 8 independent chains of 3-input max
                 float mx[8];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) mx[k] = fmaxf(s[k], s[k + 8]);
+                for (int q = 0; q < 8; ++q) mx[q] = fmaxf(s[q], s[q + 8]);
 #pragma unroll
-                for (int i = 16; i < kBN; i += 16)
+                for (int x = 16; x < kBN; x += 16)
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) mx[k] = fmax3(mx[k], s[i + k], s[i + 8 + k]);
+                    for (int q = 0; q < 8; ++q) mx[q] = fmax3(mx[q], s[x + q], s[x + 8 + q]);
                 const float row_max =
                     fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
                 const float m_cand = row_max * c;
                 const float m_new = (m_cand > m + kRescaleThreshold) ? m_cand : m;
                 const float alpha = ex2_approx(m - m_new);  // 1 if unchanged, 0 on the first tile
-                const bool rescale = j > kv_begin && __any_sync(0xffffffffu, m_new != m);
+                const bool rescale = i > 0 && __any_sync(0xffffffffu, m_new != m);
                 m = m_new;
                 const float neg_m = -m;
-                // Ping-pong: the exp2 phases of the two softmax groups alternate (tile 0 step j,
-                // tile 1 step j, tile 0 step j+1, ...), so one group's exponentials overlap the
-                // other tile's MMAs instead of competing for the same issue slots and MUFU.
-                const bool turn_wait = pingpong && (t == 0 ? j > kv_begin : j <= last0);
-                if (turn_wait) {
-                    ok = mbar_wait_warp(bar(L::kBarTurn + t), (j - kv_begin - (t == 0)) & 1,
-                                        abort_flag, status_word);
+                if (i == 0 ? tw_first : i <= tw_until) {
+                    ok = mbar_wait_warp(bar(L::kBarTurn + t), (ph & kPhTurn) ? 1u : 0u, abort_flag,
+                                        status_word);
                     if (!ok) break;
+                    ph ^= kPhTurn;
                 }
                 // p = exp2(c*s - m).  Keys 0-63 go to TMEM (over S) and are published first; keys
                 // 64-127 go to this tile's smem panel, which the previous step's second-half P.V
@@ -406,19 +583,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         float x0, x1;
                         ffma2(x0, x1, s[col], s[col + 1], c, c, neg_m, neg_m);
                         const float p0 = ex2_approx(x0);
-                        const float p1 = ex2_approx(x1);
+                        const float p1v = ex2_approx(x1);
                         const int a = (i & 1) * 2;
-                        fadd2(acc[a], acc[a + 1], acc[a], acc[a + 1], p0, p1);
-                        pk[i] = pack_bf16x2(p0, p1);
+                        fadd2(acc[a], acc[a + 1], acc[a], acc[a + 1], p0, p1v);
+                        pk[i] = pack_bf16x2(p0, p1v);
                     }
                 };
-                const bool prev_pv = j > kv_begin;  // a previous step's P.V is in flight
+                const bool prev_pv = i > 0;  // a previous step's P.V is in flight
                 {
                     uint32_t pk[32];
                     exp_half(0, pk);
                     tmem_st32(s_addr, pk);
                     if (rescale) {
-                        ok = mbar_wait_warp(bar(L::kBarPVDone + t), (j - 1 - kv_begin) & 1,
+                        ok = mbar_wait_warp(bar(L::kBarPVDone + t), (ph & kPhStep) ^ 1u,
                                             abort_flag, status_word);
                         if (!ok) break;
 #pragma unroll
@@ -427,8 +604,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tmem_ld32(o_addr + cc * 32, r);
                             tmem_wait_ld();
 #pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                            for (int x = 0; x < 32; ++x)
+                                r[x] = __float_as_uint(__uint_as_float(r[x]) * alpha);
                             tmem_st32(o_addr + cc * 32, r);
                         }
                     }
@@ -440,11 +617,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t pk[32];
                     exp_half(1, pk);
                     if (prev_pv && !rescale) {
-                        ok = mbar_wait_warp(bar(L::kBarPVDone + t), (j - 1 - kv_begin) & 1,
+                        ok = mbar_wait_warp(bar(L::kBarPVDone + t), (ph & kPhStep) ^ 1u,
                                             abort_flag, status_word);
                         if (!ok) break;
                     }
-                    const uint32_t prow = sbase + L::kP1 + t * L::kP1Bytes + row * 128;
+                    const uint32_t prow = p1 + row * 128;
 #pragma unroll
                     for (int ch = 0; ch < 8; ++ch)
                         st_shared_v4(prow + ((ch ^ (row & 7)) << 4), pk[4 * ch], pk[4 * ch + 1],
@@ -453,75 +630,84 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive(bar(L::kBarPReady + 2 * t + 1));
                 }
                 l = l * alpha + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
-                // hand the turn to the other group (tile 1 only while tile 0 has steps left)
-                if (pingpong && (t == 1 ? j < last0 : true)) mbar_arrive(bar(L::kBarTurn + (t ^ 1)));
+                if (i <= ta_until) mbar_arrive(bar(L::kBarTurn + (t ^ 1)));  // hand the turn over
+                ph ^= kPhStep;
             }
-
-            if (ok) ok = mbar_wait_warp(bar(L::kBarODone + t), 0, abort_flag, status_word);
+            if (ok) ok = mbar_wait_warp(bar(L::kBarODone + t), (ph & kPhODone) ? 1u : 0u,
+                                        abort_flag, status_word);
+            ph ^= kPhODone;
+            if (!named_barrier_and(1 + t, 128, ok)) break;
+            tc_fence_after();
+            // The epilogue's coordinates, decoded again from an opaque copy of the item number so
+            // that they are not kept in registers through the step loop.
+            const FwdWork we = decode_work<kSplit>(p, opaque_int(item));
+            const int row_g = (we.tile0 + t) * kBM + row;
+            const float inv_l = 1.0f / l;
             if constexpr (kSplit) {
                 // ---- split epilogue: O_s = acc / l (fp32) and LSE_s to the workspace ----------
-                if (ok) {
-                    tc_fence_after();
-                    const float inv_l = 1.0f / l;
-                    const size_t prow =
-                        (static_cast<size_t>(split) * p.B * p.Hq + bh) * p.N + row_g;
-                    float* dst = p.ws_o + prow * D;
-#pragma unroll
-                    for (int cc = 0; cc < D / 32; ++cc) {
-                        uint32_t r[32];
-                        tmem_ld32(o_addr + cc * 32, r);  // warp-collective: every lane loads
-                        tmem_wait_ld();
-                        if (row_g < p.N) {
-#pragma unroll
-                            for (int i = 0; i < 8; ++i)
-                                st_global_v4f(dst + cc * 32 + 4 * i,
-                                              __uint_as_float(r[4 * i]) * inv_l,
-                                              __uint_as_float(r[4 * i + 1]) * inv_l,
-                                              __uint_as_float(r[4 * i + 2]) * inv_l,
-                                              __uint_as_float(r[4 * i + 3]) * inv_l);
-                        }
-                    }
-                    if (row_g < p.N) p.ws_lse[prow] = (m + __log2f(l)) * kLn2;
-                }
-            } else {
-            // ---- epilogue: O = acc / l -> bf16 -> smem (over Q_t) -> TMA store; LSE ----------
-            if (ok) {
-                tc_fence_after();
-                const float inv_l = 1.0f / l;
-                const uint32_t stage = sbase + L::kQ + t * L::kTileBytes;
+                const size_t prow =
+                    (static_cast<size_t>(we.split) * p.B * p.Hq + we.bh) * p.N + row_g;
+                float* dst = p.ws_o + prow * D;
 #pragma unroll
                 for (int cc = 0; cc < D / 32; ++cc) {
                     uint32_t r[32];
-                    tmem_ld32(o_addr + cc * 32, r);
+                    tmem_ld32(o_addr + cc * 32, r);  // warp-collective: every lane loads
                     tmem_wait_ld();
-                    const int panel = cc >> 1;
+                    if (row_g < p.N) {
 #pragma unroll
-                    for (int c16 = 0; c16 < 4; ++c16) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            w[i] = pack_bf16x2(__uint_as_float(r[c16 * 8 + 2 * i]) * inv_l,
-                                               __uint_as_float(r[c16 * 8 + 2 * i + 1]) * inv_l);
-                        const int chunk = (cc & 1) * 4 + c16;  // 16-byte chunk within the 128B row
-                        const uint32_t dst = stage + panel * L::kPanelBytes + row * 128 +
-                                             ((chunk ^ (row & 7)) << 4);
-                        st_shared_v4(dst, w[0], w[1], w[2], w[3]);
+                        for (int i = 0; i < 8; ++i)
+                            st_global_v4f(dst + cc * 32 + 4 * i, __uint_as_float(r[4 * i]) * inv_l,
+                                          __uint_as_float(r[4 * i + 1]) * inv_l,
+                                          __uint_as_float(r[4 * i + 2]) * inv_l,
+                                          __uint_as_float(r[4 * i + 3]) * inv_l);
                     }
                 }
+                if (row_g < p.N) p.ws_lse[prow] = (m + __log2f(l)) * kLn2;
+            } else {
+                // ---- epilogue: O = acc / l -> bf16, one 64-column panel at a time through this
+                // tile's P panel (free: O-done follows the last P.V), out with coalesced 16-byte
+                // stores (each warp instruction writes four 128-byte row segments); LSE.
+                const int q_row0 = (we.tile0 + t) * kBM;
+                __nv_bfloat16* obase = p.out + we.b * p.o_sb + we.hq * p.o_sh;
+                const int tid = quarter * 32 + lane;
+#pragma unroll
+                for (int h = 0; h < kPanels; ++h) {
+#pragma unroll
+                    for (int cc = 0; cc < 2; ++cc) {
+                        uint32_t r[32];
+                        tmem_ld32(o_addr + h * 64 + cc * 32, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int c16 = 0; c16 < 4; ++c16) {
+                            uint32_t v4[4];
+#pragma unroll
+                            for (int x = 0; x < 4; ++x)
+                                v4[x] = pack_bf16x2(__uint_as_float(r[c16 * 8 + 2 * x]) * inv_l,
+                                                    __uint_as_float(r[c16 * 8 + 2 * x + 1]) * inv_l);
+                            const int chunk = cc * 4 + c16;  // 16-byte chunk within the 128B row
+                            st_shared_v4(p1 + row * 128 + ((chunk ^ (row & 7)) << 4), v4[0], v4[1],
+                                         v4[2], v4[3]);
+                        }
+                    }
+                    named_barrier_sync(1 + t, 128);
+#pragma unroll
+                    for (int it = 0; it < 8; ++it) {
+                        const int flat = it * 128 + tid;
+                        const int r = flat >> 3, ch = flat & 7;
+                        uint32_t v0, v1, v2, v3;
+                        ld_shared_v4(p1 + r * 128 + ((ch ^ (r & 7)) << 4), v0, v1, v2, v3);
+                        const int col = h * 64 + ch * 8;
+                        if (q_row0 + r < p.N && col < p.d_out)
+                            st_global_v4u(obase + static_cast<long long>(q_row0 + r) * p.o_sn + col,
+                                          v0, v1, v2, v3);
+                    }
+                    named_barrier_sync(1 + t, 128);  // the panel may be written again
+                }
                 if (row_g < p.N)
-                    p.lse[static_cast<size_t>(bh) * p.N + row_g] = (m + __log2f(l)) * kLn2;
+                    p.lse[static_cast<size_t>(we.bh) * p.N + row_g] = (m + __log2f(l)) * kLn2;
             }
-            fence_proxy_async_smem();
-            named_barrier_sync(1 + t, 128);
-            if (ok && quarter == 0 && lane == 0) {
-                const uint32_t stage = sbase + L::kQ + t * L::kTileBytes;
-                for (int h = 0; h < kPanels; ++h)
-                    tma_store_4d(&tmap_o, stage + h * L::kPanelBytes, h * 64, q_tile * kBM, hq, b);
-                tma_store_commit_and_wait();
-            }
-            }  // !kSplit
-            __syncwarp();
         }
+        __syncwarp();
     }
 
     // ---- teardown ------------------------------------------------------------------------------

@@ -44,7 +44,8 @@ typedef enum {
     ATTN_ERR_HEADDIM = -4,  /* D not a multiple of 8 in [8, 256] ([8, 128] for the backward) */
     ATTN_ERR_ALIGN = -5,    /* a tensor pointer is not 16-byte aligned */
     ATTN_ERR_SCALE = -6,    /* sm_scale is not finite and positive */
-    ATTN_ERR_ARCH = -7,     /* the device is not sm_103, or its shared memory is misaligned */
+    ATTN_ERR_ARCH = -7,     /* the device is not sm_103, its shared memory is misaligned, or the
+                               library was built with an unexpected register count */
     ATTN_ERR_CUDA = -8,     /* a CUDA runtime/driver call failed; see attn_last_cuda_error() */
     ATTN_ERR_TIMEOUT = -9,  /* a device-side bounded wait expired (reported by attn_debug_status) */
     ATTN_ERR_MEMORY = -10,  /* a pointer is not device memory of the current device */
