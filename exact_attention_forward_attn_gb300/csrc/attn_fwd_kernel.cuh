@@ -15,11 +15,12 @@
 // 128-row Q tiles that it claims from a per-launch counter in global memory):
 //   warp 10     TMA producer: lane 0 claims the next work item and publishes it through a 2-slot
 //               item ring in shared memory; one lane per 64-column panel stream loads K_j, V_j
-//               through a 4-slot mbarrier ring and the Q tiles into their own buffers, so the next
-//               item's Q, K and V load while the current item finishes.
-//   warps 8, 9  MMA issuers (one lane each), warp 8 + t for Q tile t: S_t = Q_t K_j^T (SS form,
-//               fp32 in TMEM) and O_t += P_t V_j (P from TMEM, V from smem); tcgen05.commit
-//               signals completion.
+//               through a 4-slot mbarrier ring, so the next item's K and V load while the
+//               current item finishes.
+//   warps 8, 9  MMA issuers (one lane each), warp 8 + t for Q tile t: loads Q_t of each item as
+//               soon as the previous item's last S MMA has read the buffer; S_t = Q_t K_j^T (SS
+//               form, fp32 in TMEM) and O_t += P_t V_j (P from TMEM, V from smem);
+//               tcgen05.commit signals completion.  Warp 11 has no role.
 //   warps 0-3   softmax for Q tile 0, warps 4-7 for Q tile 1: one thread per query row reads its
 //               S row from TMEM, masks (diagonal causal tile / ragged last key tile only), updates
 //               m and l, rescales its O row in TMEM when m moved, writes P (bf16) over S in TMEM;
@@ -120,8 +121,8 @@ struct SmemLayout {
     static constexpr int kAbort = kTmemSlot + 8;
     static constexpr int kBytes = kAbort + 8;
     static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024 bytes
-    // producer lanes: K panels, V panels, Q tile 0 panels, Q tile 1 panels
-    static constexpr int kLoadLanes = 4 * (D / 64);
+    // producer lanes: K panels, V panels
+    static constexpr int kLoadLanes = 2 * (D / 64);
     // readers of an item ring slot besides the claiming lane: the other producer lanes, the two
     // issuer warps and the eight softmax warps (one arrival per warp)
     static constexpr int kItemReaders = kLoadLanes - 1 + 2 + 8;
@@ -275,12 +276,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ====================== TMA producer: one lane per 64-column panel stream ===============
         // One thread's bulk tensor copies are processed one after another (measured: ~29 bytes
         // per cycle per SM from one issuing thread, ~50 from two, ~85 from four), so lane h
-        // streams panel h of every K tile, lane kPanels + h panel h of every V tile, and lane
-        // 2*kPanels + t*kPanels + h panel h of Q tile t.  Each lane arrives with its own panel's
-        // bytes.  Lane 0 also claims the items.
+        // streams panel h of every K tile and lane kPanels + h panel h of every V tile; each
+        // lane arrives with its own panel's bytes.  (The Q tiles are loaded by their MMA
+        // issuers.)  Lane 0 also claims the items.
         if (lane < L::kLoadLanes) {
             int ring = 0;                // K/V ring entries of the earlier items
-            uint32_t q_loads = 0;        // Q tiles this lane loaded so far
             bool claims_done = false;    // lane 0: this CTA's claim past the end was made
             // One claim: the item number, or -1 past the end (the launch's last claim also
             // zeroes the counter).
@@ -309,20 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (item < 0) break;
                 const FwdWork w = decode_work<kSplit>(p, item);
                 if (!(w.part0 || w.part1)) continue;
-                if (lane >= 2 * kPanels) {  // Q tile t, panel h
-                    const int t = (lane - 2 * kPanels) / kPanels, h = lane % kPanels;
-                    if (t == 0 ? w.part0 : w.part1) {
-                        if (q_loads > 0 &&
-                            !mbar_wait_bounded(bar(L::kBarQFree + t), (q_loads - 1) & 1u,
-                                               abort_flag, status_word))
-                            break;
-                        mbar_arrive_expect_tx(bar(L::kBarQFull + t), L::kPanelBytes);
-                        tma_load_4d(sbase + L::kQ + t * L::kTileBytes + h * L::kPanelBytes,
-                                    &tmap_q, bar(L::kBarQFull + t), h * 64,
-                                    (w.tile0 + t) * kBM, w.hq, w.b);
-                        ++q_loads;
-                    }
-                } else {  // K (kv = 0) or V (kv = 1), panel h
+                {  // K (kv = 0) or V (kv = 1), panel h
                     const int kv = lane / kPanels, h = lane % kPanels;
                     const CUtensorMap* map = kv ? &tmap_v : &tmap_k;
                     bool ok = true;
@@ -410,6 +397,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool part = t == 0 ? w.part0 : w.part1;
             const int last = part ? (t == 0 ? w.last0 : w.last1) : w.kv_begin - 1;
             if (part) {
+                // this tile's Q for the item: lane h loads panel h once the previous item's last
+                // S MMA (which this warp issued) has read the buffer
+                if (lane < kPanels) {
+                    bool qok = q_items == 0 ||
+                               mbar_wait_bounded(bar(L::kBarQFree + t), (q_items - 1) & 1u,
+                                                 abort_flag, status_word);
+                    if (qok) {
+                        mbar_arrive_expect_tx(bar(L::kBarQFull + t), L::kPanelBytes);
+                        tma_load_4d(qa + lane * L::kPanelBytes, &tmap_q, bar(L::kBarQFull + t),
+                                    lane * 64, (w.tile0 + t) * kBM, w.hq, w.b);
+                    }
+                }
+                __syncwarp();
                 ok = mbar_wait_warp(bar(L::kBarQFull + t), q_items & 1u, abort_flag, status_word);
                 if (ok) ok = wait_full(ring);
                 if (ok) {
