@@ -1,0 +1,102 @@
+"""The persistent forward's work claiming, exercised through the C ABI.
+
+The two-tile forward runs one CTA per SM; each CTA takes one work item (a pair of Q tiles of one
+head) and then claims more from a per-launch counter, one of 64 the host hands out round robin;
+the launch's last claim sets its counter back to zero.  These tests check what that must not
+change: every item is computed exactly once whatever the launch order, the number of launches
+(more than the 64 counters), the grid size (more items than SMs, or fewer) or concurrent launches
+on other streams.  Each item's arithmetic does not depend on which CTA runs it, so repeated
+launches must give bit-identical outputs; one launch per shape is also checked against the oracle.
+"""
+import pytest
+import torch
+
+import oracle
+from exact_attention_forward_attn_gb300 import workloads as wl
+
+from test_parity_gpu import _check
+
+pytestmark = pytest.mark.gpu
+
+# More items than SMs (several claims per CTA), fewer (one static item per CTA), and a split run.
+SHAPES = [
+    wl.GQA4_CAUSAL,                                            # 256 items
+    wl.TINY_CAUSAL,                                            # 2 items
+    wl.Workload("pers-mqa-n2000", 1, 40, 1, 2000, 128, True, 41),  # 320 items, ragged N
+    wl.Workload("pers-d64-n3000", 2, 8, 4, 3000, 64, False, 42),   # 192 items, D = 64
+]
+
+
+def _inputs(w, dev):
+    q, k, v = wl.make_qkv(w)
+    return (q, k, v), tuple(t.to(dev) for t in (q, k, v))
+
+
+def test_many_launches_alternating_shapes_are_bit_identical(cuda_lib):
+    import exact_attention_forward_attn_gb300 as attn
+
+    dev = torch.device("cuda:0")
+    data = [_inputs(w, dev) for w in SHAPES]
+    first = []
+    for w, (host, (qd, kd, vd)) in zip(SHAPES, data):
+        out, lse = attn.attn_fwd(qd, kd, vd, causal=w.causal, sm_scale=w.sm_scale)
+        torch.cuda.synchronize()
+        o_ref, l_ref = oracle.attn_ref(*host, w.causal, w.sm_scale)
+        _check(out, lse, o_ref, l_ref, w.name)
+        first.append((out.clone(), lse.clone()))
+    # 3 x 4 x 13 = 156 launches: every counter slot is reused, by shapes of different grids
+    for rnd in range(13):
+        for i, (w, (host, (qd, kd, vd))) in enumerate(zip(SHAPES, data)):
+            out, lse = attn.attn_fwd(qd, kd, vd, causal=w.causal, sm_scale=w.sm_scale)
+            out2, lse2 = attn.attn_fwd(qd, kd, vd, causal=w.causal, sm_scale=w.sm_scale)
+            out3, lse3 = attn.attn_fwd(qd, kd, vd, causal=w.causal, sm_scale=w.sm_scale)
+            torch.cuda.synchronize()
+            for o, l in ((out, lse), (out2, lse2), (out3, lse3)):
+                assert torch.equal(o, first[i][0]), f"{w.name}: O differs in round {rnd}"
+                assert torch.equal(l, first[i][1]), f"{w.name}: LSE differs in round {rnd}"
+    assert attn.device_status(dev) == 0
+
+
+def test_concurrent_launches_on_two_streams(cuda_lib):
+    import exact_attention_forward_attn_gb300 as attn
+
+    dev = torch.device("cuda:0")
+    wa, wb = SHAPES[0], SHAPES[2]
+    (_, (qa, ka, va)), (_, (qb, kb, vb)) = _inputs(wa, dev), _inputs(wb, dev)
+    ref_a = attn.attn_fwd(qa, ka, va, causal=wa.causal, sm_scale=wa.sm_scale)
+    ref_b = attn.attn_fwd(qb, kb, vb, causal=wb.causal, sm_scale=wb.sm_scale)
+    torch.cuda.synchronize()
+    sa, sb = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    outs = []
+    for _ in range(20):
+        with torch.cuda.stream(sa):
+            oa = attn.attn_fwd(qa, ka, va, causal=wa.causal, sm_scale=wa.sm_scale)
+        with torch.cuda.stream(sb):
+            ob = attn.attn_fwd(qb, kb, vb, causal=wb.causal, sm_scale=wb.sm_scale)
+        outs.append((oa, ob))
+    torch.cuda.synchronize()
+    for oa, ob in outs:
+        assert torch.equal(oa[0], ref_a[0]) and torch.equal(oa[1], ref_a[1])
+        assert torch.equal(ob[0], ref_b[0]) and torch.equal(ob[1], ref_b[1])
+    assert attn.device_status(dev) == 0
+
+
+def test_split_launches_reuse_counters(cuda_lib):
+    """Split-KV launches claim (item, split) pairs through the same counters."""
+    import exact_attention_forward_attn_gb300 as attn
+
+    dev = torch.device("cuda:0")
+    w = wl.FEWHEADS
+    host, (qd, kd, vd) = _inputs(w, dev)
+    o_ref, l_ref = oracle.attn_ref(*host, w.causal, w.sm_scale)
+    base = {}
+    for n_splits in (2, 3, 4, 7) * 20:
+        out, lse = attn.attn_fwd_splitkv(qd, kd, vd, causal=w.causal, sm_scale=w.sm_scale,
+                                         num_splits=n_splits)
+        torch.cuda.synchronize()
+        if n_splits not in base:
+            _check(out, lse, o_ref, l_ref, f"{w.name} splits={n_splits}")
+            base[n_splits] = (out.clone(), lse.clone())
+        else:
+            assert torch.equal(out, base[n_splits][0]) and torch.equal(lse, base[n_splits][1])
+    assert attn.device_status(dev) == 0
