@@ -566,10 +566,9 @@ namespace {
 
 template <int D>
 int launch_bwd(const Problem& P, const CUtensorMap& mq, const CUtensorMap& mk,
-               const CUtensorMap& mv, const CUtensorMap& mdo, const CUtensorMap& mdq,
-               const CUtensorMap& mdk, const CUtensorMap& mdv, const BwdParams& bp,
-               const void* out, const void* dout, float* delta, unsigned int* status_word,
-               cudaStream_t s) {
+               const CUtensorMap& mv, const CUtensorMap& mdo, const CUtensorMap& mdk,
+               const CUtensorMap& mdv, const BwdParams& bp, const void* out, const void* dout,
+               float* delta, unsigned int* status_word, int num_sms, cudaStream_t s) {
     const long long rows = P.bh * P.N;
     attn_bwd_delta_kernel<<<static_cast<unsigned int>((rows + 7) / 8), 256, 0, s>>>(
         static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), delta,
@@ -580,8 +579,10 @@ int launch_bwd(const Problem& P, const CUtensorMap& mq, const CUtensorMap& mk,
                               DkdvSmem<D>::kAlloc, s>>>(mq, mk, mv, mdo, mdk, mdv, bp, status_word);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
-    attn_bwd_dq_kernel<D><<<static_cast<unsigned int>(P.n_tiles * P.bh), kBwdThreads,
-                            DqSmem<D>::kAlloc, s>>>(mq, mk, mv, mdo, mdq, bp, status_word);
+    // persistent: one CTA per SM (or per item, if fewer)
+    const int64_t dq_grid = std::min<int64_t>(bp.items, std::max(1, num_sms));
+    attn_bwd_dq_kernel<D><<<static_cast<unsigned int>(dq_grid), kBwdThreads, DqSmem<D>::kAlloc,
+                            s>>>(mq, mk, mv, mdo, bp, status_word);
     e = cudaGetLastError();
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
@@ -634,9 +635,8 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
     for (const void* ptr : {dout, static_cast<const void*>(dq), static_cast<const void*>(dk),
                             static_cast<const void*>(dv), static_cast<const void*>(workspace)})
         if (check_memory(ptr, dev) != ATTN_OK) return ATTN_ERR_MEMORY;
-    CUtensorMap mdo, mdq, mdk, mdv;
+    CUtensorMap mdo, mdk, mdv;
     if (!cached_tile_map(&mdo, dout, B, Hq, N, D, P.sq) ||
-        !cached_tile_map(&mdq, dq, B, Hq, N, D, P.sq) ||
         !cached_tile_map(&mdk, dk, B, Hkv, N, D, P.sk) ||
         !cached_tile_map(&mdv, dv, B, Hkv, N, D, P.sv))
         return cuda_fail(cudaErrorInvalidValue);
@@ -652,12 +652,17 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
     bp.sm_scale = sm_scale;
     bp.lse = lse;
     bp.delta = static_cast<const float*>(workspace);
+    if (P.n_tiles * P.bh > 0x7fffffffLL) return ATTN_ERR_SHAPE;
+    bp.items = static_cast<int>(P.n_tiles * P.bh);
+    bp.sched = prm.sched;
+    bp.dq = static_cast<__nv_bfloat16*>(dq);
+    bp.d_out = D;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     float* delta = static_cast<float*>(workspace);
-    return D <= 64 ? launch_bwd<64>(P, mq, mk, mv, mdo, mdq, mdk, mdv, bp, out, dout, delta,
-                                    ds->status_word, s)
-                   : launch_bwd<128>(P, mq, mk, mv, mdo, mdq, mdk, mdv, bp, out, dout, delta,
-                                     ds->status_word, s);
+    return D <= 64 ? launch_bwd<64>(P, mq, mk, mv, mdo, mdk, mdv, bp, out, dout, delta,
+                                    ds->status_word, ds->num_sms, s)
+                   : launch_bwd<128>(P, mq, mk, mv, mdo, mdk, mdv, bp, out, dout, delta,
+                                     ds->status_word, ds->num_sms, s);
 }
 
 // ------------------------------------------------------------------------------------------------

@@ -16,8 +16,9 @@
 //                           the causal mask) it forms S^T = K_j Q_i^T and dP^T = V_j dO_i^T,
 //                           P^T (bf16, in shared memory) and dS^T (bf16, in TMEM over dP^T),
 //                           and accumulates dV += P^T dO_i and dK += dS^T Q_i in TMEM.
-//   attn_bwd_dq_kernel      one CTA per (b, query head, 128-row tile i): S = Q_i K_j^T,
-//                           dP = dO_i V_j^T, dS (bf16 in TMEM over S), dQ += dS K_j.
+//   attn_bwd_dq_kernel      persistent; one work item per (b, query head, 128-row tile i):
+//                           S = Q_i K_j^T, dP = dO_i V_j^T, dS (bf16 in TMEM over S),
+//                           dQ += dS K_j.
 // Zero-filled rows past N contribute nothing: a padded query has dO = 0 and Delta = 0 (so its
 // ds and its dV term vanish), a padded key has K = V = 0 (so its dQ term vanishes) and its own
 // dK/dV rows are never stored.  Only the causal diagonal tile needs a mask.
@@ -41,6 +42,12 @@ struct BwdParams {
     float sm_scale;
     const float* lse;    // [B, Hq, N] natural-log LSE from the forward
     const float* delta;  // [B, Hq, N] dO . O
+    // dQ kernel (persistent): its work items, its claim counter (zero at launch), and dQ
+    // [B, Hq, N, d_out] bf16, contiguous
+    int items;
+    unsigned int* sched;
+    __nv_bfloat16* dq;
+    int d_out;
 };
 
 // Warps 0-7 elementwise: warp w serves TMEM lanes 32(w%4) .. 32(w%4)+31 (its quarter) and the
@@ -530,33 +537,46 @@ struct DqSmem {
     static constexpr int kK = 2 * kTileBytes;              // K ring
     static constexpr int kV = kK + kKSlots * kTileBytes;   // V ring
     static constexpr int kBars = kV + kVSlots * kTileBytes;
-    static constexpr int kBarRes = 0;
-    static constexpr int kBarKFull = 1;                      // [kKSlots]
+    static constexpr int kBarQ = 0;                          // Q_i landed (one arrive per panel)
+    static constexpr int kBarDo = 1;                         // dO_i landed
+    static constexpr int kBarQFree = 2;                      // the item's last S MMA read Q_i
+    static constexpr int kBarDoFree = 3;                     // the item's last dP MMA read dO_i
+    static constexpr int kBarKFull = 4;                      // [kKSlots]
     static constexpr int kBarKEmpty = kBarKFull + kKSlots;   // [kKSlots]
     static constexpr int kBarVFull = kBarKEmpty + kKSlots;   // [kVSlots]
     static constexpr int kBarVEmpty = kBarVFull + kVSlots;   // [kVSlots]
     static constexpr int kBarS = kBarVEmpty + kVSlots;       // [2]
     static constexpr int kBarDP = kBarS + 2;
     static constexpr int kBarDS = kBarDP + 1;
-    static constexpr int kBarDone = kBarDS + 1;
-    static constexpr int kNumBars = kBarDone + 1;
-    static constexpr int kTmemSlot = kBars + kNumBars * 8;
+    static constexpr int kBarDone = kBarDS + 1;              // the item's dQ is complete
+    static constexpr int kBarDqFree = kBarDone + 1;          // the epilogue has read dQ
+    static constexpr int kBarItemFull = kBarDqFree + 1;      // [2]
+    static constexpr int kBarItemEmpty = kBarItemFull + 2;   // [2]
+    static constexpr int kNumBars = kBarItemEmpty + 2;
+    static constexpr int kItems = kBars + kNumBars * 8;      // int[2]: the item ring
+    static constexpr int kTmemSlot = kItems + 8;
     static constexpr int kAbort = kTmemSlot + 8;
     static constexpr int kBytes = kAbort + 8;
     static constexpr int kAlloc = kBytes + 1024;
     static_assert(kAlloc <= 232448, "dQ shared memory exceeds the per-block limit");
+    // readers of an item ring slot besides the claiming lane: the other producer lanes, the two
+    // MMA warps and the eight elementwise warps (one arrival per warp)
+    static constexpr int kItemReaders = 2 * (D / 64) - 1 + 2 + 8;
 };
 
-// ------------------------------------------------------------------------------------------------
-// dQ
-// ------------------------------------------------------------------------------------------------
+// Persistent: min(items, SMs) CTAs; a work item is one (128-row query tile i, b, query head),
+// latest (heaviest under the causal mask) tiles first.  CTA c takes item c, then claims items
+// from the launch's counter (the forward's scheme, one of the same counters).  Across items every
+// mbarrier keeps counting phases: Q_i and dO_i reload as soon as the previous item's last S and
+// dP MMAs have read them, so the next item's loads and first MMAs overlap the current item's last
+// steps and its epilogue, and the first dQ MMA of an item waits until the epilogue has read the
+// previous item's dQ out of TMEM.
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q,
                        const __grid_constant__ CUtensorMap tmap_k,
                        const __grid_constant__ CUtensorMap tmap_v,
-                       const __grid_constant__ CUtensorMap tmap_do,
-                       const __grid_constant__ CUtensorMap tmap_dq, const BwdParams p,
+                       const __grid_constant__ CUtensorMap tmap_do, const BwdParams p,
                        unsigned int* status_word) {
     using L = DqSmem<D>;
     constexpr int kPanels = D / 64;
@@ -569,17 +589,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     auto bar = [=](int x) -> uint32_t { return sbase + L::kBars + 8u * x; };
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
+    volatile int* item_ring = reinterpret_cast<volatile int*>(smem + L::kItems);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    // work: query tile i (latest, i.e. heaviest under the causal mask, first), then (b, hq)
     const int bh_count = p.B * p.Hq;
-    const int i = p.n_tiles - 1 - static_cast<int>(blockIdx.x / bh_count);
-    const int bh = static_cast<int>(blockIdx.x % bh_count);
-    const int b = bh / p.Hq, hq = bh % p.Hq, hkv = hq / p.group;
-    const int n_it = p.causal ? i + 1 : p.n_tiles;  // key tiles 0 .. n_it-1
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(L::kBarRes), 2 * kPanels);  // one arrive (+ tx) per Q_i / dO_i panel
+        mbar_init(bar(L::kBarQ), kPanels);
+        mbar_init(bar(L::kBarDo), kPanels);
+        mbar_init(bar(L::kBarQFree), 1);
+        mbar_init(bar(L::kBarDoFree), 1);
         for (int s = 0; s < L::kKSlots; ++s) {
             mbar_init(bar(L::kBarKFull + s), kPanels);
             mbar_init(bar(L::kBarKEmpty + s), 1);
@@ -593,6 +611,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(bar(L::kBarDP), 1);
         mbar_init(bar(L::kBarDS), kBwdEwThreads);
         mbar_init(bar(L::kBarDone), 1);
+        mbar_init(bar(L::kBarDqFree), kBwdEwThreads);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar(L::kBarItemFull + s), 1);
+            mbar_init(bar(L::kBarItemEmpty + s), L::kItemReaders);
+        }
         *abort_flag = 0;
         fence_mbarrier_init();
         fence_proxy_async_smem();
@@ -605,185 +628,289 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    // S is double-buffered (S(it+1) is formed while the elementwise warps work on S(it)); dS is
-    // written over the S buffer it came from.
+    // S is double-buffered (S(g+1) is formed while the elementwise warps work on S(g), g counting
+    // the CTA's steps over all its items); dS is written over the S buffer it came from.
     const uint32_t t_s0 = tmem, t_dp = tmem + 128, t_dq = tmem + 256, t_s1 = tmem + 384;
+    // item -> query tile and (b, hq)
+    auto tile_of = [&](int item) { return p.n_tiles - 1 - item / bh_count; };
+    auto steps_of = [&](int i) { return p.causal ? i + 1 : p.n_tiles; };  // key tiles 0 .. n-1
+
+    // Item ring reader (all roles but the claiming lane); warps arrive once.
+    auto read_item = [&](int k, bool whole_warp) -> int {
+        const int slot = k & 1;
+        const uint32_t ph = static_cast<uint32_t>(k >> 1) & 1u;
+        bool ok;
+        if (whole_warp)
+            ok = mbar_wait_warp<true>(bar(L::kBarItemFull + slot), ph, abort_flag, status_word);
+        else
+            ok = mbar_wait_bounded<true>(bar(L::kBarItemFull + slot), ph, abort_flag, status_word);
+        if (!ok) return -1;
+        const int item = item_ring[slot];
+        if (whole_warp) {
+            __syncwarp();
+            mbar_arrive_warp(bar(L::kBarItemEmpty + slot));
+        } else {
+            mbar_arrive(bar(L::kBarItemEmpty + slot));
+        }
+        return item;
+    };
 
     if (warp == kBwdLoadWarp) {
         // one lane per panel stream (one thread's bulk copies run one after another): lanes
         // 0..kPanels-1 load a Q_i panel, then that panel of every K_j; lanes kPanels..2*kPanels-1
-        // a dO_i panel, then that panel of every V_j
+        // a dO_i panel, then that panel of every V_j.  Lane 0 also claims the items.
         if (lane < 2 * kPanels) {
             const bool kside = lane < kPanels;
             const int h = lane % kPanels;
-            mbar_arrive_expect_tx(bar(L::kBarRes), L::kPanelBytes);
-            if (kside)
-                tma_load_4d(sbase + L::kRes0 + h * L::kPanelBytes, &tmap_q, bar(L::kBarRes),
-                            h * 64, i * 128, hq, b);
-            else
-                tma_load_4d(sbase + L::kRes1 + h * L::kPanelBytes, &tmap_do, bar(L::kBarRes),
-                            h * 64, i * 128, hq, b);
             const int slots = kside ? L::kKSlots : L::kVSlots;
             const int full0 = kside ? L::kBarKFull : L::kBarVFull;
             const int empty0 = kside ? L::kBarKEmpty : L::kBarVEmpty;
-            const uint32_t ring = sbase + (kside ? L::kK : L::kV);
+            const uint32_t ring_base = sbase + (kside ? L::kK : L::kV);
             const CUtensorMap* map = kside ? &tmap_k : &tmap_v;
-            for (int it = 0; it < n_it; ++it) {
-                const int s = it % slots;
-                if (!mbar_wait_bounded<true>(bar(empty0 + s), ((it / slots) & 1) ^ 1u, abort_flag,
-                                             status_word))
+            bool claims_done = false;
+            auto claim = [&]() -> int {
+                const unsigned int c = atomicAdd(p.sched, 1u);
+                const unsigned int it = c + gridDim.x;
+                if (it < static_cast<unsigned int>(p.items)) return static_cast<int>(it);
+                claims_done = true;
+                if (c == static_cast<unsigned int>(p.items) - 1u) atomicExch(p.sched, 0u);
+                return -1;
+            };
+            int g = 0;  // K/V stream position (steps of the earlier items)
+            for (int k = 0;; ++k) {
+                int item;
+                if (lane == 0) {
+                    const int slot = k & 1;
+                    if (!mbar_wait_bounded<true>(bar(L::kBarItemEmpty + slot),
+                                                 (static_cast<uint32_t>(k >> 1) & 1u) ^ 1u,
+                                                 abort_flag, status_word))
+                        break;
+                    item = k == 0 ? static_cast<int>(blockIdx.x) : claim();
+                    item_ring[slot] = item;
+                    mbar_arrive(bar(L::kBarItemFull + slot));
+                } else {
+                    item = read_item(k, false);
+                }
+                if (item < 0) break;
+                const int i = tile_of(item), bh = item % bh_count;
+                const int b = bh / p.Hq, hq = bh % p.Hq, hkv = hq / p.group;
+                const int n_it = steps_of(i);
+                // the resident tile, once the previous item's last MMA has read its buffer
+                if (k > 0 && !mbar_wait_bounded<true>(bar(kside ? L::kBarQFree : L::kBarDoFree),
+                                                      (k - 1) & 1, abort_flag, status_word))
                     break;
-                mbar_arrive_expect_tx(bar(full0 + s), L::kPanelBytes);
-                tma_load_4d(ring + s * L::kTileBytes + h * L::kPanelBytes, map, bar(full0 + s),
-                            h * 64, it * 128, hkv, b);
+                mbar_arrive_expect_tx(bar(kside ? L::kBarQ : L::kBarDo), L::kPanelBytes);
+                tma_load_4d(sbase + (kside ? L::kRes0 : L::kRes1) + h * L::kPanelBytes,
+                            kside ? &tmap_q : &tmap_do, bar(kside ? L::kBarQ : L::kBarDo), h * 64,
+                            i * 128, hq, b);
+                bool ok = true;
+                for (int it = 0; it < n_it; ++it, ++g) {
+                    const int s = g % slots;
+                    ok = mbar_wait_bounded<true>(bar(empty0 + s), ((g / slots) & 1) ^ 1u,
+                                                 abort_flag, status_word);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(bar(full0 + s), L::kPanelBytes);
+                    tma_load_4d(ring_base + s * L::kTileBytes + h * L::kPanelBytes, map,
+                                bar(full0 + s), h * 64, it * 128, hkv, b);
+                }
+                if (!ok) break;
             }
+            // after an abort, still make this CTA's claims up to the one past the end
+            if (lane == 0)
+                while (!claims_done) (void)claim();
         }
         __syncwarp();
     } else if (warp == kBwdMmaWarp || warp == kBwdMmaWarpB) {
-        // A: S(it+1) = Q_i K_(it+1)^T ahead, then dQ += dS(it) K_it once dS(it) is ready;
-        // B: dP(it) = dO_i V_it^T, each after the elementwise warps have read the previous one.
+        // A: S(g+1) = Q_i K_(g+1)^T ahead, then dQ += dS(g) K_g once dS(g) is ready;
+        // B: dP(g) = dO_i V_g^T, each after the elementwise warps have read the previous one.
         const bool chain_a = warp == kBwdMmaWarp;
-        bool ok = mbar_wait_warp<true>(bar(L::kBarRes), 0, abort_flag, status_word);
         const uint32_t qa = sbase + L::kRes0, da = sbase + L::kRes1;
-        auto stage_k = [&](int it) { return sbase + L::kK + (it % L::kKSlots) * L::kTileBytes; };
-        auto stage_v = [&](int it) { return sbase + L::kV + (it % L::kVSlots) * L::kTileBytes; };
-        auto wait_k = [&](int it) {
-            const bool w = mbar_wait_warp<true>(bar(L::kBarKFull + it % L::kKSlots),
-                                                (it / L::kKSlots) & 1, abort_flag, status_word);
+        auto stage_k = [&](int g) { return sbase + L::kK + (g % L::kKSlots) * L::kTileBytes; };
+        auto stage_v = [&](int g) { return sbase + L::kV + (g % L::kVSlots) * L::kTileBytes; };
+        auto wait_k = [&](int g) {
+            const bool w = mbar_wait_warp<true>(bar(L::kBarKFull + g % L::kKSlots),
+                                                (g / L::kKSlots) & 1, abort_flag, status_word);
             tc_fence_after();
             return w;
         };
-        auto wait_v = [&](int it) {
-            const bool w = mbar_wait_warp<true>(bar(L::kBarVFull + it % L::kVSlots),
-                                                (it / L::kVSlots) & 1, abort_flag, status_word);
+        auto wait_v = [&](int g) {
+            const bool w = mbar_wait_warp<true>(bar(L::kBarVFull + g % L::kVSlots),
+                                                (g / L::kVSlots) & 1, abort_flag, status_word);
             tc_fence_after();
             return w;
         };
-        auto s_mma = [&](int it) {  // S(it) into buffer it&1
-            const uint32_t ka = stage_k(it);
+        auto s_mma = [&](int g) {  // S(g) into buffer g&1
+            const uint32_t ka = stage_k(g);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t off = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
-                mma_bf16_ss_warp((it & 1) ? t_s1 : t_s0, smem_desc_sw128(qa + off, 16, 1024),
+                mma_bf16_ss_warp((g & 1) ? t_s1 : t_s0, smem_desc_sw128(qa + off, 16, 1024),
                                  smem_desc_sw128(ka + off, 16, 1024), kIdescS, kk > 0);
             }
-            mma_commit_warp(bar(L::kBarS + (it & 1)));
+            mma_commit_warp(bar(L::kBarS + (g & 1)));
         };
-        if (chain_a) {
-            if (ok && n_it > 0) ok = wait_k(0);
-            if (ok && n_it > 0) s_mma(0);
-            for (int it = 0; ok && it < n_it; ++it) {
-                if (it + 1 < n_it) {
-                    ok = wait_k(it + 1);
-                    if (!ok) break;
-                    s_mma(it + 1);
+        bool ok = true;
+        int g0 = 0;  // steps of the earlier items
+        for (int k = 0; ok; ++k) {
+            const int item = read_item(k, true);
+            if (item < 0) break;
+            const int n_it = steps_of(tile_of(item));
+            if (chain_a) {
+                ok = mbar_wait_warp<true>(bar(L::kBarQ), k & 1, abort_flag, status_word);
+                if (ok) ok = wait_k(g0);
+                if (ok) {
+                    s_mma(g0);
+                    if (n_it == 1) mma_commit_warp(bar(L::kBarQFree));
                 }
-                ok = mbar_wait_warp(bar(L::kBarDS), it & 1, abort_flag, status_word);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t ka = stage_k(it), ts = (it & 1) ? t_s1 : t_s0;
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // dQ += dS K_j  (K = 128 keys)
-                    mma_bf16_ts_warp(t_dq, ts + packed_col(kk),
-                                     smem_desc_sw128(ka + kk * 2048, L::kPanelBytes, 1024),
-                                     kIdescAcc, (it > 0 || kk > 0) ? 1u : 0u);
-                mma_commit_warp(bar(L::kBarKEmpty + it % L::kKSlots));
-            }
-            if (ok) mma_commit_warp(bar(L::kBarDone));
-        } else {
-            for (int it = 0; ok && it < n_it; ++it) {
-                ok = wait_v(it);
-                if (!ok) break;
-                if (it > 0) {  // dP(it) overwrites dP(it-1): the elementwise warps must have read it
-                    ok = mbar_wait_warp<true>(bar(L::kBarDS), (it - 1) & 1, abort_flag, status_word);
+                for (int it = 0; ok && it < n_it; ++it) {
+                    const int g = g0 + it;
+                    if (it + 1 < n_it) {
+                        ok = wait_k(g + 1);
+                        if (!ok) break;
+                        s_mma(g + 1);
+                        if (it + 2 == n_it) mma_commit_warp(bar(L::kBarQFree));
+                    }
+                    ok = mbar_wait_warp(bar(L::kBarDS), g & 1, abort_flag, status_word);
+                    // the first dQ MMA overwrites the accumulator: the previous item's epilogue
+                    // must have read it
+                    if (ok && it == 0 && k > 0)
+                        ok = mbar_wait_warp(bar(L::kBarDqFree), (k - 1) & 1, abort_flag,
+                                            status_word);
                     if (!ok) break;
                     tc_fence_after();
-                }
-                const uint32_t va = stage_v(it);
+                    const uint32_t ka = stage_k(g), ts = (g & 1) ? t_s1 : t_s0;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {  // dP = dO_i V_j^T
-                    const uint32_t off = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
-                    mma_bf16_ss_warp(t_dp, smem_desc_sw128(da + off, 16, 1024),
-                                     smem_desc_sw128(va + off, 16, 1024), kIdescS, kk > 0);
+                    for (int kk = 0; kk < 8; ++kk)  // dQ += dS K_j  (K = 128 keys)
+                        mma_bf16_ts_warp(t_dq, ts + packed_col(kk),
+                                         smem_desc_sw128(ka + kk * 2048, L::kPanelBytes, 1024),
+                                         kIdescAcc, (it > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit_warp(bar(L::kBarKEmpty + g % L::kKSlots));
                 }
-                mma_commit_warp(bar(L::kBarDP));
-                mma_commit_warp(bar(L::kBarVEmpty + it % L::kVSlots));
+                if (ok) mma_commit_warp(bar(L::kBarDone));
+            } else {
+                ok = mbar_wait_warp<true>(bar(L::kBarDo), k & 1, abort_flag, status_word);
+                for (int it = 0; ok && it < n_it; ++it) {
+                    const int g = g0 + it;
+                    ok = wait_v(g);
+                    if (!ok) break;
+                    if (g > 0) {  // dP(g) overwrites dP(g-1): the elementwise warps must have read it
+                        ok = mbar_wait_warp<true>(bar(L::kBarDS), (g - 1) & 1, abort_flag,
+                                                  status_word);
+                        if (!ok) break;
+                        tc_fence_after();
+                    }
+                    const uint32_t va = stage_v(g);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {  // dP = dO_i V_j^T
+                        const uint32_t off = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
+                        mma_bf16_ss_warp(t_dp, smem_desc_sw128(da + off, 16, 1024),
+                                         smem_desc_sw128(va + off, 16, 1024), kIdescS, kk > 0);
+                    }
+                    mma_commit_warp(bar(L::kBarDP));
+                    mma_commit_warp(bar(L::kBarVEmpty + g % L::kVSlots));
+                    if (it + 1 == n_it) mma_commit_warp(bar(L::kBarDoFree));
+                }
             }
+            g0 += n_it;
         }
         __syncwarp();
     } else {
         // elementwise warps 0-7: query row `row` of tile i, keys c0 .. c0+63 of the key tile
         const int quarter = warp & 3, half = warp >> 2;
         const int row = quarter * 32 + lane;
-        const int row_g = i * 128 + row;
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
         const int c0 = half * 64;
         const float c = p.scale_log2;
-        const size_t rix = static_cast<size_t>(bh) * p.N + row_g;
-        const float lse2 = row_g < p.N ? p.lse[rix] * kLog2e : 0.f;
-        const float dlt = row_g < p.N ? p.delta[rix] : 0.f;
         bool ok = true;
-        for (int it = 0; it < n_it; ++it) {
-            const uint32_t ts = (it & 1) ? t_s1 : t_s0;
-            ok = mbar_wait_warp(bar(L::kBarS + (it & 1)), (it >> 1) & 1, abort_flag, status_word);
-            if (!ok) break;
-            tc_fence_after();
-            float pr[64];
-            {
-                uint32_t r[64];
-                tmem_ld32(lane_base + ts + c0, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-                tmem_ld32(lane_base + ts + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-                tmem_wait_ld();
+        int g = 0;  // steps of this CTA so far
+        for (int k = 0; ok; ++k) {
+            const int item = read_item(k, true);
+            if (item < 0) break;
+            const int i = tile_of(item), bh = item % bh_count;
+            const int n_it = steps_of(i);
+            const int row_g = i * 128 + row;
+            const size_t rix = static_cast<size_t>(bh) * p.N + row_g;
+            const float lse2 = row_g < p.N ? p.lse[rix] * kLog2e : 0.f;
+            const float dlt = row_g < p.N ? p.delta[rix] : 0.f;
+            for (int it = 0; it < n_it; ++it, ++g) {
+                const uint32_t ts = (g & 1) ? t_s1 : t_s0;
+                ok = mbar_wait_warp(bar(L::kBarS + (g & 1)), (g >> 1) & 1, abort_flag,
+                                    status_word);
+                if (!ok) break;
+                tc_fence_after();
+                float pr[64];
+                {
+                    uint32_t r[64];
+                    tmem_ld32(lane_base + ts + c0, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                    tmem_ld32(lane_base + ts + c0 + 32,
+                              *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+                    tmem_wait_ld();
 #pragma unroll
-                for (int k = 0; k < 64; k += 2) {
-                    float x0, x1;
-                    ffma2(x0, x1, __uint_as_float(r[k]), __uint_as_float(r[k + 1]), c, c, -lse2,
-                          -lse2);
-                    pr[k] = ex2_approx(x0);
-                    pr[k + 1] = ex2_approx(x1);
+                    for (int x = 0; x < 64; x += 2) {
+                        float x0, x1;
+                        ffma2(x0, x1, __uint_as_float(r[x]), __uint_as_float(r[x + 1]), c, c,
+                              -lse2, -lse2);
+                        pr[x] = ex2_approx(x0);
+                        pr[x + 1] = ex2_approx(x1);
+                    }
                 }
-            }
-            if (p.causal && it == i) {  // diagonal tile: key k visible to query `row` iff k <= row
+                if (p.causal && it == i) {  // diagonal tile: key x visible to query `row` iff x <= row
 #pragma unroll
-                for (int k = 0; k < 64; ++k) pr[k] = c0 + k > row ? 0.f : pr[k];
+                    for (int x = 0; x < 64; ++x) pr[x] = c0 + x > row ? 0.f : pr[x];
+                }
+                ok = mbar_wait_warp(bar(L::kBarDP), g & 1, abort_flag, status_word);
+                if (!ok) break;
+                tc_fence_after();
+                // dS in 32-column chunks; the packed dS goes over this warp's S columns (all read)
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    uint32_t r[32];
+                    tmem_ld32(lane_base + t_dp + c0 + cc * 32, r);
+                    tmem_wait_ld();
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int x = 0; x < 16; ++x) {
+                        const int kx = cc * 32 + 2 * x;
+                        float t0, t1, d0, d1;
+                        fadd2(t0, t1, __uint_as_float(r[2 * x]), __uint_as_float(r[2 * x + 1]),
+                              -dlt, -dlt);
+                        ffma2(d0, d1, pr[kx], pr[kx + 1], t0, t1, 0.f, 0.f);
+                        pk[x] = pack_bf16x2(d0, d1);
+                    }
+                    tmem_st16(lane_base + ts + c0 + cc * 16, pk);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(bar(L::kBarDS));
             }
-            ok = mbar_wait_warp(bar(L::kBarDP), it & 1, abort_flag, status_word);
+            if (!ok) break;
+            // ---- epilogue: dQ = sm_scale * acc -> bf16, this warp's columns of its row,
+            // straight from registers to global memory (16-byte stores)
+            ok = mbar_wait_warp(bar(L::kBarDone), k & 1, abort_flag, status_word);
             if (!ok) break;
             tc_fence_after();
-            // dS in 32-column chunks; the packed dS goes over this warp's S columns (all read)
+            constexpr int kCols = D / 2;  // columns per warp: half of the row
+            __nv_bfloat16* dst = p.dq + rix * p.d_out + half * kCols;
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
+            for (int cc = 0; cc < kCols / 32; ++cc) {
                 uint32_t r[32];
-                tmem_ld32(lane_base + t_dp + c0 + cc * 32, r);
+                tmem_ld32(lane_base + t_dq + half * kCols + cc * 32, r);
                 tmem_wait_ld();
-                uint32_t pk[16];
+                if (row_g < p.N) {
 #pragma unroll
-                for (int x = 0; x < 16; ++x) {
-                    const int k = cc * 32 + 2 * x;
-                    float t0, t1, d0, d1;
-                    fadd2(t0, t1, __uint_as_float(r[2 * x]), __uint_as_float(r[2 * x + 1]), -dlt,
-                          -dlt);
-                    ffma2(d0, d1, pr[k], pr[k + 1], t0, t1, 0.f, 0.f);
-                    pk[x] = pack_bf16x2(d0, d1);
+                    for (int c8 = 0; c8 < 4; ++c8) {
+                        if (half * kCols + cc * 32 + c8 * 8 >= p.d_out) break;
+                        uint32_t w[4];
+#pragma unroll
+                        for (int x = 0; x < 4; ++x)
+                            w[x] = pack_bf16x2(__uint_as_float(r[c8 * 8 + 2 * x]) * p.sm_scale,
+                                               __uint_as_float(r[c8 * 8 + 2 * x + 1]) * p.sm_scale);
+                        st_global_v4u(dst + cc * 32 + c8 * 8, w[0], w[1], w[2], w[3]);
+                    }
                 }
-                tmem_st16(lane_base + ts + c0 + cc * 16, pk);
             }
-            tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar(L::kBarDS));
-        }
-        if (ok) ok = mbar_wait_warp(bar(L::kBarDone), 0, abort_flag, status_word);
-        if (ok) {
-            tc_fence_after();
-            stage_rows_bf16<D>(sbase + L::kRes0, lane_base + t_dq, row, p.sm_scale,
-                               half * (D / 64), (half + 1) * (D / 64));
-        }
-        fence_proxy_async_smem();
-        named_barrier_sync(1, kBwdEwThreads);
-        if (ok && warp == 0 && lane == 0) {
-            for (int h = 0; h < kPanels; ++h)
-                tma_store_4d(&tmap_dq, sbase + L::kRes0 + h * L::kPanelBytes, h * 64, i * 128, hq, b);
-            tma_store_commit_and_wait();
+            mbar_arrive(bar(L::kBarDqFree));  // the next item's first dQ MMA may overwrite it
         }
         __syncwarp();
     }
