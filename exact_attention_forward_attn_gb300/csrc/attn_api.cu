@@ -358,14 +358,13 @@ int prepare(const Problem& P, DeviceState** ds, CUtensorMap* mq, CUtensorMap* mk
 // until all `items` are taken.
 template <int D, bool kSplit>
 int launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-               const CUtensorMap& mo, const AttnParams& p, unsigned int* status_word,
-               int64_t items, int num_sms, cudaStream_t stream) {
+               const AttnParams& p, unsigned int* status_word, int64_t items, int num_sms,
+               cudaStream_t stream) {
     AttnParams prm = p;
     prm.items = static_cast<int>(items);
     const int64_t grid = std::min<int64_t>(items, std::max(1, num_sms));
     attn_fwd_kernel<D, kSplit><<<static_cast<unsigned int>(grid), kThreads,
-                                 SmemLayout<D>::kAlloc, stream>>>(mq, mk, mv, mo, prm,
-                                                                  status_word);
+                                 SmemLayout<D>::kAlloc, stream>>>(mq, mk, mv, prm, status_word);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
@@ -375,9 +374,9 @@ int launch_single(int D, const CUtensorMap& mq, const CUtensorMap& mk, const CUt
                   const CUtensorMap& mo, const AttnParams& p, unsigned int* status_word,
                   int64_t grid, int num_sms, cudaStream_t stream) {
     if (D <= 64)
-        return launch_fwd<64, false>(mq, mk, mv, mo, p, status_word, grid, num_sms, stream);
+        return launch_fwd<64, false>(mq, mk, mv, p, status_word, grid, num_sms, stream);
     if (D <= 128)
-        return launch_fwd<128, false>(mq, mk, mv, mo, p, status_word, grid, num_sms, stream);
+        return launch_fwd<128, false>(mq, mk, mv, p, status_word, grid, num_sms, stream);
     attn_fwd_d256_kernel<<<static_cast<unsigned int>(grid), kW256Threads, Fwd256Smem::kAlloc,
                            stream>>>(mq, mk, mv, mo, p, status_word);
     const cudaError_t e = cudaGetLastError();
@@ -482,9 +481,9 @@ extern "C" int attn_fwd_test_stall(const void* q, const void* k, const void* v, 
     if (st != ATTN_OK) return st;
     prm.stall_item = stall_item;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return D <= 64 ? launch_fwd<64, false>(mq, mk, mv, mo, prm, ds->status_word, P.items,
+    return D <= 64 ? launch_fwd<64, false>(mq, mk, mv, prm, ds->status_word, P.items,
                                            ds->num_sms, s)
-                   : launch_fwd<128, false>(mq, mk, mv, mo, prm, ds->status_word, P.items,
+                   : launch_fwd<128, false>(mq, mk, mv, prm, ds->status_word, P.items,
                                             ds->num_sms, s);
 }
 
@@ -551,9 +550,8 @@ extern "C" int attn_fwd_splitkv(const void* q, const void* k, const void* v, voi
     prm.ws_lse = prm.ws_o + static_cast<int64_t>(n_splits) * P.bh * N * padded_dim(D);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int64_t items = P.items * n_splits;
-    st = D <= 64 ? launch_fwd<64, true>(mq, mk, mv, mo, prm, ds->status_word, items, ds->num_sms, s)
-                 : launch_fwd<128, true>(mq, mk, mv, mo, prm, ds->status_word, items, ds->num_sms,
-                                         s);
+    st = D <= 64 ? launch_fwd<64, true>(mq, mk, mv, prm, ds->status_word, items, ds->num_sms, s)
+                 : launch_fwd<128, true>(mq, mk, mv, prm, ds->status_word, items, ds->num_sms, s);
     if (st != ATTN_OK) return st;
     auto* o = static_cast<__nv_bfloat16*>(out);
     return D <= 64 ? launch_merge<64>(prm, o, D, s) : launch_merge<128>(prm, o, D, s);

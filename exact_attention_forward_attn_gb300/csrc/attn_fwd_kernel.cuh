@@ -187,8 +187,7 @@ template <int D, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
                     const __grid_constant__ CUtensorMap tmap_k,
-                    const __grid_constant__ CUtensorMap tmap_v,
-                    const __grid_constant__ CUtensorMap tmap_o, const AttnParams p,
+                    const __grid_constant__ CUtensorMap tmap_v, const AttnParams p,
                     unsigned int* status_word) {
     using L = SmemLayout<D>;
     static_assert(D == 64 || D == 128, "head dim");
