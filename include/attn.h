@@ -76,6 +76,14 @@ typedef enum {
  *   stream   a cudaStream_t of the current device, passed as void* (NULL = legacy default stream)
  *
  * Returns ATTN_OK once the kernel is enqueued on `stream`, else a negative attn_status_t.
+ *
+ * Scheduling: up to D = 128 the kernel is persistent (one CTA per SM); its CTAs claim work items
+ * from a device counter that the library hands to each launch from a pool of 64 (round robin,
+ * per device, shared with attn_fwd_strided, the split-KV entry points and the backward's dQ
+ * kernel).  Each launch returns its counter to zero, so launches in one stream, or on different
+ * streams, may follow each other freely; at most 64 such launches may be executing at the same
+ * time on one device (a CUDA graph replays its launches' counters, so a graph must not run
+ * concurrently with another replay of itself).
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
              int Hkv, int N, int D, int causal, float sm_scale, void* stream);
