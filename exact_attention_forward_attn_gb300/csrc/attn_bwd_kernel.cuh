@@ -58,7 +58,6 @@ constexpr int kBwdLoadWarp = 9;
 constexpr int kBwdMmaWarpB = 10;
 constexpr int kBwdThreads = 352;
 constexpr int kBwdEwThreads = 256;
-constexpr int kBwdStages = 2;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Delta_i = dO_i . O_i (fp32 sum of bf16 products); one warp per row, D <= 128 columns.
@@ -77,33 +76,6 @@ __global__ void __launch_bounds__(256)
     for (int off = 16; off >= 1; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (lane == 0) delta[row] = acc;
 }
-
-template <int D>
-struct BwdSmem {
-    static constexpr int kPanelBytes = 128 * 64 * 2;
-    static constexpr int kTileBytes = 128 * D * 2;
-    // resident pair (dkdv: K_j, V_j; dq: Q_i, dO_i), then kBwdStages streamed pairs
-    static constexpr int kRes0 = 0;
-    static constexpr int kRes1 = kTileBytes;
-    static constexpr int kStage = 2 * kTileBytes;  // stage s: [kStage + 2*s*tile, +2 tiles)
-    static constexpr int kVec = kStage + 2 * kBwdStages * kTileBytes;  // lse2/delta [stage][2][128]
-    static constexpr int kBars = kVec + kBwdStages * 2 * 128 * 4;
-    // barriers: res_full, stage_full[S], stage_empty[S], s_full[2], dp_full, p_ready, ds_ready,
-    // done (dkdv uses s_full[0] only)
-    static constexpr int kBarRes = 0;
-    static constexpr int kBarFull = 1;
-    static constexpr int kBarEmpty = kBarFull + kBwdStages;
-    static constexpr int kBarS = kBarEmpty + kBwdStages;
-    static constexpr int kBarDP = kBarS + 2;
-    static constexpr int kBarP = kBarDP + 1;
-    static constexpr int kBarDS = kBarP + 1;
-    static constexpr int kBarDone = kBarDS + 1;
-    static constexpr int kNumBars = kBarDone + 1;
-    static constexpr int kTmemSlot = kBars + kNumBars * 8;
-    static constexpr int kAbort = kTmemSlot + 8;
-    static constexpr int kBytes = kAbort + 8;
-    static constexpr int kAlloc = kBytes + 1024;
-};
 
 // dK/dV layout: K_j, V_j resident; a 3-slot ring of Q_i (read by S^T(i), formed a step ahead,
 // and by dK(i), issued last, so the third slot lets Q_(i+2) load while dK(i) is pending); one dO_i

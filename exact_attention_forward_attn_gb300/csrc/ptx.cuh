@@ -151,11 +151,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
-// Raise the current phase's expected transaction bytes without arriving.
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
 
 // Non-suspending poll of phase `parity` (test_wait: measured to wake the critical-path warps a
 // little sooner than the suspending try_wait).
@@ -260,31 +255,12 @@ __device__ __forceinline__ void tma_store_4d(const void* tmap, uint32_t src, int
         : "memory");
 }
 
-__device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int c0, int c1,
-                                             int c2) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-            reinterpret_cast<uint64_t>(tmap)),
-        "r"(src), "r"(c0), "r"(c1), "r"(c2)
-        : "memory");
-}
 
 __device__ __forceinline__ void tma_store_commit_and_wait() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
-// Commit the stores issued so far and wait until they have read their shared-memory source (the
-// source may then be rewritten; the global writes may still be in flight).
-__device__ __forceinline__ void tma_store_commit_and_wait_read() {
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-
-// Wait until every committed store of this thread has completed.
-__device__ __forceinline__ void tma_store_wait_all() {
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
 
 // ------------------------------------------------------------------------------------------------
 // tcgen05: tensor memory and the 5th-generation tensor-core MMA (cta_group::1)
@@ -377,12 +353,6 @@ __device__ __forceinline__ void mbar_arrive_warp(uint32_t bar) {
         : "memory");
 }
 
-// Arrive once on `bar` when every tcgen05 operation issued so far by this thread has completed.
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-        : "memory");
-}
 
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
