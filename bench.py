@@ -39,10 +39,17 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 
 
 def kernel_hash() -> str:
+    """Hash of the forward's sources with comments and whitespace removed, so that the stored
+    DRAM traffic stays attached to the code it was measured on, not to its comments."""
+    import re
+
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)  # block comments
+        src = re.sub(r"//[^\n]*", " ", src)                 # line comments
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

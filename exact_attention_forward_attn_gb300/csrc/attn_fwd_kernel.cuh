@@ -11,7 +11,7 @@
 //   recurrence (exp2 domain: scores are pre-multiplied by sm_scale*log2(e)); after the last tile
 //   O = acc / l and LSE = ln2 * (m + log2 l).  The N x N score matrix never leaves the SM.
 //
-// GB300 mapping (persistent: one CTA per SM, 352 threads, each CTA works through pairs of
+// GB300 mapping (persistent: one CTA per SM, 384 threads, each CTA works through pairs of
 // 128-row Q tiles that it claims from a per-launch counter in global memory):
 //   warp 10     TMA producer: lane 0 claims the next work item and publishes it through a 2-slot
 //               item ring in shared memory; one lane per 64-column panel stream loads K_j, V_j
@@ -23,9 +23,10 @@
 //               tcgen05.commit signals completion.  Warp 11 has no role.
 //   warps 0-3   softmax for Q tile 0, warps 4-7 for Q tile 1: one thread per query row reads its
 //               S row from TMEM, masks (diagonal causal tile / ragged last key tile only), updates
-//               m and l, rescales its O row in TMEM when m moved, writes P (bf16) over S in TMEM;
-//               after the last tile it normalises O, stages it in smem one 64-column panel at a
-//               time and TMA-stores it, and writes LSE.
+//               m and l, rescales its O row in TMEM when m moved, writes P (bf16): keys 0-63 over
+//               S in TMEM, keys 64-127 into a swizzled smem panel; after the last tile it
+//               normalises O, stages it through that panel one 64-column panel at a time and
+//               writes it with coalesced 16-byte stores, and writes LSE.
 //   The two Q tiles ping-pong: while one softmax group works, the tensor core runs the other
 //   tile's MMAs.  Across items every barrier keeps counting phases, so item k+1's first S MMAs
 //   run while item k's softmax and epilogue finish.
