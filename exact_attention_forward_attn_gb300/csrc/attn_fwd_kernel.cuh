@@ -113,8 +113,8 @@ struct SmemLayout {
     static constexpr int kBarPReady = kBarSFull + 2;          // [2 tiles][2 key halves]
     static constexpr int kBarPVDone = kBarPReady + 4;         // [2]: a step's P.V completed
     static constexpr int kBarODone = kBarPVDone + 2;          // [2]
-    static constexpr int kBarTurn = kBarODone + 2;            // [2]: softmax group t may run exp2
-    static constexpr int kBarItemFull = kBarTurn + 2;         // [2]: item ring slot written
+    static constexpr int kBarTurn = kBarODone + 2;            // [2 groups][2]: exp2 turn tokens
+    static constexpr int kBarItemFull = kBarTurn + 4;         // [2]: item ring slot written
     static constexpr int kBarItemEmpty = kBarItemFull + 2;    // [2]: item ring slot read by all
     static constexpr int kNumBars = kBarItemEmpty + 2;
     static constexpr int kItems = kBars + kNumBars * 8;       // int[2]: the item ring
@@ -218,7 +218,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(L::kBarPReady + 2 * t + 1), 128);
             mbar_init(bar(L::kBarPVDone + t), 1);
             mbar_init(bar(L::kBarODone + t), 1);
-            mbar_init(bar(L::kBarTurn + t), 128);
+            mbar_init(bar(L::kBarTurn + 2 * t + 0), 128);
+            mbar_init(bar(L::kBarTurn + 2 * t + 1), 128);
             mbar_init(bar(L::kBarItemFull + t), 1);
             mbar_init(bar(L::kBarItemEmpty + t), L::kItemReaders);
         }
@@ -473,18 +474,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t o_addr = tmem + lane_base + tmem_o_col(t);
         const uint32_t p1 = sbase + L::kP1 + t * L::kP1Bytes;  // P keys 64..127, O staging
         const float c = p.scale_log2;
-        // Barrier phases, one bit each: S-full / P.V-done step parity, turn parity, O-done
-        // parity; and (tile 0) the hand-back of the previous ping-pong item still to be taken.
-        constexpr uint32_t kPhStep = 1u, kPhTurn = 2u, kPhODone = 4u, kOwed = 8u;
+        // Barrier phases, one bit each: S-full / P.V-done step parity, O-done parity.
+        constexpr uint32_t kPhStep = 1u, kPhODone = 4u;
         uint32_t ph = 0;
+        uint32_t tok = 0;  // this group's exp2 phases that take part in the ping-pong so far
         bool ok = true;
         // The four warps of a group leave the item loop together (they share named barriers):
         // they agree on every item they read and on the outcome of every item's waits.
         for (int k = 0;; ++k) {
             const int item = read_item(k, true);
             if (!named_barrier_and(1 + t, 128, item >= 0)) break;
-            int n, lim, tw_until, ta_until;
-            bool mask_last, tw_first;
+            int n, lim, tok_until;
+            bool mask_last;
             {
                 const FwdWork w = decode_work<kSplit>(p, item);
                 if (!(t == 0 ? w.part0 : w.part1)) continue;
@@ -497,25 +498,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mask_last = p.causal ? last == q_tile
                                      : (last == p.n_tiles - 1 && (p.N % kBN) != 0);
                 lim = p.causal ? row + 1 : p.N - last * kBN;
-                // Ping-pong: the exp2 phases of the two softmax groups alternate (tile 0 step j,
-                // tile 1 step j, tile 0 step j+1, ...), so one group's exponentials overlap the
-                // other tile's MMAs instead of competing for the same issue slots and MUFU.  Tile
-                // 1 hands the turn back after each of its steps up to tile 0's last; tile 0 takes
-                // the hand-back of a ping-pong item's last step at its next item's first step, so
-                // neither turn barrier ever runs two phases ahead of its waiter.
-                //   step 0 waits iff tw_first, step i >= 1 iff i <= tw_until; step i hands the
-                //   turn over iff i <= ta_until.
-                if (t == 0) {
-                    tw_first = (ph & kOwed) != 0;
-                    tw_until = pingpong ? n - 1 : 0;
-                    ta_until = pingpong ? n - 1 : -1;
-                    ph = pingpong ? (ph | kOwed) : (ph & ~kOwed);
-                } else {
-                    const int n0 = pingpong ? w.last0 - w.kv_begin : -1;
-                    tw_first = n0 >= 0;
-                    tw_until = n0;
-                    ta_until = n0;
-                }
+                // Ping-pong through turn tokens: group 1's exp2 phase number x waits for group
+                // 0's number x, group 0's number x for group 1's number x-2, so the phases
+                // alternate in the steady state while group 0 may run up to two ahead, e.g. into
+                // the next item while group 1 finishes its item's last (diagonal) step and
+                // epilogue.  Tokens go to two barriers per group by the parity of x, so neither
+                // barrier ever holds two pending phases.  Steps i <= tok_until take part: both
+                // groups' steps up to tile 0's last one, in items where both tiles take part.
+                tok_until = !pingpong ? -1 : (t == 0 ? n - 1 : w.last0 - w.kv_begin);
             }
             float m = -INFINITY;  // running max of c*s (log2 units)
             float l = 0.f;        // running denominator
@@ -565,11 +555,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool rescale = i > 0 && __any_sync(0xffffffffu, m_new != m);
                 m = m_new;
                 const float neg_m = -m;
-                if (i == 0 ? tw_first : i <= tw_until) {
-                    ok = mbar_wait_warp(bar(L::kBarTurn + t), (ph & kPhTurn) ? 1u : 0u, abort_flag,
-                                        status_word);
+                if (i <= tok_until && (t == 1 || tok >= 2)) {
+                    const uint32_t x = t == 0 ? tok - 2 : tok;  // the other group's token
+                    ok = mbar_wait_warp(bar(L::kBarTurn + 2 * t + (x & 1)), (x >> 1) & 1u,
+                                        abort_flag, status_word);
                     if (!ok) break;
-                    ph ^= kPhTurn;
                 }
                 // p = exp2(c*s - m).  Keys 0-63 go to TMEM (over S) and are published first; keys
                 // 64-127 go to this tile's smem panel, which the previous step's second-half P.V
@@ -630,7 +620,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive(bar(L::kBarPReady + 2 * t + 1));
                 }
                 l = l * alpha + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
-                if (i <= ta_until) mbar_arrive(bar(L::kBarTurn + (t ^ 1)));  // hand the turn over
+                if (i <= tok_until) {  // token number `tok` to the other group
+                    mbar_arrive(bar(L::kBarTurn + 2 * (t ^ 1) + (tok & 1)));
+                    ++tok;
+                }
                 ph ^= kPhStep;
             }
             if (ok) ok = mbar_wait_warp(bar(L::kBarODone + t), (ph & kPhODone) ? 1u : 0u,
