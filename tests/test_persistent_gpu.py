@@ -24,6 +24,9 @@ SHAPES = [
     wl.TINY_CAUSAL,                                            # 2 items
     wl.Workload("pers-mqa-n2000", 1, 40, 1, 2000, 128, True, 41),  # 320 items, ragged N
     wl.Workload("pers-d64-n3000", 2, 8, 4, 3000, 64, False, 42),   # 192 items, D = 64
+    # 15 Q tiles per head: every head's last item has one Q tile, so items with and without
+    # the ping-pong partner alternate in every CTA's sequence
+    wl.Workload("pers-odd-n1900", 1, 24, 6, 1900, 128, True, 43),  # 192 items
 ]
 
 
@@ -44,7 +47,7 @@ def test_many_launches_alternating_shapes_are_bit_identical(cuda_lib):
         o_ref, l_ref = oracle.attn_ref(*host, w.causal, w.sm_scale)
         _check(out, lse, o_ref, l_ref, w.name)
         first.append((out.clone(), lse.clone()))
-    # 3 x 4 x 13 = 156 launches: every counter slot is reused, by shapes of different grids
+    # 3 x 5 x 13 = 195 launches: every counter slot is reused, by shapes of different grids
     for rnd in range(13):
         for i, (w, (host, (qd, kd, vd))) in enumerate(zip(SHAPES, data)):
             out, lse = attn.attn_fwd(qd, kd, vd, causal=w.causal, sm_scale=w.sm_scale)
@@ -81,12 +84,15 @@ def test_concurrent_launches_on_two_streams(cuda_lib):
     assert attn.device_status(dev) == 0
 
 
-def test_split_launches_reuse_counters(cuda_lib):
-    """Split-KV launches claim (item, split) pairs through the same counters."""
+@pytest.mark.parametrize("w", [wl.FEWHEADS, wl.Workload("pers-split-causal-n1900", 1, 4, 2, 1900,
+                                                          128, True, 44)],
+                         ids=["fewheads-n4096", "causal-n1900"])
+def test_split_launches_reuse_counters(w, cuda_lib):
+    """Split-KV launches claim (item, split) pairs through the same counters; under the causal
+    mask some items have only their second Q tile, or no tile, in a split."""
     import exact_attention_forward_attn_gb300 as attn
 
     dev = torch.device("cuda:0")
-    w = wl.FEWHEADS
     host, (qd, kd, vd) = _inputs(w, dev)
     o_ref, l_ref = oracle.attn_ref(*host, w.causal, w.sm_scale)
     base = {}
