@@ -106,3 +106,37 @@ def test_split_launches_reuse_counters(w, cuda_lib):
         else:
             assert torch.equal(out, base[n_splits][0]) and torch.equal(lse, base[n_splits][1])
     assert attn.device_status(dev) == 0
+
+
+def test_cuda_graph_replays(cuda_lib):
+    """Launches captured in a CUDA graph keep their claim counters across replays: each replay
+    starts from the zero the previous one left."""
+    import exact_attention_forward_attn_gb300 as attn
+
+    dev = torch.device("cuda:0")
+    wa, wb = SHAPES[0], SHAPES[4]
+    (_, (qa, ka, va)), (_, (qb, kb, vb)) = _inputs(wa, dev), _inputs(wb, dev)
+    ref_a = attn.attn_fwd(qa, ka, va, causal=wa.causal, sm_scale=wa.sm_scale)
+    ref_b = attn.attn_fwd(qb, kb, vb, causal=wb.causal, sm_scale=wb.sm_scale)
+    torch.cuda.synchronize()
+    oa, la = torch.empty_like(ref_a[0]), torch.empty_like(ref_a[1])
+    ob, lb = torch.empty_like(ref_b[0]), torch.empty_like(ref_b[1])
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):  # warm up on the capture stream
+        attn.attn_fwd(qa, ka, va, causal=wa.causal, sm_scale=wa.sm_scale, out=oa, lse=la)
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(2):
+            attn.attn_fwd(qa, ka, va, causal=wa.causal, sm_scale=wa.sm_scale, out=oa, lse=la)
+            attn.attn_fwd(qb, kb, vb, causal=wb.causal, sm_scale=wb.sm_scale, out=ob, lse=lb)
+    for _ in range(20):
+        oa.zero_()
+        ob.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(oa, ref_a[0]) and torch.equal(la, ref_a[1])
+        assert torch.equal(ob, ref_b[0]) and torch.equal(lb, ref_b[1])
+    assert attn.device_status(dev) == 0
