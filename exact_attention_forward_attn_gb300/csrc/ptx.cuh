@@ -152,8 +152,9 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 }
 
 
-// Non-suspending poll of phase `parity` (test_wait: measured to wake the critical-path warps a
-// little sooner than the suspending try_wait).
+// Non-suspending poll of phase `parity` (test_wait): wakes a waiting warp a little sooner than
+// the suspending try_wait, but spends the issue slots of its SM sub-partition while it polls;
+// each wait site uses the one that measured faster.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t done;
     asm volatile(
@@ -167,8 +168,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Suspending poll: the thread may wait inside the instruction (up to a hardware time limit), so
-// a role that is off the critical path leaves the issue slots of its SM sub-partition to the warps
-// that share it.
+// a waiting warp leaves the issue slots of its SM sub-partition to the warps that share it.
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
     uint32_t done;
     asm volatile(
