@@ -148,12 +148,14 @@ __global__ void __launch_bounds__(kW256Threads, 1)
         }
         __syncwarp();
     } else if (warp == kW256MmaS) {
-        // S(j) = Q K_j^T into buffer j&1, once the softmax has read S(j-2)
-        bool ok = mbar_wait_warp(bar(L::kBarQ), 0, abort_flag, status_word);
+        // S(j) = Q K_j^T into buffer j&1, once the softmax has read S(j-2).  (The issuers' and
+        // the softmax warps' waits suspend instead of polling, leaving the issue slots of their
+        // SM sub-partitions to the softmax warps: measured 2 % faster.)
+        bool ok = mbar_wait_warp<true>(bar(L::kBarQ), 0, abort_flag, status_word);
         for (int j = 0; ok && j < n_kv; ++j) {
             if (j >= 2) {
-                ok = mbar_wait_warp(bar(L::kBarSFree + (j & 1)), ((j - 2) >> 1) & 1, abort_flag,
-                                    status_word);
+                ok = mbar_wait_warp<true>(bar(L::kBarSFree + (j & 1)), ((j - 2) >> 1) & 1,
+                                          abort_flag, status_word);
                 if (!ok) break;
                 tc_fence_after();
             }
@@ -161,8 +163,8 @@ __global__ void __launch_bounds__(kW256Threads, 1)
             // released as soon as they have read it
             for (int pn = 0; ok && pn < 4; ++pn) {
                 const int k = 4 * j + pn;
-                ok = mbar_wait_warp(bar(L::kBarKFull + k % L::kKSlots), (k / L::kKSlots) & 1,
-                                    abort_flag, status_word);
+                ok = mbar_wait_warp<true>(bar(L::kBarKFull + k % L::kKSlots),
+                                          (k / L::kKSlots) & 1, abort_flag, status_word);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t kp = sbase + L::kK + (k % L::kKSlots) * L::kPanel;
@@ -182,9 +184,9 @@ __global__ void __launch_bounds__(kW256Threads, 1)
         // O += P(j) V_j: A = P from shared memory, B = the four V panels (N = 256)
         bool ok = true;
         for (int j = 0; ok && j < n_kv; ++j) {
-            ok = mbar_wait_warp(bar(L::kBarVFull), j & 1, abort_flag, status_word);
-            if (ok) ok = mbar_wait_warp(bar(L::kBarPFull + (j & 1)), (j >> 1) & 1, abort_flag,
-                                        status_word);
+            ok = mbar_wait_warp<true>(bar(L::kBarVFull), j & 1, abort_flag, status_word);
+            if (ok) ok = mbar_wait_warp<true>(bar(L::kBarPFull + (j & 1)), (j >> 1) & 1,
+                                              abort_flag, status_word);
             if (!ok) break;
             tc_fence_after();
 #pragma unroll
@@ -207,8 +209,8 @@ __global__ void __launch_bounds__(kW256Threads, 1)
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; ok && j < n_kv; ++j) {
-            ok = mbar_wait_warp(bar(L::kBarSFull + (j & 1)), (j >> 1) & 1, abort_flag,
-                                status_word);
+            ok = mbar_wait_warp<true>(bar(L::kBarSFull + (j & 1)), (j >> 1) & 1, abort_flag,
+                                      status_word);
             if (!ok) break;
             tc_fence_after();
             float s[128];
@@ -262,8 +264,8 @@ __global__ void __launch_bounds__(kW256Threads, 1)
             }
             // P.V(j-1) must have read the previous P (and landed, for the O correction)
             if (j > 0) {
-                ok = mbar_wait_warp(bar(L::kBarPvDone + ((j - 1) & 1)), ((j - 1) >> 1) & 1,
-                                    abort_flag, status_word);
+                ok = mbar_wait_warp<true>(bar(L::kBarPvDone + ((j - 1) & 1)),
+                                          ((j - 1) >> 1) & 1, abort_flag, status_word);
                 if (!ok) break;
                 tc_fence_after();
             }
