@@ -216,22 +216,25 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         __syncwarp();
     } else if (warp == kMlaMmaA) {
         // ---------------- S(i) = Q . cache tile i into S[i&1], 36 MMAs (warp-uniform issue) ----
-        bool ok = mbar_wait_warp(bar(L::kBarQ), 0, abort_flag, status_word);
-        if (ok) ok = mbar_wait_warp(bar(L::kBarQt), 0, abort_flag, status_word);
+        // (the issuers' and the softmax warps' waits suspend instead of polling, leaving the
+        // issue slots of their SM sub-partitions to the softmax warps: measured 2 % faster)
+        bool ok = mbar_wait_warp<true>(bar(L::kBarQ), 0, abort_flag, status_word);
+        if (ok) ok = mbar_wait_warp<true>(bar(L::kBarQt), 0, abort_flag, status_word);
         tc_fence_after();
         for (int i = 0; ok && i < n_t; ++i) {
             if (i >= 1) {  // the softmax has loaded S(i-1)
-                ok = mbar_wait_warp(bar(L::kBarSFree), (i - 1) & 1, abort_flag, status_word);
+                ok = mbar_wait_warp<true>(bar(L::kBarSFree), (i - 1) & 1, abort_flag,
+                                          status_word);
                 if (!ok) break;
             }
             for (int x = 0; ok && x < 5; ++x) {  // the tile's five X panels have landed
                 const int k = 5 * i + x;
-                ok = mbar_wait_warp(bar(L::kBarXFull + k % L::kXSlots), (k / L::kXSlots) & 1,
-                                    abort_flag, status_word);
+                ok = mbar_wait_warp<true>(bar(L::kBarXFull + k % L::kXSlots),
+                                          (k / L::kXSlots) & 1, abort_flag, status_word);
             }
             const int yb = ybuf(i);
-            if (ok) ok = mbar_wait_warp(bar(L::kBarYFull + yb), yphase(i), abort_flag,
-                                        status_word);
+            if (ok) ok = mbar_wait_warp<true>(bar(L::kBarYFull + yb), yphase(i), abort_flag,
+                                              status_word);
             if (!ok) break;
             tc_fence_after();
 #pragma unroll
@@ -262,7 +265,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         // ---------------- O += P(i) Y_i (four N=256 MMAs), once the softmax has written P(i) ---
         bool ok = true;
         for (int i = 0; ok && i < n_t; ++i) {
-            ok = mbar_wait_warp(bar(L::kBarPFull), i & 1, abort_flag, status_word);
+            ok = mbar_wait_warp<true>(bar(L::kBarPFull), i & 1, abort_flag, status_word);
             if (!ok) break;
             tc_fence_after();
             const int yb = ybuf(i);
@@ -282,7 +285,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         const int h = ht * kMlaHeads + row;
         const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
         const float c = p.scale_log2;
-        bool ok = mbar_wait_warp(bar(L::kBarQ), 0, abort_flag, status_word);
+        bool ok = mbar_wait_warp<true>(bar(L::kBarQ), 0, abort_flag, status_word);
         // start-up: the five staged Q panels -> TMEM (bf16 pairs, the MMA's A layout)
         if (ok) {
 #pragma unroll 1
@@ -301,7 +304,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         mbar_arrive(bar(L::kBarQt));
         float m = -INFINITY, l = 0.f;
         for (int i = 0; ok && i < n_t; ++i) {
-            ok = mbar_wait_warp(bar(L::kBarSFull), i & 1, abort_flag, status_word);
+            ok = mbar_wait_warp<true>(bar(L::kBarSFull), i & 1, abort_flag, status_word);
             if (!ok) break;
             tc_fence_after();
             float s[kMlaBN];
@@ -345,7 +348,8 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
             }
             // P(i) overwrites P(i-1) and O may need its correction: both wait for P.V(i-1)
             if (i > 0) {
-                ok = mbar_wait_warp(bar(L::kBarPvDone), (i - 1) & 1, abort_flag, status_word);
+                ok = mbar_wait_warp<true>(bar(L::kBarPvDone), (i - 1) & 1, abort_flag,
+                                          status_word);
                 if (!ok) break;
                 tc_fence_after();
             }
