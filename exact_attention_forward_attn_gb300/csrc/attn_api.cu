@@ -29,6 +29,10 @@ __device__ unsigned int g_attn_status_word = 0;
 // Claim counters of the persistent forward kernel, handed to launches round robin (so up to
 // kSchedSlots launches may run at once on a device); each launch leaves its counter at zero.
 __device__ unsigned int g_fwd_sched[gb300attn::kSchedSlots] = {};
+// Arrival counters of the MLA decode's in-kernel split merge: kMlaMergeGroups (b, head tile,
+// value half) groups per slot, slots taken from the same round robin as the claim counters.
+constexpr int kMlaMergeGroups = 512;
+__device__ unsigned int g_mla_merge[gb300attn::kSchedSlots * kMlaMergeGroups] = {};
 
 namespace {
 
@@ -132,6 +136,7 @@ struct DeviceState {
     int num_sms = 0;
     unsigned int* status_word = nullptr;
     unsigned int* sched = nullptr;  // g_fwd_sched
+    unsigned int* mla_merge = nullptr;  // g_mla_merge
     std::atomic<unsigned int> sched_next{0};
 };
 DeviceState g_devices[kMaxDevices];
@@ -176,6 +181,8 @@ int device_state(int dev, DeviceState** out) {
         e = cudaGetSymbolAddress(reinterpret_cast<void**>(&st.status_word), g_attn_status_word);
         if (e == cudaSuccess)
             e = cudaGetSymbolAddress(reinterpret_cast<void**>(&st.sched), g_fwd_sched);
+        if (e == cudaSuccess)
+            e = cudaGetSymbolAddress(reinterpret_cast<void**>(&st.mla_merge), g_mla_merge);
         bool regs_ok = true;
         if (e == cudaSuccess) e = opt_in_smem<64, false>(&regs_ok);
         if (e == cudaSuccess) e = opt_in_smem<128, false>(&regs_ok);
@@ -711,8 +718,9 @@ int mla_heuristic_splits(int64_t items, int64_t n_tiles, int64_t rows, int num_s
     return best;
 }
 
+// fp32 O_s of every split, then the LSE_s of both value halves
 int64_t mla_workspace_for(int B, int H, int n_splits) {
-    return static_cast<int64_t>(n_splits) * B * H * (kMlaDc + 1) * 4;
+    return static_cast<int64_t>(n_splits) * B * H * (kMlaDc + 2) * 4;
 }
 
 }  // namespace
@@ -805,12 +813,20 @@ extern "C" int attn_mla_decode(const void* q, const void* kv, void* out, float* 
     prm.lse = lse;
     prm.ws_o = n_splits > 1 ? static_cast<float*>(workspace) : nullptr;
     prm.ws_lse = n_splits > 1 ? prm.ws_o + static_cast<int64_t>(n_splits) * B * H * kMlaDc : nullptr;
+    // With a few splits the last CTA of each group merges them (no second launch); with many,
+    // one CTA would read too much alone, and the merge kernel spreads the rows over the GPU.
+    const bool fused = n_splits > 1 && n_splits <= kMlaMaxFusedSplits && items <= kMlaMergeGroups;
+    prm.merge_count = nullptr;
+    if (fused) {
+        const unsigned int slot = ds->sched_next.fetch_add(1u, std::memory_order_relaxed) % kSchedSlots;
+        prm.merge_count = ds->mla_merge + static_cast<size_t>(slot) * kMlaMergeGroups;
+    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     mla_decode_kernel<<<static_cast<unsigned int>(items * n_splits), kMlaThreads, MlaSmem::kAlloc,
                         s>>>(mq, mkv, prm, ds->status_word);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
-    if (n_splits > 1) {
+    if (n_splits > 1 && !fused) {
         const int64_t rows = static_cast<int64_t>(B) * H;
         const int64_t rows_per_block = 4 / mla_merge_groups(n_splits);
         mla_merge_kernel<<<static_cast<unsigned int>((rows + rows_per_block - 1) / rows_per_block),

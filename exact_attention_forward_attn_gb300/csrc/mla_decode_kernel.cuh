@@ -47,6 +47,7 @@ constexpr int kMlaHeads = 128;            // heads per CTA (M)
 constexpr int kMlaThreads = 224;
 constexpr int kMlaMmaA = 4, kMlaMmaB = 5, kMlaLoad = 6;
 constexpr float kMlaRescaleThreshold = 8.0f;  // log2 units
+constexpr int kMlaMaxFusedSplits = 4;      // up to this many splits merge inside the kernel
 
 struct MlaParams {
     int B, H, T;
@@ -57,7 +58,12 @@ struct MlaParams {
     __nv_bfloat16* out;  // [B, H, 512]            (n_splits == 1)
     float* lse;          // [B, H]                  (n_splits == 1)
     float* ws_o;         // [n_splits, B, H, 512]   (n_splits > 1): O_s = acc / l
-    float* ws_lse;       // [n_splits, B, H]        (n_splits > 1): natural-log LSE_s
+    float* ws_lse;       // [2, n_splits, B, H]     (n_splits > 1): natural-log LSE_s of each
+                         //                          value half (the halves' scores agree to
+                         //                          fp32 rounding)
+    unsigned int* merge_count;  // one arrival counter per (b, ht, r) group when the last CTA
+                                // of a group merges its splits (2..kMlaMaxFusedSplits), else
+                                // nullptr (the merge kernel runs); left at zero by every launch
 };
 
 struct MlaSmem {
@@ -86,6 +92,7 @@ struct MlaSmem {
     static constexpr int kNumBars = kBarPvDone + 1;
     static constexpr int kTmemSlot = kBars + kNumBars * 8;
     static constexpr int kAbort = kTmemSlot + 8;
+    static constexpr int kMergeFlag = kAbort + 4;  // this CTA merges its group
     static constexpr int kBytes = kAbort + 8;
     static constexpr int kAlloc = kBytes + 1024;
     static_assert(kStage + 5 * kQPanel <= kBars, "staging must fit in the last Y buffer + X ring");
@@ -99,6 +106,65 @@ constexpr uint32_t kMlaTS = 0, kMlaTP = 64, kMlaTQ = 96, kMlaTO = 256;
 // panels outside the value half, then the k_pe panel.
 __device__ __forceinline__ int mla_x_panel(int r, int x) {
     return x == 4 ? 8 : (r == 0 ? 4 + x : x);
+}
+
+// The merge of section 2.4's split-T inside the decode kernel, by the last CTA of a (b, ht, r)
+// group: warp w combines head rows h0 .. h0+31 of value half r over the token splits,
+// LSE = M + ln sum_s exp(LSE_s - M) and out_c = sum_s exp(LSE_s - LSE) O_s, from the partials the
+// group's CTAs left in L2 (read past L1, which does not see other SMs' stores).  Each lane first
+// forms the weights of its own row; per row, lane i then reads columns 4i..4i+3 and 128+4i..+3
+// of every split (1 KiB per split and row, coalesced) and writes them as bf16.
+__device__ __forceinline__ void mla_merge_warp(const MlaParams& p, int b, int ht, int r, int warp,
+                                               int lane) {
+    const size_t BH = static_cast<size_t>(p.B) * p.H;
+    const int h0 = ht * kMlaHeads + warp * 32;
+    float wt[kMlaMaxFusedSplits];
+    float lse_m = 0.f;
+    {
+        float ls[kMlaMaxFusedSplits];
+        float mx = -INFINITY;
+        const size_t bh = static_cast<size_t>(b) * p.H + min(h0 + lane, p.H - 1);
+#pragma unroll
+        for (int s = 0; s < kMlaMaxFusedSplits; ++s) {
+            ls[s] = s < p.n_splits
+                ? __ldcg(p.ws_lse + (static_cast<size_t>(r) * p.n_splits + s) * BH + bh)
+                : -INFINITY;
+            mx = fmaxf(mx, ls[s]);
+        }
+        float sum = 0.f;
+#pragma unroll
+        for (int s = 0; s < kMlaMaxFusedSplits; ++s) {
+            wt[s] = s < p.n_splits ? __expf(ls[s] - mx) : 0.f;
+            sum += wt[s];
+        }
+        const float inv = 1.0f / sum;
+#pragma unroll
+        for (int s = 0; s < kMlaMaxFusedSplits; ++s) wt[s] *= inv;
+        lse_m = mx + __logf(sum);
+    }
+#pragma unroll 4
+    for (int rr = 0; rr < 32; ++rr) {
+        if (h0 + rr >= p.H) break;  // warp-uniform
+        const size_t bh_r = static_cast<size_t>(b) * p.H + h0 + rr;
+        float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+#pragma unroll
+        for (int s = 0; s < kMlaMaxFusedSplits; ++s) {
+            const float w = __shfl_sync(0xffffffffu, wt[s], rr);
+            if (s < p.n_splits) {
+                const float4* src = reinterpret_cast<const float4*>(
+                    p.ws_o + (static_cast<size_t>(s) * BH + bh_r) * kMlaDc + r * 256);
+                const float4 v0 = __ldcg(src + lane), v1 = __ldcg(src + 32 + lane);
+                a0.x += w * v0.x; a0.y += w * v0.y; a0.z += w * v0.z; a0.w += w * v0.w;
+                a1.x += w * v1.x; a1.y += w * v1.y; a1.z += w * v1.z; a1.w += w * v1.w;
+            }
+        }
+        __nv_bfloat16* dst = p.out + bh_r * kMlaDc + r * 256;
+        *reinterpret_cast<uint2*>(dst + 4 * lane) =
+            make_uint2(pack_bf16x2(a0.x, a0.y), pack_bf16x2(a0.z, a0.w));
+        *reinterpret_cast<uint2*>(dst + 128 + 4 * lane) =
+            make_uint2(pack_bf16x2(a1.x, a1.y), pack_bf16x2(a1.z, a1.w));
+    }
+    if (r == 0 && h0 + lane < p.H) p.lse[static_cast<size_t>(b) * p.H + h0 + lane] = lse_m;
 }
 
 __global__ void __launch_bounds__(kMlaThreads, 1)
@@ -429,15 +495,37 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
                     *reinterpret_cast<uint4*>(dst + ch * 16) = make_uint4(a, b2, c2, d);
                 }
             }
-            if (h < p.H && r == 0) {
+            if (h < p.H) {
                 const size_t bh = static_cast<size_t>(b) * p.H + h;
                 if (split_out)
-                    p.ws_lse[static_cast<size_t>(split) * p.B * p.H + bh] = lse_nat;
-                else
+                    p.ws_lse[(static_cast<size_t>(r) * p.n_splits + split) * p.B * p.H + bh] =
+                        lse_nat;
+                else if (r == 0)
                     p.lse[bh] = lse_nat;
             }
         }
         __syncwarp();
+        if (p.merge_count != nullptr) {
+            // Every CTA of a (b, ht, r) group publishes its partials and arrives on the group's
+            // counter (a CTA whose waits expired arrives marked); the last arrival resets the
+            // counter and, if no CTA of the group was marked, merges the group's splits.
+            __threadfence();
+            const bool all_ok = named_barrier_and(1, 128, ok);
+            volatile int* merge_flag = reinterpret_cast<volatile int*>(smem + L::kMergeFlag);
+            if (threadIdx.x == 0) {
+                unsigned int* cnt = p.merge_count + blockIdx.x / p.n_splits;
+                const unsigned int add = all_ok ? 1u : 0x10001u;
+                const unsigned int old = atomicAdd(cnt, add);
+                const bool last = (old & 0xffffu) == static_cast<unsigned int>(p.n_splits - 1);
+                if (last) atomicExch(cnt, 0u);
+                *merge_flag = (last && ((old + add) >> 16) == 0u) ? 1 : 0;
+            }
+            named_barrier_sync(1, 128);
+            if (*merge_flag) {
+                __threadfence();
+                mla_merge_warp(p, b, ht, r, warp, lane);
+            }
+        }
     }
     tc_fence_before();
     __syncthreads();

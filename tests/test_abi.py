@@ -161,9 +161,10 @@ def _mla(lib, q=S, kv=S * 2, out=S * 4, lse=S * 5, B=1, H=128, T=4096, d_c=512, 
 
 
 def test_mla_workspace_bytes(lib):
-    # n_splits * B * H * (512 + 1) fp32, splits clamped to the 64-token tiles
-    assert lib.attn_mla_decode_workspace_bytes(2, 128, 4096, 4) == 4 * 2 * 128 * 513 * 4
-    assert lib.attn_mla_decode_workspace_bytes(1, 16, 100, 8) == 2 * 1 * 16 * 513 * 4
+    # n_splits * B * H * (512 + 2) fp32 (each split's O and both value halves' LSE), splits
+    # clamped to the 64-token tiles
+    assert lib.attn_mla_decode_workspace_bytes(2, 128, 4096, 4) == 4 * 2 * 128 * 514 * 4
+    assert lib.attn_mla_decode_workspace_bytes(1, 16, 100, 8) == 2 * 1 * 16 * 514 * 4
     assert lib.attn_mla_decode_workspace_bytes(1, 16, 64, 8) == 0  # one tile: no split
     assert lib.attn_mla_decode_workspace_bytes(1, 16, 4096, 1) == 0
     assert lib.attn_mla_decode_workspace_bytes(0, 16, 4096, 4) == 0

@@ -105,3 +105,24 @@ def test_device_errors_are_reported(cuda_lib):
                              lse.data_ptr(), 1, 4, 8, 512, 64, ctypes.c_float(0.1), 1, None, 0,
                              None)
     assert st == -10  # host memory for q
+
+
+def test_fused_merge_counters_reused():
+    """With 2-4 splits the last CTA of each group merges in the decode kernel, through arrival
+    counters the library hands out round robin from a pool of 64 slots; 3 x 30 launches reuse
+    every slot, and each launch must give the bits of the first."""
+    cases = [(wl.MLA_RAGGED, 2), (wl.MlaWorkload("mla-fuse-h1", 3, 1, 65, 96), 2),
+             (wl.MlaWorkload("mla-fuse-h200", 2, 200, 700, 97), 4)]
+    data, first = [], []
+    for w, splits in cases:
+        q, kv, out, lse = _run(w, splits)
+        _check(out, lse, q, kv, w.sm_scale)
+        data.append((q, kv))
+        first.append((out.clone(), lse.clone()))
+    for _ in range(30):
+        outs = [attn.mla_decode(q, kv, w.sm_scale, num_splits=splits)
+                for (w, splits), (q, kv) in zip(cases, data)]
+        torch.cuda.synchronize()
+        for (o, l), (o0, l0) in zip(outs, first):
+            assert torch.equal(o, o0) and torch.equal(l, l0)
+    assert attn.device_status() == 0

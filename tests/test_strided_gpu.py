@@ -67,3 +67,38 @@ def test_unaligned_stride_is_rejected(cuda_lib):
     q, k, v = (t.cuda() for t in wl.make_qkv(w))
     with pytest.raises(attn.AttnError, match="ATTN_ERR_STRIDE"):
         attn.attn_fwd(_padded(q, 4), k, v)  # row stride 68 elements = 136 bytes
+
+
+def test_offsets_beyond_2_31_elements(cuda_lib):
+    """Batch strides of 2^31 + 1024 elements: the second batch of q, k, v and out lies more than
+    2^31 elements (4 GiB) past its tensor's base, so every address the TMA maps and the epilogue
+    form needs 64-bit arithmetic.  The gap between out's two batches must stay untouched."""
+    import exact_attention_forward_attn_gb300 as attn
+
+    w = wl.random_case(2, 4, 2, 300, 128, True, 39)
+    q, k, v = wl.make_qkv(w)
+    S = (1 << 31) + 1024
+    per_b = [t[0].numel() for t in (q, k, v)]
+    offs = [0, per_b[0], per_b[0] + per_b[1]]
+    # q, k and v share one buffer (inputs may overlap each other); out has its own
+    inp = torch.empty(S + sum(per_b), dtype=torch.bfloat16, device="cuda")
+    views = []
+    for t, off in zip((q, k, v), offs):
+        view = inp.as_strided(t.shape, (S, t.shape[2] * t.shape[3], t.shape[3], 1), off)
+        view.copy_(t)
+        views.append(view)
+    obuf = torch.empty(S + per_b[0], dtype=torch.bfloat16, device="cuda")
+    sentinel = -7.5
+    band = 1 << 20
+    obuf[per_b[0]:per_b[0] + band].fill_(sentinel)  # just after batch 0
+    obuf[S - band:S].fill_(sentinel)                # just before batch 1
+    out = obuf.as_strided(q.shape, (S, q.shape[2] * q.shape[3], q.shape[3], 1), 0)
+    out, lse = attn.attn_fwd(*views, causal=w.causal, sm_scale=w.sm_scale, out=out)
+    torch.cuda.synchronize()
+    assert attn.device_status() == 0
+    assert (obuf[per_b[0]:per_b[0] + band] == sentinel).all()
+    assert (obuf[S - band:S] == sentinel).all()
+    o_ref, l_ref = oracle.attn_ref(q, k, v, w.causal, w.sm_scale)
+    _check(out.contiguous(), lse, o_ref, l_ref, f"64-bit offsets {w.name}")
+    del views, out, inp, obuf
+    torch.cuda.empty_cache()
