@@ -34,6 +34,8 @@ SIGNATURES = {
                                   _c_int, _c_float, _vp, _vp, _vp, _vp, _vp]),
     "attn_mla_decode": (_c_int, [_vp, _vp, _vp, _vp] + [_c_int] * 5 + [_c_float, _c_int, _vp,
                                                                       ctypes.c_size_t, _vp]),
+    "attn_mla_decode_test_stall": (_c_int, [_vp, _vp, _vp, _vp] + [_c_int] * 5
+                                   + [_c_float, _c_int, _vp, ctypes.c_size_t, _c_int, _vp]),
     "attn_mla_decode_num_splits": (_c_int, [_c_int, _c_int, _c_int]),
     "attn_mla_decode_workspace_bytes": (ctypes.c_size_t, [_c_int, _c_int, _c_int, _c_int]),
 }

@@ -741,9 +741,11 @@ extern "C" size_t attn_mla_decode_workspace_bytes(int B, int H, int T, int num_s
     return static_cast<size_t>(mla_workspace_for(B, H, num_splits));
 }
 
-extern "C" int attn_mla_decode(const void* q, const void* kv, void* out, float* lse, int B, int H,
-                               int T, int d_c, int d_r, float sm_scale, int num_splits,
-                               void* workspace, size_t workspace_bytes, void* stream) {
+namespace {
+
+int mla_decode_run(const void* q, const void* kv, void* out, float* lse, int B, int H, int T,
+                   int d_c, int d_r, float sm_scale, int num_splits, void* workspace,
+                   size_t workspace_bytes, void* stream, int stall_tile) {
     if (B < 0 || H <= 0 || T <= 0) return ATTN_ERR_SHAPE;
     if (d_c != kMlaDc || d_r != kMlaDr) return ATTN_ERR_HEADDIM;
     if (!std::isfinite(sm_scale) || !(sm_scale > 0.f)) return ATTN_ERR_SCALE;
@@ -813,6 +815,7 @@ extern "C" int attn_mla_decode(const void* q, const void* kv, void* out, float* 
     prm.lse = lse;
     prm.ws_o = n_splits > 1 ? static_cast<float*>(workspace) : nullptr;
     prm.ws_lse = n_splits > 1 ? prm.ws_o + static_cast<int64_t>(n_splits) * B * H * kMlaDc : nullptr;
+    prm.stall_tile = stall_tile;
     // With a few splits the last CTA of each group merges them (no second launch); with many,
     // one CTA would read too much alone, and the merge kernel spreads the rows over the GPU.
     const bool fused = n_splits > 1 && n_splits <= kMlaMaxFusedSplits && items <= kMlaMergeGroups;
@@ -836,6 +839,24 @@ extern "C" int attn_mla_decode(const void* q, const void* kv, void* out, float* 
         if (e != cudaSuccess) return cuda_fail(e);
     }
     return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" int attn_mla_decode(const void* q, const void* kv, void* out, float* lse, int B, int H,
+                               int T, int d_c, int d_r, float sm_scale, int num_splits,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+    return mla_decode_run(q, kv, out, lse, B, H, T, d_c, d_r, sm_scale, num_splits, workspace,
+                          workspace_bytes, stream, -1);
+}
+
+extern "C" int attn_mla_decode_test_stall(const void* q, const void* kv, void* out, float* lse,
+                                          int B, int H, int T, int d_c, int d_r, float sm_scale,
+                                          int num_splits, void* workspace,
+                                          size_t workspace_bytes, int stall_tile, void* stream) {
+    if (stall_tile < 0) return ATTN_ERR_SHAPE;
+    return mla_decode_run(q, kv, out, lse, B, H, T, d_c, d_r, sm_scale, num_splits, workspace,
+                          workspace_bytes, stream, stall_tile);
 }
 
 extern "C" const char* attn_status_string(int status) {

@@ -219,6 +219,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    static_assert(L::kBarDoFull < 32, "load barriers must fit the ArmedPhases mask");
     const uint32_t t_s = tmem, t_dp = tmem + 128, t_dv = tmem + 256, t_dk = tmem + 384;
     auto it_head = [=](int it) { return hkv * p.group + it / per_head; };
     auto it_tile = [=](int it) { return i_first + it % per_head; };
@@ -227,9 +228,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // ---------------- producer: lanes 0..kPanels-1 issue the Q panels and lanes kPanels..
         // 2*kPanels-1 the dO panels (one thread's bulk copies run one after another), every lane
         // stages 4+4 vector entries, fetched into registers one iteration ahead ------------------
+        ArmedPhases armed;  // this lane's loads (by barrier index), drained after an abort
         if (lane < 2 * kPanels) {  // K_j / V_j panel lane % kPanels
             const int h = lane % kPanels;
             mbar_arrive_expect_tx(bar(L::kBarRes), L::kPanelBytes);
+            armed.arm(L::kBarRes, 0u);
             if (lane < kPanels)
                 tma_load_4d(sbase + L::kRes0 + h * L::kPanelBytes, &tmap_k, bar(L::kBarRes),
                             h * 64, j * 128, hkv, b);
@@ -258,6 +261,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (ok && lane < kPanels) {
                 const int h = lane;
                 mbar_arrive_expect_tx(bar(L::kBarQFull + s), L::kPanelBytes);
+                armed.arm(L::kBarQFull + s, static_cast<uint32_t>(it / L::kQSlots));
                 tma_load_4d(sbase + L::kQ + s * L::kTileBytes + h * L::kPanelBytes, &tmap_q,
                             bar(L::kBarQFull + s), h * 64, it_tile(it) * 128, it_head(it), b);
             }
@@ -278,6 +282,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (ok && lane >= kPanels && lane < 2 * kPanels) {
                 const int h = lane - kPanels;
                 mbar_arrive_expect_tx(bar(L::kBarDoFull), L::kPanelBytes);
+                armed.arm(L::kBarDoFull, static_cast<uint32_t>(it));
                 tma_load_4d(sbase + L::kDO + h * L::kPanelBytes, &tmap_do, bar(L::kBarDoFull),
                             h * 64, it_tile(it) * 128, it_head(it), b);
             }
@@ -291,6 +296,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (ok) load_vec(it);
             if (ok) load_do(it);
         }
+        if (*abort_flag) armed.drain(bar(0), globaltimer_ns() + kDrainLimitNs);
         __syncwarp();
     } else if (warp == kBwdMmaWarp || warp == kBwdMmaWarpB) {
         // ---------------- MMA issuers (warp-uniform, elected lane) -----------------------------
@@ -600,6 +606,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    static_assert(L::kBarVFull + L::kVSlots <= 32, "load barriers must fit the ArmedPhases mask");
     // S is double-buffered (S(g+1) is formed while the elementwise warps work on S(g), g counting
     // the CTA's steps over all its items); dS is written over the S buffer it came from.
     const uint32_t t_s0 = tmem, t_dp = tmem + 128, t_dq = tmem + 256, t_s1 = tmem + 384;
@@ -632,6 +639,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // 0..kPanels-1 load a Q_i panel, then that panel of every K_j; lanes kPanels..2*kPanels-1
         // a dO_i panel, then that panel of every V_j.  Lane 0 also claims the items.
         if (lane < 2 * kPanels) {
+            ArmedPhases armed;  // this lane's loads (by barrier index), drained after an abort
             const bool kside = lane < kPanels;
             const int h = lane % kPanels;
             const int slots = kside ? L::kKSlots : L::kVSlots;
@@ -672,6 +680,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                                       (k - 1) & 1, abort_flag, status_word))
                     break;
                 mbar_arrive_expect_tx(bar(kside ? L::kBarQ : L::kBarDo), L::kPanelBytes);
+                armed.arm(kside ? L::kBarQ : L::kBarDo, static_cast<uint32_t>(k));
                 tma_load_4d(sbase + (kside ? L::kRes0 : L::kRes1) + h * L::kPanelBytes,
                             kside ? &tmap_q : &tmap_do, bar(kside ? L::kBarQ : L::kBarDo), h * 64,
                             i * 128, hq, b);
@@ -682,6 +691,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                                  abort_flag, status_word);
                     if (!ok) break;
                     mbar_arrive_expect_tx(bar(full0 + s), L::kPanelBytes);
+                    armed.arm(full0 + s, static_cast<uint32_t>(g / slots));
                     tma_load_4d(ring_base + s * L::kTileBytes + h * L::kPanelBytes, map,
                                 bar(full0 + s), h * 64, it * 128, hkv, b);
                 }
@@ -690,6 +700,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             // after an abort, still make this CTA's claims up to the one past the end
             if (lane == 0)
                 while (!claims_done) (void)claim();
+            if (*abort_flag) armed.drain(bar(0), globaltimer_ns() + kDrainLimitNs);
         }
         __syncwarp();
     } else if (warp == kBwdMmaWarp || warp == kBwdMmaWarpB) {

@@ -117,6 +117,8 @@ __global__ void __launch_bounds__(kW256Threads, 1)
         // One thread's bulk tensor copies are processed one after another (~29 bytes per cycle
         // per SM from one issuing thread), so every 16 KiB panel stream has its own lane.
         static_assert(L::kKSlots == 4, "K panel p of every key tile goes to slot p");
+        static_assert(L::kBarVFull < 32, "load barriers must fit the ArmedPhases mask");
+        ArmedPhases armed;  // this lane's loads (by barrier index), drained after an abort
         if (lane < 4) {  // Q panel `lane` once, then K panel `lane` of every key tile
             const int pn = lane;
             if (pn == 0) {
@@ -124,6 +126,7 @@ __global__ void __launch_bounds__(kW256Threads, 1)
                 tma_prefetch_desc(&tmap_k);
             }
             mbar_arrive_expect_tx(bar(L::kBarQ), L::kPanel);
+            armed.arm(L::kBarQ, 0u);
             tma_load_4d(sbase + L::kQ + pn * L::kPanel, &tmap_q, bar(L::kBarQ), pn * 64,
                         m_tile * 128, hq, b);
             for (int j = 0; j < n_kv; ++j) {
@@ -131,6 +134,7 @@ __global__ void __launch_bounds__(kW256Threads, 1)
                                              status_word))
                     break;
                 mbar_arrive_expect_tx(bar(L::kBarKFull + pn), L::kPanel);
+                armed.arm(L::kBarKFull + pn, static_cast<uint32_t>(j));
                 tma_load_4d(sbase + L::kK + pn * L::kPanel, &tmap_k, bar(L::kBarKFull + pn),
                             pn * 64, j * 128, hkv, b);
             }
@@ -142,10 +146,12 @@ __global__ void __launch_bounds__(kW256Threads, 1)
                                              status_word))
                     break;
                 mbar_arrive_expect_tx(bar(L::kBarVFull), L::kPanel);
+                armed.arm(L::kBarVFull, static_cast<uint32_t>(j));
                 tma_load_4d(sbase + L::kV + pn * L::kPanel, &tmap_v, bar(L::kBarVFull), pn * 64,
                             j * 128, hkv, b);
             }
         }
+        if (*abort_flag) armed.drain(bar(0), globaltimer_ns() + kDrainLimitNs);
         __syncwarp();
     } else if (warp == kW256MmaS) {
         // S(j) = Q K_j^T into buffer j&1, once the softmax has read S(j-2).  (The issuers' and

@@ -281,6 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // lane arrives with its own panel's bytes.  (The Q tiles are loaded by their MMA
         // issuers.)  Lane 0 also claims the items.
         if (lane < L::kLoadLanes) {
+            ArmedPhases kv_armed;        // this lane's loads, drained after an abort
             int ring = 0;                // K/V ring entries of the earlier items
             bool claims_done = false;    // lane 0: this CTA's claim past the end was made
             // One claim: the item number, or -1 past the end (the launch's last claim also
@@ -323,6 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (!ok) break;
                         if (idx == p.stall_item) continue;  // test hook: never deliver this entry
                         mbar_arrive_expect_tx(bar(L::kBarKvFull + slot), L::kPanelBytes);
+                        kv_armed.arm(slot, ph);
                         tma_load_4d(sbase + L::kKV + slot * L::kTileBytes + h * L::kPanelBytes,
                                     map, bar(L::kBarKvFull + slot), h * 64, j * kBN, w.hkv, w.b);
                     }
@@ -334,6 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // launch's claim count (and the counter's reset) stays exact.
             if (lane == 0)
                 while (!claims_done) (void)claim();
+            if (*abort_flag) kv_armed.drain(bar(L::kBarKvFull), globaltimer_ns() + kDrainLimitNs);
         }
         __syncwarp();
     } else if (warp == kMmaWarp0 || warp == kMmaWarp0 + 1) {
@@ -386,6 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  kIdescPV, 1u);
         };
 
+        ArmedPhases q_armed;   // this lane's Q loads, drained after an abort
         int ring = 0;          // K/V ring entries of the earlier items
         uint32_t steps = 0;    // KV steps this tile ran in earlier items (P-ready phases)
         uint32_t q_items = 0;  // items this tile took part in (Q-full phases)
@@ -406,6 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                  abort_flag, status_word);
                     if (qok) {
                         mbar_arrive_expect_tx(bar(L::kBarQFull + t), L::kPanelBytes);
+                        q_armed.arm(t, q_items);
                         tma_load_4d(qa + lane * L::kPanelBytes, &tmap_q, bar(L::kBarQFull + t),
                                     lane * 64, (w.tile0 + t) * kBM, w.hq, w.b);
                     }
@@ -464,6 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ring += 2 * (w.kv_end - w.kv_begin);
         }
+        if (*abort_flag) q_armed.drain(bar(L::kBarQFull), globaltimer_ns() + kDrainLimitNs);
         __syncwarp();
     }
     } else {

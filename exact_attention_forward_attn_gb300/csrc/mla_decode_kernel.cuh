@@ -64,6 +64,7 @@ struct MlaParams {
     unsigned int* merge_count;  // one arrival counter per (b, ht, r) group when the last CTA
                                 // of a group merges its splits (2..kMlaMaxFusedSplits), else
                                 // nullptr (the merge kernel runs); left at zero by every launch
+    int stall_tile;  // test hook: >= 0 withholds the X panels of this token tile (else -1)
 };
 
 struct MlaSmem {
@@ -232,7 +233,9 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         // processed one after another (~29 bytes per cycle per SM from one issuing thread), so
         // lanes 0-4 stream the five X panels of every tile and lanes 5-8 its four value panels;
         // lanes 0-8 first load one Q panel each ------------------------------------------------
+        static_assert(L::kBarYFull + L::kYBufs <= 32, "load barriers must fit the ArmedPhases mask");
         if (lane < kMlaPanels) {
+            ArmedPhases armed;  // this lane's loads (by barrier index), drained after an abort
             if (lane == 0) {
                 tma_prefetch_desc(&tmap_q);
                 tma_prefetch_desc(&tmap_kv);
@@ -241,6 +244,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
             // lanes 0-3: the value-side Q panels -> smem slots 0-3; lanes 4-8: the X-side Q
             // panels -> staging, for TMEM
             mbar_arrive_expect_tx(bar(L::kBarQ), L::kQPanel);
+            armed.arm(L::kBarQ, 0u);
             if (lane < 4)
                 tma_load_3d(sbase + L::kQ + lane * L::kQPanel, &tmap_q, bar(L::kBarQ),
                             (4 * r + lane) * 64, ht * kMlaHeads, b);
@@ -256,7 +260,9 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
                                                  ((k / L::kXSlots) & 1) ^ 1u, abort_flag,
                                                  status_word);
                     if (!ok) break;
+                    if (t_begin + i == p.stall_tile) continue;  // test hook: never deliver it
                     mbar_arrive_expect_tx(bar(L::kBarXFull + slot), L::kKvPanel);
+                    armed.arm(L::kBarXFull + slot, static_cast<uint32_t>(k / L::kXSlots));
                     tma_load_3d(sbase + L::kX + slot * L::kKvPanel, &tmap_kv,
                                 bar(L::kBarXFull + slot), mla_x_panel(r, x) * 64,
                                 (t_begin + i) * kMlaBN, b);
@@ -273,11 +279,13 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
                                                  abort_flag, status_word))
                         break;
                     mbar_arrive_expect_tx(bar(L::kBarYFull + yb), L::kKvPanel);
+                    armed.arm(L::kBarYFull + yb, yphase(i));
                     tma_load_3d(sbase + L::kY + (4 * yb + y) * L::kKvPanel, &tmap_kv,
                                 bar(L::kBarYFull + yb), (4 * r + y) * 64, (t_begin + i) * kMlaBN,
                                 b);
                 }
             }
+            if (*abort_flag) armed.drain(bar(0), globaltimer_ns() + kDrainLimitNs);
         }
         __syncwarp();
     } else if (warp == kMlaMmaA) {

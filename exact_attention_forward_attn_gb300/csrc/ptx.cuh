@@ -221,6 +221,30 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity,
     return __all_sync(0xffffffffu, ok);
 }
 
+// The phases a thread armed for its own bulk copies on a group of consecutive mbarriers (a load
+// ring): bit s of `armed` says it armed barrier s, bit s of `parity` is that phase's parity.  A
+// CTA that gave up (an expired wait) drains them before it exits, so that no copy of its own still
+// lands in shared memory that a later CTA may own.  Each wait ends at `deadline` at the latest: a
+// phase that another thread never armed does not complete, but this thread's copies have landed
+// long before then.
+constexpr uint64_t kDrainLimitNs = 2000000ull;  // 2 ms for all of a CTA's drains together
+
+struct ArmedPhases {
+    uint32_t armed = 0u, parity = 0u;
+    __device__ __forceinline__ void arm(int s, uint32_t ph) {
+        armed |= 1u << s;
+        parity = (parity & ~(1u << s)) | ((ph & 1u) << s);
+    }
+    __device__ __forceinline__ void drain(uint32_t bar0, uint64_t deadline) const {
+        for (uint32_t m = armed; m != 0u; m &= m - 1u) {
+            const int s = __ffs(static_cast<int>(m)) - 1;
+            while (!mbar_try_wait(bar0 + 8u * static_cast<uint32_t>(s), (parity >> s) & 1u) &&
+                   globaltimer_ns() < deadline) {
+            }
+        }
+    }
+};
+
 // ------------------------------------------------------------------------------------------------
 // TMA (tensor copies between global and shared memory); no multicast.
 // ------------------------------------------------------------------------------------------------

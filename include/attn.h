@@ -272,6 +272,20 @@ int attn_fwd_test_stall(const void* q, const void* k, const void* v, void* out, 
                         int Hq, int Hkv, int N, int D, int causal, float sm_scale, int stall_item,
                         void* stream);
 
+/*
+ * attn_mla_decode_test_stall - the same test hook for attn_mla_decode (arguments as there).
+ *
+ * The producer of every CTA whose token range holds 64-token tile `stall_tile` (>= 0) withholds
+ * that tile's cache panels, so those CTAs' bounded waits expire after about one second and they
+ * stop, free their tensor memory and return.  A split group with such a CTA is not merged: out
+ * and lse hold garbage there, the status word records the expiry, the group's arrival counter is
+ * still reset, and the next call computes correctly.  Use tiny problems.
+ */
+int attn_mla_decode_test_stall(const void* q, const void* kv, void* out, float* lse, int B, int H,
+                               int T, int d_c, int d_r, float sm_scale, int num_splits,
+                               void* workspace, size_t workspace_bytes, int stall_tile,
+                               void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -31,7 +31,8 @@ def test_header_declares_the_boundary():
          "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_bytes", "attn_fwd_splitkv_num_splits",
          "attn_fwd_splitkv_noalloc", "attn_fwd_splitkv_noalloc_max_bytes", "attn_fwd_strided",
          "attn_fwd_test_stall", "attn_bwd", "attn_bwd_workspace_bytes", "attn_mla_decode",
-         "attn_mla_decode_num_splits", "attn_mla_decode_workspace_bytes"])
+         "attn_mla_decode_test_stall", "attn_mla_decode_num_splits",
+         "attn_mla_decode_workspace_bytes"])
 
 
 def test_library_exports_every_declared_symbol(lib):

@@ -58,3 +58,37 @@ def test_stall_item_past_the_end_stalls_nothing(cuda_lib):
     assert lib.attn_debug_status(stream) == 0
     o_ref, l_ref = oracle.attn_ref(q, k, v, True, w.sm_scale)
     _check(out, lse, o_ref, l_ref, "stall item beyond the ring")
+
+
+def test_mla_expired_wait_skips_the_fused_merge_and_resets_its_counters(cuda_lib):
+    """MLA decode with two splits merged in the kernel: the CTAs of split 1 are starved of one
+    cache tile and time out.  Each group's last arrival must then skip the merge (out and lse
+    keep their zeros) but still reset its counter; 70 further launches bring every counter slot,
+    the stalled launch's included, round again and must all merge correctly."""
+    import exact_attention_forward_attn_gb300 as attn
+    from test_mla_gpu import _check as mla_check
+
+    lib = cuda_lib
+    w = wl.MlaWorkload("mla-stall", 1, 16, 256, 98)  # 4 token tiles: split 1 holds tiles 2-3
+    q, kv = wl.make_mla(w, device="cuda")
+    splits = 2
+    need = attn.mla_decode_workspace_bytes(w.B, w.H, w.T, splits)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    out = torch.zeros(w.B, w.H, 512, dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros(w.B, w.H, dtype=torch.float32, device="cuda")
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    assert lib.attn_debug_status(stream) == 0
+    st = lib.attn_mla_decode_test_stall(q.data_ptr(), kv.data_ptr(), out.data_ptr(),
+                                        lse.data_ptr(), w.B, w.H, w.T, 512, 64,
+                                        ctypes.c_float(w.sm_scale), splits, ws.data_ptr(), need,
+                                        3, stream)
+    assert st == 0
+    assert lib.attn_debug_status(stream) == -9  # ATTN_ERR_TIMEOUT
+    assert lib.attn_debug_status(stream) == 0
+    assert torch.all(out == 0) and torch.all(lse == 0)
+    runs = [attn.mla_decode(q, kv, w.sm_scale, num_splits=splits) for _ in range(70)]
+    torch.cuda.synchronize()
+    assert attn.device_status() == 0
+    for o, l in runs[1:]:
+        assert torch.equal(o, runs[0][0]) and torch.equal(l, runs[0][1])
+    mla_check(runs[-1][0], runs[-1][1], q, kv, w.sm_scale)
