@@ -29,10 +29,6 @@ __device__ unsigned int g_attn_status_word = 0;
 // Claim counters of the persistent forward kernel, handed to launches round robin (so up to
 // kSchedSlots launches may run at once on a device); each launch leaves its counter at zero.
 __device__ unsigned int g_fwd_sched[gb300attn::kSchedSlots] = {};
-// Arrival counters of the MLA decode's in-kernel split merge: kMlaMergeGroups (b, head tile,
-// value half) groups per slot, slots taken from the same round robin as the claim counters.
-constexpr int kMlaMergeGroups = 512;
-__device__ unsigned int g_mla_merge[gb300attn::kSchedSlots * kMlaMergeGroups] = {};
 
 namespace {
 
@@ -136,7 +132,6 @@ struct DeviceState {
     int num_sms = 0;
     unsigned int* status_word = nullptr;
     unsigned int* sched = nullptr;  // g_fwd_sched
-    unsigned int* mla_merge = nullptr;  // g_mla_merge
     std::atomic<unsigned int> sched_next{0};
 };
 DeviceState g_devices[kMaxDevices];
@@ -181,8 +176,6 @@ int device_state(int dev, DeviceState** out) {
         e = cudaGetSymbolAddress(reinterpret_cast<void**>(&st.status_word), g_attn_status_word);
         if (e == cudaSuccess)
             e = cudaGetSymbolAddress(reinterpret_cast<void**>(&st.sched), g_fwd_sched);
-        if (e == cudaSuccess)
-            e = cudaGetSymbolAddress(reinterpret_cast<void**>(&st.mla_merge), g_mla_merge);
         bool regs_ok = true;
         if (e == cudaSuccess) e = opt_in_smem<64, false>(&regs_ok);
         if (e == cudaSuccess) e = opt_in_smem<128, false>(&regs_ok);
@@ -718,9 +711,11 @@ int mla_heuristic_splits(int64_t items, int64_t n_tiles, int64_t rows, int num_s
     return best;
 }
 
-// fp32 O_s of every split, then the LSE_s of both value halves
+// fp32 O_s and LSE_s of every split, for the merge kernel (2..kMlaMaxClusterSplits splits merge
+// inside a cluster and need none)
 int64_t mla_workspace_for(int B, int H, int n_splits) {
-    return static_cast<int64_t>(n_splits) * B * H * (kMlaDc + 2) * 4;
+    if (n_splits <= kMlaMaxClusterSplits) return 0;
+    return static_cast<int64_t>(n_splits) * B * H * (kMlaDc + 1) * 4;
 }
 
 }  // namespace
@@ -737,7 +732,6 @@ extern "C" size_t attn_mla_decode_workspace_bytes(int B, int H, int T, int num_s
     if (B <= 0 || H <= 0 || T <= 0 || num_splits < 0 || num_splits > kMaxSplits) return 0;
     if (num_splits == 0) num_splits = attn_mla_decode_num_splits(B, H, T);
     num_splits = static_cast<int>(std::min<int64_t>(num_splits, mla_tiles(T)));
-    if (num_splits <= 1) return 0;
     return static_cast<size_t>(mla_workspace_for(B, H, num_splits));
 }
 
@@ -771,8 +765,8 @@ int mla_decode_run(const void* q, const void* kv, void* out, float* lse, int B, 
     // default one needs the SM count first.
     auto check_workspace = [&](int n_splits) {
         if (items * n_splits > 0x7fffffffLL) return ATTN_ERR_SHAPE;
-        if (n_splits <= 1) return ATTN_OK;
         const int64_t need = mla_workspace_for(B, H, n_splits);
+        if (need == 0) return ATTN_OK;
         if (!workspace) return ATTN_ERR_NULL;
         if (reinterpret_cast<uintptr_t>(workspace) & 15u) return ATTN_ERR_ALIGN;
         if (static_cast<int64_t>(workspace_bytes) < need) return ATTN_ERR_WORKSPACE;
@@ -798,7 +792,8 @@ int mla_decode_run(const void* q, const void* kv, void* out, float* lse, int B, 
     }
     for (const void* ptr : {q, kv, static_cast<const void*>(out), static_cast<const void*>(lse)})
         if (check_memory(ptr, dev) != ATTN_OK) return ATTN_ERR_MEMORY;
-    if (n_splits > 1 && check_memory(workspace, dev) != ATTN_OK) return ATTN_ERR_MEMORY;
+    const bool cluster = n_splits > 1 && n_splits <= kMlaMaxClusterSplits;
+    if (n_splits > 1 && !cluster && check_memory(workspace, dev) != ATTN_OK) return ATTN_ERR_MEMORY;
 
     CUtensorMap mq, mkv;
     if (!make_mla_map(&mq, q, B, H, kMlaHeads) || !make_mla_map(&mkv, kv, B, T, kMlaBN))
@@ -813,23 +808,35 @@ int mla_decode_run(const void* q, const void* kv, void* out, float* lse, int B, 
     prm.scale_log2 = sm_scale * 1.4426950408889634f;
     prm.out = static_cast<__nv_bfloat16*>(out);
     prm.lse = lse;
-    prm.ws_o = n_splits > 1 ? static_cast<float*>(workspace) : nullptr;
-    prm.ws_lse = n_splits > 1 ? prm.ws_o + static_cast<int64_t>(n_splits) * B * H * kMlaDc : nullptr;
+    // With a few splits the CTAs of a group form a cluster and merge through distributed shared
+    // memory (no partials in global memory, no second launch); with more, the partials go to the
+    // workspace and the merge kernel spreads the rows over the GPU.
+    prm.cluster_merge = cluster ? 1 : 0;
+    prm.ws_o = n_splits > 1 && !cluster ? static_cast<float*>(workspace) : nullptr;
+    prm.ws_lse = prm.ws_o ? prm.ws_o + static_cast<int64_t>(n_splits) * B * H * kMlaDc : nullptr;
     prm.stall_tile = stall_tile;
-    // With a few splits the last CTA of each group merges them (no second launch); with many,
-    // one CTA would read too much alone, and the merge kernel spreads the rows over the GPU.
-    const bool fused = n_splits > 1 && n_splits <= kMlaMaxFusedSplits && items <= kMlaMergeGroups;
-    prm.merge_count = nullptr;
-    if (fused) {
-        const unsigned int slot = ds->sched_next.fetch_add(1u, std::memory_order_relaxed) % kSchedSlots;
-        prm.merge_count = ds->mla_merge + static_cast<size_t>(slot) * kMlaMergeGroups;
-    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    mla_decode_kernel<<<static_cast<unsigned int>(items * n_splits), kMlaThreads, MlaSmem::kAlloc,
-                        s>>>(mq, mkv, prm, ds->status_word);
-    e = cudaGetLastError();
+    if (cluster) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned int>(items * n_splits));
+        cfg.blockDim = dim3(kMlaThreads);
+        cfg.dynamicSmemBytes = MlaSmem::kAlloc;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned int>(n_splits);  // the group's splits
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, mla_decode_kernel, mq, mkv, prm, ds->status_word);
+    } else {
+        mla_decode_kernel<<<static_cast<unsigned int>(items * n_splits), kMlaThreads,
+                            MlaSmem::kAlloc, s>>>(mq, mkv, prm, ds->status_word);
+        e = cudaGetLastError();
+    }
     if (e != cudaSuccess) return cuda_fail(e);
-    if (n_splits > 1 && !fused) {
+    if (n_splits > 1 && !cluster) {
         const int64_t rows = static_cast<int64_t>(B) * H;
         const int64_t rows_per_block = 4 / mla_merge_groups(n_splits);
         mla_merge_kernel<<<static_cast<unsigned int>((rows + rows_per_block - 1) / rows_per_block),

@@ -47,7 +47,7 @@ constexpr int kMlaHeads = 128;            // heads per CTA (M)
 constexpr int kMlaThreads = 224;
 constexpr int kMlaMmaA = 4, kMlaMmaB = 5, kMlaLoad = 6;
 constexpr float kMlaRescaleThreshold = 8.0f;  // log2 units
-constexpr int kMlaMaxFusedSplits = 4;      // up to this many splits merge inside the kernel
+constexpr int kMlaMaxClusterSplits = 4;    // up to this many splits merge inside a cluster
 
 struct MlaParams {
     int B, H, T;
@@ -57,13 +57,12 @@ struct MlaParams {
     float scale_log2;  // sm_scale * log2(e)
     __nv_bfloat16* out;  // [B, H, 512]            (n_splits == 1)
     float* lse;          // [B, H]                  (n_splits == 1)
-    float* ws_o;         // [n_splits, B, H, 512]   (n_splits > 1): O_s = acc / l
-    float* ws_lse;       // [2, n_splits, B, H]     (n_splits > 1): natural-log LSE_s of each
-                         //                          value half (the halves' scores agree to
-                         //                          fp32 rounding)
-    unsigned int* merge_count;  // one arrival counter per (b, ht, r) group when the last CTA
-                                // of a group merges its splits (2..kMlaMaxFusedSplits), else
-                                // nullptr (the merge kernel runs); left at zero by every launch
+    // 2..kMlaMaxClusterSplits splits: the n_splits CTAs of a (b, ht, r) group form a cluster and
+    // merge through distributed shared memory (no workspace); more: the workspace below and
+    // mla_merge_kernel.
+    int cluster_merge;
+    float* ws_o;         // [n_splits, B, H, 512]   (n_splits > kMlaMaxClusterSplits): O_s = acc / l
+    float* ws_lse;       // [n_splits, B, H]        (idem): natural-log LSE_s
     int stall_tile;  // test hook: >= 0 withholds the X panels of this token tile (else -1)
 };
 
@@ -93,10 +92,13 @@ struct MlaSmem {
     static constexpr int kNumBars = kBarPvDone + 1;
     static constexpr int kTmemSlot = kBars + kNumBars * 8;
     static constexpr int kAbort = kTmemSlot + 8;
-    static constexpr int kMergeFlag = kAbort + 4;  // this CTA merges its group
     static constexpr int kBytes = kAbort + 8;
     static constexpr int kAlloc = kBytes + 1024;
     static_assert(kStage + 5 * kQPanel <= kBars, "staging must fit in the last Y buffer + X ring");
+    // cluster merge: each row's LSE_s beside the staged O_s (the X ring is idle by then)
+    static constexpr int kLseStage = kX;
+    static_assert(kLseStage >= 4 * 32768 && kLseStage + kMlaHeads * 4 <= kBars,
+                  "the staged LSE must not overlap the staged O");
     static_assert(kAlloc <= 232448, "MLA shared memory exceeds the per-block limit");
 };
 
@@ -109,63 +111,70 @@ __device__ __forceinline__ int mla_x_panel(int r, int x) {
     return x == 4 ? 8 : (r == 0 ? 4 + x : x);
 }
 
-// The merge of section 2.4's split-T inside the decode kernel, by the last CTA of a (b, ht, r)
-// group: warp w combines head rows h0 .. h0+31 of value half r over the token splits,
-// LSE = M + ln sum_s exp(LSE_s - M) and out_c = sum_s exp(LSE_s - LSE) O_s, from the partials the
-// group's CTAs left in L2 (read past L1, which does not see other SMs' stores).  Each lane first
-// forms the weights of its own row; per row, lane i then reads columns 4i..4i+3 and 128+4i..+3
-// of every split (1 KiB per split and row, coalesced) and writes them as bf16.
-__device__ __forceinline__ void mla_merge_warp(const MlaParams& p, int b, int ht, int r, int warp,
-                                               int lane) {
-    const size_t BH = static_cast<size_t>(p.B) * p.H;
-    const int h0 = ht * kMlaHeads + warp * 32;
-    float wt[kMlaMaxFusedSplits];
-    float lse_m = 0.f;
-    {
-        float ls[kMlaMaxFusedSplits];
-        float mx = -INFINITY;
-        const size_t bh = static_cast<size_t>(b) * p.H + min(h0 + lane, p.H - 1);
+// The merge of section 2.4's split-T inside a thread-block cluster: the n_splits CTAs of a
+// (b, ht, r) group are one cluster, each has staged its O_s = acc / l (fp32; row rr of warp w at
+// w * 32 KiB + rr KiB, 16-byte chunk ch at (ch ^ rr) * 16) and its LSE_s (kLseStage[row]) in its
+// own shared memory, and CTA s combines rows s*R .. s*R + R - 1 of the 128-row tile (R = 128 /
+// n_splits, rounded up) by reading every CTA's staging through distributed shared memory:
+// LSE = M + ln sum_s exp(LSE_s - M) and out_c = sum_s exp(LSE_s - LSE) O_s.  A warp takes a row at
+// a time, lane i columns 4i..4i+3 and 128+4i..+3.  If a CTA of the cluster gave up (its abort
+// flag), nothing is merged; its expiry is in the status word.
+__device__ __forceinline__ void mla_cluster_merge(const MlaParams& p, uint32_t sbase, int b,
+                                                  int ht, int r, int rank, int warp, int lane) {
+    using L = MlaSmem;
+    const int ns = p.n_splits;
+    uint32_t peer[kMlaMaxClusterSplits];
+    bool aborted = false;
 #pragma unroll
-        for (int s = 0; s < kMlaMaxFusedSplits; ++s) {
-            ls[s] = s < p.n_splits
-                ? __ldcg(p.ws_lse + (static_cast<size_t>(r) * p.n_splits + s) * BH + bh)
-                : -INFINITY;
+    for (int s = 0; s < kMlaMaxClusterSplits; ++s) {
+        peer[s] = s < ns ? dsmem_addr(sbase, static_cast<uint32_t>(s)) : 0u;
+        if (s < ns) aborted |= ld_dsmem_u32(peer[s] + L::kAbort) != 0u;
+    }
+    if (aborted) return;
+    const int per = (kMlaHeads + ns - 1) / ns;
+    const int row_end = min((rank + 1) * per, kMlaHeads);
+    for (int row = rank * per + warp; row < row_end; row += 4) {
+        const int h = ht * kMlaHeads + row;
+        if (h >= p.H) break;  // warp-uniform; later rows are past H too
+        float ls[kMlaMaxClusterSplits];
+        float mx = -INFINITY;
+#pragma unroll
+        for (int s = 0; s < kMlaMaxClusterSplits; ++s) {
+            ls[s] = s < ns ? __uint_as_float(ld_dsmem_u32(peer[s] + L::kLseStage + row * 4))
+                           : -INFINITY;
             mx = fmaxf(mx, ls[s]);
         }
         float sum = 0.f;
 #pragma unroll
-        for (int s = 0; s < kMlaMaxFusedSplits; ++s) {
-            wt[s] = s < p.n_splits ? __expf(ls[s] - mx) : 0.f;
-            sum += wt[s];
+        for (int s = 0; s < kMlaMaxClusterSplits; ++s) {
+            ls[s] = s < ns ? __expf(ls[s] - mx) : 0.f;
+            sum += ls[s];
         }
         const float inv = 1.0f / sum;
-#pragma unroll
-        for (int s = 0; s < kMlaMaxFusedSplits; ++s) wt[s] *= inv;
-        lse_m = mx + __logf(sum);
-    }
-#pragma unroll 4
-    for (int rr = 0; rr < 32; ++rr) {
-        if (h0 + rr >= p.H) break;  // warp-uniform
-        const size_t bh_r = static_cast<size_t>(b) * p.H + h0 + rr;
+        const int rr = row & 31;
+        const uint32_t off = static_cast<uint32_t>((row >> 5) * 32768 + rr * 1024);
         float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
 #pragma unroll
-        for (int s = 0; s < kMlaMaxFusedSplits; ++s) {
-            const float w = __shfl_sync(0xffffffffu, wt[s], rr);
-            if (s < p.n_splits) {
-                const float4* src = reinterpret_cast<const float4*>(
-                    p.ws_o + (static_cast<size_t>(s) * BH + bh_r) * kMlaDc + r * 256);
-                const float4 v0 = __ldcg(src + lane), v1 = __ldcg(src + 32 + lane);
-                a0.x += w * v0.x; a0.y += w * v0.y; a0.z += w * v0.z; a0.w += w * v0.w;
-                a1.x += w * v1.x; a1.y += w * v1.y; a1.z += w * v1.z; a1.w += w * v1.w;
+        for (int s = 0; s < kMlaMaxClusterSplits; ++s) {
+            if (s < ns) {
+                const float w = ls[s] * inv;
+                uint32_t x0, x1, x2, x3, y0, y1, y2, y3;
+                ld_dsmem_v4(peer[s] + off + ((lane ^ rr) << 4), x0, x1, x2, x3);
+                ld_dsmem_v4(peer[s] + off + (((lane + 32) ^ rr) << 4), y0, y1, y2, y3);
+                a0.x += w * __uint_as_float(x0); a0.y += w * __uint_as_float(x1);
+                a0.z += w * __uint_as_float(x2); a0.w += w * __uint_as_float(x3);
+                a1.x += w * __uint_as_float(y0); a1.y += w * __uint_as_float(y1);
+                a1.z += w * __uint_as_float(y2); a1.w += w * __uint_as_float(y3);
             }
         }
-        __nv_bfloat16* dst = p.out + bh_r * kMlaDc + r * 256;
+        const size_t bh = static_cast<size_t>(b) * p.H + h;
+        __nv_bfloat16* dst = p.out + bh * kMlaDc + r * 256;
         *reinterpret_cast<uint2*>(dst + 4 * lane) =
             make_uint2(pack_bf16x2(a0.x, a0.y), pack_bf16x2(a0.z, a0.w));
         *reinterpret_cast<uint2*>(dst + 128 + 4 * lane) =
             make_uint2(pack_bf16x2(a1.x, a1.y), pack_bf16x2(a1.z, a1.w));
+        if (r == 0 && lane == 0) p.lse[bh] = mx + __logf(sum);
     }
-    if (r == 0 && h0 + lane < p.H) p.lse[static_cast<size_t>(b) * p.H + h0 + lane] = lse_m;
 }
 
 __global__ void __launch_bounds__(kMlaThreads, 1)
@@ -491,7 +500,8 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
             __syncwarp();
             const int row_bytes = chunks * 16;
             const int h0 = ht * kMlaHeads + warp * 32;  // this warp's first head
-            for (int rr = 0; rr < 32; ++rr) {
+            // (under the cluster merge the staged rows stay where they are)
+            for (int rr = 0; rr < (p.cluster_merge ? 0 : 32); ++rr) {
                 if (h0 + rr >= p.H) break;  // warp-uniform
                 const size_t bh_r = static_cast<size_t>(b) * p.H + h0 + rr;
                 uint8_t* dst = split_out
@@ -503,43 +513,28 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
                     *reinterpret_cast<uint4*>(dst + ch * 16) = make_uint4(a, b2, c2, d);
                 }
             }
-            if (h < p.H) {
+            if (p.cluster_merge) {
+                reinterpret_cast<float*>(smem + L::kLseStage)[row] = lse_nat;
+            } else if (h < p.H) {
                 const size_t bh = static_cast<size_t>(b) * p.H + h;
-                if (split_out)
-                    p.ws_lse[(static_cast<size_t>(r) * p.n_splits + split) * p.B * p.H + bh] =
-                        lse_nat;
-                else if (r == 0)
+                if (split_out && r == 0)
+                    p.ws_lse[static_cast<size_t>(split) * p.B * p.H + bh] = lse_nat;
+                else if (!split_out && r == 0)
                     p.lse[bh] = lse_nat;
             }
         }
         __syncwarp();
-        if (p.merge_count != nullptr) {
-            // Every CTA of a (b, ht, r) group publishes its partials and arrives on the group's
-            // counter (a CTA whose waits expired arrives marked); the last arrival resets the
-            // counter and, if no CTA of the group was marked, merges the group's splits.
-            __threadfence();
-            const bool all_ok = named_barrier_and(1, 128, ok);
-            volatile int* merge_flag = reinterpret_cast<volatile int*>(smem + L::kMergeFlag);
-            if (threadIdx.x == 0) {
-                unsigned int* cnt = p.merge_count + blockIdx.x / p.n_splits;
-                const unsigned int add = all_ok ? 1u : 0x10001u;
-                const unsigned int old = atomicAdd(cnt, add);
-                const bool last = (old & 0xffffu) == static_cast<unsigned int>(p.n_splits - 1);
-                if (last) atomicExch(cnt, 0u);
-                *merge_flag = (last && ((old + add) >> 16) == 0u) ? 1 : 0;
-            }
-            named_barrier_sync(1, 128);
-            if (*merge_flag) {
-                __threadfence();
-                mla_merge_warp(p, b, ht, r, warp, lane);
-            }
-        }
     }
     tc_fence_before();
     __syncthreads();
     if (warp == kMlaMmaA) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
+    }
+    if (p.cluster_merge) {
+        cluster_sync_all();  // every CTA of the cluster has staged its O_s and LSE_s (or gave up)
+        if (warp < 4) mla_cluster_merge(p, sbase, b, ht, r, split, warp, lane);
+        cluster_sync_all();  // no CTA leaves while another still reads its shared memory
     }
 }
 

@@ -246,6 +246,38 @@ struct ArmedPhases {
 };
 
 // ------------------------------------------------------------------------------------------------
+// Thread-block clusters: the cluster-wide barrier and distributed shared memory (a CTA reading
+// the shared memory of another CTA of its cluster).
+// ------------------------------------------------------------------------------------------------
+// Every thread of every CTA in the cluster arrives (release: its shared-memory writes become
+// visible to the cluster) and waits for all the others (acquire).  Warp-converged callers only.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+                 ::: "memory");
+}
+
+// The address, in the cluster's shared window, of shared address `addr` of CTA `rank`.
+__device__ __forceinline__ uint32_t dsmem_addr(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void ld_dsmem_v4(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c,
+                                            uint32_t& d) {
+    asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
+                 : "r"(addr)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_dsmem_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// ------------------------------------------------------------------------------------------------
 // TMA (tensor copies between global and shared memory); no multicast.
 // ------------------------------------------------------------------------------------------------
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {

@@ -80,7 +80,7 @@ typedef enum {
  * Scheduling: up to D = 128 the kernel is persistent (one CTA per SM); its CTAs claim work items
  * from a device counter that the library hands to each launch from a pool of 64 (round robin,
  * per device, shared with attn_fwd_strided, the split-KV entry points, the backward's dQ
- * kernel and attn_mla_decode's in-kernel merge).  Each launch returns its counter to zero, so launches in one stream, or on different
+ * kernel).  Each launch returns its counter to zero, so launches in one stream, or on different
  * streams, may follow each other freely; at most 64 such launches may be executing at the same
  * time on one device (a CUDA graph replays its launches' counters, so a graph must not run
  * concurrently with another replay of itself).
@@ -238,15 +238,16 @@ size_t attn_bwd_workspace_bytes(int B, int Hq, int N);
  *               Clamped to the number of 64-token tiles.  With one split the workspace is unused.
  *   workspace   device memory, 16-byte aligned, of at least
  *               attn_mla_decode_workspace_bytes(B, H, T, num_splits) bytes when that is nonzero
- *               (per-split fp32 partials and LSEs); owned by the caller, contents ignored.
+ *               (per-split fp32 partials and LSEs, needed above 4 splits); owned by the
+ *               caller, contents ignored.
  *   T >= 1 and H >= 1; B == 0 is a no-op.  Outputs, inputs and the workspace must not overlap.
  *   Pointers are device pointers of the current device, owned by the caller.
  *
  * Returns ATTN_OK once enqueued, else a negative attn_status_t and nothing is written.  One
- * kernel runs; with 2-4 splits the last CTA of each (batch, 128-head tile, value half) merges
- * the splits in it, through an arrival counter taken from the pool that attn_fwd's scheduling
- * paragraph describes (same limit on concurrent launches); with more splits a merge kernel
- * follows.  Device-side wait expiries go to attn_debug_status.
+ * kernel runs; with 2-4 splits the split CTAs of each (batch, 128-head tile, value half) form a
+ * thread-block cluster and merge through distributed shared memory; with more splits the
+ * partials go to the workspace and a merge kernel follows.  Device-side wait expiries go to
+ * attn_debug_status.
  */
 int attn_mla_decode(const void* q, const void* kv, void* out, float* lse, int B, int H, int T,
                     int d_c, int d_r, float sm_scale, int num_splits, void* workspace,
@@ -277,9 +278,9 @@ int attn_fwd_test_stall(const void* q, const void* k, const void* v, void* out, 
  *
  * The producer of every CTA whose token range holds 64-token tile `stall_tile` (>= 0) withholds
  * that tile's cache panels, so those CTAs' bounded waits expire after about one second and they
- * stop, free their tensor memory and return.  A split group with such a CTA is not merged: out
- * and lse hold garbage there, the status word records the expiry, the group's arrival counter is
- * still reset, and the next call computes correctly.  Use tiny problems.
+ * stop, free their tensor memory and return.  A cluster with such a CTA is not merged: out and
+ * lse hold garbage there, the status word records the expiry, and the next call computes
+ * correctly.  Use tiny problems.
  */
 int attn_mla_decode_test_stall(const void* q, const void* kv, void* out, float* lse, int B, int H,
                                int T, int d_c, int d_r, float sm_scale, int num_splits,

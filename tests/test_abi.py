@@ -156,16 +156,19 @@ def test_bwd_workspace_bytes(lib):
 
 
 def _mla(lib, q=S, kv=S * 2, out=S * 4, lse=S * 5, B=1, H=128, T=4096, d_c=512, d_r=64,
-         scale=192 ** -0.5, splits=4, ws=S * 8, ws_bytes=1 << 30):
+         scale=192 ** -0.5, splits=8, ws=S * 8, ws_bytes=1 << 30):
+    # 8 splits: above the cluster merge's 4, so the workspace is needed and checked
     return lib.attn_mla_decode(q, kv, out, lse, B, H, T, d_c, d_r, ctypes.c_float(scale), splits,
                                ws, ws_bytes, None)
 
 
 def test_mla_workspace_bytes(lib):
-    # n_splits * B * H * (512 + 2) fp32 (each split's O and both value halves' LSE), splits
-    # clamped to the 64-token tiles
-    assert lib.attn_mla_decode_workspace_bytes(2, 128, 4096, 4) == 4 * 2 * 128 * 514 * 4
-    assert lib.attn_mla_decode_workspace_bytes(1, 16, 100, 8) == 2 * 1 * 16 * 514 * 4
+    # above 4 splits n_splits * B * H * (512 + 1) fp32 (each split's O and LSE); 2-4 splits merge
+    # inside a cluster and need none; splits are clamped to the 64-token tiles
+    assert lib.attn_mla_decode_workspace_bytes(2, 128, 4096, 8) == 8 * 2 * 128 * 513 * 4
+    assert lib.attn_mla_decode_workspace_bytes(2, 128, 4096, 5) == 5 * 2 * 128 * 513 * 4
+    assert lib.attn_mla_decode_workspace_bytes(2, 128, 4096, 4) == 0
+    assert lib.attn_mla_decode_workspace_bytes(1, 16, 100, 8) == 0  # clamped to 2 splits
     assert lib.attn_mla_decode_workspace_bytes(1, 16, 64, 8) == 0  # one tile: no split
     assert lib.attn_mla_decode_workspace_bytes(1, 16, 4096, 1) == 0
     assert lib.attn_mla_decode_workspace_bytes(0, 16, 4096, 4) == 0

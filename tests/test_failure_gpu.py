@@ -60,11 +60,10 @@ def test_stall_item_past_the_end_stalls_nothing(cuda_lib):
     _check(out, lse, o_ref, l_ref, "stall item beyond the ring")
 
 
-def test_mla_expired_wait_skips_the_fused_merge_and_resets_its_counters(cuda_lib):
-    """MLA decode with two splits merged in the kernel: the CTAs of split 1 are starved of one
-    cache tile and time out.  Each group's last arrival must then skip the merge (out and lse
-    keep their zeros) but still reset its counter; 70 further launches bring every counter slot,
-    the stalled launch's included, round again and must all merge correctly."""
+def test_mla_expired_wait_skips_the_cluster_merge(cuda_lib):
+    """MLA decode with two splits merged inside a cluster: the CTAs of split 1 are starved of one
+    cache tile and time out.  Their clusters must then skip the merge (out and lse keep their
+    zeros), the expiry must reach the host, and 70 further launches must all merge correctly."""
     import exact_attention_forward_attn_gb300 as attn
     from test_mla_gpu import _check as mla_check
 

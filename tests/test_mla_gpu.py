@@ -2,7 +2,8 @@
 
 Element by element on seeded inputs: the DeepSeek-V3 widths (d_c = 512, d_r = 64, 128 heads),
 one decode query per head, with ragged token counts (tail tiles), head counts below and above one
-128-head tile, one token, and the token axis run whole or split (with the merge kernel).
+128-head tile, one token, and the token axis run whole or split (2-4 splits merged inside a thread-block
+cluster, more by the merge kernel).
 Tolerance as for the forward: |dO| <= 2e-2 + 2e-2 |O| elementwise, |dLSE| <= 1e-3.
 """
 import ctypes
@@ -107,12 +108,14 @@ def test_device_errors_are_reported(cuda_lib):
     assert st == -10  # host memory for q
 
 
-def test_fused_merge_counters_reused():
-    """With 2-4 splits the last CTA of each group merges in the decode kernel, through arrival
-    counters the library hands out round robin from a pool of 64 slots; 3 x 30 launches reuse
-    every slot, and each launch must give the bits of the first."""
+def test_cluster_merge_repeated_launches():
+    """With 2-4 splits the split CTAs of a group form a thread-block cluster and merge through
+    distributed shared memory: one head, a partial second head tile and 3 or 4 splits (rows
+    shared unevenly among the cluster's CTAs); 30 more launches of each must give the bits of
+    the first."""
     cases = [(wl.MLA_RAGGED, 2), (wl.MlaWorkload("mla-fuse-h1", 3, 1, 65, 96), 2),
-             (wl.MlaWorkload("mla-fuse-h200", 2, 200, 700, 97), 4)]
+             (wl.MlaWorkload("mla-fuse-h200", 2, 200, 700, 97), 4),
+             (wl.MlaWorkload("mla-fuse-h72", 1, 72, 1000, 99), 3)]
     data, first = [], []
     for w, splits in cases:
         q, kv, out, lse = _run(w, splits)
