@@ -695,6 +695,8 @@ int64_t mla_tiles(int T) { return (static_cast<int64_t>(T) + kMlaBN - 1) / kMlaB
 // 1.8 us): CTAs run in waves of one per SM, and a split run also writes each split's fp32
 // partial rows (2 KiB per head) and merges them, about 0.57 tile per thousand partial rows
 // plus half a tile for the merge launch.  The least costly count wins (fewest splits on ties).
+// (With 2-4 splits the merge runs inside a cluster and costs less than this; the model was
+// fitted to the global-memory merge and still picks the faster count at B = 16 and 32.)
 int mla_heuristic_splits(int64_t items, int64_t n_tiles, int64_t rows, int num_sms) {
     const int64_t max_s = std::min<int64_t>(n_tiles, kMaxSplits);
     int best = 1;
