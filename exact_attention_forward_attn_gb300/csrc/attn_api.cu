@@ -139,13 +139,13 @@ DeviceState g_devices[kMaxDevices];
 // Opt in to the large shared-memory carve-out, and check that the kernel was built with the
 // per-thread register count its setmaxnreg split assumes (a launch with fewer registers would
 // leave the softmax warpgroups waiting for registers that do not exist).
-template <int D, bool kSplit>
+template <int D, bool kSplit, bool kOne = false>
 cudaError_t opt_in_smem(bool* regs_ok) {
     cudaFuncAttributes a;
-    cudaError_t e = cudaFuncGetAttributes(&a, attn_fwd_kernel<D, kSplit>);
+    cudaError_t e = cudaFuncGetAttributes(&a, attn_fwd_kernel<D, kSplit, kOne>);
     if (e != cudaSuccess) return e;
     if (a.numRegs != kLaunchRegs) *regs_ok = false;
-    return cudaFuncSetAttribute(attn_fwd_kernel<D, kSplit>,
+    return cudaFuncSetAttribute(attn_fwd_kernel<D, kSplit, kOne>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 SmemLayout<D>::kAlloc);
 }
@@ -181,6 +181,8 @@ int device_state(int dev, DeviceState** out) {
         if (e == cudaSuccess) e = opt_in_smem<128, false>(&regs_ok);
         if (e == cudaSuccess) e = opt_in_smem<64, true>(&regs_ok);
         if (e == cudaSuccess) e = opt_in_smem<128, true>(&regs_ok);
+        if (e == cudaSuccess) e = opt_in_smem<64, false, true>(&regs_ok);
+        if (e == cudaSuccess) e = opt_in_smem<128, false, true>(&regs_ok);
         if (e == cudaSuccess) e = opt_in_bwd_smem<64>();
         if (e == cudaSuccess) e = opt_in_bwd_smem<128>();
         if (e == cudaSuccess)
@@ -356,27 +358,33 @@ int prepare(const Problem& P, DeviceState** ds, CUtensorMap* mq, CUtensorMap* mk
 
 // The persistent two-tile kernel: one CTA per SM (or per item, if fewer), each claiming items
 // until all `items` are taken.
-template <int D, bool kSplit>
+template <int D, bool kSplit, bool kOne = false>
 int launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                const AttnParams& p, unsigned int* status_word, int64_t items, int num_sms,
                cudaStream_t stream) {
     AttnParams prm = p;
     prm.items = static_cast<int>(items);
     const int64_t grid = std::min<int64_t>(items, std::max(1, num_sms));
-    attn_fwd_kernel<D, kSplit><<<static_cast<unsigned int>(grid), kThreads,
-                                 SmemLayout<D>::kAlloc, stream>>>(mq, mk, mv, prm, status_word);
+    attn_fwd_kernel<D, kSplit, kOne><<<static_cast<unsigned int>(grid), kThreads,
+                                       SmemLayout<D>::kAlloc, stream>>>(mq, mk, mv, prm,
+                                                                        status_word);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
 
-// The single-pass forward for head dimension D: two Q tiles per CTA up to D = 128, one above.
+// The single-pass forward for head dimension D: two Q tiles per work item up to D = 128 (one if
+// `one_tile`), one Q tile per CTA above.
 int launch_single(int D, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                   const CUtensorMap& mo, const AttnParams& p, unsigned int* status_word,
-                  int64_t grid, int num_sms, cudaStream_t stream) {
+                  int64_t grid, int num_sms, cudaStream_t stream, bool one_tile = false) {
     if (D <= 64)
-        return launch_fwd<64, false>(mq, mk, mv, p, status_word, grid, num_sms, stream);
+        return one_tile
+            ? launch_fwd<64, false, true>(mq, mk, mv, p, status_word, grid, num_sms, stream)
+            : launch_fwd<64, false>(mq, mk, mv, p, status_word, grid, num_sms, stream);
     if (D <= 128)
-        return launch_fwd<128, false>(mq, mk, mv, p, status_word, grid, num_sms, stream);
+        return one_tile
+            ? launch_fwd<128, false, true>(mq, mk, mv, p, status_word, grid, num_sms, stream)
+            : launch_fwd<128, false>(mq, mk, mv, p, status_word, grid, num_sms, stream);
     attn_fwd_d256_kernel<<<static_cast<unsigned int>(grid), kW256Threads, Fwd256Smem::kAlloc,
                            stream>>>(mq, mk, mv, mo, p, status_word);
     const cudaError_t e = cudaGetLastError();
@@ -425,6 +433,18 @@ int64_t workspace_bytes_for(int64_t bh, int64_t N, int64_t D, int n_splits) {
 
 }  // namespace
 
+// With fewer Q-tile pairs than half the SMs, one Q tile per work item, so that twice as many SMs
+// work: a pair hides the S -> softmax -> P.V latency of one tile behind the other's, but when
+// pairs would leave most SMs idle the extra SMs gain more.  (Single-pass launches only; the
+// split-KV path fills the SMs with splits instead.)
+static bool prefer_single_tiles(Problem& P, const DeviceState* ds, AttnParams* prm) {
+    if (P.D > 128 || P.n_tiles < 2 || 2 * P.items > ds->num_sms) return false;
+    prm->n_pairs = static_cast<int>(P.n_tiles);
+    P.items = P.n_tiles * P.bh;
+    prm->items = static_cast<int>(P.items);
+    return true;
+}
+
 extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B,
                         int Hq, int Hkv, int N, int D, int causal, float sm_scale, void* stream) {
     Problem P{q, k, v, out, lse, B, Hq, Hkv, N, D, causal, sm_scale};
@@ -436,8 +456,10 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* out, 
     AttnParams prm;
     st = prepare(P, &ds, &mq, &mk, &mv, &mo, &prm);
     if (st != ATTN_OK) return st;
+    const bool one_tile = prefer_single_tiles(P, ds, &prm);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return launch_single(D, mq, mk, mv, mo, prm, ds->status_word, P.items, ds->num_sms, s);
+    return launch_single(D, mq, mk, mv, mo, prm, ds->status_word, P.items, ds->num_sms, s,
+                         one_tile);
 }
 
 extern "C" int attn_fwd_strided(const void* q, const void* k, const void* v, void* out,
@@ -461,8 +483,10 @@ extern "C" int attn_fwd_strided(const void* q, const void* k, const void* v, voi
     AttnParams prm;
     st = prepare(P, &ds, &mq, &mk, &mv, &mo, &prm);
     if (st != ATTN_OK) return st;
+    const bool one_tile = prefer_single_tiles(P, ds, &prm);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return launch_single(D, mq, mk, mv, mo, prm, ds->status_word, P.items, ds->num_sms, s);
+    return launch_single(D, mq, mk, mv, mo, prm, ds->status_word, P.items, ds->num_sms, s,
+                         one_tile);
 }
 
 extern "C" int attn_fwd_test_stall(const void* q, const void* k, const void* v, void* out,

@@ -74,7 +74,7 @@ struct AttnParams {
     int group;         // Hq / Hkv
     int causal;
     int n_tiles;       // ceil(N / 128): number of Q tiles and of KV tiles per head
-    int n_pairs;       // ceil(n_tiles / 2): work items per (b, hq)
+    int n_pairs;       // work items per (b, hq): ceil(n_tiles / 2), or n_tiles with one Q tile each
     float scale_log2;  // sm_scale * log2(e)
     int kv_block;      // (batch, KV head) pairs per scheduling block (their K/V fit in L2)
     float* lse;        // [B, Hq, N] fp32
@@ -147,7 +147,7 @@ struct FwdWork {
 // block, Q-tile pairs heaviest (latest) first, then the KV heads, then the query heads sharing
 // each KV head.  Items are claimed in this order, so the CTAs working at any time read K/V of one
 // block (which stays in L2), and every block (and so the launch) ends on its lightest causal pairs.
-template <bool kSplit>
+template <bool kSplit, bool kOne>
 __device__ __forceinline__ FwdWork decode_work(const AttnParams& p, int item) {
     FwdWork w;
     w.split = 0;
@@ -166,7 +166,7 @@ __device__ __forceinline__ FwdWork decode_work(const AttnParams& p, int item) {
     w.hkv = bh_kv % p.Hkv;
     w.hq = w.hkv * p.group + rem;
     w.bh = w.b * p.Hq + w.hq;
-    w.tile0 = 2 * pair;
+    w.tile0 = kOne ? pair : 2 * pair;
     // Each Q tile t uses [kv_begin, last_t]; under the causal mask its last tile is its diagonal
     // (BM == BN, so it has the Q tile's index).  A Q tile takes part if that range is not empty
     // (always, unless a later split starts past it).
@@ -175,7 +175,7 @@ __device__ __forceinline__ FwdWork decode_work(const AttnParams& p, int item) {
     w.last0 = min(kv_limit - 1, p.causal ? w.tile0 : p.n_tiles - 1);
     w.last1 = min(kv_limit - 1, p.causal ? w.tile0 + 1 : p.n_tiles - 1);
     w.part0 = w.last0 >= w.kv_begin;
-    w.part1 = w.tile0 + 1 < p.n_tiles && w.last1 >= w.kv_begin;
+    w.part1 = !kOne && w.tile0 + 1 < p.n_tiles && w.last1 >= w.kv_begin;
     w.kv_end = (w.part1 ? w.last1 : w.last0) + 1;
     return w;
 }
@@ -184,7 +184,9 @@ __device__ __forceinline__ FwdWork decode_work(const AttnParams& p, int item) {
 // kSplit = true:  the KV range of one split (split index innermost in the item number); the fp32
 //                 O of that range (normalised by its own denominator) and its LSE go to the
 //                 workspace, and attn_splitkv_merge_kernel combines the splits.
-template <int D, bool kSplit>
+// kOne = true:    one Q tile per work item (the second tile's issuer and softmax group idle),
+//                 for launches whose pairs would leave most SMs idle.
+template <int D, bool kSplit, bool kOne = false>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
                     const __grid_constant__ CUtensorMap tmap_k,
@@ -309,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     item = read_item(k, false);
                 }
                 if (item < 0) break;
-                const FwdWork w = decode_work<kSplit>(p, item);
+                const FwdWork w = decode_work<kSplit, kOne>(p, item);
                 if (!(w.part0 || w.part1)) continue;
                 {  // K (kv = 0) or V (kv = 1), panel h
                     const int kv = lane / kPanels, h = lane % kPanels;
@@ -397,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; ok; ++k) {
             const int item = read_item(k, true);
             if (item < 0) break;
-            const FwdWork w = decode_work<kSplit>(p, item);
+            const FwdWork w = decode_work<kSplit, kOne>(p, item);
             if (!(w.part0 || w.part1)) continue;
             const bool part = t == 0 ? w.part0 : w.part1;
             const int last = part ? (t == 0 ? w.last0 : w.last1) : w.kv_begin - 1;
@@ -496,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int n, lim, tok_until;
             bool mask_last;
             {
-                const FwdWork w = decode_work<kSplit>(p, item);
+                const FwdWork w = decode_work<kSplit, kOne>(p, item);
                 if (!(t == 0 ? w.part0 : w.part1)) continue;
                 const bool pingpong = w.part0 && w.part1;
                 const int q_tile = w.tile0 + t;
@@ -643,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             // The epilogue's coordinates, decoded again from an opaque copy of the item number so
             // that they are not kept in registers through the step loop.
-            const FwdWork we = decode_work<kSplit>(p, opaque_int(item));
+            const FwdWork we = decode_work<kSplit, kOne>(p, opaque_int(item));
             const int row_g = (we.tile0 + t) * kBM + row;
             const float inv_l = 1.0f / l;
             if constexpr (kSplit) {
