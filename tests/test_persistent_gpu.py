@@ -140,3 +140,25 @@ def test_cuda_graph_replays(cuda_lib):
         assert torch.equal(oa, ref_a[0]) and torch.equal(la, ref_a[1])
         assert torch.equal(ob, ref_b[0]) and torch.equal(lb, ref_b[1])
     assert attn.device_status(dev) == 0
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+def test_one_tile_items_match_pairs(causal, cuda_lib):
+    """A launch with few Q-tile pairs runs one Q tile per work item; the same heads inside a
+    larger batch run as pairs.  Each tile's arithmetic is the same either way, so the first
+    batch's outputs must be bit-identical."""
+    import exact_attention_forward_attn_gb300 as attn
+
+    dev = torch.device("cuda:0")
+    small = wl.Workload("one-tile-n640", 1, 8, 2, 640, 128, causal, 45)  # 24 pairs < SMs / 2
+    big = wl.Workload("pairs-n640", 8, 8, 2, 640, 128, causal, 46)       # 192 pairs
+    q1, k1, v1 = wl.make_qkv(small)
+    qb, kb, vb = wl.make_qkv(big)
+    qb[0], kb[0], vb[0] = q1[0], k1[0], v1[0]
+    o1, l1 = attn.attn_fwd(q1.to(dev), k1.to(dev), v1.to(dev), causal=causal)
+    ob, lb = attn.attn_fwd(qb.to(dev), kb.to(dev), vb.to(dev), causal=causal)
+    torch.cuda.synchronize()
+    assert torch.equal(o1[0], ob[0]) and torch.equal(l1[0], lb[0])
+    o_ref, l_ref = oracle.attn_ref(q1, k1, v1, causal, small.sm_scale)
+    _check(o1, l1, o_ref, l_ref, small.name)
+    assert attn.device_status(dev) == 0
