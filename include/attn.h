@@ -77,7 +77,9 @@ typedef enum {
  *
  * Returns ATTN_OK once the kernel is enqueued on `stream`, else a negative attn_status_t.
  *
- * Scheduling: up to D = 128 the kernel is persistent (one CTA per SM); its CTAs claim work items
+ * Scheduling: up to D = 128 the kernel is persistent (one CTA per SM); a work item is a pair of
+ * 128-row Q tiles of one head, or a single Q tile when pairs would leave more than half of the
+ * SMs idle (the results are the same bits either way).  Its CTAs claim work items
  * from a device counter that the library hands to each launch from a pool of 64 (round robin,
  * per device, shared with attn_fwd_strided, the split-KV entry points, the backward's dQ
  * kernel).  Each launch returns its counter to zero, so launches in one stream, or on different
