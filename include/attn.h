@@ -81,7 +81,7 @@ typedef enum {
  * 128-row Q tiles of one head, or a single Q tile when pairs would leave more than half of the
  * SMs idle (the results are the same bits either way).  Its CTAs claim work items
  * from a device counter that the library hands to each launch from a pool of 64 (round robin,
- * per device, shared with attn_fwd_strided, the split-KV entry points, the backward's dQ
+ * per device, shared with attn_fwd_strided, the split-KV entry points and the backward's dQ
  * kernel).  Each launch returns its counter to zero, so launches in one stream, or on different
  * streams, may follow each other freely; at most 64 such launches may be executing at the same
  * time on one device (a CUDA graph replays its launches' counters, so a graph must not run
