@@ -28,6 +28,10 @@
 //   have read it, so loads run 2.4 tiles ahead).  The TMEM-bound Q panels are staged through the
 //   second Y buffer and the X ring at start.
 // Warps: 0-3 softmax (one head row per thread), 4 issues S, 5 issues P.V, 6 loads.
+// Token splits: with 2..kMlaMaxClusterSplits splits the split CTAs of one (batch, head tile,
+// value half) are a thread-block cluster and combine their partial outputs through distributed
+// shared memory at the end (mla_cluster_merge); with more, the partials go to a global workspace
+// and mla_merge_kernel combines them.
 #pragma once
 
 #include <cuda.h>
