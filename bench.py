@@ -199,6 +199,63 @@ def time_oracle(w, q, k, v, seconds_target: float, max_rows: int = 4096):
     return n, rate
 
 
+def causal_work(w, rows=None) -> float:
+    """Visible (query, key) pairs of workload w, over all rows or over the sampled `rows`
+    [B, Hq, R] (under the causal mask row i sees i + 1 keys)."""
+    if rows is None:
+        per_head = w.N * (w.N + 1) / 2 if w.causal else float(w.N) * w.N
+        return per_head * w.B * w.Hq
+    if w.causal:
+        return float((rows.long() + 1).sum().item())
+    return float(rows.numel()) * w.N
+
+
+def cpu_baseline_table(gpu_us=None):
+    """The oracle as it stands, timed on the host cores at all cores and at one core: the five
+    configurations in full (one-core C3, 0.27 TFLOP, on 128 seeded rows per head, extrapolated),
+    the long-context lengths on the 64 seeded rows per head the parity tests compare,
+    extrapolated to every row by the exact work ratio (visible query-key pairs), labelled."""
+    import oracle
+    from exact_attention_forward_attn_gb300 import workloads as wl
+
+    all_cores = oracle.default_threads()
+    table = []
+
+    def timed(fn, repeats):
+        ts = []
+        for _ in range(repeats):
+            t0 = time.perf_counter()
+            fn()
+            ts.append(time.perf_counter() - t0)
+        return statistics.median(ts)
+
+    for w in (wl.TINY_NONCAUSAL, wl.TINY_CAUSAL, wl.GQA4_CAUSAL, wl.GQA8_CAUSAL, wl.MHA,
+              wl.MHA_OUTLIER, wl.MQA, *wl.LONG.values()):
+        q, k, v = wl.make_qkv(w)
+        entry = {"workload": w.name, "gflop": w.flops / 1e9}
+        for label, threads in (("all_cores", all_cores), ("one_core", 1)):
+            long_cfg = w.N > 4096
+            if long_cfg or (threads == 1 and w.flops > 1e11):
+                rows = wl.sample_rows(w, 64 if long_cfg else 128)
+                dt = timed(lambda: oracle.attn_ref(q, k, v, w.causal, w.sm_scale,
+                                                   rows=rows.numpy(), n_threads=threads), 1)
+                scale = causal_work(w) / causal_work(w, rows)
+                entry[label] = {"s": dt * scale, "kind": "extrapolated",
+                                "sample": f"{rows.shape[2]} seeded rows per head, {dt:.2f} s"}
+            else:
+                reps = 3 if w.flops < 2e10 else 1
+                dt = timed(lambda: oracle.attn_ref(q, k, v, w.causal, w.sm_scale,
+                                                   n_threads=threads), reps)
+                entry[label] = {"s": dt, "kind": "full"}
+            entry[label]["cores"] = threads
+            entry[label]["tflops"] = w.flops / entry[label]["s"] / 1e12
+        if gpu_us and w.name in gpu_us:
+            entry["gpu_us"] = gpu_us[w.name]
+            entry["speedup_vs_all_cores"] = entry["all_cores"]["s"] * 1e6 / gpu_us[w.name]
+        table.append(entry)
+    return table
+
+
 def run_reference(args, w):
     """The reference arm: the fp64 CPU oracle as it stands, on the host cores."""
     import oracle
@@ -347,7 +404,7 @@ def main():
                     help="with --profile: which path --workload names (backward: the three "
                          "backward kernels on a forward workload; mla: an MLA decode workload)")
     ap.add_argument("--no-sweep", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+    ap.add_argument("--cpu-seconds", type=float, default=8.0,
                     help="target duration of the oracle's bounded CPU-baseline sample")
     ap.add_argument("--ref-step-seconds", type=float, default=1.0,
                     help="target duration of one reference-arm step")
@@ -672,6 +729,7 @@ def main():
 
     # ---- CPU baseline: the oracle as it stands, bounded sample, rank 0 at N=1 only -----------
     cpu = None
+    cpu_table = []
     if rank == 0 and world == 1:
         import oracle
 
@@ -686,6 +744,10 @@ def main():
                "kind": "oracle",
                "sample": f"{n_rows} seeded query rows per head x {w.B * w.Hq} heads of {w.name}; "
                          f"{f / 1e9:.2f} GFLOP in {dt:.1f} s"}
+        if not args.no_sweep:
+            gpu_us = {c["workload"]: c["us"] for c in configs}
+            gpu_us.update({f"long-gqa8-causal-n{x['N']}": x["ms"] * 1e3 for x in sweep})
+            cpu_table = cpu_baseline_table(gpu_us)
 
     if rank == 0:
         line = {
@@ -696,7 +758,7 @@ def main():
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": args.steps, "clocks": clocks, "configs": configs, "sweep": sweep,
             "low_occupancy": low_occ, "wide_heads": wide, "backward": backward,
-            "mla_decode": mla,
+            "mla_decode": mla, "cpu_baseline_table": cpu_table,
             "kernel_sha": kernel_hash(),
         }
         print(json.dumps(line), flush=True)

@@ -26,8 +26,8 @@ using namespace gb300attn;
 
 // Device status word: kernels OR failure flags into it (see attn_debug_status).
 __device__ unsigned int g_attn_status_word = 0;
-// Claim counters of the persistent forward kernel, handed to launches round robin (so up to
-// kSchedSlots launches may run at once on a device); each launch leaves its counter at zero.
+// Claim counters of the persistent kernels, handed to launches round robin; each launch leaves
+// its counter at zero, and a launch that reuses a counter waits for the counter's previous launch.
 __device__ unsigned int g_fwd_sched[gb300attn::kSchedSlots] = {};
 
 namespace {
@@ -123,6 +123,13 @@ bool cached_tile_map(CUtensorMap* map, const void* base, int64_t B, int64_t H, i
     return true;
 }
 
+// One claim counter and the completion event of the last launch that used it.
+struct SchedSlot {
+    std::mutex lock;           // held from the wait on `done` until `done` is recorded again
+    cudaEvent_t done = nullptr;
+    bool recorded = false;
+};
+
 // Per-device one-time set-up: architecture check, SM count, status-word address, smem opt-in.
 constexpr int kMaxDevices = 64;
 struct DeviceState {
@@ -133,6 +140,7 @@ struct DeviceState {
     unsigned int* status_word = nullptr;
     unsigned int* sched = nullptr;  // g_fwd_sched
     std::atomic<unsigned int> sched_next{0};
+    SchedSlot slots[kSchedSlots];
 };
 DeviceState g_devices[kMaxDevices];
 
@@ -350,9 +358,43 @@ int prepare(const Problem& P, DeviceState** ds, CUtensorMap* mq, CUtensorMap* mk
     prm->o_sh = P.so.h;
     prm->o_sn = P.so.n;
     prm->d_out = P.D;
-    const unsigned int slot =
-        (*ds)->sched_next.fetch_add(1u, std::memory_order_relaxed) % kSchedSlots;
-    prm->sched = (*ds)->sched + slot;
+    prm->sched = nullptr;  // set by with_claim_counter around the launch
+    return ATTN_OK;
+}
+
+// Runs launch(counter) with a claim counter that no other executing launch holds.  The counter
+// is one of the device's kSchedSlots, taken round robin; the stream first waits for the event
+// recorded after the counter's previous launch, so two launches that share a counter never run
+// at the same time, however many streams or host threads launch.  The slot's lock is held until
+// that event is recorded again, so two host threads never interleave on one slot.  While the
+// stream is being captured into a CUDA graph the host cannot order the graph's future replays
+// against other launches, so a captured launch gets no counter (nullptr) and the kernel uses its
+// static schedule.
+template <class Launch>
+int with_claim_counter(DeviceState* ds, cudaStream_t s, Launch&& launch) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(s, &cap);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (cap != cudaStreamCaptureStatusNone) return launch(static_cast<unsigned int*>(nullptr));
+    const unsigned int idx = ds->sched_next.fetch_add(1u, std::memory_order_relaxed) % kSchedSlots;
+    SchedSlot& slot = ds->slots[idx];
+    std::lock_guard<std::mutex> guard(slot.lock);
+    if (slot.done == nullptr) {
+        e = cudaEventCreateWithFlags(&slot.done, cudaEventDisableTiming);
+        if (e != cudaSuccess) {
+            slot.done = nullptr;
+            return cuda_fail(e);
+        }
+    }
+    if (slot.recorded) {
+        e = cudaStreamWaitEvent(s, slot.done, 0);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    const int st = launch(ds->sched + idx);
+    if (st != ATTN_OK) return st;
+    e = cudaEventRecord(slot.done, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    slot.recorded = true;
     return ATTN_OK;
 }
 
@@ -360,33 +402,33 @@ int prepare(const Problem& P, DeviceState** ds, CUtensorMap* mq, CUtensorMap* mk
 // until all `items` are taken.
 template <int D, bool kSplit, bool kOne = false>
 int launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-               const AttnParams& p, unsigned int* status_word, int64_t items, int num_sms,
-               cudaStream_t stream) {
+               const AttnParams& p, DeviceState* ds, int64_t items, cudaStream_t stream) {
     AttnParams prm = p;
     prm.items = static_cast<int>(items);
-    const int64_t grid = std::min<int64_t>(items, std::max(1, num_sms));
-    attn_fwd_kernel<D, kSplit, kOne><<<static_cast<unsigned int>(grid), kThreads,
-                                       SmemLayout<D>::kAlloc, stream>>>(mq, mk, mv, prm,
-                                                                        status_word);
-    const cudaError_t e = cudaGetLastError();
-    return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+    const int64_t grid = std::min<int64_t>(items, std::max(1, ds->num_sms));
+    return with_claim_counter(ds, stream, [&](unsigned int* counter) {
+        prm.sched = counter;
+        attn_fwd_kernel<D, kSplit, kOne><<<static_cast<unsigned int>(grid), kThreads,
+                                           SmemLayout<D>::kAlloc, stream>>>(mq, mk, mv, prm,
+                                                                            ds->status_word);
+        const cudaError_t e = cudaGetLastError();
+        return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+    });
 }
 
 // The single-pass forward for head dimension D: two Q tiles per work item up to D = 128 (one if
 // `one_tile`), one Q tile per CTA above.
 int launch_single(int D, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                  const CUtensorMap& mo, const AttnParams& p, unsigned int* status_word,
-                  int64_t grid, int num_sms, cudaStream_t stream, bool one_tile = false) {
+                  const CUtensorMap& mo, const AttnParams& p, DeviceState* ds, int64_t grid,
+                  cudaStream_t stream, bool one_tile = false) {
     if (D <= 64)
-        return one_tile
-            ? launch_fwd<64, false, true>(mq, mk, mv, p, status_word, grid, num_sms, stream)
-            : launch_fwd<64, false>(mq, mk, mv, p, status_word, grid, num_sms, stream);
+        return one_tile ? launch_fwd<64, false, true>(mq, mk, mv, p, ds, grid, stream)
+                        : launch_fwd<64, false>(mq, mk, mv, p, ds, grid, stream);
     if (D <= 128)
-        return one_tile
-            ? launch_fwd<128, false, true>(mq, mk, mv, p, status_word, grid, num_sms, stream)
-            : launch_fwd<128, false>(mq, mk, mv, p, status_word, grid, num_sms, stream);
+        return one_tile ? launch_fwd<128, false, true>(mq, mk, mv, p, ds, grid, stream)
+                        : launch_fwd<128, false>(mq, mk, mv, p, ds, grid, stream);
     attn_fwd_d256_kernel<<<static_cast<unsigned int>(grid), kW256Threads, Fwd256Smem::kAlloc,
-                           stream>>>(mq, mk, mv, mo, p, status_word);
+                           stream>>>(mq, mk, mv, mo, p, ds->status_word);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
@@ -458,8 +500,7 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* out, 
     if (st != ATTN_OK) return st;
     const bool one_tile = prefer_single_tiles(P, ds, &prm);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return launch_single(D, mq, mk, mv, mo, prm, ds->status_word, P.items, ds->num_sms, s,
-                         one_tile);
+    return launch_single(D, mq, mk, mv, mo, prm, ds, P.items, s, one_tile);
 }
 
 extern "C" int attn_fwd_strided(const void* q, const void* k, const void* v, void* out,
@@ -485,8 +526,7 @@ extern "C" int attn_fwd_strided(const void* q, const void* k, const void* v, voi
     if (st != ATTN_OK) return st;
     const bool one_tile = prefer_single_tiles(P, ds, &prm);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return launch_single(D, mq, mk, mv, mo, prm, ds->status_word, P.items, ds->num_sms, s,
-                         one_tile);
+    return launch_single(D, mq, mk, mv, mo, prm, ds, P.items, s, one_tile);
 }
 
 extern "C" int attn_fwd_test_stall(const void* q, const void* k, const void* v, void* out,
@@ -505,10 +545,8 @@ extern "C" int attn_fwd_test_stall(const void* q, const void* k, const void* v, 
     if (st != ATTN_OK) return st;
     prm.stall_item = stall_item;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return D <= 64 ? launch_fwd<64, false>(mq, mk, mv, prm, ds->status_word, P.items,
-                                           ds->num_sms, s)
-                   : launch_fwd<128, false>(mq, mk, mv, prm, ds->status_word, P.items,
-                                            ds->num_sms, s);
+    return D <= 64 ? launch_fwd<64, false>(mq, mk, mv, prm, ds, P.items, s)
+                   : launch_fwd<128, false>(mq, mk, mv, prm, ds, P.items, s);
 }
 
 extern "C" int attn_fwd_splitkv_num_splits(int B, int Hq, int N, int D, int causal) {
@@ -574,8 +612,8 @@ extern "C" int attn_fwd_splitkv(const void* q, const void* k, const void* v, voi
     prm.ws_lse = prm.ws_o + static_cast<int64_t>(n_splits) * P.bh * N * padded_dim(D);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int64_t items = P.items * n_splits;
-    st = D <= 64 ? launch_fwd<64, true>(mq, mk, mv, prm, ds->status_word, items, ds->num_sms, s)
-                 : launch_fwd<128, true>(mq, mk, mv, prm, ds->status_word, items, ds->num_sms, s);
+    st = D <= 64 ? launch_fwd<64, true>(mq, mk, mv, prm, ds, items, s)
+                 : launch_fwd<128, true>(mq, mk, mv, prm, ds, items, s);
     if (st != ATTN_OK) return st;
     auto* o = static_cast<__nv_bfloat16*>(out);
     return D <= 64 ? launch_merge<64>(prm, o, D, s) : launch_merge<128>(prm, o, D, s);
@@ -589,8 +627,11 @@ namespace {
 template <int D>
 int launch_bwd(const Problem& P, const CUtensorMap& mq, const CUtensorMap& mk,
                const CUtensorMap& mv, const CUtensorMap& mdo, const CUtensorMap& mdk,
-               const CUtensorMap& mdv, const BwdParams& bp, const void* out, const void* dout,
-               float* delta, unsigned int* status_word, int num_sms, cudaStream_t s) {
+               const CUtensorMap& mdv, const BwdParams& bp_in, const void* out, const void* dout,
+               float* delta, DeviceState* ds, cudaStream_t s) {
+    BwdParams bp = bp_in;
+    unsigned int* status_word = ds->status_word;
+    const int num_sms = ds->num_sms;
     const long long rows = P.bh * P.N;
     attn_bwd_delta_kernel<<<static_cast<unsigned int>((rows + 7) / 8), 256, 0, s>>>(
         static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), delta,
@@ -603,10 +644,13 @@ int launch_bwd(const Problem& P, const CUtensorMap& mq, const CUtensorMap& mk,
     if (e != cudaSuccess) return cuda_fail(e);
     // persistent: one CTA per SM (or per item, if fewer)
     const int64_t dq_grid = std::min<int64_t>(bp.items, std::max(1, num_sms));
-    attn_bwd_dq_kernel<D><<<static_cast<unsigned int>(dq_grid), kBwdThreads, DqSmem<D>::kAlloc,
-                            s>>>(mq, mk, mv, mdo, bp, status_word);
-    e = cudaGetLastError();
-    return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+    return with_claim_counter(ds, s, [&](unsigned int* counter) {
+        bp.sched = counter;
+        attn_bwd_dq_kernel<D><<<static_cast<unsigned int>(dq_grid), kBwdThreads,
+                                DqSmem<D>::kAlloc, s>>>(mq, mk, mv, mdo, bp, status_word);
+        const cudaError_t e2 = cudaGetLastError();
+        return e2 == cudaSuccess ? ATTN_OK : cuda_fail(e2);
+    });
 }
 
 }  // namespace
@@ -676,15 +720,13 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
     bp.delta = static_cast<const float*>(workspace);
     if (P.n_tiles * P.bh > 0x7fffffffLL) return ATTN_ERR_SHAPE;
     bp.items = static_cast<int>(P.n_tiles * P.bh);
-    bp.sched = prm.sched;
+    bp.sched = nullptr;  // set by with_claim_counter around the dQ launch
     bp.dq = static_cast<__nv_bfloat16*>(dq);
     bp.d_out = D;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     float* delta = static_cast<float*>(workspace);
-    return D <= 64 ? launch_bwd<64>(P, mq, mk, mv, mdo, mdk, mdv, bp, out, dout, delta,
-                                    ds->status_word, ds->num_sms, s)
-                   : launch_bwd<128>(P, mq, mk, mv, mdo, mdk, mdv, bp, out, dout, delta,
-                                     ds->status_word, ds->num_sms, s);
+    return D <= 64 ? launch_bwd<64>(P, mq, mk, mv, mdo, mdk, mdv, bp, out, dout, delta, ds, s)
+                   : launch_bwd<128>(P, mq, mk, mv, mdo, mdk, mdv, bp, out, dout, delta, ds, s);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -956,10 +998,11 @@ constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB
 static __device__ __align__(256) unsigned char g_splitkv_scratch[kNoAllocScratchBytes];
 
 // In host code `g_splitkv_scratch` only names a host-side stand-in for the device array, so the
-// device address is looked up once per device (with that device current) and cached.
+// device address is looked up per device (with that device current) and cached once the lookup
+// has succeeded.  A failed lookup (for instance one attempted while a stream capture forbids it)
+// is not cached: the next call tries again.
 struct ScratchState {
-    std::once_flag once;
-    cudaError_t error = cudaSuccess;
+    std::mutex lock;
     void* ptr = nullptr;
 };
 ScratchState g_scratch[kMaxDevices];
@@ -970,11 +1013,13 @@ int scratch_address(void** out) {
     if (e != cudaSuccess) return cuda_fail(e);
     if (dev < 0 || dev >= kMaxDevices) return cuda_fail(cudaErrorInvalidDevice);
     ScratchState& st = g_scratch[dev];
-    std::call_once(st.once, [&st] {
-        st.error = cudaGetSymbolAddress(&st.ptr, g_splitkv_scratch);
-        if (st.error != cudaSuccess) st.ptr = nullptr;
-    });
-    if (st.error != cudaSuccess) return cuda_fail(st.error);
+    std::lock_guard<std::mutex> guard(st.lock);
+    if (st.ptr == nullptr) {
+        void* ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_splitkv_scratch);
+        if (e != cudaSuccess) return cuda_fail(e);
+        st.ptr = ptr;
+    }
     *out = st.ptr;
     return ATTN_OK;
 }

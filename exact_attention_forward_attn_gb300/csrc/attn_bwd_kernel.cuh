@@ -42,7 +42,8 @@ struct BwdParams {
     float sm_scale;
     const float* lse;    // [B, Hq, N] natural-log LSE from the forward
     const float* delta;  // [B, Hq, N] dO . O
-    // dQ kernel (persistent): its work items, its claim counter (zero at launch), and dQ
+    // dQ kernel (persistent): its work items, its claim counter (zero at launch; nullptr: the
+    // static schedule), and dQ
     // [B, Hq, N, d_out] bf16, contiguous
     int items;
     unsigned int* sched;
@@ -544,7 +545,8 @@ struct DqSmem {
 
 // Persistent: min(items, SMs) CTAs; a work item is one (128-row query tile i, b, query head),
 // latest (heaviest under the causal mask) tiles first.  CTA c takes item c, then claims items
-// from the launch's counter (the forward's scheme, one of the same counters).  Across items every
+// from the launch's counter (the forward's scheme, one of the same counters, or its static
+// schedule in a captured graph).  Across items every
 // mbarrier keeps counting phases: Q_i and dO_i reload as soon as the previous item's last S and
 // dP MMAs have read them, so the next item's loads and first MMAs overlap the current item's last
 // steps and its epilogue, and the first dQ MMA of an item waits until the epilogue has read the
@@ -648,13 +650,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const uint32_t ring_base = sbase + (kside ? L::kK : L::kV);
             const CUtensorMap* map = kside ? &tmap_k : &tmap_v;
             bool claims_done = false;
+            int claim_round = 0;
             auto claim = [&]() -> int {
-                const unsigned int c = atomicAdd(p.sched, 1u);
-                const unsigned int it = c + gridDim.x;
-                if (it < static_cast<unsigned int>(p.items)) return static_cast<int>(it);
-                claims_done = true;
-                if (c == static_cast<unsigned int>(p.items) - 1u) atomicExch(p.sched, 0u);
-                return -1;
+                return claim_next_item(p.sched, p.items, claim_round, claims_done);
             };
             int g = 0;  // K/V stream position (steps of the earlier items)
             for (int k = 0;; ++k) {

@@ -63,11 +63,37 @@ static_assert(32 * (2 * kSoftmaxRegs + kOtherRegs) <= 16384, "sub-partition regi
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLn2 = 0.69314718055994530942f;
-// Claim counters: the host hands each launch one of kSchedSlots counters, round robin.  CTA c
-// takes item c first, then claims items gridDim.x + 0, 1, 2, ... from the counter until a claim
-// falls past the end; so a launch makes exactly `items` claims, and the CTA whose claim returns
-// items - 1 (the last one) zeroes the counter for the next launch that gets this slot.
+// Claim counters: the host hands each launch one of kSchedSlots counters, and a launch that
+// reuses a counter is ordered after the counter's previous launch, so no two launches executing
+// at the same time share one.  CTA c takes item c first, then claims items gridDim.x + 0, 1, 2,
+// ... from the counter until a claim falls past the end; so a launch makes exactly `items`
+// claims, and the CTA whose claim returns items - 1 (the last one) zeroes the counter for the
+// next launch that gets it.  A launch without a counter (sched == nullptr: one captured into a
+// CUDA graph, whose replays the host cannot order) uses a static schedule instead: in round r
+// CTA c takes item r * gridDim.x + c, or r * gridDim.x + gridDim.x - 1 - c in odd rounds (a snake
+// over the heaviest-first item order, so the rounds' heavy and light items even out).
 constexpr int kSchedSlots = 64;
+
+// The next item after this CTA's first one (item blockIdx.x), or -1 past the end; `round` counts
+// this CTA's items so far, `done` is set by the claim past the end.
+__device__ __forceinline__ int claim_next_item(unsigned int* sched, int items, int& round,
+                                               bool& done) {
+    const unsigned int n = static_cast<unsigned int>(items);
+    if (sched == nullptr) {
+        const unsigned int r = static_cast<unsigned int>(++round);
+        const unsigned int g = gridDim.x;
+        const unsigned int it = r * g + ((r & 1u) ? g - 1u - blockIdx.x : blockIdx.x);
+        if (it < n) return static_cast<int>(it);
+        done = true;
+        return -1;
+    }
+    const unsigned int c = atomicAdd(sched, 1u);
+    const unsigned int it = c + gridDim.x;
+    if (it < n) return static_cast<int>(it);
+    done = true;
+    if (c == n - 1u) atomicExch(sched, 0u);
+    return -1;
+}
 
 struct AttnParams {
     int B, Hq, Hkv, N;
@@ -87,7 +113,7 @@ struct AttnParams {
     // so the waits on it expire and the failure is reported through the status word.
     int stall_item;
     int items;             // work items of the launch (Q-tile pairs x splits)
-    unsigned int* sched;   // this launch's claim counter (persistent kernels), zero at launch
+    unsigned int* sched;   // this launch's claim counter, zero at launch (nullptr: static schedule)
     // O for the two-tile kernel's own stores: base, element strides of batch, head and row, and
     // the head dimension (columns at and past it are padding, not part of O)
     __nv_bfloat16* out;
@@ -286,15 +312,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             ArmedPhases kv_armed;        // this lane's loads, drained after an abort
             int ring = 0;                // K/V ring entries of the earlier items
             bool claims_done = false;    // lane 0: this CTA's claim past the end was made
+            int claim_round = 0;         // lane 0: items this CTA has taken
             // One claim: the item number, or -1 past the end (the launch's last claim also
             // zeroes the counter).
             auto claim = [&]() -> int {
-                const unsigned int c = atomicAdd(p.sched, 1u);
-                const unsigned int it = c + gridDim.x;
-                if (it < static_cast<unsigned int>(p.items)) return static_cast<int>(it);
-                claims_done = true;
-                if (c == static_cast<unsigned int>(p.items) - 1u) atomicExch(p.sched, 0u);
-                return -1;
+                return claim_next_item(p.sched, p.items, claim_round, claims_done);
             };
             for (int k = 0;; ++k) {
                 int item;

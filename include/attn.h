@@ -82,10 +82,12 @@ typedef enum {
  * SMs idle (the results are the same bits either way).  Its CTAs claim work items
  * from a device counter that the library hands to each launch from a pool of 64 (round robin,
  * per device, shared with attn_fwd_strided, the split-KV entry points and the backward's dQ
- * kernel).  Each launch returns its counter to zero, so launches in one stream, or on different
- * streams, may follow each other freely; at most 64 such launches may be executing at the same
- * time on one device (a CUDA graph replays its launches' counters, so a graph must not run
- * concurrently with another replay of itself).
+ * kernel).  Each launch returns its counter to zero, and before a launch reuses a counter its
+ * stream waits (cudaStreamWaitEvent) for the counter's previous launch to finish, so any number
+ * of launches from any streams or host threads may overlap.  A launch made while its stream is
+ * being captured into a CUDA graph takes no counter: its CTAs follow a static schedule instead
+ * (a few per cent slower on long causal problems), so graphs may replay on any streams, also
+ * concurrently with each other.
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
              int Hkv, int N, int D, int causal, float sm_scale, void* stream);
@@ -159,9 +161,13 @@ int attn_fwd_splitkv_num_splits(int B, int Hq, int N, int D, int causal);
  *
  *   Arguments, outputs and result: as attn_fwd_splitkv, without the workspace arguments.
  *   A problem whose partials need more than the buffer holds (attn_fwd_splitkv_workspace_bytes()
- *   > attn_fwd_splitkv_noalloc_max_bytes()) returns ATTN_ERR_SCRATCH before touching the device.
+ *   > attn_fwd_splitkv_noalloc_max_bytes()) returns ATTN_ERR_SCRATCH before any launch.  With an
+ *   explicit num_splits the check runs before any CUDA call; with num_splits = 0 the default
+ *   split count needs the device's SM count first (the same one-time device query every entry
+ *   point makes), so that check follows it.
  *   The buffer's device address is looked up the first time this is called on a device (with that
- *   device current); make that first call before capturing any stream.
+ *   device current); make that first call before capturing any stream.  A lookup that fails is
+ *   not remembered: the next call on that device tries again.
  *   All calls share the one buffer, and it keeps the last call's partials (nothing in it needs to
  *   start at zero).  Calls that overlap on the GPU - on different streams, or from several host
  *   threads without ordering - race on it and may return wrong results; serialise them.

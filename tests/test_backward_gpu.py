@@ -1,11 +1,20 @@
 """GPU parity of the backward (attn_bwd, by recompute) against the fp64 oracle's gradients.
 
-Tolerance: the pages state none for the backward.  The GPU path rounds P and dS to bf16 before
-the MMAs (as the pages' forward rounds P before P.V), forms dO.O from the bf16 O, and stores bf16
-gradients; each of these is a relative rounding of 2^-9, and dS = P (dP - dO.O) can cancel.  The
-bound used, per gradient tensor G with reference R, is
-    |G - R| <= 2e-2 * max|R| + 2e-2 * |R|      element-wise,
-i.e. the forward's bf16 tolerance with the absolute part scaled to the tensor's magnitude.
+Tolerance (the pages state none for the backward).  The GPU path rounds P and dS to bf16 before
+the MMAs (as the pages' forward rounds P before P.V), forms Delta_i = dO_i . O_i from the stored
+bf16 O (as the pages' backward reads the saved output), and stores bf16 gradients.  Each of these
+is a relative rounding of about 2^-9 of the terms it touches, so the bound is set per gradient
+ROW (one query row of dq, one key row of dk / dv), never by the largest element of the tensor:
+
+    |G - R| <= 2e-2 * max|R_row| + 2e-2 * |R|                           (dk, dv)
+    |G - R| <= 2e-2 * max|R_row| + 2e-2 * |R| + sm_scale * 2^-8 * a_i * |c_i|      (dq)
+
+with a_i = sum_d |dO_id| |O_id| and c_i = sum_j P_ij k_j (the oracle's forward with K in place of
+V).  dq_i is linear in Delta_i (dq_i = sm_scale sum_j P_ij (dP_ij - Delta_i) k_j), so an O that
+is off by one bf16 unit (relative 2^-8) per element moves dq_i by at most sm_scale * 2^-8 * a_i *
+|c_i|: on query rows that see few keys dS cancels and this term, not the row's own size, sets
+the attainable accuracy.  On top, every tensor must satisfy ||G - R|| / ||R|| <= 1e-2 (the
+measured and simulated figure is 2-3e-3).
 """
 import math
 
@@ -19,15 +28,32 @@ from exact_attention_forward_attn_gb300 import workloads as wl
 pytestmark = pytest.mark.gpu
 
 
-def _grad_check(name, g, ref):
+def _grad_check(name, g, ref, extra=None):
+    """Per-row elementwise bound (plus the Delta term for dq) and a relative-L2 bound."""
     g = g.float().cpu().numpy().astype(np.float64)
-    scale = float(np.max(np.abs(ref))) if ref.size else 1.0
-    err = np.abs(g - ref)
-    bad = err > 2e-2 * scale + 2e-2 * np.abs(ref)
     assert np.all(np.isfinite(g)), f"{name}: non-finite"
-    assert not bad.any(), (f"{name}: {int(bad.sum())}/{bad.size} out of tolerance; "
-                           f"max err {err.max():.3e} (max|ref| {scale:.3e})")
-    return float(err.max() / max(scale, 1e-30))
+    err = np.abs(g - ref)
+    row = np.max(np.abs(ref), axis=-1, keepdims=True)
+    bound = 2e-2 * row + 2e-2 * np.abs(ref)
+    if extra is not None:
+        bound = bound + extra
+    bad = err > bound
+    assert not bad.any(), (
+        f"{name}: {int(bad.sum())}/{bad.size} out of tolerance; worst err/bound "
+        f"{float(np.max(err / np.maximum(bound, 1e-300))):.2f} at "
+        f"{np.unravel_index(np.argmax(err / np.maximum(bound, 1e-300)), err.shape)}")
+    rel = float(np.linalg.norm(g - ref) / max(np.linalg.norm(ref), 1e-300))
+    assert rel <= 1e-2, f"{name}: relative L2 error {rel:.2e} > 1e-2"
+    return rel
+
+
+def _dq_delta_term(q, k, v, do, causal, sm_scale):
+    """sm_scale * 2^-8 * a_i * |c_i|: how far dq_i moves when Delta_i is formed from an O that is
+    one bf16 unit off per element (a_i = sum_d |dO_id||O_id|, c_i = sum_j P_ij k_j)."""
+    o, _ = oracle.attn_ref(q, k, v, causal, sm_scale)
+    c, _ = oracle.attn_ref(q, k, k, causal, sm_scale)
+    a = np.sum(np.abs(do.double().numpy()) * np.abs(o), axis=-1, keepdims=True)
+    return sm_scale * 2.0 ** -8 * a * np.abs(c)
 
 
 def _dout(w, seed):
@@ -60,8 +86,9 @@ def test_backward_matches_oracle(w, cuda_lib):
     torch.cuda.synchronize()
     assert attn.device_status() == 0
     rq, rk, rv = oracle.attn_bwd_ref(q, k, v, do, w.causal, w.sm_scale)
-    e = [_grad_check(n, g, r) for n, g, r in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv))]
-    print(f"{w.name}: relative max errors dq {e[0]:.2e} dk {e[1]:.2e} dv {e[2]:.2e}")
+    extra = _dq_delta_term(q, k, v, do, w.causal, w.sm_scale)
+    e = [_grad_check("dq", dq, rq, extra), _grad_check("dk", dk, rk), _grad_check("dv", dv, rv)]
+    print(f"{w.name}: relative L2 errors dq {e[0]:.2e} dk {e[1]:.2e} dv {e[2]:.2e}")
 
 
 def test_autograd_function(cuda_lib):
@@ -78,6 +105,6 @@ def test_autograd_function(cuda_lib):
     out.backward(do.cuda())
     torch.cuda.synchronize()
     rq, rk, rv = oracle.attn_bwd_ref(q, k, v, do, True, w.sm_scale)
-    _grad_check("dq", qd.grad, rq)
+    _grad_check("dq", qd.grad, rq, _dq_delta_term(q, k, v, do, True, w.sm_scale))
     _grad_check("dk", kd.grad, rk)
     _grad_check("dv", vd.grad, rv)

@@ -3,7 +3,9 @@
 Tolerance (the pages' bf16 check, read as torch.assert_close semantics, plus the LSE bound):
     |O_gpu - O_ref| <= 2e-2 + 2e-2 * |O_ref|   for every element,
     |LSE_gpu - LSE_ref| <= 1e-3                 for every row.
-Full-size long-context workloads are compared on 64 seeded query rows per head.
+The five configurations are compared in full (C3, B=1 Hq=64 N=4096, is 0.27 TFLOP of fp64 work:
+seconds on the host cores); only the long-context sweep (N >= 8192) and the wide-head workload are
+compared on 64 seeded query rows per head.
 """
 import ctypes
 
@@ -51,7 +53,8 @@ def _check(o_gpu, l_gpu, o_ref, l_ref, label):
     return float(err.max()), float(lerr.max())
 
 
-FULL = [wl.TINY_NONCAUSAL, wl.TINY_CAUSAL, wl.GQA4_CAUSAL, wl.MHA, wl.MHA_OUTLIER, wl.MQA]
+FULL = [wl.TINY_NONCAUSAL, wl.TINY_CAUSAL, wl.GQA4_CAUSAL, wl.GQA8_CAUSAL, wl.MHA, wl.MHA_OUTLIER,
+        wl.MQA]
 
 
 @pytest.mark.parametrize("w", FULL, ids=[w.name for w in FULL])
@@ -62,7 +65,7 @@ def test_config_full_output(w, cuda_lib):
     _check(out, lse, o_ref, l_ref, w.name)
 
 
-SAMPLED = [wl.GQA8_CAUSAL, *wl.LONG.values(), wl.WIDE]
+SAMPLED = [*wl.LONG.values(), wl.WIDE]
 
 
 @pytest.mark.parametrize("w", SAMPLED, ids=[w.name for w in SAMPLED])

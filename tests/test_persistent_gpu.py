@@ -2,10 +2,12 @@
 
 The two-tile forward runs one CTA per SM; each CTA takes one work item (a pair of Q tiles of one
 head) and then claims more from a per-launch counter, one of 64 the host hands out round robin;
-the launch's last claim sets its counter back to zero.  These tests check what that must not
-change: every item is computed exactly once whatever the launch order, the number of launches
-(more than the 64 counters), the grid size (more items than SMs, or fewer) or concurrent launches
-on other streams.  Each item's arithmetic does not depend on which CTA runs it, so repeated
+the launch's last claim sets its counter back to zero, and a launch that reuses a counter waits
+for the counter's previous launch.  Launches captured into a CUDA graph take no counter and use
+the kernel's static schedule.  These tests check what that must not change: every item is
+computed exactly once whatever the launch order, the number of launches (more than the 64
+counters), the grid size (more items than SMs, or fewer), concurrent launches on many streams,
+or graph replays.  Each item's arithmetic does not depend on which CTA runs it, so repeated
 launches must give bit-identical outputs; one launch per shape is also checked against the oracle.
 """
 import pytest
@@ -84,6 +86,33 @@ def test_concurrent_launches_on_two_streams(cuda_lib):
     assert attn.device_status(dev) == 0
 
 
+def test_eighty_concurrent_launches_on_eighty_streams(cuda_lib):
+    """More overlapping launches than there are claim counters: the 65th launch reuses the
+    first one's counter and must wait for it, not share it.  Every launch is enqueued (two
+    shapes, alternating) before anything is synchronised; all 80 results must be the serial
+    launches' bits."""
+    import exact_attention_forward_attn_gb300 as attn
+
+    dev = torch.device("cuda:0")
+    shapes = [wl.Workload("conc-a-n2048", 1, 16, 4, 2048, 128, True, 51),   # 128 items
+              wl.Workload("conc-b-n3000", 1, 24, 8, 3000, 128, False, 52)]  # 288 items
+    data = [_inputs(w, dev)[1] for w in shapes]
+    ref = []
+    for w, (qd, kd, vd) in zip(shapes, data):
+        ref.append(attn.attn_fwd(qd, kd, vd, causal=w.causal, sm_scale=w.sm_scale))
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(dev) for _ in range(80)]
+    outs = []
+    for i, st in enumerate(streams):
+        w, (qd, kd, vd) = shapes[i % 2], data[i % 2]
+        with torch.cuda.stream(st):
+            outs.append(attn.attn_fwd(qd, kd, vd, causal=w.causal, sm_scale=w.sm_scale))
+    torch.cuda.synchronize()
+    for i, (o, l) in enumerate(outs):
+        assert torch.equal(o, ref[i % 2][0]) and torch.equal(l, ref[i % 2][1]), f"launch {i}"
+    assert attn.device_status(dev) == 0
+
+
 @pytest.mark.parametrize("w", [wl.FEWHEADS, wl.Workload("pers-split-causal-n1900", 1, 4, 2, 1900,
                                                           128, True, 44)],
                          ids=["fewheads-n4096", "causal-n1900"])
@@ -109,8 +138,8 @@ def test_split_launches_reuse_counters(w, cuda_lib):
 
 
 def test_cuda_graph_replays(cuda_lib):
-    """Launches captured in a CUDA graph keep their claim counters across replays: each replay
-    starts from the zero the previous one left."""
+    """Launches captured in a CUDA graph run the static schedule (no claim counter), so every
+    replay computes every item once."""
     import exact_attention_forward_attn_gb300 as attn
 
     dev = torch.device("cuda:0")
@@ -161,4 +190,45 @@ def test_one_tile_items_match_pairs(causal, cuda_lib):
     assert torch.equal(o1[0], ob[0]) and torch.equal(l1[0], lb[0])
     o_ref, l_ref = oracle.attn_ref(q1, k1, v1, causal, small.sm_scale)
     _check(o1, l1, o_ref, l_ref, small.name)
+    assert attn.device_status(dev) == 0
+
+
+def test_graphs_of_the_same_launches_replay_concurrently(cuda_lib):
+    """Two graphs captured from the same launches, replayed at the same time on two streams
+    (and beside an eager launch of the same shape): captured launches hold no shared state."""
+    import exact_attention_forward_attn_gb300 as attn
+
+    dev = torch.device("cuda:0")
+    w = SHAPES[2]
+    _, (qd, kd, vd) = _inputs(w, dev)
+    ref = attn.attn_fwd(qd, kd, vd, causal=w.causal, sm_scale=w.sm_scale)
+    torch.cuda.synchronize()
+    bufs = [(torch.empty_like(ref[0]), torch.empty_like(ref[1])) for _ in range(2)]
+    graphs = []
+    for o, l in bufs:
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            attn.attn_fwd(qd, kd, vd, causal=w.causal, sm_scale=w.sm_scale, out=o, lse=l)
+        torch.cuda.current_stream(dev).wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(3):
+                attn.attn_fwd(qd, kd, vd, causal=w.causal, sm_scale=w.sm_scale, out=o, lse=l)
+        graphs.append(g)
+    s0, s1, s2 = (torch.cuda.Stream(dev) for _ in range(3))
+    for _ in range(10):
+        for (o, l) in bufs:
+            o.zero_()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s0):
+            graphs[0].replay()
+        with torch.cuda.stream(s1):
+            graphs[1].replay()
+        with torch.cuda.stream(s2):
+            eager = attn.attn_fwd(qd, kd, vd, causal=w.causal, sm_scale=w.sm_scale)
+        torch.cuda.synchronize()
+        for o, l in (*bufs, eager):
+            assert torch.equal(o, ref[0]) and torch.equal(l, ref[1])
     assert attn.device_status(dev) == 0

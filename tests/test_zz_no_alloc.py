@@ -11,6 +11,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from exact_attention_forward_attn_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
@@ -38,6 +39,12 @@ def _close(o_new, l_new, o_ref, l_ref):
     assert (l_new - l_ref).abs().max().item() <= LSE_ATOL
 
 
+def _noalloc(lib, w, splits, q, k, v, out, lse):
+    return lib.attn_fwd_splitkv_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                        lse.data_ptr(), w.B, w.Hq, w.Hkv, w.N, w.D, int(w.causal),
+                                        ctypes.c_float(w.sm_scale), splits, _stream())
+
+
 def test_noalloc_matches_the_workspace_entry_point_on_two_calls(cuda_lib):
     lib = cuda_lib
     cases = [(wl.FEWHEADS, 4), (wl.random_case(2, 4, 2, 700, 128, True, 21), 3)]
@@ -53,14 +60,42 @@ def test_noalloc_matches_the_workspace_entry_point_on_two_calls(cuda_lib):
         assert st == 0
         out = torch.full_like(out_ref, float("nan"))
         lse = torch.full_like(lse_ref, float("nan"))
-        st = lib.attn_fwd_splitkv_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(),
-                                          out.data_ptr(), lse.data_ptr(), w.B, w.Hq, w.Hkv, w.N,
-                                          w.D, int(w.causal), ctypes.c_float(w.sm_scale), splits,
-                                          _stream())
-        assert st == 0
+        assert _noalloc(lib, w, splits, q, k, v, out, lse) == 0
         torch.cuda.synchronize()
         assert lib.attn_debug_status(_stream()) == 0
         _close(out, lse, out_ref, lse_ref)
+
+
+def test_noalloc_matches_the_oracle(cuda_lib):
+    """Not only the workspace entry point: the fp64 oracle, on a causal ragged case."""
+    lib = cuda_lib
+    w = wl.random_case(1, 4, 2, 1100, 128, True, 22)
+    q, k, v, out, lse = _inputs(w)
+    assert _noalloc(lib, w, 4, q, k, v, out, lse) == 0
+    torch.cuda.synchronize()
+    assert lib.attn_debug_status(_stream()) == 0
+    o_ref, l_ref = oracle.attn_ref(q.cpu(), k.cpu(), v.cpu(), w.causal, w.sm_scale)
+    o = out.float().cpu().numpy().astype(np.float64)
+    assert not (np.abs(o - o_ref) > O_ATOL + O_RTOL * np.abs(o_ref)).any()
+    assert np.abs(lse.cpu().numpy().astype(np.float64) - l_ref).max() <= LSE_ATOL
+
+
+def test_noalloc_allocates_nothing(cuda_lib):
+    """Free device memory (driver view) and torch's allocator are unchanged across calls."""
+    lib = cuda_lib
+    w = wl.FEWHEADS
+    q, k, v, out, lse = _inputs(w)
+    assert _noalloc(lib, w, 4, q, k, v, out, lse) == 0  # first call: the buffer's address lookup
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    torch0 = torch.cuda.memory_allocated()
+    for splits in (4, 2, 0):
+        assert _noalloc(lib, w, splits, q, k, v, out, lse) == 0
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0, f"free device memory changed by {free0 - free1} bytes"
+    assert torch.cuda.memory_allocated() == torch0
+    assert lib.attn_debug_status(_stream()) == 0
 
 
 def test_noalloc_rejects_problems_beyond_its_buffer(cuda_lib):
@@ -72,3 +107,15 @@ def test_noalloc_rejects_problems_beyond_its_buffer(cuda_lib):
     st = lib.attn_fwd_splitkv_noalloc(gap, 2 * gap, 3 * gap, 4 * gap, 5 * gap, B, Hq, Hkv, N, D,
                                       1, ctypes.c_float(D ** -0.5), splits, _stream())
     assert st == -14  # ATTN_ERR_SCRATCH
+
+
+def test_noalloc_default_split_count_fits_its_buffer(cuda_lib):
+    """num_splits = 0: the library splits only while the query tiles leave SMs idle, so the
+    default split count's partials stay within the buffer (checked over a sweep of shapes)."""
+    lib = cuda_lib
+    cap = lib.attn_fwd_splitkv_noalloc_max_bytes()
+    for B in (1, 2, 4):
+        for Hq in (1, 2, 4, 8, 16, 32):
+            for N in (512, 1024, 4096, 8192, 16384, 32768, 65536, 131072):
+                for D in (64, 128):
+                    assert lib.attn_fwd_splitkv_workspace_bytes(B, Hq, N, D, 0) <= cap
