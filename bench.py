@@ -33,6 +33,7 @@ UNIT = "TFLOPS"
 DEFAULT_WORKLOAD = "long-gqa8-causal-n32768"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 KERNEL_SOURCES = ["exact_attention_forward_attn_gb300/csrc/attn_fwd_kernel.cuh",
+                  "exact_attention_forward_attn_gb300/csrc/attn_fwd_pair_kernel.cuh",
                   "exact_attention_forward_attn_gb300/csrc/ptx.cuh",
                   "exact_attention_forward_attn_gb300/csrc/attn_api.cu"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
@@ -573,6 +574,34 @@ def main():
             sweep.append({"N": n, "ms": ms, "tflops": tf, "frac": tf / peak})
             del sq, sk, sv, so, sl
 
+    # ---- context: the two D = 128 forward kernels side by side (the one-CTA kernel attn_fwd
+    # runs, and the CTA-pair kernel whose M = 256 MMAs span two SMs), through the test hook -----
+    kernels = []
+    if not args.no_sweep and rank == 0:
+        lib = _lib.load()
+        sh = ctypes.c_void_p(stream.cuda_stream)
+        for wk in (wl.LONG[8192], wl.LONG[32768]):
+            kq, kk_, kv_ = (t.to(dev) for t in wl.make_qkv(wk))
+            ko = torch.empty_like(kq)
+            kl = torch.empty(wk.B, wk.Hq, wk.N, dtype=torch.float32, device=dev)
+            kargs = (kq.data_ptr(), kk_.data_ptr(), kv_.data_ptr(), ko.data_ptr(), kl.data_ptr(),
+                     wk.B, wk.Hq, wk.Hkv, wk.N, wk.D, int(wk.causal), ctypes.c_float(wk.sm_scale))
+            entry = {"workload": wk.name}
+            for name, kid in (("one_cta", 1), ("pair", 2)):
+                def kstep(kid=kid):
+                    assert lib.attn_fwd_test_kernel(*kargs, kid, -1, sh) == 0
+
+                with torch.cuda.stream(stream):
+                    for _ in range(3):
+                        kstep()
+                ms = statistics.median(timed_launches(kstep, stream, 10))
+                entry[f"{name}_ms"] = ms
+                entry[f"{name}_tflops"] = wk.flops / (ms * 1e-3) / 1e12
+            kernels.append(entry)
+            del kq, kk_, kv_, ko, kl
+        if attn.device_status(dev) != 0:
+            raise SystemExit("device status word reports an expired wait in the kernels leg")
+
     # ---- context: wide heads (D = 256, one Q tile per CTA) on a long causal sequence ---------
     wide = []
     if not args.no_sweep and rank == 0:
@@ -757,7 +786,8 @@ def main():
             "config": config_of(w, "inputs and output exceed the 129 MB L2; no flush"),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": args.steps, "clocks": clocks, "configs": configs, "sweep": sweep,
-            "low_occupancy": low_occ, "wide_heads": wide, "backward": backward,
+            "low_occupancy": low_occ, "wide_heads": wide, "forward_kernels": kernels,
+            "backward": backward,
             "mla_decode": mla, "cpu_baseline_table": cpu_table,
             "kernel_sha": kernel_hash(),
         }

@@ -28,6 +28,8 @@ SIGNATURES = {
     "attn_fwd_splitkv_noalloc_max_bytes": (ctypes.c_size_t, []),
     "attn_fwd_test_stall": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
                                      _c_int, _c_int, _c_float, _c_int, _vp]),
+    "attn_fwd_test_kernel": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
+                                      _c_int, _c_int, _c_float, _c_int, _c_int, _vp]),
     "attn_bwd": (_c_int, [_vp] * 9 + [_c_int] * 6 + [_c_float, _vp, ctypes.c_size_t, _vp]),
     "attn_bwd_workspace_bytes": (ctypes.c_size_t, [_c_int, _c_int, _c_int]),
     "attn_fwd_strided": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int,

@@ -20,7 +20,7 @@ LIB_NAME = "libgb300attn.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
 SOURCES = [os.path.join(CSRC, "attn_api.cu")]
 DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in (
-    "attn_fwd_kernel.cuh", "attn_fwd_d256_kernel.cuh", "attn_bwd_kernel.cuh",
+    "attn_fwd_kernel.cuh", "attn_fwd_pair_kernel.cuh", "attn_fwd_d256_kernel.cuh", "attn_bwd_kernel.cuh",
     "mla_decode_kernel.cuh", "ptx.cuh")] + [
     os.path.join(INCLUDE, "attn.h")]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]

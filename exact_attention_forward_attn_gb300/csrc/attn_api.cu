@@ -20,6 +20,7 @@
 #include "attn_bwd_kernel.cuh"
 #include "attn_fwd_d256_kernel.cuh"
 #include "attn_fwd_kernel.cuh"
+#include "attn_fwd_pair_kernel.cuh"
 #include "mla_decode_kernel.cuh"
 
 using namespace gb300attn;
@@ -68,10 +69,10 @@ struct Strides {
 
 Strides contiguous_strides(int64_t H, int64_t N, int64_t D) { return {D, N * D, H * N * D}; }
 
-// 4-D view [B, H, N, D] (innermost D); box = 64 (D) x 128 (rows) x 1 x 1, 128B swizzle.
+// 4-D view [B, H, N, D] (innermost D); box = 64 (D) x box_rows (rows) x 1 x 1, 128B swizzle.
 // Rows >= N of a head are out of bounds: zero-filled on load, dropped on store.
 bool make_tile_map(CUtensorMap* map, const void* base, int64_t B, int64_t H, int64_t N, int64_t D,
-                   const Strides& st) {
+                   const Strides& st, int box_rows) {
     EncodeTiledFn enc = encode_tiled();
     if (!enc) return false;
     const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N),
@@ -79,7 +80,7 @@ bool make_tile_map(CUtensorMap* map, const void* base, int64_t B, int64_t H, int
     const cuuint64_t strides[3] = {static_cast<cuuint64_t>(st.n * 2),
                                    static_cast<cuuint64_t>(st.h * 2),
                                    static_cast<cuuint64_t>(st.b * 2)};
-    const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(kBM), 1, 1};
+    const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_rows), 1, 1};
     const cuuint32_t elem_strides[4] = {1, 1, 1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
                box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -92,9 +93,10 @@ bool make_tile_map(CUtensorMap* map, const void* base, int64_t B, int64_t H, int
 struct MapKey {
     const void* base;
     int64_t B, H, N, D, sn, sh, sb;
+    int box_rows;
     bool operator==(const MapKey& o) const {
         return base == o.base && B == o.B && H == o.H && N == o.N && D == o.D && sn == o.sn &&
-               sh == o.sh && sb == o.sb;
+               sh == o.sh && sb == o.sb && box_rows == o.box_rows;
     }
 };
 struct MapCache {
@@ -107,14 +109,14 @@ struct MapCache {
 thread_local MapCache t_maps;
 
 bool cached_tile_map(CUtensorMap* map, const void* base, int64_t B, int64_t H, int64_t N,
-                     int64_t D, const Strides& st) {
-    const MapKey key{base, B, H, N, D, st.n, st.h, st.b};
+                     int64_t D, const Strides& st, int box_rows = kBM) {
+    const MapKey key{base, B, H, N, D, st.n, st.h, st.b, box_rows};
     for (int i = 0; i < MapCache::kEntries; ++i)
         if (t_maps.valid[i] && t_maps.key[i] == key) {
             *map = t_maps.map[i];
             return true;
         }
-    if (!make_tile_map(map, base, B, H, N, D, st)) return false;
+    if (!make_tile_map(map, base, B, H, N, D, st, box_rows)) return false;
     const int slot = t_maps.next;
     t_maps.next = (slot + 1) % MapCache::kEntries;
     t_maps.key[slot] = key;
@@ -141,6 +143,7 @@ struct DeviceState {
     unsigned int* sched = nullptr;  // g_fwd_sched
     std::atomic<unsigned int> sched_next{0};
     SchedSlot slots[kSchedSlots];
+    int pair_clusters = 0;  // CTA pairs of the pair kernel that fit on the device at once
 };
 DeviceState g_devices[kMaxDevices];
 
@@ -156,6 +159,29 @@ cudaError_t opt_in_smem(bool* regs_ok) {
     return cudaFuncSetAttribute(attn_fwd_kernel<D, kSplit, kOne>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 SmemLayout<D>::kAlloc);
+}
+
+// The pair kernel: shared-memory opt-in, its register count, and how many CTA pairs fit on the
+// device at once (a pair needs two SMs of one GPC).
+cudaError_t opt_in_pair(bool* regs_ok, int* clusters) {
+    cudaFuncAttributes a;
+    cudaError_t e = cudaFuncGetAttributes(&a, attn_fwd_pair_kernel);
+    if (e != cudaSuccess) return e;
+    if (a.numRegs != kLaunchRegs) *regs_ok = false;
+    e = cudaFuncSetAttribute(attn_fwd_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             PairSmem::kAlloc);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = PairSmem::kAlloc;
+    *clusters = 0;
+    // If the device cannot say (or fits no pair), the forward runs on single CTAs only.
+    if (cudaOccupancyMaxActiveClusters(clusters, attn_fwd_pair_kernel, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        *clusters = 0;
+    }
+    return cudaSuccess;
 }
 
 template <int D>
@@ -200,6 +226,7 @@ int device_state(int dev, DeviceState** out) {
             e = cudaFuncSetAttribute(attn_fwd_d256_kernel,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      Fwd256Smem::kAlloc);
+        if (e == cudaSuccess) e = opt_in_pair(&regs_ok, &st.pair_clusters);
         if (e != cudaSuccess) { st.status = ATTN_ERR_CUDA; st.cuda_error = e; return; }
         if (!regs_ok) st.status = ATTN_ERR_ARCH;
     });
@@ -416,6 +443,35 @@ int launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
     });
 }
 
+// The single pass runs on the one-CTA kernel for every shape: measured on GB300 the pair kernel
+// is slower wherever it can run (0.62-0.85x at N = 512-32768), its M = 256 MMAs issuing more
+// slowly per SM and each step's handshakes crossing between the two SMs; attn_fwd_test_kernel
+// still runs it.
+
+// The pair kernel over all quads of the problem: min(quads, pairs that fit) clusters of two CTAs,
+// each pair claiming quads until all are taken.  K and V are read in half tiles (64-row boxes).
+int launch_pair(const Problem& P, const CUtensorMap& mq, const AttnParams& p_in, DeviceState* ds,
+                cudaStream_t stream) {
+    CUtensorMap mk64, mv64;
+    if (!cached_tile_map(&mk64, P.k, P.B, P.Hkv, P.N, P.D, P.sk, 64) ||
+        !cached_tile_map(&mv64, P.v, P.B, P.Hkv, P.N, P.D, P.sv, 64))
+        return cuda_fail(cudaErrorInvalidValue);
+    AttnParams prm = p_in;
+    const int64_t quads = (P.n_tiles + 3) / 4;
+    const int64_t items = quads * P.bh;
+    if (items > 0x7fffffffLL) return ATTN_ERR_SHAPE;
+    prm.n_pairs = static_cast<int>(quads);
+    prm.items = static_cast<int>(items);
+    const int64_t pairs = std::min<int64_t>(items, ds->pair_clusters);
+    return with_claim_counter(ds, stream, [&](unsigned int* counter) {
+        prm.sched = counter;
+        attn_fwd_pair_kernel<<<static_cast<unsigned int>(2 * pairs), kThreads, PairSmem::kAlloc,
+                               stream>>>(mq, mk64, mv64, prm, ds->status_word);
+        const cudaError_t e = cudaGetLastError();
+        return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+    });
+}
+
 // The single-pass forward for head dimension D: two Q tiles per work item up to D = 128 (one if
 // `one_tile`), one Q tile per CTA above.
 int launch_single(int D, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
@@ -545,6 +601,31 @@ extern "C" int attn_fwd_test_stall(const void* q, const void* k, const void* v, 
     if (st != ATTN_OK) return st;
     prm.stall_item = stall_item;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return D <= 64 ? launch_fwd<64, false>(mq, mk, mv, prm, ds, P.items, s)
+                   : launch_fwd<128, false>(mq, mk, mv, prm, ds, P.items, s);
+}
+
+extern "C" int attn_fwd_test_kernel(const void* q, const void* k, const void* v, void* out,
+                                    float* lse, int B, int Hq, int Hkv, int N, int D, int causal,
+                                    float sm_scale, int kernel, int stall_item, void* stream) {
+    if (kernel != 1 && kernel != 2) return ATTN_ERR_SHAPE;
+    if (stall_item < -1) return ATTN_ERR_SHAPE;
+    if (D > 128 || (kernel == 2 && D <= 64)) return ATTN_ERR_HEADDIM;
+    Problem P{q, k, v, out, lse, B, Hq, Hkv, N, D, causal, sm_scale};
+    bool empty = false;
+    int st = validate(P, &empty);
+    if (st != ATTN_OK || empty) return st;
+    DeviceState* ds = nullptr;
+    CUtensorMap mq, mk, mv, mo;
+    AttnParams prm;
+    st = prepare(P, &ds, &mq, &mk, &mv, &mo, &prm);
+    if (st != ATTN_OK) return st;
+    prm.stall_item = stall_item;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (kernel == 2) {
+        if (ds->pair_clusters < 1) return ATTN_ERR_ARCH;
+        return launch_pair(P, mq, prm, ds, s);
+    }
     return D <= 64 ? launch_fwd<64, false>(mq, mk, mv, prm, ds, P.items, s)
                    : launch_fwd<128, false>(mq, mk, mv, prm, ds, P.items, s);
 }

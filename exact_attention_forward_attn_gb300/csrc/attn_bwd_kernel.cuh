@@ -652,7 +652,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             bool claims_done = false;
             int claim_round = 0;
             auto claim = [&]() -> int {
-                return claim_next_item(p.sched, p.items, claim_round, claims_done);
+                return claim_next_item(p.sched, p.items, claim_round, claims_done, blockIdx.x,
+                                       gridDim.x);
             };
             int g = 0;  // K/V stream position (steps of the earlier items)
             for (int k = 0;; ++k) {

@@ -74,21 +74,22 @@ constexpr float kLn2 = 0.69314718055994530942f;
 // over the heaviest-first item order, so the rounds' heavy and light items even out).
 constexpr int kSchedSlots = 64;
 
-// The next item after this CTA's first one (item blockIdx.x), or -1 past the end; `round` counts
-// this CTA's items so far, `done` is set by the claim past the end.
+// The next item after this worker's first one (item `first`, of `workers` working in parallel:
+// CTAs, or CTA pairs), or -1 past the end; `round` counts this worker's items so far, `done` is
+// set by the claim past the end.
 __device__ __forceinline__ int claim_next_item(unsigned int* sched, int items, int& round,
-                                               bool& done) {
+                                               bool& done, unsigned int first,
+                                               unsigned int workers) {
     const unsigned int n = static_cast<unsigned int>(items);
     if (sched == nullptr) {
         const unsigned int r = static_cast<unsigned int>(++round);
-        const unsigned int g = gridDim.x;
-        const unsigned int it = r * g + ((r & 1u) ? g - 1u - blockIdx.x : blockIdx.x);
+        const unsigned int it = r * workers + ((r & 1u) ? workers - 1u - first : first);
         if (it < n) return static_cast<int>(it);
         done = true;
         return -1;
     }
     const unsigned int c = atomicAdd(sched, 1u);
-    const unsigned int it = c + gridDim.x;
+    const unsigned int it = c + workers;
     if (it < n) return static_cast<int>(it);
     done = true;
     if (c == n - 1u) atomicExch(sched, 0u);
@@ -316,7 +317,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // One claim: the item number, or -1 past the end (the launch's last claim also
             // zeroes the counter).
             auto claim = [&]() -> int {
-                return claim_next_item(p.sched, p.items, claim_round, claims_done);
+                return claim_next_item(p.sched, p.items, claim_round, claims_done, blockIdx.x,
+                                       gridDim.x);
             };
             for (int k = 0;; ++k) {
                 int item;

@@ -282,6 +282,27 @@ int attn_fwd_test_stall(const void* q, const void* k, const void* v, void* out, 
                         void* stream);
 
 /*
+ * attn_fwd_test_kernel - test and benchmark hook: attn_fwd on a chosen forward kernel.
+ *
+ * Runs the problem (arguments as attn_fwd, contiguous tensors) on the kernel named by `kernel`,
+ * so that tests can check each kernel on any shape and benchmarks can time them side by side:
+ *   kernel = 1  the one-CTA kernel, two 128-row Q tiles per work item (D <= 128), the kernel
+ *               attn_fwd runs up to D = 128;
+ *   kernel = 2  the CTA-pair kernel: a cluster of two CTAs on two SMs shares every tcgen05 MMA
+ *               (cta_group::2, M = 256), each SM loading and reading half of every K and V tile;
+ *               four Q tiles per work item (64 < D <= 128; ATTN_ERR_HEADDIM otherwise,
+ *               ATTN_ERR_ARCH if no CTA pair fits on the device).  Measured slower than kernel 1
+ *               on GB300, so attn_fwd does not use it.
+ * stall_item: -1, or a K/V ring entry to withhold as in attn_fwd_test_stall (on CTA pairs both
+ * CTAs withhold their halves of it).
+ * The results are those of attn_fwd (the same definition; fp32 accumulation may group the work
+ * differently).  Any other value of `kernel` returns ATTN_ERR_SHAPE.
+ */
+int attn_fwd_test_kernel(const void* q, const void* k, const void* v, void* out, float* lse,
+                         int B, int Hq, int Hkv, int N, int D, int causal, float sm_scale,
+                         int kernel, int stall_item, void* stream);
+
+/*
  * attn_mla_decode_test_stall - the same test hook for attn_mla_decode (arguments as there).
  *
  * The producer of every CTA whose token range holds 64-token tile `stall_tile` (>= 0) withholds
