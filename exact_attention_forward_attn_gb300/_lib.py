@@ -1,6 +1,9 @@
 """ctypes loader for the C ABI in ``include/attn.h`` (``_build/libgb300attn.so``).
 
 There is no fallback: if the library has not been built (``build.build()``), loading raises.
+With ``ATTN_DEBUG_LIB=1`` in the environment the index-checking debug build
+(``_build/libgb300attn_debug.so``, ``build.build(debug=True)``) is loaded instead, for running
+the whole test suite under its checks.
 """
 from __future__ import annotations
 
@@ -8,7 +11,7 @@ import ctypes
 import os
 import threading
 
-from .build import LIB_PATH
+from .build import DEBUG_LIB_PATH, LIB_PATH
 
 # Every symbol include/attn.h declares, with its ctypes signature.
 _c_int, _c_float, _vp = ctypes.c_int, ctypes.c_float, ctypes.c_void_p
@@ -52,7 +55,7 @@ def load(path: str | None = None):
     with _lock:
         if _lib is not None and path is None:
             return _lib
-        p = path or LIB_PATH
+        p = path or (DEBUG_LIB_PATH if os.environ.get("ATTN_DEBUG_LIB") == "1" else LIB_PATH)
         if not os.path.exists(p):
             raise RuntimeError(
                 f"CUDA library not found at {p}; build it first "

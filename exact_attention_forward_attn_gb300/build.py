@@ -18,6 +18,9 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_NAME = "libgb300attn.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
+# The debug build (-DATTN_DEBUG): every kernel checks the indices behind its computed stores and
+# records a failed check in the device status word instead of storing (no trap).
+DEBUG_LIB_PATH = os.path.join(BUILD_DIR, "libgb300attn_debug.so")
 SOURCES = [os.path.join(CSRC, "attn_api.cu")]
 DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in (
     "attn_fwd_kernel.cuh", "attn_fwd_pair_kernel.cuh", "attn_fwd_d256_kernel.cuh", "attn_bwd_kernel.cuh",
@@ -44,20 +47,25 @@ def nvcc_command(out_path: str, extra=()) -> list:
             f"-I{CSRC}", f"-Xlinker", f"-rpath,{lib64}", *extra, "-o", out_path, *SOURCES]
 
 
-def is_fresh() -> bool:
-    if not os.path.exists(LIB_PATH):
+def is_fresh(path: str = LIB_PATH) -> bool:
+    if not os.path.exists(path):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(path)
     return all(os.path.getmtime(p) <= t for p in DEPENDS)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Compile the library unless it is up to date; returns its path."""
-    if is_fresh() and not force and not ptxas_info:
-        return LIB_PATH
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
+          debug: bool = False) -> str:
+    """Compile the library (or, with debug=True, its index-checking debug build) unless it is up
+    to date; returns its path."""
+    path = DEBUG_LIB_PATH if debug else LIB_PATH
+    if is_fresh(path) and not force and not ptxas_info:
+        return path
     os.makedirs(BUILD_DIR, exist_ok=True)
-    tmp = f"{LIB_PATH}.{os.getpid()}.tmp"
+    tmp = f"{path}.{os.getpid()}.tmp"
     extra = ["-Xptxas", "-v"] if ptxas_info else []
+    if debug:
+        extra.append("-DATTN_DEBUG")
     cmd = nvcc_command(tmp, extra)
     if verbose:
         print(" ".join(cmd), file=sys.stderr)
@@ -66,9 +74,10 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
         raise RuntimeError(f"nvcc failed ({res.returncode}):\n{res.stdout}\n{res.stderr}")
     if ptxas_info or verbose:
         print(res.stdout + res.stderr, file=sys.stderr)
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, path)
+    return path
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv,
+                debug="--debug" in sys.argv))

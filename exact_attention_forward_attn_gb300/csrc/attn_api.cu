@@ -25,8 +25,8 @@
 
 using namespace gb300attn;
 
-// Device status word: kernels OR failure flags into it (see attn_debug_status).
-__device__ unsigned int g_attn_status_word = 0;
+// The device status word (g_attn_status_word, ptx.cuh): kernels OR failure flags into it; the
+// host reads and clears it in attn_debug_status.
 // Claim counters of the persistent kernels, handed to launches round robin; each launch leaves
 // its counter at zero, and a launch that reuses a counter waits for the counter's previous launch.
 __device__ unsigned int g_fwd_sched[gb300attn::kSchedSlots] = {};
@@ -1041,6 +1041,8 @@ extern "C" const char* attn_status_string(int status) {
         case ATTN_ERR_SCRATCH:
             return "problem needs more split-KV scratch than the built-in buffer "
                    "(attn_fwd_splitkv_noalloc_max_bytes)";
+        case ATTN_ERR_RANGE:
+            return "an index check of the debug build failed (the access was skipped)";
         default: return "unknown status";
     }
 }
@@ -1061,6 +1063,7 @@ extern "C" int attn_debug_status(void* stream) {
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e);
     if (word & kDevTimeout) return ATTN_ERR_TIMEOUT;
+    if (word & kDevRange) return ATTN_ERR_RANGE;
     return (word & kDevSmemAlign) ? ATTN_ERR_ARCH : ATTN_OK;
 }
 

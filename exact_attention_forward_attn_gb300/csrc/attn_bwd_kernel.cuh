@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(256)
     for (int d = lane; d < D; d += 32) acc += __bfloat162float(o[d]) * __bfloat162float(g[d]);
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) delta[row] = acc;
+    if (lane == 0 && ATTN_DCHECK(row < rows)) delta[row] = acc;
 }
 
 // dK/dV layout: K_j, V_j resident; a 3-slot ring of Q_i (read by S^T(i), formed a step ahead,
@@ -486,7 +486,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         fence_proxy_async_smem();
         named_barrier_sync(1, kBwdEwThreads);
-        if (ok && warp == 0 && lane == 0) {
+        if (ok && warp == 0 && lane == 0 &&
+            ATTN_DCHECK(b < p.B && hkv < p.Hkv && j < p.n_tiles)) {
             for (int h = 0; h < kPanels; ++h) {
                 tma_store_4d(&tmap_dk, sbase + L::kRes0 + h * L::kPanelBytes, h * 64, j * 128, hkv, b);
                 tma_store_4d(&tmap_dv, sbase + L::kRes1 + h * L::kPanelBytes, h * 64, j * 128, hkv, b);
@@ -878,7 +879,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 uint32_t r[32];
                 tmem_ld32(lane_base + t_dq + half * kCols + cc * 32, r);
                 tmem_wait_ld();
-                if (row_g < p.N) {
+                if (row_g < p.N && ATTN_DCHECK(rix < static_cast<size_t>(p.B) * p.Hq * p.N)) {
 #pragma unroll
                     for (int c8 = 0; c8 < 4; ++c8) {
                         if (half * kCols + cc * 32 + c8 * 8 >= p.d_out) break;

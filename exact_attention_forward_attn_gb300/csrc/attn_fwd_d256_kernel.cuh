@@ -327,13 +327,13 @@ __global__ void __launch_bounds__(kW256Threads, 1)
                     st_shared_v4(prow + ((chunk ^ (row & 7)) << 4), w[0], w[1], w[2], w[3]);
                 }
             }
-            if (row_g < p.N)
+            if (row_g < p.N && ATTN_DCHECK(b < p.B && hq < p.Hq && m_tile < p.n_tiles))
                 p.lse[(static_cast<size_t>(b) * p.Hq + hq) * p.N + row_g] =
                     (m + __log2f(l)) * 0.69314718055994531f;
         }
         fence_proxy_async_smem();
         named_barrier_sync(1, 128);
-        if (ok && warp == 0 && lane == 0) {
+        if (ok && warp == 0 && lane == 0 && ATTN_DCHECK(b < p.B && hq < p.Hq && m_tile < p.n_tiles)) {
             for (int pn = 0; pn < 4; ++pn)
                 tma_store_4d(&tmap_o, sbase + L::kQ + pn * L::kPanel, pn * 64, m_tile * 128, hq, b);
             tma_store_commit_and_wait();

@@ -207,6 +207,13 @@ __device__ __forceinline__ FwdWork decode_work(const AttnParams& p, int item) {
     return w;
 }
 
+// Index invariants of a decoded work item (checked in debug builds).
+__device__ __forceinline__ bool work_in_range(const AttnParams& p, const FwdWork& w) {
+    return w.b >= 0 && w.b < p.B && w.hq >= 0 && w.hq < p.Hq && w.hkv >= 0 && w.hkv < p.Hkv &&
+           w.hkv == w.hq / p.group && w.tile0 >= 0 && w.tile0 < p.n_tiles && w.kv_begin >= 0 &&
+           w.kv_end <= p.n_tiles && w.split >= 0 && w.split < p.n_splits;
+}
+
 // kSplit = false: the whole KV range, bf16 O and LSE written to the outputs.
 // kSplit = true:  the KV range of one split (split index innermost in the item number); the fp32
 //                 O of that range (normalised by its own denominator) and its LSE go to the
@@ -336,6 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (item < 0) break;
                 const FwdWork w = decode_work<kSplit, kOne>(p, item);
+                if (lane == 0) (void)ATTN_DCHECK(item < p.items && work_in_range(p, w));
                 if (!(w.part0 || w.part1)) continue;
                 {  // K (kv = 0) or V (kv = 1), panel h
                     const int kv = lane / kPanels, h = lane % kPanels;
@@ -682,7 +690,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t r[32];
                     tmem_ld32(o_addr + cc * 32, r);  // warp-collective: every lane loads
                     tmem_wait_ld();
-                    if (row_g < p.N) {
+                    if (row_g < p.N && ATTN_DCHECK(work_in_range(p, we))) {
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
                             st_global_v4f(dst + cc * 32 + 4 * i, __uint_as_float(r[4 * i]) * inv_l,
@@ -691,7 +699,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                           __uint_as_float(r[4 * i + 3]) * inv_l);
                     }
                 }
-                if (row_g < p.N) p.ws_lse[prow] = (m + __log2f(l)) * kLn2;
+                if (row_g < p.N &&
+                    ATTN_DCHECK(prow < static_cast<size_t>(p.n_splits) * p.B * p.Hq * p.N))
+                    p.ws_lse[prow] = (m + __log2f(l)) * kLn2;
             } else {
                 // ---- epilogue: O = acc / l -> bf16, one 64-column panel at a time through this
                 // tile's P panel (free: O-done follows the last P.V), out with coalesced 16-byte
@@ -726,13 +736,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         uint32_t v0, v1, v2, v3;
                         ld_shared_v4(p1 + r * 128 + ((ch ^ (r & 7)) << 4), v0, v1, v2, v3);
                         const int col = h * 64 + ch * 8;
-                        if (q_row0 + r < p.N && col < p.d_out)
+                        if (q_row0 + r < p.N && col < p.d_out && ATTN_DCHECK(work_in_range(p, we)))
                             st_global_v4u(obase + static_cast<long long>(q_row0 + r) * p.o_sn + col,
                                           v0, v1, v2, v3);
                     }
                     named_barrier_sync(1 + t, 128);  // the panel may be written again
                 }
-                if (row_g < p.N)
+                if (row_g < p.N &&
+                    ATTN_DCHECK(static_cast<size_t>(we.bh) * p.N + row_g <
+                                static_cast<size_t>(p.B) * p.Hq * p.N))
                     p.lse[static_cast<size_t>(we.bh) * p.N + row_g] = (m + __log2f(l)) * kLn2;
             }
         }
@@ -768,6 +780,7 @@ __global__ void __launch_bounds__(256)
     const int i = static_cast<int>(row % N);
     const int last_kv = causal ? i / kBN : n_tiles - 1;
     const int n_valid = min(n_splits, last_kv / split_tiles + 1);
+    (void)ATTN_DCHECK(n_valid >= 1 && n_valid <= n_splits && last_kv < n_tiles);
     const size_t plane = static_cast<size_t>(BH) * N;  // rows per split
     float mx = -INFINITY;
     for (int s = 0; s < n_valid; ++s) mx = fmaxf(mx, ws_lse[s * plane + row]);

@@ -235,6 +235,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 if (item < 0) break;
                 const FwdWork w = decode_quad_work(p, item);
+                if (lane == 0) (void)ATTN_DCHECK(item < p.items && work_in_range(p, w));
                 {
                     const int kv = lane >> 1, h = lane & 1;
                     const CUtensorMap* map = kv ? &tmap_v : &tmap_k;
@@ -616,13 +617,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     uint32_t v0, v1, v2, v3;
                     ld_shared_v4(p1 + r * 128 + ((ch ^ (r & 7)) << 4), v0, v1, v2, v3);
                     const int col = h * 64 + ch * 8;
-                    if (q_row0 + r < p.N && col < p.d_out)
+                    if (q_row0 + r < p.N && col < p.d_out && ATTN_DCHECK(work_in_range(p, we)))
                         st_global_v4u(obase + static_cast<long long>(q_row0 + r) * p.o_sn + col,
                                       v0, v1, v2, v3);
                 }
                 named_barrier_sync(1 + t, 128);
             }
-            if (row_g < p.N)
+            if (row_g < p.N &&
+                ATTN_DCHECK(static_cast<size_t>(we.bh) * p.N + row_g <
+                            static_cast<size_t>(p.B) * p.Hq * p.N))
                 p.lse[static_cast<size_t>(we.bh) * p.N + row_g] = (m + __log2f(l)) * kLn2;
         }
         __syncwarp();

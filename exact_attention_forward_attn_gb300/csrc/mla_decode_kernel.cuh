@@ -172,6 +172,7 @@ __device__ __forceinline__ void mla_cluster_merge(const MlaParams& p, uint32_t s
             }
         }
         const size_t bh = static_cast<size_t>(b) * p.H + h;
+        if (!ATTN_DCHECK(b < p.B && r < 2)) continue;
         __nv_bfloat16* dst = p.out + bh * kMlaDc + r * 256;
         *reinterpret_cast<uint2*>(dst + 4 * lane) =
             make_uint2(pack_bf16x2(a0.x, a0.y), pack_bf16x2(a0.z, a0.w));
@@ -507,6 +508,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
             // (under the cluster merge the staged rows stay where they are)
             for (int rr = 0; rr < (p.cluster_merge ? 0 : 32); ++rr) {
                 if (h0 + rr >= p.H) break;  // warp-uniform
+                if (!ATTN_DCHECK(b < p.B && split < p.n_splits && r < 2)) break;
                 const size_t bh_r = static_cast<size_t>(b) * p.H + h0 + rr;
                 uint8_t* dst = split_out
                     ? reinterpret_cast<uint8_t*>(p.ws_o + (static_cast<size_t>(split) * p.B * p.H + bh_r) * kMlaDc + r * 256)
@@ -519,7 +521,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
             }
             if (p.cluster_merge) {
                 reinterpret_cast<float*>(smem + L::kLseStage)[row] = lse_nat;
-            } else if (h < p.H) {
+            } else if (h < p.H && ATTN_DCHECK(b < p.B && split < p.n_splits)) {
                 const size_t bh = static_cast<size_t>(b) * p.H + h;
                 if (split_out && r == 0)
                     p.ws_lse[static_cast<size_t>(split) * p.B * p.H + bh] = lse_nat;
@@ -616,7 +618,8 @@ __global__ void __launch_bounds__(kMlaMergeThreads)
         uint2 w2;
         w2.x = pack_bf16x2(acc.x * inv, acc.y * inv);
         w2.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-        *reinterpret_cast<uint2*>(out + static_cast<size_t>(row) * kMlaDc + 4 * col) = w2;
+        if (ATTN_DCHECK(row < BH && col < kMlaDc / 4))
+            *reinterpret_cast<uint2*>(out + static_cast<size_t>(row) * kMlaDc + 4 * col) = w2;
         if (col == 0) lse[row] = stats[rl][1];
     }
 }

@@ -181,9 +181,26 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
     return done != 0;
 }
 
-// Device-side failure flags (OR-ed into the library's status word).
+// Device-side failure flags, OR-ed into the library's status word (the host reads and clears it).
 constexpr unsigned kDevTimeout = 1u;
 constexpr unsigned kDevSmemAlign = 2u;  // dynamic shared memory not 1024-byte aligned
+constexpr unsigned kDevRange = 4u;      // an index check of the debug build failed
+
+__device__ unsigned int g_attn_status_word = 0;
+
+// ATTN_DCHECK(cond): in a debug build (ATTN_DEBUG defined) evaluates cond and, when it is false,
+// records kDevRange in the status word; its value is cond, so `if (ATTN_DCHECK(i < n)) a[i] = x;`
+// skips the access it guards.  In the ordinary build it is the constant true and cond is not
+// evaluated.  Nothing traps either way.
+#ifdef ATTN_DEBUG
+__device__ __forceinline__ bool debug_check(bool ok) {
+    if (!ok) atomicOr(&g_attn_status_word, kDevRange);
+    return ok;
+}
+#define ATTN_DCHECK(cond) (::gb300attn::debug_check(static_cast<bool>(cond)))
+#else
+#define ATTN_DCHECK(cond) true
+#endif
 
 // Time a wait may take before the CTA gives up (1 s; a healthy wait takes microseconds).
 constexpr uint64_t kWaitLimitNs = 1000000000ull;

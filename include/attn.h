@@ -53,7 +53,9 @@ typedef enum {
     ATTN_ERR_SPLITS = -12,  /* num_splits outside [0, 64] */
     ATTN_ERR_WORKSPACE = -13, /* workspace smaller than attn_fwd_splitkv_workspace_bytes() */
     ATTN_ERR_SCRATCH = -14, /* attn_fwd_splitkv_noalloc: more scratch needed than it has */
-    ATTN_ERR_STRIDE = -15   /* attn_fwd_strided: a stride is not usable by the TMA */
+    ATTN_ERR_STRIDE = -15,  /* attn_fwd_strided: a stride is not usable by the TMA */
+    ATTN_ERR_RANGE = -16    /* debug build only: an index check failed (reported by
+                               attn_debug_status; the access was skipped) */
 } attn_status_t;
 
 /*
@@ -188,9 +190,14 @@ int attn_last_cuda_error(void);
 /*
  * attn_debug_status - synchronise `stream`, then read and clear the device status word.
  * Returns ATTN_OK if no kernel of this library recorded a failure since the last call,
- * ATTN_ERR_TIMEOUT if a device-side bounded wait expired, ATTN_ERR_ARCH if a kernel found its
+ * ATTN_ERR_TIMEOUT if a device-side bounded wait expired, ATTN_ERR_RANGE if (in the debug build,
+ * compiled with ATTN_DEBUG) a kernel's index check failed, ATTN_ERR_ARCH if a kernel found its
  * dynamic shared memory not 1024-byte aligned (it then did no work), or ATTN_ERR_CUDA if the
  * synchronisation itself failed.  The status word is shared by all streams of the device.
+ * The debug build checks, before each store whose address it computes, that the indices behind
+ * it are in range (the decoded work item: batch, heads, tiles, split; rows of O, LSE, dQ, Delta
+ * and the split partials); a failed check records ATTN_ERR_RANGE and skips the store.  It stands
+ * in for a memory checker: it never traps.
  */
 int attn_debug_status(void* stream);
 

@@ -46,6 +46,15 @@ def test_library_exports_every_declared_symbol(lib):
     assert set(_lib.SIGNATURES) == set(_declared_functions())
 
 
+def test_debug_build_exports_every_declared_symbol():
+    """The index-checking debug build (ATTN_DEBUG) compiles and exports the same boundary."""
+    path = build.build(debug=True)
+    nm = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True,
+                        check=True).stdout
+    exported = set(re.findall(r"\bT\s+(\w+)$", nm, re.M))
+    assert set(_declared_functions()) <= exported
+
+
 def test_built_for_sm_103a_only():
     cmd = build.nvcc_command("/dev/null")
     assert "arch=compute_103a,code=sm_103a" in cmd
