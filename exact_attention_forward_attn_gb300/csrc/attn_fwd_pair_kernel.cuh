@@ -10,11 +10,15 @@
 //
 // Why pairs.  In the one-CTA kernel every K/V step moves ~320 KB through each SM's shared memory
 // (the K and V tiles written by the TMA, read by the S and P.V MMAs of both Q tiles, plus P's
-// shared-memory half), and shared memory, not the tensor pipe, sets its pace.  Here a cluster of
-// two CTAs on two SMs shares every MMA: M = 256 query rows, CTA r supplying rows 128r..128r+127
-// of A (its own Q or P) and half of B - for S = Q K^T keys 64r..64r+63 of the key tile, for
-// O += P V output columns 64r..64r+63 of V - so each SM loads and reads half of every K and V
-// tile: ~224 KB per step.  CTA r's tensor memory holds its own 128 rows of S and O.
+// shared-memory half), close to what an SM's shared memory delivers.  Here a cluster of two CTAs
+// on two SMs shares every MMA: M = 256 query rows, CTA r supplying rows 128r..128r+127 of A (its
+// own Q or P) and half of B - for S = Q K^T keys 64r..64r+63 of the key tile, for O += P V
+// output columns 64r..64r+63 of V - so each SM loads and reads half of every K and V tile:
+// ~224 KB per step.  CTA r's tensor memory holds its own 128 rows of S and O.
+// Measured on GB300 it is nevertheless slower than the one-CTA kernel (0.62-0.85x): a pair MMA
+// takes ~96 (SS) / ~123 (TS) cycles to issue for 64 cycles of work per SM, so two issuers per
+// two SMs halve the issue capacity per SM, and every step's commits and P-ready arrives cross
+// between the SMs.  attn_fwd therefore does not use it; attn_fwd_test_kernel runs it.
 //
 // Work item: a quad of four 128-row Q tiles of one (b, hq).  M-tile t (t = 0, 1) of the item is
 // rows 512u + 256t .. + 255; CTA r holds Q tile 4u + 2t + r of it.  Under the causal mask an
