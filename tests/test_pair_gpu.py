@@ -119,3 +119,19 @@ def test_pair_kernel_expired_wait_is_reported(cuda_lib):
     o_s = torch.stack([o2[b, h].cpu()[idx[b, h]] for b in range(w.B) for h in range(w.Hq)])
     l_s = torch.stack([l2[b, h].cpu()[idx[b, h]] for b in range(w.B) for h in range(w.Hq)])
     _check(o_s.reshape(o_ref.shape), l_s.reshape(l_ref.shape), o_ref, l_ref, "after the stall")
+
+
+def test_pair_kernel_long_ragged_sequence(cuda_lib):
+    """N = 70000 (137 quads per head, the last one ragged): 32 seeded rows per head."""
+    w = wl.random_case(1, 4, 1, 70000, 128, True, 2103)
+    q, k, v = wl.make_qkv(w)
+    out, lse = _run(cuda_lib, w, q.cuda(), k.cuda(), v.cuda(), 2)
+    rows = wl.sample_rows(w, 32)
+    rows[..., -1] = w.N - 1
+    rows = rows.sort(dim=-1).values
+    o_ref, l_ref = oracle.attn_ref(q, k, v, True, w.sm_scale, rows=rows.numpy())
+    idx = rows.long()
+    o_c, l_c = out.cpu(), lse.cpu()
+    o_s = torch.stack([o_c[0, h][idx[0, h]] for h in range(w.Hq)])
+    l_s = torch.stack([l_c[0, h][idx[0, h]] for h in range(w.Hq)])
+    _check(o_s.reshape(o_ref.shape), l_s.reshape(l_ref.shape), o_ref, l_ref, w.name)

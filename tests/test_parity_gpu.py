@@ -204,3 +204,35 @@ def test_gpu_side_argument_errors(cuda_lib):
     assert call(q.data_ptr(), q.data_ptr()) == -11           # out aliases q
     assert call(q.data_ptr(), out.data_ptr()) == 0
     torch.cuda.synchronize()
+
+
+LARGE = [
+    # (B, Hq, Hkv, N, D, causal): sequences beyond the configurations (ragged and power of two),
+    # and many short heads (items >> SMs)
+    (1, 2, 1, 100000, 128, True), (1, 2, 1, 131072, 128, True), (1, 2, 2, 65536, 64, False),
+    (64, 32, 8, 128, 128, True), (16, 48, 16, 300, 128, False),
+]
+
+
+@pytest.mark.parametrize("shape", LARGE, ids=[f"b{b}h{h}k{kv}n{n}d{d}{'c' if c else ''}"
+                                              for b, h, kv, n, d, c in LARGE])
+def test_large_shapes_sampled_rows(shape, cuda_lib):
+    """Long sequences and many heads: 32 seeded rows per head against the oracle (the first and
+    last rows included), every row finite and inside the convex hull of V."""
+    B, Hq, Hkv, N, D, causal = shape
+    w = wl.random_case(B, Hq, Hkv, N, D, causal, seed=3000 + N % 997 + D)
+    q, k, v = wl.make_qkv(w)
+    out, lse = _gpu(w, q, k, v)
+    rows = wl.sample_rows(w, min(32, N))
+    rows[..., 0] = 0
+    rows[..., -1] = N - 1
+    rows = rows.sort(dim=-1).values
+    o_ref, l_ref = oracle.attn_ref(q, k, v, w.causal, w.sm_scale, rows=rows.numpy())
+    idx = rows.long()
+    o_c, l_c = out.cpu(), lse.cpu()
+    o_s = torch.stack([o_c[b, h][idx[b, h]] for b in range(B) for h in range(Hq)])
+    l_s = torch.stack([l_c[b, h][idx[b, h]] for b in range(B) for h in range(Hq)])
+    _check(o_s.reshape(o_ref.shape), l_s.reshape(l_ref.shape), o_ref, l_ref, w.name)
+    o_all = out.float()
+    assert torch.isfinite(o_all).all() and torch.isfinite(lse).all()
+    assert o_all.abs().amax().item() <= v.float().abs().amax().item() * (1 + 1e-2) + 1e-2
