@@ -211,11 +211,28 @@ def causal_work(w, rows=None) -> float:
     return float(rows.numel()) * w.N
 
 
-def cpu_baseline_table(gpu_us=None):
+def _parity(o_gpu, l_gpu, o_ref, l_ref):
+    """max|dO|, max|dLSE| and whether every element is within the tolerance of the tests
+    (|dO| <= 2e-2 + 2e-2 |O_ref|, |dLSE| <= 1e-3)."""
+    import numpy as np
+
+    o = o_gpu.float().numpy().astype(np.float64)
+    l = l_gpu.numpy().astype(np.float64)
+    err = np.abs(o - o_ref)
+    lerr = np.abs(l - l_ref)
+    ok = bool(np.all(np.isfinite(o)) and not (err > 2e-2 + 2e-2 * np.abs(o_ref)).any()
+              and lerr.max() <= 1e-3)
+    return {"max_abs_dO": float(err.max()), "max_abs_dLSE": float(lerr.max()),
+            "within_tolerance": ok}
+
+
+def cpu_baseline_table(gpu_us=None, gpu_out=None):
     """The oracle as it stands, timed on the host cores at all cores and at one core: the five
     configurations in full (one-core C3, 0.27 TFLOP, on 128 seeded rows per head, extrapolated),
     the long-context lengths on the 64 seeded rows per head the parity tests compare,
-    extrapolated to every row by the exact work ratio (visible query-key pairs), labelled."""
+    extrapolated to every row by the exact work ratio (visible query-key pairs), labelled.
+    Where `gpu_out` holds the GPU's O and LSE of a workload (CPU tensors; for the long lengths
+    the rows the parity tests sample), the all-core run's results are also compared with them."""
     import oracle
     from exact_attention_forward_attn_gb300 import workloads as wl
 
@@ -238,16 +255,22 @@ def cpu_baseline_table(gpu_us=None):
             long_cfg = w.N > 4096
             if long_cfg or (threads == 1 and w.flops > 1e11):
                 rows = wl.sample_rows(w, 64 if long_cfg else 128)
-                dt = timed(lambda: oracle.attn_ref(q, k, v, w.causal, w.sm_scale,
-                                                   rows=rows.numpy(), n_threads=threads), 1)
+                res = {}
+                dt = timed(lambda: res.setdefault(0, oracle.attn_ref(
+                    q, k, v, w.causal, w.sm_scale, rows=rows.numpy(), n_threads=threads)), 1)
+                if long_cfg and threads == all_cores and gpu_out and w.name in gpu_out:
+                    entry["parity_sampled_rows"] = _parity(*gpu_out[w.name], *res[0])
                 scale = causal_work(w) / causal_work(w, rows)
                 entry[label] = {"s": dt * scale, "kind": "extrapolated",
                                 "sample": f"{rows.shape[2]} seeded rows per head, {dt:.2f} s"}
             else:
                 reps = 3 if w.flops < 2e10 else 1
-                dt = timed(lambda: oracle.attn_ref(q, k, v, w.causal, w.sm_scale,
-                                                   n_threads=threads), reps)
+                res = {}
+                dt = timed(lambda: res.__setitem__(0, oracle.attn_ref(
+                    q, k, v, w.causal, w.sm_scale, n_threads=threads)), reps)
                 entry[label] = {"s": dt, "kind": "full"}
+                if threads == all_cores and gpu_out and w.name in gpu_out:
+                    entry["parity"] = _parity(*gpu_out[w.name], *res[0])
             entry[label]["cores"] = threads
             entry[label]["tflops"] = w.flops / entry[label]["s"] / 1e12
         if gpu_us and w.name in gpu_us:
@@ -552,11 +575,23 @@ def main():
 
     # ---- context: the other long-context lengths (same kernel), not the headline -------------
     sweep = []
+    gpu_out = {}  # CPU copies of GPU outputs the CPU-baseline leg compares with the oracle
+
+    def keep_rows(wk, o, l):  # the rows the parity tests sample, for the long lengths
+        rows = wl.sample_rows(wk, 64).long()
+        oc, lc = o.cpu(), l.cpu()
+        gpu_out[wk.name] = (
+            torch.stack([oc[b, h][rows[b, h]] for b in range(wk.B) for h in range(wk.Hq)])
+            .reshape(wk.B, wk.Hq, -1, wk.D),
+            torch.stack([lc[b, h][rows[b, h]] for b in range(wk.B) for h in range(wk.Hq)])
+            .reshape(wk.B, wk.Hq, -1))
+
     if not args.no_sweep and rank == 0:
         for n in sorted(wl.LONG):
             if n == w.N and w.name.startswith("long"):
                 sweep.append({"N": n, "ms": mean_launch_ms, "tflops": achieved,
                               "frac": achieved / peak})
+                keep_rows(w, out, lse)
                 continue
             ws = wl.LONG[n]
             sq, sk, sv = (t.to(dev) for t in wl.make_qkv(ws))
@@ -572,6 +607,7 @@ def main():
             ms = statistics.mean(timed_launches(sstep, stream, 20))
             tf = ws.flops / (ms * 1e-3) / 1e12
             sweep.append({"N": n, "ms": ms, "tflops": tf, "frac": tf / peak})
+            keep_rows(ws, so, sl)
             del sq, sk, sv, so, sl
 
     # ---- context: the two D = 128 forward kernels side by side (the one-CTA kernel attn_fwd
@@ -649,6 +685,7 @@ def main():
                             "D": wc.D, "causal": wc.causal, "us": ms * 1e3, "tflops": tf,
                             "frac": tf / peak, "gbs": gbs, "hbm_frac": gbs / hbm,
                             "l2": "256 MB flush before each launch"})
+            gpu_out[wc.name] = (co.cpu(), cl.cpu())
             del cq, ck, cv, co, cl
 
     # ---- context: low-occupancy configurations, single pass vs split-KV (key-axis splits) -----
@@ -776,7 +813,7 @@ def main():
         if not args.no_sweep:
             gpu_us = {c["workload"]: c["us"] for c in configs}
             gpu_us.update({f"long-gqa8-causal-n{x['N']}": x["ms"] * 1e3 for x in sweep})
-            cpu_table = cpu_baseline_table(gpu_us)
+            cpu_table = cpu_baseline_table(gpu_us, gpu_out)
 
     if rank == 0:
         line = {

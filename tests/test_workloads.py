@@ -73,3 +73,25 @@ def test_mla_workloads_shapes_scale_and_determinism():
     assert torch.equal(q, q2) and torch.equal(kv, kv2)
     assert w.flops == 2 * 128 * 4096 * (576 + 512)
     assert w.bytes == 2 * 4096 * 576 + 2 * 128 * 576 + 2 * 128 * 512 + 4 * 128
+
+
+def test_bench_work_ratio_and_parity_helpers():
+    """bench.py's extrapolation ratio counts visible (query, key) pairs exactly, and its parity
+    summary applies the tests' tolerance."""
+    import numpy as np
+    import torch
+
+    import bench
+
+    w = wl.random_case(1, 2, 1, 10, 64, True, 1)
+    rows = torch.tensor([[[0, 9], [3, 4]]], dtype=torch.int32)
+    assert bench.causal_work(w) == 2 * 55                    # 1 + 2 + ... + 10 keys per head
+    assert bench.causal_work(w, rows) == (1 + 10) + (4 + 5)
+    wn = w.with_(causal=False)
+    assert bench.causal_work(wn) == 2 * 100 and bench.causal_work(wn, rows) == 4 * 10
+    ref_o = np.zeros((1, 2, 3, 4))
+    ref_l = np.zeros((1, 2, 3))
+    good = bench._parity(torch.full((1, 2, 3, 4), 0.015), torch.zeros(1, 2, 3), ref_o, ref_l)
+    bad = bench._parity(torch.full((1, 2, 3, 4), 0.03), torch.zeros(1, 2, 3), ref_o, ref_l)
+    assert good["within_tolerance"] and not bad["within_tolerance"]
+    assert abs(bad["max_abs_dO"] - 0.03) < 1e-6
