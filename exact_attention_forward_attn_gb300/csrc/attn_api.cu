@@ -15,6 +15,7 @@
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <utility>
 
 #include "attn.h"
 #include "attn_bwd_kernel.cuh"
@@ -427,9 +428,14 @@ int with_claim_counter(DeviceState* ds, cudaStream_t s, Launch&& launch) {
 
 // The persistent two-tile kernel: one CTA per SM (or per item, if fewer), each claiming items
 // until all `items` are taken.
-template <int D, bool kSplit, bool kOne = false>
+// `after` (if given) launches what must follow the kernel directly on the stream (the split
+// kernel's merge), inside the claim counter's scope.
+int no_follow_up() { return ATTN_OK; }
+
+template <int D, bool kSplit, bool kOne = false, class After = int (*)()>
 int launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-               const AttnParams& p, DeviceState* ds, int64_t items, cudaStream_t stream) {
+               const AttnParams& p, DeviceState* ds, int64_t items, cudaStream_t stream,
+               After&& after = no_follow_up) {
     AttnParams prm = p;
     prm.items = static_cast<int>(items);
     const int64_t grid = std::min<int64_t>(items, std::max(1, ds->num_sms));
@@ -439,7 +445,8 @@ int launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
                                            SmemLayout<D>::kAlloc, stream>>>(mq, mk, mv, prm,
                                                                             ds->status_word);
         const cudaError_t e = cudaGetLastError();
-        return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+        if (e != cudaSuccess) return cuda_fail(e);
+        return after();
     });
 }
 
@@ -489,14 +496,34 @@ int launch_single(int D, const CUtensorMap& mq, const CUtensorMap& mk, const CUt
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
 
+// Launches `kernel` right behind the previous kernel on `stream` with programmatic dependent
+// launch: it may be scheduled before that kernel has finished (once all of that kernel's CTAs
+// have started) and waits for it itself (griddep_wait) before it reads that kernel's results,
+// so its launch and set-up overlap the previous kernel's tail.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 template <int D>
 int launch_merge(const AttnParams& p, __nv_bfloat16* out, int d_out, cudaStream_t stream) {
     const int64_t rows = static_cast<int64_t>(p.B) * p.Hq * p.N;
     const int64_t blocks = (rows + kMergeThreads / 32 - 1) / (kMergeThreads / 32);
-    attn_splitkv_merge_kernel<D><<<static_cast<unsigned int>(blocks), kMergeThreads, 0, stream>>>(
-        p.ws_o, p.ws_lse, out, p.lse, p.B * p.Hq, p.N, d_out, p.n_tiles, p.causal, p.n_splits,
-        p.split_tiles);
-    const cudaError_t e = cudaGetLastError();
+    const cudaError_t e = launch_dependent(
+        attn_splitkv_merge_kernel<D>, dim3(static_cast<unsigned int>(blocks)), dim3(kMergeThreads),
+        0, stream, static_cast<const float*>(p.ws_o), static_cast<const float*>(p.ws_lse), out,
+        p.lse, p.B * p.Hq, p.N, d_out, p.n_tiles, p.causal, p.n_splits, p.split_tiles);
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
 
@@ -693,11 +720,14 @@ extern "C" int attn_fwd_splitkv(const void* q, const void* k, const void* v, voi
     prm.ws_lse = prm.ws_o + static_cast<int64_t>(n_splits) * P.bh * N * padded_dim(D);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int64_t items = P.items * n_splits;
-    st = D <= 64 ? launch_fwd<64, true>(mq, mk, mv, prm, ds, items, s)
-                 : launch_fwd<128, true>(mq, mk, mv, prm, ds, items, s);
-    if (st != ATTN_OK) return st;
     auto* o = static_cast<__nv_bfloat16*>(out);
-    return D <= 64 ? launch_merge<64>(prm, o, D, s) : launch_merge<128>(prm, o, D, s);
+    // the merge kernel follows the split kernel directly (programmatic dependent launch): the
+    // claim counter's completion event is recorded after both
+    auto after = [&]() {
+        return D <= 64 ? launch_merge<64>(prm, o, D, s) : launch_merge<128>(prm, o, D, s);
+    };
+    return D <= 64 ? launch_fwd<64, true>(mq, mk, mv, prm, ds, items, s, after)
+                   : launch_fwd<128, true>(mq, mk, mv, prm, ds, items, s, after);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -714,23 +744,27 @@ int launch_bwd(const Problem& P, const CUtensorMap& mq, const CUtensorMap& mk,
     unsigned int* status_word = ds->status_word;
     const int num_sms = ds->num_sms;
     const long long rows = P.bh * P.N;
-    attn_bwd_delta_kernel<<<static_cast<unsigned int>((rows + 7) / 8), 256, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), delta,
-        rows, P.D);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e);
-    attn_bwd_dkdv_kernel<D><<<static_cast<unsigned int>(P.n_tiles * P.bh_kv), kBwdThreads,
-                              DkdvSmem<D>::kAlloc, s>>>(mq, mk, mv, mdo, mdk, mdv, bp, status_word);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e);
-    // persistent: one CTA per SM (or per item, if fewer)
+    // persistent dQ: one CTA per SM (or per item, if fewer)
     const int64_t dq_grid = std::min<int64_t>(bp.items, std::max(1, num_sms));
+    // Delta, then dK/dV and dQ each launched directly behind the previous kernel (programmatic
+    // dependent launch: each waits for its predecessor before reading what it wrote); the claim
+    // counter (dQ's) covers the whole chain, so nothing else separates them on the stream.
     return with_claim_counter(ds, s, [&](unsigned int* counter) {
         bp.sched = counter;
-        attn_bwd_dq_kernel<D><<<static_cast<unsigned int>(dq_grid), kBwdThreads,
-                                DqSmem<D>::kAlloc, s>>>(mq, mk, mv, mdo, bp, status_word);
-        const cudaError_t e2 = cudaGetLastError();
-        return e2 == cudaSuccess ? ATTN_OK : cuda_fail(e2);
+        attn_bwd_delta_kernel<<<static_cast<unsigned int>((rows + 7) / 8), 256, 0, s>>>(
+            static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout),
+            delta, rows, P.D);
+        cudaError_t e = cudaGetLastError();
+        if (e == cudaSuccess)
+            e = launch_dependent(attn_bwd_dkdv_kernel<D>,
+                                 dim3(static_cast<unsigned int>(P.n_tiles * P.bh_kv)),
+                                 dim3(kBwdThreads), DkdvSmem<D>::kAlloc, s, mq, mk, mv, mdo, mdk,
+                                 mdv, bp, status_word);
+        if (e == cudaSuccess)
+            e = launch_dependent(attn_bwd_dq_kernel<D>, dim3(static_cast<unsigned int>(dq_grid)),
+                                 dim3(kBwdThreads), DqSmem<D>::kAlloc, s, mq, mk, mv, mdo, bp,
+                                 status_word);
+        return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
     });
 }
 
@@ -988,10 +1022,11 @@ int mla_decode_run(const void* q, const void* kv, void* out, float* lse, int B, 
     if (n_splits > 1 && !cluster) {
         const int64_t rows = static_cast<int64_t>(B) * H;
         const int64_t rows_per_block = 4 / mla_merge_groups(n_splits);
-        mla_merge_kernel<<<static_cast<unsigned int>((rows + rows_per_block - 1) / rows_per_block),
-                           kMlaMergeThreads, 0, s>>>(
-            prm.ws_o, prm.ws_lse, prm.out, lse, static_cast<int>(rows), n_splits);
-        e = cudaGetLastError();
+        e = launch_dependent(
+            mla_merge_kernel,
+            dim3(static_cast<unsigned int>((rows + rows_per_block - 1) / rows_per_block)),
+            dim3(kMlaMergeThreads), 0, s, static_cast<const float*>(prm.ws_o),
+            static_cast<const float*>(prm.ws_lse), prm.out, lse, static_cast<int>(rows), n_splits);
         if (e != cudaSuccess) return cuda_fail(e);
     }
     return ATTN_OK;

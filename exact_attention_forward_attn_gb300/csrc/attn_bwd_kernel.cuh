@@ -68,6 +68,7 @@ __global__ void __launch_bounds__(256)
                           long long rows, int D) {
     const int lane = threadIdx.x & 31;
     const long long row = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
+    griddep_launch_dependents();  // the dK/dV kernel waits for Delta itself
     if (row >= rows) return;
     const __nv_bfloat16* o = out + row * D;
     const __nv_bfloat16* g = dout + row * D;
@@ -179,6 +180,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    griddep_launch_dependents();  // the dQ kernel is launched right after this one
 
     // work: key tile j (smallest, i.e. heaviest under the causal mask, first), then (b, h_kv)
     const int bkv_count = p.B * p.Hkv;
@@ -288,6 +290,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                             h * 64, it_tile(it) * 128, it_head(it), b);
             }
         };
+        griddep_wait();  // Delta comes from the kernel launched right before this one
         if (n_it > 0) {
             fetch(0);
             load_q(0);
@@ -799,6 +802,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         __syncwarp();
     } else {
         // elementwise warps 0-7: query row `row` of tile i, keys c0 .. c0+63 of the key tile
+        griddep_wait();  // Delta is complete once the kernel launched right before this one is
         const int quarter = warp & 3, half = warp >> 2;
         const int row = quarter * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;

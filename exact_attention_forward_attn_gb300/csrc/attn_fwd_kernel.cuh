@@ -243,6 +243,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // the split instantiation's merge kernel may be scheduled as soon as every CTA has started
+    // (it waits for this kernel's partials itself)
+    if constexpr (kSplit) griddep_launch_dependents();
 
     // ---- setup (once per CTA) ------------------------------------------------------------------
     if (threadIdx.x == 0) {
@@ -776,6 +779,7 @@ __global__ void __launch_bounds__(256)
     constexpr int kCols = D / 32;
     const int lane = threadIdx.x & 31;
     const long long row = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
+    griddep_wait();  // launched as the split kernel's dependant: its partials are complete
     if (row >= static_cast<long long>(BH) * N) return;
     const int i = static_cast<int>(row % N);
     const int last_kv = causal ? i / kBN : n_tiles - 1;

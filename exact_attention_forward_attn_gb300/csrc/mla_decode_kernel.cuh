@@ -197,6 +197,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    griddep_launch_dependents();  // the merge kernel (more than 4 splits) waits for us itself
 
     // work: blockIdx = ((b * n_ht + ht) * 2 + r) * n_splits + split
     int item = static_cast<int>(blockIdx.x);
@@ -570,6 +571,7 @@ __global__ void __launch_bounds__(kMlaMergeThreads)
     const int g = (tid / kCols) % groups, col = tid % kCols;
     const int row = static_cast<int>(blockIdx.x) * rows_per_block + rl;
     const bool live = row < BH;
+    griddep_wait();  // launched as the decode kernel's dependant: its partials are complete
     if (live && g == 0 && col < 32) {  // one warp per row: weights and statistics
         const int lane = col;
         float mx = -INFINITY;

@@ -263,6 +263,22 @@ struct ArmedPhases {
 };
 
 // ------------------------------------------------------------------------------------------------
+// Programmatic dependent launch: a kernel launched right after another one on the same stream
+// with the programmatic-serialization attribute may start before the first one has finished.
+// The first kernel signals that its dependant may be scheduled (griddep_launch_dependents; its
+// CTAs run on regardless); the dependant blocks in griddep_wait until the first kernel has
+// completed and its memory is visible, before it touches anything the first kernel wrote.  In a
+// kernel launched without the attribute both are no-ops.
+// ------------------------------------------------------------------------------------------------
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// ------------------------------------------------------------------------------------------------
 // Thread-block clusters: the cluster-wide barrier and distributed shared memory (a CTA reading
 // the shared memory of another CTA of its cluster).
 // ------------------------------------------------------------------------------------------------

@@ -232,3 +232,49 @@ def test_graphs_of_the_same_launches_replay_concurrently(cuda_lib):
         for o, l in (*bufs, eager):
             assert torch.equal(o, ref[0]) and torch.equal(l, ref[1])
     assert attn.device_status(dev) == 0
+
+
+def test_dependent_launch_chains_in_a_cuda_graph(cuda_lib):
+    """The split-KV forward (partials kernel + merge kernel), the backward (Delta, dK/dV, dQ) and
+    the MLA decode with the merge kernel launch their second kernels as programmatic dependants;
+    captured into a CUDA graph and replayed, they give the eager launches' bits."""
+    import exact_attention_forward_attn_gb300 as attn
+
+    dev = torch.device("cuda:0")
+    w = wl.Workload("graph-chain", 1, 4, 2, 1500, 128, True, 47)
+    _, (qd, kd, vd) = _inputs(w, dev)
+    gen = torch.Generator().manual_seed(48)
+    do = torch.randn(qd.shape, generator=gen).to(torch.bfloat16).to(dev)
+    wm = wl.MlaWorkload("graph-mla", 1, 128, 2048, 49)
+    qm, kvm = wl.make_mla(wm, device=dev)
+    ws = torch.empty(attn.splitkv_workspace_bytes(w.B, w.Hq, w.N, w.D, 3), dtype=torch.uint8,
+                     device=dev)
+    wsm = torch.empty(max(16, attn.mla_decode_workspace_bytes(wm.B, wm.H, wm.T, 8)),
+                      dtype=torch.uint8, device=dev)
+
+    def run():
+        o, l = attn.attn_fwd_splitkv(qd, kd, vd, causal=True, num_splits=3, workspace=ws)
+        o2, l2 = attn.attn_fwd(qd, kd, vd, causal=True)
+        g = attn.attn_bwd(qd, kd, vd, o2, l2, do, causal=True)
+        m = attn.mla_decode(qm, kvm, wm.sm_scale, num_splits=8, workspace=wsm)
+        return (o, l, *g, *m)
+
+    ref = [t.clone() for t in run()]
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        run()
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        outs = run()
+    for _ in range(5):
+        for t in outs:
+            t.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        for a, b in zip(outs, ref):
+            assert torch.equal(a, b)
+    assert attn.device_status(dev) == 0
