@@ -418,12 +418,13 @@ int with_claim_counter(DeviceState* ds, cudaStream_t s, Launch&& launch) {
         e = cudaStreamWaitEvent(s, slot.done, 0);
         if (e != cudaSuccess) return cuda_fail(e);
     }
+    // The event is recorded whatever the launch returned: a chain that failed part-way may have
+    // enqueued a kernel that uses the counter, and the counter's next launch must wait for it.
     const int st = launch(ds->sched + idx);
-    if (st != ATTN_OK) return st;
     e = cudaEventRecord(slot.done, s);
-    if (e != cudaSuccess) return cuda_fail(e);
-    slot.recorded = true;
-    return ATTN_OK;
+    if (e == cudaSuccess) slot.recorded = true;
+    if (st != ATTN_OK) return st;
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
 
 // The persistent two-tile kernel: one CTA per SM (or per item, if fewer), each claiming items
