@@ -210,6 +210,7 @@ LARGE = [
     # (B, Hq, Hkv, N, D, causal): sequences beyond the configurations (ragged and power of two),
     # and many short heads (items >> SMs)
     (1, 2, 1, 100000, 128, True), (1, 2, 1, 131072, 128, True), (1, 2, 2, 65536, 64, False),
+    (1, 1, 1, 1 << 20, 64, True),  # a million keys: 4096 work items of up to 8192 key steps
     (64, 32, 8, 128, 128, True), (16, 48, 16, 300, 128, False),
 ]
 
