@@ -115,6 +115,12 @@ def attn_fwd(q, k, v, causal: bool = False, sm_scale: float | None = None, out=N
     return out, lse
 
 
+def fwd_num_splits(B: int, Hq: int, N: int, D: int, causal: bool = False) -> int:
+    """Key-axis splits ``attn_fwd`` itself uses for these sizes on the current device (1: single
+    pass; more: the splits of each work item merge inside a thread-block cluster)."""
+    return int(_lib.load().attn_fwd_num_splits(B, Hq, N, D, int(bool(causal))))
+
+
 def splitkv_num_splits(B: int, Hq: int, N: int, D: int, causal: bool = False) -> int:
     """Split count the library suggests for these sizes on the current device."""
     return int(_lib.load().attn_fwd_splitkv_num_splits(B, Hq, N, D, int(bool(causal))))
@@ -127,9 +133,10 @@ def splitkv_workspace_bytes(B: int, Hq: int, N: int, D: int, num_splits: int = 0
 
 def attn_fwd_splitkv(q, k, v, causal: bool = False, sm_scale: float | None = None,
                      num_splits: int = 0, workspace=None, out=None, lse=None):
-    """Split-KV forward (partials over key-axis splits + fused merge); same result as
-    ``attn_fwd`` up to rounding.  ``workspace``: optional CUDA tensor of at least
-    ``splitkv_workspace_bytes(...)`` bytes (allocated here when omitted)."""
+    """Split-KV forward (partials over key-axis splits + merge); same result as ``attn_fwd`` up
+    to rounding.  ``workspace``: optional CUDA tensor of at least ``splitkv_workspace_bytes(...)``
+    bytes (allocated here when omitted; left untouched when 2-4 splits merge inside clusters).
+    ``num_splits=1`` runs the single pass."""
     import torch
 
     B, Hq, Hkv, N, D = _check_inputs(q, k, v)

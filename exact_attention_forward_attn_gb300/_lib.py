@@ -26,6 +26,9 @@ SIGNATURES = {
     "attn_fwd_splitkv_workspace_bytes": (ctypes.c_size_t, [_c_int, _c_int, _c_int, _c_int,
                                                             _c_int]),
     "attn_fwd_splitkv_num_splits": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int]),
+    "attn_fwd_num_splits": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int]),
+    "attn_fwd_test_split_choice": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                            ctypes.POINTER(_c_int), _c_int, ctypes.c_longlong]),
     "attn_fwd_splitkv_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
                                           _c_int, _c_int, _c_int, _c_float, _c_int, _vp]),
     "attn_fwd_splitkv_noalloc_max_bytes": (ctypes.c_size_t, []),

@@ -14,8 +14,10 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <functional>
 #include <mutex>
 #include <utility>
+#include <vector>
 
 #include "attn.h"
 #include "attn_bwd_kernel.cuh"
@@ -145,19 +147,22 @@ struct DeviceState {
     std::atomic<unsigned int> sched_next{0};
     SchedSlot slots[kSchedSlots];
     int pair_clusters = 0;  // CTA pairs of the pair kernel that fit on the device at once
+    // clusters of n split CTAs (n = 2..kMaxClusterSplits) that fit on the device at once, for
+    // D <= 64 ([0]) and D <= 128 ([1])
+    int cluster_fit[2][kMaxClusterSplits + 1] = {};
 };
 DeviceState g_devices[kMaxDevices];
 
 // Opt in to the large shared-memory carve-out, and check that the kernel was built with the
 // per-thread register count its setmaxnreg split assumes (a launch with fewer registers would
 // leave the softmax warpgroups waiting for registers that do not exist).
-template <int D, bool kSplit, bool kOne = false>
+template <int D, bool kSplit, bool kOne = false, bool kCluster = false>
 cudaError_t opt_in_smem(bool* regs_ok) {
     cudaFuncAttributes a;
-    cudaError_t e = cudaFuncGetAttributes(&a, attn_fwd_kernel<D, kSplit, kOne>);
+    cudaError_t e = cudaFuncGetAttributes(&a, attn_fwd_kernel<D, kSplit, kOne, kCluster>);
     if (e != cudaSuccess) return e;
     if (a.numRegs != kLaunchRegs) *regs_ok = false;
-    return cudaFuncSetAttribute(attn_fwd_kernel<D, kSplit, kOne>,
+    return cudaFuncSetAttribute(attn_fwd_kernel<D, kSplit, kOne, kCluster>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 SmemLayout<D>::kAlloc);
 }
@@ -183,6 +188,32 @@ cudaError_t opt_in_pair(bool* regs_ok, int* clusters) {
         *clusters = 0;
     }
     return cudaSuccess;
+}
+
+// How many clusters of n CTAs of the cluster-merge split kernel fit on the device at once (a
+// cluster needs n SMs of one GPC).  If the device cannot say, none: the split-KV path then
+// always uses its workspace and merge kernel.
+template <int D>
+void query_cluster_fit(int* fit) {
+    for (int n = 2; n <= kMaxClusterSplits; ++n) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned int>(n));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = SmemLayout<D>::kAlloc;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned int>(n);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        fit[n] = 0;
+        if (cudaOccupancyMaxActiveClusters(&fit[n], attn_fwd_kernel<D, true, false, true>, &cfg) !=
+            cudaSuccess) {
+            (void)cudaGetLastError();
+            fit[n] = 0;
+        }
+    }
 }
 
 template <int D>
@@ -218,6 +249,8 @@ int device_state(int dev, DeviceState** out) {
         if (e == cudaSuccess) e = opt_in_smem<128, true>(&regs_ok);
         if (e == cudaSuccess) e = opt_in_smem<64, false, true>(&regs_ok);
         if (e == cudaSuccess) e = opt_in_smem<128, false, true>(&regs_ok);
+        if (e == cudaSuccess) e = opt_in_smem<64, true, false, true>(&regs_ok);
+        if (e == cudaSuccess) e = opt_in_smem<128, true, false, true>(&regs_ok);
         if (e == cudaSuccess) e = opt_in_bwd_smem<64>();
         if (e == cudaSuccess) e = opt_in_bwd_smem<128>();
         if (e == cudaSuccess)
@@ -228,6 +261,10 @@ int device_state(int dev, DeviceState** out) {
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      Fwd256Smem::kAlloc);
         if (e == cudaSuccess) e = opt_in_pair(&regs_ok, &st.pair_clusters);
+        if (e == cudaSuccess) {
+            query_cluster_fit<64>(st.cluster_fit[0]);
+            query_cluster_fit<128>(st.cluster_fit[1]);
+        }
         if (e != cudaSuccess) { st.status = ATTN_ERR_CUDA; st.cuda_error = e; return; }
         if (!regs_ok) st.status = ATTN_ERR_ARCH;
     });
@@ -528,6 +565,40 @@ int launch_merge(const AttnParams& p, __nv_bfloat16* out, int d_out, cudaStream_
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
 
+// Split-KV with 2..kMaxClusterSplits splits: the splits of a work item are one thread-block
+// cluster, one work unit per CTA (so no claim counter), and they merge their partials through
+// distributed shared memory at the end: no workspace, no merge kernel.
+template <int D>
+int launch_cluster_split(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                         const AttnParams& p, DeviceState* ds, int64_t units,
+                         cudaStream_t stream) {
+    AttnParams prm = p;
+    prm.items = static_cast<int>(units);
+    prm.sched = nullptr;
+    prm.ws_o = nullptr;
+    prm.ws_lse = nullptr;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned int>(units));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = SmemLayout<D>::kAlloc;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned int>(p.n_splits);  // the item's splits
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, attn_fwd_kernel<D, true, false, true>, mq, mk,
+                                             mv, prm, ds->status_word);
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+// Whether `items` work items split n ways run as clusters that all fit on the device at once.
+bool cluster_fits(const DeviceState* ds, int D, int64_t items, int n) {
+    return n >= 2 && n <= kMaxClusterSplits && D <= 128 && items <= ds->cluster_fit[D > 64][n];
+}
+
 // Effective split layout for a requested count: tiles per split and the number of non-empty
 // splits (every split but the last holds split_tiles KV tiles).
 void split_layout(int64_t n_tiles, int requested, int* split_tiles, int* n_splits) {
@@ -537,24 +608,211 @@ void split_layout(int64_t n_tiles, int requested, int* split_tiles, int* n_split
     *n_splits = static_cast<int>((n_tiles + tps - 1) / tps);
 }
 
-// Split only when the query tiles alone leave SMs idle, and only as far as every split keeps at
-// least kMinSplitTiles key tiles: below that the per-CTA start-up, the fp32 partials and the
-// merge launch cost more than the extra parallelism gains (measured on mha-n512 / mqa-n512).
-constexpr int64_t kMinSplitTiles = 4;
-int heuristic_splits(int64_t items, int64_t n_tiles, int num_sms) {
-    if (items >= num_sms) return 1;
-    int64_t s = num_sms / items;
-    if (s > n_tiles / kMinSplitTiles) s = n_tiles / kMinSplitTiles;
-    if (s > 16) s = 16;
-    return s < 1 ? 1 : static_cast<int>(s);
-}
-
 // The kernels compute on D padded to 64 or 128 columns (the TMA zero-fills the rest), so the
 // fp32 partials are D_pad wide.
 int64_t padded_dim(int64_t D) { return D <= 64 ? 64 : 128; }
 
 int64_t workspace_bytes_for(int64_t bh, int64_t N, int64_t D, int n_splits) {
     return static_cast<int64_t>(n_splits) * bh * N * (padded_dim(D) + 1) * 4;
+}
+
+// ---- split choice: a cost model of the forward's launches -------------------------------------
+// Estimated time (us) of a launch, calibrated on GB300 against CUDA-event times of 80 problems
+// (B = 1, Hq 1-8, N 1024-16384, D 64 and 128, causal or not; cold L2) for the single pass and for
+// 2-4 splits on either split path; it ranks the choices within ~7 % RMS:
+//   kLaunchUs        launch, start-up and tail of a persistent or one-unit-per-CTA launch
+//   kPairStepUs      a key tile of a work unit in which both of its Q tiles take part
+//   kLoneStepUs      a key tile of a unit with one Q tile taking part (one-tile items; the
+//                    causal diagonal's extra step)
+//   kUnitUs          a unit's Q load and epilogue
+//   kMergeUs + traffic / kMergeBytesPerUs   the workspace path: fp32 partials written by the split
+//                    kernel and read by the merge kernel (n_splits x rows x (D_pad + 1) x 4 bytes,
+//                    both ways), the merge's own launch hidden behind the split kernel's tail
+//   kClusterLaunchUs the cluster path's launch, start-up and in-cluster merge (staging O and LSE
+//                    in shared memory and reading the peers' rows through distributed shared
+//                    memory)
+// The persistent launches claim units heaviest first, so their makespan is that of list
+// scheduling in claim order over min(units, SMs) workers; a cluster launch runs every unit at
+// once (one wave), so its makespan is its longest unit.
+constexpr double kLaunchUs = 10.0, kPairStepUs = 1.2, kLoneStepUs = 1.0, kUnitUs = 0.5;
+constexpr double kSkipUnitUs = 0.2;  // a unit whose Q tiles see none of its split's keys
+constexpr double kMergeUs = 2.0, kMergeBytesPerUs = 3.0e6;
+constexpr double kClusterLaunchUs = 17.5;
+constexpr int kModelMaxSplits = 16;
+
+struct ForwardShape {
+    int64_t bh, n_tiles;
+    int D;
+    bool causal;
+};
+
+// What the model needs of the device: its SM count and how many clusters of n split CTAs fit at
+// once (for the shape's head dimension).
+struct SplitDevice {
+    int num_sms;
+    int cluster_fit[kMaxClusterSplits + 1];
+    bool fits(int64_t items, int n) const {
+        return n >= 2 && n <= kMaxClusterSplits && items <= cluster_fit[n];
+    }
+};
+SplitDevice split_device(const DeviceState* ds, int D) {
+    SplitDevice d{ds->num_sms, {}};
+    for (int n = 0; n <= kMaxClusterSplits; ++n) d.cluster_fit[n] = ds->cluster_fit[D > 64][n];
+    return d;
+}
+
+// Key-tile steps of Q tiles 2p and 2p + 1 (s0, s1) within KV tiles [kb, ke).
+inline void unit_steps(const ForwardShape& f, int64_t p, int64_t kb, int64_t ke, int64_t* s0,
+                       int64_t* s1) {
+    const int64_t t0 = 2 * p, t1 = 2 * p + 1;
+    const int64_t l0 = std::min(ke - 1, f.causal ? t0 : f.n_tiles - 1);
+    const int64_t l1 = std::min(ke - 1, f.causal ? t1 : f.n_tiles - 1);
+    *s0 = std::max<int64_t>(0, l0 - kb + 1);
+    *s1 = t1 < f.n_tiles ? std::max<int64_t>(0, l1 - kb + 1) : 0;
+}
+
+inline double unit_cost(int64_t s0, int64_t s1) {
+    if (s0 == 0 && s1 == 0) return kSkipUnitUs;
+    return kUnitUs + kPairStepUs * static_cast<double>(std::min(s0, s1)) +
+           kLoneStepUs * static_cast<double>(std::max(s0, s1) - std::min(s0, s1));
+}
+
+// List scheduling over `workers`, units in claim order: each goes to the earliest-free worker.
+class Makespan {
+  public:
+    explicit Makespan(int64_t workers) : free_(static_cast<size_t>(workers), 0.0) {}
+    void add(double cost) {
+        std::pop_heap(free_.begin(), free_.end(), std::greater<double>());
+        free_.back() += cost;
+        std::push_heap(free_.begin(), free_.end(), std::greater<double>());
+    }
+    double value() const { return *std::max_element(free_.begin(), free_.end()); }
+
+  private:
+    std::vector<double> free_;  // min-heap of the workers' finishing times
+};
+
+// The single pass: pairs of Q tiles, or single Q tiles when pairs would leave more than half of
+// the SMs idle (as prefer_single_tiles decides).
+double estimate_single(const ForwardShape& f, int num_sms) {
+    const int64_t pairs = (f.n_tiles + 1) / 2;
+    const bool one = 2 * pairs * f.bh <= num_sms;
+    const int64_t items = (one ? f.n_tiles : pairs) * f.bh;
+    Makespan ms(std::min<int64_t>(items, num_sms));
+    if (one) {
+        for (int64_t t = f.n_tiles - 1; t >= 0; --t) {
+            const double c = kUnitUs + kLoneStepUs * static_cast<double>(f.causal ? t + 1 : f.n_tiles);
+            for (int64_t h = 0; h < f.bh; ++h) ms.add(c);
+        }
+    } else {
+        for (int64_t p = pairs - 1; p >= 0; --p) {
+            int64_t s0, s1;
+            unit_steps(f, p, 0, f.n_tiles, &s0, &s1);
+            const double c = unit_cost(s0, s1);
+            for (int64_t h = 0; h < f.bh; ++h) ms.add(c);
+        }
+    }
+    return kLaunchUs + ms.value();
+}
+
+// n splits of tps key tiles each; `cluster`: merged inside one-wave clusters, else through the
+// workspace and the merge kernel.
+double estimate_split(const ForwardShape& f, int tps, int n, bool cluster, int num_sms) {
+    const int64_t pairs = (f.n_tiles + 1) / 2;
+    if (cluster) {  // one wave: the longest unit (the last pair's, or the first split's)
+        double longest = 0.0;
+        for (int64_t p = pairs - 1; p >= std::max<int64_t>(0, pairs - 2); --p)
+            for (int k = 0; k < n; ++k) {
+                int64_t s0, s1;
+                unit_steps(f, p, int64_t(k) * tps, std::min<int64_t>(f.n_tiles, int64_t(k + 1) * tps),
+                           &s0, &s1);
+                longest = std::max(longest, unit_cost(s0, s1));
+            }
+        return kClusterLaunchUs + longest;
+    }
+    Makespan ms(std::min<int64_t>(pairs * f.bh * n, num_sms));
+    for (int64_t p = pairs - 1; p >= 0; --p) {
+        double c[kMaxSplits];
+        for (int k = 0; k < n; ++k) {
+            int64_t s0, s1;
+            unit_steps(f, p, int64_t(k) * tps, std::min<int64_t>(f.n_tiles, int64_t(k + 1) * tps),
+                       &s0, &s1);
+            c[k] = unit_cost(s0, s1);
+        }
+        for (int64_t h = 0; h < f.bh; ++h)
+            for (int k = 0; k < n; ++k) ms.add(c[k]);
+    }
+    const double traffic = 2.0 * n * static_cast<double>(f.bh) * f.n_tiles * kBM *
+                           (padded_dim(f.D) + 1) * 4.0;
+    return kLaunchUs + ms.value() + kMergeUs + traffic / kMergeBytesPerUs;
+}
+
+// The split count with the lowest estimate: the single pass or 2..kModelMaxSplits splits
+// (cluster_only: only splits that merge inside one-wave clusters, as attn_fwd can run without a
+// workspace; max_ws: the largest workspace a workspace-path candidate may need).  Problems with at
+// least twice as many Q-tile pairs as SMs are not split: their single pass already fills the SMs
+// in balanced waves.  A split must beat the single pass by kSplitMarginUs.
+constexpr double kSplitMarginUs = 1.0;
+int choose_splits(const ForwardShape& f, const SplitDevice& dev, bool cluster_only,
+                  int64_t max_ws) {
+    const int64_t pairs = (f.n_tiles + 1) / 2;
+    const int64_t items = pairs * f.bh;
+    if (f.D > 128 || f.n_tiles < 2 || items >= 2 * static_cast<int64_t>(dev.num_sms)) return 1;
+    int best = 1;
+    double best_us = estimate_single(f, dev.num_sms) - kSplitMarginUs;
+    int last_n = 1;
+    for (int want = 2; want <= (cluster_only ? kMaxClusterSplits : kModelMaxSplits); ++want) {
+        int tps = 0, n = 0;
+        split_layout(f.n_tiles, want, &tps, &n);
+        if (n == last_n) continue;  // the same layout as a smaller request
+        last_n = n;
+        const bool cluster = dev.fits(items, n);
+        if (cluster_only && !cluster) continue;
+        if (!cluster_only && workspace_bytes_for(f.bh, f.n_tiles * kBM, f.D, n) > max_ws) continue;
+        const double us = estimate_split(f, tps, n, cluster, dev.num_sms);
+        if (us < best_us) {
+            best = n;
+            best_us = us;
+        }
+    }
+    return best;
+}
+
+// attn_fwd's own split: cluster candidates only, closed form (no simulation of more than one
+// wave), so it costs the launch path nothing worth measuring.
+int auto_splits(const Problem& P, const DeviceState* ds) {
+    if (2 * P.items > ds->num_sms) return 1;  // pairs beyond half the SMs: no cluster split fits
+    const ForwardShape f{P.bh, P.n_tiles, P.D, P.causal != 0};
+    return choose_splits(f, split_device(ds, P.D), true, 0);
+}
+
+// attn_fwd_splitkv's default split count, cached per shape (the list-scheduling estimate of a
+// few thousand units takes up to a few milliseconds of host time).
+struct SplitCacheKey {
+    int64_t bh, n_tiles, max_ws;
+    int dev, D, causal;
+    bool operator==(const SplitCacheKey& o) const {
+        return bh == o.bh && n_tiles == o.n_tiles && max_ws == o.max_ws && dev == o.dev &&
+               D == o.D && causal == o.causal;
+    }
+};
+std::mutex g_split_cache_lock;
+std::vector<std::pair<SplitCacheKey, int>> g_split_cache;  // small; cleared when it grows
+
+int default_splits(int64_t bh, int64_t N, int D, bool causal, int64_t max_ws,
+                   const DeviceState* ds, int dev) {
+    const ForwardShape f{bh, (N + kBM - 1) / kBM, D <= 64 ? 64 : 128, causal};
+    const SplitCacheKey key{bh, f.n_tiles, max_ws, dev, f.D, causal ? 1 : 0};
+    {
+        std::lock_guard<std::mutex> guard(g_split_cache_lock);
+        for (const auto& e : g_split_cache)
+            if (e.first == key) return e.second;
+    }
+    const int n = choose_splits(f, split_device(ds, D), false, max_ws);
+    std::lock_guard<std::mutex> guard(g_split_cache_lock);
+    if (g_split_cache.size() >= 1024) g_split_cache.clear();
+    g_split_cache.emplace_back(key, n);
+    return n;
 }
 
 }  // namespace
@@ -571,20 +829,44 @@ static bool prefer_single_tiles(Problem& P, const DeviceState* ds, AttnParams* p
     return true;
 }
 
+// The forward of a validated, non-empty problem: the single pass, or (allow_split) the split
+// that auto_splits picks.
+static int run_forward(Problem& P, bool allow_split, cudaStream_t s) {
+    DeviceState* ds = nullptr;
+    CUtensorMap mq, mk, mv, mo;
+    AttnParams prm;
+    int st = prepare(P, &ds, &mq, &mk, &mv, &mo, &prm);
+    if (st != ATTN_OK) return st;
+    const int n = allow_split ? auto_splits(P, ds) : 1;
+    if (n > 1) {
+        split_layout(P.n_tiles, n, &prm.split_tiles, &prm.n_splits);
+        return P.D <= 64 ? launch_cluster_split<64>(mq, mk, mv, prm, ds, P.items * prm.n_splits, s)
+                         : launch_cluster_split<128>(mq, mk, mv, prm, ds, P.items * prm.n_splits, s);
+    }
+    const bool one_tile = prefer_single_tiles(P, ds, &prm);
+    return launch_single(P.D, mq, mk, mv, mo, prm, ds, P.items, s, one_tile);
+}
+
 extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B,
                         int Hq, int Hkv, int N, int D, int causal, float sm_scale, void* stream) {
     Problem P{q, k, v, out, lse, B, Hq, Hkv, N, D, causal, sm_scale};
     bool empty = false;
-    int st = validate(P, &empty);
+    const int st = validate(P, &empty);
     if (st != ATTN_OK || empty) return st;
+    return run_forward(P, true, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int attn_fwd_num_splits(int B, int Hq, int N, int D, int causal) {
+    if (B <= 0 || Hq <= 0 || N <= 0 || D % 8 != 0 || D < 8 || D > 256) return 1;
     DeviceState* ds = nullptr;
-    CUtensorMap mq, mk, mv, mo;
-    AttnParams prm;
-    st = prepare(P, &ds, &mq, &mk, &mv, &mo, &prm);
-    if (st != ATTN_OK) return st;
-    const bool one_tile = prefer_single_tiles(P, ds, &prm);
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return launch_single(D, mq, mk, mv, mo, prm, ds, P.items, s, one_tile);
+    if (current_device_state(&ds) != ATTN_OK) return 1;
+    Problem P{};
+    P.D = D;
+    P.causal = causal;
+    P.bh = static_cast<int64_t>(B) * Hq;
+    P.n_tiles = (static_cast<int64_t>(N) + kBM - 1) / kBM;
+    P.items = (P.n_tiles + 1) / 2 * P.bh;
+    return auto_splits(P, ds);
 }
 
 extern "C" int attn_fwd_strided(const void* q, const void* k, const void* v, void* out,
@@ -601,16 +883,9 @@ extern "C" int attn_fwd_strided(const void* q, const void* k, const void* v, voi
     P.sv = {v_strides[2], v_strides[1], v_strides[0]};
     P.so = {o_strides[2], o_strides[1], o_strides[0]};
     bool empty = false;
-    int st = validate(P, &empty);
+    const int st = validate(P, &empty);
     if (st != ATTN_OK || empty) return st;
-    DeviceState* ds = nullptr;
-    CUtensorMap mq, mk, mv, mo;
-    AttnParams prm;
-    st = prepare(P, &ds, &mq, &mk, &mv, &mo, &prm);
-    if (st != ATTN_OK) return st;
-    const bool one_tile = prefer_single_tiles(P, ds, &prm);
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return launch_single(D, mq, mk, mv, mo, prm, ds, P.items, s, one_tile);
+    return run_forward(P, true, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int attn_fwd_test_stall(const void* q, const void* k, const void* v, void* out,
@@ -636,7 +911,7 @@ extern "C" int attn_fwd_test_stall(const void* q, const void* k, const void* v, 
 extern "C" int attn_fwd_test_kernel(const void* q, const void* k, const void* v, void* out,
                                     float* lse, int B, int Hq, int Hkv, int N, int D, int causal,
                                     float sm_scale, int kernel, int stall_item, void* stream) {
-    if (kernel != 1 && kernel != 2) return ATTN_ERR_SHAPE;
+    if (kernel < 1 || kernel > 3) return ATTN_ERR_SHAPE;
     if (stall_item < -1) return ATTN_ERR_SHAPE;
     if (D > 128 || (kernel == 2 && D <= 64)) return ATTN_ERR_HEADDIM;
     Problem P{q, k, v, out, lse, B, Hq, Hkv, N, D, causal, sm_scale};
@@ -654,31 +929,73 @@ extern "C" int attn_fwd_test_kernel(const void* q, const void* k, const void* v,
         if (ds->pair_clusters < 1) return ATTN_ERR_ARCH;
         return launch_pair(P, mq, prm, ds, s);
     }
+    if (kernel == 3) {  // two key-axis splits merged inside clusters
+        split_layout(P.n_tiles, 2, &prm.split_tiles, &prm.n_splits);
+        if (prm.n_splits != 2 || !cluster_fits(ds, D, P.items, 2)) return ATTN_ERR_SHAPE;
+        return D <= 64 ? launch_cluster_split<64>(mq, mk, mv, prm, ds, P.items * 2, s)
+                       : launch_cluster_split<128>(mq, mk, mv, prm, ds, P.items * 2, s);
+    }
     return D <= 64 ? launch_fwd<64, false>(mq, mk, mv, prm, ds, P.items, s)
                    : launch_fwd<128, false>(mq, mk, mv, prm, ds, P.items, s);
 }
 
-extern "C" int attn_fwd_splitkv_num_splits(int B, int Hq, int N, int D, int causal) {
-    (void)causal;
-    if (B <= 0 || Hq <= 0 || N <= 0 || D > 128) return 1;  // D > 128: single pass only
-    DeviceState* ds = nullptr;
-    if (current_device_state(&ds) != ATTN_OK) return 1;
+extern "C" int attn_fwd_test_split_choice(int B, int Hq, int N, int D, int causal, int num_sms,
+                                          const int* cluster_fit, int cluster_only,
+                                          long long max_ws) {
+    if (B <= 0 || Hq <= 0 || N <= 0 || D % 8 != 0 || D < 8 || D > 256 || num_sms <= 0 ||
+        !cluster_fit || max_ws < 0)
+        return ATTN_ERR_SHAPE;
+    SplitDevice dev{num_sms, {}};
+    for (int n = 2; n <= kMaxClusterSplits; ++n) dev.cluster_fit[n] = cluster_fit[n - 2];
+    const int64_t bh = static_cast<int64_t>(B) * Hq;
     const int64_t n_tiles = (static_cast<int64_t>(N) + kBM - 1) / kBM;
-    const int64_t items = (n_tiles + 1) / 2 * static_cast<int64_t>(B) * Hq;
-    int tps = 0, n = 0;
-    split_layout(n_tiles, heuristic_splits(items, n_tiles, ds->num_sms), &tps, &n);
-    return n;
+    if (cluster_only && 2 * ((n_tiles + 1) / 2) * bh > num_sms) return 1;  // as auto_splits
+    const ForwardShape f{bh, n_tiles, D, causal != 0};
+    const int n = choose_splits(f, dev, cluster_only != 0, max_ws);
+    int tps = 0, eff = 0;
+    split_layout(n_tiles, n, &tps, &eff);
+    return eff;
+}
+
+namespace {
+// The default split count for these sizes on the current device (1 on any failure), limited to
+// splits whose workspace fits max_ws bytes.
+int splitkv_default(int B, int Hq, int N, int D, int causal, int64_t max_ws) {
+    if (B <= 0 || Hq <= 0 || N <= 0 || D % 8 != 0 || D < 8 || D > 128) return 1;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 1;
+    }
+    DeviceState* ds = nullptr;
+    if (device_state(dev, &ds) != ATTN_OK) return 1;
+    const int n = default_splits(static_cast<int64_t>(B) * Hq, N, D, causal != 0, max_ws, ds, dev);
+    int tps = 0, eff = 0;
+    split_layout((static_cast<int64_t>(N) + kBM - 1) / kBM, n, &tps, &eff);
+    return eff;
+}
+}  // namespace
+
+extern "C" int attn_fwd_splitkv_num_splits(int B, int Hq, int N, int D, int causal) {
+    return splitkv_default(B, Hq, N, D, causal, INT64_MAX);
 }
 
 extern "C" size_t attn_fwd_splitkv_workspace_bytes(int B, int Hq, int N, int D, int num_splits) {
     if (B <= 0 || Hq <= 0 || N <= 0 || D % 8 != 0 || D < 8 || D > 256) return 0;
     if (D > 128) return 0;  // single pass
-    if (num_splits == 0) num_splits = attn_fwd_splitkv_num_splits(B, Hq, N, D, 0);
     const int64_t n_tiles = (static_cast<int64_t>(N) + kBM - 1) / kBM;
-    int tps = 0, n = 0;
-    split_layout(n_tiles, num_splits, &tps, &n);
-    if (n <= 1) return 0;
-    return static_cast<size_t>(workspace_bytes_for(static_cast<int64_t>(B) * Hq, N, D, n));
+    const int64_t bh = static_cast<int64_t>(B) * Hq;
+    auto bytes = [&](int requested) -> int64_t {
+        int tps = 0, n = 0;
+        split_layout(n_tiles, requested, &tps, &n);
+        return n <= 1 ? 0 : workspace_bytes_for(bh, N, D, n);
+    };
+    // The default count depends on the causal mask, which this query does not take: enough for
+    // either.
+    if (num_splits == 0)
+        return static_cast<size_t>(std::max(bytes(attn_fwd_splitkv_num_splits(B, Hq, N, D, 0)),
+                                            bytes(attn_fwd_splitkv_num_splits(B, Hq, N, D, 1))));
+    return static_cast<size_t>(bytes(num_splits));
 }
 
 extern "C" int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* out,
@@ -694,9 +1011,11 @@ extern "C" int attn_fwd_splitkv(const void* q, const void* k, const void* v, voi
     int split_tiles = 0, n_splits = 0;
     split_layout(P.n_tiles, num_splits, &split_tiles, &n_splits);
     if (D > 128) n_splits = 1;  // the wide-head kernel has no split variant
-    if (n_splits <= 1)  // one split is the ordinary forward; the workspace is not touched
-        return attn_fwd(q, k, v, out, lse, B, Hq, Hkv, N, D, causal, sm_scale, stream);
+    if (n_splits <= 1)  // one split is the single pass; the workspace is not touched
+        return run_forward(P, false, static_cast<cudaStream_t>(stream));
 
+    // The workspace is checked the same way whichever path runs below, so the call's result
+    // does not depend on how many clusters the device fits.
     const int64_t need = workspace_bytes_for(P.bh, N, D, n_splits);
     if (!workspace) return ATTN_ERR_NULL;
     if (reinterpret_cast<uintptr_t>(workspace) & 15u) return ATTN_ERR_ALIGN;
@@ -717,10 +1036,17 @@ extern "C" int attn_fwd_splitkv(const void* q, const void* k, const void* v, voi
         return ATTN_ERR_MEMORY;
     prm.n_splits = n_splits;
     prm.split_tiles = split_tiles;
-    prm.ws_o = static_cast<float*>(workspace);
-    prm.ws_lse = prm.ws_o + static_cast<int64_t>(n_splits) * P.bh * N * padded_dim(D);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int64_t items = P.items * n_splits;
+    // Splits whose clusters all fit on the device at once merge inside their cluster (the
+    // workspace stays untouched); otherwise the persistent split kernel writes the partials to
+    // the workspace and the merge kernel combines them (its dynamic claims balance the uneven
+    // causal splits over several waves, which a one-unit-per-CTA cluster launch cannot).
+    if (cluster_fits(ds, D, P.items, n_splits))
+        return D <= 64 ? launch_cluster_split<64>(mq, mk, mv, prm, ds, items, s)
+                       : launch_cluster_split<128>(mq, mk, mv, prm, ds, items, s);
+    prm.ws_o = static_cast<float*>(workspace);
+    prm.ws_lse = prm.ws_o + static_cast<int64_t>(n_splits) * P.bh * N * padded_dim(D);
     auto* o = static_cast<__nv_bfloat16*>(out);
     // the merge kernel follows the split kernel directly (programmatic dependent launch): the
     // claim counter's completion event is recorded after both
@@ -1114,7 +1440,7 @@ extern "C" int attn_debug_status(void* stream) {
 // ------------------------------------------------------------------------------------------------
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB
+constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;  // 64 MiB
 static __device__ __align__(256) unsigned char g_splitkv_scratch[kNoAllocScratchBytes];
 
 // In host code `g_splitkv_scratch` only names a host-side stand-in for the device array, so the
@@ -1157,7 +1483,10 @@ extern "C" int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void
     bool empty = false;
     const int st = validate(P, &empty);
     if (st != ATTN_OK || empty) return st;
-    if (num_splits == 0) num_splits = attn_fwd_splitkv_num_splits(B, Hq, N, D, causal);
+    // the default: the best split count whose partials fit the buffer
+    if (num_splits == 0)
+        num_splits = splitkv_default(B, Hq, N, D, causal,
+                                     static_cast<int64_t>(kNoAllocScratchBytes));
     int split_tiles = 0, n_splits = 0;
     split_layout(P.n_tiles, num_splits, &split_tiles, &n_splits);
     if (D > 128) n_splits = 1;

@@ -214,13 +214,186 @@ __device__ __forceinline__ bool work_in_range(const AttnParams& p, const FwdWork
            w.kv_end <= p.n_tiles && w.split >= 0 && w.split < p.n_splits;
 }
 
+// Up to this many splits of a work item run as one thread-block cluster and merge through
+// distributed shared memory (cluster dimensions up to 8 are portable; 4 keeps the merge's
+// registers within the non-softmax warps' budget).
+constexpr int kMaxClusterSplits = 4;
+
+// Split partials staged for the cluster merge, in the CTA's own shared memory once its MMAs are
+// done: O_s of Q tile t (fp32, normalised by its own l) over the K/V ring at t * 128 * D * 4 bytes,
+// row r at r * D * 4, its 16-byte chunk c at (c ^ (r & (D/4 - 1))) * 16 (so that a warp's 32 rows
+// written at once spread over all banks); LSE_s of the 2 x 128 rows (natural log; -inf where the
+// tile took no part in this split) in the first P panel, and the merge's weights of the rows
+// this CTA combines after them.
+template <int D>
+__device__ __forceinline__ uint32_t cluster_o_stage(int t, int r, int c) {
+    return static_cast<uint32_t>(SmemLayout<D>::kKV + t * kBM * D * 4 + r * D * 4 +
+                                 ((c ^ (r & (D / 4 - 1))) << 4));
+}
+template <int D>
+__device__ __forceinline__ uint32_t cluster_lse_stage(int t, int r) {
+    return static_cast<uint32_t>(SmemLayout<D>::kP1 + (t * kBM + r) * 4);
+}
+// weight of split s for the i-th row this CTA merges (i < 2 * 128 / 2)
+template <int D>
+__device__ __forceinline__ uint32_t cluster_weight(int i, int s) {
+    return static_cast<uint32_t>(SmemLayout<D>::kP1 + 2 * kBM * 4 + (i * kMaxClusterSplits + s) * 4);
+}
+static_assert(kStages >= 4, "O staging (2 x 128 x D fp32) fits in the K/V ring (kStages x 128 x D bf16)");
+static_assert(2 * kBM * 4 + kBM * kMaxClusterSplits * 4 <= 2 * kBM * 64 * 2,
+              "LSE staging and weights fit in the P panels");
+
+// The softmax warps (warp w: Q tile w / 4, TMEM lane quarter w % 4) stage their rows.
+template <int D>
+__device__ __forceinline__ void cluster_stage_split(uint32_t sbase, uint32_t tmem, int warp,
+                                                    int lane, float m, float l, bool have) {
+    const int t = warp >> 2, quarter = warp & 3, row = quarter * 32 + lane;
+    const uint32_t o_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + tmem_o_col(t);
+    if (have) {  // uniform over the warp (the tile's four warps agree on the item)
+        tc_fence_after();
+        const float inv_l = 1.0f / l;
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t r[32];
+            tmem_ld32(o_addr + cc * 32, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                st_shared_v4(sbase + cluster_o_stage<D>(t, row, cc * 8 + i),
+                             __float_as_uint(__uint_as_float(r[4 * i]) * inv_l),
+                             __float_as_uint(__uint_as_float(r[4 * i + 1]) * inv_l),
+                             __float_as_uint(__uint_as_float(r[4 * i + 2]) * inv_l),
+                             __float_as_uint(__uint_as_float(r[4 * i + 3]) * inv_l));
+        }
+    }
+    const float lse = have ? (m + __log2f(l)) * kLn2 : -INFINITY;
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(sbase + cluster_lse_stage<D>(t, row)), "f"(lse)
+                 : "memory");
+}
+
+// The merge of section 2.4's split-T inside the cluster: CTA s combines rows s*R .. s*R + R - 1
+// (R = 128 / splits, rounded up) of each Q tile of the work item, reading every CTA's staging
+// through distributed shared memory: LSE = M + ln sum_s exp(LSE_s - M), O = sum_s exp(LSE_s -
+// LSE) O_s, over the splits that hold visible keys (LSE_s > -inf).  First one thread per row
+// reads the row's LSE_s, writes LSE and keeps the weights exp(LSE_s - LSE) in shared memory;
+// then D/4 lanes per row read the O_s rows (16 bytes a lane from every split at once) and store
+// O.  Every thread of the CTA calls this (it holds a CTA barrier).  If a CTA of the cluster gave
+// up (its abort flag), nothing is merged; the expiry is in the status word.
+template <int D, bool kOne>
+__device__ __forceinline__ void cluster_merge_splits(const AttnParams& p, uint32_t sbase) {
+    using L = SmemLayout<D>;
+    const int n = p.n_splits;
+    uint32_t peer[kMaxClusterSplits];
+    bool aborted = false;
+#pragma unroll
+    for (int s = 0; s < kMaxClusterSplits; ++s) {
+        peer[s] = s < n ? dsmem_addr(sbase, static_cast<uint32_t>(s)) : 0u;
+        if (s < n) aborted |= ld_dsmem_u32(peer[s] + L::kAbort) != 0u;
+    }
+    if (aborted) return;  // uniform over the cluster: every thread read the same flags
+    const FwdWork w = decode_work<true, kOne>(p, static_cast<int>(blockIdx.x));
+    constexpr int kTiles = kOne ? 1 : 2;
+    const int per = (kBM + n - 1) / n;
+    const int r0 = static_cast<int>(cluster_ctarank()) * per;
+    const int rows = min(per, kBM - r0);  // rows of each tile this CTA merges
+    auto q_of = [&](int i) { return (w.tile0 + i / rows) * kBM + r0 + i % rows; };
+    // Only the softmax warps (threads 0..255) work here: they run with the larger register budget.
+    constexpr int kWorkers = 256;
+    const int tid = static_cast<int>(threadIdx.x);
+    // 1. weights and LSE, one thread per row
+    if (tid < kWorkers) {
+        for (int i = tid; i < kTiles * rows; i += kWorkers) {
+            const int q = q_of(i);
+            if (q >= p.N) continue;
+            const int t = i / rows, r = r0 + i % rows;
+            float ls[kMaxClusterSplits];
+            float mx = -INFINITY;
+#pragma unroll
+            for (int s = 0; s < kMaxClusterSplits; ++s) {
+                ls[s] = s < n ? __uint_as_float(ld_dsmem_u32(peer[s] + cluster_lse_stage<D>(t, r)))
+                              : -INFINITY;
+                mx = fmaxf(mx, ls[s]);
+            }
+            float sum = 0.f;
+#pragma unroll
+            for (int s = 0; s < kMaxClusterSplits; ++s) {
+                ls[s] = ls[s] > -INFINITY ? expf(ls[s] - mx) : 0.f;
+                sum += ls[s];
+            }
+            const float inv = 1.0f / sum;
+#pragma unroll
+            for (int s = 0; s < kMaxClusterSplits; ++s)
+                asm volatile("st.shared.f32 [%0], %1;" ::"r"(sbase + cluster_weight<D>(i, s)),
+                             "f"(ls[s] * inv)
+                             : "memory");
+            if (ATTN_DCHECK(static_cast<size_t>(w.bh) * p.N + q <
+                            static_cast<size_t>(p.B) * p.Hq * p.N))
+                p.lse[static_cast<size_t>(w.bh) * p.N + q] = mx + logf(sum);
+        }
+    }
+    __syncthreads();
+    // 2. O: D/4 lanes per row, two rows per pass so that 2 x splits loads are in flight a lane
+    if (tid < kWorkers) {
+        constexpr int kLanes = D / 4, kStep = kWorkers / kLanes;
+        const int c = tid % kLanes, col = 4 * c;
+        __nv_bfloat16* obase = p.out + w.b * p.o_sb + w.hq * p.o_sh;
+        for (int i0 = tid / kLanes; i0 < kTiles * rows; i0 += 2 * kStep) {
+            uint32_t v[2][kMaxClusterSplits][4];
+            bool live[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int i = i0 + u * kStep;
+                live[u] = i < kTiles * rows && q_of(i) < p.N;
+                const int t = i / rows, r = r0 + i % rows;
+#pragma unroll
+                for (int s = 0; s < kMaxClusterSplits; ++s)
+                    if (live[u] && s < n)
+                        ld_dsmem_v4(peer[s] + cluster_o_stage<D>(t, r, c), v[u][s][0], v[u][s][1],
+                                    v[u][s][2], v[u][s][3]);
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                if (!live[u]) continue;
+                const int i = i0 + u * kStep;
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int s = 0; s < kMaxClusterSplits; ++s) {
+                    if (s < n) {
+                        float wgt;
+                        asm volatile("ld.shared.f32 %0, [%1];"
+                                     : "=f"(wgt)
+                                     : "r"(sbase + cluster_weight<D>(i, s))
+                                     : "memory");
+                        if (wgt != 0.f)  // a split without visible keys staged no O
+#pragma unroll
+                            for (int x = 0; x < 4; ++x)
+                                acc[x] += wgt * __uint_as_float(v[u][s][x]);
+                    }
+                }
+                if (col < p.d_out && ATTN_DCHECK(work_in_range(p, w))) {
+                    uint2 o;
+                    o.x = pack_bf16x2(acc[0], acc[1]);
+                    o.y = pack_bf16x2(acc[2], acc[3]);
+                    *reinterpret_cast<uint2*>(obase + static_cast<long long>(q_of(i)) * p.o_sn +
+                                              col) = o;
+                }
+            }
+        }
+    }
+}
+
 // kSplit = false: the whole KV range, bf16 O and LSE written to the outputs.
 // kSplit = true:  the KV range of one split (split index innermost in the item number); the fp32
 //                 O of that range (normalised by its own denominator) and its LSE go to the
 //                 workspace, and attn_splitkv_merge_kernel combines the splits.
 // kOne = true:    one Q tile per work item (the second tile's issuer and softmax group idle),
 //                 for launches whose pairs would leave most SMs idle.
-template <int D, bool kSplit, bool kOne = false>
+// kCluster = true (with kSplit): the splits of one work item are one thread-block cluster, one
+//                 CTA per split (launched with one work unit per CTA and no claim counter); at
+//                 the end every CTA stages its O_s = acc / l and LSE_s in its own shared memory
+//                 and the cluster combines them through distributed shared memory
+//                 (cluster_merge_splits): no partial reaches global memory, no merge kernel runs.
+template <int D, bool kSplit, bool kOne = false, bool kCluster = false>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
                     const __grid_constant__ CUtensorMap tmap_k,
@@ -307,6 +480,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return item;
     };
+
+    // kCluster: the softmax threads keep their tile's final m and l (one work item per CTA)
+    float cl_m = -INFINITY, cl_l = 0.f;
+    bool cl_have = false;  // this thread's Q tile took part in this CTA's split
 
     // Each role's code follows its warpgroup's register budget (setmaxnreg at the top of the
     // warpgroup's branch), so the compiler allocates the softmax code with kSoftmaxRegs.
@@ -683,7 +860,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const FwdWork we = decode_work<kSplit, kOne>(p, opaque_int(item));
             const int row_g = (we.tile0 + t) * kBM + row;
             const float inv_l = 1.0f / l;
-            if constexpr (kSplit) {
+            if constexpr (kCluster) {
+                // ---- staged in the teardown, once every MMA of the CTA has completed ----------
+                cl_m = m;
+                cl_l = l;
+                cl_have = true;
+                (void)row_g;
+                (void)inv_l;
+            } else if constexpr (kSplit) {
                 // ---- split epilogue: O_s = acc / l (fp32) and LSE_s to the workspace ----------
                 const size_t prow =
                     (static_cast<size_t>(we.split) * p.B * p.Hq + we.bh) * p.N + row_g;
@@ -757,6 +941,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- teardown ------------------------------------------------------------------------------
     tc_fence_before();
     __syncthreads();
+    if constexpr (kCluster) {
+        // (after an abort the K/V ring may still be a TMA destination: nothing is staged)
+        if (warp < 8) cluster_stage_split<D>(sbase, tmem, warp, lane, cl_m, cl_l,
+                                             cl_have && *abort_flag == 0);
+        cluster_sync_all();  // every CTA's partials are staged (and visible to the cluster)
+        cluster_merge_splits<D, kOne>(p, sbase);
+        cluster_sync_all();  // no CTA leaves while another may still read its staging
+    }
     if (warp == kMmaWarp0) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);

@@ -81,7 +81,12 @@ typedef enum {
  *
  * Scheduling: up to D = 128 the kernel is persistent (one CTA per SM); a work item is a pair of
  * 128-row Q tiles of one head, or a single Q tile when pairs would leave more than half of the
- * SMs idle (the results are the same bits either way).  Its CTAs claim work items
+ * SMs idle (the results are the same bits either way).  When even single tiles leave most SMs
+ * idle and the key axis is long, attn_fwd splits the key axis instead (attn_fwd_num_splits()
+ * says how many ways, 1 = no split): the 2-4 splits of each pair of Q tiles run as a
+ * thread-block cluster whose CTAs merge their partial results through distributed shared memory
+ * as attn_fwd_splitkv describes, with no workspace and no second kernel (the result then
+ * differs from the single pass by rounding only).  Its CTAs claim work items
  * from a device counter that the library hands to each launch from a pool of 64 (round robin,
  * per device, shared with attn_fwd_strided, the split-KV entry points and the backward's dQ
  * kernel).  Each launch returns its counter to zero, and before a launch reuses a counter its
@@ -93,6 +98,22 @@ typedef enum {
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
              int Hkv, int N, int D, int causal, float sm_scale, void* stream);
+
+/* Key-axis splits attn_fwd (and attn_fwd_strided) use for these sizes on the current device: 1
+ * (single pass) unless the Q tiles leave most SMs idle and a calibrated cost model (a fixed
+ * cost plus a cost per key tile of the longest work item, for the single pass and for 2-4
+ * splits merged inside clusters) gives the split a margin of at least 1 us; also 1 for invalid
+ * sizes. */
+int attn_fwd_num_splits(int B, int Hq, int N, int D, int causal);
+
+/* attn_fwd_test_split_choice - test hook: the split count the library's cost model picks for
+ * these sizes on a device described by the arguments, touching no device: num_sms SMs and
+ * cluster_fit[0..2] clusters of 2, 3 and 4 split CTAs fitting on it at once.  cluster_only != 0
+ * gives attn_fwd's choice (as attn_fwd_num_splits), else attn_fwd_splitkv's default among the
+ * counts whose workspace is at most max_ws bytes (as attn_fwd_splitkv_num_splits, uncached, when
+ * max_ws is LLONG_MAX).  Returns the count, or ATTN_ERR_SHAPE for invalid arguments. */
+int attn_fwd_test_split_choice(int B, int Hq, int N, int D, int causal, int num_sms,
+                               const int* cluster_fit, int cluster_only, long long max_ws);
 
 /*
  * attn_fwd_strided - attn_fwd for tensors that are not contiguous, e.g. the [B, N, H, D] layout
@@ -120,35 +141,45 @@ int attn_fwd_strided(const void* q, const void* k, const void* v, void* out, flo
  * split of the key axis produces a partial result (here: O over that split's keys, normalised by
  * that split's own denominator, in fp32, and that split's natural-log LSE), and a safe-softmax
  * merge combines them: LSE = M + ln sum_s exp(LSE_s - M) with M = max_s LSE_s, and
- * O = sum_s exp(LSE_s - LSE) O_s.  The merge is a second kernel on the same stream.  This raises
- * the number of CTAs for problems whose query tiles alone do not fill the GPU (short sequences,
- * few heads); the result equals attn_fwd's up to rounding.
+ * O = sum_s exp(LSE_s - LSE) O_s.  With 2-4 splits whose clusters all fit on the device at once
+ * (one wave), the splits of each work item run as a thread-block cluster and merge through
+ * distributed shared memory at the end of the kernel; otherwise the persistent split kernel
+ * writes the partials to `workspace` and a merge kernel follows on the same stream (its dynamic
+ * claims balance uneven causal splits over several waves).  This raises the number of CTAs for
+ * problems whose query tiles alone do not fill the GPU (short sequences, few heads); the result
+ * equals attn_fwd's up to rounding.
  *
  *   q, k, v, out, lse, B, Hq, Hkv, N, D, causal, sm_scale, stream: as for attn_fwd.
  *   num_splits       requested number of key-axis splits, 0..64; 0 picks
  *                    attn_fwd_splitkv_num_splits().  Splits hold ceil(ceil(N/128)/num_splits)
- *                    key tiles of 128, so fewer splits may be used.  One split is attn_fwd;
+ *                    key tiles of 128, so fewer splits may be used.  One split is
+ *                    attn_fwd's single pass (never split further);
  *                    D > 128 always runs as one split (the wide-head kernel has no split form).
  *   workspace        device memory of at least attn_fwd_splitkv_workspace_bytes(B, Hq, N, D,
  *                    num_splits) bytes, 16-byte aligned, owned by the caller; its previous
- *                    contents are ignored and it holds partial results afterwards.  It must not
- *                    overlap the inputs or outputs, and calls that run concurrently on the GPU
- *                    must not share it.  May be NULL when the call resolves to one split.
+ *                    contents are ignored and it holds partial results afterwards (it is
+ *                    checked, but left untouched, when the splits merge inside clusters).  It
+ *                    must not overlap the inputs or outputs, and calls that run concurrently on
+ *                    the GPU must not share it.  May be NULL when the call resolves to one split.
  *   workspace_bytes  size of `workspace` in bytes.
  *
- * Returns ATTN_OK once both kernels are enqueued, else a negative attn_status_t (nothing written).
+ * Returns ATTN_OK once its kernels are enqueued, else a negative attn_status_t (nothing written).
  */
 int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* out, float* lse, int B,
                      int Hq, int Hkv, int N, int D, int causal, float sm_scale, int num_splits,
                      void* workspace, size_t workspace_bytes, void* stream);
 
 /* Workspace bytes attn_fwd_splitkv needs for these sizes (0 if the call resolves to one split or
- * the sizes are invalid).  num_splits == 0 uses attn_fwd_splitkv_num_splits(). */
+ * the sizes are invalid).  num_splits == 0: enough for attn_fwd_splitkv_num_splits()'s count,
+ * with or without the causal mask (the larger of the two). */
 size_t attn_fwd_splitkv_workspace_bytes(int B, int Hq, int N, int D, int num_splits);
 
-/* Suggested split count for the current device: when the query tiles alone leave SMs idle,
- * as many splits as fit the SMs while every split keeps at least 4 key tiles (at most 16);
- * else 1. */
+/* Suggested split count for the current device (attn_fwd_splitkv's default): the count, from 1
+ * (single pass) to 16, with the lowest estimated time under a cost model calibrated on GB300
+ * (launch, per-unit and per-key-tile costs; the heaviest-first claim order simulated as list
+ * scheduling over the SMs; the workspace path's partial traffic, or the cluster path's in-cluster
+ * merge).  A split must win by 1 us; problems with at least twice as many Q-tile pairs as SMs are
+ * not split.  The result is cached per shape (its first evaluation takes up to a few ms). */
 int attn_fwd_splitkv_num_splits(int B, int Hq, int N, int D, int causal);
 
 /*
@@ -164,9 +195,10 @@ int attn_fwd_splitkv_num_splits(int B, int Hq, int N, int D, int causal);
  *   Arguments, outputs and result: as attn_fwd_splitkv, without the workspace arguments.
  *   A problem whose partials need more than the buffer holds (attn_fwd_splitkv_workspace_bytes()
  *   > attn_fwd_splitkv_noalloc_max_bytes()) returns ATTN_ERR_SCRATCH before any launch.  With an
- *   explicit num_splits the check runs before any CUDA call; with num_splits = 0 the default
- *   split count needs the device's SM count first (the same one-time device query every entry
- *   point makes), so that check follows it.
+ *   explicit num_splits the check runs before any CUDA call.  With num_splits = 0 the default is
+ *   the split count attn_fwd_splitkv_num_splits() would choose among those whose partials fit
+ *   the buffer (the choice needs the device's SM count: the same one-time device query every
+ *   entry point makes), so it never returns ATTN_ERR_SCRATCH.
  *   The buffer's device address is looked up the first time this is called on a device (with that
  *   device current); make that first call before capturing any stream.  A lookup that fails is
  *   not remembered: the next call on that device tries again.
@@ -299,9 +331,13 @@ int attn_fwd_test_stall(const void* q, const void* k, const void* v, void* out, 
  *               (cta_group::2, M = 256), each SM loading and reading half of every K and V tile;
  *               four Q tiles per work item (64 < D <= 128; ATTN_ERR_HEADDIM otherwise,
  *               ATTN_ERR_ARCH if no CTA pair fits on the device).  Measured slower than kernel 1
- *               on GB300, so attn_fwd does not use it.
+ *               on GB300, so attn_fwd does not use it;
+ *   kernel = 3  the one-CTA kernel over two key-axis splits whose CTA pairs are clusters that
+ *               merge through distributed shared memory (D <= 128; ATTN_ERR_SHAPE unless the
+ *               key axis has at least two tiles and all the clusters fit on the device at once).
  * stall_item: -1, or a K/V ring entry to withhold as in attn_fwd_test_stall (on CTA pairs both
- * CTAs withhold their halves of it).
+ * CTAs withhold their halves of it; in split clusters every CTA withholds it, and no cluster
+ * merges).
  * The results are those of attn_fwd (the same definition; fp32 accumulation may group the work
  * differently).  Any other value of `kernel` returns ATTN_ERR_SHAPE.
  */

@@ -28,6 +28,7 @@ def _declared_functions():
 def test_header_declares_the_boundary():
     assert _declared_functions() == sorted(
         ["attn_fwd", "attn_status_string", "attn_last_cuda_error", "attn_debug_status",
+         "attn_fwd_num_splits", "attn_fwd_test_split_choice",
          "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_bytes", "attn_fwd_splitkv_num_splits",
          "attn_fwd_splitkv_noalloc", "attn_fwd_splitkv_noalloc_max_bytes", "attn_fwd_strided",
          "attn_fwd_test_stall", "attn_fwd_test_kernel", "attn_bwd", "attn_bwd_workspace_bytes",
@@ -218,6 +219,7 @@ def test_kernel_hook_rejects_what_its_kernels_do_not_run(lib):
     def call(D, kernel):
         return lib.attn_fwd_test_kernel(S, S * 2, S * 3, S * 4, S * 5, 1, 2, 1, 128, D, 0,
                                         ctypes.c_float(0.1), kernel, -1, None)
-    assert call(128, 0) == -2 and call(128, 3) == -2   # no such kernel: ATTN_ERR_SHAPE
-    assert call(256, 1) == -4 and call(256, 2) == -4   # wide heads: neither
+    assert call(128, 0) == -2 and call(128, 4) == -2   # no such kernel: ATTN_ERR_SHAPE
+    assert call(256, 1) == -4 and call(256, 2) == -4   # wide heads: none of them
+    assert call(256, 3) == -4
     assert call(64, 2) == -4                           # the pair kernel is for D in (64, 128]

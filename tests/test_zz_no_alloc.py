@@ -110,12 +110,25 @@ def test_noalloc_rejects_problems_beyond_its_buffer(cuda_lib):
 
 
 def test_noalloc_default_split_count_fits_its_buffer(cuda_lib):
-    """num_splits = 0: the library splits only while the query tiles leave SMs idle, so the
-    default split count's partials stay within the buffer (checked over a sweep of shapes)."""
+    """num_splits = 0: the default is the best split count whose partials fit the buffer, so it
+    never runs out of it, also where attn_fwd_splitkv's own default would need more."""
     lib = cuda_lib
     cap = lib.attn_fwd_splitkv_noalloc_max_bytes()
-    for B in (1, 2, 4):
-        for Hq in (1, 2, 4, 8, 16, 32):
-            for N in (512, 1024, 4096, 8192, 16384, 32768, 65536, 131072):
-                for D in (64, 128):
-                    assert lib.attn_fwd_splitkv_workspace_bytes(B, Hq, N, D, 0) <= cap
+    over = [(B, Hq, N, D) for B in (1, 2) for Hq in (1, 2, 4) for N in (32768, 65536)
+            for D in (64, 128) if lib.attn_fwd_splitkv_workspace_bytes(B, Hq, N, D, 0) > cap]
+    cases = [wl.random_case(1, 4, 1, 8192, 128, True, 23), wl.random_case(1, 8, 2, 8192, 64, True, 24)]
+    if over:  # a shape whose unlimited default exceeds the buffer, when the sweep finds one
+        B, Hq, N, D = over[0]
+        cases.append(wl.random_case(B, Hq, 1, N, D, False, 25))
+    for w in cases:
+        q, k, v, out, lse = _inputs(w)
+        assert _noalloc(lib, w, 0, q, k, v, out, lse) == 0
+        torch.cuda.synchronize()
+        assert lib.attn_debug_status(_stream()) == 0
+        ref = torch.empty_like(out)
+        ref_l = torch.empty_like(lse)
+        assert lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), ref.data_ptr(),
+                            ref_l.data_ptr(), w.B, w.Hq, w.Hkv, w.N, w.D, int(w.causal),
+                            ctypes.c_float(w.sm_scale), _stream()) == 0
+        torch.cuda.synchronize()
+        _close(out, lse, ref, ref_l)
