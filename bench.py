@@ -688,20 +688,22 @@ def main():
             gpu_out[wc.name] = (co.cpu(), cl.cpu())
             del cq, ck, cv, co, cl
 
-    # ---- context: low-occupancy configurations, single pass vs split-KV (key-axis splits) -----
+    # ---- context: low-occupancy configurations: attn_fwd (which may split the key axis into
+    # clusters itself), the forced single pass and the split-KV entry point ---------------------
     low_occ = []
     if not args.no_sweep and rank == 0:
-        for ws_ in (wl.MHA, wl.MQA, wl.FEWHEADS):
+        for ws_ in (wl.MHA, wl.MQA, wl.FEWHEADS, wl.FEWHEADS_CAUSAL):
             lq, lk, lv = (t.to(dev) for t in wl.make_qkv(ws_))
             lo = torch.empty_like(lq)
             ll = torch.empty(ws_.B, ws_.Hq, ws_.N, dtype=torch.float32, device=dev)
-            # the library's choice, or 2 forced splits where it declines to split
-            n_sp = max(2, attn.splitkv_num_splits(ws_.B, ws_.Hq, ws_.N, ws_.D, ws_.causal))
+            # split-KV: the library's default, or 2 forced splits where it declines to split
+            dflt = attn.splitkv_num_splits(ws_.B, ws_.Hq, ws_.N, ws_.D, ws_.causal)
+            n_sp = max(2, dflt)
             wbuf = torch.empty(max(1, attn.splitkv_workspace_bytes(ws_.B, ws_.Hq, ws_.N, ws_.D,
                                                                    n_sp)),
                                dtype=torch.uint8, device=dev)
 
-            # Pre-bound C-ABI calls: these kernels take ~15-35 us, less than the Python
+            # Pre-bound C-ABI calls: these kernels take ~15-100 us, not much more than the Python
             # binding's per-call host time, which would otherwise be what gets measured.
             lib = _lib.load()
             sh = ctypes.c_void_p(stream.cuda_stream)
@@ -709,16 +711,20 @@ def main():
                       ws_.B, ws_.Hq, ws_.Hkv, ws_.N, ws_.D, int(ws_.causal),
                       ctypes.c_float(ws_.sm_scale))
 
-            def single():
+            def fwd():
                 assert lib.attn_fwd(*common, sh) == 0
+
+            def single():  # one split: the single pass, never split further
+                assert lib.attn_fwd_splitkv(*common, 1, None, 0, sh) == 0
 
             def split():
                 assert lib.attn_fwd_splitkv(*common, n_sp, wbuf.data_ptr(), wbuf.numel(), sh) == 0
 
-            entry = {"workload": ws_.name, "splits": n_sp,
-                     "library_choice": attn.splitkv_num_splits(ws_.B, ws_.Hq, ws_.N, ws_.D,
-                                                               ws_.causal)}
-            for name, fn in (("single", single), ("splitkv", split)):
+            entry = {"workload": ws_.name, "causal": ws_.causal,
+                     "attn_fwd_splits": attn.fwd_num_splits(ws_.B, ws_.Hq, ws_.N, ws_.D,
+                                                            ws_.causal),
+                     "splits": n_sp, "library_choice": dflt}
+            for name, fn in (("attn_fwd", fwd), ("single", single), ("splitkv", split)):
                 ms = cold_launch_ms(fn, stream, flush, 30)
                 entry[f"{name}_us"] = ms * 1e3
                 entry[f"{name}_tflops"] = ws_.flops / (ms * 1e-3) / 1e12

@@ -71,6 +71,9 @@ MQA = Workload("mqa-n512", 1, 16, 1, 512, 128, False, 4)
 # Few query heads over a longer sequence: 32 query tiles in all, far fewer than the SMs, so the
 # key axis is split (split-KV forward).  Not one of the five configurations; a context workload.
 FEWHEADS = Workload("fewheads-n4096", 1, 2, 1, 4096, 128, False, 8)
+# Few causal heads over a long sequence: 128 pairs of Q tiles, the split-KV default splits the key
+# axis in two (more clusters than fit at once: the workspace path).  A context workload.
+FEWHEADS_CAUSAL = Workload("fewheads-causal-n8192", 1, 4, 1, 8192, 128, True, 9)
 LONG = {n: Workload(f"long-gqa8-causal-n{n}", 1, 32, 8, n, 128, True, s)
         for n, s in ((8192, 5), (16384, 6), (32768, 7))}
 
@@ -79,7 +82,7 @@ LONG = {n: Workload(f"long-gqa8-causal-n{n}", 1, 32, 8, n, 128, True, s)
 WIDE = Workload("wide-d256-causal-n8192", 1, 16, 4, 8192, 256, True, 9)
 
 CONFIGS = [TINY_NONCAUSAL, TINY_CAUSAL, GQA4_CAUSAL, GQA8_CAUSAL, MHA, MHA_OUTLIER, MQA,
-           *LONG.values(), FEWHEADS, WIDE]
+           *LONG.values(), FEWHEADS, FEWHEADS_CAUSAL, WIDE]
 BY_NAME = {w.name: w for w in CONFIGS}
 
 
