@@ -165,3 +165,32 @@ def test_cluster_split_reports_an_expired_wait_and_merges_nothing(cuda_lib):
     assert lib.attn_fwd_test_kernel(*args, -1, stream) == 0
     assert lib.attn_debug_status(stream) == 0
     _check(out, lse, *oracle.attn_ref(q, k, v, False, w.sm_scale), "cluster split after expiry")
+
+
+def test_cluster_split_in_a_cuda_graph(cuda_lib):
+    """attn_fwd's cluster split captured into a CUDA graph (no claim counter is involved) and
+    replayed on another stream gives the eager launch's bits."""
+    import exact_attention_forward_attn_gb300 as attn
+
+    w = wl.FEWHEADS
+    q, k, v = (t.cuda() for t in wl.make_qkv(w))
+    assert attn.fwd_num_splits(w.B, w.Hq, w.N, w.D, w.causal) > 1
+    o_ref, l_ref = attn.attn_fwd(q, k, v, causal=w.causal, sm_scale=w.sm_scale)
+    out = torch.zeros_like(q)
+    lse = torch.zeros(w.B, w.Hq, w.N, dtype=torch.float32, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # warm up on the capturing stream
+        attn.attn_fwd(q, k, v, causal=w.causal, sm_scale=w.sm_scale, out=out, lse=lse)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        attn.attn_fwd(q, k, v, causal=w.causal, sm_scale=w.sm_scale, out=out, lse=lse)
+    for _ in range(2):
+        out.zero_()
+        lse.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert attn.device_status() == 0
+        assert torch.equal(out, o_ref) and torch.equal(lse, l_ref)
