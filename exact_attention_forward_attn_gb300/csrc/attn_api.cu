@@ -34,6 +34,13 @@ using namespace gb300attn;
 // its counter at zero, and a launch that reuses a counter waits for the counter's previous launch.
 __device__ unsigned int g_fwd_sched[gb300attn::kSchedSlots] = {};
 
+// attn_fwd's own split-KV partials (when its cost model picks the workspace path): a fixed device
+// buffer of kFwdScratchSlots slots, leased to one launch at a time like the claim counters, so
+// that attn_fwd never allocates and never shares partials between launches that overlap.
+constexpr int kFwdScratchSlots = 2;
+constexpr size_t kFwdScratchBytes = size_t(64) << 20;  // per slot
+__device__ __align__(256) unsigned char g_fwd_scratch[kFwdScratchSlots * kFwdScratchBytes];
+
 namespace {
 
 constexpr int kMaxSplits = 64;
@@ -147,6 +154,9 @@ struct DeviceState {
     std::atomic<unsigned int> sched_next{0};
     SchedSlot slots[kSchedSlots];
     int pair_clusters = 0;  // CTA pairs of the pair kernel that fit on the device at once
+    unsigned char* fwd_scratch = nullptr;  // g_fwd_scratch
+    std::atomic<unsigned int> scratch_next{0};
+    SchedSlot scratch_slots[kFwdScratchSlots];
     // clusters of n split CTAs (n = 2..kMaxClusterSplits) that fit on the device at once, for
     // D <= 64 ([0]) and D <= 128 ([1])
     int cluster_fit[2][kMaxClusterSplits + 1] = {};
@@ -242,6 +252,8 @@ int device_state(int dev, DeviceState** out) {
         e = cudaGetSymbolAddress(reinterpret_cast<void**>(&st.status_word), g_attn_status_word);
         if (e == cudaSuccess)
             e = cudaGetSymbolAddress(reinterpret_cast<void**>(&st.sched), g_fwd_sched);
+        if (e == cudaSuccess)
+            e = cudaGetSymbolAddress(reinterpret_cast<void**>(&st.fwd_scratch), g_fwd_scratch);
         bool regs_ok = true;
         if (e == cudaSuccess) e = opt_in_smem<64, false>(&regs_ok);
         if (e == cudaSuccess) e = opt_in_smem<128, false>(&regs_ok);
@@ -778,41 +790,81 @@ int choose_splits(const ForwardShape& f, const SplitDevice& dev, bool cluster_on
     return best;
 }
 
-// attn_fwd's own split: cluster candidates only, closed form (no simulation of more than one
-// wave), so it costs the launch path nothing worth measuring.
-int auto_splits(const Problem& P, const DeviceState* ds) {
-    if (2 * P.items > ds->num_sms) return 1;  // pairs beyond half the SMs: no cluster split fits
-    const ForwardShape f{P.bh, P.n_tiles, P.D, P.causal != 0};
-    return choose_splits(f, split_device(ds, P.D), true, 0);
-}
-
 // attn_fwd_splitkv's default split count, cached per shape (the list-scheduling estimate of a
 // few thousand units takes up to a few milliseconds of host time).
 struct SplitCacheKey {
     int64_t bh, n_tiles, max_ws;
-    int dev, D, causal;
+    int dev, D, causal, cluster_only;
     bool operator==(const SplitCacheKey& o) const {
         return bh == o.bh && n_tiles == o.n_tiles && max_ws == o.max_ws && dev == o.dev &&
-               D == o.D && causal == o.causal;
+               D == o.D && causal == o.causal && cluster_only == o.cluster_only;
     }
 };
 std::mutex g_split_cache_lock;
 std::vector<std::pair<SplitCacheKey, int>> g_split_cache;  // small; cleared when it grows
 
 int default_splits(int64_t bh, int64_t N, int D, bool causal, int64_t max_ws,
-                   const DeviceState* ds, int dev) {
+                   const DeviceState* ds, int dev, bool cluster_only = false) {
     const ForwardShape f{bh, (N + kBM - 1) / kBM, D <= 64 ? 64 : 128, causal};
-    const SplitCacheKey key{bh, f.n_tiles, max_ws, dev, f.D, causal ? 1 : 0};
+    // the cases choose_splits settles at once (most problems) skip the cache
+    if (D > 128 || f.n_tiles < 2 || (f.n_tiles + 1) / 2 * bh >= 2 * int64_t(ds->num_sms)) return 1;
+    const SplitCacheKey key{bh, f.n_tiles, max_ws, dev, f.D, causal ? 1 : 0, cluster_only ? 1 : 0};
     {
         std::lock_guard<std::mutex> guard(g_split_cache_lock);
         for (const auto& e : g_split_cache)
             if (e.first == key) return e.second;
     }
-    const int n = choose_splits(f, split_device(ds, D), false, max_ws);
+    const int n = choose_splits(f, split_device(ds, D), cluster_only, max_ws);
     std::lock_guard<std::mutex> guard(g_split_cache_lock);
     if (g_split_cache.size() >= 1024) g_split_cache.clear();
     g_split_cache.emplace_back(key, n);
     return n;
+}
+
+// attn_fwd's own split.  Outside a graph capture, for contiguous outputs, both split paths are
+// candidates (the workspace path's partials in a leased slot of g_fwd_scratch); while the stream
+// is being captured (the host cannot order a graph's replays against other users of a slot) and
+// for strided outputs (the merge kernel writes contiguous rows), only splits that merge inside
+// one-wave clusters.
+int auto_splits(const Problem& P, const DeviceState* ds, bool cluster_only) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 1;
+    }
+    return default_splits(P.bh, P.N, P.D, P.causal != 0,
+                          cluster_only ? 0 : static_cast<int64_t>(kFwdScratchBytes), ds, dev,
+                          cluster_only);
+}
+
+// Runs launch(scratch) with one of the device's kFwdScratchSlots slots of g_fwd_scratch that no
+// other executing launch holds: the slots are taken round robin, and the stream first waits for
+// the event recorded after the slot's previous launch (under the slot's lock, as for the claim
+// counters).  Not for streams being captured.
+template <class Launch>
+int with_scratch(DeviceState* ds, cudaStream_t s, Launch&& launch) {
+    const unsigned int idx =
+        ds->scratch_next.fetch_add(1u, std::memory_order_relaxed) % kFwdScratchSlots;
+    SchedSlot& slot = ds->scratch_slots[idx];
+    std::lock_guard<std::mutex> guard(slot.lock);
+    cudaError_t e = cudaSuccess;
+    if (slot.done == nullptr) {
+        e = cudaEventCreateWithFlags(&slot.done, cudaEventDisableTiming);
+        if (e != cudaSuccess) {
+            slot.done = nullptr;
+            return cuda_fail(e);
+        }
+    }
+    if (slot.recorded) {
+        e = cudaStreamWaitEvent(s, slot.done, 0);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    // recorded whatever the launch returned (a chain that failed part-way may have enqueued work)
+    const int st = launch(ds->fwd_scratch + static_cast<size_t>(idx) * kFwdScratchBytes);
+    e = cudaEventRecord(slot.done, s);
+    if (e == cudaSuccess) slot.recorded = true;
+    if (st != ATTN_OK) return st;
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
 
 }  // namespace
@@ -837,11 +889,33 @@ static int run_forward(Problem& P, bool allow_split, cudaStream_t s) {
     AttnParams prm;
     int st = prepare(P, &ds, &mq, &mk, &mv, &mo, &prm);
     if (st != ATTN_OK) return st;
-    const int n = allow_split ? auto_splits(P, ds) : 1;
+    int n = 1;
+    if (allow_split) {
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        const cudaError_t e = cudaStreamIsCapturing(s, &cap);
+        if (e != cudaSuccess) return cuda_fail(e);
+        n = auto_splits(P, ds, cap != cudaStreamCaptureStatusNone || P.strided);
+    }
     if (n > 1) {
         split_layout(P.n_tiles, n, &prm.split_tiles, &prm.n_splits);
-        return P.D <= 64 ? launch_cluster_split<64>(mq, mk, mv, prm, ds, P.items * prm.n_splits, s)
-                         : launch_cluster_split<128>(mq, mk, mv, prm, ds, P.items * prm.n_splits, s);
+        const int64_t units = P.items * prm.n_splits;
+        if (cluster_fits(ds, P.D, P.items, prm.n_splits))
+            return P.D <= 64 ? launch_cluster_split<64>(mq, mk, mv, prm, ds, units, s)
+                             : launch_cluster_split<128>(mq, mk, mv, prm, ds, units, s);
+        // the workspace path (auto_splits allowed it: not capturing, contiguous output, partials
+        // within one scratch slot)
+        return with_scratch(ds, s, [&](unsigned char* scratch) {
+            prm.ws_o = reinterpret_cast<float*>(scratch);
+            prm.ws_lse = prm.ws_o + static_cast<int64_t>(prm.n_splits) * P.bh * P.N *
+                                        padded_dim(P.D);
+            auto* o = static_cast<__nv_bfloat16*>(P.out);
+            auto after = [&]() {
+                return P.D <= 64 ? launch_merge<64>(prm, o, P.D, s)
+                                 : launch_merge<128>(prm, o, P.D, s);
+            };
+            return P.D <= 64 ? launch_fwd<64, true>(mq, mk, mv, prm, ds, units, s, after)
+                             : launch_fwd<128, true>(mq, mk, mv, prm, ds, units, s, after);
+        });
     }
     const bool one_tile = prefer_single_tiles(P, ds, &prm);
     return launch_single(P.D, mq, mk, mv, mo, prm, ds, P.items, s, one_tile);
@@ -866,7 +940,8 @@ extern "C" int attn_fwd_num_splits(int B, int Hq, int N, int D, int causal) {
     P.bh = static_cast<int64_t>(B) * Hq;
     P.n_tiles = (static_cast<int64_t>(N) + kBM - 1) / kBM;
     P.items = (P.n_tiles + 1) / 2 * P.bh;
-    return auto_splits(P, ds);
+    P.N = N;
+    return auto_splits(P, ds, false);
 }
 
 extern "C" int attn_fwd_strided(const void* q, const void* k, const void* v, void* out,
@@ -949,7 +1024,6 @@ extern "C" int attn_fwd_test_split_choice(int B, int Hq, int N, int D, int causa
     for (int n = 2; n <= kMaxClusterSplits; ++n) dev.cluster_fit[n] = cluster_fit[n - 2];
     const int64_t bh = static_cast<int64_t>(B) * Hq;
     const int64_t n_tiles = (static_cast<int64_t>(N) + kBM - 1) / kBM;
-    if (cluster_only && 2 * ((n_tiles + 1) / 2) * bh > num_sms) return 1;  // as auto_splits
     const ForwardShape f{bh, n_tiles, D, causal != 0};
     const int n = choose_splits(f, dev, cluster_only != 0, max_ws);
     int tps = 0, eff = 0;

@@ -81,12 +81,16 @@ typedef enum {
  *
  * Scheduling: up to D = 128 the kernel is persistent (one CTA per SM); a work item is a pair of
  * 128-row Q tiles of one head, or a single Q tile when pairs would leave more than half of the
- * SMs idle (the results are the same bits either way).  When even single tiles leave most SMs
- * idle and the key axis is long, attn_fwd splits the key axis instead (attn_fwd_num_splits()
- * says how many ways, 1 = no split): the 2-4 splits of each pair of Q tiles run as a
- * thread-block cluster whose CTAs merge their partial results through distributed shared memory
- * as attn_fwd_splitkv describes, with no workspace and no second kernel (the result then
- * differs from the single pass by rounding only).  Its CTAs claim work items
+ * SMs idle (the results are the same bits either way).  When the Q tiles leave SMs idle and the
+ * key axis is long, attn_fwd splits the key axis instead, as attn_fwd_splitkv describes
+ * (attn_fwd_num_splits() says how many ways; the result then differs from the single pass by
+ * rounding only): the splits of each pair of Q tiles either run as a thread-block cluster whose
+ * CTAs merge through distributed shared memory, or the persistent split kernel writes its
+ * partials to one of two 64 MiB slots of a device buffer compiled into the library and a merge
+ * kernel follows.  A slot is leased to one launch at a time (a later launch's stream waits for
+ * the slot's previous launch, as for the claim counters below), so overlapping calls stay
+ * correct; while the stream is being captured into a CUDA graph, and for attn_fwd_strided, only
+ * the cluster form is used.  Its CTAs claim work items
  * from a device counter that the library hands to each launch from a pool of 64 (round robin,
  * per device, shared with attn_fwd_strided, the split-KV entry points and the backward's dQ
  * kernel).  Each launch returns its counter to zero, and before a launch reuses a counter its
@@ -99,19 +103,19 @@ typedef enum {
 int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
              int Hkv, int N, int D, int causal, float sm_scale, void* stream);
 
-/* Key-axis splits attn_fwd (and attn_fwd_strided) use for these sizes on the current device: 1
- * (single pass) unless the Q tiles leave most SMs idle and a calibrated cost model (a fixed
- * cost plus a cost per key tile of the longest work item, for the single pass and for 2-4
- * splits merged inside clusters) gives the split a margin of at least 1 us; also 1 for invalid
- * sizes. */
+/* Key-axis splits attn_fwd uses for these sizes on the current device (outside a graph
+ * capture): 1 (single pass) unless the cost model of attn_fwd_splitkv_num_splits(), limited to
+ * workspaces of one 64 MiB scratch slot, gives a split a margin of at least 1 us; also 1 for
+ * invalid sizes. */
 int attn_fwd_num_splits(int B, int Hq, int N, int D, int causal);
 
 /* attn_fwd_test_split_choice - test hook: the split count the library's cost model picks for
  * these sizes on a device described by the arguments, touching no device: num_sms SMs and
  * cluster_fit[0..2] clusters of 2, 3 and 4 split CTAs fitting on it at once.  cluster_only != 0
- * gives attn_fwd's choice (as attn_fwd_num_splits), else attn_fwd_splitkv's default among the
- * counts whose workspace is at most max_ws bytes (as attn_fwd_splitkv_num_splits, uncached, when
- * max_ws is LLONG_MAX).  Returns the count, or ATTN_ERR_SHAPE for invalid arguments. */
+ * gives the choice among splits that merge inside clusters only (attn_fwd's while its stream is
+ * captured, and attn_fwd_strided's), else the choice among the counts whose workspace is at most
+ * max_ws bytes (attn_fwd's with 64 MiB, attn_fwd_splitkv_num_splits's with LLONG_MAX; uncached).
+ * Returns the count, or ATTN_ERR_SHAPE for invalid arguments. */
 int attn_fwd_test_split_choice(int B, int Hq, int N, int D, int causal, int num_sms,
                                const int* cluster_fit, int cluster_only, long long max_ws);
 

@@ -46,7 +46,7 @@ def test_attn_fwd_splits_low_occupancy_problems(w, cuda_lib):
     import exact_attention_forward_attn_gb300 as attn
 
     n = attn.fwd_num_splits(w.B, w.Hq, w.N, w.D, w.causal)
-    assert 2 <= n <= 4, n
+    assert n >= 2, n
     q, k, v = wl.make_qkv(w)
     out, lse = attn.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=w.causal, sm_scale=w.sm_scale)
     torch.cuda.synchronize()
@@ -105,6 +105,75 @@ def test_long_causal_split_sampled_rows(cuda_lib):
     torch.cuda.synchronize()
     assert attn.device_status() == 0
     _sampled(w, q, k, v, out, lse)
+
+
+@pytest.mark.parametrize("shape", [(1, 4, 1, 8192, 128), (1, 1, 1, 32768, 128), (1, 2, 1, 12000, 64)],
+                         ids=["hq4-n8192", "hq1-n32768", "hq2-n12000-d64"])
+def test_attn_fwd_workspace_split_on_causal_few_heads(shape, cuda_lib):
+    """Causal few-head problems whose pairs are more clusters than fit at once: attn_fwd splits
+    them through its own scratch slots (persistent split kernel + merge kernel)."""
+    import exact_attention_forward_attn_gb300 as attn
+
+    B, Hq, Hkv, N, D = shape
+    w = wl.random_case(B, Hq, Hkv, N, D, True, 92)
+    assert attn.fwd_num_splits(B, Hq, N, D, True) >= 2
+    q, k, v = wl.make_qkv(w)
+    out, lse = attn.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=True, sm_scale=w.sm_scale)
+    torch.cuda.synchronize()
+    assert attn.device_status() == 0
+    _sampled(w, q, k, v, out, lse)
+
+
+def test_attn_fwd_scratch_slots_under_concurrent_streams(cuda_lib):
+    """Six streams run attn_fwd's workspace split at once, three rounds: the scratch slots are
+    leased one launch at a time, so every result equals the same call made alone."""
+    import exact_attention_forward_attn_gb300 as attn
+
+    ws_ = [wl.random_case(1, 4, 1, 8192, 128, True, 93 + i) for i in range(6)]
+    ins = [tuple(t.cuda() for t in wl.make_qkv(w)) for w in ws_]
+    refs = []
+    for w, (q, k, v) in zip(ws_, ins):
+        refs.append(attn.attn_fwd(q, k, v, causal=True, sm_scale=w.sm_scale))
+        torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in ws_]
+    outs = [(torch.empty_like(q), torch.empty(1, w.Hq, w.N, device="cuda"))
+            for w, (q, _, _) in zip(ws_, ins)]
+    for _ in range(3):
+        for o, l in outs:
+            o.zero_()
+            l.zero_()
+        torch.cuda.synchronize()
+        for st, w, (q, k, v), (o, l) in zip(streams, ws_, ins, outs):
+            st.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(st):
+                attn.attn_fwd(q, k, v, causal=True, sm_scale=w.sm_scale, out=o, lse=l)
+        torch.cuda.synchronize()
+        assert attn.device_status() == 0
+        for (o, l), (ro, rl) in zip(outs, refs):
+            assert torch.equal(o, ro) and torch.equal(l, rl)
+
+
+def test_attn_fwd_under_capture_does_not_use_the_scratch(cuda_lib):
+    """While its stream is captured, attn_fwd takes only cluster splits: for four causal heads of
+    8192 rows (too many pairs for one wave of clusters) that is the single pass, bit for bit."""
+    import exact_attention_forward_attn_gb300 as attn
+
+    w = wl.random_case(1, 4, 1, 8192, 128, True, 99)
+    q, k, v = (t.cuda() for t in wl.make_qkv(w))
+    assert attn.fwd_num_splits(w.B, w.Hq, w.N, w.D, True) >= 2  # outside a capture
+    o1, l1 = attn.attn_fwd_splitkv(q, k, v, causal=True, sm_scale=w.sm_scale, num_splits=1)
+    out = torch.zeros_like(q)
+    lse = torch.zeros(w.B, w.Hq, w.N, dtype=torch.float32, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        attn.attn_fwd(q, k, v, causal=True, sm_scale=w.sm_scale, out=out, lse=lse)
+    g.replay()
+    torch.cuda.synchronize()
+    assert attn.device_status() == 0
+    assert torch.equal(out, o1) and torch.equal(lse, l1)
 
 
 def test_splitkv_default_on_causal_few_heads_uses_the_workspace(cuda_lib):

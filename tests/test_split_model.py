@@ -11,6 +11,7 @@ from exact_attention_forward_attn_gb300 import workloads as wl
 SMS = 152
 FIT = (76, 48, 36)
 UNLIMITED = 2 ** 62
+FWD_SCRATCH = 64 << 20  # one slot of attn_fwd's own split scratch
 
 
 @pytest.fixture(scope="module")
@@ -29,6 +30,7 @@ def _choice(lib, B, Hq, N, D, causal, cluster_only, max_ws=UNLIMITED, sms=SMS, f
                          ids=lambda w: w.name)
 def test_the_five_configurations_run_the_single_pass(w, lib):
     assert _choice(lib, w.B, w.Hq, w.N, w.D, w.causal, True) == 1
+    assert _choice(lib, w.B, w.Hq, w.N, w.D, w.causal, False, max_ws=FWD_SCRATCH) == 1
     assert _choice(lib, w.B, w.Hq, w.N, w.D, w.causal, False) == 1
 
 
@@ -40,8 +42,10 @@ def test_few_heads_over_long_keys_split(lib):
     assert _choice(lib, w.B, w.Hq, w.N, w.D, w.causal, True) == 4
     assert _choice(lib, w.B, w.Hq, w.N, w.D, w.causal, False) == 4
     # causal few heads: the persistent split kernel's balanced claims win (measured 72 against 95
-    # us at four heads of 8192 rows), which attn_fwd (no workspace) cannot take
+    # us at four heads of 8192 rows); attn_fwd takes that path through its scratch slots, except
+    # under graph capture (cluster splits only: 128 pairs are more clusters than fit at once)
     assert _choice(lib, 1, 4, 8192, 128, True, False) >= 2
+    assert _choice(lib, 1, 4, 8192, 128, True, False, max_ws=FWD_SCRATCH) >= 2
     assert _choice(lib, 1, 4, 8192, 128, True, True) == 1
 
 
@@ -69,6 +73,12 @@ def test_default_respects_a_workspace_limit(lib):
             n = _choice(lib, B, Hq, N, D, c, False, max_ws=limit)
             assert n >= 1
             assert lib.attn_fwd_splitkv_workspace_bytes(B, Hq, N, D, n) <= limit
+
+
+def test_attn_fwd_scratch_limit_caps_the_split(lib):
+    # one causal head of 65536 rows: 4 splits need 135 MB of partials, beyond a 64 MiB slot
+    n = _choice(lib, 1, 1, 65536, 128, False, False, max_ws=FWD_SCRATCH)
+    assert lib.attn_fwd_splitkv_workspace_bytes(1, 1, 65536, 128, n) <= FWD_SCRATCH
 
 
 def test_single_query_tile_and_wide_heads(lib):
