@@ -60,8 +60,8 @@ def test_splitkv_close_to_single_pass_and_ignores_stale_workspace(cuda_lib):
 def test_splitkv_heuristic_splits_low_occupancy_shapes(cuda_lib):
     import exact_attention_forward_attn_gb300 as attn
 
-    # 32 query tiles of 32 key tiles each on a GPU with >100 SMs: split (>= 4 key tiles per
-    # split); 4 key tiles per query tile (N=512) or enough query tiles (the long workload): do not
+    # 32 query tiles of 32 key tiles each on a GPU with >100 SMs: the cost model splits; 4 key
+    # tiles per query tile (N=512) or enough query tiles (the long workload): it does not
     assert attn.splitkv_num_splits(1, 2, 4096, 128) > 1
     assert attn.splitkv_num_splits(1, 32, 512, 128) == 1
     assert attn.splitkv_num_splits(1, 16, 512, 128) == 1
