@@ -439,23 +439,16 @@ int prepare(const Problem& P, DeviceState** ds, CUtensorMap* mq, CUtensorMap* mk
     return ATTN_OK;
 }
 
-// Runs launch(counter) with a claim counter that no other executing launch holds.  The counter
-// is one of the device's kSchedSlots, taken round robin; the stream first waits for the event
-// recorded after the counter's previous launch, so two launches that share a counter never run
-// at the same time, however many streams or host threads launch.  The slot's lock is held until
-// that event is recorded again, so two host threads never interleave on one slot.  While the
-// stream is being captured into a CUDA graph the host cannot order the graph's future replays
-// against other launches, so a captured launch gets no counter (nullptr) and the kernel uses its
-// static schedule.
+// Runs launch() on stream `s` holding `slot`: the stream first waits for the event recorded
+// after the slot's previous launch, so two launches that hold one slot never run at the same
+// time, however many streams or host threads launch; the slot's lock is held until that event is
+// recorded again, so two host threads never interleave on one slot.  The event is recorded
+// whatever the launch returned: a chain that failed part-way may have enqueued a kernel that uses
+// the slot, and the slot's next launch must wait for it.
 template <class Launch>
-int with_claim_counter(DeviceState* ds, cudaStream_t s, Launch&& launch) {
-    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-    cudaError_t e = cudaStreamIsCapturing(s, &cap);
-    if (e != cudaSuccess) return cuda_fail(e);
-    if (cap != cudaStreamCaptureStatusNone) return launch(static_cast<unsigned int*>(nullptr));
-    const unsigned int idx = ds->sched_next.fetch_add(1u, std::memory_order_relaxed) % kSchedSlots;
-    SchedSlot& slot = ds->slots[idx];
+int on_slot(SchedSlot& slot, cudaStream_t s, Launch&& launch) {
     std::lock_guard<std::mutex> guard(slot.lock);
+    cudaError_t e = cudaSuccess;
     if (slot.done == nullptr) {
         e = cudaEventCreateWithFlags(&slot.done, cudaEventDisableTiming);
         if (e != cudaSuccess) {
@@ -467,13 +460,26 @@ int with_claim_counter(DeviceState* ds, cudaStream_t s, Launch&& launch) {
         e = cudaStreamWaitEvent(s, slot.done, 0);
         if (e != cudaSuccess) return cuda_fail(e);
     }
-    // The event is recorded whatever the launch returned: a chain that failed part-way may have
-    // enqueued a kernel that uses the counter, and the counter's next launch must wait for it.
-    const int st = launch(ds->sched + idx);
+    const int st = launch();
     e = cudaEventRecord(slot.done, s);
     if (e == cudaSuccess) slot.recorded = true;
     if (st != ATTN_OK) return st;
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+// Runs launch(counter) with a claim counter that no other executing launch holds: one of the
+// device's kSchedSlots, taken round robin and held as on_slot describes.  While the stream is
+// being captured into a CUDA graph the host cannot order the graph's future replays against
+// other launches, so a captured launch gets no counter (nullptr) and the kernel uses its static
+// schedule.
+template <class Launch>
+int with_claim_counter(DeviceState* ds, cudaStream_t s, Launch&& launch) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    const cudaError_t e = cudaStreamIsCapturing(s, &cap);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (cap != cudaStreamCaptureStatusNone) return launch(static_cast<unsigned int*>(nullptr));
+    const unsigned int idx = ds->sched_next.fetch_add(1u, std::memory_order_relaxed) % kSchedSlots;
+    return on_slot(ds->slots[idx], s, [&]() { return launch(ds->sched + idx); });
 }
 
 // The persistent two-tile kernel: one CTA per SM (or per item, if fewer), each claiming items
@@ -838,33 +844,14 @@ int auto_splits(const Problem& P, const DeviceState* ds, bool cluster_only) {
 }
 
 // Runs launch(scratch) with one of the device's kFwdScratchSlots slots of g_fwd_scratch that no
-// other executing launch holds: the slots are taken round robin, and the stream first waits for
-// the event recorded after the slot's previous launch (under the slot's lock, as for the claim
-// counters).  Not for streams being captured.
+// other executing launch holds: taken round robin and held as on_slot describes.  Not for
+// streams being captured.
 template <class Launch>
 int with_scratch(DeviceState* ds, cudaStream_t s, Launch&& launch) {
     const unsigned int idx =
         ds->scratch_next.fetch_add(1u, std::memory_order_relaxed) % kFwdScratchSlots;
-    SchedSlot& slot = ds->scratch_slots[idx];
-    std::lock_guard<std::mutex> guard(slot.lock);
-    cudaError_t e = cudaSuccess;
-    if (slot.done == nullptr) {
-        e = cudaEventCreateWithFlags(&slot.done, cudaEventDisableTiming);
-        if (e != cudaSuccess) {
-            slot.done = nullptr;
-            return cuda_fail(e);
-        }
-    }
-    if (slot.recorded) {
-        e = cudaStreamWaitEvent(s, slot.done, 0);
-        if (e != cudaSuccess) return cuda_fail(e);
-    }
-    // recorded whatever the launch returned (a chain that failed part-way may have enqueued work)
-    const int st = launch(ds->fwd_scratch + static_cast<size_t>(idx) * kFwdScratchBytes);
-    e = cudaEventRecord(slot.done, s);
-    if (e == cudaSuccess) slot.recorded = true;
-    if (st != ATTN_OK) return st;
-    return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+    unsigned char* scratch = ds->fwd_scratch + static_cast<size_t>(idx) * kFwdScratchBytes;
+    return on_slot(ds->scratch_slots[idx], s, [&]() { return launch(scratch); });
 }
 
 }  // namespace

@@ -215,8 +215,8 @@ __device__ __forceinline__ bool work_in_range(const AttnParams& p, const FwdWork
 }
 
 // Up to this many splits of a work item run as one thread-block cluster and merge through
-// distributed shared memory (cluster dimensions up to 8 are portable; 4 keeps the merge's
-// registers within the non-softmax warps' budget).
+// distributed shared memory (cluster dimensions up to 8 are portable; with 4 a merging thread
+// keeps two rows' loads from every split in registers at once).
 constexpr int kMaxClusterSplits = 4;
 
 // Split partials staged for the cluster merge, in the CTA's own shared memory once its MMAs are
@@ -234,7 +234,7 @@ template <int D>
 __device__ __forceinline__ uint32_t cluster_lse_stage(int t, int r) {
     return static_cast<uint32_t>(SmemLayout<D>::kP1 + (t * kBM + r) * 4);
 }
-// weight of split s for the i-th row this CTA merges (i < 2 * 128 / 2)
+// weight of split s for the i-th row this CTA merges (i < 128: both tiles' rows, at most 2 x 64)
 template <int D>
 __device__ __forceinline__ uint32_t cluster_weight(int i, int s) {
     return static_cast<uint32_t>(SmemLayout<D>::kP1 + 2 * kBM * 4 + (i * kMaxClusterSplits + s) * 4);
