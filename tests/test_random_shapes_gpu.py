@@ -5,7 +5,8 @@ or 8), N in 1..2300, D a multiple of 8 in 8..256, causal or not; each runs conti
 attn_fwd, as a [B, N, H, D] view through attn_fwd_strided, through attn_fwd_splitkv with 2-5
 splits (D <= 128), and on the CTA-pair kernel (64 < D <= 128).  Every element of every result
 is compared with the fp64 oracle at the tests' tolerance (|dO| <= 2e-2 + 2e-2 |O_ref|,
-|dLSE| <= 1e-3).
+|dLSE| <= 1e-3).  Twelve more (one or two heads over 2000-12000 keys) exercise the splits that
+attn_fwd and the split-KV default choose for themselves, on 32 sampled rows per head.
 """
 import ctypes
 import random
@@ -81,3 +82,49 @@ def test_random_shape_every_entry_point(shape, cuda_lib):
         torch.cuda.synchronize()
         assert cuda_lib.attn_debug_status(stream) == 0
         _check(out_p, lse_p, o_ref, l_ref, f"pair {w.name}")
+
+
+def _split_shapes(n=12, seed=20261203):
+    """Few heads over long key axes, where attn_fwd splits the key axis itself."""
+    rng = random.Random(seed)
+    out = []
+    for i in range(n):
+        hkv = rng.randint(1, 2)
+        hq = hkv * rng.choice([1, 2])
+        N = rng.randint(2000, 12000)
+        D = rng.choice([64, 80, 96, 128])
+        out.append((rng.randint(1, 2), hq, hkv, N, D, rng.random() < 0.5, 5000 + i))
+    return out
+
+
+SPLIT_SHAPES = _split_shapes()
+
+
+@pytest.mark.parametrize("shape", SPLIT_SHAPES, ids=[f"b{b}h{h}k{k}n{n}d{d}{'c' if c else ''}"
+                                                     for b, h, k, n, d, c, _ in SPLIT_SHAPES])
+def test_random_split_shapes_sampled_rows(shape, cuda_lib):
+    """attn_fwd's own split (in clusters or through its scratch, as its cost model picks) and the
+    split-KV default, against the oracle on 32 seeded rows per head (the first and last included)."""
+    import exact_attention_forward_attn_gb300 as attn
+
+    B, Hq, Hkv, N, D, causal, seed = shape
+    w = wl.random_case(B, Hq, Hkv, N, D, causal, seed)
+    q, k, v = wl.make_qkv(w)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    rows = wl.sample_rows(w, 32)
+    rows[..., 0] = 0
+    rows[..., -1] = N - 1
+    rows = rows.sort(dim=-1).values
+    o_ref, l_ref = oracle.attn_ref(q, k, v, causal, w.sm_scale, rows=rows.numpy())
+    idx = rows.long()
+    for name, (out, lse) in (
+            ("attn_fwd", attn.attn_fwd(qd, kd, vd, causal=causal, sm_scale=w.sm_scale)),
+            ("splitkv", attn.attn_fwd_splitkv(qd, kd, vd, causal=causal, sm_scale=w.sm_scale))):
+        torch.cuda.synchronize()
+        assert attn.device_status() == 0
+        o_c, l_c = out.cpu(), lse.cpu()
+        o_s = torch.stack([o_c[b, h][idx[b, h]] for b in range(B) for h in range(Hq)])
+        l_s = torch.stack([l_c[b, h][idx[b, h]] for b in range(B) for h in range(Hq)])
+        splits = attn.fwd_num_splits(B, Hq, N, D, causal)
+        _check(o_s.reshape(o_ref.shape), l_s.reshape(l_ref.shape), o_ref, l_ref,
+               f"{name} (attn_fwd splits {splits}) {w.name}")
