@@ -77,7 +77,7 @@ typedef enum {
  *   sm_scale score scale (callers usually pass 1/sqrt(D)); finite and > 0
  *   stream   a cudaStream_t of the current device, passed as void* (NULL = legacy default stream)
  *
- * Returns ATTN_OK once the kernel is enqueued on `stream`, else a negative attn_status_t.
+ * Returns ATTN_OK once its kernels are enqueued on `stream`, else a negative attn_status_t.
  *
  * Scheduling: up to D = 128 the kernel is persistent (one CTA per SM); a work item is a pair of
  * 128-row Q tiles of one head, or a single Q tile when pairs would leave more than half of the
@@ -90,7 +90,7 @@ typedef enum {
  * kernel follows.  A slot is leased to one launch at a time (a later launch's stream waits for
  * the slot's previous launch, as for the claim counters below), so overlapping calls stay
  * correct; while the stream is being captured into a CUDA graph, and for attn_fwd_strided, only
- * the cluster form is used.  Its CTAs claim work items
+ * the cluster form is used.  The persistent kernels' CTAs claim work items
  * from a device counter that the library hands to each launch from a pool of 64 (round robin,
  * per device, shared with attn_fwd_strided, the split-KV entry points and the backward's dQ
  * kernel).  Each launch returns its counter to zero, and before a launch reuses a counter its
