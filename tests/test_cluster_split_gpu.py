@@ -263,3 +263,44 @@ def test_cluster_split_in_a_cuda_graph(cuda_lib):
         torch.cuda.synchronize()
         assert attn.device_status() == 0
         assert torch.equal(out, o_ref) and torch.equal(lse, l_ref)
+
+
+def test_scratch_and_counters_from_several_host_threads(cuda_lib):
+    """Four host threads, each with its own stream, call attn_fwd at the same time on problems
+    that take the scratch path, the cluster path and the single pass; the slot leases and claim
+    counters keep every result equal to the same call made alone."""
+    import threading
+
+    import exact_attention_forward_attn_gb300 as attn
+
+    shapes = [wl.random_case(1, 4, 1, 8192, 128, True, 110),   # workspace split, own scratch
+              wl.FEWHEADS,                                      # cluster split
+              wl.random_case(1, 32, 8, 2048, 128, True, 111),  # single pass (persistent)
+              wl.random_case(1, 1, 1, 16384, 64, True, 112)]   # workspace split, D = 64
+    ins = [tuple(t.cuda() for t in wl.make_qkv(w)) for w in shapes]
+    refs = []
+    for w, (q, k, v) in zip(shapes, ins):
+        refs.append(attn.attn_fwd(q, k, v, causal=w.causal, sm_scale=w.sm_scale))
+    torch.cuda.synchronize()
+    errors = []
+
+    def worker(i):
+        try:
+            w, (q, k, v) = shapes[i], ins[i]
+            st = torch.cuda.Stream()
+            with torch.cuda.stream(st):
+                for _ in range(8):
+                    o, l = attn.attn_fwd(q, k, v, causal=w.causal, sm_scale=w.sm_scale)
+                    st.synchronize()
+                    if not (torch.equal(o, refs[i][0]) and torch.equal(l, refs[i][1])):
+                        errors.append(f"{w.name}: result differs")
+        except Exception as e:  # reported below, on the main thread
+            errors.append(f"{shapes[i].name}: {e!r}")
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(len(shapes))]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    assert attn.device_status() == 0
