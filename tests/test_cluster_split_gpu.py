@@ -304,3 +304,21 @@ def test_scratch_and_counters_from_several_host_threads(cuda_lib):
         th.join()
     assert not errors, errors
     assert attn.device_status() == 0
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 1, 6000, 8, False), (1, 1, 1, 6000, 40, True),
+                                   (1, 2, 1, 3000, 16, False), (2, 1, 1, 5000, 72, True)],
+                         ids=["d8", "d40-causal", "d16", "d72-causal-b2"])
+def test_attn_fwd_split_narrow_heads(shape, cuda_lib):
+    """Head dimensions below the padded width (the merge writes only the first D columns) on
+    problems attn_fwd splits, against the oracle on sampled rows."""
+    import exact_attention_forward_attn_gb300 as attn
+
+    B, Hq, Hkv, N, D, causal = shape
+    w = wl.random_case(B, Hq, Hkv, N, D, causal, 120 + D)
+    assert attn.fwd_num_splits(B, Hq, N, D, causal) >= 2
+    q, k, v = wl.make_qkv(w)
+    out, lse = attn.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal, sm_scale=w.sm_scale)
+    torch.cuda.synchronize()
+    assert attn.device_status() == 0
+    _sampled(w, q, k, v, out, lse)
