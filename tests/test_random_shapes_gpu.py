@@ -5,8 +5,9 @@ or 8), N in 1..2300, D a multiple of 8 in 8..256, causal or not; each runs conti
 attn_fwd, as a [B, N, H, D] view through attn_fwd_strided, through attn_fwd_splitkv with 2-5
 splits (D <= 128), and on the CTA-pair kernel (64 < D <= 128).  Every element of every result
 is compared with the fp64 oracle at the tests' tolerance (|dO| <= 2e-2 + 2e-2 |O_ref|,
-|dLSE| <= 1e-3).  Twelve more (one or two heads over 2000-12000 keys) exercise the splits that
-attn_fwd and the split-KV default choose for themselves, on 32 sampled rows per head.
+|dLSE| <= 1e-3).  Twenty more (one or two heads over 2000-16000 keys, D a multiple of 8 up to
+128) exercise the splits that attn_fwd and the split-KV default choose for themselves, on 32
+sampled rows per head.
 """
 import ctypes
 import random
@@ -84,15 +85,15 @@ def test_random_shape_every_entry_point(shape, cuda_lib):
         _check(out_p, lse_p, o_ref, l_ref, f"pair {w.name}")
 
 
-def _split_shapes(n=12, seed=20261203):
+def _split_shapes(n=20, seed=20261203):
     """Few heads over long key axes, where attn_fwd splits the key axis itself."""
     rng = random.Random(seed)
     out = []
     for i in range(n):
         hkv = rng.randint(1, 2)
         hq = hkv * rng.choice([1, 2])
-        N = rng.randint(2000, 12000)
-        D = rng.choice([64, 80, 96, 128])
+        N = rng.randint(2000, 16000)
+        D = 8 * rng.randint(1, 16)
         out.append((rng.randint(1, 2), hq, hkv, N, D, rng.random() < 0.5, 5000 + i))
     return out
 
