@@ -576,10 +576,14 @@ template <int D>
 int launch_merge(const AttnParams& p, __nv_bfloat16* out, int d_out, cudaStream_t stream) {
     const int64_t rows = static_cast<int64_t>(p.B) * p.Hq * p.N;
     const int64_t blocks = (rows + kMergeThreads / 32 - 1) / (kMergeThreads / 32);
+    const bool contiguous = p.o_sn == d_out && p.o_sh == static_cast<long long>(p.N) * d_out &&
+                            p.o_sb == static_cast<long long>(p.Hq) * p.N * d_out;
     const cudaError_t e = launch_dependent(
-        attn_splitkv_merge_kernel<D>, dim3(static_cast<unsigned int>(blocks)), dim3(kMergeThreads),
+        contiguous ? attn_splitkv_merge_kernel<D, false> : attn_splitkv_merge_kernel<D, true>,
+        dim3(static_cast<unsigned int>(blocks)), dim3(kMergeThreads),
         0, stream, static_cast<const float*>(p.ws_o), static_cast<const float*>(p.ws_lse), out,
-        p.lse, p.B * p.Hq, p.N, d_out, p.n_tiles, p.causal, p.n_splits, p.split_tiles);
+        p.lse, p.B * p.Hq, p.Hq, p.N, d_out, p.o_sb, p.o_sh, p.o_sn, p.n_tiles, p.causal,
+        p.n_splits, p.split_tiles);
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
 
@@ -827,11 +831,10 @@ int default_splits(int64_t bh, int64_t N, int D, bool causal, int64_t max_ws,
     return n;
 }
 
-// attn_fwd's own split.  Outside a graph capture, for contiguous outputs, both split paths are
-// candidates (the workspace path's partials in a leased slot of g_fwd_scratch); while the stream
-// is being captured (the host cannot order a graph's replays against other users of a slot) and
-// for strided outputs (the merge kernel writes contiguous rows), only splits that merge inside
-// one-wave clusters.
+// attn_fwd's own split.  Outside a graph capture both split paths are candidates (the workspace
+// path's partials in a leased slot of g_fwd_scratch); while the stream is being captured (the
+// host cannot order a graph's replays against other users of a slot), only splits that merge
+// inside one-wave clusters.
 int auto_splits(const Problem& P, const DeviceState* ds, bool cluster_only) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -881,7 +884,7 @@ static int run_forward(Problem& P, bool allow_split, cudaStream_t s) {
         cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
         const cudaError_t e = cudaStreamIsCapturing(s, &cap);
         if (e != cudaSuccess) return cuda_fail(e);
-        n = auto_splits(P, ds, cap != cudaStreamCaptureStatusNone || P.strided);
+        n = auto_splits(P, ds, cap != cudaStreamCaptureStatusNone);
     }
     if (n > 1) {
         split_layout(P.n_tiles, n, &prm.split_tiles, &prm.n_splits);
@@ -889,8 +892,8 @@ static int run_forward(Problem& P, bool allow_split, cudaStream_t s) {
         if (cluster_fits(ds, P.D, P.items, prm.n_splits))
             return P.D <= 64 ? launch_cluster_split<64>(mq, mk, mv, prm, ds, units, s)
                              : launch_cluster_split<128>(mq, mk, mv, prm, ds, units, s);
-        // the workspace path (auto_splits allowed it: not capturing, contiguous output, partials
-        // within one scratch slot)
+        // the workspace path (auto_splits allowed it: not capturing, partials within one scratch
+        // slot)
         return with_scratch(ds, s, [&](unsigned char* scratch) {
             prm.ws_o = reinterpret_cast<float*>(scratch);
             prm.ws_lse = prm.ws_o + static_cast<int64_t>(prm.n_splits) * P.bh * P.N *

@@ -961,12 +961,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 // before its last visible key tile) are combined as
 //   LSE = M + ln sum_s exp(LSE_s - M),  M = max_s LSE_s,   O = sum_s exp(LSE_s - LSE) * O_s.
 // One warp per row; lane k owns D/32 consecutive columns (coalesced 16-byte loads per split).
-// D is the padded width of the partials; only the first d_out columns of each row go to `out`.
-template <int D>
+// D is the padded width of the partials; only the first d_out columns of each row go to `out`:
+// rows of d_out elements one after another, or (kStrided) rows addressed through element strides
+// (batch o_sb, head o_sh, row o_sn; each a multiple of 8).  The contiguous instantiation keeps
+// its index arithmetic (and registers, so the blocks in flight of this memory-streaming kernel)
+// to the row number alone.
+template <int D, bool kStrided>
 __global__ void __launch_bounds__(256)
     attn_splitkv_merge_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_lse,
                               __nv_bfloat16* __restrict__ out, float* __restrict__ lse, int BH,
-                              int N, int d_out, int n_tiles, int causal, int n_splits,
+                              int Hq, int N, int d_out, long long o_sb, long long o_sh,
+                              long long o_sn, int n_tiles, int causal, int n_splits,
                               int split_tiles) {
     constexpr int kCols = D / 32;
     const int lane = threadIdx.x & 31;
@@ -998,7 +1003,18 @@ __global__ void __launch_bounds__(256)
     }
     const float inv = 1.0f / wsum;
     const int c0 = lane * kCols;
-    __nv_bfloat16* o = out + row * d_out + c0;
+    __nv_bfloat16* o;
+    if constexpr (kStrided) {
+        const int bh = static_cast<int>(row / N);  // BH < 2^31
+        const int b = bh / Hq;
+        o = out + b * o_sb + (bh - b * Hq) * o_sh + i * o_sn + c0;
+    } else {
+        (void)Hq;
+        (void)o_sb;
+        (void)o_sh;
+        (void)o_sn;
+        o = out + row * d_out + c0;
+    }
     if (d_out == D) {  // full width: one 8-byte (D=128) or 4-byte (D=64) store per lane
         if constexpr (kCols == 4) {
             uint2 packed;

@@ -89,8 +89,7 @@ typedef enum {
  * partials to one of two 64 MiB slots of a device buffer compiled into the library and a merge
  * kernel follows.  A slot is leased to one launch at a time (a later launch's stream waits for
  * the slot's previous launch, as for the claim counters below), so overlapping calls stay
- * correct; while the stream is being captured into a CUDA graph, and for attn_fwd_strided, only
- * the cluster form is used.  The persistent kernels' CTAs claim work items
+ * correct; while the stream is being captured into a CUDA graph only the cluster form is used.  The persistent kernels' CTAs claim work items
  * from a device counter that the library hands to each launch from a pool of 64 (round robin,
  * per device, shared with attn_fwd_strided, the split-KV entry points and the backward's dQ
  * kernel).  Each launch returns its counter to zero, and before a launch reuses a counter its
@@ -113,7 +112,7 @@ int attn_fwd_num_splits(int B, int Hq, int N, int D, int causal);
  * these sizes on a device described by the arguments, touching no device: num_sms SMs and
  * cluster_fit[0..2] clusters of 2, 3 and 4 split CTAs fitting on it at once.  cluster_only != 0
  * gives the choice among splits that merge inside clusters only (attn_fwd's while its stream is
- * captured, and attn_fwd_strided's), else the choice among the counts whose workspace is at most
+ * captured), else the choice among the counts whose workspace is at most
  * max_ws bytes (attn_fwd's with 64 MiB, attn_fwd_splitkv_num_splits's with LLONG_MAX; uncached).
  * Returns the count, or ATTN_ERR_SHAPE for invalid arguments. */
 int attn_fwd_test_split_choice(int B, int Hq, int N, int D, int causal, int num_sms,

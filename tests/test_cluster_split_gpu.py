@@ -322,3 +322,27 @@ def test_attn_fwd_split_narrow_heads(shape, cuda_lib):
     torch.cuda.synchronize()
     assert attn.device_status() == 0
     _sampled(w, q, k, v, out, lse)
+
+
+@pytest.mark.parametrize("shape", [(1, 4, 1, 8192, 128), (1, 4, 2, 8192, 96)],
+                         ids=["d128", "d96-padded-rows"])
+def test_strided_workspace_split(shape, cuda_lib):
+    """[B, N, H, D] views through attn_fwd_strided on a causal few-head problem that splits
+    through attn_fwd's scratch: the merge kernel writes O through the caller's strides (rows of
+    D + 8 elements here, whose 8 padding elements keep their guard pattern)."""
+    import exact_attention_forward_attn_gb300 as attn
+
+    B, Hq, Hkv, N, D = shape
+    w = wl.random_case(B, Hq, Hkv, N, D, True, 130 + D)
+    assert attn.fwd_num_splits(B, Hq, N, D, True) >= 2
+    q, k, v = wl.make_qkv(w)
+    qs, ks, vs = (t.transpose(1, 2).contiguous().cuda().transpose(1, 2) for t in (q, k, v))
+    g = Guarded(B * N * Hq * (D + 8) * 2)
+    full = g.typed(torch.bfloat16, (B, N, Hq, D + 8))
+    out = full[..., :D].transpose(1, 2)  # [B, H, N, D] view with row stride Hq * (D + 8)
+    o, lse = attn.attn_fwd(qs, ks, vs, causal=True, sm_scale=w.sm_scale, out=out)
+    torch.cuda.synchronize()
+    assert attn.device_status() == 0
+    assert g.intact()
+    assert bool((full[..., D:].contiguous().view(torch.uint8) == PATTERN).all())
+    _sampled(w, q, k, v, o.contiguous(), lse)
