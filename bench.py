@@ -602,8 +602,8 @@ def main():
             return start.elapsed_time(end)
 
         e2e_run(2)
-        # the host<->device copies' rate varies from run to run on shared machines (other jobs'
-        # copies): three runs, the median one reported, all three listed
+        # the host<->device copy rate can vary from run to run (the host's memory system may be
+        # busy with other work): three runs, the median one reported, all three listed
         runs = sorted(e2e_run(n_e2e) for _ in range(3))
         total = runs[1]
         # the last step's results, back on the host, match the device-side run's (the grouped
