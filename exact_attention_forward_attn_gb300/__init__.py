@@ -87,8 +87,10 @@ def attn_fwd(q, k, v, causal: bool = False, sm_scale: float | None = None, out=N
     Returns ``(out, lse)``: out bf16 [B,Hq,N,D], lse fp32 [B,Hq,N].  ``out``/``lse`` may be passed
     preallocated (right shape and dtype).  q, k, v, out may be strided views (e.g. [B, N, H, D]
     memory seen as [B, H, N, D]) as long as D is contiguous and the other strides are multiples of
-    8 elements; those go through ``attn_fwd_strided`` without a copy.  Raises ``AttnError`` on a
-    nonzero status.
+    8 elements; those go through ``attn_fwd_strided`` without a copy.  Problems whose query tiles
+    leave SMs idle over a long key axis may be split along the keys by the library itself
+    (``fwd_num_splits`` says how many ways; the result equals the single pass up to rounding).
+    Raises ``AttnError`` on a nonzero status.
     """
     import torch
 
